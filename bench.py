@@ -1,0 +1,355 @@
+"""Benchmark: layer-streamed training step (forward + backward, every weight
+streamed from pinned host memory, every gradient streamed back) on the
+LLaMA-3.1-8B-shaped decoder, one GPU per process.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mine|reference] [--workload llama8b|...]
+
+Prints one JSON line (rank 0). Multi-GPU runs are independent replicas (each
+GPU trains its own batch through its own context; nothing is exchanged), so
+`value` is the sum of tokens over all ranks divided by the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOADS = {
+    # name: (layers, hidden, heads, kv_heads, head_dim, ffn, vocab, theta, B, S, K, bf16 host params)
+    "llama8b": (32, 4096, 32, 8, 128, 14336, 128256, 5e5, 2, 4096, 4, True),
+    "llama8b_long": (32, 4096, 32, 8, 128, 14336, 128256, 5e5, 1, 16384, 8, True),
+    "small": (8, 1024, 16, 16, 64, 2816, 32000, 1e4, 4, 2048, 4, False),
+    "tiny": (2, 64, 4, 4, 16, 172, 256, 1e4, 2, 32, 1, False),
+}
+METRIC = "train tokens/sec (fwd+bwd, weights streamed from host) at 8B shape; % roofline"
+
+
+def read_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return json.load(f), "measured"
+    except OSError:
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        fd, self.path = tempfile.mkstemp(suffix=".csv")
+        os.close(fd)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) < 8:
+                    continue
+                try:
+                    sm.append(float(parts[0]))
+                    smax.append(float(parts[1]))
+                except ValueError:
+                    continue
+                for n, v in zip(names, parts[4:8]):
+                    if v.lower() in ("active", "1", "0x1"):
+                        reasons.add(n)
+        os.unlink(self.path)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def model_flops(shape, B, S):
+    """Algorithmic work of one step, as counted for the roofline: per decoder
+    layer 2*T*P_lin for each of forward, recompute, input-gradient and
+    weight-gradient products, plus causal attention (forward, recompute and
+    2.5x backward); head 4 GEMM-equivalents (two logit passes, dX, dW)."""
+    L, h, nq, nkv, d, F, V = shape[:7]
+    T = B * S
+    P_lin = h * (nq * d) * 2 + 2 * h * (nkv * d) + 3 * h * F
+    A = 2.0 * B * nq * d * S * (S + 1)
+    layer = 2.0 * T * P_lin * 4 + A * (1 + 1 + 2.5)
+    head = 4 * 2.0 * T * V * h
+    return layer, head, P_lin
+
+
+def host_link_probe(torch, nbytes=436 * 2**20):
+    """Pinned H2D alone, D2H alone, and both at once (GB/s), CUDA events."""
+    host_a = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    host_b = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
+    dev_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    dev_b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+
+    def timed(fn, reps=5):
+        best = 1e9
+        for _ in range(reps):
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            fn()
+            torch.cuda.synchronize()
+            best = min(best, time.perf_counter() - t0)
+        return best
+
+    def h2d():
+        with torch.cuda.stream(s1):
+            dev_a.copy_(host_a, non_blocking=True)
+
+    def d2h():
+        with torch.cuda.stream(s2):
+            host_b.copy_(dev_b, non_blocking=True)
+
+    def both():
+        h2d()
+        d2h()
+
+    t_h2d, t_d2h, t_both = timed(h2d), timed(d2h), timed(both)
+    out = {"h2d_gbs": nbytes / t_h2d / 1e9, "d2h_gbs": nbytes / t_d2h / 1e9,
+           "h2d_concurrent_gbs": nbytes / t_both / 1e9, "d2h_concurrent_gbs": nbytes / t_both / 1e9}
+    del host_a, host_b, dev_a, dev_b
+    return out
+
+
+def cpu_oracle_sample(shape, S_sample, seed=5):
+    """Time the CPU oracle (single thread) on one decoder layer plus the head
+    of this shape at B=1, S=S_sample, and extrapolate to the full depth:
+    t(L layers) = t(1 layer + head) + (L-1) * t_layer, with t_layer taken by
+    the layer's share of the sample's work."""
+    import oracle
+    import seedgen
+    L, h, nq, nkv, d, F, V, theta = shape[:8]
+    cfg = oracle.Config(1, h, nq, nkv, d, F, V, theta, 1e-5)
+    packed = np.zeros(oracle.packed_bytes(cfg, True), np.uint8)
+    offs = []
+    for unit, t, name, shp, is_gain in oracle.tensor_list(cfg):
+        off, nb = oracle.tensor_offset(cfg, unit, t, True)
+        offs.append((unit, t, off, int(np.prod(shp)), is_gain))
+    seedgen.fill_packed_params(packed.ctypes.data, offs, True, seed)
+    tok, lab = seedgen.tokens_and_labels(1, S_sample, V, seed + 1)
+    t0 = time.perf_counter()
+    oracle.forward_backward(cfg, packed, tok, lab, bf16=True)
+    t1 = time.perf_counter() - t0
+    layer_f, head_f, P_lin = model_flops((1, h, nq, nkv, d, F, V), 1, S_sample)
+    layer_f_plain = layer_f * 3 / 4  # the oracle does no recompute
+    frac_layer = layer_f_plain / (layer_f_plain + head_f * 3 / 4)
+    t_layer = t1 * frac_layer
+    t_full = t1 + (L - 1) * t_layer
+    return S_sample / t_full, t1
+
+
+def run_reference(args, shape, B, S):
+    """The reference arm: the CPU oracle as it stands, timed on this host."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    S_sample = 8
+    vals = []
+    for i in range(args.warmup + args.steps):
+        v, t1 = cpu_oracle_sample(shape, S_sample, seed=100 + i)
+        if i >= args.warmup:
+            vals.append(v)
+    value = float(np.median(vals))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": args.workload, "global_batch": B, "seq_len": S, "parallelism": "replicas"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                         "sample": f"one decoder layer + LM head of the {args.workload} shape at B=1, S={S_sample}, "
+                                   f"single-threaded fp32 oracle, extrapolated linearly to {shape[0]} layers"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=5)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="mine", choices=["mine", "reference"])
+    ap.add_argument("--workload", default="llama8b", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fuse-top", action="store_true", help="recompute the top block too")
+    ap.add_argument("--serial", action="store_true", help="ablation: serialise weight copies and compute")
+    args = ap.parse_args()
+    wl = WORKLOADS[args.workload]
+    shape, (B, S, K, bf16) = wl[:8], wl[8:]
+    if args.impl == "reference":
+        return run_reference(args, shape, B, S)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    os.environ.setdefault("MT_TRACE", "2")
+    if args.no_fuse_top:
+        os.environ["MT_FUSE_TOP_BLOCK"] = "0"
+    if args.serial:
+        os.environ["MT_SERIAL"] = "1"
+    import torch
+    torch.cuda.set_device(local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    import layer_streamed_gb300 as mt
+    import seedgen
+    mt.build()
+    L, h, nq, nkv, d, F, V, theta = shape
+    cfg = mt.make_cfg(L, h, nq, nkv, d, F, V, theta, 1e-5, B, S, K, mt.MT_BF16 if bf16 else mt.MT_F32)
+    budget = mt.mt_required_budget(cfg)
+    arena = torch.empty(budget, dtype=torch.uint8, device="cuda")
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    sess = mt.Session(mt.ModelShape(L, h, nq, nkv, d, F, V, theta, 1e-5), B, S, K,
+                      mt.MT_BF16 if bf16 else mt.MT_F32, device_budget=budget, device_arena=arena.data_ptr(),
+                      streams=[s.cuda_stream for s in streams])
+    # Parameters: N(0, 0.02) matrices, unit RMSNorm gains, per-rank seed.
+    offs = []
+    for unit in range(L + 2):
+        nt = 1 if unit == 0 else (9 if unit <= L else 2)
+        for t in range(nt):
+            off, nbytes = sess.offset(unit, t)
+            is_gain = (unit >= 1 and unit <= L and t in (0, 5)) or (unit == L + 1 and t == 0)
+            offs.append((unit, t, off, nbytes // (2 if bf16 else 4), is_gain))
+    t0 = time.perf_counter()
+    seedgen.fill_packed_params(sess.params_ptr, offs, bf16, seed=21 + rank)
+    init_s = time.perf_counter() - t0
+    tok, lab = seedgen.tokens_and_labels(B, S, V, seed=22 + rank)
+
+    link = host_link_probe(torch)
+    for _ in range(args.warmup):
+        sess.step(tok, lab, K)
+    comp, d2h_stream = streams[0], streams[2]
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    agg = {}
+    clocks = ClockSampler(local)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    wall0 = time.perf_counter()
+    ev0.record(comp)
+    losses = []
+    for _ in range(args.steps):
+        losses.append(sess.step(tok, lab, K))
+        st = sess.stats()
+        for k, v in st.items():
+            agg[k] = agg.get(k, 0) + v
+    ev1.record(d2h_stream)
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    dev_ms = ev0.elapsed_time(ev1)
+    if dist:
+        t = torch.tensor([dev_ms, wall], device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dev_ms, wall = float(t[0]), float(t[1])
+        if rank != 0:
+            dist.destroy_process_group()
+            sess.close()
+            return
+    T = B * S
+    steps = args.steps
+    value = world * T * steps / (dev_ms / 1e3)
+    e2e = world * T * steps / wall
+    peaks, peak_kind = read_peaks()
+    gemm_tflops = agg["gemm_flop"] / (agg["gemm_ms"] / 1e3) / 1e12 if agg.get("gemm_ms") else None
+    peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
+    layer_f, head_f, P_lin = model_flops(shape, B, S)
+    step_flop = L * layer_f + head_f
+    # Roofline of the whole step: per unit, the slower of its work at the
+    # tensor-core peak and its streamed bytes at the measured host link.
+    h2d_bw = link["h2d_concurrent_gbs"] * 1e9
+    d2h_bw = link["d2h_concurrent_gbs"] * 1e9
+    per_step_h2d = agg["h2d_bytes"] / steps
+    per_step_d2h = agg["d2h_bytes"] / steps
+    layer_h2d = per_step_h2d * (L * P_lin * 2) / max(1.0, (L * P_lin * 2 + 2 * V * h * 2)) / L
+    t_layer = max(layer_f / (peak_tf * 1e12), layer_h2d / h2d_bw, 4.0 * (P_lin + 2 * h) / d2h_bw)
+    t_head = max(head_f / (peak_tf * 1e12), (per_step_h2d - L * layer_h2d) / h2d_bw, (2.0 * V * h * 4) / d2h_bw)
+    t_roof = L * t_layer + t_head
+    ms_per_step = dev_ms / steps
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_per_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "global_batch": B * world, "seq_len": S, "checkpoint_every": K,
+                   "layers": L, "hidden": h, "heads": f"{nq}q/{nkv}kv x {d}", "ffn": F, "vocab": V,
+                   "host_params": "bf16" if bf16 else "fp32", "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (every step streams all weights from host)"},
+        "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(per_step_h2d + 2 * T * 4),
+                "d2h_bytes_per_step": int(per_step_d2h + 4)},
+        "gpu_launches": int(agg["n_launches"]),
+        "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": (gemm_tflops / peak_tf) if gemm_tflops else None, "traffic": None,
+                     "kernel": "gemm (tcgen05, all GEMM launches of the step)",
+                     "peak_kind": f"{peak_kind} bf16_tflops_sustained"},
+        "step_roofline": {"t_roof_ms": t_roof * 1e3, "t_measured_ms": ms_per_step, "frac": t_roof * 1e3 / ms_per_step,
+                          "model_tflops_per_s": step_flop / (ms_per_step / 1e3) / 1e12,
+                          "h2d_hidden_frac": agg["h2d_hidden_frac"] / steps,
+                          "d2h_hidden_frac": agg["d2h_hidden_frac"] / steps,
+                          "attn_tflops": (agg["attn_flop"] / (agg["attn_ms"] / 1e3) / 1e12) if agg.get("attn_ms")
+                          else None,
+                          "gemm_ms_per_step": agg["gemm_ms"] / steps, "attn_ms_per_step": agg["attn_ms"] / steps,
+                          "compute_busy_ms_per_step": agg["compute_busy_ms"] / steps},
+        "host_link": link,
+        "clocks": clk,
+        "loss": losses[-1],
+        "init_s": init_s,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        v, t1 = cpu_oracle_sample(shape, 8)
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
+                                "sample": f"one decoder layer + LM head of the {args.workload} shape at B=1, S=8 "
+                                          f"({t1:.1f} s single-threaded fp32 oracle), extrapolated linearly to "
+                                          f"{L} layers; host has {os.cpu_count()} cores"}
+    print(json.dumps(line), flush=True)
+    sess.close()
+    if dist:
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,255 @@
+/* mt.h — C ABI of the layer-streamed training library (libmt.so).
+ *
+ * One training step of a Llama-style decoder on ONE GPU whose parameters all
+ * live in pinned host memory ("MegaTrain: Full Precision Training of 100B+
+ * Parameter Large Language Models on a Single GPU"):
+ *  - the host owns parameters and gradients; the GPU holds an empty layer
+ *    template bound to whatever weights stream in (section 核心方法);
+ *  - forward: each layer's packed weights are copied H2D into one of two
+ *    ping-pong device buffers while the previous layer computes; the residual
+ *    stream is checkpointed every K layers (section 方法步骤详情, stage 1);
+ *  - loss anchor: final norm, LM head and cross-entropy, head gradients
+ *    offloaded (stage 2);
+ *  - backward: per block of K layers, top block first, restore the block's
+ *    checkpoint, recompute its forward, then back-propagate it layer by
+ *    layer, copying each layer's gradients D2H on a separate stream
+ *    (stage 3);
+ *  - three CUDA streams (compute, weight-in, grad-out) ordered only by CUDA
+ *    events: weight-ready, backward-done, buffer-free (section 技术新颖性).
+ *
+ * Conventions for every function below:
+ *  - integer status returns: MT_OK (0) or a negative mt_status; no function
+ *    aborts the process or lets a C++ exception cross this boundary;
+ *  - a context is not thread-safe; use one per thread and per GPU;
+ *  - pointers documented as "host" are CPU addresses, "device" are CUDA
+ *    device addresses on the context's device; the caller keeps ownership of
+ *    every buffer it passes in.
+ */
+#ifndef MT_H
+#define MT_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MT_ABI_VERSION 1
+
+typedef enum {
+  MT_OK = 0,
+  MT_ERR_ARG = -1,         /* bad argument (null pointer, size out of range, token id >= vocab, ...) */
+  MT_ERR_BUDGET = -2,      /* the device budget cannot hold the buffers this call needs */
+  MT_ERR_NOT_PINNED = -3,  /* a host buffer is not page-locked CUDA host memory */
+  MT_ERR_ALIGN = -4,       /* a host buffer is not 4096-byte aligned */
+  MT_ERR_CUDA = -5,        /* a CUDA runtime/driver call failed (text in mt_last_error) */
+  MT_ERR_TIMEOUT = -6,     /* a bounded wait (host event poll or device barrier) ran out */
+  MT_ERR_STATE = -7,       /* call out of order (e.g. forward_backward before bind) */
+  MT_ERR_UNSUPPORTED = -8, /* configuration outside what the kernels implement */
+  MT_ERR_DEVICE = -9       /* a kernel reported an internal error through the device error word */
+} mt_status;
+
+typedef enum { MT_F32 = 0, MT_BF16 = 1 } mt_dtype;
+
+/* Model and capacity description.
+ * Shapes: hidden h, n_heads query heads and n_kv_heads key/value heads of
+ * head_dim d (n_heads % n_kv_heads == 0; query head j reads KV head
+ * j / (n_heads / n_kv_heads)), SwiGLU FFN width ffn_dim, untied vocab.
+ * Supported: h % 64 == 0, d in {16, 32, 64, 128}, for MT_BF16 params
+ * ffn_dim % 8 == 0; any ffn_dim >= 1 for MT_F32 params.
+ * max_batch * max_seq bounds the tokens of one call; max_K bounds the
+ * checkpoint interval. param_dtype is the dtype of the host parameters that
+ * will be bound. n_experts/top_k/expert_ffn must be 0 (dense decoder). */
+typedef struct {
+  int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
+  float rope_theta, norm_eps;
+  int32_t max_batch, max_seq, max_K;
+  int32_t param_dtype; /* mt_dtype */
+  int32_t n_experts, top_k, expert_ffn;
+} mt_layer_cfg;
+
+typedef struct mt_ctx mt_ctx;
+
+/* Packed host parameter layout ("each layer's state packed into one
+ * contiguous block aligned to a 4 KB page", MegaTrain, section 技术新颖性):
+ *  unit 0        : embedding E[vocab, h]                       (tensor 0)
+ *  unit 1..L     : one decoder layer each, tensors in order
+ *                  0 w_attn_norm[h], 1 Wq[n_heads*d, h], 2 Wk[n_kv_heads*d, h],
+ *                  3 Wv[n_kv_heads*d, h], 4 Wo[h, n_heads*d], 5 w_ffn_norm[h],
+ *                  6 Wg[ffn, h], 7 Wu[ffn, h], 8 Wd[h, ffn]
+ *  unit L+1      : 0 w_final_norm[h], 1 W_out[vocab, h]
+ * Matrices are row-major [out, in] (y = x W^T). Every tensor starts on a
+ * 256-byte boundary, every unit on a 4096-byte boundary. The gradient buffer
+ * uses the same layout with fp32 elements. */
+size_t mt_packed_bytes(const mt_layer_cfg* cfg, mt_dtype dtype);
+
+/* Byte offset and byte size of tensor `tensor` of unit `unit` in the packed
+ * layout of `dtype`. Returns MT_ERR_ARG for an unknown unit/tensor. */
+int mt_tensor_offset(const mt_layer_cfg* cfg, mt_dtype dtype, int unit, int tensor, size_t* off, size_t* bytes);
+
+/* Device bytes a context needs for cfg (all K in [1, max_K], batches up to
+ * max_batch x max_seq): two weight buffers, two gradient staging buffers,
+ * checkpoints, one K-block of saved activations and fixed workspace.
+ * Returns 0 if cfg is invalid. */
+size_t mt_required_budget(const mt_layer_cfg* cfg);
+
+/* Create a context on the current CUDA device. Allocates one device arena of
+ * mt_required_budget(cfg) bytes (MT_ERR_BUDGET if that exceeds
+ * device_budget_bytes) and three streams. *out is set only on MT_OK. */
+int mt_create(const mt_layer_cfg* cfg, size_t device_budget_bytes, mt_ctx** out);
+
+/* Same, but adopt a caller-owned device arena of device_budget_bytes
+ * (256-byte aligned; e.g. a PyTorch tensor) and, if streams is non-null,
+ * three caller-owned cudaStream_t values {compute, weight-in, grad-out}.
+ * The caller keeps them alive until mt_destroy. */
+int mt_create_ex(const mt_layer_cfg* cfg, size_t device_budget_bytes, void* device_arena, void* const* streams,
+                 mt_ctx** out);
+
+/* Bind the packed host parameters (layout above, dtype == cfg.param_dtype).
+ * host_params must be page-locked CUDA host memory (MT_ERR_NOT_PINNED),
+ * 4096-byte aligned (MT_ERR_ALIGN), at least mt_packed_bytes bytes, and stay
+ * valid and unmodified during every mt_forward_backward call. No copy is
+ * made; re-binding replaces the pointer. */
+int mt_bind_host_params(mt_ctx* ctx, const void* host_params, mt_dtype dtype);
+
+/* One training step: forward, loss, backward, all gradients to host.
+ *  tokens, labels : host int32 [B, S], values in [0, vocab) (MT_ERR_ARG otherwise)
+ *  B, S           : 1 <= B*S, B <= max_batch, S <= max_seq
+ *  K              : checkpoint interval, 1 <= K <= min(n_layers, max_K); n_layers % K
+ *                   may be nonzero (the top block is then partial)
+ *  host_grad_out  : pinned host fp32 buffer, mt_packed_bytes(cfg, MT_F32) bytes,
+ *                   4096-byte aligned; OVERWRITTEN with dLoss/dtheta in the
+ *                   packed layout (embedding rows of unused tokens are 0)
+ *  loss_out       : host; Loss = mean over the B*S positions of
+ *                   logsumexp(z_t) - z_t[label_t]
+ * Synchronous: on return every gradient has landed. Results are bitwise
+ * independent of K. */
+int mt_forward_backward(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
+                        float* host_grad_out, float* loss_out);
+
+/* Per-step measurements of the last mt_forward_backward call (CUDA events). */
+typedef struct {
+  double step_ms;          /* first H2D issue to last D2H completion */
+  double compute_busy_ms;  /* sum of compute-stream segment times */
+  double h2d_ms, d2h_ms;   /* sum of copy durations on the weight-in / grad-out streams */
+  double h2d_bytes, d2h_bytes;
+  double h2d_hidden_frac;  /* fraction of H2D copy time overlapped by compute segments */
+  double d2h_hidden_frac;
+  int32_t n_h2d, n_d2h, n_units;
+  int32_t timing_enabled;  /* 0: MT_TRACE=0 (no events); 1: per-unit events; 2: also per-kernel events */
+  /* With MT_TRACE=2: summed device time and algorithmic work of the GEMM
+   * launches (2*M*N*K flop each) and of the attention launches (causal
+   * lower-triangle flop), timed with CUDA events on the compute stream. */
+  double gemm_ms, gemm_flop, attn_ms, attn_flop;
+  int32_t n_gemm, n_attn;
+  int32_t n_launches;      /* kernels launched by this step (all trace levels) */
+  int32_t reserved;
+} mt_stats;
+int mt_get_stats(const mt_ctx* ctx, mt_stats* out);
+
+/* Arena partition of a context (bytes). */
+typedef struct {
+  size_t total, weight_buffers, grad_buffers, checkpoints, block_activations, workspace;
+} mt_memory_plan;
+int mt_get_memory_plan(const mt_ctx* ctx, mt_memory_plan* out);
+
+/* Text of the last error on ctx (never null; "" if none). */
+const char* mt_last_error(const mt_ctx* ctx);
+
+/* Destroy streams/events it created and free the arena it allocated. Null is ignored. */
+void mt_destroy(mt_ctx* ctx);
+
+/* Page-locked, 4096-byte aligned host memory (cudaHostAlloc); null on failure. */
+void* mt_host_alloc(size_t bytes);
+void mt_host_free(void* p);
+
+/* Test hook: make the n-th (1-based) weight copy issue or host event wait of
+ * the next mt_forward_backward calls on ctx fail as if the CUDA call had
+ * failed (kind 1 = copy issue -> MT_ERR_CUDA) or timed out (kind 2 = wait ->
+ * MT_ERR_TIMEOUT). kind 0 clears it. Host-side only: nothing is injected
+ * into the GPU. */
+int mt_debug_inject_fault(mt_ctx* ctx, int kind, int nth);
+
+/* ---------------------------------------------------------------------------
+ * Kernel-level entry points (the layer template's operations, exposed for
+ * testing and measurement). All tensor pointers are DEVICE pointers on the
+ * current device; `stream` is a cudaStream_t (null = legacy default stream).
+ * Calls are asynchronous; errors in launch configuration are returned, and
+ * device-side barrier timeouts are reported by mt_op_device_error.
+ * bf16 tensors are raw 16-bit bfloat16 storage.
+ * ------------------------------------------------------------------------- */
+
+/* GEMM on the tensor cores, bf16 operands, fp32 accumulation.
+ *  mode MT_GEMM_NT: C[M,N] = A[M,K] * B[N,K]^T   (forward: y = x W^T)
+ *  mode MT_GEMM_NN: C[M,N] = A[M,K] * B[K,N]     (input gradient: dx = dy W)
+ *  mode MT_GEMM_TN: C[M,N] = A[K,M]^T * B[K,N]   (weight gradient: dW = dy^T x)
+ * lda/ldb are the row strides (elements) of A and B as stored; they must be
+ * multiples of 8 and the base pointers 16-byte aligned.
+ *  epi MT_EPI_BF16  : C bf16 = round(acc)
+ *  epi MT_EPI_F32   : C fp32 = acc
+ *  epi MT_EPI_F32_ADD: C fp32 = addend + acc (addend may equal C; row stride ldc)
+ * ldc is C's row stride in elements. */
+enum { MT_GEMM_NT = 0, MT_GEMM_NN = 1, MT_GEMM_TN = 2 };
+enum { MT_EPI_BF16 = 0, MT_EPI_F32 = 1, MT_EPI_F32_ADD = 2 };
+int mt_op_gemm(int mode, int epi, const void* A, const void* B, void* C, const void* addend, int M, int N, int K,
+               int lda, int ldb, int ldc, void* stream);
+
+/* RMSNorm forward: y[t] = bf16(x[t] * w * rstd[t]), rstd[t] = 1/sqrt(mean(x[t]^2) + eps).
+ * x fp32 [T,h], w fp32 [h], y bf16 [T,h], rstd fp32 [T]. */
+int mt_op_rmsnorm_fwd(const float* x, const float* w, void* y, float* rstd, int T, int h, float eps, void* stream);
+
+/* RMSNorm backward with residual: dx = resid + rstd*(dy*w - xhat*mean(dy*w*xhat)),
+ * xhat = x*rstd; dx fp32 (and bf16 copy dx_bf16 if non-null); dw fp32 [h] = sum_t dy*xhat
+ * (fixed-order reduction; workspace fp32 of mt_op_rmsnorm_bwd_workspace(T,h) floats).
+ * resid may be null (treated as 0) or equal dx. */
+size_t mt_op_rmsnorm_bwd_workspace(int T, int h);
+int mt_op_rmsnorm_bwd(const float* x, const float* w, const float* rstd, const float* dy, const float* resid,
+                      float* dx, void* dx_bf16, float* dw, float* workspace, int T, int h, void* stream);
+
+/* RoPE in place on bf16 x laid out [B*S, row_stride] where heads
+ * [head0, head0 + n_heads) of width d start at column head0*d; dir +1
+ * rotates by +pos*theta^(-2i/d) on the half-split pairs (i, i+d/2), -1 by the
+ * opposite angle (the backward). table: device fp32 workspace of S*d floats
+ * (overwritten with the cos/sin table). d must be a multiple of 8. */
+int mt_op_rope(void* x, float* table, int B, int S, int row_stride, int head0, int n_heads, int d, float theta,
+               int dir, void* stream);
+
+/* Causal GQA attention forward on bf16 q/k/v/o with row strides (elements):
+ * q [B*S, ldq] heads at columns j*d, k/v [B*S, ldkv], o [B*S, ldo];
+ * lse fp32 [B, n_heads, S] (natural-log logsumexp of the scaled scores). */
+int mt_op_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S, int n_heads,
+                        int n_kv_heads, int d, int ldq, int ldkv, int ldo, void* stream);
+
+/* Attention backward: dq [B*S, ldq], dk/dv [B*S, ldkv] bf16 outputs
+ * (overwritten); do_ bf16 [B*S, ldo]; workspace fp32 of
+ * mt_op_attention_bwd_workspace(B,S,n_heads) floats. Deterministic. */
+size_t mt_op_attention_bwd_workspace(int B, int S, int n_heads);
+int mt_op_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_, const float* lse,
+                        void* dq, void* dk, void* dv, float* workspace, int B, int S, int n_heads, int n_kv_heads,
+                        int d, int ldq, int ldkv, int ldo, void* stream);
+
+/* SwiGLU on gu bf16 [T, 2*ld] (gate columns [0,F), up columns [ld, ld+F)):
+ * forward act bf16 [T, ld] = silu(g)*u (padding columns F..ld-1 written 0);
+ * backward in place: gu <- (dact*u*silu'(g), dact*silu(g)). */
+int mt_op_swiglu_fwd(const void* gu, void* act, int T, int F, int ld, void* stream);
+int mt_op_swiglu_bwd(void* gu, const void* dact, int T, int F, int ld, void* stream);
+
+/* Cross-entropy loss over logits produced by an NT product with a vocab
+ * slice (never materialising [T, vocab]): see mt_op_lmhead_ce. Computes
+ * loss = scale * sum_t (lse_t - z_t[label_t]) and dX [T,h] fp32 =
+ * dz W_out, dW_out fp32 [V,h] = dz^T X, dz = scale*(softmax - onehot),
+ * for X bf16 [T,h], W_out bf16 [V,h]; labels device int32 [T].
+ * loss_dev is a device float. workspace bytes: mt_op_lmhead_ce_workspace. */
+size_t mt_op_lmhead_ce_workspace(int T, int V, int h);
+int mt_op_lmhead_ce(const void* X, const void* W, const int32_t* labels, float scale, float* dX, float* dW,
+                    float* loss_dev, void* workspace, int T, int V, int h, void* stream);
+
+/* Device error word of the kernels (barrier timeouts etc.): returns and
+ * clears it (0 = none). Synchronizes the device. */
+int mt_op_device_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MT_H */

@@ -1,0 +1,543 @@
+// Bandwidth-bound kernels of the layer template: RMSNorm forward/backward,
+// RoPE, SwiGLU forward/backward, embedding gather / deterministic
+// scatter-add, weight casts, and the cross-entropy reductions of the loss
+// anchor ("MegaTrain", section 方法步骤详情, stage 2: loss and head gradient).
+// All global accesses are 128-bit and coalesced where the shapes allow;
+// reductions are warp shuffles plus a fixed-order cross-warp step, so every
+// result is bitwise reproducible run to run.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mt {
+namespace {
+
+constexpr int kThreads = 256;
+
+__device__ __forceinline__ float block_sum(float v, float* red) {
+  v = warp_sum(v);
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  __syncthreads();
+  if (l == 0) red[w] = v;
+  __syncthreads();
+  float s = 0.f;
+  const int nw = blockDim.x >> 5;
+  for (int i = 0; i < nw; ++i) s += red[i];  // same order in every thread
+  return s;
+}
+
+__device__ __forceinline__ void store_bf16x4(uint16_t* dst, float a, float b, float c, float d) {
+  uint2 u;
+  u.x = pack_bf2(a, b);
+  u.y = pack_bf2(c, d);
+  *(uint2*)dst = u;
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm forward: one block per row.
+// ---------------------------------------------------------------------------
+__global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w, uint16_t* __restrict__ y,
+                                   float* __restrict__ rstd, int h, float eps) {
+  __shared__ float red[32];
+  const size_t t = blockIdx.x;
+  const float4* xr = (const float4*)(x + t * h);
+  const float4* w4 = (const float4*)w;
+  const int n4 = h >> 2;
+  float ss = 0.f;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = xr[i];
+    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+  }
+  ss = block_sum(ss, red);
+  const float r = rsqrtf(ss / (float)h + eps);
+  if (threadIdx.x == 0) rstd[t] = r;
+  uint16_t* yr = y + t * h;
+  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
+    const float4 v = xr[i], g = w4[i];
+    store_bf16x4(yr + 4 * i, v.x * r * g.x, v.y * r * g.y, v.z * r * g.z, v.w * r * g.w);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// RMSNorm backward: a block owns ROWS consecutive rows; each thread owns a
+// fixed set of float4 columns and accumulates its share of dw over its rows
+// in registers (row order), then writes a per-block partial; a second kernel
+// adds the partials in block order.
+// ---------------------------------------------------------------------------
+constexpr int kNormBwdRows = 32;
+constexpr int kMaxV = 8;  // h <= 8 * 4 * 256 = 8192
+
+__global__ void rmsnorm_bwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                   const float* __restrict__ rstd, const float* __restrict__ dy,
+                                   const float* resid, float* dx, uint16_t* __restrict__ dxb,
+                                   float* __restrict__ part, int T, int h) {
+  __shared__ float red[32];
+  const int n4 = h >> 2;
+  float4 acc[kMaxV];
+#pragma unroll
+  for (int j = 0; j < kMaxV; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  const float inv_h = 1.f / (float)h;
+  const int r0 = blockIdx.x * kNormBwdRows;
+  const int r1 = min(T, r0 + kNormBwdRows);
+  for (int t = r0; t < r1; ++t) {
+    const float4* xr = (const float4*)(x + (size_t)t * h);
+    const float4* gr = (const float4*)(dy + (size_t)t * h);
+    const float r = rstd[t];
+    float dot = 0.f;
+#pragma unroll
+    for (int j = 0; j < kMaxV; ++j) {
+      const int i = threadIdx.x + j * kThreads;
+      if (i < n4) {
+        const float4 xv = xr[i], gv = gr[i], wv = ((const float4*)w)[i];
+        dot += gv.x * wv.x * xv.x + gv.y * wv.y * xv.y + gv.z * wv.z * xv.z + gv.w * wv.w * xv.w;
+      }
+    }
+    dot = block_sum(dot, red) * r;
+    const float mean = dot * inv_h;
+#pragma unroll
+    for (int j = 0; j < kMaxV; ++j) {
+      const int i = threadIdx.x + j * kThreads;
+      if (i < n4) {
+        const float4 xv = xr[i], gv = gr[i], wv = ((const float4*)w)[i];
+        const float4 xh = make_float4(xv.x * r, xv.y * r, xv.z * r, xv.w * r);
+        float4 o = make_float4(r * (gv.x * wv.x - xh.x * mean), r * (gv.y * wv.y - xh.y * mean),
+                               r * (gv.z * wv.z - xh.z * mean), r * (gv.w * wv.w - xh.w * mean));
+        if (resid) {
+          const float4 rv = ((const float4*)(resid + (size_t)t * h))[i];
+          o.x += rv.x;
+          o.y += rv.y;
+          o.z += rv.z;
+          o.w += rv.w;
+        }
+        ((float4*)(dx + (size_t)t * h))[i] = o;
+        if (dxb) store_bf16x4(dxb + (size_t)t * h + 4 * i, o.x, o.y, o.z, o.w);
+        acc[j].x += gv.x * xh.x;
+        acc[j].y += gv.y * xh.y;
+        acc[j].z += gv.z * xh.z;
+        acc[j].w += gv.w * xh.w;
+      }
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < kMaxV; ++j) {
+    const int i = threadIdx.x + j * kThreads;
+    if (i < n4) ((float4*)(part + (size_t)blockIdx.x * h))[i] = acc[j];
+  }
+}
+
+__global__ void sum_partials_kernel(const float* __restrict__ part, int nparts, int n, float* __restrict__ out) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= n) return;
+  float s = 0.f;
+  for (int b = 0; b < nparts; ++b) s += part[(size_t)b * n + c];
+  out[c] = s;
+}
+
+// ---------------------------------------------------------------------------
+// RoPE: half-split pairs (i, i + d/2), angle = pos * theta^(-2i/d).
+// The table is built in double precision (large positions times small
+// frequencies need it), then rounded to fp32.
+// ---------------------------------------------------------------------------
+__global__ void rope_table_kernel(float2* tab, int S, int d, double theta) {
+  const int half = d / 2;
+  const int idx = blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= S * half) return;
+  const int pos = idx / half, i = idx % half;
+  const double freq = pow(theta, -2.0 * (double)i / (double)d);
+  double s, c;
+  sincos((double)pos * freq, &s, &c);
+  tab[idx] = make_float2((float)c, (float)s);
+}
+
+// One thread rotates 4 consecutive pairs of one head of one token.
+__global__ void rope_apply_kernel(uint16_t* x, const float2* __restrict__ tab, int T, int S, int row_stride, int head0,
+                                  int n_heads, int d, float sgn) {
+  const int half = d / 2, quads = half / 4;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  const size_t total = (size_t)T * n_heads * quads;
+  if (idx >= total) return;
+  const int qd = (int)(idx % quads);
+  const int head = (int)((idx / quads) % n_heads);
+  const int t = (int)(idx / ((size_t)quads * n_heads));
+  const int pos = t % S;
+  uint16_t* base = x + (size_t)t * row_stride + (size_t)(head0 + head) * d;
+  const int i0 = qd * 4;
+  uint2 lo = *(const uint2*)(base + i0);
+  uint2 hi = *(const uint2*)(base + half + i0);
+  float a[4] = {bf2f(lo.x & 0xffff), bf2f(lo.x >> 16), bf2f(lo.y & 0xffff), bf2f(lo.y >> 16)};
+  float b[4] = {bf2f(hi.x & 0xffff), bf2f(hi.x >> 16), bf2f(hi.y & 0xffff), bf2f(hi.y >> 16)};
+  float ra[4], rb[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 cs = tab[(size_t)pos * half + i0 + j];
+    const float sn = sgn * cs.y;
+    ra[j] = a[j] * cs.x - b[j] * sn;
+    rb[j] = a[j] * sn + b[j] * cs.x;
+  }
+  lo.x = pack_bf2(ra[0], ra[1]);
+  lo.y = pack_bf2(ra[2], ra[3]);
+  hi.x = pack_bf2(rb[0], rb[1]);
+  hi.y = pack_bf2(rb[2], rb[3]);
+  *(uint2*)(base + i0) = lo;
+  *(uint2*)(base + half + i0) = hi;
+}
+
+// ---------------------------------------------------------------------------
+// SwiGLU: a = silu(g) * u, silu(g) = g / (1 + e^-g).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float sigmoidf_(float g) { return 1.f / (1.f + __expf(-g)); }
+
+__global__ void swiglu_fwd_vec_kernel(const uint16_t* __restrict__ gu, uint16_t* __restrict__ act, int T, int ld) {
+  const int per_row = ld / 8;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)T * per_row) return;
+  const size_t t = idx / per_row;
+  const int c = (int)(idx % per_row) * 8;
+  const uint4 g4 = *(const uint4*)(gu + t * 2 * ld + c);
+  const uint4 u4 = *(const uint4*)(gu + t * 2 * ld + ld + c);
+  const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float g0 = bf2f(gw[j] & 0xffff), g1 = bf2f(gw[j] >> 16);
+    const float u0 = bf2f(uw[j] & 0xffff), u1 = bf2f(uw[j] >> 16);
+    o[j] = pack_bf2(g0 * sigmoidf_(g0) * u0, g1 * sigmoidf_(g1) * u1);
+  }
+  *(uint4*)(act + t * ld + c) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+__global__ void swiglu_fwd_kernel(const uint16_t* __restrict__ gu, uint16_t* __restrict__ act, int T, int F, int ld) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)T * ld) return;
+  const size_t t = idx / ld;
+  const int c = (int)(idx % ld);
+  float a = 0.f;
+  if (c < F) {
+    const float g = bf2f(gu[t * 2 * ld + c]), u = bf2f(gu[t * 2 * ld + ld + c]);
+    a = g * sigmoidf_(g) * u;
+  }
+  act[t * ld + c] = f2bf(a);
+}
+
+// d/dg = dact * u * sig(g) * (1 + g * (1 - sig(g)));  d/du = dact * silu(g)
+__global__ void swiglu_bwd_vec_kernel(uint16_t* gu, const uint16_t* __restrict__ dact, int T, int ld) {
+  const int per_row = ld / 8;
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)T * per_row) return;
+  const size_t t = idx / per_row;
+  const int c = (int)(idx % per_row) * 8;
+  uint4* gp = (uint4*)(gu + t * 2 * ld + c);
+  uint4* up = (uint4*)(gu + t * 2 * ld + ld + c);
+  const uint4 g4 = *gp, u4 = *up, d4 = *(const uint4*)(dact + t * ld + c);
+  const uint32_t gw[4] = {g4.x, g4.y, g4.z, g4.w}, uw[4] = {u4.x, u4.y, u4.z, u4.w}, dw[4] = {d4.x, d4.y, d4.z, d4.w};
+  uint32_t og[4], ou[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    float gg[2] = {bf2f(gw[j] & 0xffff), bf2f(gw[j] >> 16)};
+    float uu[2] = {bf2f(uw[j] & 0xffff), bf2f(uw[j] >> 16)};
+    float dd[2] = {bf2f(dw[j] & 0xffff), bf2f(dw[j] >> 16)};
+    float rg[2], ru[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float s = sigmoidf_(gg[e]);
+      rg[e] = dd[e] * uu[e] * s * (1.f + gg[e] * (1.f - s));
+      ru[e] = dd[e] * gg[e] * s;
+    }
+    og[j] = pack_bf2(rg[0], rg[1]);
+    ou[j] = pack_bf2(ru[0], ru[1]);
+  }
+  *gp = make_uint4(og[0], og[1], og[2], og[3]);
+  *up = make_uint4(ou[0], ou[1], ou[2], ou[3]);
+}
+
+__global__ void swiglu_bwd_kernel(uint16_t* gu, const uint16_t* __restrict__ dact, int T, int F, int ld) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)T * ld) return;
+  const size_t t = idx / ld;
+  const int c = (int)(idx % ld);
+  uint16_t* gp = gu + t * 2 * ld + c;
+  uint16_t* up = gp + ld;
+  if (c >= F) {  // padding columns carry no gradient
+    *gp = 0;
+    *up = 0;
+    return;
+  }
+  const float g = bf2f(*gp), u = bf2f(*up), d = bf2f(dact[t * ld + c]);
+  const float s = sigmoidf_(g);
+  *gp = f2bf(d * u * s * (1.f + g * (1.f - s)));
+  *up = f2bf(d * g * s);
+}
+
+// ---------------------------------------------------------------------------
+// Embedding
+// ---------------------------------------------------------------------------
+__global__ void embed_gather_kernel(const void* __restrict__ E, int bf16, int row0, int rows,
+                                    const int32_t* __restrict__ tok, float* __restrict__ h0, int h) {
+  const int t = blockIdx.x;
+  const int v = tok[t] - row0;
+  if (v < 0 || v >= rows) return;
+  float4* dst = (float4*)(h0 + (size_t)t * h);
+  for (int i = threadIdx.x; i < h / 4; i += blockDim.x) {
+    if (bf16) {
+      const uint2 u = ((const uint2*)((const uint16_t*)E + (size_t)v * h))[i];
+      dst[i] = make_float4(bf2f(u.x & 0xffff), bf2f(u.x >> 16), bf2f(u.y & 0xffff), bf2f(u.y >> 16));
+    } else {
+      dst[i] = ((const float4*)((const float*)E + (size_t)v * h))[i];
+    }
+  }
+}
+
+__global__ void embed_scatter_kernel(const int32_t* __restrict__ perm, const int32_t* __restrict__ start, int row0,
+                                     const float* __restrict__ dh0, float* __restrict__ dE, int h) {
+  const int r = blockIdx.x;
+  const int s0 = start[row0 + r], s1 = start[row0 + r + 1];
+  float4* dst = (float4*)(dE + (size_t)r * h);
+  for (int i = threadIdx.x; i < h / 4; i += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = s0; j < s1; ++j) {
+      const float4 g = ((const float4*)(dh0 + (size_t)perm[j] * h))[i];
+      acc.x += g.x;
+      acc.y += g.y;
+      acc.z += g.z;
+      acc.w += g.w;
+    }
+    dst[i] = acc;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Casts
+// ---------------------------------------------------------------------------
+__global__ void cast_rows_kernel(const float* __restrict__ src, uint16_t* __restrict__ dst, int rows_src,
+                                 int rows_dst, int cols, int ld) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)rows_dst * ld) return;
+  const size_t r = idx / ld;
+  const int c = (int)(idx % ld);
+  dst[idx] = (c < cols && r < (size_t)rows_src) ? f2bf(src[r * cols + c]) : (uint16_t)0;
+}
+
+__global__ void cast_f32_bf16_vec_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const float4 v = src[i];
+  uint2 u;
+  u.x = pack_bf2(v.x, v.y);
+  u.y = pack_bf2(v.z, v.w);
+  dst[i] = u;
+}
+
+__global__ void gains_kernel(const void* __restrict__ src, int bf16, float* __restrict__ dst, int n) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n) return;
+  dst[i] = bf16 ? bf2f(((const uint16_t*)src)[i]) : ((const float*)src)[i];
+}
+
+// ---------------------------------------------------------------------------
+// Cross-entropy over vocab slices. Per row, a running (max, sum of
+// exp(z - max)) pair is kept per thread and merged across the block in a
+// fixed order; slices are merged in slice order by ce_finalize.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void lse_merge(float& m, float& s, float m2, float s2) {
+  if (m2 == -INFINITY) return;
+  if (m == -INFINITY) {
+    m = m2;
+    s = s2;
+    return;
+  }
+  if (m2 > m) {
+    s = s * __expf(m - m2) + s2;
+    m = m2;
+  } else {
+    s += s2 * __expf(m2 - m);
+  }
+}
+
+__global__ void ce_stats_kernel(const float* __restrict__ z, int R, int ld, int row0,
+                                const int32_t* __restrict__ labels, float2* __restrict__ part,
+                                float* __restrict__ zlab) {
+  __shared__ float sm[32], ss[32];
+  const size_t t = blockIdx.x;
+  const float* zr = z + t * ld;
+  float m = -INFINITY, s = 0.f;
+  for (int c = threadIdx.x; c < R; c += blockDim.x) lse_merge(m, s, zr[c], 1.f);
+  // warp merge
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o), s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    lse_merge(m, s, m2, s2);
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) {
+    sm[w] = m;
+    ss[w] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = -INFINITY, Sx = 0.f;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) lse_merge(M, Sx, sm[i], ss[i]);
+    part[t] = make_float2(M, Sx);
+    const int lab = labels[t] - row0;
+    if (lab >= 0 && lab < R) zlab[t] = zr[lab];
+  }
+}
+
+__global__ void ce_finalize_kernel(const float2* __restrict__ part, int nslices, const float* __restrict__ zlab,
+                                   float* __restrict__ lse, float* __restrict__ terms, int T) {
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  float M = -INFINITY, Sx = 0.f;
+  for (int s = 0; s < nslices; ++s) {
+    const float2 p = part[(size_t)s * T + t];
+    lse_merge(M, Sx, p.x, p.y);
+  }
+  const float l = M + logf(Sx);
+  lse[t] = l;
+  terms[t] = l - zlab[t];
+}
+
+// Single block: fixed-order sum of the per-token terms.
+__global__ void sum_scaled_kernel(const float* __restrict__ terms, int T, float scale, float* __restrict__ out) {
+  __shared__ float red[32];
+  float s = 0.f;
+  for (int t = threadIdx.x; t < T; t += blockDim.x) s += terms[t];
+  s = block_sum(s, red);
+  if (threadIdx.x == 0) *out = s * scale;
+}
+
+__global__ void ce_grad_kernel(const float* __restrict__ z, int T, int R, int ld, int row0,
+                               const int32_t* __restrict__ labels, const float* __restrict__ lse, float scale,
+                               uint16_t* __restrict__ dz) {
+  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (idx >= (size_t)T * R) return;
+  const size_t t = idx / R;
+  const int c = (int)(idx % R);
+  float g = __expf(z[t * ld + c] - lse[t]);
+  if (labels[t] - row0 == c) g -= 1.f;
+  dz[t * ld + c] = f2bf(g * scale);
+}
+
+inline unsigned blocks_for(size_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
+
+}  // namespace
+
+int rmsnorm_fwd(const float* x, const float* w, uint16_t* y, float* rstd, int T, int h, float eps, cudaStream_t st) {
+  if (T <= 0 || h <= 0 || (h & 3)) return -1;
+  rmsnorm_fwd_kernel<<<T, kThreads, 0, st>>>(x, w, y, rstd, h, eps);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+size_t rmsnorm_bwd_partials(int T, int h) { return (size_t)((T + kNormBwdRows - 1) / kNormBwdRows) * h; }
+
+int rmsnorm_bwd(const float* x, const float* w, const float* rstd, const float* dy, const float* resid, float* dx,
+                uint16_t* dx_bf16, float* dw, float* work, int T, int h, cudaStream_t st) {
+  if (T <= 0 || h <= 0 || (h & 3) || h > kMaxV * 4 * kThreads) return -1;
+  const int nb = (T + kNormBwdRows - 1) / kNormBwdRows;
+  rmsnorm_bwd_kernel<<<nb, kThreads, 0, st>>>(x, w, rstd, dy, resid, dx, dx_bf16, work, T, h);
+  count_launches(1);
+  sum_partials_kernel<<<blocks_for(h, 256), 256, 0, st>>>(work, nb, h, dw);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int rope_table(float2* tab, int S, int d, float theta, cudaStream_t st) {
+  if (S <= 0 || d <= 0 || (d & 1)) return -1;
+  rope_table_kernel<<<blocks_for((size_t)S * d / 2, 256), 256, 0, st>>>(tab, S, d, (double)theta);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int rope_apply(uint16_t* x, const float2* tab, int B, int S, int row_stride, int head0, int n_heads, int d, int dir,
+               cudaStream_t st) {
+  if (d % 8 || (row_stride & 3) || B <= 0 || S <= 0) return -1;
+  const size_t total = (size_t)B * S * n_heads * (d / 8);
+  rope_apply_kernel<<<blocks_for(total, 256), 256, 0, st>>>(x, tab, B * S, S, row_stride, head0, n_heads, d,
+                                                            dir >= 0 ? 1.f : -1.f);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int swiglu_fwd(const uint16_t* gu, uint16_t* act, int T, int F, int ld, cudaStream_t st) {
+  if (T <= 0 || F <= 0 || ld < F) return -1;
+  if (F == ld && (ld % 8) == 0)
+    swiglu_fwd_vec_kernel<<<blocks_for((size_t)T * ld / 8, 256), 256, 0, st>>>(gu, act, T, ld);
+  else
+    swiglu_fwd_kernel<<<blocks_for((size_t)T * ld, 256), 256, 0, st>>>(gu, act, T, F, ld);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int swiglu_bwd(uint16_t* gu, const uint16_t* dact, int T, int F, int ld, cudaStream_t st) {
+  if (T <= 0 || F <= 0 || ld < F) return -1;
+  if (F == ld && (ld % 8) == 0)
+    swiglu_bwd_vec_kernel<<<blocks_for((size_t)T * ld / 8, 256), 256, 0, st>>>(gu, dact, T, ld);
+  else
+    swiglu_bwd_kernel<<<blocks_for((size_t)T * ld, 256), 256, 0, st>>>(gu, dact, T, F, ld);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int embed_gather(const void* E_slice, bool bf16, int row0, int rows, const int32_t* tok, float* h0, int T, int h,
+                 cudaStream_t st) {
+  if (T <= 0 || (h & 3)) return -1;
+  embed_gather_kernel<<<T, 256, 0, st>>>(E_slice, bf16 ? 1 : 0, row0, rows, tok, h0, h);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int embed_scatter(const int32_t* perm, const int32_t* start, int row0, int rows, const float* dh0, float* dE, int h,
+                  cudaStream_t st) {
+  if (rows <= 0 || (h & 3)) return -1;
+  embed_scatter_kernel<<<rows, 256, 0, st>>>(perm, start, row0, dh0, dE, h);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int cast_rows_f32_bf16(const float* src, uint16_t* dst, int rows_src, int rows_dst, int cols, int ld_dst,
+                       cudaStream_t st) {
+  if (rows_src <= 0 || rows_dst < rows_src || cols <= 0 || ld_dst < cols) return -1;
+  cast_rows_kernel<<<blocks_for((size_t)rows_dst * ld_dst, 256), 256, 0, st>>>(src, dst, rows_src, rows_dst, cols,
+                                                                               ld_dst);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int cast_f32_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st) {
+  if (n % 4) return -1;
+  cast_f32_bf16_vec_kernel<<<blocks_for(n / 4, 256), 256, 0, st>>>((const float4*)src, (uint2*)dst, n / 4);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int gains_to_f32(const void* src, bool bf16, float* dst, int n, cudaStream_t st) {
+  gains_kernel<<<blocks_for(n, 256), 256, 0, st>>>(src, bf16 ? 1 : 0, dst, n);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int ce_slice_stats(const float* logits, int T, int R, int ld, int row0, const int32_t* labels, float2* part,
+                   float* zlab, cudaStream_t st) {
+  if (T <= 0 || R <= 0 || ld < R) return -1;
+  ce_stats_kernel<<<T, 256, 0, st>>>(logits, R, ld, row0, labels, part, zlab);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int ce_finalize(const float2* part, int nslices, const float* zlab, float* lse, float* loss_terms, float* loss,
+                int T, float scale, cudaStream_t st) {
+  ce_finalize_kernel<<<blocks_for(T, 256), 256, 0, st>>>(part, nslices, zlab, lse, loss_terms, T);
+  count_launches(1);
+  sum_scaled_kernel<<<1, 1024, 0, st>>>(loss_terms, T, scale, loss);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int ce_slice_grad(const float* logits, int T, int R, int ld, int row0, const int32_t* labels, const float* lse,
+                  float scale, uint16_t* dz, cudaStream_t st) {
+  if (T <= 0 || R <= 0 || ld < R) return -1;
+  ce_grad_kernel<<<blocks_for((size_t)T * R, 256), 256, 0, st>>>(logits, T, R, ld, row0, labels, lse, scale, dz);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace mt

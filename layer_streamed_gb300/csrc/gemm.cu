@@ -1,0 +1,341 @@
+// Dense bf16 GEMM on the 5th-generation tensor cores (tcgen05), fp32
+// accumulation in tensor memory, operands staged by TMA.
+//
+// The layer template's linear maps (QKV, O, gate-up, down, LM head) in their
+// three forms: forward y = x W^T (both operands K-major), input gradient
+// dx = dy W (B stored [K, N], MN-major), weight gradient dW = dy^T x (both
+// operands MN-major, the reduction runs over tokens). MegaTrain (section
+// 核心方法) describes the template as CUDA kernels for the attention and MLP
+// blocks bound to streamed weights; here weights arrive as plain device
+// pointers per launch, so the kernel holds no persistent weight state.
+//
+// Structure: persistent CTAs (one per SM), 128 x BN output tiles, K in steps
+// of 64 (one 128-byte swizzle row), STAGES-deep TMA ring; warp 0 issues TMA,
+// warp 1 issues tcgen05.mma from one thread, warps 2-5 drain the two TMEM
+// accumulators (2 x BN columns) so the epilogue of tile i overlaps the
+// mainloop of tile i+1. Each output tile is produced by one CTA with a fixed
+// K order, so results do not depend on the grid size (deterministic).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mt {
+
+MT_DEVICE_ERROR_READER(gemm_take_device_error)
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES = (BN == 256) ? 4 : 6;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int TMEM_COLS = 2 * BN;
+};
+
+// Tile order: groups of GROUP_M row-blocks, row-block fastest inside a group,
+// so a wave of CTAs shares a band of A rows and a few B column-blocks in L2.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_blk) {
+  constexpr int GROUP_M = 16;
+  const int per_group = GROUP_M * num_n;
+  const int g = tile / per_group;
+  const int first_m = g * GROUP_M;
+  const int gsize = min(num_m - first_m, GROUP_M);
+  const int r = tile - g * per_group;
+  m_blk = first_m + r % gsize;
+  n_blk = r / gsize;
+}
+
+template <int BN, bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  using C = GemmCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * A_BYTES;
+  uint64_t* full = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 4);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int num_m = (p.M + BM - 1) / BM, num_n = (p.N + BN - 1) / BN;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (p.K + BK - 1) / BK;
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, mb, nb);
+        const int m0 = mb * BM, n0 = nb * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          mbar_wait(&empty[stage], phase ^ 1, abort_flag, kErrTimeoutTma);
+          mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+          uint8_t* a_dst = sA + stage * A_BYTES;
+          uint8_t* b_dst = sB + stage * C::B_BYTES;
+          if (!A_MN) {
+            tma_load_2d(a_dst, &tmA, &full[stage], kb * BK, m0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * 8192, &tmA, &full[stage], m0 + 64 * j, kb * BK);
+          }
+          if (!B_MN) {
+            tma_load_2d(b_dst, &tmB, &full[stage], kb * BK, n0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, &full[stage], n0 + 64 * j, kb * BK);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {  // MMA issuer
+      constexpr uint32_t IDESC = make_idesc(BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, kErrTimeoutMma);
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          mbar_wait(&full[stage], phase, abort_flag, kErrTimeoutMma);
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? make_sdesc(a_base + kk * 2048, 8192, 1024) : make_sdesc(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? make_sdesc(b_base + kk * 2048, 8192, 1024) : make_sdesc(b_base + kk * 32, 16, 1024);
+            tc_mma(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+          }
+          tc_commit(&empty[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        tc_commit(&tfull[acc]);
+      }
+    }
+    __syncwarp();
+  } else {  // epilogue warps 2..5; warp w reads TMEM lanes 32*(w%4) .. +31
+    const uint32_t q = warp & 3;
+    int local = 0;
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, mb, nb);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      mbar_wait(&tfull[acc], acc_phase, abort_flag, kErrTimeoutEpi);
+      tc_fence_after();
+      const int row = mb * BM + q * 32 + lane;
+      const bool row_ok = row < p.M;
+#pragma unroll 1
+      for (int c = 0; c < BN / 32; ++c) {
+        uint32_t r[32];
+        __syncwarp();
+        tmem_ld32(tmem_base + ((q * 32) << 16) + acc * BN + c * 32, r);
+        tmem_ld_wait();
+        const int col0 = nb * BN + c * 32;
+        if (row_ok && col0 < p.N) {
+        const bool full_cols = p.vec && col0 + 32 <= p.N;
+        if (p.epi == EPI_BF16) {
+          uint16_t* out = (uint16_t*)p.C + (size_t)row * p.ldc + col0;
+          if (full_cols) {
+            uint4* o4 = (uint4*)out;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              uint4 w;
+              w.x = pack_bf2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+              w.y = pack_bf2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+              w.z = pack_bf2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+              w.w = pack_bf2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+              o4[v] = w;
+            }
+          } else {
+            for (int j = 0; j < 32 && col0 + j < p.N; ++j) out[j] = f2bf(__uint_as_float(r[j]));
+          }
+        } else {
+          float* out = (float*)p.C + (size_t)row * p.ldc + col0;
+          const float* add = p.epi == EPI_F32_ADD ? (const float*)p.addend + (size_t)row * p.ldc + col0 : nullptr;
+          if (full_cols) {
+#pragma unroll
+            for (int v = 0; v < 8; ++v) {
+              float4 w = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                     __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+              if (add) {
+                const float4 a = ((const float4*)add)[v];
+                w.x += a.x;
+                w.y += a.y;
+                w.z += a.z;
+                w.w += a.w;
+              }
+              ((float4*)out)[v] = w;
+            }
+          } else {
+            for (int j = 0; j < 32 && col0 + j < p.N; ++j) out[j] = __uint_as_float(r[j]) + (add ? add[j] : 0.f);
+          }
+        }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+    }
+  }
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+template <int BN, bool A_MN, bool B_MN>
+int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st) {
+  using C = GemmCfg<BN>;
+  static bool attr_set = false;
+  auto kern = gemm_kernel<BN, A_MN, B_MN>;
+  if (!attr_set) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
+    attr_set = true;
+  }
+  const int tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+  const int grid = tiles < mt_host::num_sms() ? tiles : mt_host::num_sms();
+  kern<<<grid, 192, C::SMEM, st>>>(ta, tb, p);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+// Tensor map of a bf16 matrix stored row-major with `rows` rows of `cols`
+// valid elements and row stride `ld` (elements). box_inner is along cols.
+int make_map(CUtensorMap* m, const void* base, int rows, int cols, int ld, int box_inner, int box_outer) {
+  const uint64_t gdim[2] = {(uint64_t)cols, (uint64_t)rows};
+  const uint64_t gstride[1] = {(uint64_t)ld * 2};
+  const uint32_t box[2] = {(uint32_t)box_inner, (uint32_t)box_outer};
+  return mt_host::encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, gdim, gstride, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS
+             ? 0
+             : -1;
+}
+
+}  // namespace
+
+int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int lda, int ldb, cudaStream_t st) {
+  GemmParams p = pin;
+  if (p.M <= 0 || p.N <= 0 || p.K <= 0 || !p.C || p.epi < EPI_BF16 || p.epi > EPI_F32_ADD) return -1;
+  if ((lda & 7) || (ldb & 7) || ((uintptr_t)A & 15) || ((uintptr_t)B & 15)) return -1;
+  if (p.epi == EPI_F32_ADD && !p.addend) return -1;
+  // 16-byte stores need 16-byte aligned rows; otherwise the epilogue stores element by element.
+  const int esz = p.epi == EPI_BF16 ? 2 : 4;
+  p.vec = (((uintptr_t)p.C & 15) == 0 && ((size_t)p.ldc * esz) % 16 == 0 &&
+           (p.epi != EPI_F32_ADD || ((uintptr_t)p.addend & 15) == 0))
+              ? 1
+              : 0;
+  // BN = 256 unless that leaves most SMs idle.
+  const int tiles256 = ((p.M + BM - 1) / BM) * ((p.N + 255) / 256);
+  const bool wide = tiles256 >= mt_host::num_sms();
+  const int BN = wide ? 256 : 128;
+  CUtensorMap ta, tb;
+  int rc = 0;
+  if (mode == GEMM_NT) {  // A [M,K] K-major, B [N,K] K-major
+    rc |= make_map(&ta, A, p.M, p.K, lda, 64, BM);
+    rc |= make_map(&tb, B, p.N, p.K, ldb, 64, BN);
+    if (rc) return -1;
+    return wide ? launch<256, false, false>(ta, tb, p, st) : launch<128, false, false>(ta, tb, p, st);
+  }
+  if (mode == GEMM_NN) {  // A [M,K] K-major, B stored [K,N]: MN-major
+    rc |= make_map(&ta, A, p.M, p.K, lda, 64, BM);
+    rc |= make_map(&tb, B, p.K, p.N, ldb, 64, 64);
+    if (rc) return -1;
+    return wide ? launch<256, false, true>(ta, tb, p, st) : launch<128, false, true>(ta, tb, p, st);
+  }
+  if (mode == GEMM_TN) {  // A stored [K,M], B stored [K,N]: both MN-major
+    rc |= make_map(&ta, A, p.K, p.M, lda, 64, 64);
+    rc |= make_map(&tb, B, p.K, p.N, ldb, 64, 64);
+    if (rc) return -1;
+    return wide ? launch<256, true, true>(ta, tb, p, st) : launch<128, true, true>(ta, tb, p, st);
+  }
+  (void)BN;
+  return -1;
+}
+
+}  // namespace mt
+
+namespace mt_host {
+
+CUresult encode_tiled(CUtensorMap* map, CUtensorMapDataType dt, uint32_t rank, const void* gaddr,
+                      const uint64_t* gdim, const uint64_t* gstride_bytes, const uint32_t* box,
+                      CUtensorMapSwizzle swz) {
+  typedef CUresult (*Fn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*, const cuuint64_t*,
+                         const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                         CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+  static Fn fn = nullptr;
+  if (!fn) {
+    cudaDriverEntryPointQueryResult q;
+    void* f = nullptr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || !f)
+      return CUDA_ERROR_NOT_FOUND;
+    fn = (Fn)f;
+  }
+  cuuint32_t estr[5] = {1, 1, 1, 1, 1};
+  return fn(map, dt, rank, const_cast<void*>(gaddr), (const cuuint64_t*)gdim, (const cuuint64_t*)gstride_bytes,
+            (const cuuint32_t*)box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
+int num_sms() {
+  static int n = 0;
+  if (!n) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+    if (n <= 0) n = 1;
+  }
+  return n;
+}
+
+}  // namespace mt_host

@@ -1,0 +1,86 @@
+// Internal launch interface of the layer-template kernels (host side).
+// Every launcher returns 0 on success and -1 on a bad argument or a failed
+// launch; none allocates memory.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace mt {
+
+// Number of kernels launched by the launchers below (host-side counter,
+// read by the runtime to report launches per step).
+extern long g_kernel_launches;
+inline void count_launches(int n) { g_kernel_launches += n; }
+
+enum { GEMM_NT = 0, GEMM_NN = 1, GEMM_TN = 2 };
+enum { EPI_BF16 = 0, EPI_F32 = 1, EPI_F32_ADD = 2 };
+
+struct GemmParams {
+  int M, N, K;
+  int epi;
+  void* C;
+  const void* addend;  // EPI_F32_ADD: C = addend + acc (same row stride)
+  int ldc;
+  int vec;  // set by gemm_bf16: 1 if C rows allow 16-byte stores
+};
+
+// C[M,N] = op(A) op(B) with bf16 operands, fp32 accumulation (see gemm.cu).
+int gemm_bf16(int mode, const GemmParams& p, const void* A, const void* B, int lda, int ldb, cudaStream_t st);
+
+// RMSNorm (elementwise.cu)
+int rmsnorm_fwd(const float* x, const float* w, uint16_t* y, float* rstd, int T, int h, float eps, cudaStream_t st);
+size_t rmsnorm_bwd_partials(int T, int h);  // floats of workspace
+int rmsnorm_bwd(const float* x, const float* w, const float* rstd, const float* dy, const float* resid, float* dx,
+                uint16_t* dx_bf16, float* dw, float* work, int T, int h, cudaStream_t st);
+
+// RoPE table [S, d/2] of (cos, sin) and in-place rotation of bf16 heads.
+int rope_table(float2* tab, int S, int d, float theta, cudaStream_t st);
+int rope_apply(uint16_t* x, const float2* tab, int B, int S, int row_stride, int head0, int n_heads, int d, int dir,
+               cudaStream_t st);
+
+// SwiGLU on gu [T, 2*ld] (gate [0,F), up [ld, ld+F)).
+int swiglu_fwd(const uint16_t* gu, uint16_t* act, int T, int F, int ld, cudaStream_t st);
+int swiglu_bwd(uint16_t* gu, const uint16_t* dact, int T, int F, int ld, cudaStream_t st);
+
+// Embedding rows [row0, row0+rows) of E (fp32 or bf16, row stride h):
+// h0[t] = E[tok[t]] for tokens in range.
+int embed_gather(const void* E_slice, bool bf16, int row0, int rows, const int32_t* tok, float* h0, int T, int h,
+                 cudaStream_t st);
+// dE[v - row0] = sum over t with tok[t] = v (in ascending t) of dh0[t], for
+// every v in the slice; perm/start: tokens stably sorted by id (CSR over vocab).
+int embed_scatter(const int32_t* perm, const int32_t* start, int row0, int rows, const float* dh0, float* dE, int h,
+                  cudaStream_t st);
+
+// Weight preparation: fp32 [rows_src, cols] -> bf16 [rows_dst, ld_dst]
+// (rows >= rows_src and columns >= cols are zero); bf16/fp32 gains -> fp32.
+int cast_rows_f32_bf16(const float* src, uint16_t* dst, int rows_src, int rows_dst, int cols, int ld_dst,
+                       cudaStream_t st);
+int gains_to_f32(const void* src, bool bf16, float* dst, int n, cudaStream_t st);
+
+// Cross-entropy over vocab slices of materialised fp32 logits [T, R] (row
+// stride ld): per-row (max, sum exp) partials, merged in slice order.
+int ce_slice_stats(const float* logits, int T, int R, int ld, int row0, const int32_t* labels, float2* part,
+                   float* zlab, cudaStream_t st);
+int ce_finalize(const float2* part, int nslices, const float* zlab, float* lse, float* loss_terms, float* loss,
+                int T, float scale, cudaStream_t st);
+int ce_slice_grad(const float* logits, int T, int R, int ld, int row0, const int32_t* labels, const float* lse,
+                  float scale, uint16_t* dz, cudaStream_t st);
+
+// Attention (attention.cu)
+int attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int B, int S,
+                  int nq, int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
+size_t attention_bwd_workspace(int B, int S, int nq);  // floats
+int attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
+                  const float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv, float* work, int B, int S, int nq,
+                  int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
+
+// Read and clear the device error words of the kernels that wait on
+// barriers (0 = no error). Synchronous with respect to the device.
+uint32_t gemm_take_device_error();
+uint32_t attention_take_device_error();
+
+// fp32 -> bf16 copy of a dense buffer.
+int cast_f32_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st);
+
+}  // namespace mt

@@ -1,0 +1,118 @@
+// Kernel-level C entry points (declared in include/mt.h): thin argument
+// checks in front of the layer-template launchers, for tests and
+// measurement. They allocate nothing.
+#include "../../include/mt.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace mt;
+
+namespace {
+inline cudaStream_t S(void* s) { return (cudaStream_t)s; }
+inline int rc(int r) {
+  if (r == 0) return MT_OK;
+  return cudaPeekAtLastError() != cudaSuccess ? MT_ERR_CUDA : MT_ERR_ARG;
+}
+size_t rup(size_t x, size_t a) { return (x + a - 1) / a * a; }
+}  // namespace
+
+extern "C" {
+
+int mt_op_gemm(int mode, int epi, const void* A, const void* B, void* C, const void* addend, int M, int N, int K,
+               int lda, int ldb, int ldc, void* stream) {
+  if (!A || !B || !C) return MT_ERR_ARG;
+  GemmParams p{M, N, K, epi, C, addend, ldc, 0};
+  return rc(gemm_bf16(mode, p, A, B, lda, ldb, S(stream)));
+}
+
+int mt_op_rmsnorm_fwd(const float* x, const float* w, void* y, float* rstd, int T, int h, float eps, void* stream) {
+  if (!x || !w || !y || !rstd) return MT_ERR_ARG;
+  return rc(rmsnorm_fwd(x, w, (uint16_t*)y, rstd, T, h, eps, S(stream)));
+}
+
+size_t mt_op_rmsnorm_bwd_workspace(int T, int h) { return rmsnorm_bwd_partials(T, h); }
+
+int mt_op_rmsnorm_bwd(const float* x, const float* w, const float* rstd, const float* dy, const float* resid,
+                      float* dx, void* dx_bf16, float* dw, float* workspace, int T, int h, void* stream) {
+  if (!x || !w || !rstd || !dy || !dx || !dw || !workspace) return MT_ERR_ARG;
+  return rc(rmsnorm_bwd(x, w, rstd, dy, resid, dx, (uint16_t*)dx_bf16, dw, workspace, T, h, S(stream)));
+}
+
+int mt_op_rope(void* x, float* table, int B, int S_, int row_stride, int head0, int n_heads, int d, float theta,
+               int dir, void* stream) {
+  if (!x || !table || B < 1 || S_ < 1 || d < 8 || (dir != 1 && dir != -1)) return MT_ERR_ARG;
+  float2* tab = (float2*)table;
+  if (rope_table(tab, S_, d, theta, S(stream))) return rc(-1);
+  return rc(rope_apply((uint16_t*)x, tab, B, S_, row_stride, head0, n_heads, d, dir, S(stream)));
+}
+
+int mt_op_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_, int n_heads,
+                        int n_kv_heads, int d, int ldq, int ldkv, int ldo, void* stream) {
+  if (!q || !k || !v || !o || !lse) return MT_ERR_ARG;
+  return rc(attention_fwd((const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, (uint16_t*)o, lse, B, S_,
+                          n_heads, n_kv_heads, d, ldq, ldkv, ldo, S(stream)));
+}
+
+size_t mt_op_attention_bwd_workspace(int B, int S_, int n_heads) { return attention_bwd_workspace(B, S_, n_heads); }
+
+int mt_op_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_, const float* lse,
+                        void* dq, void* dk, void* dv, float* workspace, int B, int S_, int n_heads, int n_kv_heads,
+                        int d, int ldq, int ldkv, int ldo, void* stream) {
+  if (!q || !k || !v || !o || !do_ || !lse || !dq || !dk || !dv || !workspace) return MT_ERR_ARG;
+  return rc(attention_bwd((const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, (const uint16_t*)o,
+                          (const uint16_t*)do_, lse, (uint16_t*)dq, (uint16_t*)dk, (uint16_t*)dv, workspace, B, S_,
+                          n_heads, n_kv_heads, d, ldq, ldkv, ldo, S(stream)));
+}
+
+int mt_op_swiglu_fwd(const void* gu, void* act, int T, int F, int ld, void* stream) {
+  if (!gu || !act) return MT_ERR_ARG;
+  return rc(swiglu_fwd((const uint16_t*)gu, (uint16_t*)act, T, F, ld, S(stream)));
+}
+
+int mt_op_swiglu_bwd(void* gu, const void* dact, int T, int F, int ld, void* stream) {
+  if (!gu || !dact) return MT_ERR_ARG;
+  return rc(swiglu_bwd((uint16_t*)gu, (const uint16_t*)dact, T, F, ld, S(stream)));
+}
+
+size_t mt_op_lmhead_ce_workspace(int T, int V, int h) {
+  (void)h;
+  const size_t ld = rup((size_t)V, 8);
+  return rup((size_t)T * ld * 4, 256) + rup((size_t)T * ld * 2, 256) + rup((size_t)T * 8, 256) +
+         3 * rup((size_t)T * 4, 256);
+}
+
+int mt_op_lmhead_ce(const void* X, const void* W, const int32_t* labels, float scale, float* dX, float* dW,
+                    float* loss_dev, void* workspace, int T, int V, int h, void* stream) {
+  if (!X || !W || !labels || !dX || !dW || !loss_dev || !workspace || T < 1 || V < 1 || h < 1) return MT_ERR_ARG;
+  const int ld = (int)rup((size_t)V, 8);
+  uint8_t* w = (uint8_t*)workspace;
+  float* logits = (float*)w;
+  w += rup((size_t)T * ld * 4, 256);
+  uint16_t* dz = (uint16_t*)w;
+  w += rup((size_t)T * ld * 2, 256);
+  float2* part = (float2*)w;
+  w += rup((size_t)T * 8, 256);
+  float* zlab = (float*)w;
+  w += rup((size_t)T * 4, 256);
+  float* lse = (float*)w;
+  w += rup((size_t)T * 4, 256);
+  float* terms = (float*)w;
+  cudaStream_t st = S(stream);
+  GemmParams p1{T, V, h, EPI_F32, logits, nullptr, ld, 0};
+  if (gemm_bf16(GEMM_NT, p1, X, W, h, h, st)) return rc(-1);
+  if (ce_slice_stats(logits, T, V, ld, 0, labels, part, zlab, st)) return rc(-1);
+  if (ce_finalize(part, 1, zlab, lse, terms, loss_dev, T, scale, st)) return rc(-1);
+  if (ce_slice_grad(logits, T, V, ld, 0, labels, lse, scale, dz, st)) return rc(-1);
+  GemmParams p2{T, h, V, EPI_F32, dX, nullptr, h, 0};
+  if (gemm_bf16(GEMM_NN, p2, dz, W, ld, h, st)) return rc(-1);
+  GemmParams p3{V, h, T, EPI_F32, dW, nullptr, h, 0};
+  if (gemm_bf16(GEMM_TN, p3, dz, X, ld, h, st)) return rc(-1);
+  return MT_OK;
+}
+
+int mt_op_device_error(void) {
+  cudaDeviceSynchronize();
+  return (int)(gemm_take_device_error() | attention_take_device_error());
+}
+
+}  // extern "C"

@@ -1,0 +1,1179 @@
+// Host runtime of the layer-streamed step: packed layout, device arena
+// partition, and the StreamIn-Bind-Compute-Offload schedule over three CUDA
+// streams ordered by events ("MegaTrain: Full Precision Training of 100B+
+// Parameter Large Language Models on a Single GPU", sections 核心方法,
+// 方法步骤详情 and 技术新颖性).
+//
+//  - Host memory is the parameter and gradient store; the device holds two
+//    weight buffers (ping-pong: the copy of unit i+1 runs while unit i
+//    computes), two gradient staging buffers (the D2H copy of layer i's
+//    gradients runs while layer i-1 back-propagates), the residual-stream
+//    checkpoints h_0, h_K, h_2K, ... and the saved activations of one block
+//    of K layers.
+//  - The weight stream waits "buffer-free" before overwriting a buffer and
+//    records "weight-ready"; the compute stream waits "weight-ready", and
+//    "gradient-buffer-free" before writing a staging buffer, then records
+//    "backward-done"; the grad stream waits "backward-done", copies, records
+//    "gradient-buffer-free". No host barrier inside the step; no CUDA graph
+//    (the bound weights change every unit).
+//  - Block loop (the pages' loop bounds overrun L when L is a multiple of K;
+//    the reading taken here): blocks b = ceil(L/K)-1 .. 0 cover layers
+//    bK+1 .. min((b+1)K, L); the top block's activations are still in the
+//    block arena after the forward pass, so it is not recomputed (the
+//    result is identical; RoundPipe's "fused stage" observation).
+#include <algorithm>
+#include <chrono>
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <thread>
+#include <vector>
+
+#include "../../include/mt.h"
+#include "common.cuh"
+#include "kernels.h"
+
+using namespace mt;
+
+namespace mt {
+long g_kernel_launches = 0;
+}
+
+namespace {
+
+size_t rup(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+// ---------------------------------------------------------------------------
+// Packed layout
+// ---------------------------------------------------------------------------
+int tensors_in_unit(const mt_layer_cfg& c, int u) {
+  if (u == 0) return 1;
+  if (u >= 1 && u <= c.n_layers) return 9;
+  if (u == c.n_layers + 1) return 2;
+  return 0;
+}
+
+size_t tensor_numel(const mt_layer_cfg& c, int u, int t) {
+  const size_t h = c.hidden, qd = (size_t)c.n_heads * c.head_dim, kd = (size_t)c.n_kv_heads * c.head_dim,
+               F = c.ffn_dim, V = c.vocab;
+  if (u == 0) return V * h;
+  if (u == c.n_layers + 1) return t == 0 ? h : V * h;
+  static const int kind[9] = {0, 1, 2, 2, 3, 0, 4, 4, 4};
+  switch (kind[t]) {
+    case 0: return h;
+    case 1: return qd * h;
+    case 2: return kd * h;
+    case 3: return h * qd;
+    default: return F * h;
+  }
+}
+
+// offsets[u][t] in bytes for element size esz; returns total bytes.
+size_t build_layout(const mt_layer_cfg& c, size_t esz, std::vector<std::vector<size_t>>* offs) {
+  size_t pos = 0;
+  if (offs) offs->assign(c.n_layers + 2, {});
+  for (int u = 0; u <= c.n_layers + 1; ++u) {
+    pos = rup(pos, 4096);
+    for (int t = 0; t < tensors_in_unit(c, u); ++t) {
+      pos = rup(pos, 256);
+      if (offs) (*offs)[u].push_back(pos);
+      pos += tensor_numel(c, u, t) * esz;
+    }
+  }
+  return rup(pos, 4096);
+}
+
+bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
+  auto fail = [&](const char* m) {
+    if (why) *why = m;
+    return false;
+  };
+  if (c.n_layers < 1 || c.hidden < 64 || c.n_heads < 1 || c.n_kv_heads < 1 || c.ffn_dim < 1 || c.vocab < 1)
+    return fail("non-positive dimension");
+  if (c.hidden % 64) return fail("hidden must be a multiple of 64");
+  if (c.hidden > 8192) return fail("hidden above 8192 is not supported");
+  if (c.n_heads % c.n_kv_heads) return fail("n_heads must be a multiple of n_kv_heads");
+  if (c.head_dim != 16 && c.head_dim != 32 && c.head_dim != 64 && c.head_dim != 128)
+    return fail("head_dim must be 16, 32, 64 or 128");
+  if (c.param_dtype != MT_F32 && c.param_dtype != MT_BF16) return fail("param_dtype must be MT_F32 or MT_BF16");
+  if (c.param_dtype == MT_BF16 && c.ffn_dim % 8) return fail("bf16 params need ffn_dim % 8 == 0");
+  if (c.max_batch < 1 || c.max_seq < 1 || c.max_K < 1) return fail("max_batch, max_seq, max_K must be >= 1");
+  if (c.n_experts || c.top_k || c.expert_ffn) return fail("mixture-of-experts layers are not implemented");
+  if (!(c.rope_theta > 0.f) || !(c.norm_eps > 0.f)) return fail("rope_theta and norm_eps must be positive");
+  if ((double)c.max_batch * c.max_seq > 2147483647.0 / 4) return fail("too many tokens");
+  return true;
+}
+
+// ---------------------------------------------------------------------------
+// Arena plan
+// ---------------------------------------------------------------------------
+struct Plan {
+  // dims
+  int L, h, nq, nkv, d, F, Fp, V, qd, kd, qkv, Tmax;
+  size_t esz;
+  // slicing of vocab-sized units
+  int head_rows, n_head_slices, emb_rows, n_emb_slices, embg_rows, n_embg_slices;
+  // sizes
+  size_t wbuf, wcast, gbuf, ckpt_one, act_layer, fixed_ws, dyn_max, total;
+  // activation layout inside one block-arena slot (byte offsets)
+  size_t o_x, o_a, o_rstd1, o_qkv, o_o, o_lse, o_hmid, o_m, o_rstd2, o_gu, o_act;
+};
+
+size_t layer_cast_bytes(const Plan& p) {  // device bf16 view of one layer (fp32 params)
+  return rup((size_t)p.qkv * p.h * 2, 256) + rup((size_t)p.h * p.qd * 2, 256) + rup((size_t)2 * p.Fp * p.h * 2, 256) +
+         rup((size_t)p.h * p.Fp * 2, 256);
+}
+
+bool make_plan(const mt_layer_cfg& c, Plan* P) {
+  Plan& p = *P;
+  p.L = c.n_layers;
+  p.h = c.hidden;
+  p.nq = c.n_heads;
+  p.nkv = c.n_kv_heads;
+  p.d = c.head_dim;
+  p.F = c.ffn_dim;
+  p.Fp = c.param_dtype == MT_BF16 ? c.ffn_dim : (int)rup(c.ffn_dim, 8);
+  p.V = c.vocab;
+  p.qd = p.nq * p.d;
+  p.kd = p.nkv * p.d;
+  p.qkv = p.qd + 2 * p.kd;
+  p.Tmax = c.max_batch * c.max_seq;
+  p.esz = c.param_dtype == MT_BF16 ? 2 : 4;
+  std::vector<std::vector<size_t>> o;
+  build_layout(c, p.esz, &o);
+  const size_t layer_bytes = (o[1][8] + tensor_numel(c, 1, 8) * p.esz) - o[1][0];
+  // vocab slices: the fewest equal slices (multiples of 256 rows) that fit a layer buffer
+  auto slices = [&](size_t row_bytes, size_t cap, int* rows, int* n) {
+    int ns = (int)std::max<size_t>(1, (p.V * row_bytes + cap - 1) / cap);
+    while (true) {
+      int r = (int)rup((p.V + ns - 1) / ns, 256);
+      if (r > p.V) r = p.V;
+      if ((size_t)r * row_bytes <= cap || r <= 256) {
+        *rows = r;
+        *n = (p.V + r - 1) / r;
+        return;
+      }
+      ++ns;
+    }
+  };
+  slices((size_t)p.h * p.esz, layer_bytes, &p.head_rows, &p.n_head_slices);
+  slices((size_t)p.h * p.esz, layer_bytes, &p.emb_rows, &p.n_emb_slices);
+  const size_t layer_grad_bytes = layer_bytes / p.esz * 4;
+  slices((size_t)p.h * 4, layer_grad_bytes, &p.embg_rows, &p.n_embg_slices);
+  p.wbuf = rup(std::max({layer_bytes, (size_t)p.head_rows * p.h * p.esz, (size_t)p.emb_rows * p.h * p.esz}), 4096);
+  p.wcast = p.esz == 4 ? rup(std::max(layer_cast_bytes(p), (size_t)p.head_rows * p.h * 2), 4096) : 0;
+  p.gbuf = rup(std::max({layer_grad_bytes, (size_t)p.head_rows * p.h * 4, (size_t)p.embg_rows * p.h * 4,
+                         (size_t)p.h * 4}),
+               4096);
+  const size_t T = p.Tmax, h = p.h;
+  p.ckpt_one = rup(T * h * 4, 256);
+  size_t a = 0;
+  auto take = [&](size_t bytes) {
+    size_t r = a;
+    a += rup(bytes, 256);
+    return r;
+  };
+  p.o_x = take(T * h * 4);
+  p.o_a = take(T * h * 2);
+  p.o_rstd1 = take(T * 4);
+  p.o_qkv = take(T * p.qkv * 2);
+  p.o_o = take(T * p.qd * 2);
+  p.o_lse = take(T * p.nq * 4);
+  p.o_hmid = take(T * h * 4);
+  p.o_m = take(T * h * 2);
+  p.o_rstd2 = take(T * 4);
+  p.o_gu = take(T * 2 * p.Fp * 2);
+  p.o_act = take(T * p.Fp * 2);
+  p.act_layer = rup(a, 4096);
+  // fixed workspace (see Ctx::carve)
+  size_t w = 0;
+  auto ws = [&](size_t bytes) { w += rup(bytes, 256); };
+  ws(T * h * 4);                                   // h_top (h_L)
+  ws(T * h * 4);                                   // dh
+  ws(T * h * 2);                                   // dh bf16
+  ws(T * h * 4);                                   // dm / da / dxf
+  ws(T * h * 2);                                   // dhmid bf16
+  ws(T * p.qd * 2);                                // do
+  ws(T * p.qkv * 2);                               // dqkv
+  ws(attention_bwd_workspace(c.max_batch, c.max_seq, p.nq) * 4);
+  ws(rmsnorm_bwd_partials((int)T, p.h) * 4);
+  ws(T * h * 2);                                   // xf bf16
+  ws(T * 4);                                       // rstd_f
+  ws(T * (size_t)p.head_rows * 4);                 // logits slice fp32
+  ws(T * (size_t)p.head_rows * 2);                 // dz slice bf16
+  ws((size_t)p.n_head_slices * T * 8);             // CE partials
+  ws(T * 4 * 3);                                   // zlab, lse, terms
+  ws(256);                                         // loss
+  ws((T * 3 + p.V + 1) * 4);                       // tokens, labels, perm, start
+  ws((size_t)c.max_seq * p.d / 2 * 8);             // rope table
+  ws(2 * 2 * (size_t)p.h * 4);                     // gains of the two weight slots
+  ws((size_t)p.h * 4 * 2);                         // final norm gain (raw + fp32)
+  p.fixed_ws = w;
+  // dynamic part: checkpoints for ceil(L/K) blocks + K activation slots
+  p.dyn_max = 0;
+  for (int K = 1; K <= std::min(c.max_K, p.L); ++K) {
+    const size_t nb = (p.L + K - 1) / K;
+    p.dyn_max = std::max(p.dyn_max, nb * p.ckpt_one + (size_t)K * p.act_layer);
+  }
+  p.total = 2 * p.wbuf + 2 * p.wcast + 2 * p.gbuf + p.fixed_ws + p.dyn_max + 4096;
+  return true;
+}
+
+// One use of a streamed weight unit (or vocab slice) by the compute stream.
+enum ItemKind { IT_EMB = 0, IT_LAYER = 1, IT_HEAD = 2 };
+struct Item {
+  int kind, index;  // layer index 1..L, or slice index
+  bool operator==(const Item& o) const { return kind == o.kind && index == o.index; }
+};
+
+// Pool of timing events.
+struct Seg {
+  int stream;  // 0 compute, 1 h2d, 2 d2h
+  cudaEvent_t a, b;
+  double bytes;
+};
+// Per-kernel timing (trace level 2): category 0 GEMM, 1 attention.
+struct OpSeg {
+  int cat;
+  cudaEvent_t a, b;
+  double flop;
+};
+
+}  // namespace
+
+struct mt_ctx {
+  mt_layer_cfg cfg;
+  Plan P;
+  std::vector<std::vector<size_t>> off_p, off_g;  // host param layout, fp32 grad layout
+  int device = 0;
+  cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
+  bool own_streams = false;
+  cudaEvent_t ev_wready[2], ev_wfree[2], ev_bwd_done[2], ev_gfree[2], ev_done = nullptr;
+  uint8_t* arena = nullptr;
+  size_t arena_bytes = 0;
+  bool own_arena = false;
+  // carved regions
+  uint8_t* wbuf[2];
+  uint16_t* wcast[2];
+  float* gbuf[2];
+  uint8_t* dyn = nullptr;
+  float *h_top, *dh, *dm, *attn_ws, *norm_ws, *rstd_f, *logits, *zlab, *lse, *terms, *loss_dev, *gains[2], *wf32;
+  uint16_t *dh_b, *dhmid_b, *do_b, *dqkv, *xf_b, *dz;
+  float2 *ce_part, *rope_tab;
+  int32_t *tok_d, *lab_d, *perm_d, *start_d;
+  void* wf_raw;
+  int32_t* host_stage = nullptr;  // pinned: tokens, labels, perm, start
+  int rope_S = -1;
+  const void* host_params = nullptr;
+  std::string err;
+  mt_stats stats{};
+  int trace = 1;
+  bool fuse_top = true;
+  std::vector<Seg> segs;
+  std::vector<OpSeg> opsegs;
+  long launches_at_start = 0;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  cudaEvent_t ev_base = nullptr;
+  int fault_kind = 0, fault_nth = 0, fault_count = 0;
+  // resident weight slots
+  Item slot_item[2];
+  bool slot_valid[2];
+  int gslot = 0;
+};
+
+namespace {
+
+int set_err(mt_ctx* c, int code, const std::string& m) {
+  if (c) c->err = m;
+  return code;
+}
+
+#define CK(call)                                                                               \
+  do {                                                                                         \
+    cudaError_t e_ = (call);                                                                   \
+    if (e_ != cudaSuccess)                                                                     \
+      return set_err(ctx, MT_ERR_CUDA, std::string(#call) + ": " + cudaGetErrorString(e_));  \
+  } while (0)
+#define CKL(call)                                                                \
+  do {                                                                           \
+    if ((call) != 0) {                                                           \
+      cudaError_t e_ = cudaGetLastError();                                       \
+      return set_err(ctx, e_ != cudaSuccess ? MT_ERR_CUDA : MT_ERR_ARG,          \
+                     std::string(#call) + " failed: " + cudaGetErrorString(e_)); \
+    }                                                                            \
+  } while (0)
+
+int carve(mt_ctx* ctx) {
+  const Plan& p = ctx->P;
+  uint8_t* cur = (uint8_t*)rup((uintptr_t)ctx->arena, 4096);
+  auto take = [&](size_t bytes) {
+    uint8_t* r = cur;
+    cur += rup(bytes, 256);
+    return r;
+  };
+  for (int i = 0; i < 2; ++i) ctx->wbuf[i] = take(p.wbuf);
+  for (int i = 0; i < 2; ++i) ctx->wcast[i] = p.wcast ? (uint16_t*)take(p.wcast) : nullptr;
+  for (int i = 0; i < 2; ++i) ctx->gbuf[i] = (float*)take(p.gbuf);
+  const size_t T = p.Tmax, h = p.h;
+  ctx->h_top = (float*)take(T * h * 4);
+  ctx->dh = (float*)take(T * h * 4);
+  ctx->dh_b = (uint16_t*)take(T * h * 2);
+  ctx->dm = (float*)take(T * h * 4);
+  ctx->dhmid_b = (uint16_t*)take(T * h * 2);
+  ctx->do_b = (uint16_t*)take(T * p.qd * 2);
+  ctx->dqkv = (uint16_t*)take(T * p.qkv * 2);
+  ctx->attn_ws = (float*)take(attention_bwd_workspace(ctx->cfg.max_batch, ctx->cfg.max_seq, p.nq) * 4);
+  ctx->norm_ws = (float*)take(rmsnorm_bwd_partials((int)T, p.h) * 4);
+  ctx->xf_b = (uint16_t*)take(T * h * 2);
+  ctx->rstd_f = (float*)take(T * 4);
+  ctx->logits = (float*)take(T * (size_t)p.head_rows * 4);
+  ctx->dz = (uint16_t*)take(T * (size_t)p.head_rows * 2);
+  ctx->ce_part = (float2*)take((size_t)p.n_head_slices * T * 8);
+  ctx->zlab = (float*)take(T * 4);
+  ctx->lse = (float*)take(T * 4);
+  ctx->terms = (float*)take(T * 4);
+  ctx->loss_dev = (float*)take(256);
+  int32_t* ints = (int32_t*)take((T * 3 + p.V + 1) * 4);
+  ctx->tok_d = ints;
+  ctx->lab_d = ints + T;
+  ctx->perm_d = ints + 2 * T;
+  ctx->start_d = ints + 3 * T;
+  ctx->rope_tab = (float2*)take((size_t)ctx->cfg.max_seq * p.d / 2 * 8);
+  ctx->gains[0] = (float*)take(2 * (size_t)p.h * 4);
+  ctx->gains[1] = (float*)take(2 * (size_t)p.h * 4);
+  ctx->wf_raw = take((size_t)p.h * 4);
+  ctx->wf32 = (float*)take((size_t)p.h * 4);
+  ctx->dyn = cur;
+  cur += p.dyn_max;
+  if ((size_t)(cur - ctx->arena) > ctx->arena_bytes) return set_err(ctx, MT_ERR_BUDGET, "arena too small for plan");
+  return MT_OK;
+}
+
+// Bounded host wait on an event: polls with a deadline instead of blocking.
+int wait_event(mt_ctx* ctx, cudaEvent_t ev, double seconds) {
+  if (ctx->fault_kind == 2 && ++ctx->fault_count == ctx->fault_nth)
+    return set_err(ctx, MT_ERR_TIMEOUT, "injected wait timeout");
+  const auto t0 = std::chrono::steady_clock::now();
+  while (true) {
+    cudaError_t e = cudaEventQuery(ev);
+    if (e == cudaSuccess) return MT_OK;
+    if (e != cudaErrorNotReady) return set_err(ctx, MT_ERR_CUDA, std::string("event: ") + cudaGetErrorString(e));
+    const double el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+    if (el > seconds) return set_err(ctx, MT_ERR_TIMEOUT, "step did not finish in time");
+    std::this_thread::sleep_for(std::chrono::microseconds(el < 0.01 ? 20 : 200));
+  }
+}
+
+cudaEvent_t next_event(mt_ctx* ctx) {
+  if (ctx->ev_used >= ctx->ev_pool.size()) {
+    cudaEvent_t e;
+    if (cudaEventCreate(&e) != cudaSuccess) return nullptr;
+    ctx->ev_pool.push_back(e);
+  }
+  return ctx->ev_pool[ctx->ev_used++];
+}
+
+// Timing segment helpers (only when tracing).
+struct SegScope {
+  mt_ctx* ctx;
+  int idx = -1;
+  cudaStream_t st;
+  SegScope(mt_ctx* c, int stream_id, cudaStream_t s, double bytes) : ctx(c), st(s) {
+    if (!c->trace) return;
+    cudaEvent_t a = next_event(c), b = next_event(c);
+    if (!a || !b) return;
+    cudaEventRecord(a, s);
+    c->segs.push_back(Seg{stream_id, a, b, bytes});
+    idx = (int)c->segs.size() - 1;
+  }
+  ~SegScope() {
+    if (idx >= 0) cudaEventRecord(ctx->segs[idx].b, st);
+  }
+};
+
+struct LayerView {  // bf16 matrices and fp32 gains of one bound layer
+  const uint16_t *wqkv, *wo, *wgu, *wd;
+  int ldd;  // row stride of Wd
+  const float *w1, *w2;
+};
+
+struct ActSlot {
+  float *x, *rstd1, *lse, *hmid, *rstd2;
+  uint16_t *a, *qkv, *o, *m, *gu, *act;
+};
+
+ActSlot act_slot(mt_ctx* ctx, int K, int nb, int j) {
+  const Plan& p = ctx->P;
+  uint8_t* base = ctx->dyn + (size_t)nb * p.ckpt_one + (size_t)j * p.act_layer;
+  ActSlot s;
+  s.x = (float*)(base + p.o_x);
+  s.a = (uint16_t*)(base + p.o_a);
+  s.rstd1 = (float*)(base + p.o_rstd1);
+  s.qkv = (uint16_t*)(base + p.o_qkv);
+  s.o = (uint16_t*)(base + p.o_o);
+  s.lse = (float*)(base + p.o_lse);
+  s.hmid = (float*)(base + p.o_hmid);
+  s.m = (uint16_t*)(base + p.o_m);
+  s.rstd2 = (float*)(base + p.o_rstd2);
+  s.gu = (uint16_t*)(base + p.o_gu);
+  s.act = (uint16_t*)(base + p.o_act);
+  (void)K;
+  return s;
+}
+
+float* ckpt(mt_ctx* ctx, int b) { return (float*)(ctx->dyn + (size_t)b * ctx->P.ckpt_one); }
+
+// Brackets one kernel launch with events when per-kernel tracing is on.
+struct OpTimer {
+  mt_ctx* ctx;
+  int idx = -1;
+  OpTimer(mt_ctx* c, int cat, double flop) : ctx(c) {
+    if (c->trace < 2) return;
+    cudaEvent_t a = next_event(c), b = next_event(c);
+    if (!a || !b) return;
+    cudaEventRecord(a, c->s_comp);
+    c->opsegs.push_back(OpSeg{cat, a, b, flop});
+    idx = (int)c->opsegs.size() - 1;
+  }
+  ~OpTimer() {
+    if (idx >= 0) cudaEventRecord(ctx->opsegs[idx].b, ctx->s_comp);
+  }
+};
+
+int gemm(mt_ctx* ctx, int mode, int epi, const void* A, const void* B, void* C, const void* add, int M, int N, int K,
+         int lda, int ldb, int ldc) {
+  GemmParams p{M, N, K, epi, C, add, ldc, 0};
+  OpTimer timer(ctx, 0, 2.0 * M * N * K);
+  if (gemm_bf16(mode, p, A, B, lda, ldb, ctx->s_comp) != 0) {
+    cudaError_t e = cudaGetLastError();
+    char buf[256];
+    snprintf(buf, sizeof buf, "gemm mode %d M=%d N=%d K=%d lda=%d ldb=%d ldc=%d failed: %s", mode, M, N, K, lda, ldb,
+             ldc, cudaGetErrorString(e));
+    return set_err(ctx, e != cudaSuccess ? MT_ERR_CUDA : MT_ERR_ARG, buf);
+  }
+  return MT_OK;
+}
+
+#define CKR(x)              \
+  do {                      \
+    int r_ = (x);           \
+    if (r_ != MT_OK) return r_; \
+  } while (0)
+
+}  // namespace
+
+// ===========================================================================
+// The step
+// ===========================================================================
+namespace {
+
+struct Step {
+  mt_ctx* ctx;
+  int B, S, T, K, nb;
+  float* host_grad;
+  std::vector<Item> seq;        // compute-stream consumption order
+  std::vector<int> slot_of;     // slot per step
+  std::vector<char> needs_load; // load before step
+  const Plan& P() const { return ctx->P; }
+};
+
+void plan_sequence(Step& st) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  auto& q = st.seq;
+  for (int s = 0; s < p.n_emb_slices; ++s) q.push_back({IT_EMB, s});
+  for (int l = 1; l <= p.L; ++l) q.push_back({IT_LAYER, l});
+  for (int s = 0; s < p.n_head_slices; ++s) q.push_back({IT_HEAD, s});
+  for (int s = p.n_head_slices - 1; s >= 0; --s) q.push_back({IT_HEAD, s});
+  for (int b = st.nb - 1; b >= 0; --b) {
+    const int lo = b * st.K + 1, hi = std::min((b + 1) * st.K, p.L);
+    const bool recompute = !(b == st.nb - 1 && ctx->fuse_top);
+    if (recompute)
+      for (int l = lo; l <= hi; ++l) q.push_back({IT_LAYER, l});
+    for (int l = hi; l >= lo; --l) q.push_back({IT_LAYER, -l});  // negative: backward use
+  }
+  // slots: a step reuses a slot that already holds its unit, otherwise loads
+  // into the slot the previous step did not use.
+  Item held[2] = {{-1, 0}, {-1, 0}};
+  int prev = 1;
+  for (size_t i = 0; i < q.size(); ++i) {
+    Item key{q[i].kind, std::abs(q[i].index)};
+    int s = -1;
+    for (int k = 0; k < 2; ++k)
+      if (held[k] == key) s = k;
+    if (s >= 0) {
+      st.slot_of.push_back(s);
+      st.needs_load.push_back(0);
+    } else {
+      s = 1 - prev;
+      held[s] = key;
+      st.slot_of.push_back(s);
+      st.needs_load.push_back(1);
+    }
+    prev = s;
+  }
+}
+
+// H2D copy of step i's weights into its slot (weight stream).
+int issue_load(Step& st, size_t i) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  const Item it = st.seq[i];
+  const int slot = st.slot_of[i];
+  const uint8_t* hp = (const uint8_t*)ctx->host_params;
+  size_t src_off = 0, bytes = 0;
+  const int L = p.L;
+  if (it.kind == IT_LAYER) {
+    const int l = std::abs(it.index);
+    src_off = ctx->off_p[l][0];
+    bytes = ctx->off_p[l][8] + tensor_numel(ctx->cfg, l, 8) * p.esz - src_off;
+  } else if (it.kind == IT_EMB) {
+    const int r0 = it.index * p.emb_rows, rows = std::min(p.emb_rows, p.V - r0);
+    src_off = ctx->off_p[0][0] + (size_t)r0 * p.h * p.esz;
+    bytes = (size_t)rows * p.h * p.esz;
+  } else {
+    const int r0 = it.index * p.head_rows, rows = std::min(p.head_rows, p.V - r0);
+    src_off = ctx->off_p[L + 1][1] + (size_t)r0 * p.h * p.esz;
+    bytes = (size_t)rows * p.h * p.esz;
+  }
+  if (ctx->fault_kind == 1 && ++ctx->fault_count == ctx->fault_nth)
+    return set_err(ctx, MT_ERR_CUDA, "injected copy-issue failure");
+  CK(cudaStreamWaitEvent(ctx->s_h2d, ctx->ev_wfree[slot], 0));
+  {
+    SegScope sg(ctx, 1, ctx->s_h2d, (double)bytes);
+    CK(cudaMemcpyAsync(ctx->wbuf[slot], hp + src_off, bytes, cudaMemcpyHostToDevice, ctx->s_h2d));
+  }
+  CK(cudaEventRecord(ctx->ev_wready[slot], ctx->s_h2d));
+  ctx->stats.h2d_bytes += (double)bytes;
+  ctx->stats.n_h2d += 1;
+  return MT_OK;
+}
+
+// Bind a loaded layer: fp32 params are cast into the slot's bf16 view.
+int bind_layer(Step& st, int l, int slot, bool fresh, LayerView* v) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  const uint8_t* base = ctx->wbuf[slot];
+  const size_t u0 = ctx->off_p[l][0];
+  auto at = [&](int t) { return base + (ctx->off_p[l][t] - u0); };
+  float* g = ctx->gains[slot];
+  if (p.esz == 2) {
+    v->wqkv = (const uint16_t*)at(1);
+    v->wo = (const uint16_t*)at(4);
+    v->wgu = (const uint16_t*)at(6);
+    v->wd = (const uint16_t*)at(8);
+    v->ldd = p.F;
+    if (fresh) {
+      CKL(gains_to_f32(at(0), true, g, p.h, ctx->s_comp));
+      CKL(gains_to_f32(at(5), true, g + p.h, p.h, ctx->s_comp));
+    }
+  } else {
+    uint16_t* c = ctx->wcast[slot];
+    uint16_t* cqkv = c;
+    uint16_t* co = cqkv + rup((size_t)p.qkv * p.h * 2, 256) / 2;
+    uint16_t* cgu = co + rup((size_t)p.h * p.qd * 2, 256) / 2;
+    uint16_t* cd = cgu + rup((size_t)2 * p.Fp * p.h * 2, 256) / 2;
+    if (fresh) {
+      // Wq, Wk, Wv are contiguous in the packed layout (hidden % 64 == 0)
+      CKL(cast_rows_f32_bf16((const float*)at(1), cqkv, p.qkv, p.qkv, p.h, p.h, ctx->s_comp));
+      CKL(cast_rows_f32_bf16((const float*)at(4), co, p.h, p.h, p.qd, p.qd, ctx->s_comp));
+      CKL(cast_rows_f32_bf16((const float*)at(6), cgu, p.F, p.Fp, p.h, p.h, ctx->s_comp));
+      CKL(cast_rows_f32_bf16((const float*)at(7), cgu + (size_t)p.Fp * p.h, p.F, p.Fp, p.h, p.h, ctx->s_comp));
+      CKL(cast_rows_f32_bf16((const float*)at(8), cd, p.h, p.h, p.F, p.Fp, ctx->s_comp));
+      CKL(gains_to_f32(at(0), false, g, p.h, ctx->s_comp));
+      CKL(gains_to_f32(at(5), false, g + p.h, p.h, ctx->s_comp));
+    }
+    v->wqkv = cqkv;
+    v->wo = co;
+    v->wgu = cgu;
+    v->wd = cd;
+    v->ldd = p.Fp;
+  }
+  v->w1 = g;
+  v->w2 = g + p.h;
+  return MT_OK;
+}
+
+const uint16_t* bind_head(Step& st, int s, int slot, bool fresh, int* rows) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  const int r0 = s * p.head_rows;
+  *rows = std::min(p.head_rows, p.V - r0);
+  if (p.esz == 2) return (const uint16_t*)ctx->wbuf[slot];
+  if (fresh) {
+    if (cast_rows_f32_bf16((const float*)ctx->wbuf[slot], ctx->wcast[slot], *rows, *rows, p.h, p.h, ctx->s_comp))
+      return nullptr;
+  }
+  return ctx->wcast[slot];
+}
+
+// x_in / x_out of layer l (1-based) for checkpoint interval K.
+float* layer_input(Step& st, int l) {
+  const int i = l - 1;  // index of the input residual h_{l-1}
+  if (i % st.K == 0) return ckpt(st.ctx, i / st.K);
+  return act_slot(st.ctx, st.K, st.nb, i % st.K).x;
+}
+float* layer_output(Step& st, int l) {
+  if (l == st.ctx->P.L) return st.ctx->h_top;
+  return layer_input(st, l + 1);
+}
+
+// Causal attention forward work: Q K^T and P V over the lower triangle,
+// 2 * (2 * B * n_q * d * S(S+1)/2) flop; the backward is 2.5 times that.
+double attn_flop(const Step& st, const Plan& p) {
+  return 2.0 * st.B * p.nq * (double)p.d * st.S * (st.S + 1.0);
+}
+
+int layer_forward(Step& st, int l, const LayerView& w) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  const int T = st.T, h = p.h;
+  ActSlot a = act_slot(ctx, st.K, st.nb, (l - 1) % st.K);
+  float* x = layer_input(st, l);
+  float* y = layer_output(st, l);
+  cudaStream_t s = ctx->s_comp;
+  CKL(rmsnorm_fwd(x, w.w1, a.a, a.rstd1, T, h, ctx->cfg.norm_eps, s));
+  CKR(gemm(ctx, GEMM_NT, EPI_BF16, a.a, w.wqkv, a.qkv, nullptr, T, p.qkv, h, h, h, p.qkv));
+  CKL(rope_apply(a.qkv, ctx->rope_tab, st.B, st.S, p.qkv, 0, p.nq + p.nkv, p.d, +1, s));
+  {
+    OpTimer timer(ctx, 1, attn_flop(st, p));
+    CKL(attention_fwd(a.qkv, a.qkv + p.qd, a.qkv + p.qd + p.kd, a.o, a.lse, st.B, st.S, p.nq, p.nkv, p.d, p.qkv,
+                      p.qkv, p.qd, s));
+  }
+  CKR(gemm(ctx, GEMM_NT, EPI_F32_ADD, a.o, w.wo, a.hmid, x, T, h, p.qd, p.qd, p.qd, h));
+  CKL(rmsnorm_fwd(a.hmid, w.w2, a.m, a.rstd2, T, h, ctx->cfg.norm_eps, s));
+  CKR(gemm(ctx, GEMM_NT, EPI_BF16, a.m, w.wgu, a.gu, nullptr, T, 2 * p.Fp, h, h, h, 2 * p.Fp));
+  CKL(swiglu_fwd(a.gu, a.act, T, p.F, p.Fp, s));
+  CKR(gemm(ctx, GEMM_NT, EPI_F32_ADD, a.act, w.wd, y, a.hmid, T, h, p.Fp, p.Fp, w.ldd, h));
+  return MT_OK;
+}
+
+// Gradient staging slot handshake.
+int grad_slot_begin(Step& st, int* g) {
+  mt_ctx* ctx = st.ctx;
+  *g = ctx->gslot;
+  ctx->gslot ^= 1;
+  CK(cudaStreamWaitEvent(ctx->s_comp, ctx->ev_gfree[*g], 0));
+  return MT_OK;
+}
+int grad_slot_end(Step& st, int g, size_t host_off, size_t bytes) {
+  mt_ctx* ctx = st.ctx;
+  CK(cudaEventRecord(ctx->ev_bwd_done[g], ctx->s_comp));
+  CK(cudaStreamWaitEvent(ctx->s_d2h, ctx->ev_bwd_done[g], 0));
+  {
+    SegScope sg(ctx, 2, ctx->s_d2h, (double)bytes);
+    CK(cudaMemcpyAsync((uint8_t*)st.host_grad + host_off, ctx->gbuf[g], bytes, cudaMemcpyDeviceToHost, ctx->s_d2h));
+  }
+  CK(cudaEventRecord(ctx->ev_gfree[g], ctx->s_d2h));
+  ctx->stats.d2h_bytes += (double)bytes;
+  ctx->stats.n_d2h += 1;
+  return MT_OK;
+}
+
+int layer_backward(Step& st, int l, const LayerView& w) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  const int T = st.T, h = p.h, Fp = p.Fp, F = p.F;
+  ActSlot a = act_slot(ctx, st.K, st.nb, (l - 1) % st.K);
+  float* x = layer_input(st, l);
+  cudaStream_t s = ctx->s_comp;
+  int g;
+  CKR(grad_slot_begin(st, &g));
+  float* G = ctx->gbuf[g];
+  const size_t u0 = ctx->off_g[l][0];
+  auto GT = [&](int t) { return (float*)((uint8_t*)G + (ctx->off_g[l][t] - u0)); };
+  // h_out = h_mid + act Wd^T
+  CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dh_b, a.act, GT(8), nullptr, h, F, T, h, Fp, F));
+  CKR(gemm(ctx, GEMM_NN, EPI_BF16, ctx->dh_b, w.wd, a.act, nullptr, T, Fp, h, h, w.ldd, Fp));  // dact -> act slot
+  CKL(swiglu_bwd(a.gu, a.act, T, F, Fp, s));                                                   // gu <- dgu
+  if (Fp == F) {
+    CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, 2 * F, h, T, 2 * Fp, h, h));
+  } else {
+    CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, F, h, T, 2 * Fp, h, h));
+    CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu + Fp, a.m, GT(7), nullptr, F, h, T, 2 * Fp, h, h));
+  }
+  CKR(gemm(ctx, GEMM_NN, EPI_F32, a.gu, w.wgu, ctx->dm, nullptr, T, h, 2 * Fp, 2 * Fp, h, h));
+  // RMSNorm 2 (+ residual): dh_mid written over h_mid (row-local, in place)
+  CKL(rmsnorm_bwd(a.hmid, w.w2, a.rstd2, ctx->dm, ctx->dh, a.hmid, ctx->dhmid_b, GT(5), ctx->norm_ws, T, h, s));
+  // h_mid = x + o Wo^T
+  CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dhmid_b, a.o, GT(4), nullptr, h, p.qd, T, h, p.qd, p.qd));
+  CKR(gemm(ctx, GEMM_NN, EPI_BF16, ctx->dhmid_b, w.wo, ctx->do_b, nullptr, T, p.qd, h, h, p.qd, p.qd));
+  {
+    OpTimer timer(ctx, 1, 2.5 * attn_flop(st, p));
+    CKL(attention_bwd(a.qkv, a.qkv + p.qd, a.qkv + p.qd + p.kd, a.o, ctx->do_b, a.lse, ctx->dqkv,
+                      ctx->dqkv + p.qd, ctx->dqkv + p.qd + p.kd, ctx->attn_ws, st.B, st.S, p.nq, p.nkv, p.d, p.qkv,
+                      p.qkv, p.qd, s));
+  }
+  CKL(rope_apply(ctx->dqkv, ctx->rope_tab, st.B, st.S, p.qkv, 0, p.nq + p.nkv, p.d, -1, s));
+  CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dqkv, a.a, GT(1), nullptr, p.qkv, h, T, p.qkv, h, h));
+  CKR(gemm(ctx, GEMM_NN, EPI_F32, ctx->dqkv, w.wqkv, ctx->dm, nullptr, T, h, p.qkv, p.qkv, h, h));
+  // RMSNorm 1 (+ residual): new dh
+  CKL(rmsnorm_bwd(x, w.w1, a.rstd1, ctx->dm, a.hmid, ctx->dh, ctx->dh_b, GT(0), ctx->norm_ws, T, h, s));
+  const size_t bytes = ctx->off_g[l][8] + tensor_numel(ctx->cfg, l, 8) * 4 - u0;
+  return grad_slot_end(st, g, u0, bytes);
+}
+
+int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss_out) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  const int T = st.T, h = p.h, L = p.L;
+  cudaStream_t s = ctx->s_comp;
+
+  // Host preparation: stable counting sort of token ids for the
+  // deterministic embedding scatter.
+  int32_t* hs = ctx->host_stage;
+  std::memcpy(hs, tokens, (size_t)T * 4);
+  std::memcpy(hs + T, labels, (size_t)T * 4);
+  int32_t* perm = hs + 2 * T;
+  int32_t* start = hs + 3 * T;
+  std::memset(start, 0, (size_t)(p.V + 1) * 4);
+  for (int t = 0; t < T; ++t) start[tokens[t] + 1]++;
+  for (int v = 0; v < p.V; ++v) start[v + 1] += start[v];
+  {
+    std::vector<int32_t> fill(start, start + p.V);
+    for (int t = 0; t < T; ++t) perm[fill[tokens[t]]++] = t;
+  }
+  ctx->segs.clear();
+  ctx->opsegs.clear();
+  ctx->ev_used = 0;
+  ctx->stats = mt_stats{};
+  ctx->stats.timing_enabled = ctx->trace;
+  ctx->launches_at_start = g_kernel_launches;
+  ctx->gslot = 0;
+  ctx->fault_count = 0;
+  // Fresh step: the previous step fully drained, so every buffer is free.
+  if (ctx->trace) CK(cudaEventRecord(ctx->ev_base, s));
+  cudaGetLastError();
+  CK(cudaMemcpyAsync(ctx->tok_d, hs, (size_t)(3 * T + p.V + 1) * 4, cudaMemcpyHostToDevice, s));
+  // The copy streams wait for the step start so that their timestamps are
+  // ordered after the base event and no buffer of the previous step is live.
+  cudaEvent_t ev_start = next_event(ctx);
+  CK(cudaEventRecord(ev_start, s));
+  CK(cudaStreamWaitEvent(ctx->s_h2d, ev_start, 0));
+  CK(cudaStreamWaitEvent(ctx->s_d2h, ev_start, 0));
+  if (ctx->rope_S != st.S) {
+    CKL(rope_table(ctx->rope_tab, st.S, p.d, ctx->cfg.rope_theta, s));
+    ctx->rope_S = st.S;
+  }
+  // Final-norm gain: tiny copy on the weight stream.
+  {
+    const size_t wf_bytes = (size_t)h * p.esz;
+    CK(cudaMemcpyAsync(ctx->wf_raw, (const uint8_t*)ctx->host_params + ctx->off_p[L + 1][0], wf_bytes,
+                       cudaMemcpyHostToDevice, ctx->s_h2d));
+    cudaEvent_t e = next_event(ctx);
+    CK(cudaEventRecord(e, ctx->s_h2d));
+    CK(cudaStreamWaitEvent(s, e, 0));
+    CKL(gains_to_f32(ctx->wf_raw, p.esz == 2, ctx->wf32, h, s));
+  }
+
+  plan_sequence(st);
+  const size_t n = st.seq.size();
+  ctx->stats.n_units = (int)n;
+  if (st.needs_load[0]) CKR(issue_load(st, 0));
+  int head_pass2_count = 0;
+  bool first_dxf = true;
+  for (size_t i = 0; i < n; ++i) {
+    if (i + 1 < n && st.needs_load[i + 1]) CKR(issue_load(st, i + 1));
+    const Item it = st.seq[i];
+    const int slot = st.slot_of[i];
+    const bool fresh = st.needs_load[i];
+    if (fresh) CK(cudaStreamWaitEvent(s, ctx->ev_wready[slot], 0));
+    {
+      SegScope sg(ctx, 0, s, 0);
+      if (it.kind == IT_EMB) {
+        const int r0 = it.index * p.emb_rows, rows = std::min(p.emb_rows, p.V - r0);
+        CKL(embed_gather(ctx->wbuf[slot], p.esz == 2, r0, rows, ctx->tok_d, ckpt(ctx, 0), T, h, s));
+      } else if (it.kind == IT_LAYER) {
+        const int l = std::abs(it.index);
+        LayerView w;
+        CKR(bind_layer(st, l, slot, fresh, &w));
+        if (it.index > 0) {
+          CKR(layer_forward(st, l, w));
+        } else {
+          CKR(layer_backward(st, l, w));
+        }
+      } else {  // head slice
+        int rows;
+        const uint16_t* W = bind_head(st, it.index, slot, fresh, &rows);
+        if (!W) return set_err(ctx, MT_ERR_CUDA, "head cast failed");
+        const int r0 = it.index * p.head_rows;
+        const bool pass2 = (int)i >= p.n_emb_slices + L + p.n_head_slices;
+        if (!pass2) {
+          if (it.index == 0) CKL(rmsnorm_fwd(ctx->h_top, ctx->wf32, ctx->xf_b, ctx->rstd_f, T, h, ctx->cfg.norm_eps, s));
+          CKR(gemm(ctx, GEMM_NT, EPI_F32, ctx->xf_b, W, ctx->logits, nullptr, T, rows, h, h, h, p.head_rows));
+          CKL(ce_slice_stats(ctx->logits, T, rows, p.head_rows, r0, ctx->lab_d, ctx->ce_part + (size_t)it.index * T,
+                             ctx->zlab, s));
+          if (it.index == p.n_head_slices - 1)
+            CKL(ce_finalize(ctx->ce_part, p.n_head_slices, ctx->zlab, ctx->lse, ctx->terms, ctx->loss_dev, T,
+                            1.f / (float)T, s));
+        } else {
+          CKR(gemm(ctx, GEMM_NT, EPI_F32, ctx->xf_b, W, ctx->logits, nullptr, T, rows, h, h, h, p.head_rows));
+          CKL(ce_slice_grad(ctx->logits, T, rows, p.head_rows, r0, ctx->lab_d, ctx->lse, 1.f / (float)T, ctx->dz, s));
+          CKR(gemm(ctx, GEMM_NN, first_dxf ? EPI_F32 : EPI_F32_ADD, ctx->dz, W, ctx->dm, ctx->dm, T, h, rows,
+                   p.head_rows, h, h));
+          first_dxf = false;
+          int g;
+          CKR(grad_slot_begin(st, &g));
+          CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dz, ctx->xf_b, ctx->gbuf[g], nullptr, rows, h, T, p.head_rows, h, h));
+          CKR(grad_slot_end(st, g, ctx->off_g[L + 1][1] + (size_t)r0 * h * 4, (size_t)rows * h * 4));
+          if (++head_pass2_count == p.n_head_slices) {
+            // final norm backward -> dh_L, and its gain gradient
+            CKR(grad_slot_begin(st, &g));
+            CKL(rmsnorm_bwd(ctx->h_top, ctx->wf32, ctx->rstd_f, ctx->dm, nullptr, ctx->dh, ctx->dh_b, ctx->gbuf[g],
+                            ctx->norm_ws, T, h, s));
+            CKR(grad_slot_end(st, g, ctx->off_g[L + 1][0], (size_t)h * 4));
+          }
+        }
+      }
+    }
+    CK(cudaEventRecord(ctx->ev_wfree[slot], s));
+  }
+  // Embedding backward: dense gradient slices from dh_0.
+  for (int sl = 0; sl < p.n_embg_slices; ++sl) {
+    const int r0 = sl * p.embg_rows, rows = std::min(p.embg_rows, p.V - r0);
+    int g;
+    CKR(grad_slot_begin(st, &g));
+    {
+      SegScope sg(ctx, 0, s, 0);
+      CKL(embed_scatter(ctx->perm_d, ctx->start_d, r0, rows, ctx->dh, ctx->gbuf[g], h, s));
+    }
+    CKR(grad_slot_end(st, g, ctx->off_g[0][0] + (size_t)r0 * h * 4, (size_t)rows * h * 4));
+  }
+  // Completion: the grad stream's last copy, and the loss.
+  float* loss_host = (float*)(ctx->host_stage + 3 * (size_t)p.Tmax + p.V + 1);
+  CK(cudaStreamWaitEvent(ctx->s_d2h, ctx->ev_wfree[0], 0));
+  CK(cudaStreamWaitEvent(ctx->s_d2h, ctx->ev_wfree[1], 0));
+  CK(cudaMemcpyAsync(loss_host, ctx->loss_dev, 4, cudaMemcpyDeviceToHost, ctx->s_d2h));
+  cudaEvent_t h2d_end = next_event(ctx);
+  CK(cudaEventRecord(h2d_end, ctx->s_h2d));
+  CK(cudaStreamWaitEvent(ctx->s_d2h, h2d_end, 0));
+  CK(cudaEventRecord(ctx->ev_done, ctx->s_d2h));
+  CKR(wait_event(ctx, ctx->ev_done, 3600.0));
+  *loss_out = *loss_host;
+  return MT_OK;
+}
+
+void compute_stats(mt_ctx* ctx) {
+  ctx->stats.n_launches = (int32_t)(g_kernel_launches - ctx->launches_at_start);
+  for (auto& o : ctx->opsegs) {
+    float ms = 0;
+    if (cudaEventElapsedTime(&ms, o.a, o.b) != cudaSuccess) continue;
+    if (o.cat == 0) {
+      ctx->stats.gemm_ms += ms;
+      ctx->stats.gemm_flop += o.flop;
+      ctx->stats.n_gemm += 1;
+    } else {
+      ctx->stats.attn_ms += ms;
+      ctx->stats.attn_flop += o.flop;
+      ctx->stats.n_attn += 1;
+    }
+  }
+  if (!ctx->trace || ctx->segs.empty()) return;
+  struct Iv {
+    double a, b;
+  };
+  std::vector<Iv> comp, h2d, d2h;
+  double end = 0;
+  for (auto& sg : ctx->segs) {
+    float ta = 0, tb = 0;
+    if (cudaEventElapsedTime(&ta, ctx->ev_base, sg.a) != cudaSuccess) continue;
+    if (cudaEventElapsedTime(&tb, ctx->ev_base, sg.b) != cudaSuccess) continue;
+    Iv v{ta, tb};
+    end = std::max(end, (double)tb);
+    if (sg.stream == 0) comp.push_back(v);
+    else if (sg.stream == 1) h2d.push_back(v);
+    else d2h.push_back(v);
+  }
+  std::sort(comp.begin(), comp.end(), [](const Iv& x, const Iv& y) { return x.a < y.a; });
+  std::vector<Iv> uni;
+  for (auto& v : comp) {
+    if (!uni.empty() && v.a <= uni.back().b) uni.back().b = std::max(uni.back().b, v.b);
+    else uni.push_back(v);
+  }
+  double busy = 0;
+  for (auto& v : uni) busy += v.b - v.a;
+  auto hidden = [&](const std::vector<Iv>& cps, double* total) {
+    double tot = 0, hid = 0;
+    for (auto& c : cps) {
+      tot += c.b - c.a;
+      for (auto& u : uni) {
+        const double lo = std::max(c.a, u.a), hi = std::min(c.b, u.b);
+        if (hi > lo) hid += hi - lo;
+      }
+    }
+    *total = tot;
+    return tot > 0 ? hid / tot : 1.0;
+  };
+  ctx->stats.compute_busy_ms = busy;
+  ctx->stats.h2d_hidden_frac = hidden(h2d, &ctx->stats.h2d_ms);
+  ctx->stats.d2h_hidden_frac = hidden(d2h, &ctx->stats.d2h_ms);
+  ctx->stats.step_ms = end;
+}
+
+}  // namespace
+
+// ===========================================================================
+// C ABI
+// ===========================================================================
+extern "C" {
+
+size_t mt_packed_bytes(const mt_layer_cfg* cfg, mt_dtype dtype) {
+  if (!cfg || cfg->n_layers < 1) return 0;
+  return build_layout(*cfg, dtype == MT_BF16 ? 2 : 4, nullptr);
+}
+
+int mt_tensor_offset(const mt_layer_cfg* cfg, mt_dtype dtype, int unit, int tensor, size_t* off, size_t* bytes) {
+  if (!cfg || !off || !bytes || unit < 0 || unit > cfg->n_layers + 1 || tensor < 0 ||
+      tensor >= tensors_in_unit(*cfg, unit))
+    return MT_ERR_ARG;
+  std::vector<std::vector<size_t>> o;
+  const size_t esz = dtype == MT_BF16 ? 2 : 4;
+  build_layout(*cfg, esz, &o);
+  *off = o[unit][tensor];
+  *bytes = tensor_numel(*cfg, unit, tensor) * esz;
+  return MT_OK;
+}
+
+size_t mt_required_budget(const mt_layer_cfg* cfg) {
+  if (!cfg || !cfg_valid(*cfg, nullptr)) return 0;
+  Plan p;
+  make_plan(*cfg, &p);
+  return p.total;
+}
+
+static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void* const* streams, mt_ctx** out) {
+  if (!cfg || !out) return MT_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  if (!cfg_valid(*cfg, &why)) {
+    fprintf(stderr, "mt_create: %s\n", why.c_str());
+    return (cfg->n_experts || cfg->top_k || cfg->expert_ffn || cfg->hidden % 64 ||
+            (cfg->head_dim != 16 && cfg->head_dim != 32 && cfg->head_dim != 64 && cfg->head_dim != 128))
+               ? MT_ERR_UNSUPPORTED
+               : MT_ERR_ARG;
+  }
+  mt_ctx* ctx = new (std::nothrow) mt_ctx();
+  if (!ctx) return MT_ERR_CUDA;
+  ctx->cfg = *cfg;
+  make_plan(*cfg, &ctx->P);
+  if (ctx->P.total > budget) {
+    delete ctx;
+    return MT_ERR_BUDGET;
+  }
+  build_layout(*cfg, ctx->P.esz, &ctx->off_p);
+  build_layout(*cfg, 4, &ctx->off_g);
+  const char* tr = getenv("MT_TRACE");
+  ctx->trace = tr ? atoi(tr) : 1;
+  if (ctx->trace < 0 || ctx->trace > 2) ctx->trace = 1;
+  const char* ft = getenv("MT_FUSE_TOP_BLOCK");
+  ctx->fuse_top = !(ft && ft[0] == '0');
+  auto fail = [&](int code, const char* m, cudaError_t e) {
+    fprintf(stderr, "mt_create: %s: %s\n", m, cudaGetErrorString(e));
+    mt_destroy(ctx);
+    return code;
+  };
+  cudaError_t e;
+  if ((e = cudaGetDevice(&ctx->device)) != cudaSuccess) return fail(MT_ERR_CUDA, "cudaGetDevice", e);
+  if (arena) {
+    if ((uintptr_t)arena & 255) {
+      mt_destroy(ctx);
+      return MT_ERR_ALIGN;
+    }
+    ctx->arena = (uint8_t*)arena;
+    ctx->arena_bytes = budget;
+    ctx->own_arena = false;
+  } else {
+    ctx->arena_bytes = ctx->P.total;
+    if ((e = cudaMalloc(&ctx->arena, ctx->arena_bytes)) != cudaSuccess) return fail(MT_ERR_BUDGET, "cudaMalloc", e);
+    ctx->own_arena = true;
+  }
+  if (streams) {
+    ctx->s_comp = (cudaStream_t)streams[0];
+    ctx->s_h2d = (cudaStream_t)streams[1];
+    ctx->s_d2h = (cudaStream_t)streams[2];
+    ctx->own_streams = false;
+  } else {
+    if ((e = cudaStreamCreateWithFlags(&ctx->s_comp, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&ctx->s_h2d, cudaStreamNonBlocking)) != cudaSuccess ||
+        (e = cudaStreamCreateWithFlags(&ctx->s_d2h, cudaStreamNonBlocking)) != cudaSuccess)
+      return fail(MT_ERR_CUDA, "stream create", e);
+    ctx->own_streams = true;
+  }
+  for (int i = 0; i < 2; ++i) {
+    if ((e = cudaEventCreateWithFlags(&ctx->ev_wready[i], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&ctx->ev_wfree[i], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&ctx->ev_bwd_done[i], cudaEventDisableTiming)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&ctx->ev_gfree[i], cudaEventDisableTiming)) != cudaSuccess)
+      return fail(MT_ERR_CUDA, "event create", e);
+  }
+  if ((e = cudaEventCreateWithFlags(&ctx->ev_done, cudaEventDisableTiming)) != cudaSuccess ||
+      (e = cudaEventCreate(&ctx->ev_base)) != cudaSuccess)
+    return fail(MT_ERR_CUDA, "event create", e);
+  const size_t stage_ints = 3 * (size_t)ctx->P.Tmax + ctx->P.V + 1 + 64;
+  if ((e = cudaHostAlloc((void**)&ctx->host_stage, stage_ints * 4, cudaHostAllocDefault)) != cudaSuccess)
+    return fail(MT_ERR_CUDA, "cudaHostAlloc", e);
+  if (carve(ctx) != MT_OK) {
+    mt_destroy(ctx);
+    return MT_ERR_BUDGET;
+  }
+  *out = ctx;
+  return MT_OK;
+}
+
+int mt_create(const mt_layer_cfg* cfg, size_t device_budget_bytes, mt_ctx** out) {
+  return create_impl(cfg, device_budget_bytes, nullptr, nullptr, out);
+}
+
+int mt_create_ex(const mt_layer_cfg* cfg, size_t device_budget_bytes, void* device_arena, void* const* streams,
+                 mt_ctx** out) {
+  if (!device_arena) return MT_ERR_ARG;
+  return create_impl(cfg, device_budget_bytes, device_arena, streams, out);
+}
+
+int mt_bind_host_params(mt_ctx* ctx, const void* host_params, mt_dtype dtype) {
+  if (!ctx || !host_params) return set_err(ctx, MT_ERR_ARG, "null argument");
+  if ((int)dtype != ctx->cfg.param_dtype) return set_err(ctx, MT_ERR_ARG, "dtype differs from cfg.param_dtype");
+  if ((uintptr_t)host_params & 4095) return set_err(ctx, MT_ERR_ALIGN, "host params not 4096-byte aligned");
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host_params) != cudaSuccess || at.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return set_err(ctx, MT_ERR_NOT_PINNED, "host params are not page-locked CUDA host memory");
+  }
+  ctx->host_params = host_params;
+  return MT_OK;
+}
+
+int mt_forward_backward(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
+                        float* host_grad_out, float* loss_out) {
+  if (!ctx) return MT_ERR_ARG;
+  ctx->err.clear();
+  if (!ctx->host_params) return set_err(ctx, MT_ERR_STATE, "no parameters bound");
+  if (!tokens || !labels || !host_grad_out || !loss_out) return set_err(ctx, MT_ERR_ARG, "null argument");
+  if (B < 1 || S < 1 || B > ctx->cfg.max_batch || S > ctx->cfg.max_seq)
+    return set_err(ctx, MT_ERR_ARG, "B or S outside [1, max]");
+  if (K < 1 || K > ctx->cfg.max_K || K > ctx->cfg.n_layers) return set_err(ctx, MT_ERR_ARG, "K outside [1, min(L, max_K)]");
+  const int T = B * S;
+  for (int t = 0; t < T; ++t)
+    if (tokens[t] < 0 || tokens[t] >= ctx->cfg.vocab || labels[t] < 0 || labels[t] >= ctx->cfg.vocab)
+      return set_err(ctx, MT_ERR_ARG, "token or label id outside [0, vocab)");
+  if ((uintptr_t)host_grad_out & 4095) return set_err(ctx, MT_ERR_ALIGN, "grad buffer not 4096-byte aligned");
+  cudaPointerAttributes at;
+  if (cudaPointerGetAttributes(&at, host_grad_out) != cudaSuccess || at.type != cudaMemoryTypeHost) {
+    cudaGetLastError();
+    return set_err(ctx, MT_ERR_NOT_PINNED, "grad buffer is not page-locked CUDA host memory");
+  }
+  int cur = 0;
+  cudaGetDevice(&cur);
+  if (cur != ctx->device) cudaSetDevice(ctx->device);
+  Step st{ctx, B, S, T, K, (ctx->cfg.n_layers + K - 1) / K, host_grad_out, {}, {}, {}};
+  const auto t0 = std::chrono::steady_clock::now();
+  int rc = run_step(st, tokens, labels, loss_out);
+  if (rc != MT_OK) {
+    // Drain whatever was enqueued so the context stays usable/destroyable.
+    const std::string msg = ctx->err;
+    cudaEventRecord(ctx->ev_done, ctx->s_comp);
+    ctx->fault_kind = 0;
+    wait_event(ctx, ctx->ev_done, 600.0);
+    cudaStreamSynchronize(ctx->s_h2d);
+    cudaStreamSynchronize(ctx->s_d2h);
+    cudaGetLastError();
+    ctx->err = msg;
+  } else {
+    const uint32_t derr = gemm_take_device_error() | attention_take_device_error();
+    if (derr) {
+      char b[96];
+      snprintf(b, sizeof b, "device error word 0x%x (barrier timeout inside a kernel)", derr);
+      rc = set_err(ctx, MT_ERR_DEVICE, b);
+    } else {
+      cudaError_t e = cudaGetLastError();
+      if (e != cudaSuccess) rc = set_err(ctx, MT_ERR_CUDA, cudaGetErrorString(e));
+    }
+    compute_stats(ctx);
+    if (!ctx->trace)
+      ctx->stats.step_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+  }
+  if (cur != ctx->device) cudaSetDevice(cur);
+  return rc;
+}
+
+int mt_get_stats(const mt_ctx* ctx, mt_stats* out) {
+  if (!ctx || !out) return MT_ERR_ARG;
+  *out = ctx->stats;
+  return MT_OK;
+}
+
+int mt_get_memory_plan(const mt_ctx* ctx, mt_memory_plan* out) {
+  if (!ctx || !out) return MT_ERR_ARG;
+  const Plan& p = ctx->P;
+  out->total = p.total;
+  out->weight_buffers = 2 * p.wbuf + 2 * p.wcast;
+  out->grad_buffers = 2 * p.gbuf;
+  out->workspace = p.fixed_ws;
+  size_t ck = 0, ac = 0;
+  for (int K = 1; K <= std::min(ctx->cfg.max_K, p.L); ++K) {
+    const size_t nb = (p.L + K - 1) / K;
+    if (nb * p.ckpt_one + (size_t)K * p.act_layer == p.dyn_max) {
+      ck = nb * p.ckpt_one;
+      ac = (size_t)K * p.act_layer;
+    }
+  }
+  out->checkpoints = ck;
+  out->block_activations = ac;
+  return MT_OK;
+}
+
+const char* mt_last_error(const mt_ctx* ctx) { return ctx ? ctx->err.c_str() : "null context"; }
+
+void mt_destroy(mt_ctx* ctx) {
+  if (!ctx) return;
+  if (ctx->s_comp) cudaStreamSynchronize(ctx->s_comp);
+  if (ctx->s_h2d) cudaStreamSynchronize(ctx->s_h2d);
+  if (ctx->s_d2h) cudaStreamSynchronize(ctx->s_d2h);
+  for (int i = 0; i < 2; ++i) {
+    if (ctx->ev_wready[i]) cudaEventDestroy(ctx->ev_wready[i]);
+    if (ctx->ev_wfree[i]) cudaEventDestroy(ctx->ev_wfree[i]);
+    if (ctx->ev_bwd_done[i]) cudaEventDestroy(ctx->ev_bwd_done[i]);
+    if (ctx->ev_gfree[i]) cudaEventDestroy(ctx->ev_gfree[i]);
+  }
+  if (ctx->ev_done) cudaEventDestroy(ctx->ev_done);
+  if (ctx->ev_base) cudaEventDestroy(ctx->ev_base);
+  for (auto e : ctx->ev_pool) cudaEventDestroy(e);
+  if (ctx->own_streams) {
+    if (ctx->s_comp) cudaStreamDestroy(ctx->s_comp);
+    if (ctx->s_h2d) cudaStreamDestroy(ctx->s_h2d);
+    if (ctx->s_d2h) cudaStreamDestroy(ctx->s_d2h);
+  }
+  if (ctx->own_arena && ctx->arena) cudaFree(ctx->arena);
+  if (ctx->host_stage) cudaFreeHost(ctx->host_stage);
+  delete ctx;
+}
+
+// cudaHostAlloc may return less than page alignment for small requests, so
+// over-allocate and keep the original pointer just below the aligned one.
+void* mt_host_alloc(size_t bytes) {
+  void* p = nullptr;
+  const size_t total = (bytes ? bytes : 1) + 4096 + 16;
+  if (cudaHostAlloc(&p, total, cudaHostAllocDefault) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  const uintptr_t a = ((uintptr_t)p + 16 + 4095) & ~(uintptr_t)4095;
+  ((void**)a)[-1] = p;
+  return (void*)a;
+}
+
+void mt_host_free(void* p) {
+  if (p) cudaFreeHost(((void**)p)[-1]);
+}
+
+int mt_debug_inject_fault(mt_ctx* ctx, int kind, int nth) {
+  if (!ctx || kind < 0 || kind > 2 || (kind && nth < 1)) return MT_ERR_ARG;
+  ctx->fault_kind = kind;
+  ctx->fault_nth = nth;
+  return MT_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,229 @@
+"""End-to-end parity of the streamed step (mt_forward_backward) against the
+CPU oracle, K-invariance, and the boundary's error behaviour.
+
+Tolerances (bf16 compute, fp32 accumulation and fp32 residual stream, as
+stated for this path): loss within 1e-2 relative; every gradient tensor with
+relative L2 error <= 2e-2 and cosine >= 0.999; gradients bitwise identical
+for every checkpoint interval K.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests.common import LLAMA8B, SMALL, TINY, TINY_GQA, cosine, make_params, make_tokens, rel_l2, with_layers
+from tests.gpu_util import need_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def open_session(mt, cfg, B, S, max_K, bf16=False):
+    shape = mt.ModelShape(cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
+                          cfg.vocab, cfg.rope_theta, cfg.norm_eps)
+    return mt.Session(shape, B, S, max_K, mt.MT_BF16 if bf16 else mt.MT_F32)
+
+
+def compare(cfg, grads_gpu, grads_ref, tok, loss_gpu, loss_ref, tol_l2=2e-2, tol_cos=0.999):
+    assert abs(loss_gpu - loss_ref) <= 1e-2 * abs(loss_ref), (loss_gpu, loss_ref)
+    G, R = oracle.unpack(cfg, grads_gpu), oracle.unpack(cfg, grads_ref)
+    used = np.zeros(cfg.vocab, bool)
+    used[np.asarray(tok).ravel()] = True
+    errs = {}
+    for name in R:
+        g, r = G[name], R[name]
+        if name == "embed":
+            assert np.all(g[~used] == 0.0)
+            g, r = g[used], r[used]
+        errs[name] = (rel_l2(g, r), cosine(g, r))
+    table = "\n".join(f"{k:24s} rel_l2 {e:.3e} cos {c:.6f}" for k, (e, c) in errs.items())
+    print(f"loss gpu {loss_gpu:.6f} oracle {loss_ref:.6f}\n{table}")
+    bad = {k: v for k, v in errs.items() if not (v[0] <= tol_l2 and v[1] >= tol_cos)}
+    assert not bad, table
+    return errs
+
+
+def run_case(cfg, B, S, K, seed_w, seed_t, bf16=False, max_K=None):
+    torch, mt = need_gpu()
+    tok, lab = make_tokens(cfg, B, S, seed_t)
+    packed = make_params(cfg, seed_w, bf16=bf16)
+    with open_session(mt, cfg, B, S, max_K or K, bf16) as s:
+        s.params[:] = packed
+        loss = s.step(tok, lab, K)
+        grads = s.grads.copy()
+        stats = s.stats()
+    return tok, lab, packed, loss, grads, stats
+
+
+@pytest.mark.parametrize("K", [1, 2])
+def test_tiny_mha_matches_oracle(K):
+    tok, lab, packed, loss, grads, _ = run_case(TINY, 2, 32, K, 1, 2)
+    l_ref, g_ref = oracle.forward_backward(TINY, packed, tok, lab)
+    compare(TINY, grads, g_ref, tok, loss, l_ref)
+
+
+def test_tiny_gqa_matches_oracle():
+    tok, lab, packed, loss, grads, _ = run_case(TINY_GQA, 2, 32, 1, 3, 4)
+    l_ref, g_ref = oracle.forward_backward(TINY_GQA, packed, tok, lab)
+    compare(TINY_GQA, grads, g_ref, tok, loss, l_ref)
+
+
+def test_ragged_batch_and_partial_top_block():
+    """B=3, S=37 (no size is a tile multiple), 3 layers with K=2 (top block partial)."""
+    cfg = with_layers(TINY_GQA, 3)
+    tok, lab, packed, loss, grads, _ = run_case(cfg, 3, 37, 2, 5, 6)
+    l_ref, g_ref = oracle.forward_backward(cfg, packed, tok, lab)
+    compare(cfg, grads, g_ref, tok, loss, l_ref)
+
+
+def test_single_token():
+    tok, lab, packed, loss, grads, _ = run_case(TINY, 1, 1, 1, 7, 8, max_K=1)
+    l_ref, g_ref = oracle.forward_backward(TINY, packed, tok, lab)
+    compare(TINY, grads, g_ref, tok, loss, l_ref)
+
+
+def test_bitwise_identical_across_K():
+    torch, mt = need_gpu()
+    cfg = with_layers(TINY_GQA, 4)
+    tok, lab = make_tokens(cfg, 2, 32, 10)
+    packed = make_params(cfg, 9)
+    out = {}
+    with open_session(mt, cfg, 2, 32, 4) as s:
+        s.params[:] = packed
+        for K in (1, 2, 3, 4, 1):
+            loss = s.step(tok, lab, K)
+            out.setdefault(K, []).append((loss, s.grads.copy()))
+    base_loss, base = out[1][0]
+    for K, runs in out.items():
+        for loss, g in runs:
+            assert loss == base_loss, K
+            assert np.array_equal(g.view(np.uint32), base.view(np.uint32)), K
+
+
+def test_zero_head_gives_ln_vocab():
+    torch, mt = need_gpu()
+    cfg = TINY
+    tok, lab = make_tokens(cfg, 2, 32, 12)
+    packed = make_params(cfg, 11)
+    oracle.unpack(cfg, packed)["w_out"][...] = 0.0
+    with open_session(mt, cfg, 2, 32, 1) as s:
+        s.params[:] = packed
+        loss = s.step(tok, lab, 1)
+    assert abs(loss - math.log(cfg.vocab)) < 1e-3
+
+
+def test_small_widths_bf16_host_params():
+    """The small decoder's widths (hidden 1024, 16 x 64 heads, FFN 2816, vocab
+    32000) with two layers, bf16 host weights, at a sequence the oracle
+    finishes in seconds; several vocab slices of the head."""
+    cfg = with_layers(SMALL, 2)
+    tok, lab, packed, loss, grads, _ = run_case(cfg, 1, 96, 1, 13, 14, bf16=True)
+    l_ref, g_ref = oracle.forward_backward(cfg, packed, tok, lab, bf16=True)
+    compare(cfg, grads, g_ref, tok, loss, l_ref)
+
+
+def test_llama8b_widths_two_layers():
+    """Two layers of the 8B shape (hidden 4096, 32 q / 8 kv heads x 128, FFN
+    14336, vocab 128256, theta 5e5), bf16 host weights, S=40."""
+    cfg = with_layers(LLAMA8B, 2)
+    tok, lab, packed, loss, grads, _ = run_case(cfg, 1, 40, 2, 21, 22, bf16=True)
+    l_ref, g_ref = oracle.forward_backward(cfg, packed, tok, lab, bf16=True)
+    compare(cfg, grads, g_ref, tok, loss, l_ref)
+
+
+def test_stats_report_streaming():
+    _, _, _, _, _, st = run_case(with_layers(TINY, 4), 2, 32, 2, 15, 16)
+    assert st["n_h2d"] > 0 and st["n_d2h"] > 0
+    assert st["h2d_bytes"] > 0 and st["d2h_bytes"] > 0
+    assert 0.0 <= st["h2d_hidden_frac"] <= 1.0
+
+
+def test_boundary_errors():
+    torch, mt = need_gpu()
+    cfg = TINY
+    tok, lab = make_tokens(cfg, 2, 32, 17)
+    with open_session(mt, cfg, 2, 32, 2) as s:
+        s.params[:] = make_params(cfg, 18)
+        bad_tok = tok.copy()
+        bad_tok[0, 0] = cfg.vocab
+        cases = [
+            (lambda: s.step(bad_tok, lab, 1), mt.MT_ERR_ARG),
+            (lambda: s.step(tok, lab, 0), mt.MT_ERR_ARG),
+            (lambda: s.step(tok, lab, 3), mt.MT_ERR_ARG),  # K > max_K
+            (lambda: mt.mt_forward_backward(s.ctx, np.zeros((3, 32), np.int32), np.zeros((3, 32), np.int32), 1,
+                                            s.grads_ptr), mt.MT_ERR_ARG),  # B > max_batch
+        ]
+        for fn, code in cases:
+            with pytest.raises(mt.MtError) as e:
+                fn()
+            assert e.value.code == code
+        # unpinned gradient buffer
+        plain = np.zeros(s.grad_bytes // 4 + 1024, np.float32)
+        addr = (plain.ctypes.data + 4095) // 4096 * 4096
+        with pytest.raises(mt.MtError) as e:
+            mt.mt_forward_backward(s.ctx, tok, lab, 1, addr)
+        assert e.value.code == mt.MT_ERR_NOT_PINNED
+        # still usable afterwards
+        loss = s.step(tok, lab, 1)
+        assert np.isfinite(loss)
+    # binding unpinned params
+    with open_session(mt, cfg, 2, 32, 1) as s:
+        plain = np.zeros(s.param_bytes + 8192, np.uint8)
+        addr = (plain.ctypes.data + 4095) // 4096 * 4096
+        with pytest.raises(mt.MtError) as e:
+            mt.mt_bind_host_params(s.ctx, addr, mt.MT_F32)
+        assert e.value.code == mt.MT_ERR_NOT_PINNED
+        with pytest.raises(mt.MtError) as e:
+            mt.mt_bind_host_params(s.ctx, s.params_ptr + 256, mt.MT_F32)
+        assert e.value.code == mt.MT_ERR_ALIGN
+
+
+def test_budget_too_small():
+    torch, mt = need_gpu()
+    cfg = mt.make_cfg(2, 64, 4, 4, 16, 172, 256, max_batch=2, max_seq=32, max_K=1)
+    need = mt.mt_required_budget(cfg)
+    with pytest.raises(mt.MtError) as e:
+        mt.mt_create(cfg, need - 1)
+    assert e.value.code == mt.MT_ERR_BUDGET
+
+
+def test_injected_host_faults_leave_context_usable():
+    """A failed weight-copy issue and a timed-out host wait are reported as
+    errors (injected on the host; nothing is done to the GPU), and the next
+    step succeeds with the same result."""
+    torch, mt = need_gpu()
+    cfg = with_layers(TINY, 3)
+    tok, lab = make_tokens(cfg, 2, 32, 19)
+    with open_session(mt, cfg, 2, 32, 2) as s:
+        s.params[:] = make_params(cfg, 20)
+        ref_loss = s.step(tok, lab, 2)
+        ref = s.grads.copy()
+        for kind, code in ((1, mt.MT_ERR_CUDA), (2, mt.MT_ERR_TIMEOUT)):
+            mt.mt_debug_inject_fault(s.ctx, kind, 3 if kind == 1 else 1)
+            with pytest.raises(mt.MtError) as e:
+                s.step(tok, lab, 2)
+            assert e.value.code == code
+            mt.mt_debug_inject_fault(s.ctx, 0, 0)
+            assert s.step(tok, lab, 2) == ref_loss
+            assert np.array_equal(s.grads, ref)
+
+
+def test_create_ex_with_torch_arena_and_streams():
+    torch, mt = need_gpu()
+    cfg = TINY
+    shape = mt.ModelShape(cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
+                          cfg.vocab, cfg.rope_theta, cfg.norm_eps)
+    c = mt.make_cfg(cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim, cfg.vocab,
+                    max_batch=2, max_seq=32, max_K=1)
+    need = mt.mt_required_budget(c)
+    arena = torch.empty(need, dtype=torch.uint8, device="cuda")
+    streams = [torch.cuda.Stream() for _ in range(3)]
+    tok, lab = make_tokens(cfg, 2, 32, 23)
+    packed = make_params(cfg, 24)
+    with mt.Session(shape, 2, 32, 1, mt.MT_F32, device_budget=need, device_arena=arena.data_ptr(),
+                    streams=[s.cuda_stream for s in streams]) as s:
+        s.params[:] = packed
+        loss = s.step(tok, lab, 1)
+        g = s.grads.copy()
+    l_ref, g_ref = oracle.forward_backward(cfg, packed, tok, lab)
+    compare(cfg, g, g_ref, tok, loss, l_ref)

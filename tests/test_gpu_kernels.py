@@ -1,0 +1,222 @@
+"""GPU parity of the layer-template kernels against the CPU oracle.
+
+Inputs are seeded normals rounded to bf16, so both sides see exactly the same
+operand values; the oracle accumulates in double. Tolerances follow from the
+arithmetic: fp32 accumulation of bf16 products is accurate to ~1e-6 relative
+for these reduction lengths, and rounding a result to bf16 costs at most
+2^-9 relative per element (RMS about 1.1e-3), so
+  fp32 outputs: relative L2 error <= 1e-4,
+  bf16 outputs: relative L2 error <= 6e-3,
+and kernels whose output feeds through another bf16 rounding (attention
+probabilities, SwiGLU) get <= 1.5e-2.
+"""
+import numpy as np
+import pytest
+
+import oracle
+import seedgen
+from tests.common import bf16_round, rel_l2
+from tests.gpu_util import from_dev, need_gpu, to_dev_bf16, to_dev_f32
+
+pytestmark = pytest.mark.gpu
+
+
+def _normal(shape, seed, std=1.0):
+    return seedgen.normal(int(np.prod(shape)), seed, 7, std).reshape(shape)
+
+
+GEMM_SHAPES = [
+    (128, 256, 64),     # one tile
+    (64, 192, 64),      # smaller than a tile (the tiny decoder's QKV)
+    (200, 300, 136),    # ragged M, N, K
+    (1000, 520, 328),   # several tiles, ragged
+    (2048, 4096, 200),  # enough tiles for the 256-wide variant, ragged K
+]
+
+
+@pytest.mark.parametrize("mode", ["nt", "nn", "tn"])
+@pytest.mark.parametrize("shape", GEMM_SHAPES, ids=lambda s: "x".join(map(str, s)))
+def test_gemm_modes_against_oracle(mode, shape):
+    torch, mt = need_gpu()
+    M, N, K = shape
+    a_shape = (M, K) if mode in ("nt", "nn") else (K, M)
+    b_shape = (N, K) if mode == "nt" else (K, N)
+    # operands are stored with row strides padded to 8 elements (TMA needs
+    # 16-byte strides); only the logical a_shape/b_shape part is used
+    pad = lambda n: (n + 7) // 8 * 8
+    A_st = np.zeros((a_shape[0], pad(a_shape[1])), np.float32)
+    B_st = np.zeros((b_shape[0], pad(b_shape[1])), np.float32)
+    A_st[:, :a_shape[1]] = _normal(a_shape, M + 1)
+    B_st[:, :b_shape[1]] = _normal(b_shape, N + 2)
+    A, a32 = to_dev_bf16(torch, A_st)
+    B, b32 = to_dev_bf16(torch, B_st)
+    a32, b32 = a32[:, :a_shape[1]], b32[:, :b_shape[1]]
+    ref = oracle.matmul(mode, a32, b32)
+    add = _normal((M, N), 5)
+    mode_id = {"nt": mt.MT_GEMM_NT, "nn": mt.MT_GEMM_NN, "tn": mt.MT_GEMM_TN}[mode]
+    lda, ldb = A_st.shape[1], B_st.shape[1]
+    # fp32 out
+    C = torch.full((M, N), float("nan"), device="cuda")
+    mt.mt_op_gemm(mode_id, mt.MT_EPI_F32, A, B, C, None, M, N, K, lda, ldb, N)
+    torch.cuda.synchronize()
+    assert mt.mt_op_device_error() == 0
+    assert rel_l2(from_dev(C), ref) < 1e-4
+    # fp32 out = addend + acc, in place
+    C2 = to_dev_f32(torch, add)
+    mt.mt_op_gemm(mode_id, mt.MT_EPI_F32_ADD, A, B, C2, C2, M, N, K, lda, ldb, N)
+    assert rel_l2(from_dev(C2), ref + add) < 1e-4
+    # bf16 out
+    Cb = torch.zeros((M, N), dtype=torch.bfloat16, device="cuda")
+    mt.mt_op_gemm(mode_id, mt.MT_EPI_BF16, A, B, Cb, None, M, N, K, lda, ldb, N)
+    assert rel_l2(from_dev(Cb), ref) < 6e-3
+
+
+def test_gemm_strided_operands_and_unaligned_output():
+    """Row strides larger than the logical width, and an fp32 output whose row
+    stride is not a multiple of 4 elements (element-wise store path)."""
+    torch, mt = need_gpu()
+    M, N, K = 130, 172, 96
+    A_full, a32 = to_dev_bf16(torch, _normal((M, K + 32), 11))
+    B_full, b32 = to_dev_bf16(torch, _normal((N, K + 8), 12))
+    ref = oracle.matmul("nt", a32[:, :K], b32[:, :K])
+    C = torch.zeros((M, N + 1), device="cuda")
+    mt.mt_op_gemm(mt.MT_GEMM_NT, mt.MT_EPI_F32, A_full, B_full, C, None, M, N, K, K + 32, K + 8, N + 1)
+    assert rel_l2(from_dev(C)[:, :N], ref) < 1e-4
+    assert np.all(from_dev(C)[:, N] == 0)
+
+
+def test_gemm_rejects_misaligned_strides():
+    torch, mt = need_gpu()
+    A = torch.zeros((64, 70), dtype=torch.bfloat16, device="cuda")
+    C = torch.zeros((64, 64), device="cuda")
+    with pytest.raises(mt.MtError):
+        mt.mt_op_gemm(mt.MT_GEMM_NT, mt.MT_EPI_F32, A, A, C, None, 64, 64, 70, 70, 70, 64)
+
+
+def test_gemm_sampled_at_full_8b_qkv_shape():
+    """The 8B QKV projection (M=8192 tokens, N=6144, K=4096), checked on 2000
+    sampled outputs computed one by one by the oracle."""
+    torch, mt = need_gpu()
+    M, N, K = 8192, 6144, 4096
+    A, a32 = to_dev_bf16(torch, _normal((M, K), 3, 0.5))
+    B, b32 = to_dev_bf16(torch, _normal((N, K), 4, 0.02))
+    C = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    mt.mt_op_gemm(mt.MT_GEMM_NT, mt.MT_EPI_F32, A, B, C, None, M, N, K, K, K, N)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    rows, cols = rng.integers(0, M, 2000), rng.integers(0, N, 2000)
+    ref = oracle.matmul_sampled("nt", a32, b32, rows, cols)
+    got = from_dev(C)[rows, cols]
+    assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref)) + 1e-6
+
+
+def test_rmsnorm_forward_backward():
+    torch, mt = need_gpu()
+    T, h, eps = 77, 320, 1e-5
+    x = _normal((T, h), 21)
+    w = 1.0 + 0.1 * _normal((h,), 22)
+    dy = _normal((T, h), 23)
+    res = _normal((T, h), 24)
+    X, W = to_dev_f32(torch, x), to_dev_f32(torch, w)
+    Y = torch.empty((T, h), dtype=torch.bfloat16, device="cuda")
+    R = torch.empty(T, device="cuda")
+    mt.mt_op_rmsnorm_fwd(X, W, Y, R, T, h, eps)
+    y_ref, r_ref = oracle.rmsnorm_fwd(x, w, eps)
+    assert rel_l2(from_dev(Y), y_ref) < 6e-3
+    assert rel_l2(from_dev(R), r_ref) < 1e-5
+    DX = torch.empty((T, h), device="cuda")
+    DXb = torch.empty((T, h), dtype=torch.bfloat16, device="cuda")
+    DW = torch.empty(h, device="cuda")
+    ws = torch.empty(mt.mt_op_rmsnorm_bwd_workspace(T, h), device="cuda")
+    mt.mt_op_rmsnorm_bwd(X, W, R, to_dev_f32(torch, dy), to_dev_f32(torch, res), DX, DXb, DW, ws, T, h)
+    dx_ref, dw_ref = oracle.rmsnorm_bwd(x, w, dy, eps)
+    assert rel_l2(from_dev(DX), dx_ref + res) < 1e-5
+    assert rel_l2(from_dev(DXb), dx_ref + res) < 6e-3
+    assert rel_l2(from_dev(DW), dw_ref) < 1e-5
+
+
+@pytest.mark.parametrize("d", [16, 64, 128])
+def test_rope_forward_and_inverse(d):
+    torch, mt = need_gpu()
+    B, S, nq, nkv, theta = 2, 37, 4, 2, 5e5
+    width = (nq + 2 * nkv) * d
+    x = _normal((B * S, width), 31 + d)
+    X, x32 = to_dev_bf16(torch, x)
+    tab = torch.empty(S * d, device="cuda")
+    mt.mt_op_rope(X, tab, B, S, width, 0, nq + nkv, d, theta, 1)
+    got = from_dev(X).reshape(B, S, nq + 2 * nkv, d)
+    ref = oracle.rope(x32.reshape(B, S, nq + 2 * nkv, d)[:, :, :nq + nkv], theta)
+    assert rel_l2(got[:, :, :nq + nkv], ref) < 6e-3
+    np.testing.assert_array_equal(got[:, :, nq + nkv:], x32.reshape(B, S, -1, d)[:, :, nq + nkv:])  # v untouched
+    mt.mt_op_rope(X, tab, B, S, width, 0, nq + nkv, d, theta, -1)
+    assert rel_l2(from_dev(X), x32) < 1e-2
+
+
+@pytest.mark.parametrize("F,ld", [(172, 176), (256, 256)])
+def test_swiglu_forward_backward(F, ld):
+    torch, mt = need_gpu()
+    T = 53
+    g, u, da = _normal((T, F), 41), _normal((T, F), 42), _normal((T, F), 43)
+    gu = np.zeros((T, 2 * ld), np.float32)
+    gu[:, :F], gu[:, ld:ld + F] = g, u
+    GU, gu32 = to_dev_bf16(torch, gu)
+    DA = np.zeros((T, ld), np.float32)
+    DA[:, :F] = da
+    DAd, da32 = to_dev_bf16(torch, DA)
+    ACT = torch.full((T, ld), 7.0, dtype=torch.bfloat16, device="cuda")
+    mt.mt_op_swiglu_fwd(GU, ACT, T, F, ld)
+    a_ref, dg_ref, du_ref = oracle.swiglu(gu32[:, :F], gu32[:, ld:ld + F], da32[:, :F])
+    act = from_dev(ACT)
+    assert rel_l2(act[:, :F], a_ref) < 6e-3
+    assert np.all(act[:, F:] == 0)
+    mt.mt_op_swiglu_bwd(GU, DAd, T, F, ld)
+    out = from_dev(GU)
+    assert rel_l2(out[:, :F], dg_ref) < 6e-3
+    assert rel_l2(out[:, ld:ld + F], du_ref) < 6e-3
+
+
+@pytest.mark.parametrize("d,S,nq,nkv", [(16, 32, 4, 4), (64, 200, 4, 2), (128, 130, 8, 2), (128, 1, 2, 1)])
+def test_attention_forward_backward(d, S, nq, nkv):
+    torch, mt = need_gpu()
+    B = 2
+    q, k, v, do = (_normal((B, S, n, d), 50 + i) for i, n in enumerate((nq, nkv, nkv, nq)))
+    Q, q32 = to_dev_bf16(torch, q)
+    Kd, k32 = to_dev_bf16(torch, k)
+    Vd, v32 = to_dev_bf16(torch, v)
+    DO, do32 = to_dev_bf16(torch, do)
+    O = torch.empty((B, S, nq, d), dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((B, nq, S), device="cuda")
+    mt.mt_op_attention_fwd(Q, Kd, Vd, O, LSE, B, S, nq, nkv, d, nq * d, nkv * d, nq * d)
+    o_ref, lse_ref, *_ = oracle.attention(q32, k32, v32)
+    assert rel_l2(from_dev(O), o_ref) < 1.5e-2
+    assert np.max(np.abs(from_dev(LSE) - lse_ref)) < 1e-3
+    dQ = torch.empty_like(Q)
+    dK = torch.empty_like(Kd)
+    dV = torch.empty_like(Vd)
+    ws = torch.empty(mt.mt_op_attention_bwd_workspace(B, S, nq), device="cuda")
+    mt.mt_op_attention_bwd(Q, Kd, Vd, O, DO, LSE, dQ, dK, dV, ws, B, S, nq, nkv, d, nq * d, nkv * d, nq * d)
+    _, _, dq_ref, dk_ref, dv_ref = oracle.attention(q32, k32, v32, do32)
+    assert rel_l2(from_dev(dQ), dq_ref) < 2e-2
+    assert rel_l2(from_dev(dK), dk_ref) < 2e-2
+    assert rel_l2(from_dev(dV), dv_ref) < 2e-2
+    assert mt.mt_op_device_error() == 0
+
+
+def test_lmhead_cross_entropy():
+    torch, mt = need_gpu()
+    T, V, h = 96, 1000, 128
+    X, x32 = to_dev_bf16(torch, _normal((T, h), 61))
+    W, w32 = to_dev_bf16(torch, _normal((V, h), 62, 0.1))
+    lab = np.random.default_rng(1).integers(0, V, T).astype(np.int32)
+    LAB = torch.from_numpy(lab).cuda()
+    dX = torch.empty((T, h), device="cuda")
+    dW = torch.empty((V, h), device="cuda")
+    loss = torch.zeros(1, device="cuda")
+    ws = torch.empty(mt.mt_op_lmhead_ce_workspace(T, V, h), dtype=torch.uint8, device="cuda")
+    mt.mt_op_lmhead_ce(X, W, LAB, 1.0 / T, dX, dW, loss, ws, T, V, h)
+    z = oracle.matmul("nt", x32, w32)
+    l_ref, dz = oracle.cross_entropy(z, lab)
+    assert abs(float(loss.item()) - l_ref) < 1e-4 * abs(l_ref)
+    dzb = bf16_round(dz)
+    assert rel_l2(from_dev(dX), oracle.matmul("nn", dzb, w32)) < 6e-3
+    assert rel_l2(from_dev(dW), oracle.matmul("tn", dzb, x32)) < 6e-3
