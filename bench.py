@@ -32,6 +32,12 @@ WORKLOADS = {
     "tiny": (2, 64, 4, 4, 16, 172, 256, 1e4, 2, 32, 1, False),
 }
 METRIC = "train tokens/sec (fwd+bwd, weights streamed from host) at 8B shape; % roofline"
+_T0 = time.time()
+
+
+def log(msg: str) -> None:
+    sys.stderr.write(f"[bench +{time.time() - _T0:7.1f}s] {msg}\n")
+    sys.stderr.flush()
 
 
 def read_peaks():
@@ -205,9 +211,19 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fuse-top", action="store_true", help="recompute the top block too")
     ap.add_argument("--serial", action="store_true", help="ablation: serialise weight copies and compute")
+    ap.add_argument("--layers", type=int, default=None, help="diagnostic override of the layer count")
+    ap.add_argument("--seq", type=int, default=None, help="diagnostic override of the sequence length")
+    ap.add_argument("--batch", type=int, default=None, help="diagnostic override of the batch")
     args = ap.parse_args()
-    wl = WORKLOADS[args.workload]
-    shape, (B, S, K, bf16) = wl[:8], wl[8:]
+    wl = list(WORKLOADS[args.workload])
+    if args.layers:
+        wl[0] = args.layers
+    if args.seq:
+        wl[9] = args.seq
+    if args.batch:
+        wl[8] = args.batch
+    shape, (B, S, K, bf16) = tuple(wl[:8]), wl[8:]
+    K = min(K, shape[0])
     if args.impl == "reference":
         return run_reference(args, shape, B, S)
 
@@ -232,6 +248,7 @@ def main():
     L, h, nq, nkv, d, F, V, theta = shape
     cfg = mt.make_cfg(L, h, nq, nkv, d, F, V, theta, 1e-5, B, S, K, mt.MT_BF16 if bf16 else mt.MT_F32)
     budget = mt.mt_required_budget(cfg)
+    log(f"workload {args.workload} L={L} B={B} S={S} K={K}: device arena {budget / 2**30:.2f} GiB")
     arena = torch.empty(budget, dtype=torch.uint8, device="cuda")
     streams = [torch.cuda.Stream() for _ in range(3)]
     sess = mt.Session(mt.ModelShape(L, h, nq, nkv, d, F, V, theta, 1e-5), B, S, K,
@@ -245,14 +262,19 @@ def main():
             off, nbytes = sess.offset(unit, t)
             is_gain = (unit >= 1 and unit <= L and t in (0, 5)) or (unit == L + 1 and t == 0)
             offs.append((unit, t, off, nbytes // (2 if bf16 else 4), is_gain))
+    log(f"context created; pinned host params {sess.param_bytes / 2**30:.2f} GiB, grads {sess.grad_bytes / 2**30:.2f} GiB")
     t0 = time.perf_counter()
     seedgen.fill_packed_params(sess.params_ptr, offs, bf16, seed=21 + rank)
     init_s = time.perf_counter() - t0
     tok, lab = seedgen.tokens_and_labels(B, S, V, seed=22 + rank)
 
+    log(f"parameters filled in {init_s:.1f} s")
     link = host_link_probe(torch)
-    for _ in range(args.warmup):
+    log(f"host link {link}")
+    for i in range(args.warmup):
+        t1 = time.perf_counter()
         sess.step(tok, lab, K)
+        log(f"warmup step {i}: {time.perf_counter() - t1:.3f} s")
     comp, d2h_stream = streams[0], streams[2]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     agg = {}
@@ -272,6 +294,7 @@ def main():
     ev1.record(d2h_stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    log(f"timed {args.steps} steps in {wall:.3f} s")
     clk = clocks.stop()
     dev_ms = ev0.elapsed_time(ev1)
     if dist:
@@ -340,6 +363,7 @@ def main():
         "init_s": init_s,
     }
     if not args.no_cpu_baseline and world == 1:
+        log("timing the CPU oracle sample")
         v, t1 = cpu_oracle_sample(shape, 8)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": f"one decoder layer + LM head of the {args.workload} shape at B=1, S=8 "

@@ -1,0 +1,812 @@
+// Causal GQA flash attention on the 5th-generation tensor cores.
+//
+// Forward (one CTA per (128-row query tile, query head, sequence)): Q stays
+// in shared memory, K/V tiles stream through a two-stage TMA ring;
+// S = Q K^T lands in tensor memory (two S buffers so the next product
+// overlaps this tile's softmax), the softmax warps (one thread per query
+// row) apply the causal mask and the online-softmax update, write P as bf16
+// into shared memory in the MMA operand layout, and O += P V accumulates in
+// tensor memory. The running maximum is only moved (and O rescaled) when it
+// grows by more than 2^8, which keeps every exponent bounded while skipping
+// most rescales; the final O / l and log-sum-exp use the same reference, so
+// the result is exact up to rounding.
+//
+// Backward: delta = rowsum(dO * O) first; then one pass per 128-row KV tile
+// (all query heads of its group, all query tiles at or after it) computes
+// S^T = K Q^T and dP^T = V dO^T, P^T = exp(S^T - lse), dS^T = P^T (dP^T -
+// delta), and accumulates dV += P^T dO, dK += dS^T Q in tensor memory; a
+// separate pass per query tile accumulates dQ += dS K. Each output row is
+// produced by one CTA with a fixed loop order: deterministic.
+//
+// Operand layouts (128-byte swizzle, 1024-byte aligned tiles):
+//  Q/K/V/dO tiles come from TMA as [128 rows][64 head-dim] boxes (head dims
+//  below 64 are zero-filled by TMA), which is K-major for Q K^T-type
+//  products and MN-major for P V-type products. P / dS tiles are written by
+//  the softmax threads as [128 rows][128] K-major (two 64-column blocks).
+#include "common.cuh"
+#include "kernels.h"
+
+namespace mt {
+
+MT_DEVICE_ERROR_READER(attention_tc_take_device_error)
+
+namespace {
+
+constexpr int TILE = 128;
+constexpr int BOX = 128 * 64 * 2;  // one [128 rows][64] bf16 box = 16 KB
+
+// ---- small device helpers --------------------------------------------------
+__device__ __forceinline__ void tma_load_4d(void* dst, const CUtensorMap* map, uint64_t* bar, int x, int y, int z,
+                                            int w) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4, %5}], "
+      "[%6];" ::"r"(smem_u32(dst)),
+      "l"((uint64_t)map), "r"(x), "r"(y), "r"(z), "r"(w), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Load a [128 rows][D] tile of one head (D/64 boxes, at least one).
+template <int D>
+__device__ __forceinline__ void load_head_tile(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int head,
+                                               int row0, int b) {
+#pragma unroll
+  for (int i = 0; i < (D + 63) / 64; ++i) tma_load_4d(dst + i * BOX, map, bar, i * 64, head, row0, b);
+}
+template <int D>
+constexpr uint32_t tile_bytes() {
+  return ((D + 63) / 64) * BOX;
+}
+
+// Write columns [32c, 32c+32) of row r of a [128][128] K-major swizzled tile.
+__device__ __forceinline__ void st_tile_row32(uint8_t* tile, int r, int c, const float (&v)[32]) {
+  uint8_t* rowp = tile + (c >> 1) * 16384 + r * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int chunk = (c & 1) * 4 + i;
+    uint4 w;
+    w.x = pack_bf2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf2(v[8 * i + 6], v[8 * i + 7]);
+    *(uint4*)(rowp + ((chunk ^ (r & 7)) << 4)) = w;
+  }
+}
+
+// K-major A/B descriptor of the k-th 16-wide step of a [128][64*n] tile.
+__device__ __forceinline__ uint64_t kmaj_desc(const uint8_t* tile, int kk) {
+  return make_sdesc(smem_u32(tile) + (kk >> 2) * BOX + (kk & 3) * 32, 16, 1024);
+}
+// MN-major B descriptor (N = head dim, K = rows) of the k-th 16-row step.
+__device__ __forceinline__ uint64_t mnmaj_desc(const uint8_t* tile, int kk) {
+  return make_sdesc(smem_u32(tile) + kk * 2048, BOX, 1024);
+}
+
+__device__ __forceinline__ void store_row_bf16(uint16_t* dst, const uint32_t (&r)[32], int n, float mul) {
+  // n valid columns (<= 32); dst 16-byte aligned when n == 32
+  if (n == 32) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+      uint4 w;
+      w.x = pack_bf2(__uint_as_float(r[8 * v + 0]) * mul, __uint_as_float(r[8 * v + 1]) * mul);
+      w.y = pack_bf2(__uint_as_float(r[8 * v + 2]) * mul, __uint_as_float(r[8 * v + 3]) * mul);
+      w.z = pack_bf2(__uint_as_float(r[8 * v + 4]) * mul, __uint_as_float(r[8 * v + 5]) * mul);
+      w.w = pack_bf2(__uint_as_float(r[8 * v + 6]) * mul, __uint_as_float(r[8 * v + 7]) * mul);
+      ((uint4*)dst)[v] = w;
+    }
+  } else {
+#pragma unroll
+    for (int v = 0; v < 2; ++v) {  // n == 16
+      uint4 w;
+      w.x = pack_bf2(__uint_as_float(r[8 * v + 0]) * mul, __uint_as_float(r[8 * v + 1]) * mul);
+      w.y = pack_bf2(__uint_as_float(r[8 * v + 2]) * mul, __uint_as_float(r[8 * v + 3]) * mul);
+      w.z = pack_bf2(__uint_as_float(r[8 * v + 4]) * mul, __uint_as_float(r[8 * v + 5]) * mul);
+      w.w = pack_bf2(__uint_as_float(r[8 * v + 6]) * mul, __uint_as_float(r[8 * v + 7]) * mul);
+      ((uint4*)dst)[v] = w;
+    }
+  }
+}
+
+struct AttnArgs {
+  uint16_t* o;       // fwd output / unused
+  float* lse;        // [B, nq, S] natural log
+  const float* lse_in;
+  const float* delta;
+  uint16_t *dq, *dk, *dv;
+  int B, S, nq, nkv, ldq, ldkv, ldo;
+  float scale_log2;  // log2(e) / sqrt(d)
+  float scale;       // 1 / sqrt(d)
+};
+
+constexpr float kLn2 = 0.69314718055994530942f;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units
+
+// ===========================================================================
+// Forward
+// ===========================================================================
+template <int D>
+struct FwdSmem {
+  static constexpr int Q = 0;
+  static constexpr int K0 = Q + tile_bytes<D>();
+  static constexpr int V0 = K0 + 2 * tile_bytes<D>();
+  static constexpr int P = V0 + 2 * tile_bytes<D>();
+  static constexpr int BAR = P + 2 * BOX;
+  static constexpr int TOTAL = BAR + 256;
+  static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;  // one CTA per SM
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                       const __grid_constant__ CUtensorMap tv, AttnArgs a) {
+  using L = FwdSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(sm + L::BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;   // [2]
+  uint64_t* kv_empty = bars + 3;  // [2]
+  uint64_t* s_full = bars + 5;    // [2]
+  uint64_t* s_empty = bars + 7;   // [2]
+  uint64_t* p_full = bars + 9;
+  uint64_t* o_done = bars + 10;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 11);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int nqt = (a.S + TILE - 1) / TILE;
+  const int qt = nqt - 1 - (int)blockIdx.x;  // longest tiles first
+  const int j = blockIdx.y, b = blockIdx.z;
+  const int g = j / (a.nq / a.nkv);
+  const int ntiles = qt + 1;
+  const uint32_t warp = warp_id(), lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+    }
+    mbar_init(p_full, 4);
+    mbar_init(o_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;  // S0: +0, S1: +128, O: +256
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      mbar_arrive_expect_tx(q_full, tile_bytes<D>());
+      load_head_tile<D>(sm + L::Q, &tq, q_full, j, qt * TILE, b);
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t & 1;
+        mbar_wait(&kv_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&kv_full[st], 2 * tile_bytes<D>());
+        load_head_tile<D>(sm + L::K0 + st * tile_bytes<D>(), &tk, &kv_full[st], g, t * TILE, b);
+        load_head_tile<D>(sm + L::V0 + st * tile_bytes<D>(), &tv, &kv_full[st], g, t * TILE, b);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = make_idesc(128, 128, false, false);
+      constexpr uint32_t IDESC_O = make_idesc(128, D < 64 ? 64 : D, false, true);  // padded head dims read zeros
+      constexpr int KS = D / 16;  // K steps of Q K^T (zero-padded columns skipped)
+      mbar_wait(q_full, 0, abort_flag, kErrTimeoutAttn);
+      auto issue_pv = [&](int t) {
+        const int st = t & 1;
+        mbar_wait(p_full, t & 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+        const uint8_t* vt = sm + L::V0 + st * tile_bytes<D>();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          tc_mma(tmem + 256, kmaj_desc(sm + L::P, kk), mnmaj_desc(vt, kk), IDESC_O, (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(o_done);
+        tc_commit(&kv_empty[st]);
+      };
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t & 1;
+        mbar_wait(&kv_full[st], (t >> 1) & 1, abort_flag, kErrTimeoutAttn);
+        mbar_wait(&s_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+        const uint8_t* kt = sm + L::K0 + st * tile_bytes<D>();
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)
+          tc_mma(tmem + st * 128, kmaj_desc(sm + L::Q, kk), kmaj_desc(kt, kk), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(&s_full[st]);
+        if (t > 0) issue_pv(t - 1);
+      }
+      issue_pv(ntiles - 1);
+    }
+    __syncwarp();
+  } else {
+    // softmax / epilogue: thread owns query row r of the tile
+    const uint32_t q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int trow = qt * TILE + r;  // position in the sequence
+    const uint32_t lane_base = (q4 * 32) << 16;
+    float m_ref = -INFINITY, l = 0.f;
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t & 1;
+      mbar_wait(&s_full[st], (t >> 1) & 1, abort_flag, kErrTimeoutAttn);
+      tc_fence_after();
+      const int kv0 = t * TILE;
+      const bool diag = (t == qt);
+      const bool tail = kv0 + TILE > a.S;
+      // pass 1: row maximum
+      float mx = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_base + st * 128 + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int kv = kv0 + c * 32 + i;
+          const bool ok = !((diag && kv > trow) || (tail && kv >= a.S));
+          if (ok) mx = fmaxf(mx, __uint_as_float(v[i]));
+        }
+      }
+      const float m_new = mx * a.scale_log2;
+      // the previous P V product must be complete before O or P is touched
+      if (t > 0) mbar_wait(o_done, (t - 1) & 1, abort_flag, kErrTimeoutAttn);
+      tc_fence_after();
+      // The rescale touches O through warp-collective tensor-memory loads and
+      // stores, so the decision is taken per warp: if any row of the warp
+      // needs a new reference maximum, every row of the warp moves its
+      // reference to max(m_new, m_ref) (alpha = 1 where nothing changes).
+      if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold) || t == 0) {
+        const float m_use = fmaxf(m_new, m_ref);
+        const float alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_use);
+        l *= alpha;
+        if (t > 0) {
+#pragma unroll 1
+          for (int c = 0; c < (D + 31) / 32; ++c) {
+            uint32_t v[32];
+            __syncwarp();
+            tmem_ld32(tmem + lane_base + 256 + c * 32, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
+            tmem_st32(tmem + lane_base + 256 + c * 32, v);
+          }
+          tmem_st_wait();
+        }
+        m_ref = m_use;
+      }
+      // pass 2: probabilities (relative to m_ref), row sum, P to shared memory
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_base + st * 128 + c * 32, v);
+        tmem_ld_wait();
+        float p[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int kv = kv0 + c * 32 + i;
+          const bool ok = !((diag && kv > trow) || (tail && kv >= a.S));
+          p[i] = ok ? exp2f(__uint_as_float(v[i]) * a.scale_log2 - m_ref) : 0.f;
+          l += p[i];
+        }
+        st_tile_row32(sm + L::P, r, c, p);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&s_empty[st]);
+        mbar_arrive(p_full);
+      }
+    }
+    // epilogue: O / l and the log-sum-exp
+    mbar_wait(o_done, (ntiles - 1) & 1, abort_flag, kErrTimeoutAttn);
+    tc_fence_after();
+    const bool row_ok = trow < a.S;
+    const float inv_l = 1.f / l;
+    uint16_t* orow = a.o + ((size_t)b * a.S + trow) * a.ldo + (size_t)j * D;
+#pragma unroll 1
+    for (int c = 0; c < (D + 31) / 32; ++c) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld32(tmem + lane_base + 256 + c * 32, v);
+      tmem_ld_wait();
+      if (row_ok) store_row_bf16(orow + c * 32, v, D < 32 ? D : 32, inv_l);
+    }
+    if (row_ok) a.lse[((size_t)b * a.nq + j) * a.S + trow] = (m_ref + log2f(l)) * kLn2;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// Backward, dK/dV pass: CTA = (128-row KV tile, KV head, sequence).
+// TMEM: S^T +0, dP^T +128, dV +256, dK +384.
+// ===========================================================================
+template <int D>
+struct DkvSmem {
+  static constexpr int K = 0;
+  static constexpr int V = K + tile_bytes<D>();
+  static constexpr int Q = V + tile_bytes<D>();
+  static constexpr int DO = Q + tile_bytes<D>();
+  static constexpr int P = DO + tile_bytes<D>();
+  static constexpr int DS = P + 2 * BOX;
+  static constexpr int LSE = DS + 2 * BOX;    // 128 floats
+  static constexpr int DELTA = LSE + 512;     // 128 floats
+  static constexpr int BAR = DELTA + 512;
+  static constexpr int TOTAL = BAR + 256;
+  static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                           AttnArgs a) {
+  using L = DkvSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(sm + L::BAR);
+  uint64_t* kv_full = bars + 0;
+  uint64_t* qdo_full = bars + 1;
+  uint64_t* qdo_empty = bars + 2;
+  uint64_t* s_full = bars + 3;
+  uint64_t* s_empty = bars + 4;
+  uint64_t* p_full = bars + 5;
+  uint64_t* pd_done = bars + 6;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 7);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  float* s_lse = (float*)(sm + L::LSE);
+  float* s_delta = (float*)(sm + L::DELTA);
+
+  const int nt = (a.S + TILE - 1) / TILE;
+  const int kt = (int)blockIdx.x;  // KV tile (short first: low tiles have the most work, scheduled first by y order)
+  const int g = blockIdx.y, b = blockIdx.z;
+  const int grp = a.nq / a.nkv;
+  const int nq_tiles = nt - kt;   // query tiles kt .. nt-1
+  const int iters = grp * nq_tiles;
+  const uint32_t warp = warp_id(), lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(kv_full, 1);
+    mbar_init(qdo_full, 1);
+    mbar_init(qdo_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 4);
+    mbar_init(p_full, 4);
+    mbar_init(pd_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(kv_full, 2 * tile_bytes<D>());
+      load_head_tile<D>(sm + L::K, &tk, kv_full, g, kt * TILE, b);
+      load_head_tile<D>(sm + L::V, &tv, kv_full, g, kt * TILE, b);
+      for (int it = 0; it < iters; ++it) {
+        const int j = g * grp + it / nq_tiles;
+        const int qt = kt + it % nq_tiles;
+        mbar_wait(qdo_empty, (it & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(qdo_full, 2 * tile_bytes<D>());
+        load_head_tile<D>(sm + L::Q, &tq, qdo_full, j, qt * TILE, b);
+        load_head_tile<D>(sm + L::DO, &tdo, qdo_full, j, qt * TILE, b);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = make_idesc(128, 128, false, false);
+      constexpr uint32_t IDESC_G = make_idesc(128, D < 64 ? 64 : D, false, true);
+      constexpr int KS = D / 16;
+      mbar_wait(kv_full, 0, abort_flag, kErrTimeoutAttn);
+      for (int it = 0; it < iters; ++it) {
+        mbar_wait(qdo_full, it & 1, abort_flag, kErrTimeoutAttn);
+        mbar_wait(s_empty, (it & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)  // S^T = K Q^T
+          tc_mma(tmem + 0, kmaj_desc(sm + L::K, kk), kmaj_desc(sm + L::Q, kk), IDESC_S, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)  // dP^T = V dO^T
+          tc_mma(tmem + 128, kmaj_desc(sm + L::V, kk), kmaj_desc(sm + L::DO, kk), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(s_full);
+        mbar_wait(p_full, it & 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q
+          tc_mma(tmem + 256, kmaj_desc(sm + L::P, kk), mnmaj_desc(sm + L::DO, kk), IDESC_G,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+          tc_mma(tmem + 384, kmaj_desc(sm + L::DS, kk), mnmaj_desc(sm + L::Q, kk), IDESC_G,
+                 (it > 0 || kk > 0) ? 1u : 0u);
+        }
+        tc_commit(pd_done);
+        tc_commit(qdo_empty);
+      }
+    }
+    __syncwarp();
+  } else {
+    const uint32_t q4 = warp & 3;
+    const int r = q4 * 32 + lane;       // KV row of the tile
+    const int srow = kt * TILE + r;     // KV position
+    const uint32_t lane_base = (q4 * 32) << 16;
+    const int tid = threadIdx.x - 64;   // 0..127
+    for (int it = 0; it < iters; ++it) {
+      const int j = g * grp + it / nq_tiles;
+      const int qt = kt + it % nq_tiles;
+      const int q0 = qt * TILE;
+      // per-column log-sum-exp (log2 units) and delta of this query tile
+      named_bar_sync(1, 128);  // previous iteration finished reading s_lse / s_delta
+      {
+        const int tq = q0 + tid;
+        const size_t ri = ((size_t)b * a.nq + j) * a.S + tq;
+        s_lse[tid] = tq < a.S ? a.lse_in[ri] * 1.4426950408889634f : INFINITY;
+        s_delta[tid] = tq < a.S ? a.delta[ri] : 0.f;
+      }
+      named_bar_sync(1, 128);
+      mbar_wait(s_full, it & 1, abort_flag, kErrTimeoutAttn);
+      tc_fence_after();
+      // the previous iteration's dV/dK products must be done with P / dS
+      if (it > 0) mbar_wait(pd_done, (it - 1) & 1, abort_flag, kErrTimeoutAttn);
+      const bool diag = (qt == kt);
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dv[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_base + 0 + c * 32, sv);
+        tmem_ld32(tmem + lane_base + 128 + c * 32, dv);
+        tmem_ld_wait();
+        float p[32], ds[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int col = c * 32 + i;
+          const int tq = q0 + col;
+          const bool ok = !(diag && tq < srow) && tq < a.S;  // query at or after key
+          const float pv = ok ? exp2f(__uint_as_float(sv[i]) * a.scale_log2 - s_lse[col]) : 0.f;
+          p[i] = pv;
+          ds[i] = pv * (__uint_as_float(dv[i]) - s_delta[col]);
+        }
+        st_tile_row32(sm + L::P, r, c, p);
+        st_tile_row32(sm + L::DS, r, c, ds);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(s_empty);
+        mbar_arrive(p_full);
+      }
+    }
+    mbar_wait(pd_done, (iters - 1) & 1, abort_flag, kErrTimeoutAttn);
+    tc_fence_after();
+    const bool row_ok = srow < a.S;
+    const size_t orow = ((size_t)b * a.S + srow) * a.ldkv + (size_t)g * D;
+#pragma unroll 1
+    for (int c = 0; c < (D + 31) / 32; ++c) {
+      uint32_t v[32], k[32];
+      __syncwarp();
+      tmem_ld32(tmem + lane_base + 256 + c * 32, v);
+      tmem_ld32(tmem + lane_base + 384 + c * 32, k);
+      tmem_ld_wait();
+      if (row_ok) {
+        store_row_bf16(a.dv + orow + c * 32, v, D < 32 ? D : 32, 1.f);
+        store_row_bf16(a.dk + orow + c * 32, k, D < 32 ? D : 32, a.scale);
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// ===========================================================================
+// Backward, dQ pass: CTA = (128-row query tile, query head, sequence).
+// TMEM: S +0, dP +128, dQ +256.
+// ===========================================================================
+template <int D>
+struct DqSmem {
+  static constexpr int Q = 0;
+  static constexpr int DO = Q + tile_bytes<D>();
+  static constexpr int K = DO + tile_bytes<D>();
+  static constexpr int V = K + tile_bytes<D>();
+  static constexpr int DS = V + tile_bytes<D>();
+  static constexpr int BAR = DS + 2 * BOX;
+  static constexpr int TOTAL = BAR + 256;
+  static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
+};
+
+template <int D>
+__global__ void __launch_bounds__(192, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+                          const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
+                          AttnArgs a) {
+  using L = DqSmem<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint64_t* bars = (uint64_t*)(sm + L::BAR);
+  uint64_t* q_full = bars + 0;
+  uint64_t* kv_full = bars + 1;
+  uint64_t* kv_empty = bars + 2;
+  uint64_t* s_full = bars + 3;
+  uint64_t* s_empty = bars + 4;
+  uint64_t* p_full = bars + 5;
+  uint64_t* g_done = bars + 6;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 7);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const int nqt = (a.S + TILE - 1) / TILE;
+  const int qt = nqt - 1 - (int)blockIdx.x;
+  const int j = blockIdx.y, b = blockIdx.z;
+  const int g = j / (a.nq / a.nkv);
+  const int ntiles = qt + 1;
+  const uint32_t warp = warp_id(), lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    mbar_init(q_full, 1);
+    mbar_init(kv_full, 1);
+    mbar_init(kv_empty, 1);
+    mbar_init(s_full, 1);
+    mbar_init(s_empty, 4);
+    mbar_init(p_full, 4);
+    mbar_init(g_done, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      prefetch_tmap(&tq);
+      prefetch_tmap(&tk);
+      prefetch_tmap(&tv);
+      prefetch_tmap(&tdo);
+      mbar_arrive_expect_tx(q_full, 2 * tile_bytes<D>());
+      load_head_tile<D>(sm + L::Q, &tq, q_full, j, qt * TILE, b);
+      load_head_tile<D>(sm + L::DO, &tdo, q_full, j, qt * TILE, b);
+      for (int t = 0; t < ntiles; ++t) {
+        mbar_wait(kv_empty, (t & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(kv_full, 2 * tile_bytes<D>());
+        load_head_tile<D>(sm + L::K, &tk, kv_full, g, t * TILE, b);
+        load_head_tile<D>(sm + L::V, &tv, kv_full, g, t * TILE, b);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0) {
+      constexpr uint32_t IDESC_S = make_idesc(128, 128, false, false);
+      constexpr uint32_t IDESC_G = make_idesc(128, D < 64 ? 64 : D, false, true);
+      constexpr int KS = D / 16;
+      mbar_wait(q_full, 0, abort_flag, kErrTimeoutAttn);
+      for (int t = 0; t < ntiles; ++t) {
+        mbar_wait(kv_full, t & 1, abort_flag, kErrTimeoutAttn);
+        mbar_wait(s_empty, (t & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)  // S = Q K^T
+          tc_mma(tmem + 0, kmaj_desc(sm + L::Q, kk), kmaj_desc(sm + L::K, kk), IDESC_S, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)  // dP = dO V^T
+          tc_mma(tmem + 128, kmaj_desc(sm + L::DO, kk), kmaj_desc(sm + L::V, kk), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(s_full);
+        mbar_wait(p_full, t & 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)  // dQ += dS K
+          tc_mma(tmem + 256, kmaj_desc(sm + L::DS, kk), mnmaj_desc(sm + L::K, kk), IDESC_G,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(g_done);
+        tc_commit(kv_empty);
+      }
+    }
+    __syncwarp();
+  } else {
+    const uint32_t q4 = warp & 3;
+    const int r = q4 * 32 + lane;
+    const int trow = qt * TILE + r;
+    const uint32_t lane_base = (q4 * 32) << 16;
+    const bool row_ok = trow < a.S;
+    const size_t ri = ((size_t)b * a.nq + j) * a.S + (row_ok ? trow : 0);
+    const float lse2 = row_ok ? a.lse_in[ri] * 1.4426950408889634f : 0.f;
+    const float dl = row_ok ? a.delta[ri] : 0.f;
+    for (int t = 0; t < ntiles; ++t) {
+      mbar_wait(s_full, t & 1, abort_flag, kErrTimeoutAttn);
+      tc_fence_after();
+      if (t > 0) mbar_wait(g_done, (t - 1) & 1, abort_flag, kErrTimeoutAttn);
+      const int kv0 = t * TILE;
+      const bool diag = (t == qt);
+      const bool tail = kv0 + TILE > a.S;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t sv[32], dv[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_base + 0 + c * 32, sv);
+        tmem_ld32(tmem + lane_base + 128 + c * 32, dv);
+        tmem_ld_wait();
+        float ds[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int kv = kv0 + c * 32 + i;
+          const bool ok = row_ok && !((diag && kv > trow) || (tail && kv >= a.S));
+          const float pv = ok ? exp2f(__uint_as_float(sv[i]) * a.scale_log2 - lse2) : 0.f;
+          ds[i] = pv * (__uint_as_float(dv[i]) - dl);
+        }
+        st_tile_row32(sm + L::DS, r, c, ds);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(s_empty);
+        mbar_arrive(p_full);
+      }
+    }
+    mbar_wait(g_done, (ntiles - 1) & 1, abort_flag, kErrTimeoutAttn);
+    tc_fence_after();
+    uint16_t* orow = a.dq + ((size_t)b * a.S + trow) * a.ldq + (size_t)j * D;
+#pragma unroll 1
+    for (int c = 0; c < (D + 31) / 32; ++c) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld32(tmem + lane_base + 256 + c * 32, v);
+      tmem_ld_wait();
+      if (row_ok) store_row_bf16(orow + c * 32, v, D < 32 ? D : 32, a.scale);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
+// delta[b, j, t] = sum_e dO[t, j, e] * O[t, j, e]  (one warp per row)
+__global__ void attn_delta_tc_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
+                                     float* __restrict__ delta, int B, int S, int nq, int d, int ldo) {
+  const size_t wid = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  if (wid >= (size_t)B * S * nq) return;
+  const int j = (int)(wid % nq);
+  const int t = (int)((wid / nq) % S);
+  const int b = (int)(wid / ((size_t)nq * S));
+  const size_t off = ((size_t)b * S + t) * ldo + (size_t)j * d;
+  float s = 0.f;
+  for (int e = lane_id() * 2; e < d; e += 64) {
+    const uint32_t ov = *(const uint32_t*)(o + off + e), gv = *(const uint32_t*)(dout + off + e);
+    s += bf2f(ov & 0xffff) * bf2f(gv & 0xffff) + bf2f(ov >> 16) * bf2f(gv >> 16);
+  }
+  s = warp_sum(s);
+  if (lane_id() == 0) delta[((size_t)b * nq + j) * S + t] = s;
+}
+
+// 4D map over a [B, S, heads, d] view with row stride ld (elements).
+int head_map(CUtensorMap* m, const void* base, int d, int heads, int S, int B, int ld) {
+  const uint64_t gdim[4] = {(uint64_t)d, (uint64_t)heads, (uint64_t)S, (uint64_t)B};
+  const uint64_t gstride[3] = {(uint64_t)d * 2, (uint64_t)ld * 2, (uint64_t)S * ld * 2};
+  const uint32_t box[4] = {64, 1, 128, 1};
+  return mt_host::encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, gdim, gstride, box,
+                               CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS
+             ? 0
+             : -1;
+}
+
+template <typename K>
+bool set_smem(K kern, int bytes) {
+  return cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) == cudaSuccess;
+}
+
+template <int D>
+int fwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, AttnArgs& a, cudaStream_t st) {
+  CUtensorMap tq, tk, tv;
+  if (head_map(&tq, q, D, a.nq, a.S, a.B, a.ldq) || head_map(&tk, k, D, a.nkv, a.S, a.B, a.ldkv) ||
+      head_map(&tv, v, D, a.nkv, a.S, a.B, a.ldkv))
+    return -1;
+  static bool init = false;
+  if (!init) {
+    if (!set_smem(attn_fwd_tc_kernel<D>, FwdSmem<D>::ALLOC)) return -1;
+    init = true;
+  }
+  dim3 grid((a.S + TILE - 1) / TILE, a.nq, a.B);
+  attn_fwd_tc_kernel<D><<<grid, 192, FwdSmem<D>::ALLOC, st>>>(tq, tk, tv, a);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+template <int D>
+int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
+               AttnArgs& a, float* delta, cudaStream_t st) {
+  CUtensorMap tq, tk, tv, tdo;
+  if (head_map(&tq, q, D, a.nq, a.S, a.B, a.ldq) || head_map(&tk, k, D, a.nkv, a.S, a.B, a.ldkv) ||
+      head_map(&tv, v, D, a.nkv, a.S, a.B, a.ldkv) || head_map(&tdo, dout, D, a.nq, a.S, a.B, a.ldo))
+    return -1;
+  static bool init = false;
+  if (!init) {
+    if (!set_smem(attn_bwd_dkv_tc_kernel<D>, DkvSmem<D>::ALLOC) || !set_smem(attn_bwd_dq_tc_kernel<D>, DqSmem<D>::ALLOC))
+      return -1;
+    init = true;
+  }
+  const size_t rows = (size_t)a.B * a.S * a.nq;
+  attn_delta_tc_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(o, dout, delta, a.B, a.S, a.nq, D, a.ldo);
+  a.delta = delta;
+  const int nt = (a.S + TILE - 1) / TILE;
+  attn_bwd_dkv_tc_kernel<D><<<dim3(nt, a.nkv, a.B), 192, DkvSmem<D>::ALLOC, st>>>(tq, tk, tv, tdo, a);
+  attn_bwd_dq_tc_kernel<D><<<dim3(nt, a.nq, a.B), 192, DqSmem<D>::ALLOC, st>>>(tq, tk, tv, tdo, a);
+  count_launches(3);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+bool tc_ok(int B, int S, int nq, int nkv, int d, int ldq, int ldkv, int ldo, const void* q, const void* k,
+           const void* v) {
+  if (B <= 0 || S <= 0 || nq <= 0 || nkv <= 0 || nq % nkv) return false;
+  if (d != 16 && d != 32 && d != 64 && d != 128) return false;
+  if ((ldq & 7) || (ldkv & 7) || (ldo & 7)) return false;
+  if (((uintptr_t)q & 15) || ((uintptr_t)k & 15) || ((uintptr_t)v & 15)) return false;
+  return true;
+}
+
+}  // namespace
+
+int attention_fwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int B, int S,
+                     int nq, int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st) {
+  if (!tc_ok(B, S, nq, nkv, d, ldq, ldkv, ldo, q, k, v)) return -1;
+  AttnArgs a{o, lse, nullptr, nullptr, nullptr, nullptr, nullptr, B, S, nq, nkv, ldq, ldkv, ldo,
+             1.4426950408889634f / sqrtf((float)d), 1.f / sqrtf((float)d)};
+  switch (d) {
+    case 16: return fwd_launch<16>(q, k, v, a, st);
+    case 32: return fwd_launch<32>(q, k, v, a, st);
+    case 64: return fwd_launch<64>(q, k, v, a, st);
+    default: return fwd_launch<128>(q, k, v, a, st);
+  }
+}
+
+int attention_bwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
+                     const float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv, float* work, int B, int S, int nq,
+                     int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st) {
+  if (!tc_ok(B, S, nq, nkv, d, ldq, ldkv, ldo, q, k, v)) return -1;
+  AttnArgs a{nullptr, nullptr, lse, nullptr, dq, dk, dv, B, S, nq, nkv, ldq, ldkv, ldo,
+             1.4426950408889634f / sqrtf((float)d), 1.f / sqrtf((float)d)};
+  switch (d) {
+    case 16: return bwd_launch<16>(q, k, v, o, dout, a, work, st);
+    case 32: return bwd_launch<32>(q, k, v, o, dout, a, work, st);
+    case 64: return bwd_launch<64>(q, k, v, o, dout, a, work, st);
+    default: return bwd_launch<128>(q, k, v, o, dout, a, work, st);
+  }
+}
+
+}  // namespace mt

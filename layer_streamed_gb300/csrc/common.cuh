@@ -85,6 +85,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
 // so that the kernel reaches its exit (and frees its tensor memory) quickly.
 // The limit (~2^33 SM cycles, several seconds) is far beyond any legitimate
 // wait inside one kernel.
+// The device error word doubles as a grid-wide abort signal: once any CTA
+// has timed out, waits everywhere in this translation unit give up at once
+// (until the host clears the word after the step).
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort, uint32_t err_bit) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
@@ -94,6 +97,10 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     if (mbar_try_wait(a, parity)) return true;
     if ((++spins & 255u) == 0) {
       if (*abort) return false;
+      if (*(volatile uint32_t*)&g_device_error) {
+        *abort = 1;
+        return false;
+      }
       if (clock64() - t0 > (1ll << 33)) {
         *abort = 1;
         report_error(err_bit);

@@ -79,6 +79,15 @@ int attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const
 // barriers (0 = no error). Synchronous with respect to the device.
 uint32_t gemm_take_device_error();
 uint32_t attention_take_device_error();
+uint32_t attention_tc_take_device_error();
+
+// Tensor-core flash attention (attention_tc.cu); head_dim in {16,32,64,128},
+// row strides multiples of 8. work: B*S*nq floats (delta).
+int attention_fwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int B, int S,
+                     int nq, int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
+int attention_bwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
+                     const float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv, float* work, int B, int S, int nq,
+                     int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
 
 // fp32 -> bf16 copy of a dense buffer.
 int cast_f32_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st);

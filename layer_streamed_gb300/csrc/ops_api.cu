@@ -49,7 +49,7 @@ int mt_op_rope(void* x, float* table, int B, int S_, int row_stride, int head0, 
 int mt_op_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_, int n_heads,
                         int n_kv_heads, int d, int ldq, int ldkv, int ldo, void* stream) {
   if (!q || !k || !v || !o || !lse) return MT_ERR_ARG;
-  return rc(attention_fwd((const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, (uint16_t*)o, lse, B, S_,
+  return rc(attention_fwd_tc((const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, (uint16_t*)o, lse, B, S_,
                           n_heads, n_kv_heads, d, ldq, ldkv, ldo, S(stream)));
 }
 
@@ -59,7 +59,7 @@ int mt_op_attention_bwd(const void* q, const void* k, const void* v, const void*
                         void* dq, void* dk, void* dv, float* workspace, int B, int S_, int n_heads, int n_kv_heads,
                         int d, int ldq, int ldkv, int ldo, void* stream) {
   if (!q || !k || !v || !o || !do_ || !lse || !dq || !dk || !dv || !workspace) return MT_ERR_ARG;
-  return rc(attention_bwd((const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, (const uint16_t*)o,
+  return rc(attention_bwd_tc((const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, (const uint16_t*)o,
                           (const uint16_t*)do_, lse, (uint16_t*)dq, (uint16_t*)dk, (uint16_t*)dv, workspace, B, S_,
                           n_heads, n_kv_heads, d, ldq, ldkv, ldo, S(stream)));
 }
@@ -112,7 +112,7 @@ int mt_op_lmhead_ce(const void* X, const void* W, const int32_t* labels, float s
 
 int mt_op_device_error(void) {
   cudaDeviceSynchronize();
-  return (int)(gemm_take_device_error() | attention_take_device_error());
+  return (int)(gemm_take_device_error() | attention_take_device_error() | attention_tc_take_device_error());
 }
 
 }  // extern "C"

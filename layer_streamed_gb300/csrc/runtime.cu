@@ -271,6 +271,7 @@ struct mt_ctx {
   mt_stats stats{};
   int trace = 1;
   bool fuse_top = true;
+  bool debug_sync = false;  // MT_DEBUG_SYNC=1: wait for every unit, report progress on stderr
   std::vector<Seg> segs;
   std::vector<OpSeg> opsegs;
   long launches_at_start = 0;
@@ -640,7 +641,7 @@ int layer_forward(Step& st, int l, const LayerView& w) {
   CKL(rope_apply(a.qkv, ctx->rope_tab, st.B, st.S, p.qkv, 0, p.nq + p.nkv, p.d, +1, s));
   {
     OpTimer timer(ctx, 1, attn_flop(st, p));
-    CKL(attention_fwd(a.qkv, a.qkv + p.qd, a.qkv + p.qd + p.kd, a.o, a.lse, st.B, st.S, p.nq, p.nkv, p.d, p.qkv,
+    CKL(attention_fwd_tc(a.qkv, a.qkv + p.qd, a.qkv + p.qd + p.kd, a.o, a.lse, st.B, st.S, p.nq, p.nkv, p.d, p.qkv,
                       p.qkv, p.qd, s));
   }
   CKR(gemm(ctx, GEMM_NT, EPI_F32_ADD, a.o, w.wo, a.hmid, x, T, h, p.qd, p.qd, p.qd, h));
@@ -703,7 +704,7 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   CKR(gemm(ctx, GEMM_NN, EPI_BF16, ctx->dhmid_b, w.wo, ctx->do_b, nullptr, T, p.qd, h, h, p.qd, p.qd));
   {
     OpTimer timer(ctx, 1, 2.5 * attn_flop(st, p));
-    CKL(attention_bwd(a.qkv, a.qkv + p.qd, a.qkv + p.qd + p.kd, a.o, ctx->do_b, a.lse, ctx->dqkv,
+    CKL(attention_bwd_tc(a.qkv, a.qkv + p.qd, a.qkv + p.qd + p.kd, a.o, ctx->do_b, a.lse, ctx->dqkv,
                       ctx->dqkv + p.qd, ctx->dqkv + p.qd + p.kd, ctx->attn_ws, st.B, st.S, p.nq, p.nkv, p.d, p.qkv,
                       p.qkv, p.qd, s));
   }
@@ -714,6 +715,30 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   CKL(rmsnorm_bwd(x, w.w1, a.rstd1, ctx->dm, a.hmid, ctx->dh, ctx->dh_b, GT(0), ctx->norm_ws, T, h, s));
   const size_t bytes = ctx->off_g[l][8] + tensor_numel(ctx->cfg, l, 8) * 4 - u0;
   return grad_slot_end(st, g, u0, bytes);
+}
+
+// Debug aid: wait (bounded) for the compute stream after a unit and report
+// which stream is still busy if it does not finish.
+int debug_wait(mt_ctx* ctx, size_t i, Item it, int slot, int loaded) {
+  const auto t0 = std::chrono::steady_clock::now();
+  while (true) {
+    cudaError_t e = cudaStreamQuery(ctx->s_comp);
+    const double el = std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count();
+    if (e == cudaSuccess) {
+      fprintf(stderr, "[mt] unit %zu kind %d index %d slot %d loaded %d: compute idle after %.3f s\n", i, it.kind,
+              it.index, slot, loaded, el);
+      return MT_OK;
+    }
+    if (e != cudaErrorNotReady) return set_err(ctx, MT_ERR_CUDA, cudaGetErrorString(e));
+    if (el > 60.0) {
+      fprintf(stderr, "[mt] unit %zu kind %d index %d STUCK: compute %s, weight-in %s, grad-out %s\n", i, it.kind,
+              it.index, cudaStreamQuery(ctx->s_comp) == cudaSuccess ? "idle" : "busy",
+              cudaStreamQuery(ctx->s_h2d) == cudaSuccess ? "idle" : "busy",
+              cudaStreamQuery(ctx->s_d2h) == cudaSuccess ? "idle" : "busy");
+      return set_err(ctx, MT_ERR_TIMEOUT, "debug: unit did not finish");
+    }
+    std::this_thread::sleep_for(std::chrono::microseconds(200));
+  }
 }
 
 int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss_out) {
@@ -830,6 +855,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       }
     }
     CK(cudaEventRecord(ctx->ev_wfree[slot], s));
+    if (ctx->debug_sync) CKR(debug_wait(ctx, i, it, slot, st.needs_load[i]));
   }
   // Embedding backward: dense gradient slices from dh_0.
   for (int sl = 0; sl < p.n_embg_slices; ++sl) {
@@ -970,6 +996,8 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
   if (ctx->trace < 0 || ctx->trace > 2) ctx->trace = 1;
   const char* ft = getenv("MT_FUSE_TOP_BLOCK");
   ctx->fuse_top = !(ft && ft[0] == '0');
+  const char* ds = getenv("MT_DEBUG_SYNC");
+  ctx->debug_sync = ds && ds[0] == '1';
   auto fail = [&](int code, const char* m, cudaError_t e) {
     fprintf(stderr, "mt_create: %s: %s\n", m, cudaGetErrorString(e));
     mt_destroy(ctx);
@@ -1082,7 +1110,7 @@ int mt_forward_backward(mt_ctx* ctx, const int32_t* tokens, const int32_t* label
     cudaGetLastError();
     ctx->err = msg;
   } else {
-    const uint32_t derr = gemm_take_device_error() | attention_take_device_error();
+    const uint32_t derr = gemm_take_device_error() | attention_take_device_error() | attention_tc_take_device_error();
     if (derr) {
       char b[96];
       snprintf(b, sizeof b, "device error word 0x%x (barrier timeout inside a kernel)", derr);

@@ -202,6 +202,33 @@ def test_attention_forward_backward(d, S, nq, nkv):
     assert mt.mt_op_device_error() == 0
 
 
+def test_attention_growing_scores_rescale_per_warp():
+    """Rows whose scores keep growing along the keys (so the running maximum
+    jumps in later tiles) interleaved with rows whose scores shrink, over
+    several 128-key tiles: neighbouring rows of one warp need different
+    online-softmax rescaling decisions."""
+    torch, mt = need_gpu()
+    B, S, nq, nkv, d = 1, 640, 2, 1, 128
+    rng = np.random.default_rng(7)
+    u = rng.normal(size=d)
+    u /= np.linalg.norm(u)
+    ramp = np.linspace(0.0, 1.0, S)[:, None]
+    k = (ramp * 6.0 * u[None, :] + 0.3 * rng.normal(size=(S, d))).reshape(B, S, nkv, d)
+    sign = np.where(np.arange(S) % 2 == 0, 1.0, -1.0)[:, None, None]
+    q = (sign * 6.0 * u[None, None, :] + 0.3 * rng.normal(size=(S, nq, d))).reshape(B, S, nq, d)
+    v = rng.normal(size=(B, S, nkv, d))
+    Q, q32 = to_dev_bf16(torch, q)
+    Kd, k32 = to_dev_bf16(torch, k)
+    Vd, v32 = to_dev_bf16(torch, v)
+    O = torch.empty((B, S, nq, d), dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((B, nq, S), device="cuda")
+    mt.mt_op_attention_fwd(Q, Kd, Vd, O, LSE, B, S, nq, nkv, d, nq * d, nkv * d, nq * d)
+    o_ref, lse_ref, *_ = oracle.attention(q32, k32, v32)
+    assert mt.mt_op_device_error() == 0
+    assert rel_l2(from_dev(O), o_ref) < 1.5e-2
+    assert np.max(np.abs(from_dev(LSE) - lse_ref)) < 2e-3 * np.max(np.abs(lse_ref))
+
+
 def test_lmhead_cross_entropy():
     torch, mt = need_gpu()
     T, V, h = 96, 1000, 128
