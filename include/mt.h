@@ -138,9 +138,11 @@ typedef struct {
   double d2h_hidden_frac;
   int32_t n_h2d, n_d2h, n_units;
   int32_t timing_enabled;  /* 0: MT_TRACE=0 (no events); 1: per-unit events; 2: also per-kernel events */
-  /* With MT_TRACE=2: summed device time and algorithmic work of the GEMM
-   * launches (2*M*N*K flop each) and of the attention launches (causal
-   * lower-triangle flop), timed with CUDA events on the compute stream. */
+  /* With MT_TRACE=2: summed device time and algorithmic work of a sample of
+   * the GEMM launches (2*M*N*K flop each) and of the attention launches
+   * (causal lower-triangle flop), one launch in MT_TRACE_SAMPLE (default 16)
+   * bracketed with CUDA events on the compute stream; n_gemm/n_attn count the
+   * sampled launches. */
   double gemm_ms, gemm_flop, attn_ms, attn_flop;
   int32_t n_gemm, n_attn;
   int32_t n_launches;      /* kernels launched by this step (all trace levels) */

@@ -233,6 +233,7 @@ struct Seg {
   int stream;  // 0 compute, 1 h2d, 2 d2h
   cudaEvent_t a, b;
   double bytes;
+  int unit;    // position in the step's unit sequence (-1: none)
 };
 // Per-kernel timing (trace level 2): category 0 GEMM, 1 attention.
 struct OpSeg {
@@ -272,9 +273,13 @@ struct mt_ctx {
   int trace = 1;
   bool fuse_top = true;
   bool debug_sync = false;  // MT_DEBUG_SYNC=1: wait for every unit, report progress on stderr
+  bool serial = false;      // MT_SERIAL=1: no copy/compute overlap (ablation)
+  std::string timeline;     // MT_TIMELINE=path: write the step's segments as CSV
   std::vector<Seg> segs;
   std::vector<OpSeg> opsegs;
   long launches_at_start = 0;
+  int trace_sample = 16;    // MT_TRACE_SAMPLE: time 1 in N GEMM/attention launches at trace level 2
+  long op_counter = 0;
   std::vector<cudaEvent_t> ev_pool;
   size_t ev_used = 0;
   cudaEvent_t ev_base = nullptr;
@@ -382,12 +387,12 @@ struct SegScope {
   mt_ctx* ctx;
   int idx = -1;
   cudaStream_t st;
-  SegScope(mt_ctx* c, int stream_id, cudaStream_t s, double bytes) : ctx(c), st(s) {
+  SegScope(mt_ctx* c, int stream_id, cudaStream_t s, double bytes, int unit = -1) : ctx(c), st(s) {
     if (!c->trace) return;
     cudaEvent_t a = next_event(c), b = next_event(c);
     if (!a || !b) return;
     cudaEventRecord(a, s);
-    c->segs.push_back(Seg{stream_id, a, b, bytes});
+    c->segs.push_back(Seg{stream_id, a, b, bytes, unit});
     idx = (int)c->segs.size() - 1;
   }
   ~SegScope() {
@@ -432,7 +437,9 @@ struct OpTimer {
   mt_ctx* ctx;
   int idx = -1;
   OpTimer(mt_ctx* c, int cat, double flop) : ctx(c) {
-    if (c->trace < 2) return;
+    // Events around every launch would serialise the stream far more than
+    // they measure, so only one launch in trace_sample is bracketed.
+    if (c->trace < 2 || (c->op_counter++ % c->trace_sample) != 0) return;
     cudaEvent_t a = next_event(c), b = next_event(c);
     if (!a || !b) return;
     cudaEventRecord(a, c->s_comp);
@@ -543,8 +550,9 @@ int issue_load(Step& st, size_t i) {
   if (ctx->fault_kind == 1 && ++ctx->fault_count == ctx->fault_nth)
     return set_err(ctx, MT_ERR_CUDA, "injected copy-issue failure");
   CK(cudaStreamWaitEvent(ctx->s_h2d, ctx->ev_wfree[slot], 0));
+  if (ctx->serial && i > 0) CK(cudaStreamWaitEvent(ctx->s_h2d, ctx->ev_wfree[st.slot_of[i - 1]], 0));
   {
-    SegScope sg(ctx, 1, ctx->s_h2d, (double)bytes);
+    SegScope sg(ctx, 1, ctx->s_h2d, (double)bytes, (int)i);
     CK(cudaMemcpyAsync(ctx->wbuf[slot], hp + src_off, bytes, cudaMemcpyHostToDevice, ctx->s_h2d));
   }
   CK(cudaEventRecord(ctx->ev_wready[slot], ctx->s_h2d));
@@ -669,6 +677,7 @@ int grad_slot_end(Step& st, int g, size_t host_off, size_t bytes) {
     CK(cudaMemcpyAsync((uint8_t*)st.host_grad + host_off, ctx->gbuf[g], bytes, cudaMemcpyDeviceToHost, ctx->s_d2h));
   }
   CK(cudaEventRecord(ctx->ev_gfree[g], ctx->s_d2h));
+  if (ctx->serial) CK(cudaStreamWaitEvent(ctx->s_comp, ctx->ev_gfree[g], 0));
   ctx->stats.d2h_bytes += (double)bytes;
   ctx->stats.n_d2h += 1;
   return MT_OK;
@@ -801,13 +810,15 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   int head_pass2_count = 0;
   bool first_dxf = true;
   for (size_t i = 0; i < n; ++i) {
-    if (i + 1 < n && st.needs_load[i + 1]) CKR(issue_load(st, i + 1));
+    // Ping-pong: the copy of the next unit is issued before this unit's
+    // compute (it overlaps it); in the serial ablation it waits for it.
+    if (!ctx->serial && i + 1 < n && st.needs_load[i + 1]) CKR(issue_load(st, i + 1));
     const Item it = st.seq[i];
     const int slot = st.slot_of[i];
     const bool fresh = st.needs_load[i];
     if (fresh) CK(cudaStreamWaitEvent(s, ctx->ev_wready[slot], 0));
     {
-      SegScope sg(ctx, 0, s, 0);
+      SegScope sg(ctx, 0, s, 0, (int)i);
       if (it.kind == IT_EMB) {
         const int r0 = it.index * p.emb_rows, rows = std::min(p.emb_rows, p.V - r0);
         CKL(embed_gather(ctx->wbuf[slot], p.esz == 2, r0, rows, ctx->tok_d, ckpt(ctx, 0), T, h, s));
@@ -855,6 +866,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       }
     }
     CK(cudaEventRecord(ctx->ev_wfree[slot], s));
+    if (ctx->serial && i + 1 < n && st.needs_load[i + 1]) CKR(issue_load(st, i + 1));
     if (ctx->debug_sync) CKR(debug_wait(ctx, i, it, slot, st.needs_load[i]));
   }
   // Embedding backward: dense gradient slices from dh_0.
@@ -863,7 +875,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
     int g;
     CKR(grad_slot_begin(st, &g));
     {
-      SegScope sg(ctx, 0, s, 0);
+      SegScope sg(ctx, 0, s, 0, (int)n + sl);
       CKL(embed_scatter(ctx->perm_d, ctx->start_d, r0, rows, ctx->dh, ctx->gbuf[g], h, s));
     }
     CKR(grad_slot_end(st, g, ctx->off_g[0][0] + (size_t)r0 * h * 4, (size_t)rows * h * 4));
@@ -912,6 +924,20 @@ void compute_stats(mt_ctx* ctx) {
     if (sg.stream == 0) comp.push_back(v);
     else if (sg.stream == 1) h2d.push_back(v);
     else d2h.push_back(v);
+  }
+  if (!ctx->timeline.empty()) {
+    FILE* f = fopen(ctx->timeline.c_str(), "w");
+    if (f) {
+      fprintf(f, "stream,unit,start_ms,end_ms,bytes\n");
+      for (auto& sg : ctx->segs) {
+        float ta = 0, tb = 0;
+        if (cudaEventElapsedTime(&ta, ctx->ev_base, sg.a) != cudaSuccess) continue;
+        if (cudaEventElapsedTime(&tb, ctx->ev_base, sg.b) != cudaSuccess) continue;
+        fprintf(f, "%s,%d,%.4f,%.4f,%.0f\n", sg.stream == 0 ? "compute" : sg.stream == 1 ? "h2d" : "d2h", sg.unit, ta,
+                tb, sg.bytes);
+      }
+      fclose(f);
+    }
   }
   std::sort(comp.begin(), comp.end(), [](const Iv& x, const Iv& y) { return x.a < y.a; });
   std::vector<Iv> uni;
@@ -998,6 +1024,12 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
   ctx->fuse_top = !(ft && ft[0] == '0');
   const char* ds = getenv("MT_DEBUG_SYNC");
   ctx->debug_sync = ds && ds[0] == '1';
+  const char* ts = getenv("MT_TRACE_SAMPLE");
+  if (ts && atoi(ts) > 0) ctx->trace_sample = atoi(ts);
+  const char* se = getenv("MT_SERIAL");
+  ctx->serial = se && se[0] == '1';
+  const char* tl = getenv("MT_TIMELINE");
+  if (tl) ctx->timeline = tl;
   auto fail = [&](int code, const char* m, cudaError_t e) {
     fprintf(stderr, "mt_create: %s: %s\n", m, cudaGetErrorString(e));
     mt_destroy(ctx);
