@@ -209,6 +209,27 @@ size_t mt_op_rmsnorm_bwd_workspace(int T, int h);
 int mt_op_rmsnorm_bwd(const float* x, const float* w, const float* rstd, const float* dy, const float* resid,
                       float* dx, void* dx_bf16, float* dw, float* workspace, int T, int h, void* stream);
 
+/* Allocation-free variant of mt_op_rmsnorm_bwd (same arguments and results,
+ * minus the workspace). The paper has no counterpart: this entry point serves
+ * callers that cannot allocate device memory where they call us, for example
+ * code whose device memory is owned by another component's allocator, or
+ * code that must not risk the implicit device synchronisation that
+ * cudaMalloc/cudaFree can cause. Instead of a caller buffer it uses a
+ * fixed 4 MiB array (1,048,576 floats) compiled into the library, which
+ * every GPU that loads libmt.so holds until the process exits.
+ *  - Limit: ceil(T/32) * h must be <= 1,048,576 (e.g. T = 8192 tokens at
+ *    h = 4096); larger sizes return MT_ERR_BUDGET before anything runs.
+ *  - The first call on each device looks up the array's device address
+ *    (cudaGetSymbolAddress, with that device current); make that first call
+ *    before any stream capture begins.
+ *  - All calls share the one array and it keeps the last call's contents:
+ *    calls whose executions overlap on the GPU (e.g. on two streams without
+ *    ordering between them) race on it and give wrong results. The
+ *    array needs no clearing: each call writes every entry it reads.
+ *  - It calls no cudaMalloc, cudaFree or other allocating routine. */
+int mt_op_rmsnorm_bwd_noalloc(const float* x, const float* w, const float* rstd, const float* dy, const float* resid,
+                              float* dx, void* dx_bf16, float* dw, int T, int h, void* stream);
+
 /* RoPE in place on bf16 x laid out [B*S, row_stride] where heads
  * [head0, head0 + n_heads) of width d start at column head0*d; dir +1
  * rotates by +pos*theta^(-2i/d) on the half-split pairs (i, i+d/2), -1 by the

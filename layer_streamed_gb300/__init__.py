@@ -39,7 +39,8 @@ STATUS_NAMES = {0: "MT_OK", -1: "MT_ERR_ARG", -2: "MT_ERR_BUDGET", -3: "MT_ERR_N
 EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_create", "mt_create_ex",
            "mt_bind_host_params", "mt_forward_backward", "mt_get_stats", "mt_get_memory_plan", "mt_last_error",
            "mt_destroy", "mt_host_alloc", "mt_host_free", "mt_debug_inject_fault", "mt_op_gemm",
-           "mt_op_rmsnorm_fwd", "mt_op_rmsnorm_bwd_workspace", "mt_op_rmsnorm_bwd", "mt_op_rope",
+           "mt_op_rmsnorm_fwd", "mt_op_rmsnorm_bwd_workspace", "mt_op_rmsnorm_bwd", "mt_op_rmsnorm_bwd_noalloc",
+           "mt_op_rope",
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
            "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error")
 
@@ -113,6 +114,7 @@ def lib() -> ctypes.CDLL:
         "mt_op_rmsnorm_fwd": (i32, [vp, vp, vp, vp, i32, i32, f32, vp]),
         "mt_op_rmsnorm_bwd_workspace": (sz, [i32, i32]),
         "mt_op_rmsnorm_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp]),
+        "mt_op_rmsnorm_bwd_noalloc": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp]),
         "mt_op_rope": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]),
         "mt_op_attention_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp]),
         "mt_op_attention_bwd_workspace": (sz, [i32, i32, i32]),
@@ -352,6 +354,14 @@ def mt_op_rmsnorm_bwd_workspace(T, h) -> int:
 def mt_op_rmsnorm_bwd(x, w, rstd, dy, resid, dx, dx_bf16, dw, workspace, T, h, stream=None):
     _check(lib().mt_op_rmsnorm_bwd(_ptr(x), _ptr(w), _ptr(rstd), _ptr(dy), _ptr(resid), _ptr(dx), _ptr(dx_bf16),
                                    _ptr(dw), _ptr(workspace), T, h, _stream(stream)))
+
+
+def mt_op_rmsnorm_bwd_noalloc(x, w, rstd, dy, resid, dx, dx_bf16, dw, T, h, stream=None):
+    """RMSNorm backward without a workspace argument: for callers that cannot
+    allocate device memory at the call site (see include/mt.h for the limit
+    and the sharing rules of its fixed scratch array)."""
+    _check(lib().mt_op_rmsnorm_bwd_noalloc(_ptr(x), _ptr(w), _ptr(rstd), _ptr(dy), _ptr(resid), _ptr(dx),
+                                           _ptr(dx_bf16), _ptr(dw), T, h, _stream(stream)))
 
 
 def mt_op_rope(x, table, B, S, row_stride, head0, n_heads, d, theta, direction, stream=None):

@@ -5,6 +5,8 @@
 // All global accesses are 128-bit and coalesced where the shapes allow;
 // reductions are warp shuffles plus a fixed-order cross-warp step, so every
 // result is bitwise reproducible run to run.
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -538,6 +540,49 @@ int ce_slice_grad(const float* logits, int T, int R, int ld, int row0, const int
   ce_grad_kernel<<<blocks_for((size_t)T * R, 256), 256, 0, st>>>(logits, T, R, ld, row0, labels, lse, scale, dz);
   count_launches(1);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+// ---------------------------------------------------------------------------
+// Allocation-free RMSNorm backward. Its scratch (the per-block partial sums
+// of the gain gradient) lives in a fixed array in this library's device
+// image instead of a caller buffer. Every GPU that loads the library keeps
+// the array (4 MiB) until the process exits. Host code cannot use the
+// array's name as a device address, so the address is looked up once per
+// device with cudaGetSymbolAddress (on the first call on that device, with
+// that device current) and cached.
+// ---------------------------------------------------------------------------
+namespace {
+constexpr size_t kNoAllocPartials = (size_t)1 << 20;  // floats: ceil(T/32) * h must not exceed this
+__device__ __align__(256) float g_norm_bwd_scratch[kNoAllocPartials];
+
+constexpr int kMaxDevices = 64;
+float* g_scratch_ptr[kMaxDevices] = {};
+std::mutex g_scratch_mu;
+
+int scratch_for_current_device(float** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_norm_bwd_scratch) != cudaSuccess || !p) return -1;
+    g_scratch_ptr[dev] = (float*)p;
+  }
+  *out = g_scratch_ptr[dev];
+  return 0;
+}
+}  // namespace
+
+size_t rmsnorm_bwd_noalloc_capacity() { return kNoAllocPartials; }
+
+int rmsnorm_bwd_noalloc(const float* x, const float* w, const float* rstd, const float* dy, const float* resid,
+                        float* dx, uint16_t* dx_bf16, float* dw, int T, int h, cudaStream_t st) {
+  if (T <= 0 || h <= 0 || rmsnorm_bwd_partials(T, h) > kNoAllocPartials) return -2;
+  float* scratch = nullptr;
+  if (scratch_for_current_device(&scratch)) return -1;
+  // Every partial that the reduction reads is written earlier in the same
+  // launch sequence, so the array needs no clearing between calls.
+  return rmsnorm_bwd(x, w, rstd, dy, resid, dx, dx_bf16, dw, scratch, T, h, st);
 }
 
 }  // namespace mt

@@ -34,6 +34,13 @@ size_t rmsnorm_bwd_partials(int T, int h);  // floats of workspace
 int rmsnorm_bwd(const float* x, const float* w, const float* rstd, const float* dy, const float* resid, float* dx,
                 uint16_t* dx_bf16, float* dw, float* work, int T, int h, cudaStream_t st);
 
+// The same backward with its partial sums in a fixed device array of the
+// library (no allocation, no workspace argument). Returns -2 when
+// ceil(T/32) * h exceeds rmsnorm_bwd_noalloc_capacity() floats.
+size_t rmsnorm_bwd_noalloc_capacity();
+int rmsnorm_bwd_noalloc(const float* x, const float* w, const float* rstd, const float* dy, const float* resid,
+                        float* dx, uint16_t* dx_bf16, float* dw, int T, int h, cudaStream_t st);
+
 // RoPE table [S, d/2] of (cos, sin) and in-place rotation of bf16 heads.
 int rope_table(float2* tab, int S, int d, float theta, cudaStream_t st);
 int rope_apply(uint16_t* x, const float2* tab, int B, int S, int row_stride, int head0, int n_heads, int d, int dir,

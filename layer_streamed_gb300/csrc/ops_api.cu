@@ -38,6 +38,15 @@ int mt_op_rmsnorm_bwd(const float* x, const float* w, const float* rstd, const f
   return rc(rmsnorm_bwd(x, w, rstd, dy, resid, dx, (uint16_t*)dx_bf16, dw, workspace, T, h, S(stream)));
 }
 
+int mt_op_rmsnorm_bwd_noalloc(const float* x, const float* w, const float* rstd, const float* dy, const float* resid,
+                              float* dx, void* dx_bf16, float* dw, int T, int h, void* stream) {
+  if (!x || !w || !rstd || !dy || !dx || !dw) return MT_ERR_ARG;
+  const int r = rmsnorm_bwd_noalloc(x, w, rstd, dy, resid, dx, (uint16_t*)dx_bf16, dw, T, h, S(stream));
+  if (r == -2) return MT_ERR_BUDGET;
+  if (r != 0) return cudaPeekAtLastError() != cudaSuccess ? MT_ERR_CUDA : MT_ERR_ARG;
+  return MT_OK;
+}
+
 int mt_op_rope(void* x, float* table, int B, int S_, int row_stride, int head0, int n_heads, int d, float theta,
                int dir, void* stream) {
   if (!x || !table || B < 1 || S_ < 1 || d < 8 || (dir != 1 && dir != -1)) return MT_ERR_ARG;
