@@ -150,6 +150,13 @@ typedef struct {
 } mt_stats;
 int mt_get_stats(const mt_ctx* ctx, mt_stats* out);
 
+/* Tracing of the following mt_forward_backward calls: level 0 none, 1
+ * per-unit and per-copy events (overlap statistics; the default, also set
+ * by env MT_TRACE), 2 additionally one GEMM/attention launch in `sample`
+ * bracketed by events (kernel durations; this perturbs the step's own
+ * timing, so measure step time at level 1). sample >= 1. */
+int mt_set_tracing(mt_ctx* ctx, int level, int sample);
+
 /* Arena partition of a context (bytes). */
 typedef struct {
   size_t total, weight_buffers, grad_buffers, checkpoints, block_activations, workspace;

@@ -37,7 +37,8 @@ STATUS_NAMES = {0: "MT_OK", -1: "MT_ERR_ARG", -2: "MT_ERR_BUDGET", -3: "MT_ERR_N
 
 # Every symbol include/mt.h declares.
 EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_create", "mt_create_ex",
-           "mt_bind_host_params", "mt_forward_backward", "mt_get_stats", "mt_get_memory_plan", "mt_last_error",
+           "mt_bind_host_params", "mt_forward_backward", "mt_get_stats", "mt_set_tracing", "mt_get_memory_plan",
+           "mt_last_error",
            "mt_destroy", "mt_host_alloc", "mt_host_free", "mt_debug_inject_fault", "mt_op_gemm",
            "mt_op_rmsnorm_fwd", "mt_op_rmsnorm_bwd_workspace", "mt_op_rmsnorm_bwd", "mt_op_rmsnorm_bwd_noalloc",
            "mt_op_rope",
@@ -104,6 +105,7 @@ def lib() -> ctypes.CDLL:
         "mt_bind_host_params": (i32, [vp, vp, i32]),
         "mt_forward_backward": (i32, [vp, vp, vp, i32, i32, i32, vp, P(f32)]),
         "mt_get_stats": (i32, [vp, P(mt_stats)]),
+        "mt_set_tracing": (i32, [vp, i32, i32]),
         "mt_get_memory_plan": (i32, [vp, P(mt_memory_plan)]),
         "mt_last_error": (ctypes.c_char_p, [vp]),
         "mt_destroy": (None, [vp]),
@@ -199,6 +201,10 @@ def mt_get_stats(ctx) -> dict:
     s = mt_stats()
     _check(lib().mt_get_stats(ctx, ctypes.byref(s)), ctx)
     return {f: getattr(s, f) for f, _ in mt_stats._fields_}
+
+
+def mt_set_tracing(ctx, level: int, sample: int = 16) -> None:
+    _check(lib().mt_set_tracing(ctx, level, sample), ctx)
 
 
 def mt_get_memory_plan(ctx) -> dict:
@@ -301,6 +307,9 @@ class Session:
 
     def stats(self) -> dict:
         return mt_get_stats(self.ctx)
+
+    def set_tracing(self, level: int, sample: int = 16) -> None:
+        mt_set_tracing(self.ctx, level, sample)
 
     def memory_plan(self) -> dict:
         return mt_get_memory_plan(self.ctx)

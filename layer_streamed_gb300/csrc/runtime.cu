@@ -1165,6 +1165,14 @@ int mt_get_stats(const mt_ctx* ctx, mt_stats* out) {
   return MT_OK;
 }
 
+int mt_set_tracing(mt_ctx* ctx, int level, int sample) {
+  if (!ctx || level < 0 || level > 2 || sample < 1) return MT_ERR_ARG;
+  ctx->trace = level;
+  ctx->trace_sample = sample;
+  ctx->op_counter = 0;
+  return MT_OK;
+}
+
 int mt_get_memory_plan(const mt_ctx* ctx, mt_memory_plan* out) {
   if (!ctx || !out) return MT_ERR_ARG;
   const Plan& p = ctx->P;

@@ -1,0 +1,98 @@
+"""Kernel benchmark CLI: time one layer-template kernel at a given shape.
+
+  python -m layer_streamed_gb300.kbench gemm --mode nt --M 8192 --N 28672 --K 4096 [--reps 20]
+  python -m layer_streamed_gb300.kbench attn --B 2 --S 4096 --heads 32 --kv-heads 8 --head-dim 128 [--bwd]
+
+Inputs are random bf16 tensors on the current GPU (larger than L2 at the 8B
+shapes); each launch is timed with CUDA events on the launching stream after
+warm-up. Prints one JSON line with the per-launch time and TFLOP/s.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+
+import torch
+
+import layer_streamed_gb300 as mt
+
+
+def _time(fn, reps: int, warmup: int = 3) -> float:
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        fn()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def bench_gemm(args) -> dict:
+    M, N, K = args.M, args.N, args.K
+    mode = {"nt": mt.MT_GEMM_NT, "nn": mt.MT_GEMM_NN, "tn": mt.MT_GEMM_TN}[args.mode]
+    a_shape = (M, K) if args.mode in ("nt", "nn") else (K, M)
+    b_shape = (N, K) if args.mode == "nt" else (K, N)
+    A = torch.randn(a_shape, device="cuda").to(torch.bfloat16)
+    B = (torch.randn(b_shape, device="cuda") * 0.02).to(torch.bfloat16)
+    epi = {"bf16": mt.MT_EPI_BF16, "f32": mt.MT_EPI_F32}[args.out]
+    C = torch.empty((M, N), device="cuda", dtype=torch.bfloat16 if args.out == "bf16" else torch.float32)
+    ms = _time(lambda: mt.mt_op_gemm(mode, epi, A, B, C, None, M, N, K, a_shape[1], b_shape[1], N), args.reps)
+    flop = 2.0 * M * N * K
+    return {"kernel": "gemm", "mode": args.mode, "M": M, "N": N, "K": K, "out": args.out, "ms": ms,
+            "tflops": flop / ms / 1e9}
+
+
+def bench_attn(args) -> dict:
+    B, S, nq, nkv, d = args.B, args.S, args.heads, args.kv_heads, args.head_dim
+    T, qd, kd = B * S, nq * d, nkv * d
+    ld = qd + 2 * kd
+    qkv = torch.randn((T, ld), device="cuda").to(torch.bfloat16)
+    o = torch.empty((T, qd), device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty(B * nq * S, device="cuda")
+    fwd = lambda: mt.mt_op_attention_fwd(qkv, qkv[:, qd:], qkv[:, qd + kd:], o, lse, B, S, nq, nkv, d, ld, ld, qd)
+    flop = 2.0 * B * nq * d * S * (S + 1)  # causal Q K^T and P V
+    if not args.bwd:
+        ms = _time(fwd, args.reps)
+        return {"kernel": "attention_fwd", "B": B, "S": S, "heads": nq, "kv_heads": nkv, "head_dim": d, "ms": ms,
+                "tflops": flop / ms / 1e9}
+    fwd()
+    do = torch.randn((T, qd), device="cuda").to(torch.bfloat16)
+    dqkv = torch.empty_like(qkv)
+    ws = torch.empty(mt.mt_op_attention_bwd_workspace(B, S, nq), device="cuda")
+    bwd = lambda: mt.mt_op_attention_bwd(qkv, qkv[:, qd:], qkv[:, qd + kd:], o, do, lse, dqkv, dqkv[:, qd:],
+                                         dqkv[:, qd + kd:], ws, B, S, nq, nkv, d, ld, ld, qd)
+    ms = _time(bwd, args.reps)
+    return {"kernel": "attention_bwd", "B": B, "S": S, "heads": nq, "kv_heads": nkv, "head_dim": d, "ms": ms,
+            "tflops": 2.5 * flop / ms / 1e9}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    sub = ap.add_subparsers(dest="op", required=True)
+    g = sub.add_parser("gemm")
+    g.add_argument("--mode", default="nt", choices=["nt", "nn", "tn"])
+    g.add_argument("--M", type=int, default=8192)
+    g.add_argument("--N", type=int, default=28672)
+    g.add_argument("--K", type=int, default=4096)
+    g.add_argument("--out", default="bf16", choices=["bf16", "f32"])
+    g.add_argument("--reps", type=int, default=20)
+    a = sub.add_parser("attn")
+    a.add_argument("--B", type=int, default=2)
+    a.add_argument("--S", type=int, default=4096)
+    a.add_argument("--heads", type=int, default=32)
+    a.add_argument("--kv-heads", type=int, default=8)
+    a.add_argument("--head-dim", type=int, default=128)
+    a.add_argument("--bwd", action="store_true")
+    a.add_argument("--reps", type=int, default=20)
+    args = ap.parse_args()
+    mt.build()
+    res = bench_gemm(args) if args.op == "gemm" else bench_attn(args)
+    res["device_error"] = mt.mt_op_device_error()
+    print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()
