@@ -121,21 +121,35 @@ constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
 
 // ===========================================================================
-// Forward
+// Forward. CTA = two consecutive 128-row query tiles (A = 2m, B = 2m+1) of
+// one query head and sequence; 12 warps: warp 0 TMA, warp 1 MMA issue,
+// warps 4-7 softmax of tile A, warps 8-11 softmax of tile B (warps 2-3 idle).
+// The MMA thread alternates between the tiles (PV_A(t), S_A(t+1), PV_B(t),
+// S_B(t+1)), so each softmax warpgroup works while the tensor core serves
+// the other tile. TMEM: S_A +0, S_B +128, O_A +256, O_B +384.
+// Shared: Q_A, Q_B, K (two stages), V (one stage), P_A, P_B.
 // ===========================================================================
 template <int D>
 struct FwdSmem {
-  static constexpr int Q = 0;
-  static constexpr int K0 = Q + tile_bytes<D>();
-  static constexpr int V0 = K0 + 2 * tile_bytes<D>();
-  static constexpr int P = V0 + 2 * tile_bytes<D>();
-  static constexpr int BAR = P + 2 * BOX;
+  static constexpr int QA = 0;
+  static constexpr int QB = QA + tile_bytes<D>();
+  static constexpr int K0 = QB + tile_bytes<D>();
+  static constexpr int V = K0 + 2 * tile_bytes<D>();
+  static constexpr int PA = V + tile_bytes<D>();
+  static constexpr int PB = PA + 2 * BOX;
+  static constexpr int BAR = PB + 2 * BOX;
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;  // one CTA per SM
 };
 
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, AttnArgs a) {
   using L = FwdSmem<D>;
@@ -143,32 +157,35 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [2]
-  uint64_t* kv_empty = bars + 3;  // [2]
-  uint64_t* s_full = bars + 5;    // [2]
-  uint64_t* s_empty = bars + 7;   // [2]
-  uint64_t* p_full = bars + 9;
-  uint64_t* o_done = bars + 10;
-  uint32_t* tmem_slot = (uint32_t*)(bars + 11);
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;
+  uint64_t* v_empty = bars + 6;
+  uint64_t* s_full = bars + 7;   // [2]: tile A, tile B
+  uint64_t* p_full = bars + 9;   // [2]
+  uint64_t* o_done = bars + 11;  // [2]
+  uint32_t* tmem_slot = (uint32_t*)(bars + 13);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int nqt = (a.S + TILE - 1) / TILE;
-  const int qt = nqt - 1 - (int)blockIdx.x;  // longest tiles first
+  const int npairs = (nqt + 1) / 2;
+  const int m = npairs - 1 - (int)blockIdx.x;  // longest pairs first
   const int j = blockIdx.y, b = blockIdx.z;
   const int g = j / (a.nq / a.nkv);
-  const int ntiles = qt + 1;
+  const int tA = 2 * m + 1, tB = 2 * m + 2;  // KV tiles seen by tile A / tile B
   const uint32_t warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
+    mbar_init(v_full, 1);
+    mbar_init(v_empty, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -179,21 +196,24 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *tmem_slot;  // S0: +0, S1: +128, O: +256
+  const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
     if (lane == 0) {
       prefetch_tmap(&tq);
       prefetch_tmap(&tk);
       prefetch_tmap(&tv);
-      mbar_arrive_expect_tx(q_full, tile_bytes<D>());
-      load_head_tile<D>(sm + L::Q, &tq, q_full, j, qt * TILE, b);
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t & 1;
-        mbar_wait(&kv_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(&kv_full[st], 2 * tile_bytes<D>());
-        load_head_tile<D>(sm + L::K0 + st * tile_bytes<D>(), &tk, &kv_full[st], g, t * TILE, b);
-        load_head_tile<D>(sm + L::V0 + st * tile_bytes<D>(), &tv, &kv_full[st], g, t * TILE, b);
+      mbar_arrive_expect_tx(q_full, 2 * tile_bytes<D>());
+      load_head_tile<D>(sm + L::QA, &tq, q_full, j, (2 * m) * TILE, b);
+      load_head_tile<D>(sm + L::QB, &tq, q_full, j, (2 * m + 1) * TILE, b);
+      for (int t = 0; t < tB; ++t) {
+        const int ks = t & 1;
+        mbar_wait(&k_empty[ks], ((t >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&k_full[ks], tile_bytes<D>());
+        load_head_tile<D>(sm + L::K0 + ks * tile_bytes<D>(), &tk, &k_full[ks], g, t * TILE, b);
+        mbar_wait(v_empty, (t & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(v_full, tile_bytes<D>());
+        load_head_tile<D>(sm + L::V, &tv, v_full, g, t * TILE, b);
       }
     }
     __syncwarp();
@@ -201,66 +221,103 @@ __global__ void __launch_bounds__(192, 1)
     if (lane == 0) {
       constexpr uint32_t IDESC_S = make_idesc(128, 128, false, false);
       constexpr uint32_t IDESC_O = make_idesc(128, D < 64 ? 64 : D, false, true);  // padded head dims read zeros
-      constexpr int KS = D / 16;  // K steps of Q K^T (zero-padded columns skipped)
-      mbar_wait(q_full, 0, abort_flag, kErrTimeoutAttn);
-      auto issue_pv = [&](int t) {
-        const int st = t & 1;
-        mbar_wait(p_full, t & 1, abort_flag, kErrTimeoutAttn);
-        tc_fence_after();
-        const uint8_t* vt = sm + L::V0 + st * tile_bytes<D>();
-#pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk)
-          tc_mma(tmem + 256, kmaj_desc(sm + L::P, kk), mnmaj_desc(vt, kk), IDESC_O, (t > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(o_done);
-        tc_commit(&kv_empty[st]);
-      };
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t & 1;
-        mbar_wait(&kv_full[st], (t >> 1) & 1, abort_flag, kErrTimeoutAttn);
-        mbar_wait(&s_empty[st], ((t >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        tc_fence_after();
-        const uint8_t* kt = sm + L::K0 + st * tile_bytes<D>();
+      constexpr int KS = D / 16;
+      auto issue_s = [&](int side, int t) {  // S_side(t) = Q_side K_t^T
+        const uint8_t* q = sm + (side ? L::QB : L::QA);
+        const uint8_t* kt = sm + L::K0 + (t & 1) * tile_bytes<D>();
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk)
-          tc_mma(tmem + st * 128, kmaj_desc(sm + L::Q, kk), kmaj_desc(kt, kk), IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(&s_full[st]);
-        if (t > 0) issue_pv(t - 1);
+          tc_mma(tmem + side * 128, kmaj_desc(q, kk), kmaj_desc(kt, kk), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(&s_full[side]);
+      };
+      auto issue_pv = [&](int side, int t) {  // O_side += P_side(t) V_t
+        const uint8_t* pt = sm + (side ? L::PB : L::PA);
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)
+          tc_mma(tmem + 256 + side * 128, kmaj_desc(pt, kk), mnmaj_desc(sm + L::V, kk), IDESC_O,
+                 (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&o_done[side]);
+      };
+      mbar_wait(q_full, 0, abort_flag, kErrTimeoutAttn);
+      mbar_wait(&k_full[0], 0, abort_flag, kErrTimeoutAttn);
+      tc_fence_after();
+      issue_s(0, 0);
+      issue_s(1, 0);
+      tc_commit(&k_empty[0]);
+      for (int t = 0; t < tB; ++t) {
+        const bool next = t + 1 < tB;
+        mbar_wait(v_full, t & 1, abort_flag, kErrTimeoutAttn);
+        if (t < tA) {
+          mbar_wait(&p_full[0], t & 1, abort_flag, kErrTimeoutAttn);
+          tc_fence_after();
+          issue_pv(0, t);
+          if (t + 1 < tA) {
+            mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
+            tc_fence_after();
+            issue_s(0, t + 1);
+          }
+        }
+        mbar_wait(&p_full[1], t & 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+        issue_pv(1, t);
+        tc_commit(v_empty);
+        if (next) {
+          mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
+          tc_fence_after();
+          issue_s(1, t + 1);
+          tc_commit(&k_empty[(t + 1) & 1]);
+        }
       }
-      issue_pv(ntiles - 1);
     }
     __syncwarp();
-  } else {
-    // softmax / epilogue: thread owns query row r of the tile
+  } else if (warp >= 4) {
+    // softmax / epilogue of one tile: thread owns query row r
+    const int side = warp >= 8 ? 1 : 0;
+    const int nt = side ? tB : tA;
     const uint32_t q4 = warp & 3;
     const int r = q4 * 32 + lane;
-    const int trow = qt * TILE + r;  // position in the sequence
+    const int trow = (2 * m + side) * TILE + r;  // position in the sequence
     const uint32_t lane_base = (q4 * 32) << 16;
+    const uint32_t s_col = tmem + lane_base + side * 128;
+    const uint32_t o_col = tmem + lane_base + 256 + side * 128;
+    uint8_t* ptile = sm + (side ? L::PB : L::PA);
     float m_ref = -INFINITY, l = 0.f;
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t & 1;
-      mbar_wait(&s_full[st], (t >> 1) & 1, abort_flag, kErrTimeoutAttn);
+    for (int t = 0; t < nt; ++t) {
+      mbar_wait(&s_full[side], t & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
-      const int kv0 = t * TILE;
-      const bool diag = (t == qt);
-      const bool tail = kv0 + TILE > a.S;
-      // pass 1: row maximum
-      float mx = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
+      float sv[128];
+      {
+        uint32_t v0[32], v1[32], v2[32], v3[32];
         __syncwarp();
-        tmem_ld32(tmem + lane_base + st * 128 + c * 32, v);
+        tmem_ld32(s_col + 0, v0);
+        tmem_ld32(s_col + 32, v1);
+        tmem_ld32(s_col + 64, v2);
+        tmem_ld32(s_col + 96, v3);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int kv = kv0 + c * 32 + i;
-          const bool ok = !((diag && kv > trow) || (tail && kv >= a.S));
-          if (ok) mx = fmaxf(mx, __uint_as_float(v[i]));
+          sv[i] = __uint_as_float(v0[i]);
+          sv[32 + i] = __uint_as_float(v1[i]);
+          sv[64 + i] = __uint_as_float(v2[i]);
+          sv[96 + i] = __uint_as_float(v3[i]);
         }
       }
+      const int kv0 = t * TILE;
+      if (t == nt - 1 || kv0 + TILE > a.S) {  // diagonal or sequence tail: mask
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (kv0 + i > trow || kv0 + i >= a.S) sv[i] = -INFINITY;
+      }
+      float mx8[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mx8[i] = sv[i];
+#pragma unroll
+      for (int i = 8; i < 128; ++i) mx8[i & 7] = fmaxf(mx8[i & 7], sv[i]);
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = mx * a.scale_log2;
       // the previous P V product must be complete before O or P is touched
-      if (t > 0) mbar_wait(o_done, (t - 1) & 1, abort_flag, kErrTimeoutAttn);
+      if (t > 0) mbar_wait(&o_done[side], (t - 1) & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
       // The rescale touches O through warp-collective tensor-memory loads and
       // stores, so the decision is taken per warp: if any row of the warp
@@ -268,50 +325,40 @@ __global__ void __launch_bounds__(192, 1)
       // reference to max(m_new, m_ref) (alpha = 1 where nothing changes).
       if (__any_sync(0xffffffffu, m_new > m_ref + kRescaleThreshold) || t == 0) {
         const float m_use = fmaxf(m_new, m_ref);
-        const float alpha = (m_ref == -INFINITY) ? 0.f : exp2f(m_ref - m_use);
+        const float alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_use);
         l *= alpha;
         if (t > 0) {
 #pragma unroll 1
           for (int c = 0; c < (D + 31) / 32; ++c) {
             uint32_t v[32];
             __syncwarp();
-            tmem_ld32(tmem + lane_base + 256 + c * 32, v);
+            tmem_ld32(o_col + c * 32, v);
             tmem_ld_wait();
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
-            tmem_st32(tmem + lane_base + 256 + c * 32, v);
+            tmem_st32(o_col + c * 32, v);
           }
           tmem_st_wait();
         }
         m_ref = m_use;
       }
-      // pass 2: probabilities (relative to m_ref), row sum, P to shared memory
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        __syncwarp();
-        tmem_ld32(tmem + lane_base + st * 128 + c * 32, v);
-        tmem_ld_wait();
-        float p[32];
+      // probabilities relative to m_ref (masked entries give 0), row sum, P
+      float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int kv = kv0 + c * 32 + i;
-          const bool ok = !((diag && kv > trow) || (tail && kv >= a.S));
-          p[i] = ok ? exp2f(__uint_as_float(v[i]) * a.scale_log2 - m_ref) : 0.f;
-          l += p[i];
-        }
-        st_tile_row32(sm + L::P, r, c, p);
+      for (int i = 0; i < 128; ++i) {
+        sv[i] = ex2_approx(fmaf(sv[i], a.scale_log2, -m_ref));
+        l8[i & 7] += sv[i];
       }
+      l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
+#pragma unroll
+      for (int c = 0; c < 4; ++c) st_tile_row32(ptile, r, c, *reinterpret_cast<const float(*)[32]>(&sv[32 * c]));
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&s_empty[st]);
-        mbar_arrive(p_full);
-      }
+      if (lane == 0) mbar_arrive(&p_full[side]);
     }
     // epilogue: O / l and the log-sum-exp
-    mbar_wait(o_done, (ntiles - 1) & 1, abort_flag, kErrTimeoutAttn);
+    mbar_wait(&o_done[side], (nt - 1) & 1, abort_flag, kErrTimeoutAttn);
     tc_fence_after();
     const bool row_ok = trow < a.S;
     const float inv_l = 1.f / l;
@@ -320,7 +367,7 @@ __global__ void __launch_bounds__(192, 1)
     for (int c = 0; c < (D + 31) / 32; ++c) {
       uint32_t v[32];
       __syncwarp();
-      tmem_ld32(tmem + lane_base + 256 + c * 32, v);
+      tmem_ld32(o_col + c * 32, v);
       tmem_ld_wait();
       if (row_ok) store_row_bf16(orow + c * 32, v, D < 32 ? D : 32, inv_l);
     }
@@ -742,8 +789,9 @@ int fwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, AttnArgs
     if (!set_smem(attn_fwd_tc_kernel<D>, FwdSmem<D>::ALLOC)) return -1;
     init = true;
   }
-  dim3 grid((a.S + TILE - 1) / TILE, a.nq, a.B);
-  attn_fwd_tc_kernel<D><<<grid, 192, FwdSmem<D>::ALLOC, st>>>(tq, tk, tv, a);
+  const int nqt = (a.S + TILE - 1) / TILE;
+  dim3 grid((nqt + 1) / 2, a.nq, a.B);
+  attn_fwd_tc_kernel<D><<<grid, 384, FwdSmem<D>::ALLOC, st>>>(tq, tk, tv, a);
   count_launches(1);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
