@@ -367,7 +367,10 @@ def main():
                           "attn_tflops": (kst["attn_flop"] / (kst["attn_ms"] / 1e3) / 1e12) if kst.get("attn_ms")
                           else None,
                           "gemm_ms_per_step": kst["gemm_ms"], "attn_ms_per_step": kst["attn_ms"],
-                          "compute_busy_ms_per_step": agg["compute_busy_ms"] / steps},
+                          "compute_busy_ms_per_step": agg["compute_busy_ms"] / steps,
+                          # effective rates of the step's own copies (bytes / summed copy time)
+                          "h2d_copy_gbs": agg["h2d_bytes"] / max(1e-9, agg["h2d_ms"]) / 1e6,
+                          "d2h_copy_gbs": agg["d2h_bytes"] / max(1e-9, agg["d2h_ms"]) / 1e6},
         "host_link": link,
         "clocks": clk,
         "loss": losses[-1],

@@ -382,26 +382,73 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ===========================================================================
-// Backward, dK/dV pass: CTA = (128-row KV tile, KV head, sequence).
-// TMEM: S^T +0, dP^T +128, dV +256, dK +384.
+// Backward. Both passes iterate over 64-row sub-tiles of the loop dimension,
+// so that S/dP fit twice in tensor memory (double buffer) and the operand
+// ring has three stages. 12 warps: warp 0 TMA, warp 1 MMA issue, warps 4-7
+// and 8-11 are two elementwise warpgroups that split the 64 columns of each
+// sub-tile (warpgroup A columns 0-31, B 32-63); thread = row of the 128-row
+// tile. The MMA thread issues the score products of sub-tile i+1 before the
+// gradient products of sub-tile i, so elementwise work overlaps the tensor
+// core. Operand layout of a [64 rows][64] box: 8 KB, 128-byte swizzle.
 // ===========================================================================
+constexpr int SUB = 64;
+constexpr int SBOX = 64 * 64 * 2;  // one [64 rows][64] bf16 box = 8 KB
+
+template <int D>
+constexpr uint32_t sub_bytes() {
+  return ((D + 63) / 64) * SBOX;
+}
+// K-major descriptor of the k-th 16-wide step of a [64 rows][64*n] sub-tile.
+__device__ __forceinline__ uint64_t kmaj_desc_sub(const uint8_t* tile, int kk) {
+  return make_sdesc(smem_u32(tile) + (kk >> 2) * SBOX + (kk & 3) * 32, 16, 1024);
+}
+// MN-major descriptor (N = head dim, K = 64 rows) of the k-th 16-row step.
+__device__ __forceinline__ uint64_t mnmaj_desc_sub(const uint8_t* tile, int kk) {
+  return make_sdesc(smem_u32(tile) + kk * 2048, SBOX, 1024);
+}
+// Write columns [32h, 32h+32) of row r of a [128 rows][64] K-major tile.
+__device__ __forceinline__ void st_tile64_row32(uint8_t* tile, int r, int h, const float (&v)[32]) {
+  uint8_t* rowp = tile + r * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int chunk = h * 4 + i;
+    uint4 w;
+    w.x = pack_bf2(v[8 * i + 0], v[8 * i + 1]);
+    w.y = pack_bf2(v[8 * i + 2], v[8 * i + 3]);
+    w.z = pack_bf2(v[8 * i + 4], v[8 * i + 5]);
+    w.w = pack_bf2(v[8 * i + 6], v[8 * i + 7]);
+    *(uint4*)(rowp + ((chunk ^ (r & 7)) << 4)) = w;
+  }
+}
+template <int D>
+__device__ __forceinline__ void load_head_sub(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int head, int row0,
+                                              int b) {
+#pragma unroll
+  for (int i = 0; i < (D + 63) / 64; ++i) tma_load_4d(dst + i * SBOX, map, bar, i * 64, head, row0, b);
+}
+
+constexpr int kStages = 3;
+
+// dK/dV pass: CTA = (128-row KV tile kt, KV head g, sequence b); loop over the
+// query heads of the group and the 64-row query sub-tiles at or after kt.
+// TMEM: S^T [2 x 64] +0, dP^T [2 x 64] +128, dV +256, dK +384.
 template <int D>
 struct DkvSmem {
   static constexpr int K = 0;
   static constexpr int V = K + tile_bytes<D>();
-  static constexpr int Q = V + tile_bytes<D>();
-  static constexpr int DO = Q + tile_bytes<D>();
-  static constexpr int P = DO + tile_bytes<D>();
-  static constexpr int DS = P + 2 * BOX;
-  static constexpr int LSE = DS + 2 * BOX;    // 128 floats
-  static constexpr int DELTA = LSE + 512;     // 128 floats
-  static constexpr int BAR = DELTA + 512;
+  static constexpr int Q0 = V + tile_bytes<D>();                   // [kStages] Q sub-tiles
+  static constexpr int DO0 = Q0 + kStages * sub_bytes<D>();        // [kStages] dO sub-tiles
+  static constexpr int P0 = DO0 + kStages * sub_bytes<D>();        // [2] P^T [128][64]
+  static constexpr int DS0 = P0 + 2 * BOX;                         // [2] dS^T [128][64]
+  static constexpr int LSE = DS0 + 2 * BOX;                        // [2][64] floats (log2 units)
+  static constexpr int DELTA = LSE + 2 * 64 * 4;                   // [2][64] floats
+  static constexpr int BAR = DELTA + 2 * 64 * 4;
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_bwd_dkv_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                            const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                            AttnArgs a) {
@@ -410,33 +457,38 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;
-  uint64_t* qdo_empty = bars + 2;
-  uint64_t* s_full = bars + 3;
-  uint64_t* s_empty = bars + 4;
-  uint64_t* p_full = bars + 5;
-  uint64_t* pd_done = bars + 6;
-  uint32_t* tmem_slot = (uint32_t*)(bars + 7);
+  uint64_t* qdo_full = bars + 1;   // [3]
+  uint64_t* qdo_empty = bars + 4;  // [3]
+  uint64_t* s_full = bars + 7;     // [2]
+  uint64_t* s_empty = bars + 9;    // [2]
+  uint64_t* p_full = bars + 11;    // [2]
+  uint64_t* pd_done = bars + 13;   // [2]
+  uint32_t* tmem_slot = (uint32_t*)(bars + 15);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
   float* s_lse = (float*)(sm + L::LSE);
   float* s_delta = (float*)(sm + L::DELTA);
 
-  const int nt = (a.S + TILE - 1) / TILE;
-  const int kt = (int)blockIdx.x;  // KV tile (short first: low tiles have the most work, scheduled first by y order)
+  const int nsub = (a.S + SUB - 1) / SUB;
+  const int kt = (int)blockIdx.x;
   const int g = blockIdx.y, b = blockIdx.z;
   const int grp = a.nq / a.nkv;
-  const int nq_tiles = nt - kt;   // query tiles kt .. nt-1
-  const int iters = grp * nq_tiles;
+  const int first = 2 * kt;              // first query sub-tile that can see this KV tile
+  const int per_head = nsub - first;
+  const int iters = grp * per_head;
   const uint32_t warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    mbar_init(qdo_full, 1);
-    mbar_init(qdo_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_empty, 4);
-    mbar_init(p_full, 4);
-    mbar_init(pd_done, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&qdo_full[i], 1);
+      mbar_init(&qdo_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 8);
+      mbar_init(&p_full[i], 8);
+      mbar_init(&pd_done[i], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -459,113 +511,121 @@ __global__ void __launch_bounds__(192, 1)
       load_head_tile<D>(sm + L::K, &tk, kv_full, g, kt * TILE, b);
       load_head_tile<D>(sm + L::V, &tv, kv_full, g, kt * TILE, b);
       for (int it = 0; it < iters; ++it) {
-        const int j = g * grp + it / nq_tiles;
-        const int qt = kt + it % nq_tiles;
-        mbar_wait(qdo_empty, (it & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(qdo_full, 2 * tile_bytes<D>());
-        load_head_tile<D>(sm + L::Q, &tq, qdo_full, j, qt * TILE, b);
-        load_head_tile<D>(sm + L::DO, &tdo, qdo_full, j, qt * TILE, b);
+        const int j = g * grp + it / per_head;
+        const int qs = first + it % per_head;
+        const int st = it % kStages;
+        mbar_wait(&qdo_empty[st], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * sub_bytes<D>());
+        load_head_sub<D>(sm + L::Q0 + st * sub_bytes<D>(), &tq, &qdo_full[st], j, qs * SUB, b);
+        load_head_sub<D>(sm + L::DO0 + st * sub_bytes<D>(), &tdo, &qdo_full[st], j, qs * SUB, b);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = make_idesc(128, 128, false, false);
+      constexpr uint32_t IDESC_S = make_idesc(128, SUB, false, false);
       constexpr uint32_t IDESC_G = make_idesc(128, D < 64 ? 64 : D, false, true);
       constexpr int KS = D / 16;
+      auto issue_grad = [&](int i) {
+        const int buf = i & 1, st = i % kStages;
+        mbar_wait(&p_full[buf], (i >> 1) & 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+        const uint8_t* q = sm + L::Q0 + st * sub_bytes<D>();
+        const uint8_t* dout = sm + L::DO0 + st * sub_bytes<D>();
+#pragma unroll
+        for (int kk = 0; kk < SUB / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q
+          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
+          tc_mma(tmem + 256, kmaj_desc(sm + L::P0 + buf * BOX, kk), mnmaj_desc_sub(dout, kk), IDESC_G, acc);
+          tc_mma(tmem + 384, kmaj_desc(sm + L::DS0 + buf * BOX, kk), mnmaj_desc_sub(q, kk), IDESC_G, acc);
+        }
+        tc_commit(&pd_done[buf]);
+        tc_commit(&qdo_empty[st]);
+      };
       mbar_wait(kv_full, 0, abort_flag, kErrTimeoutAttn);
       for (int it = 0; it < iters; ++it) {
-        mbar_wait(qdo_full, it & 1, abort_flag, kErrTimeoutAttn);
-        mbar_wait(s_empty, (it & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        const int buf = it & 1, st = it % kStages;
+        mbar_wait(&qdo_full[st], (it / kStages) & 1, abort_flag, kErrTimeoutAttn);
+        mbar_wait(&s_empty[buf], ((it >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
         tc_fence_after();
+        const uint8_t* q = sm + L::Q0 + st * sub_bytes<D>();
+        const uint8_t* dout = sm + L::DO0 + st * sub_bytes<D>();
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk)  // S^T = K Q^T
-          tc_mma(tmem + 0, kmaj_desc(sm + L::K, kk), kmaj_desc(sm + L::Q, kk), IDESC_S, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk)  // dP^T = V dO^T
-          tc_mma(tmem + 128, kmaj_desc(sm + L::V, kk), kmaj_desc(sm + L::DO, kk), IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(s_full);
-        mbar_wait(p_full, it & 1, abort_flag, kErrTimeoutAttn);
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q
-          tc_mma(tmem + 256, kmaj_desc(sm + L::P, kk), mnmaj_desc(sm + L::DO, kk), IDESC_G,
-                 (it > 0 || kk > 0) ? 1u : 0u);
-          tc_mma(tmem + 384, kmaj_desc(sm + L::DS, kk), mnmaj_desc(sm + L::Q, kk), IDESC_G,
-                 (it > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < KS; ++kk) {  // S^T = K Q^T ; dP^T = V dO^T
+          tc_mma(tmem + buf * 64, kmaj_desc(sm + L::K, kk), kmaj_desc_sub(q, kk), IDESC_S, kk > 0 ? 1u : 0u);
+          tc_mma(tmem + 128 + buf * 64, kmaj_desc(sm + L::V, kk), kmaj_desc_sub(dout, kk), IDESC_S,
+                 kk > 0 ? 1u : 0u);
         }
-        tc_commit(pd_done);
-        tc_commit(qdo_empty);
+        tc_commit(&s_full[buf]);
+        if (it > 0) issue_grad(it - 1);
       }
+      issue_grad(iters - 1);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
+    const int half = warp >= 8 ? 1 : 0;  // which 32 of the 64 columns
     const uint32_t q4 = warp & 3;
-    const int r = q4 * 32 + lane;       // KV row of the tile
-    const int srow = kt * TILE + r;     // KV position
+    const int r = q4 * 32 + lane;        // KV row of the tile
+    const int srow = kt * TILE + r;      // KV position
     const uint32_t lane_base = (q4 * 32) << 16;
-    const int tid = threadIdx.x - 64;   // 0..127
+    const int tid = threadIdx.x - 128;   // 0..255
     for (int it = 0; it < iters; ++it) {
-      const int j = g * grp + it / nq_tiles;
-      const int qt = kt + it % nq_tiles;
-      const int q0 = qt * TILE;
-      // per-column log-sum-exp (log2 units) and delta of this query tile
-      named_bar_sync(1, 128);  // previous iteration finished reading s_lse / s_delta
-      {
-        const int tq = q0 + tid;
-        const size_t ri = ((size_t)b * a.nq + j) * a.S + tq;
-        s_lse[tid] = tq < a.S ? a.lse_in[ri] * 1.4426950408889634f : INFINITY;
-        s_delta[tid] = tq < a.S ? a.delta[ri] : 0.f;
+      const int buf = it & 1;
+      const int j = g * grp + it / per_head;
+      const int q0 = (first + it % per_head) * SUB;
+      if (tid < 128) {  // stage this sub-tile's log-sum-exp (log2 units) and delta
+        const int c = tid & 63;
+        const int tq = q0 + c;
+        const size_t ri = ((size_t)b * a.nq + j) * a.S + (tq < a.S ? tq : 0);
+        if (tid < 64) s_lse[buf * 64 + c] = tq < a.S ? a.lse_in[ri] * 1.4426950408889634f : INFINITY;
+        else s_delta[buf * 64 + c] = tq < a.S ? a.delta[ri] : 0.f;
       }
-      named_bar_sync(1, 128);
-      mbar_wait(s_full, it & 1, abort_flag, kErrTimeoutAttn);
+      named_bar_sync(1, 256);
+      mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
-      // the previous iteration's dV/dK products must be done with P / dS
-      if (it > 0) mbar_wait(pd_done, (it - 1) & 1, abort_flag, kErrTimeoutAttn);
-      const bool diag = (qt == kt);
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dv[32];
-        __syncwarp();
-        tmem_ld32(tmem + lane_base + 0 + c * 32, sv);
-        tmem_ld32(tmem + lane_base + 128 + c * 32, dv);
-        tmem_ld_wait();
-        float p[32], ds[32];
+      uint32_t sv[32], dv[32];
+      __syncwarp();
+      tmem_ld32(tmem + lane_base + buf * 64 + half * 32, sv);
+      tmem_ld32(tmem + lane_base + 128 + buf * 64 + half * 32, dv);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[buf]);
+      float p[32], ds[32];
+      const int cbase = half * 32;
+      const bool need_mask = (q0 + cbase < srow + 1) || (q0 + cbase + 32 > a.S);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int col = c * 32 + i;
+      for (int i = 0; i < 32; ++i) {
+        const int col = cbase + i;
+        float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -s_lse[buf * 64 + col]));
+        if (need_mask) {
           const int tq = q0 + col;
-          const bool ok = !(diag && tq < srow) && tq < a.S;  // query at or after key
-          const float pv = ok ? exp2f(__uint_as_float(sv[i]) * a.scale_log2 - s_lse[col]) : 0.f;
-          p[i] = pv;
-          ds[i] = pv * (__uint_as_float(dv[i]) - s_delta[col]);
+          if (tq < srow || tq >= a.S) pv = 0.f;  // query must be at or after the key
         }
-        st_tile_row32(sm + L::P, r, c, p);
-        st_tile_row32(sm + L::DS, r, c, ds);
+        p[i] = pv;
+        ds[i] = pv * (__uint_as_float(dv[i]) - s_delta[buf * 64 + col]);
       }
+      // the gradient products of sub-tile it-2 must be done with this buffer
+      if (it >= 2) mbar_wait(&pd_done[buf], ((it >> 1) - 1) & 1, abort_flag, kErrTimeoutAttn);
+      st_tile64_row32(sm + L::P0 + buf * BOX, r, half, p);
+      st_tile64_row32(sm + L::DS0 + buf * BOX, r, half, ds);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(s_empty);
-        mbar_arrive(p_full);
-      }
+      if (lane == 0) mbar_arrive(&p_full[buf]);
     }
-    mbar_wait(pd_done, (iters - 1) & 1, abort_flag, kErrTimeoutAttn);
+    mbar_wait(&pd_done[(iters - 1) & 1], ((iters - 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
     tc_fence_after();
+    // epilogue: warpgroup A writes dV, warpgroup B writes dK
     const bool row_ok = srow < a.S;
     const size_t orow = ((size_t)b * a.S + srow) * a.ldkv + (size_t)g * D;
+    const uint32_t col = tmem + lane_base + (half ? 384 : 256);
 #pragma unroll 1
     for (int c = 0; c < (D + 31) / 32; ++c) {
-      uint32_t v[32], k[32];
+      uint32_t v[32];
       __syncwarp();
-      tmem_ld32(tmem + lane_base + 256 + c * 32, v);
-      tmem_ld32(tmem + lane_base + 384 + c * 32, k);
+      tmem_ld32(col + c * 32, v);
       tmem_ld_wait();
-      if (row_ok) {
-        store_row_bf16(a.dv + orow + c * 32, v, D < 32 ? D : 32, 1.f);
-        store_row_bf16(a.dk + orow + c * 32, k, D < 32 ? D : 32, a.scale);
-      }
+      if (row_ok) store_row_bf16((half ? a.dk : a.dv) + orow + c * 32, v, D < 32 ? D : 32, half ? a.scale : 1.f);
     }
   }
   tc_fence_before();
@@ -576,24 +636,23 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
-// ===========================================================================
-// Backward, dQ pass: CTA = (128-row query tile, query head, sequence).
-// TMEM: S +0, dP +128, dQ +256.
-// ===========================================================================
+// dQ pass: CTA = (128-row query tile qt, query head j, sequence b); loop over
+// the 64-row KV sub-tiles at or before the tile's last row.
+// TMEM: S [2 x 64] +0, dP [2 x 64] +128, dQ +256.
 template <int D>
 struct DqSmem {
   static constexpr int Q = 0;
   static constexpr int DO = Q + tile_bytes<D>();
-  static constexpr int K = DO + tile_bytes<D>();
-  static constexpr int V = K + tile_bytes<D>();
-  static constexpr int DS = V + tile_bytes<D>();
-  static constexpr int BAR = DS + 2 * BOX;
+  static constexpr int K0 = DO + tile_bytes<D>();             // [kStages]
+  static constexpr int V0 = K0 + kStages * sub_bytes<D>();    // [kStages]
+  static constexpr int DS0 = V0 + kStages * sub_bytes<D>();   // [2] dS [128][64]
+  static constexpr int BAR = DS0 + 2 * BOX;
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
 };
 
 template <int D>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(384, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                           const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tdo,
                           AttnArgs a) {
@@ -602,30 +661,35 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;
-  uint64_t* kv_empty = bars + 2;
-  uint64_t* s_full = bars + 3;
-  uint64_t* s_empty = bars + 4;
-  uint64_t* p_full = bars + 5;
-  uint64_t* g_done = bars + 6;
-  uint32_t* tmem_slot = (uint32_t*)(bars + 7);
+  uint64_t* kv_full = bars + 1;   // [3]
+  uint64_t* kv_empty = bars + 4;  // [3]
+  uint64_t* s_full = bars + 7;    // [2]
+  uint64_t* s_empty = bars + 9;   // [2]
+  uint64_t* p_full = bars + 11;   // [2]
+  uint64_t* g_done = bars + 13;   // [2]
+  uint32_t* tmem_slot = (uint32_t*)(bars + 15);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int nqt = (a.S + TILE - 1) / TILE;
-  const int qt = nqt - 1 - (int)blockIdx.x;
+  const int qt = nqt - 1 - (int)blockIdx.x;  // longest tiles first
   const int j = blockIdx.y, b = blockIdx.z;
   const int g = j / (a.nq / a.nkv);
-  const int ntiles = qt + 1;
+  const int nsub_all = (a.S + SUB - 1) / SUB;
+  const int iters = min(2 * qt + 2, nsub_all);  // KV sub-tiles 0 .. last one at or before the tile's end
   const uint32_t warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    mbar_init(kv_full, 1);
-    mbar_init(kv_empty, 1);
-    mbar_init(s_full, 1);
-    mbar_init(s_empty, 4);
-    mbar_init(p_full, 4);
-    mbar_init(g_done, 1);
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 8);
+      mbar_init(&p_full[i], 8);
+      mbar_init(&g_done[i], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -647,43 +711,54 @@ __global__ void __launch_bounds__(192, 1)
       mbar_arrive_expect_tx(q_full, 2 * tile_bytes<D>());
       load_head_tile<D>(sm + L::Q, &tq, q_full, j, qt * TILE, b);
       load_head_tile<D>(sm + L::DO, &tdo, q_full, j, qt * TILE, b);
-      for (int t = 0; t < ntiles; ++t) {
-        mbar_wait(kv_empty, (t & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(kv_full, 2 * tile_bytes<D>());
-        load_head_tile<D>(sm + L::K, &tk, kv_full, g, t * TILE, b);
-        load_head_tile<D>(sm + L::V, &tv, kv_full, g, t * TILE, b);
+      for (int it = 0; it < iters; ++it) {
+        const int st = it % kStages;
+        mbar_wait(&kv_empty[st], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&kv_full[st], 2 * sub_bytes<D>());
+        load_head_sub<D>(sm + L::K0 + st * sub_bytes<D>(), &tk, &kv_full[st], g, it * SUB, b);
+        load_head_sub<D>(sm + L::V0 + st * sub_bytes<D>(), &tv, &kv_full[st], g, it * SUB, b);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = make_idesc(128, 128, false, false);
+      constexpr uint32_t IDESC_S = make_idesc(128, SUB, false, false);
       constexpr uint32_t IDESC_G = make_idesc(128, D < 64 ? 64 : D, false, true);
       constexpr int KS = D / 16;
+      auto issue_grad = [&](int i) {
+        const int buf = i & 1, st = i % kStages;
+        mbar_wait(&p_full[buf], (i >> 1) & 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+        const uint8_t* kt = sm + L::K0 + st * sub_bytes<D>();
+#pragma unroll
+        for (int kk = 0; kk < SUB / 16; ++kk)  // dQ += dS K
+          tc_mma(tmem + 256, kmaj_desc(sm + L::DS0 + buf * BOX, kk), mnmaj_desc_sub(kt, kk), IDESC_G,
+                 (i > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&g_done[buf]);
+        tc_commit(&kv_empty[st]);
+      };
       mbar_wait(q_full, 0, abort_flag, kErrTimeoutAttn);
-      for (int t = 0; t < ntiles; ++t) {
-        mbar_wait(kv_full, t & 1, abort_flag, kErrTimeoutAttn);
-        mbar_wait(s_empty, (t & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+      for (int it = 0; it < iters; ++it) {
+        const int buf = it & 1, st = it % kStages;
+        mbar_wait(&kv_full[st], (it / kStages) & 1, abort_flag, kErrTimeoutAttn);
+        mbar_wait(&s_empty[buf], ((it >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
         tc_fence_after();
+        const uint8_t* kt = sm + L::K0 + st * sub_bytes<D>();
+        const uint8_t* vt = sm + L::V0 + st * sub_bytes<D>();
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk)  // S = Q K^T
-          tc_mma(tmem + 0, kmaj_desc(sm + L::Q, kk), kmaj_desc(sm + L::K, kk), IDESC_S, kk > 0 ? 1u : 0u);
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk)  // dP = dO V^T
-          tc_mma(tmem + 128, kmaj_desc(sm + L::DO, kk), kmaj_desc(sm + L::V, kk), IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(s_full);
-        mbar_wait(p_full, t & 1, abort_flag, kErrTimeoutAttn);
-        tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk)  // dQ += dS K
-          tc_mma(tmem + 256, kmaj_desc(sm + L::DS, kk), mnmaj_desc(sm + L::K, kk), IDESC_G,
-                 (t > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(g_done);
-        tc_commit(kv_empty);
+        for (int kk = 0; kk < KS; ++kk) {  // S = Q K^T ; dP = dO V^T
+          tc_mma(tmem + buf * 64, kmaj_desc(sm + L::Q, kk), kmaj_desc_sub(kt, kk), IDESC_S, kk > 0 ? 1u : 0u);
+          tc_mma(tmem + 128 + buf * 64, kmaj_desc(sm + L::DO, kk), kmaj_desc_sub(vt, kk), IDESC_S,
+                 kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[buf]);
+        if (it > 0) issue_grad(it - 1);
       }
+      issue_grad(iters - 1);
     }
     __syncwarp();
-  } else {
+  } else if (warp >= 4) {
+    const int half = warp >= 8 ? 1 : 0;
     const uint32_t q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const int trow = qt * TILE + r;
@@ -692,43 +767,45 @@ __global__ void __launch_bounds__(192, 1)
     const size_t ri = ((size_t)b * a.nq + j) * a.S + (row_ok ? trow : 0);
     const float lse2 = row_ok ? a.lse_in[ri] * 1.4426950408889634f : 0.f;
     const float dl = row_ok ? a.delta[ri] : 0.f;
-    for (int t = 0; t < ntiles; ++t) {
-      mbar_wait(s_full, t & 1, abort_flag, kErrTimeoutAttn);
+    for (int it = 0; it < iters; ++it) {
+      const int buf = it & 1;
+      mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
-      if (t > 0) mbar_wait(g_done, (t - 1) & 1, abort_flag, kErrTimeoutAttn);
-      const int kv0 = t * TILE;
-      const bool diag = (t == qt);
-      const bool tail = kv0 + TILE > a.S;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t sv[32], dv[32];
-        __syncwarp();
-        tmem_ld32(tmem + lane_base + 0 + c * 32, sv);
-        tmem_ld32(tmem + lane_base + 128 + c * 32, dv);
-        tmem_ld_wait();
-        float ds[32];
+      uint32_t sv[32], dv[32];
+      __syncwarp();
+      tmem_ld32(tmem + lane_base + buf * 64 + half * 32, sv);
+      tmem_ld32(tmem + lane_base + 128 + buf * 64 + half * 32, dv);
+      tmem_ld_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_empty[buf]);
+      const int kv0 = it * SUB + half * 32;
+      const bool need_mask = (kv0 + 31 > qt * TILE) || (kv0 + 32 > a.S);
+      float ds[32];
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int kv = kv0 + c * 32 + i;
-          const bool ok = row_ok && !((diag && kv > trow) || (tail && kv >= a.S));
-          const float pv = ok ? exp2f(__uint_as_float(sv[i]) * a.scale_log2 - lse2) : 0.f;
-          ds[i] = pv * (__uint_as_float(dv[i]) - dl);
+      for (int i = 0; i < 32; ++i) {
+        float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -lse2));
+        if (need_mask) {
+          const int kv = kv0 + i;
+          if (kv > trow || kv >= a.S || !row_ok) pv = 0.f;
         }
-        st_tile_row32(sm + L::DS, r, c, ds);
+        ds[i] = pv * (__uint_as_float(dv[i]) - dl);
       }
+      if (it >= 2) mbar_wait(&g_done[buf], ((it >> 1) - 1) & 1, abort_flag, kErrTimeoutAttn);
+      st_tile64_row32(sm + L::DS0 + buf * BOX, r, half, ds);
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(s_empty);
-        mbar_arrive(p_full);
-      }
+      if (lane == 0) mbar_arrive(&p_full[buf]);
     }
-    mbar_wait(g_done, (ntiles - 1) & 1, abort_flag, kErrTimeoutAttn);
+    mbar_wait(&g_done[(iters - 1) & 1], ((iters - 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
     tc_fence_after();
+    // epilogue: each warpgroup writes half of the head-dim columns
     uint16_t* orow = a.dq + ((size_t)b * a.S + trow) * a.ldq + (size_t)j * D;
+    constexpr int NCH = (D + 31) / 32;
 #pragma unroll 1
-    for (int c = 0; c < (D + 31) / 32; ++c) {
+    for (int c = half; c < NCH + (NCH == 1 ? 1 : 0); c += 2) {
+      if (c >= NCH) break;
       uint32_t v[32];
       __syncwarp();
       tmem_ld32(tmem + lane_base + 256 + c * 32, v);
@@ -762,11 +839,12 @@ __global__ void attn_delta_tc_kernel(const uint16_t* __restrict__ o, const uint1
   if (lane_id() == 0) delta[((size_t)b * nq + j) * S + t] = s;
 }
 
-// 4D map over a [B, S, heads, d] view with row stride ld (elements).
-int head_map(CUtensorMap* m, const void* base, int d, int heads, int S, int B, int ld) {
+// 4D map over a [B, S, heads, d] view with row stride ld (elements); boxes
+// of [rows][64] (one head).
+int head_map(CUtensorMap* m, const void* base, int d, int heads, int S, int B, int ld, int rows = 128) {
   const uint64_t gdim[4] = {(uint64_t)d, (uint64_t)heads, (uint64_t)S, (uint64_t)B};
   const uint64_t gstride[3] = {(uint64_t)d * 2, (uint64_t)ld * 2, (uint64_t)S * ld * 2};
-  const uint32_t box[4] = {64, 1, 128, 1};
+  const uint32_t box[4] = {64, 1, (uint32_t)rows, 1};
   return mt_host::encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, gdim, gstride, box,
                                CU_TENSOR_MAP_SWIZZLE_128B) == CUDA_SUCCESS
              ? 0
@@ -799,9 +877,13 @@ int fwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, AttnArgs
 template <int D>
 int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
                AttnArgs& a, float* delta, cudaStream_t st) {
-  CUtensorMap tq, tk, tv, tdo;
-  if (head_map(&tq, q, D, a.nq, a.S, a.B, a.ldq) || head_map(&tk, k, D, a.nkv, a.S, a.B, a.ldkv) ||
-      head_map(&tv, v, D, a.nkv, a.S, a.B, a.ldkv) || head_map(&tdo, dout, D, a.nq, a.S, a.B, a.ldo))
+  // dK/dV pass: K, V in 128-row tiles, Q, dO in 64-row sub-tiles;
+  // dQ pass: Q, dO in 128-row tiles, K, V in 64-row sub-tiles.
+  CUtensorMap tq64, tdo64, tk128, tv128, tq128, tdo128, tk64, tv64;
+  if (head_map(&tq64, q, D, a.nq, a.S, a.B, a.ldq, 64) || head_map(&tdo64, dout, D, a.nq, a.S, a.B, a.ldo, 64) ||
+      head_map(&tk128, k, D, a.nkv, a.S, a.B, a.ldkv) || head_map(&tv128, v, D, a.nkv, a.S, a.B, a.ldkv) ||
+      head_map(&tq128, q, D, a.nq, a.S, a.B, a.ldq) || head_map(&tdo128, dout, D, a.nq, a.S, a.B, a.ldo) ||
+      head_map(&tk64, k, D, a.nkv, a.S, a.B, a.ldkv, 64) || head_map(&tv64, v, D, a.nkv, a.S, a.B, a.ldkv, 64))
     return -1;
   static bool init = false;
   if (!init) {
@@ -813,8 +895,8 @@ int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const ui
   attn_delta_tc_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(o, dout, delta, a.B, a.S, a.nq, D, a.ldo);
   a.delta = delta;
   const int nt = (a.S + TILE - 1) / TILE;
-  attn_bwd_dkv_tc_kernel<D><<<dim3(nt, a.nkv, a.B), 192, DkvSmem<D>::ALLOC, st>>>(tq, tk, tv, tdo, a);
-  attn_bwd_dq_tc_kernel<D><<<dim3(nt, a.nq, a.B), 192, DqSmem<D>::ALLOC, st>>>(tq, tk, tv, tdo, a);
+  attn_bwd_dkv_tc_kernel<D><<<dim3(nt, a.nkv, a.B), 384, DkvSmem<D>::ALLOC, st>>>(tq64, tk128, tv128, tdo64, a);
+  attn_bwd_dq_tc_kernel<D><<<dim3(nt, a.nq, a.B), 384, DqSmem<D>::ALLOC, st>>>(tq128, tk64, tv64, tdo128, a);
   count_launches(3);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
