@@ -112,6 +112,29 @@ def model_flops(shape, B, S):
     return layer, head, P_lin
 
 
+def numa_pages(addrs) -> dict:
+    """Pages per NUMA node of the mappings that contain the given host
+    addresses (from /proc/self/numa_maps; empty when unavailable)."""
+    out = {}
+    try:
+        with open("/proc/self/numa_maps") as f:
+            lines = f.read().splitlines()
+    except OSError:
+        return out
+    starts = sorted((int(l.split()[0], 16), l) for l in lines)
+    for name, a in addrs.items():
+        best = None
+        for st, l in starts:
+            if st <= a:
+                best = l
+            else:
+                break
+        if best:
+            out[name] = {kv.split("=")[0]: int(kv.split("=")[1]) for kv in best.split()
+                         if kv.startswith("N") and "=" in kv}
+    return out
+
+
 def host_link_probe(torch, nbytes=436 * 2**20):
     """Pinned H2D alone, D2H alone, and both at once (GB/s), CUDA events."""
     host_a = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
@@ -269,6 +292,8 @@ def main():
     tok, lab = seedgen.tokens_and_labels(B, S, V, seed=22 + rank)
 
     log(f"parameters filled in {init_s:.1f} s")
+    placement = numa_pages({"params": sess.params_ptr, "grads": sess.grads_ptr})
+    log(f"pinned pages per NUMA node: {placement}")
     link = host_link_probe(torch)
     log(f"host link {link}")
     for i in range(args.warmup):
@@ -372,6 +397,7 @@ def main():
                           "h2d_copy_gbs": agg["h2d_bytes"] / max(1e-9, agg["h2d_ms"]) / 1e6,
                           "d2h_copy_gbs": agg["d2h_bytes"] / max(1e-9, agg["d2h_ms"]) / 1e6},
         "host_link": link,
+        "host_numa_pages": placement,
         "clocks": clk,
         "loss": losses[-1],
         "init_s": init_s,

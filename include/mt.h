@@ -245,6 +245,14 @@ int mt_op_rmsnorm_bwd_noalloc(const float* x, const float* w, const float* rstd,
 int mt_op_rope(void* x, float* table, int B, int S, int row_stride, int head0, int n_heads, int d, float theta,
                int dir, void* stream);
 
+/* The q|k|v projection with RoPE fused into the GEMM epilogue:
+ * C[M,N] bf16 = A[M,K] W[N,K]^T where columns [0, rope_cols) (whole heads of
+ * width d in {16,32,64,128}) are rotated by RoPE at position row % S before
+ * the single rounding to bf16 (theta as in mt_op_rope). table: device fp32
+ * workspace of S*d floats, overwritten. rope_cols must be a multiple of d. */
+int mt_op_gemm_rope(const void* A, const void* W, void* C, int M, int N, int K, int lda, int ldb, int ldc,
+                    float* table, int S, int d, float theta, int rope_cols, void* stream);
+
 /* Causal GQA attention forward on bf16 q/k/v/o with row strides (elements):
  * q [B*S, ldq] heads at columns j*d, k/v [B*S, ldkv], o [B*S, ldo];
  * lse fp32 [B, n_heads, S] (natural-log logsumexp of the scaled scores). */
@@ -258,6 +266,15 @@ size_t mt_op_attention_bwd_workspace(int B, int S, int n_heads);
 int mt_op_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_, const float* lse,
                         void* dq, void* dk, void* dv, float* workspace, int B, int S, int n_heads, int n_kv_heads,
                         int d, int ldq, int ldkv, int ldo, void* stream);
+
+/* mt_op_attention_bwd for q and k that were rotated by RoPE after the
+ * projection: dq and dk are returned rotated back (the gradient w.r.t. the
+ * unrotated projections), fused into the output stage. table: device fp32
+ * workspace of S*d floats, overwritten. */
+int mt_op_attention_bwd_rope(const void* q, const void* k, const void* v, const void* o, const void* do_,
+                             const float* lse, void* dq, void* dk, void* dv, float* workspace, int B, int S,
+                             int n_heads, int n_kv_heads, int d, int ldq, int ldkv, int ldo, float* table, float theta,
+                             void* stream);
 
 /* SwiGLU on gu bf16 [T, 2*ld] (gate columns [0,F), up columns [ld, ld+F)):
  * forward act bf16 [T, ld] = silu(g)*u (padding columns F..ld-1 written 0);

@@ -41,7 +41,7 @@ EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_crea
            "mt_last_error",
            "mt_destroy", "mt_host_alloc", "mt_host_free", "mt_debug_inject_fault", "mt_op_gemm",
            "mt_op_rmsnorm_fwd", "mt_op_rmsnorm_bwd_workspace", "mt_op_rmsnorm_bwd", "mt_op_rmsnorm_bwd_noalloc",
-           "mt_op_rope",
+           "mt_op_rope", "mt_op_gemm_rope", "mt_op_attention_bwd_rope",
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
            "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error")
 
@@ -118,6 +118,9 @@ def lib() -> ctypes.CDLL:
         "mt_op_rmsnorm_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp]),
         "mt_op_rmsnorm_bwd_noalloc": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, vp]),
         "mt_op_rope": (i32, [vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, vp]),
+        "mt_op_gemm_rope": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32, f32, i32, vp]),
+        "mt_op_attention_bwd_rope": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+                                           i32, vp, f32, vp]),
         "mt_op_attention_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp]),
         "mt_op_attention_bwd_workspace": (sz, [i32, i32, i32]),
         "mt_op_attention_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
@@ -376,6 +379,18 @@ def mt_op_rmsnorm_bwd_noalloc(x, w, rstd, dy, resid, dx, dx_bf16, dw, T, h, stre
 def mt_op_rope(x, table, B, S, row_stride, head0, n_heads, d, theta, direction, stream=None):
     _check(lib().mt_op_rope(_ptr(x), _ptr(table), B, S, row_stride, head0, n_heads, d, theta, direction,
                             _stream(stream)))
+
+
+def mt_op_gemm_rope(A, W, C, M, N, K, lda, ldb, ldc, table, S, d, theta, rope_cols, stream=None):
+    _check(lib().mt_op_gemm_rope(_ptr(A), _ptr(W), _ptr(C), M, N, K, lda, ldb, ldc, _ptr(table), S, d, theta,
+                                 rope_cols, _stream(stream)))
+
+
+def mt_op_attention_bwd_rope(q, k, v, o, do, lse, dq, dk, dv, workspace, B, S, nq, nkv, d, ldq, ldkv, ldo, table,
+                             theta, stream=None):
+    _check(lib().mt_op_attention_bwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
+                                          _ptr(dk), _ptr(dv), _ptr(workspace), B, S, nq, nkv, d, ldq, ldkv, ldo,
+                                          _ptr(table), theta, _stream(stream)))
 
 
 def mt_op_attention_fwd(q, k, v, o, lse, B, S, nq, nkv, d, ldq, ldkv, ldo, stream=None):

@@ -115,7 +115,65 @@ struct AttnArgs {
   int B, S, nq, nkv, ldq, ldkv, ldo;
   float scale_log2;  // log2(e) / sqrt(d)
   float scale;       // 1 / sqrt(d)
+  const float2* rope_tab;  // backward: rotate dq/dk back by RoPE (nullable), [S][d/2] (cos, sin)
 };
+
+// Store one row of a head-dim gradient (dq or dk) held in TMEM columns
+// [tcol, tcol + D), scaled by mul, optionally rotated back by RoPE (the
+// transpose of the forward rotation: (x1, x2) -> (x1 c + x2 s, -x1 s + x2 c)).
+// part/nparts split the work between warpgroups (each call is warp-collective).
+template <int D>
+__device__ __forceinline__ void store_grad_row(uint16_t* orow, uint32_t tcol, bool row_ok, float mul,
+                                               const float2* tab, int part, int nparts) {
+  constexpr int NCH = (D + 31) / 32;
+  if (!tab) {
+#pragma unroll 1
+    for (int c = part; c < NCH; c += nparts) {
+      uint32_t v[32];
+      __syncwarp();
+      tmem_ld32(tcol + c * 32, v);
+      tmem_ld_wait();
+      if (row_ok) store_row_bf16(orow + c * 32, v, D < 32 ? D : 32, mul);
+    }
+    return;
+  }
+  if (D >= 64) {
+    constexpr int P = D / 64;  // chunk distance between the halves of the head
+#pragma unroll 1
+    for (int c = part; c < P; c += nparts) {
+      uint32_t va[32], vb[32];
+      __syncwarp();
+      tmem_ld32(tcol + c * 32, va);
+      tmem_ld32(tcol + (c + P) * 32, vb);
+      tmem_ld_wait();
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float2 cs = tab[c * 32 + i];
+        const float x1 = __uint_as_float(va[i]) * mul, x2 = __uint_as_float(vb[i]) * mul;
+        va[i] = __float_as_uint(x1 * cs.x + x2 * cs.y);
+        vb[i] = __float_as_uint(-x1 * cs.y + x2 * cs.x);
+      }
+      if (row_ok) {
+        store_row_bf16(orow + c * 32, va, 32, 1.f);
+        store_row_bf16(orow + (c + P) * 32, vb, 32, 1.f);
+      }
+    }
+  } else if (part == 0) {  // D in {16, 32}: both halves in the first chunk
+    uint32_t v[32];
+    __syncwarp();
+    tmem_ld32(tcol, v);
+    tmem_ld_wait();
+    constexpr int H = D / 2;
+#pragma unroll
+    for (int i = 0; i < H; ++i) {
+      const float2 cs = tab[i];
+      const float x1 = __uint_as_float(v[i]) * mul, x2 = __uint_as_float(v[i + H]) * mul;
+      v[i] = __float_as_uint(x1 * cs.x + x2 * cs.y);
+      v[i + H] = __float_as_uint(-x1 * cs.y + x2 * cs.x);
+    }
+    if (row_ok) store_row_bf16(orow, v, D, 1.f);
+  }
+}
 
 constexpr float kLn2 = 0.69314718055994530942f;
 constexpr float kRescaleThreshold = 8.0f;  // log2 units
@@ -615,18 +673,14 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_wait(&pd_done[(iters - 1) & 1], ((iters - 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
     tc_fence_after();
-    // epilogue: warpgroup A writes dV, warpgroup B writes dK
+    // epilogue: warpgroup A writes dV, warpgroup B writes dK (rotated back by RoPE if requested)
     const bool row_ok = srow < a.S;
     const size_t orow = ((size_t)b * a.S + srow) * a.ldkv + (size_t)g * D;
-    const uint32_t col = tmem + lane_base + (half ? 384 : 256);
-#pragma unroll 1
-    for (int c = 0; c < (D + 31) / 32; ++c) {
-      uint32_t v[32];
-      __syncwarp();
-      tmem_ld32(col + c * 32, v);
-      tmem_ld_wait();
-      if (row_ok) store_row_bf16((half ? a.dk : a.dv) + orow + c * 32, v, D < 32 ? D : 32, half ? a.scale : 1.f);
-    }
+    const float2* tab = a.rope_tab ? a.rope_tab + (size_t)(row_ok ? srow : 0) * (D / 2) : nullptr;
+    if (half == 0)
+      store_grad_row<D>(a.dv + orow, tmem + lane_base + 256, row_ok, 1.f, nullptr, 0, 1);
+    else
+      store_grad_row<D>(a.dk + orow, tmem + lane_base + 384, row_ok, a.scale, tab, 0, 1);
   }
   tc_fence_before();
   __syncthreads();
@@ -800,18 +854,10 @@ __global__ void __launch_bounds__(384, 1)
     }
     mbar_wait(&g_done[(iters - 1) & 1], ((iters - 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
     tc_fence_after();
-    // epilogue: each warpgroup writes half of the head-dim columns
+    // epilogue: the two warpgroups share the head-dim columns
     uint16_t* orow = a.dq + ((size_t)b * a.S + trow) * a.ldq + (size_t)j * D;
-    constexpr int NCH = (D + 31) / 32;
-#pragma unroll 1
-    for (int c = half; c < NCH + (NCH == 1 ? 1 : 0); c += 2) {
-      if (c >= NCH) break;
-      uint32_t v[32];
-      __syncwarp();
-      tmem_ld32(tmem + lane_base + 256 + c * 32, v);
-      tmem_ld_wait();
-      if (row_ok) store_row_bf16(orow + c * 32, v, D < 32 ? D : 32, a.scale);
-    }
+    const float2* tab = a.rope_tab ? a.rope_tab + (size_t)(row_ok ? trow : 0) * (D / 2) : nullptr;
+    store_grad_row<D>(orow, tmem + lane_base + 256, row_ok, a.scale, tab, half, 2);
   }
   tc_fence_before();
   __syncthreads();
@@ -916,7 +962,7 @@ int attention_fwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
                      int nq, int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st) {
   if (!tc_ok(B, S, nq, nkv, d, ldq, ldkv, ldo, q, k, v)) return -1;
   AttnArgs a{o, lse, nullptr, nullptr, nullptr, nullptr, nullptr, B, S, nq, nkv, ldq, ldkv, ldo,
-             1.4426950408889634f / sqrtf((float)d), 1.f / sqrtf((float)d)};
+             1.4426950408889634f / sqrtf((float)d), 1.f / sqrtf((float)d), nullptr};
   switch (d) {
     case 16: return fwd_launch<16>(q, k, v, a, st);
     case 32: return fwd_launch<32>(q, k, v, a, st);
@@ -927,10 +973,10 @@ int attention_fwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
 
 int attention_bwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
                      const float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv, float* work, int B, int S, int nq,
-                     int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st) {
+                     int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st, const float2* rope_tab) {
   if (!tc_ok(B, S, nq, nkv, d, ldq, ldkv, ldo, q, k, v)) return -1;
   AttnArgs a{nullptr, nullptr, lse, nullptr, dq, dk, dv, B, S, nq, nkv, ldq, ldkv, ldo,
-             1.4426950408889634f / sqrtf((float)d), 1.f / sqrtf((float)d)};
+             1.4426950408889634f / sqrtf((float)d), 1.f / sqrtf((float)d), rope_tab};
   switch (d) {
     case 16: return bwd_launch<16>(q, k, v, o, dout, a, work, st);
     case 32: return bwd_launch<32>(q, k, v, o, dout, a, work, st);

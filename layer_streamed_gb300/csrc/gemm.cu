@@ -15,6 +15,9 @@
 // accumulators (2 x BN columns) so the epilogue of tile i overlaps the
 // mainloop of tile i+1. Each output tile is produced by one CTA with a fixed
 // K order, so results do not depend on the grid size (deterministic).
+#include <algorithm>
+#include <cstdlib>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -39,8 +42,9 @@ struct GemmCfg {
 
 // Tile order: groups of GROUP_M row-blocks, row-block fastest inside a group,
 // so a wave of CTAs shares a band of A rows and a few B column-blocks in L2.
-__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int& m_blk, int& n_blk) {
-  constexpr int GROUP_M = 16;
+// GROUP_M is chosen on the host so that the band of A fits comfortably in L2
+// (the whole of M when it does), which makes B stream from DRAM once per group.
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int GROUP_M, int& m_blk, int& n_blk) {
   const int per_group = GROUP_M * num_n;
   const int g = tile / per_group;
   const int first_m = g * GROUP_M;
@@ -48,6 +52,92 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int&
   const int r = tile - g * per_group;
   m_blk = first_m + r % gsize;
   n_blk = r / gsize;
+}
+
+// Store 32 fp32 values as bf16 at columns [col0, col0+32) of a row (partial
+// at the right edge).
+__device__ __forceinline__ void store_bf16_32(uint16_t* out, const float (&v)[32], int col0, int N, bool vec) {
+  if (vec && col0 + 32 <= N) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint4 w;
+      w.x = pack_bf2(v[8 * k + 0], v[8 * k + 1]);
+      w.y = pack_bf2(v[8 * k + 2], v[8 * k + 3]);
+      w.z = pack_bf2(v[8 * k + 4], v[8 * k + 5]);
+      w.w = pack_bf2(v[8 * k + 6], v[8 * k + 7]);
+      ((uint4*)out)[k] = w;
+    }
+  } else {
+    for (int j = 0; j < 32 && col0 + j < N; ++j) out[j] = f2bf(v[j]);
+  }
+}
+
+// bf16 epilogue with RoPE on the head columns (half-split pairs (i, i+d/2)):
+// for d >= 64 the two halves of a head are chunk pairs (c, c + d/64); for
+// d < 64 both halves sit in one 32-column chunk. Tiles are head-aligned
+// (BN is a multiple of d).
+template <int BN>
+__device__ __forceinline__ void rope_epilogue(const GemmParams& p, uint32_t tbase, int row, bool row_ok, int n0) {
+  const int d = p.rope_d, half = d >> 1;
+  const float2* tab = p.rope_tab + (size_t)(row_ok ? row % p.rope_S : 0) * half;
+  uint16_t* out = (uint16_t*)p.C + (size_t)row * p.ldc;
+  if (d >= 64) {
+    const int P = d >> 6;  // chunk distance between the halves
+#pragma unroll 1
+    for (int ca = 0; ca < BN / 32; ++ca) {
+      if ((ca % (2 * P)) >= P) continue;  // second half: handled with its partner
+      const int cb = ca + P;
+      uint32_t ra[32], rb[32];
+      __syncwarp();
+      tmem_ld32(tbase + ca * 32, ra);
+      tmem_ld32(tbase + cb * 32, rb);
+      tmem_ld_wait();
+      const int cola = n0 + ca * 32, colb = n0 + cb * 32;
+      if (!row_ok || cola >= p.N) continue;
+      const bool rot = cola < p.rope_cols;
+      const int i0 = (ca % P) * 32;  // pair index of the chunk's first column within the head
+      float fa[32], fb[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const float x1 = __uint_as_float(ra[i]), x2 = __uint_as_float(rb[i]);
+        if (rot) {
+          const float2 cs = tab[i0 + i];
+          fa[i] = x1 * cs.x - x2 * cs.y;
+          fb[i] = x1 * cs.y + x2 * cs.x;
+        } else {
+          fa[i] = x1;
+          fb[i] = x2;
+        }
+      }
+      store_bf16_32(out + cola, fa, cola, p.N, p.vec);
+      if (colb < p.N) store_bf16_32(out + colb, fb, colb, p.N, p.vec);
+    }
+  } else {
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint32_t r[32];
+      __syncwarp();
+      tmem_ld32(tbase + c * 32, r);
+      tmem_ld_wait();
+      const int col0 = n0 + c * 32;
+      if (!row_ok || col0 >= p.N) continue;
+      float f[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) {
+        const int li = i % d;  // d in {16, 32}: divides 32
+        const bool rot = col0 + i - li < p.rope_cols;
+        if (rot && li < half) {
+          const float x1 = __uint_as_float(r[i]), x2 = __uint_as_float(r[i + half]);
+          const float2 cs = tab[li];
+          f[i] = x1 * cs.x - x2 * cs.y;
+          f[i + half] = x1 * cs.y + x2 * cs.x;
+        } else if (!rot) {
+          f[i] = __uint_as_float(r[i]);
+        }
+      }
+      store_bf16_32(out + col0, f, col0, p.N, p.vec);
+    }
+  }
 }
 
 template <int BN, bool A_MN, bool B_MN>
@@ -101,7 +191,7 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         int mb, nb;
-        tile_coords(tile, num_m, num_n, mb, nb);
+        tile_coords(tile, num_m, num_n, p.group_m, mb, nb);
         const int m0 = mb * BM, n0 = nb * BN;
         for (int kb = 0; kb < num_kb; ++kb) {
           mbar_wait(&empty[stage], phase ^ 1, abort_flag, kErrTimeoutTma);
@@ -166,13 +256,20 @@ __global__ void __launch_bounds__(192, 1)
     int local = 0;
     for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
       int mb, nb;
-      tile_coords(tile, num_m, num_n, mb, nb);
+      tile_coords(tile, num_m, num_n, p.group_m, mb, nb);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       mbar_wait(&tfull[acc], acc_phase, abort_flag, kErrTimeoutEpi);
       tc_fence_after();
       const int row = mb * BM + q * 32 + lane;
       const bool row_ok = row < p.M;
+      if (p.rope_tab) {
+        rope_epilogue<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, row, row_ok, nb * BN);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&tempty[acc]);
+        continue;
+      }
 #pragma unroll 1
       for (int c = 0; c < BN / 32; ++c) {
         uint32_t r[32];
@@ -268,12 +365,28 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
   if (p.M <= 0 || p.N <= 0 || p.K <= 0 || !p.C || p.epi < EPI_BF16 || p.epi > EPI_F32_ADD) return -1;
   if ((lda & 7) || (ldb & 7) || ((uintptr_t)A & 15) || ((uintptr_t)B & 15)) return -1;
   if (p.epi == EPI_F32_ADD && !p.addend) return -1;
+  if (p.rope_tab && (p.epi != EPI_BF16 || p.rope_S <= 0 || (p.rope_d != 16 && p.rope_d != 32 && p.rope_d != 64 &&
+                                                             p.rope_d != 128) || p.rope_cols % p.rope_d))
+    return -1;
   // 16-byte stores need 16-byte aligned rows; otherwise the epilogue stores element by element.
   const int esz = p.epi == EPI_BF16 ? 2 : 4;
   p.vec = (((uintptr_t)p.C & 15) == 0 && ((size_t)p.ldc * esz) % 16 == 0 &&
            (p.epi != EPI_F32_ADD || ((uintptr_t)p.addend & 15) == 0))
               ? 1
               : 0;
+  {
+    // Band of A rows shared by one tile group: MT_GEMM_BAND_MB (default 32 MB).
+    static size_t band_budget = 0;
+    if (!band_budget) {
+      const char* e = getenv("MT_GEMM_BAND_MB");
+      const long mb = e ? atol(e) : 32;
+      band_budget = (size_t)(mb > 0 ? mb : 32) << 20;
+    }
+    const int num_m = (p.M + BM - 1) / BM;
+    const size_t band = (size_t)BM * p.K * 2;  // bytes of A per row-block
+    const int gm = (int)std::max<size_t>(1, band_budget / band);
+    p.group_m = gm < num_m ? gm : num_m;
+  }
   // BN = 256 unless that leaves most SMs idle.
   const int tiles256 = ((p.M + BM - 1) / BM) * ((p.N + 255) / 256);
   const bool wide = tiles256 >= mt_host::num_sms();

@@ -22,7 +22,13 @@ struct GemmParams {
   void* C;
   const void* addend;  // EPI_F32_ADD: C = addend + acc (same row stride)
   int ldc;
-  int vec;  // set by gemm_bf16: 1 if C rows allow 16-byte stores
+  int vec;      // set by gemm_bf16: 1 if C rows allow 16-byte stores
+  int group_m;  // set by gemm_bf16: row-blocks per tile group (L2 reuse)
+  // Optional RoPE in the bf16 epilogue: columns [0, rope_cols) form heads of
+  // width rope_d rotated by the (cos, sin) table [rope_S][rope_d/2] at
+  // position row % rope_S before the single rounding to bf16.
+  const float2* rope_tab = nullptr;
+  int rope_S = 0, rope_d = 0, rope_cols = 0;
 };
 
 // C[M,N] = op(A) op(B) with bf16 operands, fp32 accumulation (see gemm.cu).
@@ -92,9 +98,11 @@ uint32_t attention_tc_take_device_error();
 // row strides multiples of 8. work: B*S*nq floats (delta).
 int attention_fwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int B, int S,
                      int nq, int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
+// rope_tab (nullable, [S][d/2] (cos, sin)): q and k were rotated after
+// projection; dq and dk are then rotated back (inverse RoPE) before rounding.
 int attention_bwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
                      const float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv, float* work, int B, int S, int nq,
-                     int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
+                     int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st, const float2* rope_tab = nullptr);
 
 // fp32 -> bf16 copy of a dense buffer.
 int cast_f32_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st);

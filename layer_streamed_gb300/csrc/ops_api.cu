@@ -21,7 +21,7 @@ extern "C" {
 int mt_op_gemm(int mode, int epi, const void* A, const void* B, void* C, const void* addend, int M, int N, int K,
                int lda, int ldb, int ldc, void* stream) {
   if (!A || !B || !C) return MT_ERR_ARG;
-  GemmParams p{M, N, K, epi, C, addend, ldc, 0};
+  GemmParams p{M, N, K, epi, C, addend, ldc, 0, 1};
   return rc(gemm_bf16(mode, p, A, B, lda, ldb, S(stream)));
 }
 
@@ -55,6 +55,18 @@ int mt_op_rope(void* x, float* table, int B, int S_, int row_stride, int head0, 
   return rc(rope_apply((uint16_t*)x, tab, B, S_, row_stride, head0, n_heads, d, dir, S(stream)));
 }
 
+int mt_op_gemm_rope(const void* A, const void* W, void* C, int M, int N, int K, int lda, int ldb, int ldc,
+                    float* table, int S_, int d, float theta, int rope_cols, void* stream) {
+  if (!A || !W || !C || !table || S_ < 1 || d < 16 || rope_cols < 0) return MT_ERR_ARG;
+  if (rope_table((float2*)table, S_, d, theta, S(stream))) return rc(-1);
+  GemmParams p{M, N, K, EPI_BF16, C, nullptr, ldc, 0, 1};
+  p.rope_tab = (const float2*)table;
+  p.rope_S = S_;
+  p.rope_d = d;
+  p.rope_cols = rope_cols;
+  return rc(gemm_bf16(GEMM_NT, p, A, W, lda, ldb, S(stream)));
+}
+
 int mt_op_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_, int n_heads,
                         int n_kv_heads, int d, int ldq, int ldkv, int ldo, void* stream) {
   if (!q || !k || !v || !o || !lse) return MT_ERR_ARG;
@@ -71,6 +83,17 @@ int mt_op_attention_bwd(const void* q, const void* k, const void* v, const void*
   return rc(attention_bwd_tc((const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, (const uint16_t*)o,
                           (const uint16_t*)do_, lse, (uint16_t*)dq, (uint16_t*)dk, (uint16_t*)dv, workspace, B, S_,
                           n_heads, n_kv_heads, d, ldq, ldkv, ldo, S(stream)));
+}
+
+int mt_op_attention_bwd_rope(const void* q, const void* k, const void* v, const void* o, const void* do_,
+                             const float* lse, void* dq, void* dk, void* dv, float* workspace, int B, int S_,
+                             int n_heads, int n_kv_heads, int d, int ldq, int ldkv, int ldo, float* table, float theta,
+                             void* stream) {
+  if (!q || !k || !v || !o || !do_ || !lse || !dq || !dk || !dv || !workspace || !table) return MT_ERR_ARG;
+  if (rope_table((float2*)table, S_, d, theta, S(stream))) return rc(-1);
+  return rc(attention_bwd_tc((const uint16_t*)q, (const uint16_t*)k, (const uint16_t*)v, (const uint16_t*)o,
+                             (const uint16_t*)do_, lse, (uint16_t*)dq, (uint16_t*)dk, (uint16_t*)dv, workspace, B, S_,
+                             n_heads, n_kv_heads, d, ldq, ldkv, ldo, S(stream), (const float2*)table));
 }
 
 int mt_op_swiglu_fwd(const void* gu, void* act, int T, int F, int ld, void* stream) {
@@ -107,14 +130,14 @@ int mt_op_lmhead_ce(const void* X, const void* W, const int32_t* labels, float s
   w += rup((size_t)T * 4, 256);
   float* terms = (float*)w;
   cudaStream_t st = S(stream);
-  GemmParams p1{T, V, h, EPI_F32, logits, nullptr, ld, 0};
+  GemmParams p1{T, V, h, EPI_F32, logits, nullptr, ld, 0, 1};
   if (gemm_bf16(GEMM_NT, p1, X, W, h, h, st)) return rc(-1);
   if (ce_slice_stats(logits, T, V, ld, 0, labels, part, zlab, st)) return rc(-1);
   if (ce_finalize(part, 1, zlab, lse, terms, loss_dev, T, scale, st)) return rc(-1);
   if (ce_slice_grad(logits, T, V, ld, 0, labels, lse, scale, dz, st)) return rc(-1);
-  GemmParams p2{T, h, V, EPI_F32, dX, nullptr, h, 0};
+  GemmParams p2{T, h, V, EPI_F32, dX, nullptr, h, 0, 1};
   if (gemm_bf16(GEMM_NN, p2, dz, W, ld, h, st)) return rc(-1);
-  GemmParams p3{V, h, T, EPI_F32, dW, nullptr, h, 0};
+  GemmParams p3{V, h, T, EPI_F32, dW, nullptr, h, 0, 1};
   if (gemm_bf16(GEMM_TN, p3, dz, X, ld, h, st)) return rc(-1);
   return MT_OK;
 }

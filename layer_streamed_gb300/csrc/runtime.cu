@@ -31,6 +31,9 @@
 #include <thread>
 #include <vector>
 
+#include <sys/syscall.h>
+#include <unistd.h>
+
 #include "../../include/mt.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -452,8 +455,14 @@ struct OpTimer {
 };
 
 int gemm(mt_ctx* ctx, int mode, int epi, const void* A, const void* B, void* C, const void* add, int M, int N, int K,
-         int lda, int ldb, int ldc) {
-  GemmParams p{M, N, K, epi, C, add, ldc, 0};
+         int lda, int ldb, int ldc, int rope_S = 0, int rope_cols = 0) {
+  GemmParams p{M, N, K, epi, C, add, ldc, 0, 1};
+  if (rope_cols > 0) {
+    p.rope_tab = ctx->rope_tab;
+    p.rope_S = rope_S;
+    p.rope_d = ctx->P.d;
+    p.rope_cols = rope_cols;
+  }
   OpTimer timer(ctx, 0, 2.0 * M * N * K);
   if (gemm_bf16(mode, p, A, B, lda, ldb, ctx->s_comp) != 0) {
     cudaError_t e = cudaGetLastError();
@@ -645,8 +654,8 @@ int layer_forward(Step& st, int l, const LayerView& w) {
   float* y = layer_output(st, l);
   cudaStream_t s = ctx->s_comp;
   CKL(rmsnorm_fwd(x, w.w1, a.a, a.rstd1, T, h, ctx->cfg.norm_eps, s));
-  CKR(gemm(ctx, GEMM_NT, EPI_BF16, a.a, w.wqkv, a.qkv, nullptr, T, p.qkv, h, h, h, p.qkv));
-  CKL(rope_apply(a.qkv, ctx->rope_tab, st.B, st.S, p.qkv, 0, p.nq + p.nkv, p.d, +1, s));
+  // q|k|v projection with RoPE applied to the q and k heads in the epilogue
+  CKR(gemm(ctx, GEMM_NT, EPI_BF16, a.a, w.wqkv, a.qkv, nullptr, T, p.qkv, h, h, h, p.qkv, st.S, p.qd + p.kd));
   {
     OpTimer timer(ctx, 1, attn_flop(st, p));
     CKL(attention_fwd_tc(a.qkv, a.qkv + p.qd, a.qkv + p.qd + p.kd, a.o, a.lse, st.B, st.S, p.nq, p.nkv, p.d, p.qkv,
@@ -713,11 +722,11 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   CKR(gemm(ctx, GEMM_NN, EPI_BF16, ctx->dhmid_b, w.wo, ctx->do_b, nullptr, T, p.qd, h, h, p.qd, p.qd));
   {
     OpTimer timer(ctx, 1, 2.5 * attn_flop(st, p));
+    // dq and dk come out rotated back by RoPE (the forward rotated q and k)
     CKL(attention_bwd_tc(a.qkv, a.qkv + p.qd, a.qkv + p.qd + p.kd, a.o, ctx->do_b, a.lse, ctx->dqkv,
                       ctx->dqkv + p.qd, ctx->dqkv + p.qd + p.kd, ctx->attn_ws, st.B, st.S, p.nq, p.nkv, p.d, p.qkv,
-                      p.qkv, p.qd, s));
+                      p.qkv, p.qd, s, ctx->rope_tab));
   }
-  CKL(rope_apply(ctx->dqkv, ctx->rope_tab, st.B, st.S, p.qkv, 0, p.nq + p.nkv, p.d, -1, s));
   CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dqkv, a.a, GT(1), nullptr, p.qkv, h, T, p.qkv, h, h));
   CKR(gemm(ctx, GEMM_NN, EPI_F32, ctx->dqkv, w.wqkv, ctx->dm, nullptr, T, h, p.qkv, p.qkv, h, h));
   // RMSNorm 1 (+ residual): new dh
@@ -1219,22 +1228,47 @@ void mt_destroy(mt_ctx* ctx) {
   delete ctx;
 }
 
-// cudaHostAlloc may return less than page alignment for small requests, so
-// over-allocate and keep the original pointer just below the aligned one.
+// Pinned host memory from cudaHostAlloc (driver-allocated page-locked memory:
+// on this platform the copy engines stream it at the link rate, whereas
+// cudaHostRegister'ed anonymous memory of the same size streamed an order of
+// magnitude slower in measurements). The calling thread's memory policy is
+// set to prefer the host NUMA node nearest the current GPU for the duration
+// of the allocation, so that the pages land next to the GPU's link on
+// multi-node hosts. A small header just below the returned (4096-aligned)
+// pointer keeps the original allocation for mt_host_free.
+namespace {
+struct HostBlock {
+  void* base;
+  size_t bytes;
+};
+}  // namespace
+
 void* mt_host_alloc(size_t bytes) {
+  const size_t total = (bytes ? bytes : 1) + 4096 + sizeof(HostBlock);
+  int dev = 0, node = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&node, cudaDevAttrHostNumaId, dev) != cudaSuccess)
+    node = -1;
+  cudaGetLastError();
+  bool policy_set = false;
+  if (node >= 0 && node < 1024) {
+    unsigned long mask[16] = {0};
+    mask[node / 64] |= 1ul << (node % 64);
+    policy_set = syscall(SYS_set_mempolicy, 1 /* MPOL_PREFERRED */, mask, 1025ul) == 0;
+  }
   void* p = nullptr;
-  const size_t total = (bytes ? bytes : 1) + 4096 + 16;
-  if (cudaHostAlloc(&p, total, cudaHostAllocDefault) != cudaSuccess) {
+  const cudaError_t e = cudaHostAlloc(&p, total, cudaHostAllocDefault);
+  if (policy_set) syscall(SYS_set_mempolicy, 0 /* MPOL_DEFAULT */, nullptr, 0ul);
+  if (e != cudaSuccess) {
     cudaGetLastError();
     return nullptr;
   }
-  const uintptr_t a = ((uintptr_t)p + 16 + 4095) & ~(uintptr_t)4095;
-  ((void**)a)[-1] = p;
+  const uintptr_t a = ((uintptr_t)p + sizeof(HostBlock) + 4095) & ~(uintptr_t)4095;
+  *((HostBlock*)a - 1) = HostBlock{p, total};
   return (void*)a;
 }
 
 void mt_host_free(void* p) {
-  if (p) cudaFreeHost(((void**)p)[-1]);
+  if (p) cudaFreeHost(((const HostBlock*)p - 1)->base);
 }
 
 int mt_debug_inject_fault(mt_ctx* ctx, int kind, int nth) {

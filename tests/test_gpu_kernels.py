@@ -229,6 +229,49 @@ def test_attention_growing_scores_rescale_per_warp():
     assert np.max(np.abs(from_dev(LSE) - lse_ref)) < 2e-3 * np.max(np.abs(lse_ref))
 
 
+@pytest.mark.parametrize("d,nq,nkv", [(128, 4, 2), (64, 4, 4), (16, 4, 2)])
+def test_qkv_gemm_with_fused_rope(d, nq, nkv):
+    """q|k|v = a W^T with RoPE on the q and k heads in the epilogue, against
+    the oracle's product followed by its rotation."""
+    torch, mt = need_gpu()
+    B, S, h, theta = 2, 150, 256, 5e5
+    N = (nq + 2 * nkv) * d
+    A, a32 = to_dev_bf16(torch, _normal((B * S, h), 91))
+    W, w32 = to_dev_bf16(torch, _normal((N, h), 92, 0.05))
+    C = torch.empty((B * S, N), dtype=torch.bfloat16, device="cuda")
+    tab = torch.empty(S * d, device="cuda")
+    mt.mt_op_gemm_rope(A, W, C, B * S, N, h, h, h, N, tab, S, d, theta, (nq + nkv) * d)
+    ref = oracle.matmul("nt", a32, w32).reshape(B, S, nq + 2 * nkv, d)
+    ref_rot = ref.copy()
+    ref_rot[:, :, :nq + nkv] = oracle.rope(ref[:, :, :nq + nkv], theta)
+    assert rel_l2(from_dev(C).reshape(B, S, -1, d), ref_rot) < 6e-3
+
+
+@pytest.mark.parametrize("d", [128, 64, 16])
+def test_attention_backward_with_fused_inverse_rope(d):
+    """dq, dk of the RoPE'd attention come out rotated back: compare with the
+    oracle's attention backward followed by its inverse rotation."""
+    torch, mt = need_gpu()
+    B, S, nq, nkv, theta = 2, 150, 4, 2, 1e4
+    q, k, v, do = (_normal((B, S, n, d), 95 + i) for i, n in enumerate((nq, nkv, nkv, nq)))
+    Q, q32 = to_dev_bf16(torch, q)
+    Kd, k32 = to_dev_bf16(torch, k)
+    Vd, v32 = to_dev_bf16(torch, v)
+    DO, do32 = to_dev_bf16(torch, do)
+    O = torch.empty((B, S, nq, d), dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((B, nq, S), device="cuda")
+    mt.mt_op_attention_fwd(Q, Kd, Vd, O, LSE, B, S, nq, nkv, d, nq * d, nkv * d, nq * d)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(Kd), torch.empty_like(Vd)
+    ws = torch.empty(mt.mt_op_attention_bwd_workspace(B, S, nq), device="cuda")
+    tab = torch.empty(S * d, device="cuda")
+    mt.mt_op_attention_bwd_rope(Q, Kd, Vd, O, DO, LSE, dQ, dK, dV, ws, B, S, nq, nkv, d, nq * d, nkv * d, nq * d,
+                                tab, theta)
+    _, _, dq_ref, dk_ref, dv_ref = oracle.attention(q32, k32, v32, do32)
+    assert rel_l2(from_dev(dQ), oracle.rope(dq_ref, theta, -1)) < 2e-2
+    assert rel_l2(from_dev(dK), oracle.rope(dk_ref, theta, -1)) < 2e-2
+    assert rel_l2(from_dev(dV), dv_ref) < 2e-2
+
+
 def test_lmhead_cross_entropy():
     torch, mt = need_gpu()
     T, V, h = 96, 1000, 128
