@@ -253,6 +253,22 @@ int mt_op_rope(void* x, float* table, int B, int S, int row_stride, int head0, i
 int mt_op_gemm_rope(const void* A, const void* W, void* C, int M, int N, int K, int lda, int ldb, int ldc,
                     float* table, int S, int d, float theta, int rope_cols, void* stream);
 
+/* Gate-up projection with SwiGLU fused into the epilogue. W holds the gate
+ * rows [0, F) and the up rows [u_off, u_off + F) of one [u_off + F, K]
+ * matrix (bf16, row stride ldb). For X[M,K] (row stride lda) it writes
+ *   gu[m, f] = bf16(g), gu[m, u_off + f] = bf16(u)   (gu row stride 2*u_off),
+ *   act[m, f] = bf16(silu(g) * u)                     (act row stride u_off),
+ * g = X Wg^T and u = X Wu^T in fp32; u_off must be a multiple of 8, >= F. */
+int mt_op_gemm_swiglu(const void* X, const void* W, void* gu, void* act, int M, int F, int K, int lda, int ldb,
+                      int u_off, void* stream);
+
+/* Down-projection input gradient with the SwiGLU backward fused: dact =
+ * dY[M,K] Wd where Wd is stored [K, F] (row stride ldb); with g, u read from
+ * gu (layout as above), gu is overwritten in place by
+ * dg = dact*u*silu'(g), du = dact*silu(g) (dact is never stored). */
+int mt_op_gemm_swiglu_bwd(const void* dY, const void* Wd, void* gu, int M, int F, int K, int lda, int ldb, int u_off,
+                          void* stream);
+
 /* Causal GQA attention forward on bf16 q/k/v/o with row strides (elements):
  * q [B*S, ldq] heads at columns j*d, k/v [B*S, ldkv], o [B*S, ldo];
  * lse fp32 [B, n_heads, S] (natural-log logsumexp of the scaled scores). */

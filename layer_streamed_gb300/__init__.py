@@ -41,7 +41,7 @@ EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_crea
            "mt_last_error",
            "mt_destroy", "mt_host_alloc", "mt_host_free", "mt_debug_inject_fault", "mt_op_gemm",
            "mt_op_rmsnorm_fwd", "mt_op_rmsnorm_bwd_workspace", "mt_op_rmsnorm_bwd", "mt_op_rmsnorm_bwd_noalloc",
-           "mt_op_rope", "mt_op_gemm_rope", "mt_op_attention_bwd_rope",
+           "mt_op_rope", "mt_op_gemm_rope", "mt_op_attention_bwd_rope", "mt_op_gemm_swiglu", "mt_op_gemm_swiglu_bwd",
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
            "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error")
 
@@ -121,6 +121,8 @@ def lib() -> ctypes.CDLL:
         "mt_op_gemm_rope": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, i32, i32, f32, i32, vp]),
         "mt_op_attention_bwd_rope": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
                                            i32, vp, f32, vp]),
+        "mt_op_gemm_swiglu": (i32, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
+        "mt_op_gemm_swiglu_bwd": (i32, [vp, vp, vp, i32, i32, i32, i32, i32, i32, vp]),
         "mt_op_attention_fwd": (i32, [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32, i32, vp]),
         "mt_op_attention_bwd_workspace": (sz, [i32, i32, i32]),
         "mt_op_attention_bwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
@@ -391,6 +393,15 @@ def mt_op_attention_bwd_rope(q, k, v, o, do, lse, dq, dk, dv, workspace, B, S, n
     _check(lib().mt_op_attention_bwd_rope(_ptr(q), _ptr(k), _ptr(v), _ptr(o), _ptr(do), _ptr(lse), _ptr(dq),
                                           _ptr(dk), _ptr(dv), _ptr(workspace), B, S, nq, nkv, d, ldq, ldkv, ldo,
                                           _ptr(table), theta, _stream(stream)))
+
+
+def mt_op_gemm_swiglu(X, W, gu, act, M, F, K, lda, ldb, u_off, stream=None):
+    _check(lib().mt_op_gemm_swiglu(_ptr(X), _ptr(W), _ptr(gu), _ptr(act), M, F, K, lda, ldb, u_off,
+                                   _stream(stream)))
+
+
+def mt_op_gemm_swiglu_bwd(dY, Wd, gu, M, F, K, lda, ldb, u_off, stream=None):
+    _check(lib().mt_op_gemm_swiglu_bwd(_ptr(dY), _ptr(Wd), _ptr(gu), M, F, K, lda, ldb, u_off, _stream(stream)))
 
 
 def mt_op_attention_fwd(q, k, v, o, lse, B, S, nq, nkv, d, ldq, ldkv, ldo, stream=None):

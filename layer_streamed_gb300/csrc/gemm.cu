@@ -140,6 +140,84 @@ __device__ __forceinline__ void rope_epilogue(const GemmParams& p, uint32_t tbas
   }
 }
 
+__device__ __forceinline__ float silu_sig(float g) { return 1.f / (1.f + __expf(-g)); }
+
+__device__ __forceinline__ void load_bf16_32(const uint16_t* src, float (&v)[32], int col0, int N, bool vec) {
+  if (vec && col0 + 32 <= N) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const uint4 w = ((const uint4*)src)[k];
+      const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[8 * k + 2 * e] = bf2f(ws[e] & 0xffff);
+        v[8 * k + 2 * e + 1] = bf2f(ws[e] >> 16);
+      }
+    }
+  } else {
+    for (int j = 0; j < 32; ++j) v[j] = col0 + j < N ? bf2f(src[j]) : 0.f;
+  }
+}
+
+// Gated epilogue: TMEM columns [0, BN/2) hold g, [BN/2, BN) hold u for the
+// features [f0, f0 + BN/2); act = silu(g) * u is formed from the fp32
+// accumulators before rounding.
+template <int BN>
+__device__ __forceinline__ void gated_epilogue(const GemmParams& p, uint32_t tbase, int row, bool row_ok, int f0) {
+  uint16_t* grow = (uint16_t*)p.C + (size_t)row * p.ldc;
+  uint16_t* arow = p.act + (size_t)row * p.ld_act;
+#pragma unroll 1
+  for (int c = 0; c < BN / 64; ++c) {
+    uint32_t rg[32], ru[32];
+    __syncwarp();
+    tmem_ld32(tbase + c * 32, rg);
+    tmem_ld32(tbase + BN / 2 + c * 32, ru);
+    tmem_ld_wait();
+    const int col0 = f0 + c * 32;
+    if (!row_ok || col0 >= p.N) continue;
+    float g[32], u[32], a[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      g[i] = __uint_as_float(rg[i]);
+      u[i] = __uint_as_float(ru[i]);
+      a[i] = g[i] * silu_sig(g[i]) * u[i];
+    }
+    store_bf16_32(grow + col0, g, col0, p.N, p.vec);
+    store_bf16_32(grow + p.u_col + col0, u, col0, p.N, p.vec);
+    store_bf16_32(arow + col0, a, col0, p.N, p.vec);
+  }
+}
+
+// SwiGLU backward epilogue: the accumulator is dact for features
+// [n0, n0 + BN); g and u are read from gu and replaced by dg and du.
+template <int BN>
+__device__ __forceinline__ void swiglu_bwd_epilogue(const GemmParams& p, uint32_t tbase, int row, bool row_ok,
+                                                    int n0) {
+  uint16_t* gurow = p.gu + (size_t)row * p.ld_gu;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t rd[32];
+    __syncwarp();
+    tmem_ld32(tbase + c * 32, rd);
+    tmem_ld_wait();
+    const int col0 = n0 + c * 32;
+    if (!row_ok || col0 >= p.N) continue;
+    float g[32], u[32];
+    load_bf16_32(gurow + col0, g, col0, p.N, p.vec);
+    load_bf16_32(gurow + p.u_col + col0, u, col0, p.N, p.vec);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) {
+      const float d = __uint_as_float(rd[i]);
+      const float sg = silu_sig(g[i]);
+      const float dg = d * u[i] * sg * (1.f + g[i] * (1.f - sg));
+      u[i] = d * g[i] * sg;  // du
+      g[i] = dg;
+    }
+    store_bf16_32(gurow + col0, g, col0, p.N, p.vec);
+    store_bf16_32(gurow + p.u_col + col0, u, col0, p.N, p.vec);
+  }
+}
+
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
@@ -181,7 +259,8 @@ __global__ void __launch_bounds__(192, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int num_m = (p.M + BM - 1) / BM, num_n = (p.N + BN - 1) / BN;
+  const int tile_n = p.gated ? BN / 2 : BN;  // gated tiles cover BN/2 features (gate + up halves)
+  const int num_m = (p.M + BM - 1) / BM, num_n = (p.N + tile_n - 1) / tile_n;
   const int num_tiles = num_m * num_n;
   const int num_kb = (p.K + BK - 1) / BK;
 
@@ -192,7 +271,7 @@ __global__ void __launch_bounds__(192, 1)
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
         int mb, nb;
         tile_coords(tile, num_m, num_n, p.group_m, mb, nb);
-        const int m0 = mb * BM, n0 = nb * BN;
+        const int m0 = mb * BM, n0 = nb * tile_n;
         for (int kb = 0; kb < num_kb; ++kb) {
           mbar_wait(&empty[stage], phase ^ 1, abort_flag, kErrTimeoutTma);
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
@@ -204,7 +283,10 @@ __global__ void __launch_bounds__(192, 1)
 #pragma unroll
             for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * 8192, &tmA, &full[stage], m0 + 64 * j, kb * BK);
           }
-          if (!B_MN) {
+          if (!B_MN && p.gated) {  // gate rows then the matching up rows
+            tma_load_2d(b_dst, &tmB, &full[stage], kb * BK, n0);
+            tma_load_2d(b_dst + (BN / 2) * 128, &tmB, &full[stage], kb * BK, p.u_off + n0);
+          } else if (!B_MN) {
             tma_load_2d(b_dst, &tmB, &full[stage], kb * BK, n0);
           } else {
 #pragma unroll
@@ -263,8 +345,11 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int row = mb * BM + q * 32 + lane;
       const bool row_ok = row < p.M;
-      if (p.rope_tab) {
-        rope_epilogue<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, row, row_ok, nb * BN);
+      if (p.rope_tab || p.gated || p.swiglu_bwd) {
+        const uint32_t tb = tmem_base + ((q * 32) << 16) + acc * BN;
+        if (p.rope_tab) rope_epilogue<BN>(p, tb, row, row_ok, nb * BN);
+        else if (p.gated) gated_epilogue<BN>(p, tb, row, row_ok, nb * tile_n);
+        else swiglu_bwd_epilogue<BN>(p, tb, row, row_ok, nb * BN);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -387,15 +472,22 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
     const int gm = (int)std::max<size_t>(1, band_budget / band);
     p.group_m = gm < num_m ? gm : num_m;
   }
-  // BN = 256 unless that leaves most SMs idle.
+  if (p.gated && (mode != GEMM_NT || !p.act || (p.ld_act & 7) || (p.u_col & 7) || p.epi != EPI_BF16)) return -1;
+  if (p.swiglu_bwd && (mode != GEMM_NN || !p.gu || (p.ld_gu & 7) || (p.u_col & 7))) return -1;
+  if (p.swiglu_bwd) p.vec = (((uintptr_t)p.gu & 15) == 0) ? 1 : 0;
+  if (p.gated) p.vec = p.vec && (((uintptr_t)p.act & 15) == 0);
+  // BN = 256 unless that leaves most SMs idle (gated tiles are always 256 wide).
   const int tiles256 = ((p.M + BM - 1) / BM) * ((p.N + 255) / 256);
-  const bool wide = tiles256 >= mt_host::num_sms();
+  const bool wide = tiles256 >= mt_host::num_sms() || p.gated;
   const int BN = wide ? 256 : 128;
   CUtensorMap ta, tb;
   int rc = 0;
   if (mode == GEMM_NT) {  // A [M,K] K-major, B [N,K] K-major
     rc |= make_map(&ta, A, p.M, p.K, lda, 64, BM);
-    rc |= make_map(&tb, B, p.N, p.K, ldb, 64, BN);
+    if (p.gated)  // gate and up rows of one combined matrix, 128-row boxes
+      rc |= make_map(&tb, B, p.u_off + p.N, p.K, ldb, 64, 128);
+    else
+      rc |= make_map(&tb, B, p.N, p.K, ldb, 64, BN);
     if (rc) return -1;
     return wide ? launch<256, false, false>(ta, tb, p, st) : launch<128, false, false>(ta, tb, p, st);
   }

@@ -29,6 +29,17 @@ struct GemmParams {
   // position row % rope_S before the single rounding to bf16.
   const float2* rope_tab = nullptr;
   int rope_S = 0, rope_d = 0, rope_cols = 0;
+  // Gated (SwiGLU) forward, mode NT only: each 256-wide tile is rows
+  // [f0, f0+128) of B (gate) and rows [u_off + f0, u_off + f0 + 128) (up);
+  // N counts features. The epilogue writes g to C column f, u to C column
+  // u_col + f (bf16) and act = silu(g) * u to act[row * ld_act + f].
+  int gated = 0, u_off = 0, u_col = 0, ld_act = 0;
+  uint16_t* act = nullptr;
+  // SwiGLU backward epilogue (mode NN, bf16 C unused): the accumulator is
+  // dact; g, u are read from gu (row stride ld_gu, up at column u_col) and
+  // replaced in place by dg = dact*u*silu'(g), du = dact*silu(g).
+  int swiglu_bwd = 0, ld_gu = 0;
+  uint16_t* gu = nullptr;
 };
 
 // C[M,N] = op(A) op(B) with bf16 operands, fp32 accumulation (see gemm.cu).

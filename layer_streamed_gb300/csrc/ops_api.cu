@@ -67,6 +67,29 @@ int mt_op_gemm_rope(const void* A, const void* W, void* C, int M, int N, int K, 
   return rc(gemm_bf16(GEMM_NT, p, A, W, lda, ldb, S(stream)));
 }
 
+int mt_op_gemm_swiglu(const void* X, const void* W, void* gu, void* act, int M, int F, int K, int lda, int ldb,
+                      int u_off, void* stream) {
+  if (!X || !W || !gu || !act || u_off < F) return MT_ERR_ARG;
+  GemmParams p{M, F, K, EPI_BF16, gu, nullptr, 2 * u_off, 0, 1};
+  p.gated = 1;
+  p.u_off = u_off;
+  p.u_col = u_off;
+  p.act = (uint16_t*)act;
+  p.ld_act = u_off;
+  return rc(gemm_bf16(GEMM_NT, p, X, W, lda, ldb, S(stream)));
+}
+
+int mt_op_gemm_swiglu_bwd(const void* dY, const void* Wd, void* gu, int M, int F, int K, int lda, int ldb, int u_off,
+                          void* stream) {
+  if (!dY || !Wd || !gu || u_off < F) return MT_ERR_ARG;
+  GemmParams p{M, F, K, EPI_BF16, gu, nullptr, 2 * u_off, 0, 1};
+  p.swiglu_bwd = 1;
+  p.gu = (uint16_t*)gu;
+  p.ld_gu = 2 * u_off;
+  p.u_col = u_off;
+  return rc(gemm_bf16(GEMM_NN, p, dY, Wd, lda, ldb, S(stream)));
+}
+
 int mt_op_attention_fwd(const void* q, const void* k, const void* v, void* o, float* lse, int B, int S_, int n_heads,
                         int n_kv_heads, int d, int ldq, int ldkv, int ldo, void* stream) {
   if (!q || !k || !v || !o || !lse) return MT_ERR_ARG;

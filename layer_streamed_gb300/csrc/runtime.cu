@@ -454,6 +454,19 @@ struct OpTimer {
   }
 };
 
+int gemm_p(mt_ctx* ctx, int mode, const GemmParams& p, const void* A, const void* B, int lda, int ldb,
+           double flop) {
+  OpTimer timer(ctx, 0, flop);
+  if (gemm_bf16(mode, p, A, B, lda, ldb, ctx->s_comp) != 0) {
+    cudaError_t e = cudaGetLastError();
+    char buf[256];
+    snprintf(buf, sizeof buf, "gemm mode %d M=%d N=%d K=%d lda=%d ldb=%d ldc=%d failed: %s", mode, p.M, p.N, p.K, lda,
+             ldb, p.ldc, cudaGetErrorString(e));
+    return set_err(ctx, e != cudaSuccess ? MT_ERR_CUDA : MT_ERR_ARG, buf);
+  }
+  return MT_OK;
+}
+
 int gemm(mt_ctx* ctx, int mode, int epi, const void* A, const void* B, void* C, const void* add, int M, int N, int K,
          int lda, int ldb, int ldc, int rope_S = 0, int rope_cols = 0) {
   GemmParams p{M, N, K, epi, C, add, ldc, 0, 1};
@@ -463,15 +476,7 @@ int gemm(mt_ctx* ctx, int mode, int epi, const void* A, const void* B, void* C, 
     p.rope_d = ctx->P.d;
     p.rope_cols = rope_cols;
   }
-  OpTimer timer(ctx, 0, 2.0 * M * N * K);
-  if (gemm_bf16(mode, p, A, B, lda, ldb, ctx->s_comp) != 0) {
-    cudaError_t e = cudaGetLastError();
-    char buf[256];
-    snprintf(buf, sizeof buf, "gemm mode %d M=%d N=%d K=%d lda=%d ldb=%d ldc=%d failed: %s", mode, M, N, K, lda, ldb,
-             ldc, cudaGetErrorString(e));
-    return set_err(ctx, e != cudaSuccess ? MT_ERR_CUDA : MT_ERR_ARG, buf);
-  }
-  return MT_OK;
+  return gemm_p(ctx, mode, p, A, B, lda, ldb, 2.0 * M * N * K);
 }
 
 #define CKR(x)              \
@@ -663,8 +668,15 @@ int layer_forward(Step& st, int l, const LayerView& w) {
   }
   CKR(gemm(ctx, GEMM_NT, EPI_F32_ADD, a.o, w.wo, a.hmid, x, T, h, p.qd, p.qd, p.qd, h));
   CKL(rmsnorm_fwd(a.hmid, w.w2, a.m, a.rstd2, T, h, ctx->cfg.norm_eps, s));
-  CKR(gemm(ctx, GEMM_NT, EPI_BF16, a.m, w.wgu, a.gu, nullptr, T, 2 * p.Fp, h, h, h, 2 * p.Fp));
-  CKL(swiglu_fwd(a.gu, a.act, T, p.F, p.Fp, s));
+  {  // gate-up projection with SwiGLU fused: g, u (kept for the backward) and act = silu(g) u
+    GemmParams gp{T, p.Fp, h, EPI_BF16, a.gu, nullptr, 2 * p.Fp, 0, 1};
+    gp.gated = 1;
+    gp.u_off = p.Fp;
+    gp.u_col = p.Fp;
+    gp.act = a.act;
+    gp.ld_act = p.Fp;
+    CKR(gemm_p(ctx, GEMM_NT, gp, a.m, w.wgu, h, h, 2.0 * T * 2 * p.Fp * h));
+  }
   CKR(gemm(ctx, GEMM_NT, EPI_F32_ADD, a.act, w.wd, y, a.hmid, T, h, p.Fp, p.Fp, w.ldd, h));
   return MT_OK;
 }
@@ -706,8 +718,14 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   auto GT = [&](int t) { return (float*)((uint8_t*)G + (ctx->off_g[l][t] - u0)); };
   // h_out = h_mid + act Wd^T
   CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dh_b, a.act, GT(8), nullptr, h, F, T, h, Fp, F));
-  CKR(gemm(ctx, GEMM_NN, EPI_BF16, ctx->dh_b, w.wd, a.act, nullptr, T, Fp, h, h, w.ldd, Fp));  // dact -> act slot
-  CKL(swiglu_bwd(a.gu, a.act, T, F, Fp, s));                                                   // gu <- dgu
+  {  // dact = dh Wd, turned into (dg, du) in place over (g, u) by the epilogue
+    GemmParams bp{T, Fp, h, EPI_BF16, a.gu, nullptr, 2 * Fp, 0, 1};
+    bp.swiglu_bwd = 1;
+    bp.gu = a.gu;
+    bp.ld_gu = 2 * Fp;
+    bp.u_col = Fp;
+    CKR(gemm_p(ctx, GEMM_NN, bp, ctx->dh_b, w.wd, h, w.ldd, 2.0 * T * Fp * h));
+  }
   if (Fp == F) {
     CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, 2 * F, h, T, 2 * Fp, h, h));
   } else {

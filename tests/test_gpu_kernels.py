@@ -272,6 +272,47 @@ def test_attention_backward_with_fused_inverse_rope(d):
     assert rel_l2(from_dev(dV), dv_ref) < 2e-2
 
 
+@pytest.mark.parametrize("M,F,K,u_off", [(300, 384, 256, 384), (130, 172, 64, 176), (2048, 1536, 512, 1536)])
+def test_gated_gemm_fuses_swiglu(M, F, K, u_off):
+    """g|u = x [Wg;Wu]^T with act = silu(g) u formed from the fp32 products."""
+    torch, mt = need_gpu()
+    X, x32 = to_dev_bf16(torch, _normal((M, K), 101))
+    Wst = np.zeros((2 * u_off, K), np.float32)
+    Wst[:F] = _normal((F, K), 102, 0.05)
+    Wst[u_off:u_off + F] = _normal((F, K), 103, 0.05)
+    W, w32 = to_dev_bf16(torch, Wst)
+    GU = torch.zeros((M, 2 * u_off), dtype=torch.bfloat16, device="cuda")
+    ACT = torch.zeros((M, u_off), dtype=torch.bfloat16, device="cuda")
+    mt.mt_op_gemm_swiglu(X, W, GU, ACT, M, F, K, K, K, u_off)
+    g = oracle.matmul("nt", x32, w32[:F])
+    u = oracle.matmul("nt", x32, w32[u_off:u_off + F])
+    a_ref, _, _ = oracle.swiglu(g, u)
+    gu = from_dev(GU)
+    assert rel_l2(gu[:, :F], g) < 6e-3
+    assert rel_l2(gu[:, u_off:u_off + F], u) < 6e-3
+    assert rel_l2(from_dev(ACT)[:, :F], a_ref) < 6e-3
+
+
+@pytest.mark.parametrize("M,F,K,u_off", [(300, 384, 256, 384), (130, 172, 64, 176)])
+def test_down_dgrad_fuses_swiglu_backward(M, F, K, u_off):
+    """dact = dY Wd with (g, u) replaced in place by (dg, du) from fp32 dact."""
+    torch, mt = need_gpu()
+    dY, dy32 = to_dev_bf16(torch, _normal((M, K), 111))
+    Wd_st = np.zeros((K, u_off), np.float32)
+    Wd_st[:, :F] = _normal((K, F), 112, 0.05)
+    Wd, wd32 = to_dev_bf16(torch, Wd_st)
+    gu0 = np.zeros((M, 2 * u_off), np.float32)
+    gu0[:, :F] = _normal((M, F), 113)
+    gu0[:, u_off:u_off + F] = _normal((M, F), 114)
+    GU, gu32 = to_dev_bf16(torch, gu0)
+    mt.mt_op_gemm_swiglu_bwd(dY, Wd, GU, M, F, K, K, u_off, u_off)
+    dact = oracle.matmul("nn", dy32, wd32[:, :F])
+    _, dg_ref, du_ref = oracle.swiglu(gu32[:, :F], gu32[:, u_off:u_off + F], dact)
+    out = from_dev(GU)
+    assert rel_l2(out[:, :F], dg_ref) < 6e-3
+    assert rel_l2(out[:, u_off:u_off + F], du_ref) < 6e-3
+
+
 def test_lmhead_cross_entropy():
     torch, mt = need_gpu()
     T, V, h = 96, 1000, 128
