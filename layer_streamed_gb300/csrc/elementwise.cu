@@ -306,6 +306,27 @@ __global__ void embed_scatter_kernel(const int32_t* __restrict__ perm, const int
   }
 }
 
+// Compact form: one block per distinct token id u (rows perm[start[u] ..
+// start[u+1]) in ascending position order); the row sum goes to row u of
+// the dense [n_ids, h] output.
+__global__ void embed_scatter_rows_kernel(const int32_t* __restrict__ perm, const int32_t* __restrict__ start,
+                                          const float* __restrict__ dh0, float* __restrict__ rows, int h) {
+  const int u = blockIdx.x;
+  const int s0 = start[u], s1 = start[u + 1];
+  float4* dst = (float4*)(rows + (size_t)u * h);
+  for (int i = threadIdx.x; i < h / 4; i += blockDim.x) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int j = s0; j < s1; ++j) {
+      const float4 g = ((const float4*)(dh0 + (size_t)perm[j] * h))[i];
+      acc.x += g.x;
+      acc.y += g.y;
+      acc.z += g.z;
+      acc.w += g.w;
+    }
+    dst[i] = acc;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Casts
 // ---------------------------------------------------------------------------
@@ -316,6 +337,13 @@ __global__ void cast_rows_kernel(const float* __restrict__ src, uint16_t* __rest
   const size_t r = idx / ld;
   const int c = (int)(idx % ld);
   dst[idx] = (c < cols && r < (size_t)rows_src) ? f2bf(src[r * cols + c]) : (uint16_t)0;
+}
+
+__global__ void cast_bf16_f32_vec_kernel(const uint2* __restrict__ src, float4* __restrict__ dst, size_t n4) {
+  const size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n4) return;
+  const uint2 u = src[i];
+  dst[i] = make_float4(bf2f(u.x & 0xffff), bf2f(u.x >> 16), bf2f(u.y & 0xffff), bf2f(u.y >> 16));
 }
 
 __global__ void cast_f32_bf16_vec_kernel(const float4* __restrict__ src, uint2* __restrict__ dst, size_t n4) {
@@ -495,6 +523,14 @@ int embed_scatter(const int32_t* perm, const int32_t* start, int row0, int rows,
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
+int embed_scatter_rows(const int32_t* perm, const int32_t* start, int n_ids, const float* dh0, float* rows, int h,
+                       cudaStream_t st) {
+  if (n_ids <= 0 || (h & 3)) return -1;
+  embed_scatter_rows_kernel<<<n_ids, 256, 0, st>>>(perm, start, dh0, rows, h);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
 int cast_rows_f32_bf16(const float* src, uint16_t* dst, int rows_src, int rows_dst, int cols, int ld_dst,
                        cudaStream_t st) {
   if (rows_src <= 0 || rows_dst < rows_src || cols <= 0 || ld_dst < cols) return -1;
@@ -507,6 +543,13 @@ int cast_rows_f32_bf16(const float* src, uint16_t* dst, int rows_src, int rows_d
 int cast_f32_bf16(const float* src, uint16_t* dst, size_t n, cudaStream_t st) {
   if (n % 4) return -1;
   cast_f32_bf16_vec_kernel<<<blocks_for(n / 4, 256), 256, 0, st>>>((const float4*)src, (uint2*)dst, n / 4);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+int cast_bf16_f32(const uint16_t* src, float* dst, size_t n, cudaStream_t st) {
+  if (n % 4) return -1;
+  cast_bf16_f32_vec_kernel<<<blocks_for(n / 4, 256), 256, 0, st>>>((const uint2*)src, (float4*)dst, n / 4);
   count_launches(1);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

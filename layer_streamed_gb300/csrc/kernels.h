@@ -76,6 +76,12 @@ int embed_gather(const void* E_slice, bool bf16, int row0, int rows, const int32
 int embed_scatter(const int32_t* perm, const int32_t* start, int row0, int rows, const float* dh0, float* dE, int h,
                   cudaStream_t st);
 
+// Compact form over the n_ids distinct token ids: rows[u] = sum over the
+// positions perm[start[u] .. start[u+1]) of dh0 ([n_ids, h] fp32 output).
+int embed_scatter_rows(const int32_t* perm, const int32_t* start, int n_ids, const float* dh0, float* rows, int h,
+                       cudaStream_t st);
+int cast_bf16_f32(const uint16_t* src, float* dst, size_t n, cudaStream_t st);
+
 // Weight preparation: fp32 [rows_src, cols] -> bf16 [rows_dst, ld_dst]
 // (rows >= rows_src and columns >= cols are zero); bf16/fp32 gains -> fp32.
 int cast_rows_f32_bf16(const float* src, uint16_t* dst, int rows_src, int rows_dst, int cols, int ld_dst,

@@ -117,7 +117,7 @@ struct Plan {
   int L, h, nq, nkv, d, F, Fp, V, qd, kd, qkv, Tmax;
   size_t esz;
   // slicing of vocab-sized units
-  int head_rows, n_head_slices, emb_rows, n_emb_slices, embg_rows, n_embg_slices;
+  int head_rows, n_head_slices;
   // sizes
   size_t wbuf, wcast, gbuf, ckpt_one, act_layer, fixed_ws, dyn_max, total;
   // activation layout inside one block-arena slot (byte offsets)
@@ -162,14 +162,10 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
     }
   };
   slices((size_t)p.h * p.esz, layer_bytes, &p.head_rows, &p.n_head_slices);
-  slices((size_t)p.h * p.esz, layer_bytes, &p.emb_rows, &p.n_emb_slices);
   const size_t layer_grad_bytes = layer_bytes / p.esz * 4;
-  slices((size_t)p.h * 4, layer_grad_bytes, &p.embg_rows, &p.n_embg_slices);
-  p.wbuf = rup(std::max({layer_bytes, (size_t)p.head_rows * p.h * p.esz, (size_t)p.emb_rows * p.h * p.esz}), 4096);
+  p.wbuf = rup(std::max(layer_bytes, (size_t)p.head_rows * p.h * p.esz), 4096);
   p.wcast = p.esz == 4 ? rup(std::max(layer_cast_bytes(p), (size_t)p.head_rows * p.h * 2), 4096) : 0;
-  p.gbuf = rup(std::max({layer_grad_bytes, (size_t)p.head_rows * p.h * 4, (size_t)p.embg_rows * p.h * 4,
-                         (size_t)p.h * 4}),
-               4096);
+  p.gbuf = rup(std::max({layer_grad_bytes, (size_t)p.head_rows * p.h * 4, (size_t)p.h * 4}), 4096);
   const size_t T = p.Tmax, h = p.h;
   p.ckpt_one = rup(T * h * 4, 256);
   size_t a = 0;
@@ -209,7 +205,7 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   ws((size_t)p.n_head_slices * T * 8);             // CE partials
   ws(T * 4 * 3);                                   // zlab, lse, terms
   ws(256);                                         // loss
-  ws((T * 3 + p.V + 1) * 4);                       // tokens, labels, perm, start
+  ws((T * 5 + 1) * 4);                             // tokens, labels, perm, used ids, id ranges
   ws((size_t)c.max_seq * p.d / 2 * 8);             // rope table
   ws(2 * 2 * (size_t)p.h * 4);                     // gains of the two weight slots
   ws((size_t)p.h * 4 * 2);                         // final norm gain (raw + fp32)
@@ -225,7 +221,7 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
 }
 
 // One use of a streamed weight unit (or vocab slice) by the compute stream.
-enum ItemKind { IT_EMB = 0, IT_LAYER = 1, IT_HEAD = 2 };
+enum ItemKind { IT_LAYER = 1, IT_HEAD = 2 };
 struct Item {
   int kind, index;  // layer index 1..L, or slice index
   bool operator==(const Item& o) const { return kind == o.kind && index == o.index; }
@@ -266,10 +262,14 @@ struct mt_ctx {
   float *h_top, *dh, *dm, *attn_ws, *norm_ws, *rstd_f, *logits, *zlab, *lse, *terms, *loss_dev, *gains[2], *wf32;
   uint16_t *dh_b, *dhmid_b, *do_b, *dqkv, *xf_b, *dz;
   float2 *ce_part, *rope_tab;
-  int32_t *tok_d, *lab_d, *perm_d, *start_d;
+  int32_t *tok_d, *lab_d, *perm_d, *ids_d, *ids_start_d;
+  const void* host_params_dev = nullptr;  // device-side address of the bound host parameters
   void* wf_raw;
-  int32_t* host_stage = nullptr;  // pinned: tokens, labels, perm, start
+  int32_t* host_stage = nullptr;  // pinned: tokens, labels, perm, used ids, id ranges, loss
+  uint8_t* host_rows = nullptr;   // pinned staging: embedding rows of the tokens [T, h] (param dtype)
+  float* host_grad_rows = nullptr;  // pinned staging: embedding gradient rows of the used ids [T, h]
   int rope_S = -1;
+  std::vector<int32_t> csr;  // token-id counting sort (vocab + 1)
   const void* host_params = nullptr;
   std::string err;
   mt_stats stats{};
@@ -345,11 +345,12 @@ int carve(mt_ctx* ctx) {
   ctx->lse = (float*)take(T * 4);
   ctx->terms = (float*)take(T * 4);
   ctx->loss_dev = (float*)take(256);
-  int32_t* ints = (int32_t*)take((T * 3 + p.V + 1) * 4);
+  int32_t* ints = (int32_t*)take((T * 5 + 1) * 4);
   ctx->tok_d = ints;
   ctx->lab_d = ints + T;
   ctx->perm_d = ints + 2 * T;
-  ctx->start_d = ints + 3 * T;
+  ctx->ids_d = ints + 3 * T;
+  ctx->ids_start_d = ints + 4 * T;
   ctx->rope_tab = (float2*)take((size_t)ctx->cfg.max_seq * p.d / 2 * 8);
   ctx->gains[0] = (float*)take(2 * (size_t)p.h * 4);
   ctx->gains[1] = (float*)take(2 * (size_t)p.h * 4);
@@ -506,7 +507,6 @@ void plan_sequence(Step& st) {
   mt_ctx* ctx = st.ctx;
   const Plan& p = ctx->P;
   auto& q = st.seq;
-  for (int s = 0; s < p.n_emb_slices; ++s) q.push_back({IT_EMB, s});
   for (int l = 1; l <= p.L; ++l) q.push_back({IT_LAYER, l});
   for (int s = 0; s < p.n_head_slices; ++s) q.push_back({IT_HEAD, s});
   for (int s = p.n_head_slices - 1; s >= 0; --s) q.push_back({IT_HEAD, s});
@@ -552,10 +552,6 @@ int issue_load(Step& st, size_t i) {
     const int l = std::abs(it.index);
     src_off = ctx->off_p[l][0];
     bytes = ctx->off_p[l][8] + tensor_numel(ctx->cfg, l, 8) * p.esz - src_off;
-  } else if (it.kind == IT_EMB) {
-    const int r0 = it.index * p.emb_rows, rows = std::min(p.emb_rows, p.V - r0);
-    src_off = ctx->off_p[0][0] + (size_t)r0 * p.h * p.esz;
-    bytes = (size_t)rows * p.h * p.esz;
   } else {
     const int r0 = it.index * p.head_rows, rows = std::min(p.head_rows, p.V - r0);
     src_off = ctx->off_p[L + 1][1] + (size_t)r0 * p.h * p.esz;
@@ -783,18 +779,54 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   const int T = st.T, h = p.h, L = p.L;
   cudaStream_t s = ctx->s_comp;
 
-  // Host preparation: stable counting sort of token ids for the
-  // deterministic embedding scatter.
+  // The embedding gradient region of the host buffer is cleared by CPU
+  // threads while the GPU works; the rows of used tokens are written into it
+  // after the step has drained.
+  std::vector<std::thread> zeroers;
+  {
+    uint8_t* eg = (uint8_t*)st.host_grad + ctx->off_g[0][0];
+    const size_t nbytes = (size_t)p.V * h * 4;
+    const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
+    const size_t nthr = std::min<size_t>(std::max(1u, hw / 2), std::max<size_t>(1, nbytes >> 26));
+    const size_t chunk = (nbytes / nthr + 4095) & ~(size_t)4095;
+    for (size_t i = 0; i < nthr; ++i) {
+      const size_t b = i * chunk;
+      if (b >= nbytes) break;
+      const size_t n = std::min(chunk, nbytes - b);
+      zeroers.emplace_back([eg, b, n] { std::memset(eg + b, 0, n); });
+    }
+  }
+  struct Joiner {
+    std::vector<std::thread>& t;
+    ~Joiner() {
+      for (auto& x : t)
+        if (x.joinable()) x.join();
+    }
+  } joiner{zeroers};
+
+  // Host preparation: stable counting sort of token ids (positions grouped
+  // by id in ascending position order) and the list of distinct ids with
+  // their ranges, for the deterministic embedding gradient.
   int32_t* hs = ctx->host_stage;
   std::memcpy(hs, tokens, (size_t)T * 4);
   std::memcpy(hs + T, labels, (size_t)T * 4);
   int32_t* perm = hs + 2 * T;
-  int32_t* start = hs + 3 * T;
-  std::memset(start, 0, (size_t)(p.V + 1) * 4);
+  int32_t* ids = hs + 3 * T;
+  int32_t* ranges = hs + 4 * T;
+  std::vector<int32_t>& start = ctx->csr;
+  start.assign((size_t)p.V + 1, 0);
   for (int t = 0; t < T; ++t) start[tokens[t] + 1]++;
   for (int v = 0; v < p.V; ++v) start[v + 1] += start[v];
+  int n_ids = 0;
+  for (int v = 0; v < p.V; ++v)
+    if (start[v + 1] > start[v]) {
+      ids[n_ids] = v;
+      ranges[n_ids] = start[v];
+      ++n_ids;
+    }
+  ranges[n_ids] = T;
   {
-    std::vector<int32_t> fill(start, start + p.V);
+    std::vector<int32_t> fill(start.begin(), start.end() - 1);
     for (int t = 0; t < T; ++t) perm[fill[tokens[t]]++] = t;
   }
   ctx->segs.clear();
@@ -808,7 +840,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   // Fresh step: the previous step fully drained, so every buffer is free.
   if (ctx->trace) CK(cudaEventRecord(ctx->ev_base, s));
   cudaGetLastError();
-  CK(cudaMemcpyAsync(ctx->tok_d, hs, (size_t)(3 * T + p.V + 1) * 4, cudaMemcpyHostToDevice, s));
+  CK(cudaMemcpyAsync(ctx->tok_d, hs, (size_t)(5 * T + 1) * 4, cudaMemcpyHostToDevice, s));
   // The copy streams wait for the step start so that their timestamps are
   // ordered after the base event and no buffer of the previous step is live.
   cudaEvent_t ev_start = next_event(ctx);
@@ -834,6 +866,42 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   const size_t n = st.seq.size();
   ctx->stats.n_units = (int)n;
   if (st.needs_load[0]) CKR(issue_load(st, 0));
+
+  // Embedding: h_0 = E[tok]. CPU threads gather the T rows from the host
+  // table into a contiguous pinned buffer (the first layer's weights are
+  // already streaming), then one copy brings them to the device.
+  {
+    const size_t row_bytes = (size_t)h * p.esz;
+    const uint8_t* E = (const uint8_t*)ctx->host_params + ctx->off_p[0][0];
+    uint8_t* dst = ctx->host_rows;
+    const int nthr = (int)std::min<unsigned>(8, std::max(1u, std::thread::hardware_concurrency() / 2));
+    std::vector<std::thread> gth;
+    const int per = (T + nthr - 1) / nthr;
+    for (int i = 0; i < nthr; ++i) {
+      const int t0 = i * per, t1 = std::min(T, t0 + per);
+      if (t0 >= t1) break;
+      gth.emplace_back([=] {
+        for (int t = t0; t < t1; ++t) std::memcpy(dst + (size_t)t * row_bytes, E + (size_t)tokens[t] * row_bytes, row_bytes);
+      });
+    }
+    for (auto& x : gth) x.join();
+    // On the weight stream, queued right behind the first layer's copy (the
+    // copy engine serves one H2D stream at a time, so issuing it from the
+    // compute stream would put it behind the second layer's copy too).
+    void* land = p.esz == 4 ? (void*)ckpt(ctx, 0) : (void*)ctx->xf_b;
+    cudaEvent_t rows_in = next_event(ctx);
+    {
+      SegScope sg(ctx, 1, ctx->s_h2d, (double)T * row_bytes, -1);
+      CK(cudaMemcpyAsync(land, dst, (size_t)T * row_bytes, cudaMemcpyHostToDevice, ctx->s_h2d));
+    }
+    CK(cudaEventRecord(rows_in, ctx->s_h2d));
+    CK(cudaStreamWaitEvent(s, rows_in, 0));
+    if (p.esz == 2) {
+      SegScope sg(ctx, 0, s, 0, -1);
+      CKL(cast_bf16_f32(ctx->xf_b, ckpt(ctx, 0), (size_t)T * h, s));
+    }
+  }
+  ctx->stats.h2d_bytes += (double)T * h * p.esz;
   int head_pass2_count = 0;
   bool first_dxf = true;
   for (size_t i = 0; i < n; ++i) {
@@ -846,10 +914,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
     if (fresh) CK(cudaStreamWaitEvent(s, ctx->ev_wready[slot], 0));
     {
       SegScope sg(ctx, 0, s, 0, (int)i);
-      if (it.kind == IT_EMB) {
-        const int r0 = it.index * p.emb_rows, rows = std::min(p.emb_rows, p.V - r0);
-        CKL(embed_gather(ctx->wbuf[slot], p.esz == 2, r0, rows, ctx->tok_d, ckpt(ctx, 0), T, h, s));
-      } else if (it.kind == IT_LAYER) {
+      if (it.kind == IT_LAYER) {
         const int l = std::abs(it.index);
         LayerView w;
         CKR(bind_layer(st, l, slot, fresh, &w));
@@ -863,7 +928,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
         const uint16_t* W = bind_head(st, it.index, slot, fresh, &rows);
         if (!W) return set_err(ctx, MT_ERR_CUDA, "head cast failed");
         const int r0 = it.index * p.head_rows;
-        const bool pass2 = (int)i >= p.n_emb_slices + L + p.n_head_slices;
+        const bool pass2 = (int)i >= L + p.n_head_slices;
         if (!pass2) {
           if (it.index == 0) CKL(rmsnorm_fwd(ctx->h_top, ctx->wf32, ctx->xf_b, ctx->rstd_f, T, h, ctx->cfg.norm_eps, s));
           CKR(gemm(ctx, GEMM_NT, EPI_F32, ctx->xf_b, W, ctx->logits, nullptr, T, rows, h, h, h, p.head_rows));
@@ -896,19 +961,23 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
     if (ctx->serial && i + 1 < n && st.needs_load[i + 1]) CKR(issue_load(st, i + 1));
     if (ctx->debug_sync) CKR(debug_wait(ctx, i, it, slot, st.needs_load[i]));
   }
-  // Embedding backward: dense gradient slices from dh_0.
-  for (int sl = 0; sl < p.n_embg_slices; ++sl) {
-    const int r0 = sl * p.embg_rows, rows = std::min(p.embg_rows, p.V - r0);
-    int g;
-    CKR(grad_slot_begin(st, &g));
-    {
-      SegScope sg(ctx, 0, s, 0, (int)n + sl);
-      CKL(embed_scatter(ctx->perm_d, ctx->start_d, r0, rows, ctx->dh, ctx->gbuf[g], h, s));
-    }
-    CKR(grad_slot_end(st, g, ctx->off_g[0][0] + (size_t)r0 * h * 4, (size_t)rows * h * 4));
+  // Embedding backward: the gradient rows of the used ids (summed in
+  // position order) are packed densely, copied to a pinned staging buffer,
+  // and scattered into the cleared host gradient after the step drains.
+  {
+    SegScope sg(ctx, 0, s, 0, (int)n);
+    CKL(embed_scatter_rows(ctx->perm_d, ctx->ids_start_d, n_ids, ctx->dh, ctx->dm, h, s));
   }
+  cudaEvent_t emb_done = next_event(ctx);
+  CK(cudaEventRecord(emb_done, s));
+  CK(cudaStreamWaitEvent(ctx->s_d2h, emb_done, 0));
+  {
+    SegScope sg(ctx, 2, ctx->s_d2h, (double)n_ids * h * 4);
+    CK(cudaMemcpyAsync(ctx->host_grad_rows, ctx->dm, (size_t)n_ids * h * 4, cudaMemcpyDeviceToHost, ctx->s_d2h));
+  }
+  ctx->stats.d2h_bytes += (double)n_ids * h * 4;
   // Completion: the grad stream's last copy, and the loss.
-  float* loss_host = (float*)(ctx->host_stage + 3 * (size_t)p.Tmax + p.V + 1);
+  float* loss_host = (float*)(ctx->host_stage + 5 * (size_t)p.Tmax + 1);
   CK(cudaStreamWaitEvent(ctx->s_d2h, ctx->ev_wfree[0], 0));
   CK(cudaStreamWaitEvent(ctx->s_d2h, ctx->ev_wfree[1], 0));
   CK(cudaMemcpyAsync(loss_host, ctx->loss_dev, 4, cudaMemcpyDeviceToHost, ctx->s_d2h));
@@ -918,6 +987,23 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   CK(cudaEventRecord(ctx->ev_done, ctx->s_d2h));
   CKR(wait_event(ctx, ctx->ev_done, 3600.0));
   *loss_out = *loss_host;
+  // Scatter the embedding gradient rows into the (now cleared) host buffer.
+  for (auto& x : zeroers) x.join();
+  {
+    float* eg = (float*)((uint8_t*)st.host_grad + ctx->off_g[0][0]);
+    const float* src = ctx->host_grad_rows;
+    const int nthr = (int)std::min<unsigned>(8, std::max(1u, std::thread::hardware_concurrency() / 2));
+    std::vector<std::thread> sth;
+    const int per = (n_ids + nthr - 1) / nthr;
+    for (int i = 0; i < nthr; ++i) {
+      const int u0 = i * per, u1 = std::min(n_ids, u0 + per);
+      if (u0 >= u1) break;
+      sth.emplace_back([=] {
+        for (int u = u0; u < u1; ++u) std::memcpy(eg + (size_t)ids[u] * h, src + (size_t)u * h, (size_t)h * 4);
+      });
+    }
+    for (auto& x : sth) x.join();
+  }
   return MT_OK;
 }
 
@@ -1099,8 +1185,12 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
   if ((e = cudaEventCreateWithFlags(&ctx->ev_done, cudaEventDisableTiming)) != cudaSuccess ||
       (e = cudaEventCreate(&ctx->ev_base)) != cudaSuccess)
     return fail(MT_ERR_CUDA, "event create", e);
-  const size_t stage_ints = 3 * (size_t)ctx->P.Tmax + ctx->P.V + 1 + 64;
-  if ((e = cudaHostAlloc((void**)&ctx->host_stage, stage_ints * 4, cudaHostAllocDefault)) != cudaSuccess)
+  const size_t stage_ints = 5 * (size_t)ctx->P.Tmax + 1 + 64;
+  if ((e = cudaHostAlloc((void**)&ctx->host_stage, stage_ints * 4, cudaHostAllocDefault)) != cudaSuccess ||
+      (e = cudaHostAlloc((void**)&ctx->host_rows, (size_t)ctx->P.Tmax * ctx->P.h * ctx->P.esz, cudaHostAllocDefault)) !=
+          cudaSuccess ||
+      (e = cudaHostAlloc((void**)&ctx->host_grad_rows, (size_t)ctx->P.Tmax * ctx->P.h * 4, cudaHostAllocDefault)) !=
+          cudaSuccess)
     return fail(MT_ERR_CUDA, "cudaHostAlloc", e);
   if (carve(ctx) != MT_OK) {
     mt_destroy(ctx);
@@ -1129,7 +1219,13 @@ int mt_bind_host_params(mt_ctx* ctx, const void* host_params, mt_dtype dtype) {
     cudaGetLastError();
     return set_err(ctx, MT_ERR_NOT_PINNED, "host params are not page-locked CUDA host memory");
   }
+  void* dev = nullptr;
+  if (cudaHostGetDevicePointer(&dev, const_cast<void*>(host_params), 0) != cudaSuccess || !dev) {
+    cudaGetLastError();
+    return set_err(ctx, MT_ERR_NOT_PINNED, "host params are not mapped into the device address space");
+  }
   ctx->host_params = host_params;
+  ctx->host_params_dev = dev;
   return MT_OK;
 }
 
@@ -1243,6 +1339,8 @@ void mt_destroy(mt_ctx* ctx) {
   }
   if (ctx->own_arena && ctx->arena) cudaFree(ctx->arena);
   if (ctx->host_stage) cudaFreeHost(ctx->host_stage);
+  if (ctx->host_rows) cudaFreeHost(ctx->host_rows);
+  if (ctx->host_grad_rows) cudaFreeHost(ctx->host_grad_rows);
   delete ctx;
 }
 
