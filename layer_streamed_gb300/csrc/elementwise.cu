@@ -68,61 +68,103 @@ __global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, const float* __r
 constexpr int kNormBwdRows = 32;
 constexpr int kMaxV = 8;  // h <= 8 * 4 * 256 = 8192
 
-__global__ void rmsnorm_bwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
-                                   const float* __restrict__ rstd, const float* __restrict__ dy,
-                                   const float* resid, float* dx, uint16_t* __restrict__ dxb,
-                                   float* __restrict__ part, int T, int h) {
-  __shared__ float red[32];
-  const int n4 = h >> 2;
-  float4 acc[kMaxV];
+// Two 256-thread halves of a block take alternate rows of the block's 32;
+// each thread loads its V float4 of x, dy (and the residual) of a row once
+// into registers (a row's loads are all in flight together, and the other
+// half computes meanwhile). The halves' dw partials are added in a fixed order.
+__device__ __forceinline__ float half_block_sum(float v, float* red, int half, int tid) {
+  v = warp_sum(v);
+  auto sync_half = [half] {
+    if (half) asm volatile("bar.sync 2, 256;" ::: "memory");
+    else asm volatile("bar.sync 1, 256;" ::: "memory");
+  };
+  sync_half();
+  if ((tid & 31) == 0) red[half * 8 + (tid >> 5)] = v;
+  sync_half();
+  float s = 0.f;
 #pragma unroll
-  for (int j = 0; j < kMaxV; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int i = 0; i < 8; ++i) s += red[half * 8 + i];  // same order in every thread
+  return s;
+}
+
+template <int V>
+__global__ void __launch_bounds__(512) rmsnorm_bwd_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                                          const float* __restrict__ rstd, const float* __restrict__ dy,
+                                                          const float* resid, float* dx, uint16_t* __restrict__ dxb,
+                                                          float* __restrict__ part, int T, int h) {
+  __shared__ float red[16];
+  __shared__ float4 xch[V * 256];
+  const int half = threadIdx.x >> 8, tid = threadIdx.x & 255;
+  const int n4 = h >> 2;
   const float inv_h = 1.f / (float)h;
+  const float4* w4 = (const float4*)w;
+  float4 acc[V];
+#pragma unroll
+  for (int j = 0; j < V; ++j) acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
   const int r0 = blockIdx.x * kNormBwdRows;
   const int r1 = min(T, r0 + kNormBwdRows);
-  for (int t = r0; t < r1; ++t) {
-    const float4* xr = (const float4*)(x + (size_t)t * h);
-    const float4* gr = (const float4*)(dy + (size_t)t * h);
+#pragma unroll 1
+  for (int t = r0 + half; t < r1; t += 2) {
+    float4 xv[V], gv[V], rv[V];
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const int i = tid + j * 256;
+      if (i < n4) {
+        xv[j] = ((const float4*)(x + (size_t)t * h))[i];
+        gv[j] = ((const float4*)(dy + (size_t)t * h))[i];
+        if (resid) rv[j] = ((const float4*)(resid + (size_t)t * h))[i];
+      }
+    }
     const float r = rstd[t];
     float dot = 0.f;
 #pragma unroll
-    for (int j = 0; j < kMaxV; ++j) {
-      const int i = threadIdx.x + j * kThreads;
+    for (int j = 0; j < V; ++j) {
+      const int i = tid + j * 256;
       if (i < n4) {
-        const float4 xv = xr[i], gv = gr[i], wv = ((const float4*)w)[i];
-        dot += gv.x * wv.x * xv.x + gv.y * wv.y * xv.y + gv.z * wv.z * xv.z + gv.w * wv.w * xv.w;
+        const float4 wv = w4[i];
+        dot += gv[j].x * wv.x * xv[j].x + gv[j].y * wv.y * xv[j].y + gv[j].z * wv.z * xv[j].z +
+               gv[j].w * wv.w * xv[j].w;
       }
     }
-    dot = block_sum(dot, red) * r;
-    const float mean = dot * inv_h;
+    const float mean = half_block_sum(dot, red, half, tid) * r * inv_h;
 #pragma unroll
-    for (int j = 0; j < kMaxV; ++j) {
-      const int i = threadIdx.x + j * kThreads;
+    for (int j = 0; j < V; ++j) {
+      const int i = tid + j * 256;
       if (i < n4) {
-        const float4 xv = xr[i], gv = gr[i], wv = ((const float4*)w)[i];
-        const float4 xh = make_float4(xv.x * r, xv.y * r, xv.z * r, xv.w * r);
-        float4 o = make_float4(r * (gv.x * wv.x - xh.x * mean), r * (gv.y * wv.y - xh.y * mean),
-                               r * (gv.z * wv.z - xh.z * mean), r * (gv.w * wv.w - xh.w * mean));
+        const float4 wv = w4[i];
+        const float4 xh = make_float4(xv[j].x * r, xv[j].y * r, xv[j].z * r, xv[j].w * r);
+        float4 o = make_float4(r * (gv[j].x * wv.x - xh.x * mean), r * (gv[j].y * wv.y - xh.y * mean),
+                               r * (gv[j].z * wv.z - xh.z * mean), r * (gv[j].w * wv.w - xh.w * mean));
         if (resid) {
-          const float4 rv = ((const float4*)(resid + (size_t)t * h))[i];
-          o.x += rv.x;
-          o.y += rv.y;
-          o.z += rv.z;
-          o.w += rv.w;
+          o.x += rv[j].x;
+          o.y += rv[j].y;
+          o.z += rv[j].z;
+          o.w += rv[j].w;
         }
         ((float4*)(dx + (size_t)t * h))[i] = o;
         if (dxb) store_bf16x4(dxb + (size_t)t * h + 4 * i, o.x, o.y, o.z, o.w);
-        acc[j].x += gv.x * xh.x;
-        acc[j].y += gv.y * xh.y;
-        acc[j].z += gv.z * xh.z;
-        acc[j].w += gv.w * xh.w;
+        acc[j].x += gv[j].x * xh.x;
+        acc[j].y += gv[j].y * xh.y;
+        acc[j].z += gv[j].z * xh.z;
+        acc[j].w += gv[j].w * xh.w;
       }
     }
   }
+  if (half == 1) {
 #pragma unroll
-  for (int j = 0; j < kMaxV; ++j) {
-    const int i = threadIdx.x + j * kThreads;
-    if (i < n4) ((float4*)(part + (size_t)blockIdx.x * h))[i] = acc[j];
+    for (int j = 0; j < V; ++j) xch[tid + j * 256] = acc[j];
+  }
+  __syncthreads();
+  if (half == 0) {
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const int i = tid + j * 256;
+      if (i < n4) {
+        const float4 o = xch[i];
+        ((float4*)(part + (size_t)blockIdx.x * h))[i] =
+            make_float4(acc[j].x + o.x, acc[j].y + o.y, acc[j].z + o.z, acc[j].w + o.w);
+      }
+    }
   }
 }
 
@@ -463,7 +505,11 @@ int rmsnorm_bwd(const float* x, const float* w, const float* rstd, const float* 
                 uint16_t* dx_bf16, float* dw, float* work, int T, int h, cudaStream_t st) {
   if (T <= 0 || h <= 0 || (h & 3) || h > kMaxV * 4 * kThreads) return -1;
   const int nb = (T + kNormBwdRows - 1) / kNormBwdRows;
-  rmsnorm_bwd_kernel<<<nb, kThreads, 0, st>>>(x, w, rstd, dy, resid, dx, dx_bf16, work, T, h);
+  const int n4 = h / 4;
+  if (n4 <= 256) rmsnorm_bwd_kernel<1><<<nb, 512, 0, st>>>(x, w, rstd, dy, resid, dx, dx_bf16, work, T, h);
+  else if (n4 <= 512) rmsnorm_bwd_kernel<2><<<nb, 512, 0, st>>>(x, w, rstd, dy, resid, dx, dx_bf16, work, T, h);
+  else if (n4 <= 1024) rmsnorm_bwd_kernel<4><<<nb, 512, 0, st>>>(x, w, rstd, dy, resid, dx, dx_bf16, work, T, h);
+  else rmsnorm_bwd_kernel<8><<<nb, 512, 0, st>>>(x, w, rstd, dy, resid, dx, dx_bf16, work, T, h);
   count_launches(1);
   sum_partials_kernel<<<blocks_for(h, 256), 256, 0, st>>>(work, nb, h, dw);
   count_launches(1);

@@ -2,10 +2,12 @@
 
   python -m layer_streamed_gb300.kbench gemm --mode nt --M 8192 --N 28672 --K 4096 [--reps 20]
   python -m layer_streamed_gb300.kbench attn --B 2 --S 4096 --heads 32 --kv-heads 8 --head-dim 128 [--bwd]
+  python -m layer_streamed_gb300.kbench norm --T 8192 --h 4096 [--bwd]
 
 Inputs are random bf16 tensors on the current GPU (larger than L2 at the 8B
 shapes); each launch is timed with CUDA events on the launching stream after
-warm-up. Prints one JSON line with the per-launch time and TFLOP/s.
+warm-up. Prints one JSON line with the per-launch time and TFLOP/s (GB/s
+of algorithmic traffic for the norms).
 """
 from __future__ import annotations
 
@@ -69,6 +71,26 @@ def bench_attn(args) -> dict:
             "tflops": 2.5 * flop / ms / 1e9}
 
 
+def bench_norm(args) -> dict:
+    T, h = args.T, args.h
+    x = torch.randn((T, h), device="cuda")
+    w = 1.0 + 0.1 * torch.randn(h, device="cuda")
+    dy, res = torch.randn((T, h), device="cuda"), torch.randn((T, h), device="cuda")
+    y = torch.empty((T, h), device="cuda", dtype=torch.bfloat16)
+    rstd = torch.empty(T, device="cuda")
+    mt.mt_op_rmsnorm_fwd(x, w, y, rstd, T, h, 1e-5)
+    dx, dxb, dw = torch.empty_like(x), torch.empty((T, h), device="cuda", dtype=torch.bfloat16), torch.empty_like(w)
+    ws = torch.empty(mt.mt_op_rmsnorm_bwd_workspace(T, h), device="cuda")
+    if args.bwd:
+        ms = _time(lambda: mt.mt_op_rmsnorm_bwd(x, w, rstd, dy, res, dx, dxb, dw, ws, T, h), args.reps)
+        nbytes = T * h * (4 * 3 + 4 + 2)  # read x, dy, residual; write dx fp32 and bf16
+    else:
+        ms = _time(lambda: mt.mt_op_rmsnorm_fwd(x, w, y, rstd, T, h, 1e-5), args.reps)
+        nbytes = T * h * (4 + 2)
+    return {"kernel": "rmsnorm_bwd" if args.bwd else "rmsnorm_fwd", "T": T, "h": h, "ms": ms,
+            "gbs": nbytes / ms / 1e6}
+
+
 def main():
     ap = argparse.ArgumentParser()
     sub = ap.add_subparsers(dest="op", required=True)
@@ -87,9 +109,14 @@ def main():
     a.add_argument("--head-dim", type=int, default=128)
     a.add_argument("--bwd", action="store_true")
     a.add_argument("--reps", type=int, default=20)
+    n = sub.add_parser("norm")
+    n.add_argument("--T", type=int, default=8192)
+    n.add_argument("--h", type=int, default=4096)
+    n.add_argument("--bwd", action="store_true")
+    n.add_argument("--reps", type=int, default=20)
     args = ap.parse_args()
     mt.build()
-    res = bench_gemm(args) if args.op == "gemm" else bench_attn(args)
+    res = {"gemm": bench_gemm, "attn": bench_attn, "norm": bench_norm}[args.op](args)
     res["device_error"] = mt.mt_op_device_error()
     print(json.dumps(res), flush=True)
 

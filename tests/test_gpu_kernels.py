@@ -110,9 +110,13 @@ def test_gemm_sampled_at_full_8b_qkv_shape():
     assert np.max(np.abs(got - ref)) <= 1e-4 * np.max(np.abs(ref)) + 1e-6
 
 
-def test_rmsnorm_forward_backward():
+@pytest.mark.parametrize("T,h,with_res", [(77, 320, True), (45, 1800, False), (33, 4096, True), (9, 6000, True)])
+def test_rmsnorm_forward_backward(T, h, with_res):
+    """Widths that select each per-thread vector count of the backward
+    kernel (h/4 up to 256, 512, 1024, 2048 float4), ragged row counts (odd
+    rows in the last block), with and without the residual input."""
     torch, mt = need_gpu()
-    T, h, eps = 77, 320, 1e-5
+    eps = 1e-5
     x = _normal((T, h), 21)
     w = 1.0 + 0.1 * _normal((h,), 22)
     dy = _normal((T, h), 23)
@@ -128,7 +132,10 @@ def test_rmsnorm_forward_backward():
     DXb = torch.empty((T, h), dtype=torch.bfloat16, device="cuda")
     DW = torch.empty(h, device="cuda")
     ws = torch.empty(mt.mt_op_rmsnorm_bwd_workspace(T, h), device="cuda")
-    mt.mt_op_rmsnorm_bwd(X, W, R, to_dev_f32(torch, dy), to_dev_f32(torch, res), DX, DXb, DW, ws, T, h)
+    if not with_res:
+        res = np.zeros_like(res)
+    mt.mt_op_rmsnorm_bwd(X, W, R, to_dev_f32(torch, dy), to_dev_f32(torch, res) if with_res else None, DX, DXb, DW,
+                         ws, T, h)
     dx_ref, dw_ref = oracle.rmsnorm_bwd(x, w, dy, eps)
     assert rel_l2(from_dev(DX), dx_ref + res) < 1e-5
     assert rel_l2(from_dev(DXb), dx_ref + res) < 6e-3
