@@ -184,18 +184,19 @@ constexpr float kRescaleThreshold = 8.0f;  // log2 units
 // warps 4-7 softmax of tile A, warps 8-11 softmax of tile B (warps 2-3 idle).
 // The MMA thread alternates between the tiles (PV_A(t), S_A(t+1), PV_B(t),
 // S_B(t+1)), so each softmax warpgroup works while the tensor core serves
-// the other tile. TMEM: S_A +0, S_B +128, O_A +256, O_B +384.
-// Shared: Q_A, Q_B, K (two stages), V (one stage), P_A, P_B.
+// the other tile. TMEM: S_A +0, S_B +128, O_A +256, O_B +384; the softmax
+// writes P (bf16 pairs) over the first 64 columns of its S, and the PV
+// product reads it from there as its A operand (the next S product of that
+// tile is issued after the PV product, and tensor-core operations of one
+// thread run in issue order). Shared: Q_A, Q_B, K and V in two stages each.
 // ===========================================================================
 template <int D>
 struct FwdSmem {
   static constexpr int QA = 0;
   static constexpr int QB = QA + tile_bytes<D>();
   static constexpr int K0 = QB + tile_bytes<D>();
-  static constexpr int V = K0 + 2 * tile_bytes<D>();
-  static constexpr int PA = V + tile_bytes<D>();
-  static constexpr int PB = PA + 2 * BOX;
-  static constexpr int BAR = PB + 2 * BOX;
+  static constexpr int V0 = K0 + 2 * tile_bytes<D>();
+  static constexpr int BAR = V0 + 2 * tile_bytes<D>();
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;  // one CTA per SM
 };
@@ -217,12 +218,12 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* q_full = bars + 0;
   uint64_t* k_full = bars + 1;   // [2]
   uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;
-  uint64_t* v_empty = bars + 6;
-  uint64_t* s_full = bars + 7;   // [2]: tile A, tile B
-  uint64_t* p_full = bars + 9;   // [2]
-  uint64_t* o_done = bars + 11;  // [2]
-  uint32_t* tmem_slot = (uint32_t*)(bars + 13);
+  uint64_t* v_full = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;  // [2]
+  uint64_t* s_full = bars + 9;   // [2]: tile A, tile B
+  uint64_t* p_full = bars + 11;  // [2]
+  uint64_t* o_done = bars + 13;  // [2]
+  uint32_t* tmem_slot = (uint32_t*)(bars + 15);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int nqt = (a.S + TILE - 1) / TILE;
@@ -238,12 +239,12 @@ __global__ void __launch_bounds__(384, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&p_full[i], 4);
       mbar_init(&o_done[i], 1);
     }
-    mbar_init(v_full, 1);
-    mbar_init(v_empty, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -265,13 +266,14 @@ __global__ void __launch_bounds__(384, 1)
       load_head_tile<D>(sm + L::QA, &tq, q_full, j, (2 * m) * TILE, b);
       load_head_tile<D>(sm + L::QB, &tq, q_full, j, (2 * m + 1) * TILE, b);
       for (int t = 0; t < tB; ++t) {
-        const int ks = t & 1;
-        mbar_wait(&k_empty[ks], ((t >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(&k_full[ks], tile_bytes<D>());
-        load_head_tile<D>(sm + L::K0 + ks * tile_bytes<D>(), &tk, &k_full[ks], g, t * TILE, b);
-        mbar_wait(v_empty, (t & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(v_full, tile_bytes<D>());
-        load_head_tile<D>(sm + L::V, &tv, v_full, g, t * TILE, b);
+        const int st = t & 1;
+        const uint32_t free_par = ((t >> 1) & 1) ^ 1;
+        mbar_wait(&k_empty[st], free_par, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&k_full[st], tile_bytes<D>());
+        load_head_tile<D>(sm + L::K0 + st * tile_bytes<D>(), &tk, &k_full[st], g, t * TILE, b);
+        mbar_wait(&v_empty[st], free_par, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&v_full[st], tile_bytes<D>());
+        load_head_tile<D>(sm + L::V0 + st * tile_bytes<D>(), &tv, &v_full[st], g, t * TILE, b);
       }
     }
     __syncwarp();
@@ -288,12 +290,12 @@ __global__ void __launch_bounds__(384, 1)
           tc_mma(tmem + side * 128, kmaj_desc(q, kk), kmaj_desc(kt, kk), IDESC_S, kk > 0 ? 1u : 0u);
         tc_commit(&s_full[side]);
       };
-      auto issue_pv = [&](int side, int t) {  // O_side += P_side(t) V_t
-        const uint8_t* pt = sm + (side ? L::PB : L::PA);
+      auto issue_pv = [&](int side, int t) {  // O_side += P_side(t) V_t, P from tensor memory
+        const uint8_t* vt = sm + L::V0 + (t & 1) * tile_bytes<D>();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)
-          tc_mma(tmem + 256 + side * 128, kmaj_desc(pt, kk), mnmaj_desc(sm + L::V, kk), IDESC_O,
-                 (t > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(tmem + 256 + side * 128, tmem + side * 128 + kk * 8, mnmaj_desc(vt, kk), IDESC_O,
+                    (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&o_done[side]);
       };
       mbar_wait(q_full, 0, abort_flag, kErrTimeoutAttn);
@@ -304,7 +306,7 @@ __global__ void __launch_bounds__(384, 1)
       tc_commit(&k_empty[0]);
       for (int t = 0; t < tB; ++t) {
         const bool next = t + 1 < tB;
-        mbar_wait(v_full, t & 1, abort_flag, kErrTimeoutAttn);
+        mbar_wait(&v_full[t & 1], (t >> 1) & 1, abort_flag, kErrTimeoutAttn);
         if (t < tA) {
           mbar_wait(&p_full[0], t & 1, abort_flag, kErrTimeoutAttn);
           tc_fence_after();
@@ -318,7 +320,7 @@ __global__ void __launch_bounds__(384, 1)
         mbar_wait(&p_full[1], t & 1, abort_flag, kErrTimeoutAttn);
         tc_fence_after();
         issue_pv(1, t);
-        tc_commit(v_empty);
+        tc_commit(&v_empty[t & 1]);
         if (next) {
           mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
           tc_fence_after();
@@ -338,7 +340,6 @@ __global__ void __launch_bounds__(384, 1)
     const uint32_t lane_base = (q4 * 32) << 16;
     const uint32_t s_col = tmem + lane_base + side * 128;
     const uint32_t o_col = tmem + lane_base + 256 + side * 128;
-    uint8_t* ptile = sm + (side ? L::PB : L::PA);
     float m_ref = -INFINITY, l = 0.f;
     for (int t = 0; t < nt; ++t) {
       mbar_wait(&s_full[side], t & 1, abort_flag, kErrTimeoutAttn);
@@ -374,7 +375,7 @@ __global__ void __launch_bounds__(384, 1)
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = mx * a.scale_log2;
-      // the previous P V product must be complete before O or P is touched
+      // the previous P V product must be complete before O is touched
       if (t > 0) mbar_wait(&o_done[side], (t - 1) & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
       // The rescale touches O through warp-collective tensor-memory loads and
@@ -396,21 +397,28 @@ __global__ void __launch_bounds__(384, 1)
             for (int i = 0; i < 32; ++i) v[i] = __float_as_uint(__uint_as_float(v[i]) * alpha);
             tmem_st32(o_col + c * 32, v);
           }
-          tmem_st_wait();
         }
         m_ref = m_use;
       }
-      // probabilities relative to m_ref (masked entries give 0), row sum, P
+      // probabilities relative to m_ref (masked entries give 0), row sum,
+      // and P as bf16 pairs over the first 64 columns of S
       float l8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        sv[i] = ex2_approx(fmaf(sv[i], a.scale_log2, -m_ref));
-        l8[i & 7] += sv[i];
+      for (int c = 0; c < 2; ++c) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const float p0 = ex2_approx(fmaf(sv[64 * c + 2 * i], a.scale_log2, -m_ref));
+          const float p1 = ex2_approx(fmaf(sv[64 * c + 2 * i + 1], a.scale_log2, -m_ref));
+          l8[(2 * i) & 7] += p0;
+          l8[(2 * i + 1) & 7] += p1;
+          pk[i] = pack_bf2(p0, p1);
+        }
+        __syncwarp();
+        tmem_st32(s_col + 32 * c, pk);
       }
       l += ((l8[0] + l8[1]) + (l8[2] + l8[3])) + ((l8[4] + l8[5]) + (l8[6] + l8[7]));
-#pragma unroll
-      for (int c = 0; c < 4; ++c) st_tile_row32(ptile, r, c, *reinterpret_cast<const float(*)[32]>(&sv[32 * c]));
-      fence_proxy_async_smem();
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[side]);
