@@ -110,7 +110,8 @@ struct AttnArgs {
   uint16_t* o;       // fwd output / unused
   float* lse;        // [B, nq, S] natural log
   const float* lse_in;
-  const float* delta;
+  const float* delta;  // backward: [B, nq, pad64(S)] (see the delta kernel)
+  const float* lse2;   // backward: [B, nq, pad64(S)] log-sum-exp in log2 units
   uint16_t *dq, *dk, *dv;
   int B, S, nq, nkv, ldq, ldkv, ldo;
   float scale_log2;  // log2(e) / sqrt(d)
@@ -449,16 +450,28 @@ __global__ void __launch_bounds__(384, 1)
 
 // ===========================================================================
 // Backward. Both passes iterate over 64-row sub-tiles of the loop dimension,
-// so that S/dP fit twice in tensor memory (double buffer) and the operand
-// ring has three stages. 12 warps: warp 0 TMA, warp 1 MMA issue, warps 4-7
-// and 8-11 are two elementwise warpgroups that split the 64 columns of each
-// sub-tile (warpgroup A columns 0-31, B 32-63); thread = row of the 128-row
-// tile. The MMA thread issues the score products of sub-tile i+1 before the
-// gradient products of sub-tile i, so elementwise work overlaps the tensor
-// core. Operand layout of a [64 rows][64] box: 8 KB, 128-byte swizzle.
+// so that S/dP fit twice in tensor memory (double buffer); operands stream
+// through a four-stage ring. 12 warps: warp 0 TMA, warp 1 MMA issue, warps
+// 4-7 and 8-11 are two elementwise warpgroups that split the 64 columns of
+// each sub-tile (warpgroup A columns 0-31, B 32-63); thread = row of the
+// 128-row tile. The MMA thread issues the score products of sub-tile i+1
+// before the gradient products of sub-tile i, so elementwise work overlaps
+// the tensor core. The elementwise warps write P^T and dS^T (or dS) as bf16
+// pairs over the first 32 columns of their S and dP buffers, and the
+// gradient products read them from tensor memory as their A operand; tensor
+// core operations of one thread run in issue order, so the score products of
+// sub-tile i+2 (which overwrite those buffers) follow the gradient products
+// of sub-tile i. Operand layout of a [64 rows][64] box: 8 KB, 128-byte swizzle.
+//
+// The delta kernel also writes, per (sequence, query head), the log-sum-exp
+// in log2 units over S padded to a multiple of 64 (+inf on the padding, so
+// padded query rows get probability 0) beside delta (0 on the padding).
 // ===========================================================================
 constexpr int SUB = 64;
 constexpr int SBOX = 64 * 64 * 2;  // one [64 rows][64] bf16 box = 8 KB
+constexpr int kStages = 4;
+
+__host__ __device__ constexpr int pad64(int S) { return (S + 63) & ~63; }
 
 template <int D>
 constexpr uint32_t sub_bytes() {
@@ -472,43 +485,40 @@ __device__ __forceinline__ uint64_t kmaj_desc_sub(const uint8_t* tile, int kk) {
 __device__ __forceinline__ uint64_t mnmaj_desc_sub(const uint8_t* tile, int kk) {
   return make_sdesc(smem_u32(tile) + kk * 2048, SBOX, 1024);
 }
-// Write columns [32h, 32h+32) of row r of a [128 rows][64] K-major tile.
-__device__ __forceinline__ void st_tile64_row32(uint8_t* tile, int r, int h, const float (&v)[32]) {
-  uint8_t* rowp = tile + r * 128;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int chunk = h * 4 + i;
-    uint4 w;
-    w.x = pack_bf2(v[8 * i + 0], v[8 * i + 1]);
-    w.y = pack_bf2(v[8 * i + 2], v[8 * i + 3]);
-    w.z = pack_bf2(v[8 * i + 4], v[8 * i + 5]);
-    w.w = pack_bf2(v[8 * i + 6], v[8 * i + 7]);
-    *(uint4*)(rowp + ((chunk ^ (r & 7)) << 4)) = w;
-  }
-}
 template <int D>
 __device__ __forceinline__ void load_head_sub(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int head, int row0,
                                               int b) {
 #pragma unroll
   for (int i = 0; i < (D + 63) / 64; ++i) tma_load_4d(dst + i * SBOX, map, bar, i * 64, head, row0, b);
 }
-
-constexpr int kStages = 3;
+// Untiled bulk copy global -> shared; both addresses 16-byte aligned, size a
+// multiple of 16.
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+// 32 values of one row as 16 bf16 pairs into tensor-memory columns [col, col+16).
+__device__ __forceinline__ void tmem_st_bf16x32(uint32_t col, const float (&v)[32]) {
+  uint32_t pk[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) pk[i] = pack_bf2(v[2 * i], v[2 * i + 1]);
+  tmem_st16(col, pk);
+}
 
 // dK/dV pass: CTA = (128-row KV tile kt, KV head g, sequence b); loop over the
 // query heads of the group and the 64-row query sub-tiles at or after kt.
-// TMEM: S^T [2 x 64] +0, dP^T [2 x 64] +128, dV +256, dK +384.
+// TMEM: S^T [2 x 64] +0 (P^T over its first 32), dP^T [2 x 64] +128 (dS^T
+// over its first 32), dV +256, dK +384.
 template <int D>
 struct DkvSmem {
   static constexpr int K = 0;
   static constexpr int V = K + tile_bytes<D>();
   static constexpr int Q0 = V + tile_bytes<D>();                   // [kStages] Q sub-tiles
   static constexpr int DO0 = Q0 + kStages * sub_bytes<D>();        // [kStages] dO sub-tiles
-  static constexpr int P0 = DO0 + kStages * sub_bytes<D>();        // [2] P^T [128][64]
-  static constexpr int DS0 = P0 + 2 * BOX;                         // [2] dS^T [128][64]
-  static constexpr int LSE = DS0 + 2 * BOX;                        // [2][64] floats (log2 units)
-  static constexpr int DELTA = LSE + 2 * 64 * 4;                   // [2][64] floats
-  static constexpr int BAR = DELTA + 2 * 64 * 4;
+  static constexpr int LD0 = DO0 + kStages * sub_bytes<D>();       // [kStages] lse2[64], delta[64]
+  static constexpr int BAR = LD0 + kStages * 512;
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
 };
@@ -523,16 +533,13 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;   // [3]
-  uint64_t* qdo_empty = bars + 4;  // [3]
-  uint64_t* s_full = bars + 7;     // [2]
-  uint64_t* s_empty = bars + 9;    // [2]
-  uint64_t* p_full = bars + 11;    // [2]
-  uint64_t* pd_done = bars + 13;   // [2]
-  uint32_t* tmem_slot = (uint32_t*)(bars + 15);
+  uint64_t* qdo_full = bars + 1;                // [kStages]
+  uint64_t* qdo_empty = bars + 1 + kStages;     // [kStages]
+  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2]
+  uint64_t* p_full = bars + 3 + 2 * kStages;    // [2]
+  uint64_t* pd_done = bars + 5 + 2 * kStages;   // [2]
+  uint32_t* tmem_slot = (uint32_t*)(bars + 7 + 2 * kStages);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
-  float* s_lse = (float*)(sm + L::LSE);
-  float* s_delta = (float*)(sm + L::DELTA);
 
   const int nsub = (a.S + SUB - 1) / SUB;
   const int kt = (int)blockIdx.x;
@@ -541,6 +548,7 @@ __global__ void __launch_bounds__(384, 1)
   const int first = 2 * kt;              // first query sub-tile that can see this KV tile
   const int per_head = nsub - first;
   const int iters = grp * per_head;
+  const int Sp = pad64(a.S);
   const uint32_t warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
@@ -551,7 +559,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 8);
       mbar_init(&p_full[i], 8);
       mbar_init(&pd_done[i], 1);
     }
@@ -581,9 +588,12 @@ __global__ void __launch_bounds__(384, 1)
         const int qs = first + it % per_head;
         const int st = it % kStages;
         mbar_wait(&qdo_empty[st], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(&qdo_full[st], 2 * sub_bytes<D>());
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * sub_bytes<D>() + 512);
         load_head_sub<D>(sm + L::Q0 + st * sub_bytes<D>(), &tq, &qdo_full[st], j, qs * SUB, b);
         load_head_sub<D>(sm + L::DO0 + st * sub_bytes<D>(), &tdo, &qdo_full[st], j, qs * SUB, b);
+        const size_t ro = ((size_t)b * a.nq + j) * Sp + (size_t)qs * SUB;
+        bulk_load(sm + L::LD0 + st * 512, a.lse2 + ro, 256, &qdo_full[st]);
+        bulk_load(sm + L::LD0 + st * 512 + 256, a.delta + ro, 256, &qdo_full[st]);
       }
     }
     __syncwarp();
@@ -599,10 +609,10 @@ __global__ void __launch_bounds__(384, 1)
         const uint8_t* q = sm + L::Q0 + st * sub_bytes<D>();
         const uint8_t* dout = sm + L::DO0 + st * sub_bytes<D>();
 #pragma unroll
-        for (int kk = 0; kk < SUB / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q
+        for (int kk = 0; kk < SUB / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q  (A operands in TMEM)
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          tc_mma(tmem + 256, kmaj_desc(sm + L::P0 + buf * BOX, kk), mnmaj_desc_sub(dout, kk), IDESC_G, acc);
-          tc_mma(tmem + 384, kmaj_desc(sm + L::DS0 + buf * BOX, kk), mnmaj_desc_sub(q, kk), IDESC_G, acc);
+          tc_mma_ts(tmem + 256, tmem + buf * 64 + kk * 8, mnmaj_desc_sub(dout, kk), IDESC_G, acc);
+          tc_mma_ts(tmem + 384, tmem + 128 + buf * 64 + kk * 8, mnmaj_desc_sub(q, kk), IDESC_G, acc);
         }
         tc_commit(&pd_done[buf]);
         tc_commit(&qdo_empty[st]);
@@ -611,7 +621,6 @@ __global__ void __launch_bounds__(384, 1)
       for (int it = 0; it < iters; ++it) {
         const int buf = it & 1, st = it % kStages;
         mbar_wait(&qdo_full[st], (it / kStages) & 1, abort_flag, kErrTimeoutAttn);
-        mbar_wait(&s_empty[buf], ((it >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
         tc_fence_after();
         const uint8_t* q = sm + L::Q0 + st * sub_bytes<D>();
         const uint8_t* dout = sm + L::DO0 + st * sub_bytes<D>();
@@ -633,48 +642,33 @@ __global__ void __launch_bounds__(384, 1)
     const int r = q4 * 32 + lane;        // KV row of the tile
     const int srow = kt * TILE + r;      // KV position
     const uint32_t lane_base = (q4 * 32) << 16;
-    const int tid = threadIdx.x - 128;   // 0..255
+    const int cbase = half * 32;
     for (int it = 0; it < iters; ++it) {
-      const int buf = it & 1;
-      const int j = g * grp + it / per_head;
+      const int buf = it & 1, st = it % kStages;
       const int q0 = (first + it % per_head) * SUB;
-      if (tid < 128) {  // stage this sub-tile's log-sum-exp (log2 units) and delta
-        const int c = tid & 63;
-        const int tq = q0 + c;
-        const size_t ri = ((size_t)b * a.nq + j) * a.S + (tq < a.S ? tq : 0);
-        if (tid < 64) s_lse[buf * 64 + c] = tq < a.S ? a.lse_in[ri] * 1.4426950408889634f : INFINITY;
-        else s_delta[buf * 64 + c] = tq < a.S ? a.delta[ri] : 0.f;
-      }
-      named_bar_sync(1, 256);
+      const float* s_lse = (const float*)(sm + L::LD0 + st * 512);
+      const float* s_delta = s_lse + 64;
       mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
       uint32_t sv[32], dv[32];
       __syncwarp();
-      tmem_ld32(tmem + lane_base + buf * 64 + half * 32, sv);
-      tmem_ld32(tmem + lane_base + 128 + buf * 64 + half * 32, dv);
+      tmem_ld32(tmem + lane_base + buf * 64 + cbase, sv);
+      tmem_ld32(tmem + lane_base + 128 + buf * 64 + cbase, dv);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[buf]);
       float p[32], ds[32];
-      const int cbase = half * 32;
-      const bool need_mask = (q0 + cbase < srow + 1) || (q0 + cbase + 32 > a.S);
+      const bool need_mask = q0 + cbase < srow + 1;  // padded query rows have lse2 = +inf
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
         const int col = cbase + i;
-        float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -s_lse[buf * 64 + col]));
-        if (need_mask) {
-          const int tq = q0 + col;
-          if (tq < srow || tq >= a.S) pv = 0.f;  // query must be at or after the key
-        }
+        float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -s_lse[col]));
+        if (need_mask && q0 + col < srow) pv = 0.f;  // query must be at or after the key
         p[i] = pv;
-        ds[i] = pv * (__uint_as_float(dv[i]) - s_delta[buf * 64 + col]);
+        ds[i] = pv * (__uint_as_float(dv[i]) - s_delta[col]);
       }
-      // the gradient products of sub-tile it-2 must be done with this buffer
-      if (it >= 2) mbar_wait(&pd_done[buf], ((it >> 1) - 1) & 1, abort_flag, kErrTimeoutAttn);
-      st_tile64_row32(sm + L::P0 + buf * BOX, r, half, p);
-      st_tile64_row32(sm + L::DS0 + buf * BOX, r, half, ds);
-      fence_proxy_async_smem();
+      __syncwarp();
+      tmem_st_bf16x32(tmem + lane_base + buf * 64 + half * 16, p);
+      tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + half * 16, ds);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[buf]);
@@ -700,15 +694,14 @@ __global__ void __launch_bounds__(384, 1)
 
 // dQ pass: CTA = (128-row query tile qt, query head j, sequence b); loop over
 // the 64-row KV sub-tiles at or before the tile's last row.
-// TMEM: S [2 x 64] +0, dP [2 x 64] +128, dQ +256.
+// TMEM: S [2 x 64] +0, dP [2 x 64] +128 (dS over its first 32), dQ +256.
 template <int D>
 struct DqSmem {
   static constexpr int Q = 0;
   static constexpr int DO = Q + tile_bytes<D>();
   static constexpr int K0 = DO + tile_bytes<D>();             // [kStages]
   static constexpr int V0 = K0 + kStages * sub_bytes<D>();    // [kStages]
-  static constexpr int DS0 = V0 + kStages * sub_bytes<D>();   // [2] dS [128][64]
-  static constexpr int BAR = DS0 + 2 * BOX;
+  static constexpr int BAR = V0 + kStages * sub_bytes<D>();
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
 };
@@ -723,13 +716,12 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;   // [3]
-  uint64_t* kv_empty = bars + 4;  // [3]
-  uint64_t* s_full = bars + 7;    // [2]
-  uint64_t* s_empty = bars + 9;   // [2]
-  uint64_t* p_full = bars + 11;   // [2]
-  uint64_t* g_done = bars + 13;   // [2]
-  uint32_t* tmem_slot = (uint32_t*)(bars + 15);
+  uint64_t* kv_full = bars + 1;                 // [kStages]
+  uint64_t* kv_empty = bars + 1 + kStages;      // [kStages]
+  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2]
+  uint64_t* p_full = bars + 3 + 2 * kStages;    // [2]
+  uint64_t* g_done = bars + 5 + 2 * kStages;    // [2]
+  uint32_t* tmem_slot = (uint32_t*)(bars + 7 + 2 * kStages);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int nqt = (a.S + TILE - 1) / TILE;
@@ -748,7 +740,6 @@ __global__ void __launch_bounds__(384, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 8);
       mbar_init(&p_full[i], 8);
       mbar_init(&g_done[i], 1);
     }
@@ -793,9 +784,9 @@ __global__ void __launch_bounds__(384, 1)
         tc_fence_after();
         const uint8_t* kt = sm + L::K0 + st * sub_bytes<D>();
 #pragma unroll
-        for (int kk = 0; kk < SUB / 16; ++kk)  // dQ += dS K
-          tc_mma(tmem + 256, kmaj_desc(sm + L::DS0 + buf * BOX, kk), mnmaj_desc_sub(kt, kk), IDESC_G,
-                 (i > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < SUB / 16; ++kk)  // dQ += dS K  (dS in TMEM)
+          tc_mma_ts(tmem + 256, tmem + 128 + buf * 64 + kk * 8, mnmaj_desc_sub(kt, kk), IDESC_G,
+                    (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&g_done[buf]);
         tc_commit(&kv_empty[st]);
       };
@@ -803,7 +794,6 @@ __global__ void __launch_bounds__(384, 1)
       for (int it = 0; it < iters; ++it) {
         const int buf = it & 1, st = it % kStages;
         mbar_wait(&kv_full[st], (it / kStages) & 1, abort_flag, kErrTimeoutAttn);
-        mbar_wait(&s_empty[buf], ((it >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
         tc_fence_after();
         const uint8_t* kt = sm + L::K0 + st * sub_bytes<D>();
         const uint8_t* vt = sm + L::V0 + st * sub_bytes<D>();
@@ -826,8 +816,8 @@ __global__ void __launch_bounds__(384, 1)
     const int trow = qt * TILE + r;
     const uint32_t lane_base = (q4 * 32) << 16;
     const bool row_ok = trow < a.S;
-    const size_t ri = ((size_t)b * a.nq + j) * a.S + (row_ok ? trow : 0);
-    const float lse2 = row_ok ? a.lse_in[ri] * 1.4426950408889634f : 0.f;
+    const size_t ri = ((size_t)b * a.nq + j) * pad64(a.S) + (row_ok ? trow : 0);
+    const float lse2 = row_ok ? a.lse2[ri] : INFINITY;  // rows past S get probability 0
     const float dl = row_ok ? a.delta[ri] : 0.f;
     for (int it = 0; it < iters; ++it) {
       const int buf = it & 1;
@@ -838,9 +828,6 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld32(tmem + lane_base + buf * 64 + half * 32, sv);
       tmem_ld32(tmem + lane_base + 128 + buf * 64 + half * 32, dv);
       tmem_ld_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_empty[buf]);
       const int kv0 = it * SUB + half * 32;
       const bool need_mask = (kv0 + 31 > qt * TILE) || (kv0 + 32 > a.S);
       float ds[32];
@@ -849,13 +836,13 @@ __global__ void __launch_bounds__(384, 1)
         float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -lse2));
         if (need_mask) {
           const int kv = kv0 + i;
-          if (kv > trow || kv >= a.S || !row_ok) pv = 0.f;
+          if (kv > trow || kv >= a.S) pv = 0.f;
         }
         ds[i] = pv * (__uint_as_float(dv[i]) - dl);
       }
-      if (it >= 2) mbar_wait(&g_done[buf], ((it >> 1) - 1) & 1, abort_flag, kErrTimeoutAttn);
-      st_tile64_row32(sm + L::DS0 + buf * BOX, r, half, ds);
-      fence_proxy_async_smem();
+      __syncwarp();
+      tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + half * 16, ds);
+      tmem_st_wait();
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[buf]);
@@ -875,14 +862,25 @@ __global__ void __launch_bounds__(384, 1)
   }
 }
 
-// delta[b, j, t] = sum_e dO[t, j, e] * O[t, j, e]  (one warp per row)
+// Per (sequence b, query head j, position t < Sp): delta = sum_e dO O over
+// the head's columns (one warp per row) and lse2 = lse * log2(e); padding
+// rows t >= S get delta 0 and lse2 +inf. Layout [B][nq][Sp] each.
 __global__ void attn_delta_tc_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
-                                     float* __restrict__ delta, int B, int S, int nq, int d, int ldo) {
+                                     const float* __restrict__ lse, float* __restrict__ delta,
+                                     float* __restrict__ lse2, int B, int S, int Sp, int nq, int d, int ldo) {
   const size_t wid = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (wid >= (size_t)B * S * nq) return;
+  if (wid >= (size_t)B * Sp * nq) return;
   const int j = (int)(wid % nq);
-  const int t = (int)((wid / nq) % S);
-  const int b = (int)(wid / ((size_t)nq * S));
+  const int t = (int)((wid / nq) % Sp);
+  const int b = (int)(wid / ((size_t)nq * Sp));
+  const size_t ri = ((size_t)b * nq + j) * Sp + t;
+  if (t >= S) {
+    if (lane_id() == 0) {
+      delta[ri] = 0.f;
+      lse2[ri] = INFINITY;
+    }
+    return;
+  }
   const size_t off = ((size_t)b * S + t) * ldo + (size_t)j * d;
   float s = 0.f;
   for (int e = lane_id() * 2; e < d; e += 64) {
@@ -890,7 +888,10 @@ __global__ void attn_delta_tc_kernel(const uint16_t* __restrict__ o, const uint1
     s += bf2f(ov & 0xffff) * bf2f(gv & 0xffff) + bf2f(ov >> 16) * bf2f(gv >> 16);
   }
   s = warp_sum(s);
-  if (lane_id() == 0) delta[((size_t)b * nq + j) * S + t] = s;
+  if (lane_id() == 0) {
+    delta[ri] = s;
+    lse2[ri] = lse[((size_t)b * nq + j) * S + t] * 1.4426950408889634f;
+  }
 }
 
 // 4D map over a [B, S, heads, d] view with row stride ld (elements); boxes
@@ -945,15 +946,25 @@ int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const ui
       return -1;
     init = true;
   }
-  const size_t rows = (size_t)a.B * a.S * a.nq;
-  attn_delta_tc_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(o, dout, delta, a.B, a.S, a.nq, D, a.ldo);
+  const int Sp = pad64(a.S);
+  const size_t rows = (size_t)a.B * Sp * a.nq;
+  float* lse2 = delta + rows;
+  attn_delta_tc_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(o, dout, a.lse_in, delta, lse2, a.B, a.S,
+                                                                            Sp, a.nq, D, a.ldo);
   a.delta = delta;
+  a.lse2 = lse2;
   const int nt = (a.S + TILE - 1) / TILE;
   attn_bwd_dkv_tc_kernel<D><<<dim3(nt, a.nkv, a.B), 384, DkvSmem<D>::ALLOC, st>>>(tq64, tk128, tv128, tdo64, a);
   attn_bwd_dq_tc_kernel<D><<<dim3(nt, a.nq, a.B), 384, DqSmem<D>::ALLOC, st>>>(tq128, tk64, tv64, tdo128, a);
   count_launches(3);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
+
+}  // namespace
+
+size_t attention_bwd_workspace(int B, int S, int nq) { return 2 * (size_t)B * nq * pad64(S); }
+
+namespace {
 
 bool tc_ok(int B, int S, int nq, int nkv, int d, int ldq, int ldkv, int ldo, const void* q, const void* k,
            const void* v) {
@@ -969,7 +980,7 @@ bool tc_ok(int B, int S, int nq, int nkv, int d, int ldq, int ldkv, int ldo, con
 int attention_fwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int B, int S,
                      int nq, int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st) {
   if (!tc_ok(B, S, nq, nkv, d, ldq, ldkv, ldo, q, k, v)) return -1;
-  AttnArgs a{o, lse, nullptr, nullptr, nullptr, nullptr, nullptr, B, S, nq, nkv, ldq, ldkv, ldo,
+  AttnArgs a{o, lse, nullptr, nullptr, nullptr, nullptr, nullptr, nullptr, B, S, nq, nkv, ldq, ldkv, ldo,
              1.4426950408889634f / sqrtf((float)d), 1.f / sqrtf((float)d), nullptr};
   switch (d) {
     case 16: return fwd_launch<16>(q, k, v, a, st);
@@ -982,8 +993,8 @@ int attention_fwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, ui
 int attention_bwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
                      const float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv, float* work, int B, int S, int nq,
                      int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st, const float2* rope_tab) {
-  if (!tc_ok(B, S, nq, nkv, d, ldq, ldkv, ldo, q, k, v)) return -1;
-  AttnArgs a{nullptr, nullptr, lse, nullptr, dq, dk, dv, B, S, nq, nkv, ldq, ldkv, ldo,
+  if (!tc_ok(B, S, nq, nkv, d, ldq, ldkv, ldo, q, k, v) || ((uintptr_t)work & 15)) return -1;
+  AttnArgs a{nullptr, nullptr, lse, nullptr, nullptr, dq, dk, dv, B, S, nq, nkv, ldq, ldkv, ldo,
              1.4426950408889634f / sqrtf((float)d), 1.f / sqrtf((float)d), rope_tab};
   switch (d) {
     case 16: return bwd_launch<16>(q, k, v, o, dout, a, work, st);

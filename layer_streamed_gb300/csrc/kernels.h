@@ -97,22 +97,15 @@ int ce_finalize(const float2* part, int nslices, const float* zlab, float* lse, 
 int ce_slice_grad(const float* logits, int T, int R, int ld, int row0, const int32_t* labels, const float* lse,
                   float scale, uint16_t* dz, cudaStream_t st);
 
-// Attention (attention.cu)
-int attention_fwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int B, int S,
-                  int nq, int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
-size_t attention_bwd_workspace(int B, int S, int nq);  // floats
-int attention_bwd(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
-                  const float* lse, uint16_t* dq, uint16_t* dk, uint16_t* dv, float* work, int B, int S, int nq,
-                  int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
-
 // Read and clear the device error words of the kernels that wait on
 // barriers (0 = no error). Synchronous with respect to the device.
 uint32_t gemm_take_device_error();
-uint32_t attention_take_device_error();
 uint32_t attention_tc_take_device_error();
 
 // Tensor-core flash attention (attention_tc.cu); head_dim in {16,32,64,128},
-// row strides multiples of 8. work: B*S*nq floats (delta).
+// row strides multiples of 8. work: attention_bwd_workspace(B, S, nq) floats
+// (per row delta and the log-sum-exp in log2 units, S padded to 64).
+size_t attention_bwd_workspace(int B, int S, int nq);
 int attention_fwd_tc(const uint16_t* q, const uint16_t* k, const uint16_t* v, uint16_t* o, float* lse, int B, int S,
                      int nq, int nkv, int d, int ldq, int ldkv, int ldo, cudaStream_t st);
 // rope_tab (nullable, [S][d/2] (cos, sin)): q and k were rotated after

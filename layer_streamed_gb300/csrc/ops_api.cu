@@ -167,7 +167,7 @@ int mt_op_lmhead_ce(const void* X, const void* W, const int32_t* labels, float s
 
 int mt_op_device_error(void) {
   cudaDeviceSynchronize();
-  return (int)(gemm_take_device_error() | attention_take_device_error() | attention_tc_take_device_error());
+  return (int)(gemm_take_device_error() | attention_tc_take_device_error());
 }
 
 }  // extern "C"

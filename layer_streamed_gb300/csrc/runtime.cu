@@ -1265,7 +1265,7 @@ int mt_forward_backward(mt_ctx* ctx, const int32_t* tokens, const int32_t* label
     cudaGetLastError();
     ctx->err = msg;
   } else {
-    const uint32_t derr = gemm_take_device_error() | attention_take_device_error() | attention_tc_take_device_error();
+    const uint32_t derr = gemm_take_device_error() | attention_tc_take_device_error();
     if (derr) {
       char b[96];
       snprintf(b, sizeof b, "device error word 0x%x (barrier timeout inside a kernel)", derr);
