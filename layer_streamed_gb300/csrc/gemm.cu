@@ -16,6 +16,7 @@
 // mainloop of tile i+1. Each output tile is produced by one CTA with a fixed
 // K order, so results do not depend on the grid size (deterministic).
 #include <algorithm>
+#include <cstdio>
 #include <cstdlib>
 
 #include "common.cuh"
@@ -218,6 +219,66 @@ __device__ __forceinline__ void swiglu_bwd_epilogue(const GemmParams& p, uint32_
   }
 }
 
+// Epilogue of one output tile for one warp: TMEM lanes of `tb` hold row
+// `row`; columns [nb * BN, nb * BN + BN) of C (gated tiles: tile_n features).
+template <int BN>
+__device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tb, int row, bool row_ok, int nb,
+                                              int tile_n) {
+  if (p.rope_tab || p.gated || p.swiglu_bwd) {
+    if (p.rope_tab) rope_epilogue<BN>(p, tb, row, row_ok, nb * BN);
+    else if (p.gated) gated_epilogue<BN>(p, tb, row, row_ok, nb * tile_n);
+    else swiglu_bwd_epilogue<BN>(p, tb, row, row_ok, nb * BN);
+    return;
+  }
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    uint32_t r[32];
+    __syncwarp();
+    tmem_ld32(tb + c * 32, r);
+    tmem_ld_wait();
+    const int col0 = nb * BN + c * 32;
+    if (!row_ok || col0 >= p.N) continue;
+    const bool full_cols = p.vec && col0 + 32 <= p.N;
+    if (p.epi == EPI_BF16) {
+      uint16_t* out = (uint16_t*)p.C + (size_t)row * p.ldc + col0;
+      if (full_cols) {
+        uint4* o4 = (uint4*)out;
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          uint4 w;
+          w.x = pack_bf2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
+          w.y = pack_bf2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
+          w.z = pack_bf2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
+          w.w = pack_bf2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
+          o4[v] = w;
+        }
+      } else {
+        for (int j = 0; j < 32 && col0 + j < p.N; ++j) out[j] = f2bf(__uint_as_float(r[j]));
+      }
+    } else {
+      float* out = (float*)p.C + (size_t)row * p.ldc + col0;
+      const float* add = p.epi == EPI_F32_ADD ? (const float*)p.addend + (size_t)row * p.ldc + col0 : nullptr;
+      if (full_cols) {
+#pragma unroll
+        for (int v = 0; v < 8; ++v) {
+          float4 w = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                 __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+          if (add) {
+            const float4 a = ((const float4*)add)[v];
+            w.x += a.x;
+            w.y += a.y;
+            w.z += a.z;
+            w.w += a.w;
+          }
+          ((float4*)out)[v] = w;
+        }
+      } else {
+        for (int j = 0; j < 32 && col0 + j < p.N; ++j) out[j] = __uint_as_float(r[j]) + (add ? add[j] : 0.f);
+      }
+    }
+  }
+}
+
 template <int BN, bool A_MN, bool B_MN>
 __global__ void __launch_bounds__(192, 1)
     gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
@@ -344,65 +405,7 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait(&tfull[acc], acc_phase, abort_flag, kErrTimeoutEpi);
       tc_fence_after();
       const int row = mb * BM + q * 32 + lane;
-      const bool row_ok = row < p.M;
-      if (p.rope_tab || p.gated || p.swiglu_bwd) {
-        const uint32_t tb = tmem_base + ((q * 32) << 16) + acc * BN;
-        if (p.rope_tab) rope_epilogue<BN>(p, tb, row, row_ok, nb * BN);
-        else if (p.gated) gated_epilogue<BN>(p, tb, row, row_ok, nb * tile_n);
-        else swiglu_bwd_epilogue<BN>(p, tb, row, row_ok, nb * BN);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&tempty[acc]);
-        continue;
-      }
-#pragma unroll 1
-      for (int c = 0; c < BN / 32; ++c) {
-        uint32_t r[32];
-        __syncwarp();
-        tmem_ld32(tmem_base + ((q * 32) << 16) + acc * BN + c * 32, r);
-        tmem_ld_wait();
-        const int col0 = nb * BN + c * 32;
-        if (row_ok && col0 < p.N) {
-        const bool full_cols = p.vec && col0 + 32 <= p.N;
-        if (p.epi == EPI_BF16) {
-          uint16_t* out = (uint16_t*)p.C + (size_t)row * p.ldc + col0;
-          if (full_cols) {
-            uint4* o4 = (uint4*)out;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = pack_bf2(__uint_as_float(r[8 * v + 0]), __uint_as_float(r[8 * v + 1]));
-              w.y = pack_bf2(__uint_as_float(r[8 * v + 2]), __uint_as_float(r[8 * v + 3]));
-              w.z = pack_bf2(__uint_as_float(r[8 * v + 4]), __uint_as_float(r[8 * v + 5]));
-              w.w = pack_bf2(__uint_as_float(r[8 * v + 6]), __uint_as_float(r[8 * v + 7]));
-              o4[v] = w;
-            }
-          } else {
-            for (int j = 0; j < 32 && col0 + j < p.N; ++j) out[j] = f2bf(__uint_as_float(r[j]));
-          }
-        } else {
-          float* out = (float*)p.C + (size_t)row * p.ldc + col0;
-          const float* add = p.epi == EPI_F32_ADD ? (const float*)p.addend + (size_t)row * p.ldc + col0 : nullptr;
-          if (full_cols) {
-#pragma unroll
-            for (int v = 0; v < 8; ++v) {
-              float4 w = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
-                                     __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
-              if (add) {
-                const float4 a = ((const float4*)add)[v];
-                w.x += a.x;
-                w.y += a.y;
-                w.z += a.z;
-                w.w += a.w;
-              }
-              ((float4*)out)[v] = w;
-            }
-          } else {
-            for (int j = 0; j < 32 && col0 + j < p.N; ++j) out[j] = __uint_as_float(r[j]) + (add ? add[j] : 0.f);
-          }
-        }
-        }
-      }
+      epilogue_tile<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, row, row < p.M, nb, tile_n);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -413,6 +416,213 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
   }
+}
+
+// ---------------------------------------------------------------------------
+// Paired-SM form for wide tiles: a cluster of two CTAs computes 256 x 256
+// output tiles with tcgen05.mma.cta_group::2. Each CTA stages its own 128
+// rows of A and its half (128 rows of N) of B, so every SM feeds the tensor
+// core from 32 KB of shared memory per 64-deep K step instead of 48 KB, and
+// the ring holds six stages. The even CTA issues the MMAs; its accumulator
+// rows [0, 128) land in its tensor memory and rows [128, 256) in the odd
+// CTA's. Both CTAs' TMA loads complete on the even CTA's stage barrier, the
+// even CTA's commits arrive on both CTAs' stage-free and accumulator-ready
+// barriers, and both CTAs' epilogue warps report a drained accumulator to
+// the even CTA. Gated tiles put the gate rows in the even CTA's half of B and
+// the matching up rows in the odd CTA's, which gives the same accumulator
+// column layout as the single-CTA kernel.
+// ---------------------------------------------------------------------------
+struct PairCfg {
+  static constexpr int BN = 256;
+  static constexpr int B_BYTES = 128 * BK * 2;            // this CTA's half of B: 16 KB
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
+  static constexpr int STAGES = 6;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+};
+
+template <bool A_MN, bool B_MN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, GemmParams p) {
+  using C = PairCfg;
+  constexpr int BN = C::BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + C::STAGES * A_BYTES;
+  uint64_t* full = (uint64_t*)(smem + C::STAGES * C::STAGE_BYTES);  // even CTA: both halves landed
+  uint64_t* empty = full + C::STAGES;
+  uint64_t* tfull = empty + C::STAGES;
+  uint64_t* tempty = tfull + 2;             // even CTA: both CTAs drained the accumulator
+  uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
+  volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+
+  const uint32_t warp = warp_id(), lane = lane_id();
+  const uint32_t rank = cluster_rank();
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tmap(&tmA);
+    prefetch_tmap(&tmB);
+  }
+  if (warp == 1) {
+    tmem_alloc2(tmem_slot, 2 * BN);
+    tmem_relinquish2();
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // barriers of both CTAs initialised, tensor memory allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int tile_n = p.gated ? BN / 2 : BN;
+  const int num_m = (p.M + 2 * BM - 1) / (2 * BM), num_n = (p.N + tile_n - 1) / tile_n;
+  const int num_tiles = num_m * num_n;
+  const int num_kb = (p.K + BK - 1) / BK;
+  const int cl = (int)(blockIdx.x >> 1), ncl = (int)(gridDim.x >> 1);
+
+  if (warp == 0) {
+    if (lane == 0) {  // TMA producer (both CTAs)
+      const uint32_t full0 = mapa_shared(full, 0);
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = cl; tile < num_tiles; tile += ncl) {
+        int mb, nb;
+        tile_coords(tile, num_m, num_n, p.group_m, mb, nb);
+        const int m0 = mb * 2 * BM + (int)rank * BM;
+        const int nrow0 = p.gated ? (rank ? p.u_off : 0) + nb * tile_n : nb * BN + (int)rank * 128;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          mbar_wait<true>(&empty[stage], phase ^ 1, abort_flag, kErrTimeoutTma);
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], 2 * C::STAGE_BYTES);
+          const uint32_t bar = full0 + stage * 8;
+          uint8_t* a_dst = sA + stage * A_BYTES;
+          uint8_t* b_dst = sB + stage * C::B_BYTES;
+          if (!A_MN) {
+            tma_load_2d_pair(a_dst, &tmA, bar, kb * BK, m0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d_pair(a_dst + j * 8192, &tmA, bar, m0 + 64 * j, kb * BK);
+          }
+          if (!B_MN) {
+            tma_load_2d_pair(b_dst, &tmB, bar, kb * BK, nrow0);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 2; ++j) tma_load_2d_pair(b_dst + j * 8192, &tmB, bar, nrow0 + 64 * j, kb * BK);
+          }
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {  // MMA issuer (even CTA)
+      constexpr uint32_t IDESC = make_idesc(2 * BM, BN, A_MN, B_MN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int local = 0;
+      for (int tile = cl; tile < num_tiles; tile += ncl, ++local) {
+        const int acc = local & 1;
+        const uint32_t acc_phase = (local >> 1) & 1;
+        mbar_wait<true>(&tempty[acc], acc_phase ^ 1, abort_flag, kErrTimeoutMma);
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        for (int kb = 0; kb < num_kb; ++kb) {
+          mbar_wait(&full[stage], phase, abort_flag, kErrTimeoutMma);
+          tc_fence_after();
+          const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
+          const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? make_sdesc(a_base + kk * 2048, 8192, 1024) : make_sdesc(a_base + kk * 32, 16, 1024);
+            const uint64_t bd = B_MN ? make_sdesc(b_base + kk * 2048, 8192, 1024) : make_sdesc(b_base + kk * 32, 16, 1024);
+            tc_mma2(d_tmem, ad, bd, IDESC, (kb | kk) != 0);
+          }
+          tc_commit2(&empty[stage], 0x3);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        tc_commit2(&tfull[acc], 0x3);
+      }
+    }
+    __syncwarp();
+  } else {  // epilogue warps 2..5 of both CTAs; warp w reads TMEM lanes 32*(w%4) .. +31
+    const uint32_t q = warp & 3;
+    const uint32_t tempty0 = mapa_shared(tempty, 0);
+    int local = 0;
+    for (int tile = cl; tile < num_tiles; tile += ncl, ++local) {
+      int mb, nb;
+      tile_coords(tile, num_m, num_n, p.group_m, mb, nb);
+      const int acc = local & 1;
+      const uint32_t acc_phase = (local >> 1) & 1;
+      mbar_wait<true>(&tfull[acc], acc_phase, abort_flag, kErrTimeoutEpi);
+      tc_fence_after();
+      const int row = mb * 2 * BM + (int)rank * BM + q * 32 + lane;
+      epilogue_tile<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, row, row < p.M, nb, tile_n);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + acc * 8);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still address its barriers or tensor memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc2(tmem_base, 2 * BN);
+  }
+}
+
+template <bool A_MN, bool B_MN>
+int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st) {
+  auto kern = gemm_pair_kernel<A_MN, B_MN>;
+  static int max_clusters = 0;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(192);
+  cfg.dynamicSmemBytes = PairCfg::SMEM;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (!max_clusters) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM) != cudaSuccess)
+      return -1;
+    cfg.gridDim = dim3(2 * (mt_host::num_sms() / 2));
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, (const void*)kern, &cfg) != cudaSuccess || n <= 0) {
+      cudaGetLastError();
+      n = mt_host::num_sms() / 2;
+    }
+    const char* fc = getenv("MT_GEMM_PAIR_CLUSTERS");
+    if (fc && atoi(fc) > 0) n = atoi(fc);
+    const char* dbg = getenv("MT_GEMM_DEBUG");
+    if (dbg && dbg[0] == '1') fprintf(stderr, "gemm pair kernel: %d co-resident clusters\n", n);
+    max_clusters = n;
+  }
+  const int tile_n = p.gated ? PairCfg::BN / 2 : PairCfg::BN;
+  const int tiles = ((p.M + 2 * BM - 1) / (2 * BM)) * ((p.N + tile_n - 1) / tile_n);
+  const int clusters = tiles < max_clusters ? tiles : max_clusters;
+  cfg.gridDim = dim3(2 * clusters);
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, p) != cudaSuccess) return -1;
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
 template <int BN, bool A_MN, bool B_MN>
@@ -480,6 +690,19 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
   const int tiles256 = ((p.M + BM - 1) / BM) * ((p.N + 255) / 256);
   const bool wide = tiles256 >= mt_host::num_sms() || p.gated;
   const int BN = wide ? 256 : 128;
+  // Wide tiles run on SM pairs (MT_GEMM_PAIR=0 keeps them on single SMs).
+  static int pair_mode = -1;
+  if (pair_mode < 0) {
+    const char* e = getenv("MT_GEMM_PAIR");
+    pair_mode = (e && e[0] == '0') ? 0 : 1;
+  }
+  const bool pair = wide && pair_mode;
+  if (pair) {  // tile groups in units of 256-row blocks
+    const int num_m2 = (p.M + 2 * BM - 1) / (2 * BM);
+    const int gm = std::max(1, p.group_m / 2);
+    p.group_m = gm < num_m2 ? gm : num_m2;
+  }
+  const int b_rows = pair ? 128 : BN;  // K-major B box height
   CUtensorMap ta, tb;
   int rc = 0;
   if (mode == GEMM_NT) {  // A [M,K] K-major, B [N,K] K-major
@@ -487,20 +710,23 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
     if (p.gated)  // gate and up rows of one combined matrix, 128-row boxes
       rc |= make_map(&tb, B, p.u_off + p.N, p.K, ldb, 64, 128);
     else
-      rc |= make_map(&tb, B, p.N, p.K, ldb, 64, BN);
+      rc |= make_map(&tb, B, p.N, p.K, ldb, 64, b_rows);
     if (rc) return -1;
+    if (pair) return launch_pair<false, false>(ta, tb, p, st);
     return wide ? launch<256, false, false>(ta, tb, p, st) : launch<128, false, false>(ta, tb, p, st);
   }
   if (mode == GEMM_NN) {  // A [M,K] K-major, B stored [K,N]: MN-major
     rc |= make_map(&ta, A, p.M, p.K, lda, 64, BM);
     rc |= make_map(&tb, B, p.K, p.N, ldb, 64, 64);
     if (rc) return -1;
+    if (pair) return launch_pair<false, true>(ta, tb, p, st);
     return wide ? launch<256, false, true>(ta, tb, p, st) : launch<128, false, true>(ta, tb, p, st);
   }
   if (mode == GEMM_TN) {  // A stored [K,M], B stored [K,N]: both MN-major
     rc |= make_map(&ta, A, p.K, p.M, lda, 64, 64);
     rc |= make_map(&tb, B, p.K, p.N, ldb, 64, 64);
     if (rc) return -1;
+    if (pair) return launch_pair<true, true>(ta, tb, p, st);
     return wide ? launch<256, true, true>(ta, tb, p, st) : launch<128, true, true>(ta, tb, p, st);
   }
   (void)BN;
