@@ -112,6 +112,61 @@ def model_flops(shape, B, S):
     return layer, head, P_lin
 
 
+def gemm_algorithmic_bytes(shape, B, S, K, head_rows, fuse_top=True):
+    """Operand and result bytes of every GEMM launch of one step: each operand
+    read once and each result written once (bf16 activations and weights,
+    fp32 weight gradients and residual outputs; read-modify-write where the
+    epilogue adds to or rewrites its output). Returns (bytes, launches)."""
+    L, h, nq, nkv, d, F, V = shape[:7]
+    T = B * S
+    qkv = (nq + 2 * nkv) * d
+    fwd = ((T * h + qkv * h + T * qkv) * 2 +                       # QKV (+RoPE), bf16 out
+           (T * nq * d + h * nq * d) * 2 + T * h * 8 +              # O-proj, fp32 residual add
+           (T * h + 2 * F * h + 2 * T * F + T * F) * 2 +           # gate-up, writes g|u and act
+           (T * F + h * F) * 2 + T * h * 8)                        # down, fp32 residual add
+    bwd = ((T * h + T * F) * 2 + h * F * 4 +                       # dWd
+           (T * h + h * F) * 2 + 2 * T * 2 * F * 2 +               # d act -> (dg, du) in place over (g, u)
+           (2 * T * F + T * h) * 2 + 2 * F * h * 4 +               # dWg|Wu
+           (2 * T * F + 2 * F * h) * 2 + T * h * 4 +               # dm
+           (T * h + T * nq * d) * 2 + h * nq * d * 4 +             # dWo
+           (T * h + h * nq * d + T * nq * d) * 2 +                 # do
+           (T * qkv + T * h) * 2 + qkv * h * 4 +                   # dWqkv
+           (T * qkv + qkv * h) * 2 + T * h * 4)                    # dx
+    slices = (V + head_rows - 1) // head_rows
+    head = 0
+    for i in range(slices):
+        R = min(head_rows, V - i * head_rows)
+        head += 2 * ((T * h + R * h) * 2 + T * R * 4)              # logits, pass 1 and pass 2
+        head += (T * R + R * h) * 2 + T * h * (4 if i == 0 else 8)  # dX, accumulated over slices
+        head += (T * R + T * h) * 2 + R * h * 4                     # dW of the slice
+    top = L - K * ((L + K - 1) // K - 1)                            # layers of the top block
+    n_fwd = L + (L - top if fuse_top else L)
+    return n_fwd * fwd + L * bwd + head, 4 * n_fwd + 8 * L + 4 * slices
+
+
+def head_slice_rows(shape, esz):
+    """Rows of an LM-head vocab slice: the fewest equal slices (multiples of
+    256 rows) whose bytes fit one packed decoder layer (as the library sizes
+    them)."""
+    L, h, nq, nkv, d, F, V = shape[:7]
+    layer = (2 * h + (nq * d) * h * 2 + 2 * (nkv * d) * h + 3 * F * h) * esz
+    ns = max(1, (V * h * esz + layer - 1) // layer)
+    while True:
+        r = min(V, (((V + ns - 1) // ns) + 255) // 256 * 256)
+        if r * h * esz <= layer or r <= 256:
+            return r
+        ns += 1
+
+
+# DRAM traffic of the GEMM launches of one 8B step (B=2, S=4096, K=4), from
+# ncu (dram__bytes_read.sum + dram__bytes_write.sum over the 508 GEMM launches
+# of the second step of `python bench.py --steps 1 --warmup 1
+# --no-cpu-baseline`, cold cache between launches): 566.4 GB. Valid for the
+# paired-SM GEMM kernel as committed with that capture.
+GEMM_TRAFFIC_8B_STEP = 566.38e9
+GEMM_LAUNCHES_8B_STEP = 508
+
+
 def numa_pages(addrs) -> dict:
     """Pages per NUMA node of the mappings that contain the given host
     addresses (from /proc/self/numa_maps; empty when unavailable)."""
@@ -360,6 +415,10 @@ def main():
     t_head = max(head_f / (peak_tf * 1e12), (per_step_h2d - L * layer_h2d) / h2d_bw, (2.0 * V * h * 4) / d2h_bw)
     t_roof = L * t_layer + t_head
     ms_per_step = dev_ms / steps
+    gemm_bytes, gemm_launches = gemm_algorithmic_bytes(shape, B, S, K, head_slice_rows(shape, 2 if bf16 else 4),
+                                                       fuse_top=not args.no_fuse_top)
+    traffic_known = (args.workload == "llama8b" and (L, B, S, K) == (32, 2, 4096, 4) and bf16
+                     and not args.no_fuse_top and kst["n_gemm"] == GEMM_LAUNCHES_8B_STEP)
     line = {
         "metric": METRIC,
         "value": value,
@@ -381,8 +440,12 @@ def main():
                 "d2h_bytes_per_step": int(per_step_d2h + 4)},
         "gpu_launches": int(agg["n_launches"]),
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tf, "unit": "TFLOP/s",
-                     "frac": (gemm_tflops / peak_tf) if gemm_tflops else None, "traffic": None,
-                     "kernel": "gemm_kernel (tcgen05; all GEMM launches of one step, event-timed per launch)",
+                     "frac": (gemm_tflops / peak_tf) if gemm_tflops else None,
+                     "traffic": (GEMM_TRAFFIC_8B_STEP / GEMM_LAUNCHES_8B_STEP) if traffic_known else None,
+                     "traffic_unit": "bytes per launch (ncu, cold cache)",
+                     "algorithmic_bytes_per_launch": gemm_bytes / max(1, gemm_launches),
+                     "kernel": "gemm_pair_kernel / gemm_kernel (tcgen05; all GEMM launches of one step, "
+                               "event-timed per launch)",
                      "launches": kst["n_gemm"], "avg_launch_ms": kst["gemm_ms"] / max(1, kst["n_gemm"]),
                      "peak_kind": f"{peak_kind} bf16_tflops_sustained"},
         "step_roofline": {"t_roof_ms": t_roof * 1e3, "t_measured_ms": ms_per_step, "frac": t_roof * 1e3 / ms_per_step,

@@ -700,6 +700,32 @@ int grad_slot_end(Step& st, int g, size_t host_off, size_t bytes) {
   return MT_OK;
 }
 
+// Copy one finished range of a layer's gradients (packed offsets [off0,
+// off1) of the unit starting at u0) from gradient buffer g to the host, as
+// soon as the compute stream has produced it.
+int grad_piece(Step& st, int g, size_t u0, size_t off0, size_t off1) {
+  mt_ctx* ctx = st.ctx;
+  cudaEvent_t ready = next_event(ctx);
+  if (!ready) return set_err(ctx, MT_ERR_CUDA, "event pool");
+  CK(cudaEventRecord(ready, ctx->s_comp));
+  CK(cudaStreamWaitEvent(ctx->s_d2h, ready, 0));
+  {
+    SegScope sg(ctx, 2, ctx->s_d2h, (double)(off1 - off0));
+    CK(cudaMemcpyAsync((uint8_t*)st.host_grad + off0, (const uint8_t*)ctx->gbuf[g] + (off0 - u0), off1 - off0,
+                       cudaMemcpyDeviceToHost, ctx->s_d2h));
+  }
+  ctx->stats.d2h_bytes += (double)(off1 - off0);
+  ctx->stats.n_d2h += 1;
+  return MT_OK;
+}
+// After the last piece of gradient buffer g: it is free once the copies drain.
+int grad_slot_release(Step& st, int g) {
+  mt_ctx* ctx = st.ctx;
+  CK(cudaEventRecord(ctx->ev_gfree[g], ctx->s_d2h));
+  if (ctx->serial) CK(cudaStreamWaitEvent(ctx->s_comp, ctx->ev_gfree[g], 0));
+  return MT_OK;
+}
+
 int layer_backward(Step& st, int l, const LayerView& w) {
   mt_ctx* ctx = st.ctx;
   const Plan& p = ctx->P;
@@ -712,8 +738,12 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   float* G = ctx->gbuf[g];
   const size_t u0 = ctx->off_g[l][0];
   auto GT = [&](int t) { return (float*)((uint8_t*)G + (ctx->off_g[l][t] - u0)); };
+  // Gradient tensors go to the host in four contiguous packed ranges, each as
+  // soon as it is complete: [Wd], [Wg Wu], [Wo w_ffn], [w_attn Wq Wk Wv].
+  auto end_of = [&](int t) { return ctx->off_g[l][t] + tensor_numel(ctx->cfg, l, t) * 4; };
   // h_out = h_mid + act Wd^T
   CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dh_b, a.act, GT(8), nullptr, h, F, T, h, Fp, F));
+  CKR(grad_piece(st, g, u0, ctx->off_g[l][8], end_of(8)));
   {  // dact = dh Wd, turned into (dg, du) in place over (g, u) by the epilogue
     GemmParams bp{T, Fp, h, EPI_BF16, a.gu, nullptr, 2 * Fp, 0, 1};
     bp.swiglu_bwd = 1;
@@ -728,11 +758,13 @@ int layer_backward(Step& st, int l, const LayerView& w) {
     CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, F, h, T, 2 * Fp, h, h));
     CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu + Fp, a.m, GT(7), nullptr, F, h, T, 2 * Fp, h, h));
   }
+  CKR(grad_piece(st, g, u0, ctx->off_g[l][6], end_of(7)));
   CKR(gemm(ctx, GEMM_NN, EPI_F32, a.gu, w.wgu, ctx->dm, nullptr, T, h, 2 * Fp, 2 * Fp, h, h));
   // RMSNorm 2 (+ residual): dh_mid written over h_mid (row-local, in place)
   CKL(rmsnorm_bwd(a.hmid, w.w2, a.rstd2, ctx->dm, ctx->dh, a.hmid, ctx->dhmid_b, GT(5), ctx->norm_ws, T, h, s));
   // h_mid = x + o Wo^T
   CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dhmid_b, a.o, GT(4), nullptr, h, p.qd, T, h, p.qd, p.qd));
+  CKR(grad_piece(st, g, u0, ctx->off_g[l][4], end_of(5)));
   CKR(gemm(ctx, GEMM_NN, EPI_BF16, ctx->dhmid_b, w.wo, ctx->do_b, nullptr, T, p.qd, h, h, p.qd, p.qd));
   {
     OpTimer timer(ctx, 1, 2.5 * attn_flop(st, p));
@@ -745,8 +777,8 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   CKR(gemm(ctx, GEMM_NN, EPI_F32, ctx->dqkv, w.wqkv, ctx->dm, nullptr, T, h, p.qkv, p.qkv, h, h));
   // RMSNorm 1 (+ residual): new dh
   CKL(rmsnorm_bwd(x, w.w1, a.rstd1, ctx->dm, a.hmid, ctx->dh, ctx->dh_b, GT(0), ctx->norm_ws, T, h, s));
-  const size_t bytes = ctx->off_g[l][8] + tensor_numel(ctx->cfg, l, 8) * 4 - u0;
-  return grad_slot_end(st, g, u0, bytes);
+  CKR(grad_piece(st, g, u0, u0, end_of(3)));
+  return grad_slot_release(st, g);
 }
 
 // Debug aid: wait (bounded) for the compute stream after a unit and report
