@@ -376,9 +376,6 @@ __global__ void __launch_bounds__(384, 1)
       const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
                              fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const float m_new = mx * a.scale_log2;
-      // the previous P V product must be complete before O is touched
-      if (t > 0) mbar_wait(&o_done[side], (t - 1) & 1, abort_flag, kErrTimeoutAttn);
-      tc_fence_after();
       // The rescale touches O through warp-collective tensor-memory loads and
       // stores, so the decision is taken per warp: if any row of the warp
       // needs a new reference maximum, every row of the warp moves its
@@ -388,6 +385,11 @@ __global__ void __launch_bounds__(384, 1)
         const float alpha = (m_ref == -INFINITY) ? 0.f : ex2_approx(m_ref - m_use);
         l *= alpha;
         if (t > 0) {
+          // O may be touched only once the previous P V product is complete.
+          // P needs no such wait: S(t) was issued after that product and the
+          // tensor core runs one thread's operations in order.
+          mbar_wait(&o_done[side], (t - 1) & 1, abort_flag, kErrTimeoutAttn);
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < (D + 31) / 32; ++c) {
             uint32_t v[32];
