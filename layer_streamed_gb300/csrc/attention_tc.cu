@@ -459,8 +459,9 @@ __global__ void __launch_bounds__(384, 1)
 // 128-row tile. The MMA thread issues the score products of sub-tile i+1
 // before the gradient products of sub-tile i, so elementwise work overlaps
 // the tensor core. The elementwise warps write P^T and dS^T (or dS) as bf16
-// pairs over the first 32 columns of their S and dP buffers, and the
-// gradient products read them from tensor memory as their A operand; tensor
+// pairs over columns of their S and dP buffers that they have already read
+// (see packed_col), and the gradient products read them from tensor memory
+// as their A operand; tensor
 // core operations of one thread run in issue order, so the score products of
 // sub-tile i+2 (which overwrite those buffers) follow the gradient products
 // of sub-tile i. Operand layout of a [64 rows][64] box: 8 KB, 128-byte swizzle.
@@ -501,6 +502,13 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
+// Packed bf16 operands in tensor memory: each elementwise warpgroup writes
+// its 32 columns as 16 pairs over the first half of its own 32 columns of the
+// buffer (warpgroup A columns [0, 16), B [32, 48)), i.e. only over values it
+// has already read itself. K step kk (16 wide) of the operand therefore sits
+// at packed column kk * 8 for kk < 2 and 32 + (kk - 2) * 8 after.
+__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 2 ? kk * 8 : 32 + (kk - 2) * 8; }
+
 // 32 values of one row as 16 bf16 pairs into tensor-memory columns [col, col+16).
 __device__ __forceinline__ void tmem_st_bf16x32(uint32_t col, const float (&v)[32]) {
   uint32_t pk[16];
@@ -511,8 +519,8 @@ __device__ __forceinline__ void tmem_st_bf16x32(uint32_t col, const float (&v)[3
 
 // dK/dV pass: CTA = (128-row KV tile kt, KV head g, sequence b); loop over the
 // query heads of the group and the 64-row query sub-tiles at or after kt.
-// TMEM: S^T [2 x 64] +0 (P^T over its first 32), dP^T [2 x 64] +128 (dS^T
-// over its first 32), dV +256, dK +384.
+// TMEM: S^T [2 x 64] +0 (P^T packed over it), dP^T [2 x 64] +128 (dS^T
+// packed over it), dV +256, dK +384.
 template <int D>
 struct DkvSmem {
   static constexpr int K = 0;
@@ -613,8 +621,8 @@ __global__ void __launch_bounds__(384, 1)
 #pragma unroll
         for (int kk = 0; kk < SUB / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q  (A operands in TMEM)
           const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_ts(tmem + 256, tmem + buf * 64 + kk * 8, mnmaj_desc_sub(dout, kk), IDESC_G, acc);
-          tc_mma_ts(tmem + 384, tmem + 128 + buf * 64 + kk * 8, mnmaj_desc_sub(q, kk), IDESC_G, acc);
+          tc_mma_ts(tmem + 256, tmem + buf * 64 + packed_col(kk), mnmaj_desc_sub(dout, kk), IDESC_G, acc);
+          tc_mma_ts(tmem + 384, tmem + 128 + buf * 64 + packed_col(kk), mnmaj_desc_sub(q, kk), IDESC_G, acc);
         }
         tc_commit(&pd_done[buf]);
         tc_commit(&qdo_empty[st]);
@@ -659,17 +667,23 @@ __global__ void __launch_bounds__(384, 1)
       tmem_ld_wait();
       float p[32], ds[32];
       const bool need_mask = q0 + cbase < srow + 1;  // padded query rows have lse2 = +inf
+      float lse_c[32], del_c[32];  // this warpgroup's 32 columns, 16-byte loads (the stage is 512-byte aligned)
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 l4 = ((const float4*)(s_lse + cbase))[i], d4 = ((const float4*)(s_delta + cbase))[i];
+        lse_c[4 * i] = l4.x, lse_c[4 * i + 1] = l4.y, lse_c[4 * i + 2] = l4.z, lse_c[4 * i + 3] = l4.w;
+        del_c[4 * i] = d4.x, del_c[4 * i + 1] = d4.y, del_c[4 * i + 2] = d4.z, del_c[4 * i + 3] = d4.w;
+      }
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        const int col = cbase + i;
-        float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -s_lse[col]));
-        if (need_mask && q0 + col < srow) pv = 0.f;  // query must be at or after the key
+        float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -lse_c[i]));
+        if (need_mask && q0 + cbase + i < srow) pv = 0.f;  // query must be at or after the key
         p[i] = pv;
-        ds[i] = pv * (__uint_as_float(dv[i]) - s_delta[col]);
+        ds[i] = pv * (__uint_as_float(dv[i]) - del_c[i]);
       }
       __syncwarp();
-      tmem_st_bf16x32(tmem + lane_base + buf * 64 + half * 16, p);
-      tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + half * 16, ds);
+      tmem_st_bf16x32(tmem + lane_base + buf * 64 + cbase, p);
+      tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + cbase, ds);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
@@ -696,7 +710,7 @@ __global__ void __launch_bounds__(384, 1)
 
 // dQ pass: CTA = (128-row query tile qt, query head j, sequence b); loop over
 // the 64-row KV sub-tiles at or before the tile's last row.
-// TMEM: S [2 x 64] +0, dP [2 x 64] +128 (dS over its first 32), dQ +256.
+// TMEM: S [2 x 64] +0, dP [2 x 64] +128 (dS packed over it), dQ +256.
 template <int D>
 struct DqSmem {
   static constexpr int Q = 0;
@@ -787,7 +801,7 @@ __global__ void __launch_bounds__(384, 1)
         const uint8_t* kt = sm + L::K0 + st * sub_bytes<D>();
 #pragma unroll
         for (int kk = 0; kk < SUB / 16; ++kk)  // dQ += dS K  (dS in TMEM)
-          tc_mma_ts(tmem + 256, tmem + 128 + buf * 64 + kk * 8, mnmaj_desc_sub(kt, kk), IDESC_G,
+          tc_mma_ts(tmem + 256, tmem + 128 + buf * 64 + packed_col(kk), mnmaj_desc_sub(kt, kk), IDESC_G,
                     (i > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&g_done[buf]);
         tc_commit(&kv_empty[st]);
@@ -843,7 +857,7 @@ __global__ void __launch_bounds__(384, 1)
         ds[i] = pv * (__uint_as_float(dv[i]) - dl);
       }
       __syncwarp();
-      tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + half * 16, ds);
+      tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + half * 32, ds);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
