@@ -709,18 +709,26 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // dQ pass: CTA = (128-row query tile qt, query head j, sequence b); loop over
-// the 64-row KV sub-tiles at or before the tile's last row.
-// TMEM: S [2 x 64] +0, dP [2 x 64] +128 (dS packed over it), dQ +256.
+// the 128-row KV tiles 0..qt (every product is 128 wide: narrower tcgen05
+// products run well below the tensor core's rate). TMEM: S [2 x 128] +0
+// (dS packed over each warpgroup's own first 32 columns), dP [128] +256,
+// dQ +384. Once both warpgroups have read dP(t), the MMA thread issues
+// S(t+1) and dP(t+1), so they run while the elementwise warps work on t;
+// dQ += dS(t) K(t) follows when dS(t) is written.
 template <int D>
 struct DqSmem {
   static constexpr int Q = 0;
   static constexpr int DO = Q + tile_bytes<D>();
-  static constexpr int K0 = DO + tile_bytes<D>();             // [kStages]
-  static constexpr int V0 = K0 + kStages * sub_bytes<D>();    // [kStages]
-  static constexpr int BAR = V0 + kStages * sub_bytes<D>();
+  static constexpr int K0 = DO + tile_bytes<D>();   // [2] 128-row K tiles
+  static constexpr int V0 = K0 + 2 * tile_bytes<D>();  // [2] 128-row V tiles
+  static constexpr int BAR = V0 + 2 * tile_bytes<D>();
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
 };
+
+// K step kk (16 KV rows) of the packed dS operand: warpgroup kk / 4 wrote
+// its 64 columns as 32 pairs at the start of its own 64-column range.
+__device__ __forceinline__ uint32_t packed_col128(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -732,33 +740,36 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* kv_full = bars + 1;                 // [kStages]
-  uint64_t* kv_empty = bars + 1 + kStages;      // [kStages]
-  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2]
-  uint64_t* p_full = bars + 3 + 2 * kStages;    // [2]
-  uint64_t* g_done = bars + 5 + 2 * kStages;    // [2]
-  uint32_t* tmem_slot = (uint32_t*)(bars + 7 + 2 * kStages);
+  uint64_t* k_full = bars + 1;   // [2]
+  uint64_t* k_empty = bars + 3;  // [2]
+  uint64_t* v_full = bars + 5;   // [2]
+  uint64_t* v_empty = bars + 7;  // [2]
+  uint64_t* s_full = bars + 9;   // [2]: S(t) and dP(t) ready
+  uint64_t* dp_free = bars + 11;
+  uint64_t* p_full = bars + 12;
+  uint64_t* g_done = bars + 13;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 14);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int nqt = (a.S + TILE - 1) / TILE;
   const int qt = nqt - 1 - (int)blockIdx.x;  // longest tiles first
   const int j = blockIdx.y, b = blockIdx.z;
   const int g = j / (a.nq / a.nkv);
-  const int nsub_all = (a.S + SUB - 1) / SUB;
-  const int iters = min(2 * qt + 2, nsub_all);  // KV sub-tiles 0 .. last one at or before the tile's end
+  const int iters = qt + 1;  // KV tiles at or before the query tile
   const uint32_t warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < kStages; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
-    }
     for (int i = 0; i < 2; ++i) {
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
-      mbar_init(&g_done[i], 1);
     }
+    mbar_init(dp_free, 8);
+    mbar_init(p_full, 8);
+    mbar_init(g_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -781,52 +792,64 @@ __global__ void __launch_bounds__(384, 1)
       load_head_tile<D>(sm + L::Q, &tq, q_full, j, qt * TILE, b);
       load_head_tile<D>(sm + L::DO, &tdo, q_full, j, qt * TILE, b);
       for (int it = 0; it < iters; ++it) {
-        const int st = it % kStages;
-        mbar_wait(&kv_empty[st], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(&kv_full[st], 2 * sub_bytes<D>());
-        load_head_sub<D>(sm + L::K0 + st * sub_bytes<D>(), &tk, &kv_full[st], g, it * SUB, b);
-        load_head_sub<D>(sm + L::V0 + st * sub_bytes<D>(), &tv, &kv_full[st], g, it * SUB, b);
+        const int st = it & 1;
+        const uint32_t free_par = ((it >> 1) & 1) ^ 1;
+        mbar_wait(&v_empty[st], free_par, abort_flag, kErrTimeoutAttn);  // V frees first (after dP)
+        mbar_arrive_expect_tx(&v_full[st], tile_bytes<D>());
+        load_head_tile<D>(sm + L::V0 + st * tile_bytes<D>(), &tv, &v_full[st], g, it * TILE, b);
+        mbar_wait(&k_empty[st], free_par, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&k_full[st], tile_bytes<D>());
+        load_head_tile<D>(sm + L::K0 + st * tile_bytes<D>(), &tk, &k_full[st], g, it * TILE, b);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = make_idesc(128, SUB, false, false);
+      constexpr uint32_t IDESC_S = make_idesc(128, 128, false, false);
       constexpr uint32_t IDESC_G = make_idesc(128, D < 64 ? 64 : D, false, true);
       constexpr int KS = D / 16;
-      auto issue_grad = [&](int i) {
-        const int buf = i & 1, st = i % kStages;
-        mbar_wait(&p_full[buf], (i >> 1) & 1, abort_flag, kErrTimeoutAttn);
-        tc_fence_after();
-        const uint8_t* kt = sm + L::K0 + st * sub_bytes<D>();
+      auto issue_scores = [&](int t) {  // S(t) = Q K_t^T into S[t & 1]; dP(t) = dO V_t^T
+        const int st = t & 1;
+        const uint8_t* kt = sm + L::K0 + st * tile_bytes<D>();
+        const uint8_t* vt = sm + L::V0 + st * tile_bytes<D>();
 #pragma unroll
-        for (int kk = 0; kk < SUB / 16; ++kk)  // dQ += dS K  (dS in TMEM)
-          tc_mma_ts(tmem + 256, tmem + 128 + buf * 64 + packed_col(kk), mnmaj_desc_sub(kt, kk), IDESC_G,
-                    (i > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(&g_done[buf]);
-        tc_commit(&kv_empty[st]);
+        for (int kk = 0; kk < KS; ++kk)
+          tc_mma(tmem + st * 128, kmaj_desc(sm + L::Q, kk), kmaj_desc(kt, kk), IDESC_S, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)
+          tc_mma(tmem + 256, kmaj_desc(sm + L::DO, kk), kmaj_desc(vt, kk), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(&s_full[st]);
+        tc_commit(&v_empty[st]);
       };
       mbar_wait(q_full, 0, abort_flag, kErrTimeoutAttn);
+      mbar_wait(&k_full[0], 0, abort_flag, kErrTimeoutAttn);
+      mbar_wait(&v_full[0], 0, abort_flag, kErrTimeoutAttn);
+      tc_fence_after();
+      issue_scores(0);
       for (int it = 0; it < iters; ++it) {
-        const int buf = it & 1, st = it % kStages;
-        mbar_wait(&kv_full[st], (it / kStages) & 1, abort_flag, kErrTimeoutAttn);
-        tc_fence_after();
-        const uint8_t* kt = sm + L::K0 + st * sub_bytes<D>();
-        const uint8_t* vt = sm + L::V0 + st * sub_bytes<D>();
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {  // S = Q K^T ; dP = dO V^T
-          tc_mma(tmem + buf * 64, kmaj_desc(sm + L::Q, kk), kmaj_desc_sub(kt, kk), IDESC_S, kk > 0 ? 1u : 0u);
-          tc_mma(tmem + 128 + buf * 64, kmaj_desc(sm + L::DO, kk), kmaj_desc_sub(vt, kk), IDESC_S,
-                 kk > 0 ? 1u : 0u);
+        if (it + 1 < iters) {
+          const int st1 = (it + 1) & 1;
+          const uint32_t par1 = ((it + 1) >> 1) & 1;
+          mbar_wait(&k_full[st1], par1, abort_flag, kErrTimeoutAttn);
+          mbar_wait(&v_full[st1], par1, abort_flag, kErrTimeoutAttn);
+          mbar_wait(dp_free, it & 1, abort_flag, kErrTimeoutAttn);  // both warpgroups have read dP(it)
+          tc_fence_after();
+          issue_scores(it + 1);  // S[(it+1)&1] held dS(it-1), consumed by dQ products issued before
         }
-        tc_commit(&s_full[buf]);
-        if (it > 0) issue_grad(it - 1);
+        mbar_wait(p_full, it & 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+        const uint8_t* kt = sm + L::K0 + (it & 1) * tile_bytes<D>();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk)  // dQ += dS K  (dS in TMEM)
+          tc_mma_ts(tmem + 384, tmem + (it & 1) * 128 + packed_col128(kk), mnmaj_desc(kt, kk), IDESC_G,
+                    (it > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(g_done);
+        tc_commit(&k_empty[it & 1]);
       }
-      issue_grad(iters - 1);
     }
     __syncwarp();
   } else if (warp >= 4) {
-    const int half = warp >= 8 ? 1 : 0;
+    const int half = warp >= 8 ? 1 : 0;  // which 64 of the 128 KV columns
     const uint32_t q4 = warp & 3;
     const int r = q4 * 32 + lane;
     const int trow = qt * TILE + r;
@@ -837,38 +860,48 @@ __global__ void __launch_bounds__(384, 1)
     const float dl = row_ok ? a.delta[ri] : 0.f;
     for (int it = 0; it < iters; ++it) {
       const int buf = it & 1;
+      const uint32_t s_col = tmem + lane_base + buf * 128 + half * 64;
+      const uint32_t dp_col = tmem + lane_base + 256 + half * 64;
       mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
-      uint32_t sv[32], dv[32];
+      uint32_t dv0[32], dv1[32], sv0[32], sv1[32];
       __syncwarp();
-      tmem_ld32(tmem + lane_base + buf * 64 + half * 32, sv);
-      tmem_ld32(tmem + lane_base + 128 + buf * 64 + half * 32, dv);
+      tmem_ld32(dp_col, dv0);
+      tmem_ld32(dp_col + 32, dv1);
+      tmem_ld32(s_col, sv0);
+      tmem_ld32(s_col + 32, sv1);
       tmem_ld_wait();
-      const int kv0 = it * SUB + half * 32;
-      const bool need_mask = (kv0 + 31 > qt * TILE) || (kv0 + 32 > a.S);
-      float ds[32];
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dp_free);  // dP(it+1) may now be written
+      const int kv0 = it * TILE + half * 64;
+      const bool need_mask = it == qt;  // the diagonal tile (also holds the sequence tail)
+      float ds0[32], ds1[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) {
-        float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -lse2));
+        float p0 = ex2_approx(fmaf(__uint_as_float(sv0[i]), a.scale_log2, -lse2));
+        float p1 = ex2_approx(fmaf(__uint_as_float(sv1[i]), a.scale_log2, -lse2));
         if (need_mask) {
-          const int kv = kv0 + i;
-          if (kv > trow || kv >= a.S) pv = 0.f;
+          if (kv0 + i > trow || kv0 + i >= a.S) p0 = 0.f;
+          if (kv0 + 32 + i > trow || kv0 + 32 + i >= a.S) p1 = 0.f;
         }
-        ds[i] = pv * (__uint_as_float(dv[i]) - dl);
+        ds0[i] = p0 * (__uint_as_float(dv0[i]) - dl);
+        ds1[i] = p1 * (__uint_as_float(dv1[i]) - dl);
       }
       __syncwarp();
-      tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + half * 32, ds);
+      tmem_st_bf16x32(s_col, ds0);       // packed over this warpgroup's own S columns, already read
+      tmem_st_bf16x32(s_col + 16, ds1);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[buf]);
+      if (lane == 0) mbar_arrive(p_full);
     }
-    mbar_wait(&g_done[(iters - 1) & 1], ((iters - 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
+    mbar_wait(g_done, (iters - 1) & 1, abort_flag, kErrTimeoutAttn);
     tc_fence_after();
     // epilogue: the two warpgroups share the head-dim columns
     uint16_t* orow = a.dq + ((size_t)b * a.S + trow) * a.ldq + (size_t)j * D;
     const float2* tab = a.rope_tab ? a.rope_tab + (size_t)(row_ok ? trow : 0) * (D / 2) : nullptr;
-    store_grad_row<D>(orow, tmem + lane_base + 256, row_ok, a.scale, tab, half, 2);
+    store_grad_row<D>(orow, tmem + lane_base + 384, row_ok, a.scale, tab, half, 2);
   }
   tc_fence_before();
   __syncthreads();
@@ -949,12 +982,11 @@ template <int D>
 int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
                AttnArgs& a, float* delta, cudaStream_t st) {
   // dK/dV pass: K, V in 128-row tiles, Q, dO in 64-row sub-tiles;
-  // dQ pass: Q, dO in 128-row tiles, K, V in 64-row sub-tiles.
-  CUtensorMap tq64, tdo64, tk128, tv128, tq128, tdo128, tk64, tv64;
+  // dQ pass: everything in 128-row tiles.
+  CUtensorMap tq64, tdo64, tk128, tv128, tq128, tdo128;
   if (head_map(&tq64, q, D, a.nq, a.S, a.B, a.ldq, 64) || head_map(&tdo64, dout, D, a.nq, a.S, a.B, a.ldo, 64) ||
       head_map(&tk128, k, D, a.nkv, a.S, a.B, a.ldkv) || head_map(&tv128, v, D, a.nkv, a.S, a.B, a.ldkv) ||
-      head_map(&tq128, q, D, a.nq, a.S, a.B, a.ldq) || head_map(&tdo128, dout, D, a.nq, a.S, a.B, a.ldo) ||
-      head_map(&tk64, k, D, a.nkv, a.S, a.B, a.ldkv, 64) || head_map(&tv64, v, D, a.nkv, a.S, a.B, a.ldkv, 64))
+      head_map(&tq128, q, D, a.nq, a.S, a.B, a.ldq) || head_map(&tdo128, dout, D, a.nq, a.S, a.B, a.ldo))
     return -1;
   static bool init = false;
   if (!init) {
@@ -971,7 +1003,7 @@ int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const ui
   a.lse2 = lse2;
   const int nt = (a.S + TILE - 1) / TILE;
   attn_bwd_dkv_tc_kernel<D><<<dim3(nt, a.nkv, a.B), 384, DkvSmem<D>::ALLOC, st>>>(tq64, tk128, tv128, tdo64, a);
-  attn_bwd_dq_tc_kernel<D><<<dim3(nt, a.nq, a.B), 384, DqSmem<D>::ALLOC, st>>>(tq128, tk64, tv64, tdo128, a);
+  attn_bwd_dq_tc_kernel<D><<<dim3(nt, a.nq, a.B), 384, DqSmem<D>::ALLOC, st>>>(tq128, tk128, tv128, tdo128, a);
   count_launches(3);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
