@@ -714,13 +714,16 @@ __global__ void __launch_bounds__(384, 1)
 // (dS packed over each warpgroup's own first 32 columns), dP [128] +256,
 // dQ +384. Once both warpgroups have read dP(t), the MMA thread issues
 // S(t+1) and dP(t+1), so they run while the elementwise warps work on t;
-// dQ += dS(t) K(t) follows when dS(t) is written.
+// dQ += dS(t) K(t) follows when dS(t) is written. K has three stages (it is
+// held until its dQ product), V two (released after its dP product).
+constexpr int kDqKStages = 3;  // K is held until its dQ product; V only until its dP product
+
 template <int D>
 struct DqSmem {
   static constexpr int Q = 0;
   static constexpr int DO = Q + tile_bytes<D>();
-  static constexpr int K0 = DO + tile_bytes<D>();   // [2] 128-row K tiles
-  static constexpr int V0 = K0 + 2 * tile_bytes<D>();  // [2] 128-row V tiles
+  static constexpr int K0 = DO + tile_bytes<D>();                   // [3] 128-row K tiles
+  static constexpr int V0 = K0 + kDqKStages * tile_bytes<D>();      // [2] 128-row V tiles
   static constexpr int BAR = V0 + 2 * tile_bytes<D>();
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
@@ -740,15 +743,15 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* q_full = bars + 0;
-  uint64_t* k_full = bars + 1;   // [2]
-  uint64_t* k_empty = bars + 3;  // [2]
-  uint64_t* v_full = bars + 5;   // [2]
-  uint64_t* v_empty = bars + 7;  // [2]
-  uint64_t* s_full = bars + 9;   // [2]: S(t) and dP(t) ready
-  uint64_t* dp_free = bars + 11;
-  uint64_t* p_full = bars + 12;
-  uint64_t* g_done = bars + 13;
-  uint32_t* tmem_slot = (uint32_t*)(bars + 14);
+  uint64_t* k_full = bars + 1;   // [3]
+  uint64_t* k_empty = bars + 4;  // [3]
+  uint64_t* v_full = bars + 7;   // [2]
+  uint64_t* v_empty = bars + 9;  // [2]
+  uint64_t* s_full = bars + 11;  // [2]: S(t) and dP(t) ready
+  uint64_t* dp_free = bars + 13;
+  uint64_t* p_full = bars + 14;
+  uint64_t* g_done = bars + 15;
+  uint32_t* tmem_slot = (uint32_t*)(bars + 16);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int nqt = (a.S + TILE - 1) / TILE;
@@ -760,9 +763,11 @@ __global__ void __launch_bounds__(384, 1)
 
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kDqKStages; ++i) {
       mbar_init(&k_full[i], 1);
       mbar_init(&k_empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
@@ -792,14 +797,13 @@ __global__ void __launch_bounds__(384, 1)
       load_head_tile<D>(sm + L::Q, &tq, q_full, j, qt * TILE, b);
       load_head_tile<D>(sm + L::DO, &tdo, q_full, j, qt * TILE, b);
       for (int it = 0; it < iters; ++it) {
-        const int st = it & 1;
-        const uint32_t free_par = ((it >> 1) & 1) ^ 1;
-        mbar_wait(&v_empty[st], free_par, abort_flag, kErrTimeoutAttn);  // V frees first (after dP)
-        mbar_arrive_expect_tx(&v_full[st], tile_bytes<D>());
-        load_head_tile<D>(sm + L::V0 + st * tile_bytes<D>(), &tv, &v_full[st], g, it * TILE, b);
-        mbar_wait(&k_empty[st], free_par, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(&k_full[st], tile_bytes<D>());
-        load_head_tile<D>(sm + L::K0 + st * tile_bytes<D>(), &tk, &k_full[st], g, it * TILE, b);
+        const int sv = it & 1, sk = it % kDqKStages;
+        mbar_wait(&v_empty[sv], ((it >> 1) & 1) ^ 1, abort_flag, kErrTimeoutAttn);  // V frees first (after dP)
+        mbar_arrive_expect_tx(&v_full[sv], tile_bytes<D>());
+        load_head_tile<D>(sm + L::V0 + sv * tile_bytes<D>(), &tv, &v_full[sv], g, it * TILE, b);
+        mbar_wait(&k_empty[sk], ((it / kDqKStages) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&k_full[sk], tile_bytes<D>());
+        load_head_tile<D>(sm + L::K0 + sk * tile_bytes<D>(), &tk, &k_full[sk], g, it * TILE, b);
       }
     }
     __syncwarp();
@@ -810,7 +814,7 @@ __global__ void __launch_bounds__(384, 1)
       constexpr int KS = D / 16;
       auto issue_scores = [&](int t) {  // S(t) = Q K_t^T into S[t & 1]; dP(t) = dO V_t^T
         const int st = t & 1;
-        const uint8_t* kt = sm + L::K0 + st * tile_bytes<D>();
+        const uint8_t* kt = sm + L::K0 + (t % kDqKStages) * tile_bytes<D>();
         const uint8_t* vt = sm + L::V0 + st * tile_bytes<D>();
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk)
@@ -828,23 +832,22 @@ __global__ void __launch_bounds__(384, 1)
       issue_scores(0);
       for (int it = 0; it < iters; ++it) {
         if (it + 1 < iters) {
-          const int st1 = (it + 1) & 1;
-          const uint32_t par1 = ((it + 1) >> 1) & 1;
-          mbar_wait(&k_full[st1], par1, abort_flag, kErrTimeoutAttn);
-          mbar_wait(&v_full[st1], par1, abort_flag, kErrTimeoutAttn);
+          const int t1 = it + 1;
+          mbar_wait(&k_full[t1 % kDqKStages], (t1 / kDqKStages) & 1, abort_flag, kErrTimeoutAttn);
+          mbar_wait(&v_full[t1 & 1], (t1 >> 1) & 1, abort_flag, kErrTimeoutAttn);
           mbar_wait(dp_free, it & 1, abort_flag, kErrTimeoutAttn);  // both warpgroups have read dP(it)
           tc_fence_after();
           issue_scores(it + 1);  // S[(it+1)&1] held dS(it-1), consumed by dQ products issued before
         }
         mbar_wait(p_full, it & 1, abort_flag, kErrTimeoutAttn);
         tc_fence_after();
-        const uint8_t* kt = sm + L::K0 + (it & 1) * tile_bytes<D>();
+        const uint8_t* kt = sm + L::K0 + (it % kDqKStages) * tile_bytes<D>();
 #pragma unroll
         for (int kk = 0; kk < TILE / 16; ++kk)  // dQ += dS K  (dS in TMEM)
           tc_mma_ts(tmem + 384, tmem + (it & 1) * 128 + packed_col128(kk), mnmaj_desc(kt, kk), IDESC_G,
                     (it > 0 || kk > 0) ? 1u : 0u);
         tc_commit(g_done);
-        tc_commit(&k_empty[it & 1]);
+        tc_commit(&k_empty[it % kDqKStages]);
       }
     }
     __syncwarp();
