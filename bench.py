@@ -366,9 +366,13 @@ def main():
     wall0 = time.perf_counter()
     ev0.record(comp)
     losses = []
+    host_ms = []  # per step: wall time of the call minus its device span (host preparation and finishing)
     for _ in range(args.steps):
+        t_call = time.perf_counter()
         losses.append(sess.step(tok, lab, K))
+        call_ms = (time.perf_counter() - t_call) * 1e3
         st = sess.stats()
+        host_ms.append(call_ms - st["step_ms"])
         for k, v in st.items():
             agg[k] = agg.get(k, 0) + v
     ev1.record(d2h_stream)
@@ -456,6 +460,7 @@ def main():
                           else None,
                           "gemm_ms_per_step": kst["gemm_ms"], "attn_ms_per_step": kst["attn_ms"],
                           "compute_busy_ms_per_step": agg["compute_busy_ms"] / steps,
+                          "host_ms_per_step": float(np.median(host_ms)),
                           # effective rates of the step's own copies (bytes / summed copy time)
                           "h2d_copy_gbs": agg["h2d_bytes"] / max(1e-9, agg["h2d_ms"]) / 1e6,
                           "d2h_copy_gbs": agg["d2h_bytes"] / max(1e-9, agg["d2h_ms"]) / 1e6},

@@ -915,34 +915,42 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // Per (sequence b, query head j, position t < Sp): delta = sum_e dO O over
-// the head's columns (one warp per row) and lse2 = lse * log2(e); padding
-// rows t >= S get delta 0 and lse2 +inf. Layout [B][nq][Sp] each.
+// the head's columns and lse2 = lse * log2(e); padding rows t >= S get delta
+// 0 and lse2 +inf. Layout [B][nq][Sp] each. Sixteen lanes per row, 16-byte
+// loads (head dims of 64 and 128; narrower heads use 4-byte loads).
 __global__ void attn_delta_tc_kernel(const uint16_t* __restrict__ o, const uint16_t* __restrict__ dout,
                                      const float* __restrict__ lse, float* __restrict__ delta,
                                      float* __restrict__ lse2, int B, int S, int Sp, int nq, int d, int ldo) {
-  const size_t wid = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  if (wid >= (size_t)B * Sp * nq) return;
-  const int j = (int)(wid % nq);
-  const int t = (int)((wid / nq) % Sp);
-  const int b = (int)(wid / ((size_t)nq * Sp));
+  const size_t row = ((size_t)blockIdx.x * blockDim.x + threadIdx.x) >> 4;
+  const int sub = threadIdx.x & 15;
+  const bool valid = row < (size_t)B * Sp * nq;  // every lane reaches the shuffles below
+  const int j = (int)(row % nq);
+  const int t = (int)((row / nq) % Sp);
+  const int b = (int)(row / ((size_t)nq * Sp));
   const size_t ri = ((size_t)b * nq + j) * Sp + t;
-  if (t >= S) {
-    if (lane_id() == 0) {
-      delta[ri] = 0.f;
-      lse2[ri] = INFINITY;
-    }
-    return;
-  }
-  const size_t off = ((size_t)b * S + t) * ldo + (size_t)j * d;
   float s = 0.f;
-  for (int e = lane_id() * 2; e < d; e += 64) {
-    const uint32_t ov = *(const uint32_t*)(o + off + e), gv = *(const uint32_t*)(dout + off + e);
-    s += bf2f(ov & 0xffff) * bf2f(gv & 0xffff) + bf2f(ov >> 16) * bf2f(gv >> 16);
+  if (valid && t < S) {
+    const size_t off = ((size_t)b * S + t) * ldo + (size_t)j * d;
+    if ((d & 63) == 0 && (ldo & 7) == 0) {
+      for (int e = sub * 8; e < d; e += 128) {
+        const uint4 ov = *(const uint4*)(o + off + e), gv = *(const uint4*)(dout + off + e);
+        const uint32_t oa[4] = {ov.x, ov.y, ov.z, ov.w}, ga[4] = {gv.x, gv.y, gv.z, gv.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+          s += bf2f(oa[k] & 0xffff) * bf2f(ga[k] & 0xffff) + bf2f(oa[k] >> 16) * bf2f(ga[k] >> 16);
+      }
+    } else {
+      for (int e = sub * 2; e < d; e += 32) {
+        const uint32_t ov = *(const uint32_t*)(o + off + e), gv = *(const uint32_t*)(dout + off + e);
+        s += bf2f(ov & 0xffff) * bf2f(gv & 0xffff) + bf2f(ov >> 16) * bf2f(gv >> 16);
+      }
+    }
   }
-  s = warp_sum(s);
-  if (lane_id() == 0) {
+#pragma unroll
+  for (int m = 8; m >= 1; m >>= 1) s += __shfl_xor_sync(0xffffffffu, s, m);
+  if (valid && sub == 0) {
     delta[ri] = s;
-    lse2[ri] = lse[((size_t)b * nq + j) * S + t] * 1.4426950408889634f;
+    lse2[ri] = t < S ? lse[((size_t)b * nq + j) * S + t] * 1.4426950408889634f : INFINITY;
   }
 }
 
@@ -1000,7 +1008,7 @@ int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const ui
   const int Sp = pad64(a.S);
   const size_t rows = (size_t)a.B * Sp * a.nq;
   float* lse2 = delta + rows;
-  attn_delta_tc_kernel<<<(unsigned)((rows * 32 + 255) / 256), 256, 0, st>>>(o, dout, a.lse_in, delta, lse2, a.B, a.S,
+  attn_delta_tc_kernel<<<(unsigned)((rows * 16 + 255) / 256), 256, 0, st>>>(o, dout, a.lse_in, delta, lse2, a.B, a.S,
                                                                             Sp, a.nq, D, a.ldo);
   a.delta = delta;
   a.lse2 = lse2;
