@@ -431,7 +431,19 @@ __global__ void ce_stats_kernel(const float* __restrict__ z, int R, int ld, int 
   const size_t t = blockIdx.x;
   const float* zr = z + t * ld;
   float m = -INFINITY, s = 0.f;
-  for (int c = threadIdx.x; c < R; c += blockDim.x) lse_merge(m, s, zr[c], 1.f);
+  int c0 = 0;
+  if ((ld & 3) == 0 && ((uintptr_t)z & 15) == 0) {  // 16-byte loads, one merge per four values
+    const float4* z4 = (const float4*)zr;
+    const int R4 = R >> 2;
+#pragma unroll 4
+    for (int i = threadIdx.x; i < R4; i += blockDim.x) {
+      const float4 v = z4[i];
+      const float mx = fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w));
+      lse_merge(m, s, mx, (__expf(v.x - mx) + __expf(v.y - mx)) + (__expf(v.z - mx) + __expf(v.w - mx)));
+    }
+    c0 = R4 * 4;
+  }
+  for (int c = c0 + threadIdx.x; c < R; c += blockDim.x) lse_merge(m, s, zr[c], 1.f);
   // warp merge
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -476,16 +488,33 @@ __global__ void sum_scaled_kernel(const float* __restrict__ terms, int T, float 
   if (threadIdx.x == 0) *out = s * scale;
 }
 
+// Grid: x = token row, y = chunks of 1024 columns; a thread takes four
+// consecutive columns (16-byte load, 8-byte store when the rows allow).
 __global__ void ce_grad_kernel(const float* __restrict__ z, int T, int R, int ld, int row0,
                                const int32_t* __restrict__ labels, const float* __restrict__ lse, float scale,
                                uint16_t* __restrict__ dz) {
-  const size_t idx = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (idx >= (size_t)T * R) return;
-  const size_t t = idx / R;
-  const int c = (int)(idx % R);
-  float g = __expf(z[t * ld + c] - lse[t]);
-  if (labels[t] - row0 == c) g -= 1.f;
-  dz[t * ld + c] = f2bf(g * scale);
+  const size_t t = blockIdx.x;
+  const int c = (blockIdx.y * blockDim.x + threadIdx.x) * 4;
+  if (c >= R) return;
+  const float l = lse[t];
+  const int lab = labels[t] - row0;
+  const float* zr = z + t * ld;
+  uint16_t* dr = dz + t * ld;
+  if (c + 4 <= R && (ld & 3) == 0 && ((uintptr_t)z & 15) == 0 && ((uintptr_t)dz & 7) == 0) {
+    const float4 v = *(const float4*)(zr + c);
+    float g0 = __expf(v.x - l), g1 = __expf(v.y - l), g2 = __expf(v.z - l), g3 = __expf(v.w - l);
+    if (lab == c) g0 -= 1.f;
+    if (lab == c + 1) g1 -= 1.f;
+    if (lab == c + 2) g2 -= 1.f;
+    if (lab == c + 3) g3 -= 1.f;
+    *(uint2*)(dr + c) = make_uint2(pack_bf2(g0 * scale, g1 * scale), pack_bf2(g2 * scale, g3 * scale));
+  } else {
+    for (int k = c; k < c + 4 && k < R; ++k) {
+      float g = __expf(zr[k] - l);
+      if (lab == k) g -= 1.f;
+      dr[k] = f2bf(g * scale);
+    }
+  }
 }
 
 inline unsigned blocks_for(size_t n, int threads) { return (unsigned)((n + threads - 1) / threads); }
@@ -626,7 +655,8 @@ int ce_finalize(const float2* part, int nslices, const float* zlab, float* lse, 
 int ce_slice_grad(const float* logits, int T, int R, int ld, int row0, const int32_t* labels, const float* lse,
                   float scale, uint16_t* dz, cudaStream_t st) {
   if (T <= 0 || R <= 0 || ld < R) return -1;
-  ce_grad_kernel<<<blocks_for((size_t)T * R, 256), 256, 0, st>>>(logits, T, R, ld, row0, labels, lse, scale, dz);
+  ce_grad_kernel<<<dim3((unsigned)T, (unsigned)((R + 1023) / 1024)), 256, 0, st>>>(logits, T, R, ld, row0, labels, lse,
+                                                                                 scale, dz);
   count_launches(1);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
