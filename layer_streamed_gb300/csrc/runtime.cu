@@ -814,8 +814,10 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   // The embedding gradient region of the host buffer is cleared by CPU
   // threads while the GPU works; the rows of used tokens are written into it
   // after the step has drained.
+  // (Started right after the embedding rows are gathered, so that the two
+  // do not compete for the host cores while the first layer waits.)
   std::vector<std::thread> zeroers;
-  {
+  auto start_zeroers = [&] {
     uint8_t* eg = (uint8_t*)st.host_grad + ctx->off_g[0][0];
     const size_t nbytes = (size_t)p.V * h * 4;
     const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
@@ -827,7 +829,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       const size_t n = std::min(chunk, nbytes - b);
       zeroers.emplace_back([eg, b, n] { std::memset(eg + b, 0, n); });
     }
-  }
+  };
   struct Joiner {
     std::vector<std::thread>& t;
     ~Joiner() {
@@ -906,7 +908,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
     const size_t row_bytes = (size_t)h * p.esz;
     const uint8_t* E = (const uint8_t*)ctx->host_params + ctx->off_p[0][0];
     uint8_t* dst = ctx->host_rows;
-    const int nthr = (int)std::min<unsigned>(8, std::max(1u, std::thread::hardware_concurrency() / 2));
+    const int nthr = (int)std::min<unsigned>(16, std::max(1u, std::thread::hardware_concurrency()));
     std::vector<std::thread> gth;
     const int per = (T + nthr - 1) / nthr;
     for (int i = 0; i < nthr; ++i) {
@@ -917,6 +919,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       });
     }
     for (auto& x : gth) x.join();
+    start_zeroers();
     // On the weight stream, queued right behind the first layer's copy (the
     // copy engine serves one H2D stream at a time, so issuing it from the
     // compute stream would put it behind the second layer's copy too).
