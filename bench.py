@@ -144,6 +144,22 @@ def gemm_algorithmic_bytes(shape, B, S, K, head_rows, fuse_top=True):
     return n_fwd * fwd + L * bwd + head, 4 * n_fwd + 8 * L + 4 * slices
 
 
+def max_over_ranks(values, dist, device):
+    """Element-wise maximum over all ranks (the slowest replica sets the
+    time); identity without a process group."""
+    if dist is None:
+        return [float(v) for v in values]
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(v) for v in t.tolist()]
+
+
+def replica_throughput(world, tokens_per_step, steps, seconds):
+    """Whole-job tokens/s: every replica processes its own batch each step."""
+    return world * tokens_per_step * steps / seconds
+
+
 def head_slice_rows(shape, esz):
     """Rows of an LM-head vocab slice: the fewest equal slices (multiples of
     256 rows) whose bytes fit one packed decoder layer (as the library sizes
@@ -391,18 +407,16 @@ def main():
     log(f"instrumented step: {kst['n_gemm']} GEMM launches {kst['gemm_ms']:.1f} ms, "
         f"{kst['n_attn']} attention launches {kst['attn_ms']:.1f} ms")
     dev_ms = ev0.elapsed_time(ev1)
+    dev_ms, wall = max_over_ranks([dev_ms, wall], dist, "cuda")
     if dist:
-        t = torch.tensor([dev_ms, wall], device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dev_ms, wall = float(t[0]), float(t[1])
         if rank != 0:
             dist.destroy_process_group()
             sess.close()
             return
     T = B * S
     steps = args.steps
-    value = world * T * steps / (dev_ms / 1e3)
-    e2e = world * T * steps / wall
+    value = replica_throughput(world, T, steps, dev_ms / 1e3)
+    e2e = replica_throughput(world, T, steps, wall)
     peaks, peak_kind = read_peaks()
     gemm_tflops = kst["gemm_flop"] / (kst["gemm_ms"] / 1e3) / 1e12 if kst.get("gemm_ms") else None
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
