@@ -11,6 +11,7 @@ GPU trains its own batch through its own context; nothing is exchanged), so
 from __future__ import annotations
 
 import argparse
+import ctypes
 import json
 import os
 import subprocess
@@ -305,6 +306,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fuse-top", action="store_true", help="recompute the top block too")
     ap.add_argument("--serial", action="store_true", help="ablation: serialise weight copies and compute")
+    ap.add_argument("--optimizer", action="store_true",
+                    help="time mt_train_step (host AdamW applied as each unit's gradients land); allocates three "
+                         "fp32 copies of the model on the host, so use it with --layers at the 8B widths")
     ap.add_argument("--layers", type=int, default=None, help="diagnostic override of the layer count")
     ap.add_argument("--seq", type=int, default=None, help="diagnostic override of the sequence length")
     ap.add_argument("--batch", type=int, default=None, help="diagnostic override of the batch")
@@ -363,13 +367,24 @@ def main():
     tok, lab = seedgen.tokens_and_labels(B, S, V, seed=22 + rank)
 
     log(f"parameters filled in {init_s:.1f} s")
+    if args.optimizer:
+        master = np.zeros(sess.grad_bytes // 4, np.float32)
+        for unit, t, off, n, is_gain in offs:
+            o32, _ = sess.offset(unit, t, mt.MT_F32)
+            src = np.frombuffer((ctypes.c_uint8 * (n * (2 if bf16 else 4))).from_address(sess.params_ptr + off),
+                                np.uint16 if bf16 else np.float32)
+            master[o32 // 4:o32 // 4 + n] = ((src.astype(np.uint32) << 16).view(np.float32) if bf16 else src)
+        sess.bind_optimizer(mt.adamw_cfg(1e-4, 0.9, 0.95, 1e-8, 0.1), master)
+        del master
+        log(f"optimizer bound: {3 * sess.grad_bytes / 2**30:.1f} GiB of fp32 master and moments")
+    step_fn = sess.train_step if args.optimizer else sess.step
     placement = numa_pages({"params": sess.params_ptr, "grads": sess.grads_ptr})
     log(f"pinned pages per NUMA node: {placement}")
     link = host_link_probe(torch)
     log(f"host link {link}")
     for i in range(args.warmup):
         t1 = time.perf_counter()
-        sess.step(tok, lab, K)
+        step_fn(tok, lab, K)
         log(f"warmup step {i}: {time.perf_counter() - t1:.3f} s")
     comp, d2h_stream = streams[0], streams[2]
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -385,7 +400,7 @@ def main():
     host_ms = []  # per step: wall time of the call minus its device span (host preparation and finishing)
     for _ in range(args.steps):
         t_call = time.perf_counter()
-        losses.append(sess.step(tok, lab, K))
+        losses.append(step_fn(tok, lab, K))
         call_ms = (time.perf_counter() - t_call) * 1e3
         st = sess.stats()
         host_ms.append(call_ms - st["step_ms"])
@@ -453,7 +468,8 @@ def main():
         "config": {"workload": args.workload, "global_batch": B * world, "seq_len": S, "checkpoint_every": K,
                    "layers": L, "hidden": h, "heads": f"{nq}q/{nkv}kv x {d}", "ffn": F, "vocab": V,
                    "host_params": "bf16" if bf16 else "fp32", "parallelism": f"replicas x{world}",
-                   "l2": "inputs larger than L2 (every step streams all weights from host)"},
+                   "l2": "inputs larger than L2 (every step streams all weights from host)",
+                   "optimizer_step": "host AdamW included" if args.optimizer else "none (fwd+bwd)"},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(per_step_h2d + 2 * T * 4),
                 "d2h_bytes_per_step": int(per_step_d2h + 4)},
         "gpu_launches": int(agg["n_launches"]),
@@ -478,6 +494,11 @@ def main():
                           # effective rates of the step's own copies (bytes / summed copy time)
                           "h2d_copy_gbs": agg["h2d_bytes"] / max(1e-9, agg["h2d_ms"]) / 1e6,
                           "d2h_copy_gbs": agg["d2h_bytes"] / max(1e-9, agg["d2h_ms"]) / 1e6},
+        "optimizer": ({"kind": "host AdamW, per-unit as gradients land (mt_train_step)",
+                       "ms_per_step": agg["optimizer_ms"] / steps,
+                       "exposed_ms_per_step": agg["optimizer_exposed_ms"] / steps,
+                       "params_per_s": (sess.grad_bytes / 4) / (agg["optimizer_ms"] / steps / 1e3)
+                       if agg.get("optimizer_ms") else None} if args.optimizer else None),
         "host_link": link,
         "host_numa_pages": placement,
         "clocks": clk,

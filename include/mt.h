@@ -147,6 +147,10 @@ typedef struct {
   int32_t n_gemm, n_attn;
   int32_t n_launches;      /* kernels launched by this step (all trace levels) */
   int32_t reserved;
+  /* mt_train_step only: host wall time spent applying AdamW (summed over the
+   * units, measured on the optimizer thread) and the part of it after the
+   * step's last device work had finished (not hidden behind the step). */
+  double optimizer_ms, optimizer_exposed_ms;
 } mt_stats;
 int mt_get_stats(const mt_ctx* ctx, mt_stats* out);
 
@@ -162,6 +166,47 @@ typedef struct {
   size_t total, weight_buffers, grad_buffers, checkpoints, block_activations, workspace;
 } mt_memory_plan;
 int mt_get_memory_plan(const mt_ctx* ctx, mt_memory_plan* out);
+
+/* ---------------------------------------------------------------------------
+ * Optimizer step on the host (MegaTrain, section 方法步骤详情, stage 4: the CPU
+ * applies theta <- AdamUpdate(theta, grad, m, v) to the host-resident master
+ * weights once their gradients have streamed back). The update is AdamW:
+ *   m = beta1 m + (1 - beta1) g;  v = beta2 v + (1 - beta2) g^2
+ *   theta -= lr (m / (1 - beta1^t) / (sqrt(v / (1 - beta2^t)) + eps) + weight_decay theta)
+ * in fp32, on an fp32 master copy with fp32 moments (all three in the packed
+ * layout of mt_packed_bytes(cfg, MT_F32)); the parameters the GPU streams
+ * (bf16 or fp32 packed layout) receive the updated master rounded to their
+ * type (bf16: round to nearest even). Padding between tensors is untouched.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  float lr, beta1, beta2, eps, weight_decay;
+} mt_adamw_cfg;
+
+/* One AdamW update (step number `step` >= 1) of the packed units
+ * [unit_begin, unit_end) (0 = embedding, 1..n_layers = layers, n_layers+1 =
+ * final norm + head). master, m, v: host fp32 packed; grads: host fp32 packed
+ * (the layout mt_forward_backward fills); params: host, dtype params_dtype.
+ * n_threads host threads (0 = one per core). Pure host work: needs no GPU.
+ * Errors: MT_ERR_ARG for null pointers, bad units or step < 1. */
+int mt_adamw_update(const mt_layer_cfg* cfg, const mt_adamw_cfg* opt, int64_t step, int32_t unit_begin,
+                    int32_t unit_end, float* master, float* m, float* v, const float* grads, void* params,
+                    mt_dtype params_dtype, int32_t n_threads);
+
+/* Attach optimizer state to ctx (host fp32 packed arrays as above; the caller
+ * initialises master = the bound parameters in fp32 and m = v = 0, and keeps
+ * them alive). The step counter starts at 1. */
+int mt_bind_optimizer(mt_ctx* ctx, const mt_adamw_cfg* opt, float* master, float* m, float* v, int32_t n_threads);
+
+/* mt_forward_backward followed by the AdamW update of every unit, each unit
+ * updated by host threads as soon as its gradients have landed in
+ * host_grad_out (head first, layers top-down as the backward produces them,
+ * embedding last), overlapping the rest of the step. The GPU reads no unit's
+ * parameters again in a step after its gradients land, so the next call sees
+ * every unit updated (synchronous semantics: staleness 0). Returns when all
+ * updates are applied. Device errors detected before a unit's update leave
+ * that unit and the later ones untouched (MT_ERR_DEVICE). */
+int mt_train_step(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
+                  float* host_grad_out, float* loss_out);
 
 /* Text of the last error on ctx (never null; "" if none). */
 const char* mt_last_error(const mt_ctx* ctx);

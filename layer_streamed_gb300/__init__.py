@@ -43,7 +43,8 @@ EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_crea
            "mt_op_rmsnorm_fwd", "mt_op_rmsnorm_bwd_workspace", "mt_op_rmsnorm_bwd", "mt_op_rmsnorm_bwd_noalloc",
            "mt_op_rope", "mt_op_gemm_rope", "mt_op_attention_bwd_rope", "mt_op_gemm_swiglu", "mt_op_gemm_swiglu_bwd",
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
-           "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error")
+           "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error",
+           "mt_adamw_update", "mt_bind_optimizer", "mt_train_step")
 
 
 class MtError(RuntimeError):
@@ -68,7 +69,13 @@ class mt_stats(ctypes.Structure):
                 ("n_h2d", ctypes.c_int32), ("n_d2h", ctypes.c_int32), ("n_units", ctypes.c_int32),
                 ("timing_enabled", ctypes.c_int32), ("gemm_ms", ctypes.c_double), ("gemm_flop", ctypes.c_double),
                 ("attn_ms", ctypes.c_double), ("attn_flop", ctypes.c_double), ("n_gemm", ctypes.c_int32),
-                ("n_attn", ctypes.c_int32), ("n_launches", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("n_attn", ctypes.c_int32), ("n_launches", ctypes.c_int32), ("reserved", ctypes.c_int32),
+                ("optimizer_ms", ctypes.c_double), ("optimizer_exposed_ms", ctypes.c_double)]
+
+
+class mt_adamw_cfg(ctypes.Structure):
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float)]
 
 
 class mt_memory_plan(ctypes.Structure):
@@ -104,6 +111,9 @@ def lib() -> ctypes.CDLL:
         "mt_create_ex": (i32, [cfgp, sz, vp, P(vp), P(vp)]),
         "mt_bind_host_params": (i32, [vp, vp, i32]),
         "mt_forward_backward": (i32, [vp, vp, vp, i32, i32, i32, vp, P(f32)]),
+        "mt_train_step": (i32, [vp, vp, vp, i32, i32, i32, vp, P(f32)]),
+        "mt_bind_optimizer": (i32, [vp, P(mt_adamw_cfg), vp, vp, vp, i32]),
+        "mt_adamw_update": (i32, [cfgp, P(mt_adamw_cfg), ctypes.c_int64, i32, i32, vp, vp, vp, vp, vp, i32, i32]),
         "mt_get_stats": (i32, [vp, P(mt_stats)]),
         "mt_set_tracing": (i32, [vp, i32, i32]),
         "mt_get_memory_plan": (i32, [vp, P(mt_memory_plan)]),
@@ -200,6 +210,30 @@ def mt_forward_backward(ctx, tokens: np.ndarray, labels: np.ndarray, K: int, hos
     _check(lib().mt_forward_backward(ctx, tokens.ctypes.data, labels.ctypes.data, B, S, K, host_grad_out,
                                      ctypes.byref(loss)), ctx)
     return loss.value
+
+
+def mt_train_step(ctx, tokens: np.ndarray, labels: np.ndarray, K: int, host_grad_out: int) -> float:
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    labels = np.ascontiguousarray(labels, dtype=np.int32)
+    B, S = tokens.shape
+    loss = ctypes.c_float()
+    _check(lib().mt_train_step(ctx, tokens.ctypes.data, labels.ctypes.data, B, S, K, host_grad_out,
+                               ctypes.byref(loss)), ctx)
+    return loss.value
+
+
+def adamw_cfg(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0) -> mt_adamw_cfg:
+    return mt_adamw_cfg(lr, beta1, beta2, eps, weight_decay)
+
+
+def mt_bind_optimizer(ctx, opt: mt_adamw_cfg, master: int, m: int, v: int, n_threads: int = 0) -> None:
+    _check(lib().mt_bind_optimizer(ctx, ctypes.byref(opt), master, m, v, n_threads), ctx)
+
+
+def mt_adamw_update(cfg, opt: mt_adamw_cfg, step: int, unit_begin: int, unit_end: int, master: int, m: int, v: int,
+                    grads: int, params: int, params_dtype: int, n_threads: int = 0) -> None:
+    _check(lib().mt_adamw_update(ctypes.byref(cfg), ctypes.byref(opt), step, unit_begin, unit_end, master, m, v,
+                                 grads, params, params_dtype, n_threads))
 
 
 def mt_get_stats(ctx) -> dict:
@@ -309,6 +343,22 @@ class Session:
 
     def step(self, tokens: np.ndarray, labels: np.ndarray, K: int) -> float:
         return mt_forward_backward(self.ctx, tokens, labels, K, self._gp)
+
+    def bind_optimizer(self, opt: mt_adamw_cfg, master: np.ndarray, n_threads: int = 0) -> None:
+        """Attach AdamW state: `master` is the fp32 packed copy of the
+        parameters (mt_packed_bytes(cfg, MT_F32) bytes as float32); the
+        moments start at zero. The arrays are kept by the session."""
+        n = self.grad_bytes // 4
+        self.opt_master = np.ascontiguousarray(master, dtype=np.float32).reshape(-1).copy()
+        if self.opt_master.size != n:
+            raise MtError(MT_ERR_ARG, "master copy has the wrong size")
+        self.opt_m = np.zeros(n, np.float32)
+        self.opt_v = np.zeros(n, np.float32)
+        mt_bind_optimizer(self.ctx, opt, self.opt_master.ctypes.data, self.opt_m.ctypes.data, self.opt_v.ctypes.data,
+                          n_threads)
+
+    def train_step(self, tokens: np.ndarray, labels: np.ndarray, K: int) -> float:
+        return mt_train_step(self.ctx, tokens, labels, K, self._gp)
 
     def stats(self) -> dict:
         return mt_get_stats(self.ctx)

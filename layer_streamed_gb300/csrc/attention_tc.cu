@@ -29,6 +29,7 @@
 namespace mt {
 
 MT_DEVICE_ERROR_READER(attention_tc_take_device_error)
+MT_DEVICE_ERROR_PEEKER(attention_tc_peek_device_error)
 
 namespace {
 

@@ -35,6 +35,14 @@ static __device__ uint32_t g_device_error = 0;
     return e;                                                             \
   }
 
+// Read without clearing (0xffffffff if the read itself fails).
+#define MT_DEVICE_ERROR_PEEKER(fn)                                        \
+  uint32_t fn() {                                                         \
+    uint32_t e = 0;                                                       \
+    if (cudaMemcpyFromSymbol(&e, g_device_error, 4) != cudaSuccess) return 0xffffffffu; \
+    return e;                                                             \
+  }
+
 __device__ __forceinline__ void report_error(uint32_t bits) { atomicOr(&g_device_error, bits); }
 
 // ---------------------------------------------------------------------------

@@ -25,6 +25,7 @@
 namespace mt {
 
 MT_DEVICE_ERROR_READER(gemm_take_device_error)
+MT_DEVICE_ERROR_PEEKER(gemm_peek_device_error)
 
 namespace {
 

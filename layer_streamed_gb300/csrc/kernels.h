@@ -101,6 +101,8 @@ int ce_slice_grad(const float* logits, int T, int R, int ld, int row0, const int
 // barriers (0 = no error). Synchronous with respect to the device.
 uint32_t gemm_take_device_error();
 uint32_t attention_tc_take_device_error();
+uint32_t gemm_peek_device_error();  // the same words, not cleared
+uint32_t attention_tc_peek_device_error();
 
 // Tensor-core flash attention (attention_tc.cu); head_dim in {16,32,64,128},
 // row strides multiples of 8. work: attention_bwd_workspace(B, S, nq) floats

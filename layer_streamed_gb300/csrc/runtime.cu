@@ -28,6 +28,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <string>
+#include <atomic>
 #include <thread>
 #include <vector>
 
@@ -86,6 +87,88 @@ size_t build_layout(const mt_layer_cfg& c, size_t esz, std::vector<std::vector<s
     }
   }
   return rup(pos, 4096);
+}
+
+// ---------------------------------------------------------------------------
+// AdamW on the host (MegaTrain stage 4), fp32, over packed units.
+// ---------------------------------------------------------------------------
+struct AdamCoef {
+  float lr, b1, omb1, b2, omb2, bc1, bc2, eps, wd;
+};
+
+AdamCoef adam_coef(const mt_adamw_cfg& o, int64_t step) {
+  AdamCoef c;
+  c.lr = o.lr;
+  c.b1 = o.beta1;
+  c.omb1 = 1.f - o.beta1;
+  c.b2 = o.beta2;
+  c.omb2 = 1.f - o.beta2;
+  c.bc1 = (float)(1.0 / (1.0 - std::pow((double)o.beta1, (double)step)));
+  c.bc2 = (float)(1.0 / (1.0 - std::pow((double)o.beta2, (double)step)));
+  c.eps = o.eps;
+  c.wd = o.weight_decay;
+  return c;
+}
+
+inline uint16_t host_bf16_rne(float f) {
+  uint32_t u;
+  std::memcpy(&u, &f, 4);
+  if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x7fffffu)) return (uint16_t)((u >> 16) | 0x40);  // quiet NaN
+  u += 0x7fffu + ((u >> 16) & 1u);
+  return (uint16_t)(u >> 16);
+}
+
+// n elements of one tensor: master w, moments m, v, gradient g; the streamed
+// copy is pb (bf16) or pf (fp32).
+void adamw_span(const AdamCoef& c, float* w, float* m, float* v, const float* g, uint16_t* pb, float* pf, size_t n) {
+  for (size_t i = 0; i < n; ++i) {
+    const float gi = g[i];
+    const float mi = c.b1 * m[i] + c.omb1 * gi;
+    const float vi = c.b2 * v[i] + c.omb2 * (gi * gi);
+    m[i] = mi;
+    v[i] = vi;
+    const float wi = w[i];
+    const float nw = wi - c.lr * ((mi * c.bc1) / (std::sqrt(vi * c.bc2) + c.eps) + c.wd * wi);
+    w[i] = nw;
+    if (pb) pb[i] = host_bf16_rne(nw);
+    else pf[i] = nw;
+  }
+}
+
+// Update units [u0, u1) with nthr threads splitting the elements evenly.
+void adamw_units(const mt_layer_cfg& cfg, const std::vector<std::vector<size_t>>& off32,
+                 const std::vector<std::vector<size_t>>& offp, size_t esz, const AdamCoef& c, int u0, int u1,
+                 float* master, float* m, float* v, const float* grads, void* params, int nthr) {
+  struct Span {
+    size_t o32, op, n;
+  };
+  std::vector<Span> spans;
+  size_t total = 0;
+  for (int u = u0; u < u1; ++u)
+    for (int t = 0; t < tensors_in_unit(cfg, u); ++t) {
+      const size_t n = tensor_numel(cfg, u, t);
+      spans.push_back({off32[u][t] / 4, offp[u][t] / esz, n});
+      total += n;
+    }
+  if (!total) return;
+  auto run = [&](size_t lo, size_t hi) {  // element range [lo, hi) of the concatenated spans
+    size_t base = 0;
+    for (const Span& sp : spans) {
+      const size_t a = std::max(lo, base), b = std::min(hi, base + sp.n);
+      if (a < b) {
+        const size_t k = sp.o32 + (a - base), kp = sp.op + (a - base);
+        adamw_span(c, master + k, m + k, v + k, grads + k, esz == 2 ? (uint16_t*)params + kp : nullptr,
+                   esz == 4 ? (float*)params + kp : nullptr, b - a);
+      }
+      base += sp.n;
+      if (base >= hi) break;
+    }
+  };
+  const size_t per = std::max<size_t>((total + nthr - 1) / nthr, 1 << 16);
+  std::vector<std::thread> th;
+  for (size_t lo = per; lo < total; lo += per) th.emplace_back(run, lo, std::min(total, lo + per));
+  run(0, std::min(total, per));
+  for (auto& x : th) x.join();
 }
 
 bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
@@ -250,6 +333,12 @@ struct mt_ctx {
   int device = 0;
   cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
   bool own_streams = false;
+  // optimizer state (mt_bind_optimizer)
+  bool opt_bound = false;
+  mt_adamw_cfg opt{};
+  float *opt_master = nullptr, *opt_m = nullptr, *opt_v = nullptr;
+  int opt_threads = 0;
+  int64_t opt_step = 1;
   cudaEvent_t ev_wready[2], ev_wfree[2], ev_bwd_done[2], ev_gfree[2], ev_done = nullptr;
   uint8_t* arena = nullptr;
   size_t arena_bytes = 0;
@@ -500,6 +589,8 @@ struct Step {
   std::vector<Item> seq;        // compute-stream consumption order
   std::vector<int> slot_of;     // slot per step
   std::vector<char> needs_load; // load before step
+  bool train = false;                 // apply the optimizer as gradients land
+  std::vector<cudaEvent_t> landed;    // per unit (train steps): its gradients are on the host
   const Plan& P() const { return ctx->P; }
 };
 
@@ -778,6 +869,11 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   // RMSNorm 1 (+ residual): new dh
   CKL(rmsnorm_bwd(x, w.w1, a.rstd1, ctx->dm, a.hmid, ctx->dh, ctx->dh_b, GT(0), ctx->norm_ws, T, h, s));
   CKR(grad_piece(st, g, u0, u0, end_of(3)));
+  if (st.train) {
+    st.landed[l] = next_event(ctx);
+    if (!st.landed[l]) return set_err(ctx, MT_ERR_CUDA, "event pool");
+    CK(cudaEventRecord(st.landed[l], ctx->s_d2h));
+  }
   return grad_slot_release(st, g);
 }
 
@@ -988,6 +1084,11 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
             CKL(rmsnorm_bwd(ctx->h_top, ctx->wf32, ctx->rstd_f, ctx->dm, nullptr, ctx->dh, ctx->dh_b, ctx->gbuf[g],
                             ctx->norm_ws, T, h, s));
             CKR(grad_slot_end(st, g, ctx->off_g[L + 1][0], (size_t)h * 4));
+            if (st.train) {
+              st.landed[L + 1] = next_event(ctx);
+              if (!st.landed[L + 1]) return set_err(ctx, MT_ERR_CUDA, "event pool");
+              CK(cudaEventRecord(st.landed[L + 1], ctx->s_d2h));
+            }
           }
         }
       }
@@ -995,6 +1096,64 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
     CK(cudaEventRecord(ctx->ev_wfree[slot], s));
     if (ctx->serial && i + 1 < n && st.needs_load[i + 1]) CKR(issue_load(st, i + 1));
     if (ctx->debug_sync) CKR(debug_wait(ctx, i, it, slot, st.needs_load[i]));
+  }
+  // Train steps: host threads apply AdamW to each unit as soon as its
+  // gradients have landed (head first, then the layers top-down, the
+  // embedding after its scatter below). Every landed event is recorded by
+  // now, so they can be waited on from another thread.
+  struct OptRun {
+    std::atomic<int> emb_ready{0};
+    std::atomic<bool> abort{false};
+    std::atomic<int> status{MT_OK};
+    double busy_ms = 0;
+    std::thread th;
+    ~OptRun() {
+      abort = true;
+      if (th.joinable()) th.join();
+    }
+  } opt;
+  if (st.train) {
+    opt.th = std::thread([ctx, &st, &opt, &p, L] {
+      const AdamCoef coef = adam_coef(ctx->opt, ctx->opt_step);
+      const int nthr = ctx->opt_threads > 0 ? ctx->opt_threads
+                                            : (int)std::max(1u, std::thread::hardware_concurrency());
+      auto update = [&](int u) {
+        if (gemm_peek_device_error() | attention_tc_peek_device_error()) {  // garbage gradients: apply nothing
+          opt.status = MT_ERR_DEVICE;
+          return false;
+        }
+        const auto t0 = std::chrono::steady_clock::now();
+        adamw_units(ctx->cfg, ctx->off_g, ctx->off_p, p.esz, coef, u, u + 1, ctx->opt_master, ctx->opt_m,
+                    ctx->opt_v, st.host_grad, const_cast<void*>(ctx->host_params), nthr);
+        opt.busy_ms += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+        return true;
+      };
+      const auto deadline = std::chrono::steady_clock::now() + std::chrono::seconds(3600);
+      for (int u = L + 1; u >= 1; --u) {
+        while (true) {  // bounded poll of the unit's landed event
+          if (opt.abort || std::chrono::steady_clock::now() > deadline) {
+            opt.status = MT_ERR_TIMEOUT;
+            return;
+          }
+          const cudaError_t e = cudaEventQuery(st.landed[u]);
+          if (e == cudaSuccess) break;
+          if (e != cudaErrorNotReady) {
+            opt.status = MT_ERR_CUDA;
+            return;
+          }
+          std::this_thread::sleep_for(std::chrono::microseconds(100));
+        }
+        if (!update(u)) return;
+      }
+      while (!opt.emb_ready) {
+        if (opt.abort || std::chrono::steady_clock::now() > deadline) {
+          opt.status = MT_ERR_TIMEOUT;
+          return;
+        }
+        std::this_thread::sleep_for(std::chrono::microseconds(100));
+      }
+      update(0);
+    });
   }
   // Embedding backward: the gradient rows of the used ids (summed in
   // position order) are packed densely, copied to a pinned staging buffer,
@@ -1038,6 +1197,17 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       });
     }
     for (auto& x : sth) x.join();
+  }
+  if (st.train) {
+    const auto t_drained = std::chrono::steady_clock::now();
+    opt.emb_ready = 1;
+    opt.th.join();
+    ctx->stats.optimizer_ms = opt.busy_ms;
+    ctx->stats.optimizer_exposed_ms =
+        std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_drained).count();
+    if (opt.status != MT_OK)
+      return set_err(ctx, opt.status, opt.status == MT_ERR_DEVICE ? "device error before an optimizer update"
+                                                                  : "optimizer did not finish");
   }
   return MT_OK;
 }
@@ -1264,8 +1434,57 @@ int mt_bind_host_params(mt_ctx* ctx, const void* host_params, mt_dtype dtype) {
   return MT_OK;
 }
 
+int step_common(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K, float* host_grad_out,
+                float* loss_out, bool train);
+
 int mt_forward_backward(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
                         float* host_grad_out, float* loss_out) {
+  return step_common(ctx, tokens, labels, B, S, K, host_grad_out, loss_out, false);
+}
+
+int mt_train_step(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
+                  float* host_grad_out, float* loss_out) {
+  if (!ctx) return MT_ERR_ARG;
+  if (!ctx->opt_bound) return set_err(ctx, MT_ERR_STATE, "no optimizer bound");
+  const int rc = step_common(ctx, tokens, labels, B, S, K, host_grad_out, loss_out, true);
+  if (rc == MT_OK) ctx->opt_step += 1;
+  return rc;
+}
+
+int mt_bind_optimizer(mt_ctx* ctx, const mt_adamw_cfg* opt, float* master, float* m, float* v, int32_t n_threads) {
+  if (!ctx || !opt || !master || !m || !v || n_threads < 0) return set_err(ctx, MT_ERR_ARG, "null argument");
+  if (!(opt->lr >= 0.f) || !(opt->beta1 >= 0.f && opt->beta1 < 1.f) || !(opt->beta2 >= 0.f && opt->beta2 < 1.f) ||
+      !(opt->eps > 0.f) || !(opt->weight_decay >= 0.f))
+    return set_err(ctx, MT_ERR_ARG, "AdamW hyper-parameters out of range");
+  ctx->opt = *opt;
+  ctx->opt_master = master;
+  ctx->opt_m = m;
+  ctx->opt_v = v;
+  ctx->opt_threads = n_threads;
+  ctx->opt_step = 1;
+  ctx->opt_bound = true;
+  return MT_OK;
+}
+
+int mt_adamw_update(const mt_layer_cfg* cfg, const mt_adamw_cfg* opt, int64_t step, int32_t unit_begin,
+                    int32_t unit_end, float* master, float* m, float* v, const float* grads, void* params,
+                    mt_dtype params_dtype, int32_t n_threads) {
+  if (!cfg || !opt || !master || !m || !v || !grads || !params || step < 1 || n_threads < 0) return MT_ERR_ARG;
+  if (params_dtype != MT_F32 && params_dtype != MT_BF16) return MT_ERR_ARG;
+  if (unit_begin < 0 || unit_end > cfg->n_layers + 2 || unit_begin > unit_end) return MT_ERR_ARG;
+  std::string why;
+  if (!cfg_valid(*cfg, &why)) return MT_ERR_ARG;
+  std::vector<std::vector<size_t>> off32, offp;
+  const size_t esz = params_dtype == MT_BF16 ? 2 : 4;
+  build_layout(*cfg, 4, &off32);
+  build_layout(*cfg, esz, &offp);
+  const int nthr = n_threads > 0 ? n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
+  adamw_units(*cfg, off32, offp, esz, adam_coef(*opt, step), unit_begin, unit_end, master, m, v, grads, params, nthr);
+  return MT_OK;
+}
+
+int step_common(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K, float* host_grad_out,
+                float* loss_out, bool train) {
   if (!ctx) return MT_ERR_ARG;
   ctx->err.clear();
   if (!ctx->host_params) return set_err(ctx, MT_ERR_STATE, "no parameters bound");
@@ -1287,6 +1506,8 @@ int mt_forward_backward(mt_ctx* ctx, const int32_t* tokens, const int32_t* label
   cudaGetDevice(&cur);
   if (cur != ctx->device) cudaSetDevice(ctx->device);
   Step st{ctx, B, S, T, K, (ctx->cfg.n_layers + K - 1) / K, host_grad_out, {}, {}, {}};
+  st.train = train;
+  if (train) st.landed.assign(ctx->cfg.n_layers + 2, nullptr);
   const auto t0 = std::chrono::steady_clock::now();
   int rc = run_step(st, tokens, labels, loss_out);
   if (rc != MT_OK) {
