@@ -306,9 +306,10 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fuse-top", action="store_true", help="recompute the top block too")
     ap.add_argument("--serial", action="store_true", help="ablation: serialise weight copies and compute")
-    ap.add_argument("--optimizer", action="store_true",
-                    help="time mt_train_step (host AdamW applied as each unit's gradients land); allocates three "
-                         "fp32 copies of the model on the host, so use it with --layers at the 8B widths")
+    ap.add_argument("--optimizer", nargs="?", const="sync", choices=["sync", "async"], default=None,
+                    help="time train steps with the host AdamW: sync = mt_train_step (each unit updated as its "
+                         "gradients land), async = mt_train_step_async (staleness 1); allocates three fp32 copies "
+                         "of the model on the host, so use it with --layers at the 8B widths")
     ap.add_argument("--layers", type=int, default=None, help="diagnostic override of the layer count")
     ap.add_argument("--seq", type=int, default=None, help="diagnostic override of the sequence length")
     ap.add_argument("--batch", type=int, default=None, help="diagnostic override of the batch")
@@ -377,7 +378,7 @@ def main():
         sess.bind_optimizer(mt.adamw_cfg(1e-4, 0.9, 0.95, 1e-8, 0.1), master)
         del master
         log(f"optimizer bound: {3 * sess.grad_bytes / 2**30:.1f} GiB of fp32 master and moments")
-    step_fn = sess.train_step if args.optimizer else sess.step
+    step_fn = {None: sess.step, "sync": sess.train_step, "async": sess.train_step_async}[args.optimizer]
     placement = numa_pages({"params": sess.params_ptr, "grads": sess.grads_ptr})
     log(f"pinned pages per NUMA node: {placement}")
     link = host_link_probe(torch)
@@ -469,7 +470,7 @@ def main():
                    "layers": L, "hidden": h, "heads": f"{nq}q/{nkv}kv x {d}", "ffn": F, "vocab": V,
                    "host_params": "bf16" if bf16 else "fp32", "parallelism": f"replicas x{world}",
                    "l2": "inputs larger than L2 (every step streams all weights from host)",
-                   "optimizer_step": "host AdamW included" if args.optimizer else "none (fwd+bwd)"},
+                   "optimizer_step": f"host AdamW included ({args.optimizer})" if args.optimizer else "none (fwd+bwd)"},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(per_step_h2d + 2 * T * 4),
                 "d2h_bytes_per_step": int(per_step_d2h + 4)},
         "gpu_launches": int(agg["n_launches"]),
@@ -494,7 +495,9 @@ def main():
                           # effective rates of the step's own copies (bytes / summed copy time)
                           "h2d_copy_gbs": agg["h2d_bytes"] / max(1e-9, agg["h2d_ms"]) / 1e6,
                           "d2h_copy_gbs": agg["d2h_bytes"] / max(1e-9, agg["d2h_ms"]) / 1e6},
-        "optimizer": ({"kind": "host AdamW, per-unit as gradients land (mt_train_step)",
+        "optimizer": ({"kind": "host AdamW, " + ("per-unit as gradients land (mt_train_step)"
+                                                  if args.optimizer == "sync" else
+                                                  "staleness 1, units published as they land (mt_train_step_async)"),
                        "ms_per_step": agg["optimizer_ms"] / steps,
                        "exposed_ms_per_step": agg["optimizer_exposed_ms"] / steps,
                        "params_per_s": (sess.grad_bytes / 4) / (agg["optimizer_ms"] / steps / 1e3)

@@ -120,7 +120,8 @@ int mt_bind_host_params(mt_ctx* ctx, const void* host_params, mt_dtype dtype);
  *                   may be nonzero (the top block is then partial)
  *  host_grad_out  : pinned host fp32 buffer, mt_packed_bytes(cfg, MT_F32) bytes,
  *                   4096-byte aligned; OVERWRITTEN with dLoss/dtheta in the
- *                   packed layout (embedding rows of unused tokens are 0)
+ *                   packed layout (embedding rows of unused tokens are 0; the
+ *                   padding bytes between tensors are written as 0)
  *  loss_out       : host; Loss = mean over the B*S positions of
  *                   logsumexp(z_t) - z_t[label_t]
  * Synchronous: on return every gradient has landed. Results are bitwise
@@ -207,6 +208,21 @@ int mt_bind_optimizer(mt_ctx* ctx, const mt_adamw_cfg* opt, float* master, float
  * that unit and the later ones untouched (MT_ERR_DEVICE). */
 int mt_train_step(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
                   float* host_grad_out, float* loss_out);
+
+/* Asynchronous form (RoundPipe's staleness-1 optimizer, one GPU): call k runs
+ * step k on the GPU with the parameters updated through step k-2 while host
+ * threads compute the update from step k-1's gradients (the previous call's
+ * host_grad_out) into the fp32 master and moments; each unit's streamed copy
+ * is rewritten only after step k's gradients of that unit have landed, when
+ * the GPU reads that unit no more in step k (per-unit ordering instead of a
+ * whole-model barrier). So after call k the streamed parameters hold the
+ * update through step k-1. host_grad_out must not be the previous call's
+ * buffer (alternate two pinned buffers): that one is still being read. The
+ * first call applies no update. mt_optimizer_flush applies the pending
+ * update (after the last call); mt_train_step refuses while one is pending. */
+int mt_train_step_async(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
+                        float* host_grad_out, float* loss_out);
+int mt_optimizer_flush(mt_ctx* ctx);
 
 /* Text of the last error on ctx (never null; "" if none). */
 const char* mt_last_error(const mt_ctx* ctx);

@@ -44,7 +44,7 @@ EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_crea
            "mt_op_rope", "mt_op_gemm_rope", "mt_op_attention_bwd_rope", "mt_op_gemm_swiglu", "mt_op_gemm_swiglu_bwd",
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
            "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error",
-           "mt_adamw_update", "mt_bind_optimizer", "mt_train_step")
+           "mt_adamw_update", "mt_bind_optimizer", "mt_train_step", "mt_train_step_async", "mt_optimizer_flush")
 
 
 class MtError(RuntimeError):
@@ -112,6 +112,8 @@ def lib() -> ctypes.CDLL:
         "mt_bind_host_params": (i32, [vp, vp, i32]),
         "mt_forward_backward": (i32, [vp, vp, vp, i32, i32, i32, vp, P(f32)]),
         "mt_train_step": (i32, [vp, vp, vp, i32, i32, i32, vp, P(f32)]),
+        "mt_train_step_async": (i32, [vp, vp, vp, i32, i32, i32, vp, P(f32)]),
+        "mt_optimizer_flush": (i32, [vp]),
         "mt_bind_optimizer": (i32, [vp, P(mt_adamw_cfg), vp, vp, vp, i32]),
         "mt_adamw_update": (i32, [cfgp, P(mt_adamw_cfg), ctypes.c_int64, i32, i32, vp, vp, vp, vp, vp, i32, i32]),
         "mt_get_stats": (i32, [vp, P(mt_stats)]),
@@ -220,6 +222,20 @@ def mt_train_step(ctx, tokens: np.ndarray, labels: np.ndarray, K: int, host_grad
     _check(lib().mt_train_step(ctx, tokens.ctypes.data, labels.ctypes.data, B, S, K, host_grad_out,
                                ctypes.byref(loss)), ctx)
     return loss.value
+
+
+def mt_train_step_async(ctx, tokens: np.ndarray, labels: np.ndarray, K: int, host_grad_out: int) -> float:
+    tokens = np.ascontiguousarray(tokens, dtype=np.int32)
+    labels = np.ascontiguousarray(labels, dtype=np.int32)
+    B, S = tokens.shape
+    loss = ctypes.c_float()
+    _check(lib().mt_train_step_async(ctx, tokens.ctypes.data, labels.ctypes.data, B, S, K, host_grad_out,
+                                     ctypes.byref(loss)), ctx)
+    return loss.value
+
+
+def mt_optimizer_flush(ctx) -> None:
+    _check(lib().mt_optimizer_flush(ctx), ctx)
 
 
 def adamw_cfg(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0) -> mt_adamw_cfg:
@@ -360,6 +376,22 @@ class Session:
     def train_step(self, tokens: np.ndarray, labels: np.ndarray, K: int) -> float:
         return mt_train_step(self.ctx, tokens, labels, K, self._gp)
 
+    def train_step_async(self, tokens: np.ndarray, labels: np.ndarray, K: int) -> float:
+        """Staleness-1 step; gradients land in two pinned buffers in turn
+        (self.grads is the one this call wrote)."""
+        if not hasattr(self, "_gp2"):
+            self._gp2 = mt_host_alloc(self.grad_bytes)
+            self._gbufs = [self._gp, self._gp2]
+            self._gturn = 0
+        ptr = self._gbufs[self._gturn]
+        self._gturn ^= 1
+        loss = mt_train_step_async(self.ctx, tokens, labels, K, ptr)
+        self.grads = host_array(ptr, self.grad_bytes, np.float32)
+        return loss
+
+    def optimizer_flush(self) -> None:
+        mt_optimizer_flush(self.ctx)
+
     def stats(self) -> dict:
         return mt_get_stats(self.ctx)
 
@@ -380,6 +412,9 @@ class Session:
         if self._gp:
             mt_host_free(self._gp)
             self._gp = None
+        if getattr(self, "_gp2", None):
+            mt_host_free(self._gp2)
+            self._gp2 = None
 
     def __enter__(self):
         return self

@@ -131,8 +131,38 @@ void adamw_span(const AdamCoef& c, float* w, float* m, float* v, const float* g,
     const float nw = wi - c.lr * ((mi * c.bc1) / (std::sqrt(vi * c.bc2) + c.eps) + c.wd * wi);
     w[i] = nw;
     if (pb) pb[i] = host_bf16_rne(nw);
-    else pf[i] = nw;
+    else if (pf) pf[i] = nw;
   }
+}
+
+// Rewrite the streamed copy of units [u0, u1) from the fp32 master.
+void publish_units(const mt_layer_cfg& cfg, const std::vector<std::vector<size_t>>& off32,
+                   const std::vector<std::vector<size_t>>& offp, size_t esz, int u0, int u1, const float* master,
+                   void* params, int nthr) {
+  std::vector<std::thread> th;
+  for (int u = u0; u < u1; ++u)
+    for (int t = 0; t < tensors_in_unit(cfg, u); ++t) {
+      const size_t n = tensor_numel(cfg, u, t);
+      const float* src = master + off32[u][t] / 4;
+      const size_t per = std::max<size_t>((n + nthr - 1) / nthr, 1 << 16);
+      for (size_t lo = 0; lo < n; lo += per) {
+        const size_t hi = std::min(n, lo + per);
+        if (esz == 2) {
+          uint16_t* dst = (uint16_t*)params + offp[u][t] / 2;
+          th.emplace_back([=] {
+            for (size_t i = lo; i < hi; ++i) dst[i] = host_bf16_rne(src[i]);
+          });
+        } else {
+          float* dst = (float*)params + offp[u][t] / 4;
+          th.emplace_back([=] { std::memcpy(dst + lo, src + lo, (hi - lo) * 4); });
+        }
+      }
+      if (th.size() >= (size_t)nthr) {
+        for (auto& x : th) x.join();
+        th.clear();
+      }
+    }
+  for (auto& x : th) x.join();
 }
 
 // Update units [u0, u1) with nthr threads splitting the elements evenly.
@@ -157,8 +187,8 @@ void adamw_units(const mt_layer_cfg& cfg, const std::vector<std::vector<size_t>>
       const size_t a = std::max(lo, base), b = std::min(hi, base + sp.n);
       if (a < b) {
         const size_t k = sp.o32 + (a - base), kp = sp.op + (a - base);
-        adamw_span(c, master + k, m + k, v + k, grads + k, esz == 2 ? (uint16_t*)params + kp : nullptr,
-                   esz == 4 ? (float*)params + kp : nullptr, b - a);
+        adamw_span(c, master + k, m + k, v + k, grads + k, params && esz == 2 ? (uint16_t*)params + kp : nullptr,
+                   params && esz == 4 ? (float*)params + kp : nullptr, b - a);
       }
       base += sp.n;
       if (base >= hi) break;
@@ -339,6 +369,9 @@ struct mt_ctx {
   float *opt_master = nullptr, *opt_m = nullptr, *opt_v = nullptr;
   int opt_threads = 0;
   int64_t opt_step = 1;
+  // asynchronous form (mt_train_step_async): gradients of the previous call,
+  // whose update is applied during the next call
+  const float* opt_pending = nullptr;
   cudaEvent_t ev_wready[2], ev_wfree[2], ev_bwd_done[2], ev_gfree[2], ev_done = nullptr;
   uint8_t* arena = nullptr;
   size_t arena_bytes = 0;
@@ -590,6 +623,7 @@ struct Step {
   std::vector<int> slot_of;     // slot per step
   std::vector<char> needs_load; // load before step
   bool train = false;                 // apply the optimizer as gradients land
+  bool async = false;                 // apply the previous step's update, publishing units as they land
   std::vector<cudaEvent_t> landed;    // per unit (train steps): its gradients are on the host
   const Plan& P() const { return ctx->P; }
 };
@@ -794,18 +828,23 @@ int grad_slot_end(Step& st, int g, size_t host_off, size_t bytes) {
 // Copy one finished range of a layer's gradients (packed offsets [off0,
 // off1) of the unit starting at u0) from gradient buffer g to the host, as
 // soon as the compute stream has produced it.
-int grad_piece(Step& st, int g, size_t u0, size_t off0, size_t off1) {
+// Tensors t0..t1 of unit l, copied tensor by tensor (the padding between
+// them in the device buffer holds no gradient and is not copied).
+int grad_piece(Step& st, int g, int l, int t0, int t1) {
   mt_ctx* ctx = st.ctx;
+  const size_t u0 = ctx->off_g[l][0];
   cudaEvent_t ready = next_event(ctx);
   if (!ready) return set_err(ctx, MT_ERR_CUDA, "event pool");
   CK(cudaEventRecord(ready, ctx->s_comp));
   CK(cudaStreamWaitEvent(ctx->s_d2h, ready, 0));
-  {
-    SegScope sg(ctx, 2, ctx->s_d2h, (double)(off1 - off0));
-    CK(cudaMemcpyAsync((uint8_t*)st.host_grad + off0, (const uint8_t*)ctx->gbuf[g] + (off0 - u0), off1 - off0,
+  const size_t span = ctx->off_g[l][t1] + tensor_numel(ctx->cfg, l, t1) * 4 - ctx->off_g[l][t0];
+  SegScope sg(ctx, 2, ctx->s_d2h, (double)span);
+  for (int t = t0; t <= t1; ++t) {
+    const size_t off = ctx->off_g[l][t], nb = tensor_numel(ctx->cfg, l, t) * 4;
+    CK(cudaMemcpyAsync((uint8_t*)st.host_grad + off, (const uint8_t*)ctx->gbuf[g] + (off - u0), nb,
                        cudaMemcpyDeviceToHost, ctx->s_d2h));
+    ctx->stats.d2h_bytes += (double)nb;
   }
-  ctx->stats.d2h_bytes += (double)(off1 - off0);
   ctx->stats.n_d2h += 1;
   return MT_OK;
 }
@@ -829,12 +868,11 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   float* G = ctx->gbuf[g];
   const size_t u0 = ctx->off_g[l][0];
   auto GT = [&](int t) { return (float*)((uint8_t*)G + (ctx->off_g[l][t] - u0)); };
-  // Gradient tensors go to the host in four contiguous packed ranges, each as
-  // soon as it is complete: [Wd], [Wg Wu], [Wo w_ffn], [w_attn Wq Wk Wv].
-  auto end_of = [&](int t) { return ctx->off_g[l][t] + tensor_numel(ctx->cfg, l, t) * 4; };
+  // Gradient tensors go to the host in four groups, each as soon as it is
+  // complete: [Wd], [Wg Wu], [Wo w_ffn], [w_attn Wq Wk Wv].
   // h_out = h_mid + act Wd^T
   CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dh_b, a.act, GT(8), nullptr, h, F, T, h, Fp, F));
-  CKR(grad_piece(st, g, u0, ctx->off_g[l][8], end_of(8)));
+  CKR(grad_piece(st, g, l, 8, 8));
   {  // dact = dh Wd, turned into (dg, du) in place over (g, u) by the epilogue
     GemmParams bp{T, Fp, h, EPI_BF16, a.gu, nullptr, 2 * Fp, 0, 1};
     bp.swiglu_bwd = 1;
@@ -849,13 +887,13 @@ int layer_backward(Step& st, int l, const LayerView& w) {
     CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, F, h, T, 2 * Fp, h, h));
     CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu + Fp, a.m, GT(7), nullptr, F, h, T, 2 * Fp, h, h));
   }
-  CKR(grad_piece(st, g, u0, ctx->off_g[l][6], end_of(7)));
+  CKR(grad_piece(st, g, l, 6, 7));
   CKR(gemm(ctx, GEMM_NN, EPI_F32, a.gu, w.wgu, ctx->dm, nullptr, T, h, 2 * Fp, 2 * Fp, h, h));
   // RMSNorm 2 (+ residual): dh_mid written over h_mid (row-local, in place)
   CKL(rmsnorm_bwd(a.hmid, w.w2, a.rstd2, ctx->dm, ctx->dh, a.hmid, ctx->dhmid_b, GT(5), ctx->norm_ws, T, h, s));
   // h_mid = x + o Wo^T
   CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dhmid_b, a.o, GT(4), nullptr, h, p.qd, T, h, p.qd, p.qd));
-  CKR(grad_piece(st, g, u0, ctx->off_g[l][4], end_of(5)));
+  CKR(grad_piece(st, g, l, 4, 5));
   CKR(gemm(ctx, GEMM_NN, EPI_BF16, ctx->dhmid_b, w.wo, ctx->do_b, nullptr, T, p.qd, h, h, p.qd, p.qd));
   {
     OpTimer timer(ctx, 1, 2.5 * attn_flop(st, p));
@@ -868,8 +906,8 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   CKR(gemm(ctx, GEMM_NN, EPI_F32, ctx->dqkv, w.wqkv, ctx->dm, nullptr, T, h, p.qkv, p.qkv, h, h));
   // RMSNorm 1 (+ residual): new dh
   CKL(rmsnorm_bwd(x, w.w1, a.rstd1, ctx->dm, a.hmid, ctx->dh, ctx->dh_b, GT(0), ctx->norm_ws, T, h, s));
-  CKR(grad_piece(st, g, u0, u0, end_of(3)));
-  if (st.train) {
+  CKR(grad_piece(st, g, l, 0, 3));
+  if (st.train || st.async) {
     st.landed[l] = next_event(ctx);
     if (!st.landed[l]) return set_err(ctx, MT_ERR_CUDA, "event pool");
     CK(cudaEventRecord(st.landed[l], ctx->s_d2h));
@@ -913,6 +951,20 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   // (Started right after the embedding rows are gathered, so that the two
   // do not compete for the host cores while the first layer waits.)
   std::vector<std::thread> zeroers;
+  // The bytes between tensors (and after each unit) of the gradient buffer
+  // hold no gradient: written as zeros, so the whole buffer is defined.
+  {
+    uint8_t* gb = (uint8_t*)st.host_grad;
+    size_t pos = 0;
+    for (int u = 0; u <= L + 1; ++u)
+      for (int t = 0; t < tensors_in_unit(ctx->cfg, u); ++t) {
+        const size_t off = ctx->off_g[u][t];
+        if (off > pos) std::memset(gb + pos, 0, off - pos);
+        pos = off + tensor_numel(ctx->cfg, u, t) * 4;
+      }
+    const size_t total = build_layout(ctx->cfg, 4, nullptr);
+    if (total > pos) std::memset(gb + pos, 0, total - pos);
+  }
   auto start_zeroers = [&] {
     uint8_t* eg = (uint8_t*)st.host_grad + ctx->off_g[0][0];
     const size_t nbytes = (size_t)p.V * h * 4;
@@ -933,6 +985,40 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
         if (x.joinable()) x.join();
     }
   } joiner{zeroers};
+
+  // Asynchronous optimizer: the previous call's gradients are complete, so
+  // host threads compute that update (fp32 master and moments only) while
+  // this step runs; each unit's streamed copy is rewritten (published) only
+  // once this step has read that unit for the last time (see below).
+  struct AsyncRun {
+    std::vector<std::atomic<int>> done;
+    std::atomic<bool> abort{false};
+    double busy_ms = 0;
+    std::thread th;
+    explicit AsyncRun(int n) : done(n) {
+      for (auto& d : done) d = 0;
+    }
+    ~AsyncRun() {
+      abort = true;
+      if (th.joinable()) th.join();
+    }
+  } arun(L + 2);
+  const bool have_pending = st.async && ctx->opt_pending;
+  if (have_pending) {
+    arun.th = std::thread([ctx, &arun, &p, L] {
+      const AdamCoef coef = adam_coef(ctx->opt, ctx->opt_step);
+      const int nthr = ctx->opt_threads > 0 ? ctx->opt_threads
+                                            : (int)std::max(1u, std::thread::hardware_concurrency());
+      const auto t0 = std::chrono::steady_clock::now();
+      for (int u = L + 1; u >= 0; --u) {  // the order in which this step's units become publishable
+        if (arun.abort) return;
+        adamw_units(ctx->cfg, ctx->off_g, ctx->off_p, p.esz, coef, u, u + 1, ctx->opt_master, ctx->opt_m,
+                    ctx->opt_v, ctx->opt_pending, nullptr, nthr);
+        arun.done[u] = 1;
+      }
+      arun.busy_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+    });
+  }
 
   // Host preparation: stable counting sort of token ids (positions grouped
   // by id in ascending position order) and the list of distinct ids with
@@ -1084,7 +1170,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
             CKL(rmsnorm_bwd(ctx->h_top, ctx->wf32, ctx->rstd_f, ctx->dm, nullptr, ctx->dh, ctx->dh_b, ctx->gbuf[g],
                             ctx->norm_ws, T, h, s));
             CKR(grad_slot_end(st, g, ctx->off_g[L + 1][0], (size_t)h * 4));
-            if (st.train) {
+            if (st.train || st.async) {
               st.landed[L + 1] = next_event(ctx);
               if (!st.landed[L + 1]) return set_err(ctx, MT_ERR_CUDA, "event pool");
               CK(cudaEventRecord(st.landed[L + 1], ctx->s_d2h));
@@ -1112,6 +1198,42 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       if (th.joinable()) th.join();
     }
   } opt;
+  if (have_pending) {  // publisher: unit u once this step's gradients of u have landed and its update is computed
+    opt.th = std::thread([ctx, &st, &opt, &arun, &p, L] {
+      const int nthr = ctx->opt_threads > 0 ? ctx->opt_threads
+                                            : (int)std::max(1u, std::thread::hardware_concurrency());
+      const auto deadline = std::chrono::steady_clock::now() + std::chrono::seconds(3600);
+      auto wait_until = [&](auto ready) {
+        while (!ready()) {
+          if (opt.abort || std::chrono::steady_clock::now() > deadline) return false;
+          std::this_thread::sleep_for(std::chrono::microseconds(100));
+        }
+        return true;
+      };
+      for (int u = L + 1; u >= 0; --u) {
+        bool ok = true;
+        if (u >= 1) {
+          ok = wait_until([&] {
+            const cudaError_t e = cudaEventQuery(st.landed[u]);
+            if (e != cudaSuccess && e != cudaErrorNotReady) opt.status = MT_ERR_CUDA;
+            return e != cudaErrorNotReady;
+          });
+          if (opt.status != MT_OK) return;
+        }
+        // the embedding (u = 0) was gathered at the start of the step
+        if (!ok || !wait_until([&] { return arun.done[u].load() == 1; })) {
+          opt.status = MT_ERR_TIMEOUT;
+          return;
+        }
+        if (gemm_peek_device_error() | attention_tc_peek_device_error()) {
+          opt.status = MT_ERR_DEVICE;
+          return;
+        }
+        publish_units(ctx->cfg, ctx->off_g, ctx->off_p, p.esz, u, u + 1, ctx->opt_master,
+                      const_cast<void*>(ctx->host_params), nthr);
+      }
+    });
+  }
   if (st.train) {
     opt.th = std::thread([ctx, &st, &opt, &p, L] {
       const AdamCoef coef = adam_coef(ctx->opt, ctx->opt_step);
@@ -1197,6 +1319,17 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       });
     }
     for (auto& x : sth) x.join();
+  }
+  if (have_pending) {
+    const auto t_drained = std::chrono::steady_clock::now();
+    opt.th.join();
+    arun.th.join();
+    ctx->stats.optimizer_ms = arun.busy_ms;
+    ctx->stats.optimizer_exposed_ms =
+        std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_drained).count();
+    if (opt.status != MT_OK)
+      return set_err(ctx, opt.status, opt.status == MT_ERR_DEVICE ? "device error before publishing an update"
+                                                                  : "optimizer did not finish");
   }
   if (st.train) {
     const auto t_drained = std::chrono::steady_clock::now();
@@ -1435,7 +1568,7 @@ int mt_bind_host_params(mt_ctx* ctx, const void* host_params, mt_dtype dtype) {
 }
 
 int step_common(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K, float* host_grad_out,
-                float* loss_out, bool train);
+                float* loss_out, bool train, bool async_ = false);
 
 int mt_forward_backward(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
                         float* host_grad_out, float* loss_out) {
@@ -1446,9 +1579,37 @@ int mt_train_step(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int
                   float* host_grad_out, float* loss_out) {
   if (!ctx) return MT_ERR_ARG;
   if (!ctx->opt_bound) return set_err(ctx, MT_ERR_STATE, "no optimizer bound");
+  if (ctx->opt_pending) return set_err(ctx, MT_ERR_STATE, "an asynchronous update is pending; call mt_optimizer_flush");
   const int rc = step_common(ctx, tokens, labels, B, S, K, host_grad_out, loss_out, true);
   if (rc == MT_OK) ctx->opt_step += 1;
   return rc;
+}
+
+int mt_train_step_async(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
+                        float* host_grad_out, float* loss_out) {
+  if (!ctx) return MT_ERR_ARG;
+  if (!ctx->opt_bound) return set_err(ctx, MT_ERR_STATE, "no optimizer bound");
+  if (host_grad_out && host_grad_out == ctx->opt_pending)
+    return set_err(ctx, MT_ERR_ARG, "the previous call's gradient buffer is still being read; alternate two buffers");
+  const bool pending = ctx->opt_pending != nullptr;
+  const int rc = step_common(ctx, tokens, labels, B, S, K, host_grad_out, loss_out, false, true);
+  if (rc != MT_OK) return rc;
+  if (pending) ctx->opt_step += 1;
+  ctx->opt_pending = host_grad_out;
+  return MT_OK;
+}
+
+int mt_optimizer_flush(mt_ctx* ctx) {
+  if (!ctx) return MT_ERR_ARG;
+  if (!ctx->opt_bound) return set_err(ctx, MT_ERR_STATE, "no optimizer bound");
+  if (!ctx->opt_pending) return MT_OK;
+  const int nthr = ctx->opt_threads > 0 ? ctx->opt_threads : (int)std::max(1u, std::thread::hardware_concurrency());
+  const int L = ctx->cfg.n_layers;
+  adamw_units(ctx->cfg, ctx->off_g, ctx->off_p, ctx->P.esz, adam_coef(ctx->opt, ctx->opt_step), 0, L + 2,
+              ctx->opt_master, ctx->opt_m, ctx->opt_v, ctx->opt_pending, const_cast<void*>(ctx->host_params), nthr);
+  ctx->opt_step += 1;
+  ctx->opt_pending = nullptr;
+  return MT_OK;
 }
 
 int mt_bind_optimizer(mt_ctx* ctx, const mt_adamw_cfg* opt, float* master, float* m, float* v, int32_t n_threads) {
@@ -1462,6 +1623,7 @@ int mt_bind_optimizer(mt_ctx* ctx, const mt_adamw_cfg* opt, float* master, float
   ctx->opt_v = v;
   ctx->opt_threads = n_threads;
   ctx->opt_step = 1;
+  ctx->opt_pending = nullptr;
   ctx->opt_bound = true;
   return MT_OK;
 }
@@ -1484,7 +1646,7 @@ int mt_adamw_update(const mt_layer_cfg* cfg, const mt_adamw_cfg* opt, int64_t st
 }
 
 int step_common(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K, float* host_grad_out,
-                float* loss_out, bool train) {
+                float* loss_out, bool train, bool async_) {
   if (!ctx) return MT_ERR_ARG;
   ctx->err.clear();
   if (!ctx->host_params) return set_err(ctx, MT_ERR_STATE, "no parameters bound");
@@ -1507,7 +1669,8 @@ int step_common(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B
   if (cur != ctx->device) cudaSetDevice(ctx->device);
   Step st{ctx, B, S, T, K, (ctx->cfg.n_layers + K - 1) / K, host_grad_out, {}, {}, {}};
   st.train = train;
-  if (train) st.landed.assign(ctx->cfg.n_layers + 2, nullptr);
+  if (train || async_) st.landed.assign(ctx->cfg.n_layers + 2, nullptr);
+  st.async = async_;
   const auto t0 = std::chrono::steady_clock::now();
   int rc = run_step(st, tokens, labels, loss_out);
   if (rc != MT_OK) {

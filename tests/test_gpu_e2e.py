@@ -106,6 +106,25 @@ def test_bitwise_identical_across_K():
             assert np.array_equal(g.view(np.uint32), base.view(np.uint32)), K
 
 
+def test_gradient_buffer_fully_written():
+    """Every byte of the gradient buffer is defined after a step: tensors hold
+    the gradient, the padding between tensors is zero (whatever it held)."""
+    torch, mt = need_gpu()
+    cfg = with_layers(TINY_GQA, 3)
+    tok, lab = make_tokens(cfg, 2, 32, 27)
+    mask = np.zeros(oracle.packed_bytes(cfg, False) // 4, bool)
+    for unit, t, name, shape, is_gain in oracle.tensor_list(cfg):
+        off, nb = oracle.tensor_offset(cfg, unit, t, False)
+        mask[off // 4:(off + nb) // 4] = True
+    with open_session(mt, cfg, 2, 32, 2) as s:
+        s.params[:] = make_params(cfg, 28)
+        s.grads.view(np.uint32)[:] = 0xFFFFFFFF
+        s.step(tok, lab, 2)
+        g = s.grads.copy()
+    assert np.all(g.view(np.uint32)[~mask] == 0)
+    assert np.all(np.isfinite(g[mask]))
+
+
 def test_zero_head_gives_ln_vocab():
     torch, mt = need_gpu()
     cfg = TINY

@@ -80,3 +80,47 @@ def test_train_step_needs_an_optimizer():
         with pytest.raises(mt.MtError) as e:
             mt.mt_bind_optimizer(s.ctx, mt.adamw_cfg(1e-3, 1.5), s.grads_ptr, s.grads_ptr, s.grads_ptr)
         assert e.value.code == mt.MT_ERR_ARG
+
+
+def test_async_steps_follow_the_staleness_one_schedule():
+    """Three asynchronous steps and a flush equal the staggered schedule run
+    with the synchronous pieces: step k uses the parameters through k-2."""
+    torch, mt = need_gpu()
+    cfg = with_layers(TINY_GQA, 3)
+    shape = mt.ModelShape(cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
+                          cfg.vocab, cfg.rope_theta, cfg.norm_eps)
+    batches = [make_tokens(cfg, 2, 32, 40 + k) for k in range(3)]
+    packed = make_params(cfg, 44)
+    opt = mt.adamw_cfg(3e-3, 0.9, 0.999, 1e-8, 0.01)
+    units = cfg.n_layers + 2
+    with mt.Session(shape, 2, 32, 2, mt.MT_F32) as s:
+        s.params[:] = packed
+        s.bind_optimizer(opt, _master_f32(cfg, packed, False), n_threads=3)
+        got = []
+        for tok, lab in batches:
+            got.append((s.train_step_async(tok, lab, 2), s.grads.copy()))
+        with pytest.raises(mt.MtError) as e:  # a pending update blocks the synchronous form
+            s.train_step(*batches[0], 2)
+        assert e.value.code == mt.MT_ERR_STATE
+        s.optimizer_flush()
+        final = (s.params.copy(), s.opt_master.copy(), s.opt_m.copy(), s.opt_v.copy())
+    with mt.Session(shape, 2, 32, 2, mt.MT_F32) as s:
+        s.params[:] = packed
+        master = _master_f32(cfg, packed, False)
+        m, v = np.zeros_like(master), np.zeros_like(master)
+        grads = []
+
+        def update(k, g):
+            mt.mt_adamw_update(s.cfg, opt, k, 0, units, master.ctypes.data, m.ctypes.data, v.ctypes.data,
+                               g.ctypes.data, s.params_ptr, mt.MT_F32, 2)
+
+        for k, (tok, lab) in enumerate(batches):
+            loss = s.step(tok, lab, 2)  # step k+1 with the parameters through k-1
+            assert loss == got[k][0]
+            assert np.array_equal(s.grads.view(np.uint32), got[k][1].view(np.uint32))
+            grads.append(s.grads.copy())
+            if k >= 1:
+                update(k, grads[k - 1])
+        update(3, grads[2])
+        for x, y in zip((s.params, master, m, v), final):
+            assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
