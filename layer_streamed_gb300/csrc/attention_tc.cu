@@ -680,10 +680,12 @@ __global__ void __launch_bounds__(384, 1)
         float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -lse_c[i]));
         if (need_mask && q0 + cbase + i < srow) pv = 0.f;  // query must be at or after the key
         p[i] = pv;
-        ds[i] = pv * (__uint_as_float(dv[i]) - del_c[i]);
       }
       __syncwarp();
-      tmem_st_bf16x32(tmem + lane_base + buf * 64 + cbase, p);
+      tmem_st_bf16x32(tmem + lane_base + buf * 64 + cbase, p);  // in flight while dS^T is computed
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ds[i] = p[i] * (__uint_as_float(dv[i]) - del_c[i]);
+      __syncwarp();
       tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + cbase, ds);
       tmem_st_wait();
       tc_fence_before();

@@ -30,6 +30,7 @@
 #include <string>
 #include <atomic>
 #include <thread>
+#include <type_traits>
 #include <vector>
 
 #include <sys/syscall.h>
@@ -119,8 +120,11 @@ inline uint16_t host_bf16_rne(float f) {
 }
 
 // n elements of one tensor: master w, moments m, v, gradient g; the streamed
-// copy is pb (bf16) or pf (fp32).
-void adamw_span(const AdamCoef& c, float* w, float* m, float* v, const float* g, uint16_t* pb, float* pf, size_t n) {
+// copy p is bf16 (OutT = uint16_t), fp32 (float) or not written (void).
+// Non-aliasing arrays and no per-element branches, so the loop vectorizes.
+template <typename OutT>
+void adamw_span_t(const AdamCoef c, float* __restrict__ w, float* __restrict__ m, float* __restrict__ v,
+                  const float* __restrict__ g, OutT* __restrict__ p, size_t n) {
   for (size_t i = 0; i < n; ++i) {
     const float gi = g[i];
     const float mi = c.b1 * m[i] + c.omb1 * gi;
@@ -130,9 +134,19 @@ void adamw_span(const AdamCoef& c, float* w, float* m, float* v, const float* g,
     const float wi = w[i];
     const float nw = wi - c.lr * ((mi * c.bc1) / (std::sqrt(vi * c.bc2) + c.eps) + c.wd * wi);
     w[i] = nw;
-    if (pb) pb[i] = host_bf16_rne(nw);
-    else if (pf) pf[i] = nw;
+    if constexpr (std::is_same<OutT, uint16_t>::value) {
+      uint32_t u;
+      std::memcpy(&u, &nw, 4);
+      p[i] = (uint16_t)((u + 0x7fffu + ((u >> 16) & 1u)) >> 16);  // round to nearest even (finite values)
+    } else if constexpr (std::is_same<OutT, float>::value) {
+      p[i] = nw;
+    }
   }
+}
+void adamw_span(const AdamCoef& c, float* w, float* m, float* v, const float* g, uint16_t* pb, float* pf, size_t n) {
+  if (pb) adamw_span_t<uint16_t>(c, w, m, v, g, pb, n);
+  else if (pf) adamw_span_t<float>(c, w, m, v, g, pf, n);
+  else adamw_span_t<void>(c, w, m, v, g, (void*)nullptr, n);
 }
 
 // Rewrite the streamed copy of units [u0, u1) from the fp32 master.
