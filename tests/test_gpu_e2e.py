@@ -156,6 +156,39 @@ def test_llama8b_widths_two_layers():
     compare(cfg, grads, g_ref, tok, loss, l_ref)
 
 
+def test_llama8b_full_batch_K_invariance_and_zero_head():
+    """Eight layers of the 8B shape at the full batch (B=2, S=4096: 8192
+    tokens, four vocab slices of the head), bf16 host weights, in the step's
+    own launch configuration. Gradients are bitwise identical for K=4 and
+    K=1. Then, with W_out = 0, every logit is 0, so the loss is ln(V) and
+    dX = dlogits W_out vanishes: every gradient except the head's is exactly
+    zero."""
+    torch, mt = need_gpu()
+    cfg = with_layers(LLAMA8B, 8)
+    B, S = 2, 4096
+    tok, lab = make_tokens(cfg, B, S, 41)
+    packed = make_params(cfg, 42, bf16=True)
+    with open_session(mt, cfg, B, S, 4, bf16=True) as s:
+        s.params[:] = packed
+        del packed
+        loss4 = s.step(tok, lab, 4)
+        g4 = s.grads.copy()
+        loss1 = s.step(tok, lab, 1)
+        assert loss1 == loss4
+        assert np.array_equal(s.grads.view(np.uint32), g4.view(np.uint32))
+        del g4
+        assert math.isfinite(loss4) and 0.5 * math.log(cfg.vocab) < loss4 < 2.0 * math.log(cfg.vocab)
+        off, nb = oracle.tensor_offset(cfg, cfg.n_layers + 1, 1, True)
+        s.params[off:off + nb] = 0
+        loss0 = s.step(tok, lab, 4)
+        assert abs(loss0 - math.log(cfg.vocab)) < 1e-4 * math.log(cfg.vocab)
+        goff, gnb = oracle.tensor_offset(cfg, cfg.n_layers + 1, 1, False)
+        g = s.grads  # compared as floats: -0.0 counts as zero
+        assert not np.any(g[:goff // 4] != 0) and not np.any(g[(goff + gnb) // 4:] != 0)
+        assert np.any(g[goff // 4:(goff + gnb) // 4] != 0)
+    assert mt.mt_op_device_error() == 0
+
+
 def test_stats_report_streaming():
     _, _, _, _, _, st = run_case(with_layers(TINY, 4), 2, 32, 2, 15, 16)
     assert st["n_h2d"] > 0 and st["n_d2h"] > 0

@@ -279,6 +279,43 @@ def test_attention_backward_with_fused_inverse_rope(d):
     assert rel_l2(from_dev(dV), dv_ref) < 2e-2
 
 
+def test_attention_full_8b_shape_sliced():
+    """The step's attention launches at the 8B shape (B=2, S=4096, 32 query /
+    8 KV heads x 128, theta 5e5): the forward, then the backward with the
+    inverse rotation fused. Every (sequence, KV group) pair is an independent
+    causal attention problem (4 query heads over one KV head), so two of them
+    (the first and the last) are checked element by element against the
+    oracle solving that problem whole."""
+    torch, mt = need_gpu()
+    B, S, nq, nkv, d, theta = 2, 4096, 32, 8, 128, 5e5
+    grp = nq // nkv
+    q, k, v, do = (_normal((B, S, n, d), 130 + i) for i, n in enumerate((nq, nkv, nkv, nq)))
+    Q, q32 = to_dev_bf16(torch, q)
+    Kd, k32 = to_dev_bf16(torch, k)
+    Vd, v32 = to_dev_bf16(torch, v)
+    DO, do32 = to_dev_bf16(torch, do)
+    O = torch.empty((B, S, nq, d), dtype=torch.bfloat16, device="cuda")
+    LSE = torch.empty((B, nq, S), device="cuda")
+    mt.mt_op_attention_fwd(Q, Kd, Vd, O, LSE, B, S, nq, nkv, d, nq * d, nkv * d, nq * d)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(Kd), torch.empty_like(Vd)
+    ws = torch.empty(mt.mt_op_attention_bwd_workspace(B, S, nq), device="cuda")
+    tab = torch.empty(S * d, device="cuda")
+    mt.mt_op_attention_bwd_rope(Q, Kd, Vd, O, DO, LSE, dQ, dK, dV, ws, B, S, nq, nkv, d, nq * d, nkv * d, nq * d,
+                                tab, theta)
+    torch.cuda.synchronize()
+    assert mt.mt_op_device_error() == 0
+    o, lse, dq, dk, dv = (from_dev(t) for t in (O, LSE, dQ, dK, dV))
+    for b, g in ((0, 0), (B - 1, nkv - 1)):
+        hs = slice(g * grp, (g + 1) * grp)
+        o_ref, lse_ref, dq_ref, dk_ref, dv_ref = oracle.attention(
+            q32[b:b + 1, :, hs], k32[b:b + 1, :, g:g + 1], v32[b:b + 1, :, g:g + 1], do32[b:b + 1, :, hs])
+        assert rel_l2(o[b:b + 1, :, hs], o_ref) < 1.5e-2, (b, g)
+        assert np.max(np.abs(lse[b:b + 1, hs] - lse_ref)) < 1e-3, (b, g)
+        assert rel_l2(dq[b:b + 1, :, hs], oracle.rope(dq_ref, theta, -1)) < 2e-2, (b, g)
+        assert rel_l2(dk[b:b + 1, :, g:g + 1], oracle.rope(dk_ref, theta, -1)) < 2e-2, (b, g)
+        assert rel_l2(dv[b:b + 1, :, g:g + 1], dv_ref) < 2e-2, (b, g)
+
+
 @pytest.mark.parametrize("M,F,K,u_off", [(300, 384, 256, 384), (130, 172, 64, 176), (2048, 1536, 512, 1536)])
 def test_gated_gemm_fuses_swiglu(M, F, K, u_off):
     """g|u = x [Wg;Wu]^T with act = silu(g) u formed from the fp32 products."""
