@@ -37,7 +37,8 @@ def build() -> None:
 class _Cfg(ctypes.Structure):
     _fields_ = [("n_layers", ctypes.c_int32), ("hidden", ctypes.c_int32), ("n_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("ffn_dim", ctypes.c_int32),
-                ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("norm_eps", ctypes.c_double)]
+                ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_double), ("norm_eps", ctypes.c_double),
+                ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32), ("expert_ffn", ctypes.c_int32)]
 
 
 @dataclass(frozen=True)
@@ -51,14 +52,19 @@ class Config:
     vocab: int
     rope_theta: float = 1e4
     norm_eps: float = 1e-5
+    n_experts: int = 0   # > 0: every layer's FFN is a mixture of experts
+    top_k: int = 0
+    expert_ffn: int = 0
 
     def c(self) -> _Cfg:
         return _Cfg(self.n_layers, self.hidden, self.n_heads, self.n_kv_heads, self.head_dim, self.ffn_dim,
-                    self.vocab, self.rope_theta, self.norm_eps)
+                    self.vocab, self.rope_theta, self.norm_eps, self.n_experts, self.top_k, self.expert_ffn)
 
 
 # Tensor names inside a unit, in packed order.
 LAYER_TENSORS = ("w_attn_norm", "wq", "wk", "wv", "wo", "w_ffn_norm", "wg", "wu", "wd")
+MOE_LAYER_TENSORS = ("w_attn_norm", "wq", "wk", "wv", "wo", "w_ffn_norm", "w_router", "w_experts_gu",
+                     "w_experts_down")
 HEAD_TENSORS = ("w_final_norm", "w_out")
 
 
@@ -73,8 +79,8 @@ def lib():
         L.oracle_packed_bytes.argtypes = [P(_Cfg), i32]
         L.oracle_packed_bytes.restype = sz
         L.oracle_tensor_offset.argtypes = [P(_Cfg), i32, i32, i32, P(sz), P(sz)]
-        L.oracle_forward_backward_f32.argtypes = [P(_Cfg), vp, i32, vp, vp, i32, i32, dbl, vp, P(dbl), vp]
-        L.oracle_forward_backward_f64.argtypes = [P(_Cfg), vp, vp, vp, i32, i32, dbl, vp, P(dbl)]
+        L.oracle_forward_backward_f32.argtypes = [P(_Cfg), vp, i32, vp, vp, i32, i32, dbl, vp, P(dbl), vp, vp, vp]
+        L.oracle_forward_backward_f64.argtypes = [P(_Cfg), vp, vp, vp, i32, i32, dbl, vp, P(dbl), vp, vp]
         L.oracle_matmul.argtypes = [i32, i32, vp, vp, vp, i32, i32, i32]
         L.oracle_matmul_sampled.argtypes = [i32, vp, vp, i32, i32, i32, vp, vp, ctypes.c_int64, vp]
         L.oracle_rmsnorm_fwd.argtypes = [i32, vp, vp, i32, i32, dbl, vp, vp]
@@ -83,6 +89,7 @@ def lib():
         L.oracle_attention.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp]
         L.oracle_swiglu.argtypes = [i32, vp, vp, vp, sz, vp, vp, vp]
         L.oracle_cross_entropy.argtypes = [i32, vp, vp, i32, i32, dbl, P(dbl), vp]
+        L.oracle_moe_ffn.argtypes = [i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp, vp, vp, vp]
         _lib = L
     return _lib
 
@@ -112,8 +119,13 @@ def tensor_list(cfg: Config):
     h, qd, kd, F, V = cfg.hidden, cfg.n_heads * cfg.head_dim, cfg.n_kv_heads * cfg.head_dim, cfg.ffn_dim, cfg.vocab
     out = [(0, 0, "embed", (V, h), False)]
     shapes = [(h,), (qd, h), (kd, h), (kd, h), (h, qd), (h,), (F, h), (F, h), (h, F)]
+    names = LAYER_TENSORS
+    if cfg.n_experts:
+        E, Fe = cfg.n_experts, cfg.expert_ffn
+        shapes[6:] = [(E, h), (E, 2 * Fe, h), (E, h, Fe)]
+        names = MOE_LAYER_TENSORS
     for l in range(cfg.n_layers):
-        for t, (name, shp) in enumerate(zip(LAYER_TENSORS, shapes)):
+        for t, (name, shp) in enumerate(zip(names, shapes)):
             out.append((l + 1, t, f"layer{l}.{name}", shp, name.endswith("norm")))
     out.append((cfg.n_layers + 1, 0, "w_final_norm", (h,), True))
     out.append((cfg.n_layers + 1, 1, "w_out", (V, h), False))
@@ -130,12 +142,27 @@ def unpack(cfg: Config, packed: np.ndarray, bf16: bool = False) -> dict[str, np.
     return out
 
 
+def _routing(cfg: Config, T: int, route_in, want_route: bool):
+    """(route_in array or None, route_out array or None), each [L, T, top_k] int32."""
+    shape = (cfg.n_layers, T, cfg.top_k)
+    rin = None
+    if route_in is not None:
+        rin = np.ascontiguousarray(route_in, dtype=np.int32)
+        if rin.shape != shape:
+            raise ValueError(f"route_in must have shape {shape}")
+    rout = np.zeros(shape, dtype=np.int32) if want_route else None
+    return rin, rout
+
+
 def forward_backward(cfg: Config, params: np.ndarray, tokens: np.ndarray, labels: np.ndarray, bf16: bool = False,
-                     scale: float | None = None, token_losses: bool = False):
+                     scale: float | None = None, token_losses: bool = False, route_in=None,
+                     want_route: bool = False):
     """fp32 step. params: packed bytes (fp32 or bf16 layout).
 
     Returns (loss, packed fp32 grads), plus the per-position CE terms [B, S]
-    when token_losses is set."""
+    when token_losses is set, plus the experts selected in every layer
+    ([L, B*S, top_k]) when want_route is set. route_in forces that selection
+    (mixture-of-experts layers only)."""
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     labels = np.ascontiguousarray(labels, dtype=np.int32)
     B, S = tokens.shape
@@ -145,17 +172,21 @@ def forward_backward(cfg: Config, params: np.ndarray, tokens: np.ndarray, labels
     loss = ctypes.c_double()
     c = cfg.c()
     tl = np.empty((B, S), dtype=np.float32) if token_losses else None
+    rin, rout = _routing(cfg, B * S, route_in, want_route)
     rc = lib().oracle_forward_backward_f32(ctypes.byref(c), _p(params), 1 if bf16 else 0, _p(tokens), _p(labels),
-                                           B, S, scale, _p(grads), ctypes.byref(loss), _p(tl))
+                                           B, S, scale, _p(grads), ctypes.byref(loss), _p(tl), _p(rin), _p(rout))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
+    out = (loss.value, grads)
     if token_losses:
-        return loss.value, grads, tl
-    return loss.value, grads
+        out += (tl,)
+    if want_route:
+        out += (rout,)
+    return out
 
 
 def forward_backward_f64(cfg: Config, params64: np.ndarray, tokens: np.ndarray, labels: np.ndarray,
-                         scale: float | None = None):
+                         scale: float | None = None, route_in=None, want_route: bool = False):
     """fp64 step; params64 are doubles at the fp32 layout's element offsets."""
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     labels = np.ascontiguousarray(labels, dtype=np.int32)
@@ -166,10 +197,13 @@ def forward_backward_f64(cfg: Config, params64: np.ndarray, tokens: np.ndarray, 
     grads = np.zeros(packed_bytes(cfg, False) // 4, dtype=np.float64)
     loss = ctypes.c_double()
     c = cfg.c()
+    rin, rout = _routing(cfg, B * S, route_in, want_route)
     rc = lib().oracle_forward_backward_f64(ctypes.byref(c), _p(params64), _p(tokens), _p(labels), B, S, scale,
-                                           _p(grads), ctypes.byref(loss))
+                                           _p(grads), ctypes.byref(loss), _p(rin), _p(rout))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
+    if want_route:
+        return loss.value, grads, rout
     return loss.value, grads
 
 
@@ -278,3 +312,26 @@ def cross_entropy(z, labels, scale=None, want_grad=True, f64=True):
     if rc != 0:
         raise ValueError("label out of range")
     return loss.value, dz
+
+
+def moe_ffn(m, w_router, w_experts_gu, w_experts_down, top_k, dout=None, route_in=None, f64=True):
+    """Mixture-of-experts FFN on m [T, h]: w_router [E, h], w_experts_gu
+    [E, 2Fe, h] (gate rows, then up rows), w_experts_down [E, h, Fe].
+
+    Returns (out [T, h], route [T, top_k], dm, dw_router, dw_experts_gu,
+    dw_experts_down); the gradients are None unless dout is given."""
+    m, wr, wgu, wd = _f32(m), _f32(w_router), _f32(w_experts_gu), _f32(w_experts_down)
+    T, h = m.shape
+    E, Fe = wr.shape[0], wd.shape[2]
+    out = np.empty_like(m)
+    route = np.zeros((T, top_k), dtype=np.int32)
+    rin = None if route_in is None else np.ascontiguousarray(route_in, dtype=np.int32).reshape(T, top_k)
+    dm = dwr = dwgu = dwd = None
+    if dout is not None:
+        dout = _f32(dout)
+        dm, dwr, dwgu, dwd = np.empty_like(m), np.empty_like(wr), np.empty_like(wgu), np.empty_like(wd)
+    rc = lib().oracle_moe_ffn(int(f64), _p(m), _p(wr), _p(wgu), _p(wd), T, h, E, top_k, Fe, _p(rin), _p(route),
+                              _p(out), _p(dout), _p(dm), _p(dwr), _p(dwgu), _p(dwd))
+    if rc != 0:
+        raise ValueError("bad mixture-of-experts arguments")
+    return out, route, dm, dwr, dwgu, dwd

@@ -41,13 +41,17 @@ namespace {
 struct Dims {
   int L, h, nq, nkv, d, F, V;
   double theta, eps;
+  int E, topk, Fe;  // mixture-of-experts FFN when E > 0 (F unused then)
 };
 
 // ---------------------------------------------------------------------------
 // Packed layout (the library's documented host format, restated here):
 // unit 0 = embedding E[V,h]; units 1..L = one decoder layer each, holding
 // w_attn_norm[h], Wq[nq*d,h], Wk[nkv*d,h], Wv[nkv*d,h], Wo[h,nq*d],
-// w_ffn_norm[h], Wg[F,h], Wu[F,h], Wd[h,F]; unit L+1 = final norm w_f[h] and
+// w_ffn_norm[h], Wg[F,h], Wu[F,h], Wd[h,F] (mixture-of-experts layers hold
+// instead the router Wr[E,h], the experts' gate and up rows Wgu[E,2Fe,h]
+// (rows [0,Fe) gate, [Fe,2Fe) up) and their down matrices Wd[E,h,Fe], in
+// the same three places); unit L+1 = final norm w_f[h] and
 // the head W_out[V,h]. Matrices are row-major [out,in]. Every tensor starts
 // on a 256-byte boundary and every unit on a 4096-byte boundary ("layer
 // contiguous tiling ... aligned to 4KB pages", same page, 技术新颖性).
@@ -65,6 +69,10 @@ size_t tensor_elems(const Dims& D, int unit, int t) {
   const size_t h = D.h, qd = (size_t)D.nq * D.d, kd = (size_t)D.nkv * D.d, F = D.F, V = D.V;
   if (unit == 0) return V * h;
   if (unit == D.L + 1) return t == 0 ? h : V * h;
+  if (D.E > 0 && t >= 6) {
+    const size_t E = D.E, Fe = D.Fe;
+    return t == 6 ? E * h : t == 7 ? E * 2 * Fe * h : E * h * Fe;
+  }
   switch (t) {
     case 0: return h;       // w_attn_norm
     case 1: return qd * h;  // Wq
@@ -332,17 +340,197 @@ S ce_fwd_bwd(const S* z, const int32_t* labels, int T, int V, S scale, S* dz, fl
 }
 
 // ---------------------------------------------------------------------------
+// Mixture-of-experts FFN (the MoE layer of the streamed workloads, in the
+// style of Qwen3's MoE blocks; the pages name the model and its 128 experts
+// with top-8 routing, not the formulas, so this is the plain reading):
+//   router logits r = m Wr^T, p = softmax(r) over the E experts;
+//   the k experts of largest p are selected (equal p: lower index first);
+//   their weights are renormalised, w_j = p_{e_j} / sum_i p_{e_i};
+//   expert e is a SwiGLU MLP y_e(x) = (silu(x Wg_e^T) * (x Wu_e^T)) Wd_e^T;
+//   out_t = sum_j w_j y_{e_j}(m_t), summed over j = 0..k-1.
+// No shared expert, no load-balancing loss. The selection is a function of
+// the logits, so its derivative is zero almost everywhere: gradients flow
+// into Wr only through the weights w.
+// ---------------------------------------------------------------------------
+template <class S>
+struct MoeAct {
+  std::vector<S> p;                     // [T, E] router probabilities
+  std::vector<int32_t> sel;             // [T, k] selected experts
+  std::vector<S> w;                     // [T, k] renormalised weights
+  std::vector<std::vector<int>> rows;   // per expert, the slots t*k+j routed to it, ascending
+  std::vector<S> g, u, act, y;          // per slot: [T*k, Fe] (g, u, act), [T*k, h] (y)
+};
+
+// Writes out [T, h]. route_in (optional, [T, k]) replaces the selection by the
+// given experts (validated by the caller); route_out (optional) receives it.
+template <class S>
+void moe_fwd(const Dims& D, const S* m, const S* Wr, const S* Wgu, const S* Wd, int T, const int32_t* route_in,
+             int32_t* route_out, MoeAct<S>& A, S* out) {
+  const int E = D.E, k = D.topk, Fe = D.Fe, h = D.h;
+  std::vector<S> r((size_t)T * E);
+  mm_nt(m, Wr, r.data(), T, E, h);
+  A.p.assign((size_t)T * E, S(0));
+  A.sel.assign((size_t)T * k, 0);
+  A.w.assign((size_t)T * k, S(0));
+  std::vector<int> order(E);
+  for (int t = 0; t < T; ++t) {
+    const S* rt = &r[(size_t)t * E];
+    S* pt = &A.p[(size_t)t * E];
+    S mx = -INFINITY;
+    for (int e = 0; e < E; ++e) mx = std::max(mx, rt[e]);
+    S sum = 0;
+    for (int e = 0; e < E; ++e) {
+      pt[e] = std::exp(rt[e] - mx);
+      sum += pt[e];
+    }
+    for (int e = 0; e < E; ++e) pt[e] /= sum;
+    int32_t* st = &A.sel[(size_t)t * k];
+    if (route_in) {
+      for (int j = 0; j < k; ++j) st[j] = route_in[(size_t)t * k + j];
+    } else {
+      for (int e = 0; e < E; ++e) order[e] = e;
+      std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return pt[a] > pt[b]; });
+      for (int j = 0; j < k; ++j) st[j] = order[j];
+    }
+    if (route_out)
+      for (int j = 0; j < k; ++j) route_out[(size_t)t * k + j] = st[j];
+    S psel = 0;
+    for (int j = 0; j < k; ++j) psel += pt[st[j]];
+    for (int j = 0; j < k; ++j) A.w[(size_t)t * k + j] = pt[st[j]] / psel;
+  }
+  A.rows.assign(E, std::vector<int>());
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) A.rows[A.sel[(size_t)t * k + j]].push_back(t * k + j);
+  const size_t slots = (size_t)T * k;
+  A.g.assign(slots * Fe, S(0));
+  A.u.assign(slots * Fe, S(0));
+  A.act.assign(slots * Fe, S(0));
+  A.y.assign(slots * h, S(0));
+  for (int e = 0; e < E; ++e) {
+    const std::vector<int>& R = A.rows[e];
+    const int n = (int)R.size();
+    if (n == 0) continue;
+    std::vector<S> X((size_t)n * h), G((size_t)n * Fe), U((size_t)n * Fe), Act((size_t)n * Fe), Y((size_t)n * h);
+    for (int i = 0; i < n; ++i)
+      for (int c = 0; c < h; ++c) X[(size_t)i * h + c] = m[(size_t)(R[i] / k) * h + c];
+    const S* wg = Wgu + (size_t)e * 2 * Fe * h;
+    mm_nt(X.data(), wg, G.data(), n, Fe, h);
+    mm_nt(X.data(), wg + (size_t)Fe * h, U.data(), n, Fe, h);
+    swiglu_fwd(G.data(), U.data(), (size_t)n * Fe, Act.data());
+    mm_nt(Act.data(), Wd + (size_t)e * h * Fe, Y.data(), n, h, Fe);
+    for (int i = 0; i < n; ++i) {
+      for (int c = 0; c < Fe; ++c) {
+        A.g[(size_t)R[i] * Fe + c] = G[(size_t)i * Fe + c];
+        A.u[(size_t)R[i] * Fe + c] = U[(size_t)i * Fe + c];
+        A.act[(size_t)R[i] * Fe + c] = Act[(size_t)i * Fe + c];
+      }
+      for (int c = 0; c < h; ++c) A.y[(size_t)R[i] * h + c] = Y[(size_t)i * h + c];
+    }
+  }
+  for (int t = 0; t < T; ++t) {
+    S* o = out + (size_t)t * h;
+    for (int c = 0; c < h; ++c) o[c] = 0;
+    for (int j = 0; j < k; ++j) {
+      const S wj = A.w[(size_t)t * k + j];
+      const S* y = &A.y[((size_t)t * k + j) * h];
+      for (int c = 0; c < h; ++c) o[c] += wj * y[c];
+    }
+  }
+}
+
+// Backward of moe_fwd given dout [T, h]: dm [T, h] written; dWr, dWgu, dWd
+// written for every expert (zero where no slot was routed).
+template <class S>
+void moe_bwd(const Dims& D, const S* m, const S* Wr, const S* Wgu, const S* Wd, int T, const MoeAct<S>& A,
+             const S* dout, S* dm, S* dWr, S* dWgu, S* dWd) {
+  const int E = D.E, k = D.topk, Fe = D.Fe, h = D.h;
+  for (size_t i = 0; i < (size_t)E * h; ++i) dWr[i] = 0;
+  for (size_t i = 0; i < (size_t)E * 2 * Fe * h; ++i) dWgu[i] = 0;
+  for (size_t i = 0; i < (size_t)E * h * Fe; ++i) dWd[i] = 0;
+  for (size_t i = 0; i < (size_t)T * h; ++i) dm[i] = 0;
+  // out_t = sum_j w_tj y_tj:  dw_tj = <dout_t, y_tj>,  dy_tj = w_tj dout_t
+  std::vector<S> dw((size_t)T * k);
+  for (int t = 0; t < T; ++t)
+    for (int j = 0; j < k; ++j) {
+      const S* y = &A.y[((size_t)t * k + j) * h];
+      S dot = 0;
+      for (int c = 0; c < h; ++c) dot += dout[(size_t)t * h + c] * y[c];
+      dw[(size_t)t * k + j] = dot;
+    }
+  for (int e = 0; e < E; ++e) {
+    const std::vector<int>& R = A.rows[e];
+    const int n = (int)R.size();
+    if (n == 0) continue;
+    std::vector<S> X((size_t)n * h), dY((size_t)n * h), G((size_t)n * Fe), U((size_t)n * Fe), Act((size_t)n * Fe);
+    for (int i = 0; i < n; ++i) {
+      const int t = R[i] / k;
+      const S wj = A.w[R[i]];
+      for (int c = 0; c < h; ++c) {
+        X[(size_t)i * h + c] = m[(size_t)t * h + c];
+        dY[(size_t)i * h + c] = wj * dout[(size_t)t * h + c];
+      }
+      for (int c = 0; c < Fe; ++c) {
+        G[(size_t)i * Fe + c] = A.g[(size_t)R[i] * Fe + c];
+        U[(size_t)i * Fe + c] = A.u[(size_t)R[i] * Fe + c];
+        Act[(size_t)i * Fe + c] = A.act[(size_t)R[i] * Fe + c];
+      }
+    }
+    const S* wg = Wgu + (size_t)e * 2 * Fe * h;
+    const S* wd = Wd + (size_t)e * h * Fe;
+    std::vector<S> dAct((size_t)n * Fe), dG((size_t)n * Fe), dU((size_t)n * Fe), dX((size_t)n * h),
+        tmp((size_t)n * h);
+    mm_nn(dY.data(), wd, dAct.data(), n, Fe, h);                 // dact = dY Wd_e
+    mm_tn(dY.data(), Act.data(), dWd + (size_t)e * h * Fe, h, Fe, n);  // dWd_e = dY^T act
+    swiglu_bwd(G.data(), U.data(), dAct.data(), (size_t)n * Fe, dG.data(), dU.data());
+    mm_nn(dG.data(), wg, dX.data(), n, h, Fe);                   // dX = dG Wg_e + dU Wu_e
+    mm_nn(dU.data(), wg + (size_t)Fe * h, tmp.data(), n, h, Fe);
+    for (size_t i = 0; i < (size_t)n * h; ++i) dX[i] += tmp[i];
+    S* dwg = dWgu + (size_t)e * 2 * Fe * h;
+    mm_tn(dG.data(), X.data(), dwg, Fe, h, n);                   // dWg_e = dG^T X
+    mm_tn(dU.data(), X.data(), dwg + (size_t)Fe * h, Fe, h, n);  // dWu_e = dU^T X
+    for (int i = 0; i < n; ++i)
+      for (int c = 0; c < h; ++c) dm[(size_t)(R[i] / k) * h + c] += dX[(size_t)i * h + c];
+  }
+  // w_j = p_{e_j} / P with P = sum_i p_{e_i}:  dL/dp_{e_i} = (dw_i - sum_j w_j dw_j) / P
+  // for selected experts, 0 for the rest; then through the softmax,
+  // dr_e = p_e (dp_e - sum_f p_f dp_f).
+  std::vector<S> dr((size_t)T * E), dp(E);
+  for (int t = 0; t < T; ++t) {
+    const S* pt = &A.p[(size_t)t * E];
+    const int32_t* st = &A.sel[(size_t)t * k];
+    const S* wt = &A.w[(size_t)t * k];
+    const S* dwt = &dw[(size_t)t * k];
+    S psel = 0, wdw = 0;
+    for (int j = 0; j < k; ++j) {
+      psel += pt[st[j]];
+      wdw += wt[j] * dwt[j];
+    }
+    for (int e = 0; e < E; ++e) dp[e] = 0;
+    for (int j = 0; j < k; ++j) dp[st[j]] = (dwt[j] - wdw) / psel;
+    S pdp = 0;
+    for (int e = 0; e < E; ++e) pdp += pt[e] * dp[e];
+    for (int e = 0; e < E; ++e) dr[(size_t)t * E + e] = pt[e] * (dp[e] - pdp);
+  }
+  std::vector<S> dmr((size_t)T * h);
+  mm_nn(dr.data(), Wr, dmr.data(), T, h, E);  // dm += dr Wr
+  for (size_t i = 0; i < (size_t)T * h; ++i) dm[i] += dmr[i];
+  mm_tn(dr.data(), m, dWr, E, h, T);          // dWr = dr^T m
+}
+
+// ---------------------------------------------------------------------------
 // The whole step. P and G index the packed fp32 layout in elements
 // (byte offset / 4). G is fully written.
 // ---------------------------------------------------------------------------
 template <class S>
 struct LayerAct {
   std::vector<S> x, a, rstd1, q, k, v, P, o, hmid, m, rstd2, g, u, act;
+  MoeAct<S> moe;
 };
 
 template <class S>
 S forward_backward(const Dims& D, const S* P, const int32_t* tok, const int32_t* lab, int B, int Sq, S scale,
-                   S* G, float* tok_loss = nullptr) {
+                   S* G, float* tok_loss = nullptr, const int32_t* route_in = nullptr,
+                   int32_t* route_out = nullptr) {
   const int T = B * Sq, h = D.h, qd = D.nq * D.d, kd = D.nkv * D.d, F = D.F, V = D.V;
   auto off = [&](int unit, int t) { return layout_offset(D, 4, unit, t) / 4; };
   const size_t total = layout_offset(D, 4, D.L + 2, 0) / 4;
@@ -375,6 +563,14 @@ S forward_backward(const Dims& D, const S* P, const int32_t* tok, const int32_t*
     for (size_t i = 0; i < (size_t)T * h; ++i) A.hmid[i] += tmp[i];
     A.m.resize((size_t)T * h); A.rstd2.resize(T);
     rmsnorm_fwd(A.hmid.data(), P + off(u, 5), T, h, D.eps, A.m.data(), A.rstd2.data());
+    if (D.E > 0) {
+      const size_t rs = (size_t)T * D.topk;
+      moe_fwd(D, A.m.data(), P + off(u, 6), P + off(u, 7), P + off(u, 8), T, route_in ? route_in + l * rs : nullptr,
+              route_out ? route_out + l * rs : nullptr, A.moe, tmp.data());
+      hcur = A.hmid;
+      for (size_t i = 0; i < (size_t)T * h; ++i) hcur[i] += tmp[i];
+      continue;
+    }
     A.g.resize((size_t)T * F); A.u.resize((size_t)T * F); A.act.resize((size_t)T * F);
     mm_nt(A.m.data(), P + off(u, 6), A.g.data(), T, F, h);
     mm_nt(A.m.data(), P + off(u, 7), A.u.data(), T, F, h);
@@ -401,15 +597,20 @@ S forward_backward(const Dims& D, const S* P, const int32_t* tok, const int32_t*
   for (int l = D.L - 1; l >= 0; --l) {
     const int u = l + 1;
     LayerAct<S>& A = acts[l];
-    // h_out = h_mid + act Wd^T
-    mm_nn(dh.data(), P + off(u, 8), dact.data(), T, F, h);
-    mm_tn(dh.data(), A.act.data(), G + off(u, 8), h, F, T);
-    swiglu_bwd(A.g.data(), A.u.data(), dact.data(), (size_t)T * F, dg.data(), du.data());
-    mm_nn(dg.data(), P + off(u, 6), dm.data(), T, h, F);
-    mm_nn(du.data(), P + off(u, 7), tmp.data(), T, h, F);
-    for (size_t i = 0; i < (size_t)T * h; ++i) dm[i] += tmp[i];
-    mm_tn(dg.data(), A.m.data(), G + off(u, 6), F, h, T);
-    mm_tn(du.data(), A.m.data(), G + off(u, 7), F, h, T);
+    if (D.E > 0) {
+      moe_bwd(D, A.m.data(), P + off(u, 6), P + off(u, 7), P + off(u, 8), T, A.moe, dh.data(), dm.data(),
+              G + off(u, 6), G + off(u, 7), G + off(u, 8));
+    } else {
+      // h_out = h_mid + act Wd^T
+      mm_nn(dh.data(), P + off(u, 8), dact.data(), T, F, h);
+      mm_tn(dh.data(), A.act.data(), G + off(u, 8), h, F, T);
+      swiglu_bwd(A.g.data(), A.u.data(), dact.data(), (size_t)T * F, dg.data(), du.data());
+      mm_nn(dg.data(), P + off(u, 6), dm.data(), T, h, F);
+      mm_nn(du.data(), P + off(u, 7), tmp.data(), T, h, F);
+      for (size_t i = 0; i < (size_t)T * h; ++i) dm[i] += tmp[i];
+      mm_tn(dg.data(), A.m.data(), G + off(u, 6), F, h, T);
+      mm_tn(du.data(), A.m.data(), G + off(u, 7), F, h, T);
+    }
     rmsnorm_bwd(A.hmid.data(), P + off(u, 5), A.rstd2.data(), dm.data(), T, h, dhmid.data(), G + off(u, 5));
     for (size_t i = 0; i < (size_t)T * h; ++i) dhmid[i] += dh[i];
     // h_mid = x + o Wo^T
@@ -446,8 +647,25 @@ float bf16_to_f32(uint16_t b) {
 }
 
 bool valid_dims(const Dims& D) {
+  const bool ffn = D.E == 0 ? (D.F >= 1 && D.topk == 0 && D.Fe == 0)
+                            : (D.E >= 1 && D.topk >= 1 && D.topk <= D.E && D.Fe >= 1);
   return D.L >= 1 && D.h >= 1 && D.nq >= 1 && D.nkv >= 1 && D.nq % D.nkv == 0 && D.d >= 2 && D.d % 2 == 0 &&
-         D.F >= 1 && D.V >= 1;
+         D.V >= 1 && D.E >= 0 && ffn;
+}
+
+// A forced routing [L][T][k] must name k distinct experts per position.
+bool valid_routing(const Dims& D, const int32_t* route, int T) {
+  if (!route) return true;
+  if (D.E == 0) return false;
+  for (size_t r = 0; r < (size_t)D.L * T; ++r) {
+    const int32_t* st = route + r * D.topk;
+    for (int j = 0; j < D.topk; ++j) {
+      if (st[j] < 0 || st[j] >= D.E) return false;
+      for (int i = 0; i < j; ++i)
+        if (st[i] == st[j]) return false;
+    }
+  }
+  return true;
 }
 
 }  // namespace
@@ -460,11 +678,12 @@ extern "C" {
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
   double rope_theta, norm_eps;
+  int32_t n_experts, top_k, expert_ffn;  // all 0: dense SwiGLU FFN
 } oracle_cfg;
 
 static Dims to_dims(const oracle_cfg* c) {
-  return Dims{c->n_layers, c->hidden, c->n_heads, c->n_kv_heads, c->head_dim, c->ffn_dim, c->vocab, c->rope_theta,
-              c->norm_eps};
+  return Dims{c->n_layers, c->hidden, c->n_heads,   c->n_kv_heads, c->head_dim,  c->ffn_dim,
+              c->vocab,    c->rope_theta, c->norm_eps, c->n_experts, c->top_k, c->expert_ffn};
 }
 
 // dtype: 0 = fp32, 1 = bf16
@@ -491,11 +710,15 @@ static int check_tokens(const Dims& D, const int32_t* tok, const int32_t* lab, i
 // One step in fp32. params: packed host layout of dtype (0 fp32, 1 bf16).
 // grads: packed fp32 layout, fully overwritten. loss: scale * sum_t CE_t.
 // token_losses (optional, [B*S]): the unscaled CE term of every position.
+// Mixture-of-experts layers: route_in (optional, [L][B*S][top_k]) forces the
+// selected experts of every layer and position; route_out (optional, same
+// shape) receives the selection used.
 int oracle_forward_backward_f32(const oracle_cfg* c, const void* params, int dtype, const int32_t* tokens,
                                 const int32_t* labels, int B, int S, double scale, float* grads, double* loss,
-                                float* token_losses) {
+                                float* token_losses, const int32_t* route_in, int32_t* route_out) {
   const Dims D = to_dims(c);
   if (!valid_dims(D) || B < 1 || S < 1 || check_tokens(D, tokens, labels, B * S)) return -1;
+  if (!valid_routing(D, route_in, B * S) || (route_out && D.E == 0)) return -1;
   const size_t n32 = layout_offset(D, 4, D.L + 2, 0) / 4;
   std::vector<float> P(n32, 0.f);
   if (dtype == 0) {
@@ -510,17 +733,20 @@ int oracle_forward_backward_f32(const oracle_cfg* c, const void* params, int dty
         for (size_t i = 0; i < tensor_elems(D, u, t); ++i) P[o32 + i] = bf16_to_f32(s[i]);
       }
   }
-  *loss = forward_backward<float>(D, P.data(), tokens, labels, B, S, (float)scale, grads, token_losses);
+  *loss = forward_backward<float>(D, P.data(), tokens, labels, B, S, (float)scale, grads, token_losses, route_in,
+                                  route_out);
   return 0;
 }
 
 // One step in fp64; params and grads are doubles at the fp32 layout's element
 // offsets (byte offset / 4).
 int oracle_forward_backward_f64(const oracle_cfg* c, const double* params, const int32_t* tokens,
-                                const int32_t* labels, int B, int S, double scale, double* grads, double* loss) {
+                                const int32_t* labels, int B, int S, double scale, double* grads, double* loss,
+                                const int32_t* route_in, int32_t* route_out) {
   const Dims D = to_dims(c);
   if (!valid_dims(D) || B < 1 || S < 1 || check_tokens(D, tokens, labels, B * S)) return -1;
-  *loss = forward_backward<double>(D, params, tokens, labels, B, S, scale, grads);
+  if (!valid_routing(D, route_in, B * S) || (route_out && D.E == 0)) return -1;
+  *loss = forward_backward<double>(D, params, tokens, labels, B, S, scale, grads, nullptr, route_in, route_out);
   return 0;
 }
 
@@ -680,6 +906,45 @@ int oracle_swiglu(int use_f64, const float* g, const float* u, const float* da, 
     if (a) swiglu_fwd(g, u, n, a);
     if (da) swiglu_bwd(g, u, da, n, dg, du);
   }
+  return 0;
+}
+
+}  // extern "C"
+template <class S>
+static void op_moe(const float* m, const float* Wr, const float* Wgu, const float* Wd, int T, const Dims& D,
+                   const int32_t* route_in, int32_t* route_out, float* out, const float* dout, float* dm, float* dWr,
+                   float* dWgu, float* dWd) {
+  const size_t h = D.h, E = D.E, Fe = D.Fe;
+  auto M = widen<S>(m, T * h), R = widen<S>(Wr, E * h), GU = widen<S>(Wgu, E * 2 * Fe * h),
+       WD = widen<S>(Wd, E * h * Fe);
+  MoeAct<S> A;
+  std::vector<S> O(T * h);
+  moe_fwd(D, M.data(), R.data(), GU.data(), WD.data(), T, route_in, route_out, A, O.data());
+  narrow(O, out);
+  if (dout) {
+    auto DO = widen<S>(dout, T * h);
+    std::vector<S> DM(T * h), DR(E * h), DGU(E * 2 * Fe * h), DD(E * h * Fe);
+    moe_bwd(D, M.data(), R.data(), GU.data(), WD.data(), T, A, DO.data(), DM.data(), DR.data(), DGU.data(),
+            DD.data());
+    narrow(DM, dm);
+    narrow(DR, dWr);
+    narrow(DGU, dWgu);
+    narrow(DD, dWd);
+  }
+}
+extern "C" {
+// Mixture-of-experts FFN on m [T,h] with router Wr [E,h], experts' gate|up
+// Wgu [E,2Fe,h] and down Wd [E,h,Fe]: out [T,h]; route_in (optional, [T,k])
+// forces the selection, route_out (optional) receives it; if dout is given,
+// dm, dWr, dWgu, dWd are written.
+int oracle_moe_ffn(int use_f64, const float* m, const float* Wr, const float* Wgu, const float* Wd, int T, int h,
+                   int E, int k, int Fe, const int32_t* route_in, int32_t* route_out, float* out, const float* dout,
+                   float* dm, float* dWr, float* dWgu, float* dWd) {
+  Dims D{1, h, 1, 1, 2, 0, 1, 1e4, 1e-5, E, k, Fe};
+  if (T < 0 || h < 1 || !valid_dims(D) || !valid_routing(D, route_in, T)) return -1;
+  ORACLE_DISPATCH(use_f64,
+                  (op_moe<float>(m, Wr, Wgu, Wd, T, D, route_in, route_out, out, dout, dm, dWr, dWgu, dWd)),
+                  (op_moe<double>(m, Wr, Wgu, Wd, T, D, route_in, route_out, out, dout, dm, dWr, dWgu, dWd)));
   return 0;
 }
 
