@@ -60,7 +60,16 @@ typedef enum { MT_F32 = 0, MT_BF16 = 1 } mt_dtype;
  * ffn_dim % 8 == 0; any ffn_dim >= 1 for MT_F32 params.
  * max_batch * max_seq bounds the tokens of one call; max_K bounds the
  * checkpoint interval. param_dtype is the dtype of the host parameters that
- * will be bound. n_experts/top_k/expert_ffn must be 0 (dense decoder). */
+ * will be bound. n_experts = top_k = expert_ffn = 0: dense SwiGLU FFN.
+ * n_experts > 0: every layer's FFN is a mixture of experts (the MoE layer of
+ * the streamed workloads, Qwen3-MoE style, e.g. Qwen3-235B: 128 experts,
+ * top-8, expert width 1536; the pages name the model and its routing, not
+ * the formulas): router logits r = m Wr^T from the FFN-norm output m,
+ * p = softmax(r); the top_k experts of largest logit (equal: lower index)
+ * with weights p_j / sum of the chosen p; each a SwiGLU MLP of width
+ * expert_ffn; out = sum_j w_j y_j. No shared expert, no auxiliary loss.
+ * Then ffn_dim = 0, n_experts a multiple of 8 in [8, 1024], top_k in
+ * [1, min(32, n_experts)], expert_ffn % 8 == 0, and MT_BF16 params. */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
   float rope_theta, norm_eps;
@@ -78,6 +87,9 @@ typedef struct mt_ctx mt_ctx;
  *                  0 w_attn_norm[h], 1 Wq[n_heads*d, h], 2 Wk[n_kv_heads*d, h],
  *                  3 Wv[n_kv_heads*d, h], 4 Wo[h, n_heads*d], 5 w_ffn_norm[h],
  *                  6 Wg[ffn, h], 7 Wu[ffn, h], 8 Wd[h, ffn]
+ *                  (mixture of experts: 6 Wr[E, h], 7 Wgu[E, 2*Fe, h] with
+ *                  each expert's gate rows then up rows, 8 Wd[E, h, Fe];
+ *                  E = n_experts, Fe = expert_ffn)
  *  unit L+1      : 0 w_final_norm[h], 1 W_out[vocab, h]
  * Matrices are row-major [out, in] (y = x W^T). Every tensor starts on a
  * 256-byte boundary, every unit on a 4096-byte boundary. The gradient buffer
@@ -154,6 +166,12 @@ typedef struct {
   double optimizer_ms, optimizer_exposed_ms;
 } mt_stats;
 int mt_get_stats(const mt_ctx* ctx, mt_stats* out);
+
+/* Mixture of experts: the experts chosen in the last completed step,
+ * host_out[l][t][j] = the j-th choice (descending router logit) of layer l+1
+ * for token t, n = n_layers * B*S * top_k int32 (else MT_ERR_ARG).
+ * MT_ERR_STATE for a dense model or before the first step. Synchronous. */
+int mt_get_routing(const mt_ctx* ctx, int32_t* host_out, size_t n);
 
 /* Tracing of the following mt_forward_backward calls: level 0 none, 1
  * per-unit and per-copy events (overlap statistics; the default, also set

@@ -44,7 +44,8 @@ EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_crea
            "mt_op_rope", "mt_op_gemm_rope", "mt_op_attention_bwd_rope", "mt_op_gemm_swiglu", "mt_op_gemm_swiglu_bwd",
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
            "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error",
-           "mt_adamw_update", "mt_bind_optimizer", "mt_train_step", "mt_train_step_async", "mt_optimizer_flush")
+           "mt_adamw_update", "mt_bind_optimizer", "mt_train_step", "mt_train_step_async", "mt_optimizer_flush",
+           "mt_get_routing")
 
 
 class MtError(RuntimeError):
@@ -117,6 +118,7 @@ def lib() -> ctypes.CDLL:
         "mt_bind_optimizer": (i32, [vp, P(mt_adamw_cfg), vp, vp, vp, i32]),
         "mt_adamw_update": (i32, [cfgp, P(mt_adamw_cfg), ctypes.c_int64, i32, i32, vp, vp, vp, vp, vp, i32, i32]),
         "mt_get_stats": (i32, [vp, P(mt_stats)]),
+        "mt_get_routing": (i32, [vp, vp, sz]),
         "mt_set_tracing": (i32, [vp, i32, i32]),
         "mt_get_memory_plan": (i32, [vp, P(mt_memory_plan)]),
         "mt_last_error": (ctypes.c_char_p, [vp]),
@@ -166,9 +168,10 @@ def _check(rc: int, ctx=None):
 # C entry points under their own names
 # ---------------------------------------------------------------------------
 def make_cfg(n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, rope_theta=1e4, norm_eps=1e-5,
-             max_batch=1, max_seq=1, max_K=1, param_dtype=MT_F32) -> mt_layer_cfg:
+             max_batch=1, max_seq=1, max_K=1, param_dtype=MT_F32, n_experts=0, top_k=0,
+             expert_ffn=0) -> mt_layer_cfg:
     return mt_layer_cfg(n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, rope_theta, norm_eps,
-                        max_batch, max_seq, max_K, param_dtype, 0, 0, 0)
+                        max_batch, max_seq, max_K, param_dtype, n_experts, top_k, expert_ffn)
 
 
 def mt_packed_bytes(cfg: mt_layer_cfg, dtype: int) -> int:
@@ -258,6 +261,13 @@ def mt_get_stats(ctx) -> dict:
     return {f: getattr(s, f) for f, _ in mt_stats._fields_}
 
 
+def mt_get_routing(ctx, n_layers: int, T: int, top_k: int) -> np.ndarray:
+    """Experts chosen in the last step: [n_layers, T, top_k] int32."""
+    out = np.zeros((n_layers, T, top_k), dtype=np.int32)
+    _check(lib().mt_get_routing(ctx, out.ctypes.data, out.size), ctx)
+    return out
+
+
 def mt_set_tracing(ctx, level: int, sample: int = 16) -> None:
     _check(lib().mt_set_tracing(ctx, level, sample), ctx)
 
@@ -312,6 +322,9 @@ class ModelShape:
     vocab: int
     rope_theta: float = 1e4
     norm_eps: float = 1e-5
+    n_experts: int = 0  # > 0: mixture-of-experts FFN in every layer
+    top_k: int = 0
+    expert_ffn: int = 0
 
 
 class Session:
@@ -325,7 +338,7 @@ class Session:
                  device_budget: int | None = None, device_arena: int | None = None, streams=None):
         self.cfg = make_cfg(shape.n_layers, shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim,
                             shape.ffn_dim, shape.vocab, shape.rope_theta, shape.norm_eps, max_batch, max_seq,
-                            max_K, param_dtype)
+                            max_K, param_dtype, shape.n_experts, shape.top_k, shape.expert_ffn)
         self.shape = shape
         self.param_dtype = param_dtype
         need = mt_required_budget(self.cfg)
@@ -394,6 +407,10 @@ class Session:
 
     def stats(self) -> dict:
         return mt_get_stats(self.ctx)
+
+    def routing(self, T: int) -> np.ndarray:
+        """[n_layers, T, top_k] experts chosen in the last step of T tokens."""
+        return mt_get_routing(self.ctx, self.shape.n_layers, T, self.shape.top_k)
 
     def set_tracing(self, level: int, sample: int = 16) -> None:
         mt_set_tracing(self.ctx, level, sample)

@@ -15,7 +15,7 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmt.so")
-SOURCES = ["gemm.cu", "attention_tc.cu", "elementwise.cu", "runtime.cu", "ops_api.cu"]
+SOURCES = ["gemm.cu", "attention_tc.cu", "elementwise.cu", "moe.cu", "runtime.cu", "ops_api.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

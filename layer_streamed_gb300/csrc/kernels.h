@@ -67,6 +67,30 @@ int rope_apply(uint16_t* x, const float2* tab, int B, int S, int row_stride, int
 int swiglu_fwd(const uint16_t* gu, uint16_t* act, int T, int F, int ld, cudaStream_t st);
 int swiglu_bwd(uint16_t* gu, const uint16_t* dact, int T, int F, int ld, cudaStream_t st);
 
+// Mixture-of-experts routing (moe.cu). Slot t*k + j is token t's j-th
+// choice; rows are the slots grouped by expert in ascending slot order.
+// moe_route: top-k of router logits r [T,E] (ties: lower index), sel/w [T*k]
+// (descending logit, weights renormalised over the k), counts[E] (zeroed
+// here), log (optional) = a copy of sel.
+int moe_route(const float* r, int T, int E, int k, int32_t* sel, float* w, int32_t* counts, int32_t* log,
+              cudaStream_t st);
+// perm[row] = slot, spos[slot] = row for the n = T*k slots.
+int moe_permute(const int32_t* sel, int n, int E, const int32_t* counts, int32_t* perm, int32_t* spos,
+                cudaStream_t st);
+// xp[row] = m[perm[row] / k] (bf16 [n, h]).
+int moe_gather(const uint16_t* m, const int32_t* perm, int n, int k, int h, uint16_t* xp, cudaStream_t st);
+// y[t] = hmid[t] + sum_j w[t,j] yp[spos[t,j]] (fp32).
+int moe_combine(const float* hmid, const float* yp, const int32_t* spos, const float* w, int T, int k, int h,
+                float* y, cudaStream_t st);
+// dyp[spos[t,j]] = bf16(w[t,j] dh[t]), dw[t,j] = <dh[t], yp[spos[t,j]]>.
+int moe_combine_bwd(const float* dh, const float* yp, const int32_t* spos, const float* w, int T, int k, int h,
+                    uint16_t* dyp, float* dw, cudaStream_t st);
+// dm[t] = sum_j dxp[spos[t,j]] (fp32).
+int moe_unpermute(const float* dxp, const int32_t* spos, int T, int k, int h, float* dm, cudaStream_t st);
+// dr [T,E] bf16: w_j (dw_j - sum_i w_i dw_i) at the selected experts, 0 elsewhere.
+int moe_router_bwd(const float* w, const float* dw, const int32_t* sel, int T, int k, int E, uint16_t* dr,
+                   cudaStream_t st);
+
 // Embedding rows [row0, row0+rows) of E (fp32 or bf16, row stride h):
 // h0[t] = E[tok[t]] for tokens in range.
 int embed_gather(const void* E_slice, bool bf16, int row0, int rows, const int32_t* tok, float* h0, int T, int h,

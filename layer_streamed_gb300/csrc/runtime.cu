@@ -65,6 +65,10 @@ size_t tensor_numel(const mt_layer_cfg& c, int u, int t) {
                F = c.ffn_dim, V = c.vocab;
   if (u == 0) return V * h;
   if (u == c.n_layers + 1) return t == 0 ? h : V * h;
+  if (c.n_experts > 0 && t >= 6) {  // router Wr[E,h], experts' Wgu[E,2Fe,h], Wd[E,h,Fe]
+    const size_t E = c.n_experts, Fe = c.expert_ffn;
+    return t == 6 ? E * h : t == 7 ? E * 2 * Fe * h : E * h * Fe;
+  }
   static const int kind[9] = {0, 1, 2, 2, 3, 0, 4, 4, 4};
   switch (kind[t]) {
     case 0: return h;
@@ -220,8 +224,18 @@ bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
     if (why) *why = m;
     return false;
   };
-  if (c.n_layers < 1 || c.hidden < 64 || c.n_heads < 1 || c.n_kv_heads < 1 || c.ffn_dim < 1 || c.vocab < 1)
+  const bool moe = c.n_experts != 0 || c.top_k != 0 || c.expert_ffn != 0;
+  if (c.n_layers < 1 || c.hidden < 64 || c.n_heads < 1 || c.n_kv_heads < 1 || (!moe && c.ffn_dim < 1) ||
+      c.vocab < 1)
     return fail("non-positive dimension");
+  if (moe) {
+    if (c.ffn_dim != 0) return fail("mixture-of-experts layers take ffn_dim = 0");
+    if (c.n_experts < 8 || c.n_experts > 1024 || c.n_experts % 8)
+      return fail("n_experts must be a multiple of 8 in [8, 1024]");
+    if (c.top_k < 1 || c.top_k > 32 || c.top_k > c.n_experts) return fail("top_k must be in [1, min(32, n_experts)]");
+    if (c.expert_ffn < 8 || c.expert_ffn % 8) return fail("expert_ffn must be a positive multiple of 8");
+    if (c.param_dtype != MT_BF16) return fail("mixture-of-experts layers need bf16 params");
+  }
   if (c.hidden % 64) return fail("hidden must be a multiple of 64");
   if (c.hidden > 8192) return fail("hidden above 8192 is not supported");
   if (c.n_heads % c.n_kv_heads) return fail("n_heads must be a multiple of n_kv_heads");
@@ -230,9 +244,10 @@ bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
   if (c.param_dtype != MT_F32 && c.param_dtype != MT_BF16) return fail("param_dtype must be MT_F32 or MT_BF16");
   if (c.param_dtype == MT_BF16 && c.ffn_dim % 8) return fail("bf16 params need ffn_dim % 8 == 0");
   if (c.max_batch < 1 || c.max_seq < 1 || c.max_K < 1) return fail("max_batch, max_seq, max_K must be >= 1");
-  if (c.n_experts || c.top_k || c.expert_ffn) return fail("mixture-of-experts layers are not implemented");
   if (!(c.rope_theta > 0.f) || !(c.norm_eps > 0.f)) return fail("rope_theta and norm_eps must be positive");
   if ((double)c.max_batch * c.max_seq > 2147483647.0 / 4) return fail("too many tokens");
+  if (moe && (double)c.max_batch * c.max_seq * c.top_k * std::max(c.hidden, 2 * c.expert_ffn) > 2147483647.0 * 4)
+    return fail("too many routed rows");
   return true;
 }
 
@@ -242,6 +257,7 @@ bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
 struct Plan {
   // dims
   int L, h, nq, nkv, d, F, Fp, V, qd, kd, qkv, Tmax;
+  int E, topk, Fe;  // mixture-of-experts FFN when E > 0 (F = Fp = 0)
   size_t esz;
   // slicing of vocab-sized units
   int head_rows, n_head_slices;
@@ -249,6 +265,9 @@ struct Plan {
   size_t wbuf, wcast, gbuf, ckpt_one, act_layer, fixed_ws, dyn_max, total;
   // activation layout inside one block-arena slot (byte offsets)
   size_t o_x, o_a, o_rstd1, o_qkv, o_o, o_lse, o_hmid, o_m, o_rstd2, o_gu, o_act;
+  // mixture-of-experts slot: router logits, selection, weights, slot <-> row
+  // maps, and the routed rows (grouped by expert) with their activations
+  size_t o_r, o_sel, o_w, o_spos, o_perm, o_xp, o_gup, o_actp, o_yp;
 };
 
 size_t layer_cast_bytes(const Plan& p) {  // device bf16 view of one layer (fp32 params)
@@ -271,6 +290,9 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   p.qkv = p.qd + 2 * p.kd;
   p.Tmax = c.max_batch * c.max_seq;
   p.esz = c.param_dtype == MT_BF16 ? 2 : 4;
+  p.E = c.n_experts;
+  p.topk = c.top_k;
+  p.Fe = c.expert_ffn;
   std::vector<std::vector<size_t>> o;
   build_layout(c, p.esz, &o);
   const size_t layer_bytes = (o[1][8] + tensor_numel(c, 1, 8) * p.esz) - o[1][0];
@@ -312,6 +334,18 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   p.o_rstd2 = take(T * 4);
   p.o_gu = take(T * 2 * p.Fp * 2);
   p.o_act = take(T * p.Fp * 2);
+  {
+    const size_t E = p.E, R = T * p.topk, Fe = p.Fe;  // all zero for dense layers
+    p.o_r = take(T * E * 4);
+    p.o_sel = take(R * 4);
+    p.o_w = take(R * 4);
+    p.o_spos = take(R * 4);
+    p.o_perm = take(R * 4);
+    p.o_xp = take(R * h * 2);
+    p.o_gup = take(R * 2 * Fe * 2);
+    p.o_actp = take(R * Fe * 2);
+    p.o_yp = take(R * h * 4);
+  }
   p.act_layer = rup(a, 4096);
   // fixed workspace (see Ctx::carve)
   size_t w = 0;
@@ -336,6 +370,11 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   ws((size_t)c.max_seq * p.d / 2 * 8);             // rope table
   ws(2 * 2 * (size_t)p.h * 4);                     // gains of the two weight slots
   ws((size_t)p.h * 4 * 2);                         // final norm gain (raw + fp32)
+  ws(T * p.topk * (size_t)p.h * 2);                // MoE: d(routed outputs) bf16
+  ws(T * p.topk * 4);                              // MoE: d(weights)
+  ws(T * (size_t)p.E * 2);                         // MoE: d(router logits) bf16
+  ws(((size_t)p.E + 1) * 4);                       // MoE: expert counts
+  ws((size_t)p.L * T * p.topk * 4);                // MoE: routing of every layer
   p.fixed_ws = w;
   // dynamic part: checkpoints for ceil(L/K) blocks + K activation slots
   p.dyn_max = 0;
@@ -399,12 +438,21 @@ struct mt_ctx {
   uint16_t *dh_b, *dhmid_b, *do_b, *dqkv, *xf_b, *dz;
   float2 *ce_part, *rope_tab;
   int32_t *tok_d, *lab_d, *perm_d, *ids_d, *ids_start_d;
+  // mixture-of-experts: d(routed outputs), d(weights), d(router logits),
+  // expert counts, the routing of every layer; pinned copy of the counts and
+  // the counts behind each activation slot (the expert GEMMs are launched
+  // per expert from the host)
+  uint16_t *moe_dyp = nullptr, *moe_dr = nullptr;
+  float* moe_dw = nullptr;
+  int32_t *moe_counts = nullptr, *moe_route = nullptr, *moe_counts_host = nullptr;
+  std::vector<std::vector<int>> moe_slot_counts;
   const void* host_params_dev = nullptr;  // device-side address of the bound host parameters
   void* wf_raw;
   int32_t* host_stage = nullptr;  // pinned: tokens, labels, perm, used ids, id ranges, loss
   uint8_t* host_rows = nullptr;   // pinned staging: embedding rows of the tokens [T, h] (param dtype)
   float* host_grad_rows = nullptr;  // pinned staging: embedding gradient rows of the used ids [T, h]
   int rope_S = -1;
+  int last_T = 0;  // tokens of the last step that ran to completion
   std::vector<int32_t> csr;  // token-id counting sort (vocab + 1)
   const void* host_params = nullptr;
   std::string err;
@@ -492,6 +540,11 @@ int carve(mt_ctx* ctx) {
   ctx->gains[1] = (float*)take(2 * (size_t)p.h * 4);
   ctx->wf_raw = take((size_t)p.h * 4);
   ctx->wf32 = (float*)take((size_t)p.h * 4);
+  ctx->moe_dyp = (uint16_t*)take(T * p.topk * h * 2);
+  ctx->moe_dw = (float*)take(T * p.topk * 4);
+  ctx->moe_dr = (uint16_t*)take(T * (size_t)p.E * 2);
+  ctx->moe_counts = (int32_t*)take(((size_t)p.E + 1) * 4);
+  ctx->moe_route = (int32_t*)take((size_t)p.L * T * p.topk * 4);
   ctx->dyn = cur;
   cur += p.dyn_max;
   if ((size_t)(cur - ctx->arena) > ctx->arena_bytes) return set_err(ctx, MT_ERR_BUDGET, "arena too small for plan");
@@ -542,6 +595,7 @@ struct SegScope {
 
 struct LayerView {  // bf16 matrices and fp32 gains of one bound layer
   const uint16_t *wqkv, *wo, *wgu, *wd;
+  const uint16_t* wr;  // mixture-of-experts router (wgu, wd then hold all experts)
   int ldd;  // row stride of Wd
   const float *w1, *w2;
 };
@@ -549,6 +603,10 @@ struct LayerView {  // bf16 matrices and fp32 gains of one bound layer
 struct ActSlot {
   float *x, *rstd1, *lse, *hmid, *rstd2;
   uint16_t *a, *qkv, *o, *m, *gu, *act;
+  // mixture-of-experts
+  float *r, *w, *yp;
+  int32_t *sel, *spos, *perm;
+  uint16_t *xp, *gup, *actp;
 };
 
 ActSlot act_slot(mt_ctx* ctx, int K, int nb, int j) {
@@ -566,6 +624,15 @@ ActSlot act_slot(mt_ctx* ctx, int K, int nb, int j) {
   s.rstd2 = (float*)(base + p.o_rstd2);
   s.gu = (uint16_t*)(base + p.o_gu);
   s.act = (uint16_t*)(base + p.o_act);
+  s.r = (float*)(base + p.o_r);
+  s.sel = (int32_t*)(base + p.o_sel);
+  s.w = (float*)(base + p.o_w);
+  s.spos = (int32_t*)(base + p.o_spos);
+  s.perm = (int32_t*)(base + p.o_perm);
+  s.xp = (uint16_t*)(base + p.o_xp);
+  s.gup = (uint16_t*)(base + p.o_gup);
+  s.actp = (uint16_t*)(base + p.o_actp);
+  s.yp = (float*)(base + p.o_yp);
   (void)K;
   return s;
 }
@@ -718,12 +785,18 @@ int bind_layer(Step& st, int l, int slot, bool fresh, LayerView* v) {
   const size_t u0 = ctx->off_p[l][0];
   auto at = [&](int t) { return base + (ctx->off_p[l][t] - u0); };
   float* g = ctx->gains[slot];
+  v->wr = nullptr;
   if (p.esz == 2) {
     v->wqkv = (const uint16_t*)at(1);
     v->wo = (const uint16_t*)at(4);
     v->wgu = (const uint16_t*)at(6);
     v->wd = (const uint16_t*)at(8);
     v->ldd = p.F;
+    if (p.E > 0) {  // router, then all experts' gate|up and down matrices
+      v->wr = (const uint16_t*)at(6);
+      v->wgu = (const uint16_t*)at(7);
+      v->ldd = p.Fe;
+    }
     if (fresh) {
       CKL(gains_to_f32(at(0), true, g, p.h, ctx->s_comp));
       CKL(gains_to_f32(at(5), true, g + p.h, p.h, ctx->s_comp));
@@ -785,6 +858,49 @@ double attn_flop(const Step& st, const Plan& p) {
   return 2.0 * st.B * p.nq * (double)p.d * st.S * (st.S + 1.0);
 }
 
+// Mixture-of-experts FFN forward of layer l: router logits, top-k routing,
+// rows grouped by expert, one gated gate|up GEMM (SwiGLU in the epilogue) and
+// one down GEMM per expert over its block of rows, then the weighted combine
+// into the residual stream, y = h_mid + sum_j w_j y_j. The expert counts come
+// back to the host, which launches the expert GEMMs.
+int moe_ffn_forward(Step& st, int l, const LayerView& w, const ActSlot& a, float* y) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  const int T = st.T, h = p.h, E = p.E, k = p.topk, Fe = p.Fe, n = T * k;
+  cudaStream_t s = ctx->s_comp;
+  CKR(gemm(ctx, GEMM_NT, EPI_F32, a.m, w.wr, a.r, nullptr, T, E, h, h, h, E));
+  CKL(moe_route(a.r, T, E, k, a.sel, a.w, ctx->moe_counts, ctx->moe_route + (size_t)(l - 1) * T * k, s));
+  CKL(moe_permute(a.sel, n, E, ctx->moe_counts, a.perm, a.spos, s));
+  CKL(moe_gather(a.m, a.perm, n, k, h, a.xp, s));
+  CK(cudaMemcpyAsync(ctx->moe_counts_host, ctx->moe_counts, (size_t)E * 4, cudaMemcpyDeviceToHost, s));
+  CK(cudaStreamSynchronize(s));
+  std::vector<int>& cnt = ctx->moe_slot_counts[(l - 1) % st.K];
+  int total = 0;
+  for (int e = 0; e < E; ++e) {
+    cnt[e] = ctx->moe_counts_host[e];
+    total += cnt[e];
+  }
+  if (total != n) return set_err(ctx, MT_ERR_CUDA, "expert counts do not add up (device error)");
+  size_t off = 0;
+  for (int e = 0; e < E; ++e) {
+    const int Me = cnt[e];
+    if (Me > 0) {
+      GemmParams gp{Me, Fe, h, EPI_BF16, a.gup + off * 2 * Fe, nullptr, 2 * Fe, 0, 1};
+      gp.gated = 1;
+      gp.u_off = Fe;
+      gp.u_col = Fe;
+      gp.act = a.actp + off * Fe;
+      gp.ld_act = Fe;
+      CKR(gemm_p(ctx, GEMM_NT, gp, a.xp + off * h, w.wgu + (size_t)e * 2 * Fe * h, h, h, 2.0 * Me * 2 * Fe * h));
+      CKR(gemm(ctx, GEMM_NT, EPI_F32, a.actp + off * Fe, w.wd + (size_t)e * h * Fe, a.yp + off * h, nullptr, Me, h,
+               Fe, Fe, Fe, h));
+    }
+    off += (size_t)Me;
+  }
+  CKL(moe_combine(a.hmid, a.yp, a.spos, a.w, T, k, h, y, s));
+  return MT_OK;
+}
+
 int layer_forward(Step& st, int l, const LayerView& w) {
   mt_ctx* ctx = st.ctx;
   const Plan& p = ctx->P;
@@ -803,6 +919,7 @@ int layer_forward(Step& st, int l, const LayerView& w) {
   }
   CKR(gemm(ctx, GEMM_NT, EPI_F32_ADD, a.o, w.wo, a.hmid, x, T, h, p.qd, p.qd, p.qd, h));
   CKL(rmsnorm_fwd(a.hmid, w.w2, a.m, a.rstd2, T, h, ctx->cfg.norm_eps, s));
+  if (p.E > 0) return moe_ffn_forward(st, l, w, a, y);
   {  // gate-up projection with SwiGLU fused: g, u (kept for the backward) and act = silu(g) u
     GemmParams gp{T, p.Fp, h, EPI_BF16, a.gu, nullptr, 2 * p.Fp, 0, 1};
     gp.gated = 1;
@@ -870,6 +987,53 @@ int grad_slot_release(Step& st, int g) {
   return MT_OK;
 }
 
+// Mixture-of-experts FFN backward of layer l, from dh (the gradient of the
+// layer output) to ctx->dm (the gradient of the FFN input m); writes the
+// experts' and the router's gradients and sends them to the host.
+int moe_ffn_backward(Step& st, int l, const LayerView& w, const ActSlot& a, int g, float* g_router,
+                     float* g_gu, float* g_down) {
+  mt_ctx* ctx = st.ctx;
+  const Plan& p = ctx->P;
+  const int T = st.T, h = p.h, E = p.E, k = p.topk, Fe = p.Fe;
+  cudaStream_t s = ctx->s_comp;
+  const std::vector<int>& cnt = ctx->moe_slot_counts[(l - 1) % st.K];
+  CKL(moe_combine_bwd(ctx->dh, a.yp, a.spos, a.w, T, k, h, ctx->moe_dyp, ctx->moe_dw, s));
+  float* dxp = a.yp;  // the routed outputs are consumed: their rows take d(routed inputs)
+  size_t off = 0;
+  for (int e = 0; e < E; ++e) {
+    const int Me = cnt[e];
+    float* gd = g_down + (size_t)e * h * Fe;
+    float* ggu = g_gu + (size_t)e * 2 * Fe * h;
+    if (Me == 0) {  // no rows routed to e: its gradients are zero
+      CK(cudaMemsetAsync(gd, 0, (size_t)h * Fe * 4, s));
+      CK(cudaMemsetAsync(ggu, 0, (size_t)2 * Fe * h * 4, s));
+      continue;
+    }
+    const uint16_t* dy = ctx->moe_dyp + off * h;
+    uint16_t* gu = a.gup + off * 2 * Fe;
+    // y_e = act Wd_e^T: dWd_e = dY^T act, dact = dY Wd_e -> (dg, du) in place over (g, u)
+    CKR(gemm(ctx, GEMM_TN, EPI_F32, dy, a.actp + off * Fe, gd, nullptr, h, Fe, Me, h, Fe, Fe));
+    GemmParams bp{Me, Fe, h, EPI_BF16, gu, nullptr, 2 * Fe, 0, 1};
+    bp.swiglu_bwd = 1;
+    bp.gu = gu;
+    bp.ld_gu = 2 * Fe;
+    bp.u_col = Fe;
+    CKR(gemm_p(ctx, GEMM_NN, bp, dy, w.wd + (size_t)e * h * Fe, h, Fe, 2.0 * Me * Fe * h));
+    // g|u = x Wgu_e^T: dWgu_e = d(g|u)^T x, dx = d(g|u) Wgu_e
+    CKR(gemm(ctx, GEMM_TN, EPI_F32, gu, a.xp + off * h, ggu, nullptr, 2 * Fe, h, Me, 2 * Fe, h, h));
+    CKR(gemm(ctx, GEMM_NN, EPI_F32, gu, w.wgu + (size_t)e * 2 * Fe * h, dxp + off * h, nullptr, Me, h, 2 * Fe,
+             2 * Fe, h, h));
+    off += (size_t)Me;
+  }
+  CKR(grad_piece(st, g, l, 7, 8));
+  CKL(moe_unpermute(dxp, a.spos, T, k, h, ctx->dm, s));
+  // router: dr, then dm += dr Wr and dWr = dr^T m
+  CKL(moe_router_bwd(a.w, ctx->moe_dw, a.sel, T, k, E, ctx->moe_dr, s));
+  CKR(gemm(ctx, GEMM_NN, EPI_F32_ADD, ctx->moe_dr, w.wr, ctx->dm, ctx->dm, T, h, E, E, h, h));
+  CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->moe_dr, a.m, g_router, nullptr, E, h, T, E, h, h));
+  return grad_piece(st, g, l, 6, 6);
+}
+
 int layer_backward(Step& st, int l, const LayerView& w) {
   mt_ctx* ctx = st.ctx;
   const Plan& p = ctx->P;
@@ -883,26 +1047,31 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   const size_t u0 = ctx->off_g[l][0];
   auto GT = [&](int t) { return (float*)((uint8_t*)G + (ctx->off_g[l][t] - u0)); };
   // Gradient tensors go to the host in four groups, each as soon as it is
-  // complete: [Wd], [Wg Wu], [Wo w_ffn], [w_attn Wq Wk Wv].
-  // h_out = h_mid + act Wd^T
-  CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dh_b, a.act, GT(8), nullptr, h, F, T, h, Fp, F));
-  CKR(grad_piece(st, g, l, 8, 8));
-  {  // dact = dh Wd, turned into (dg, du) in place over (g, u) by the epilogue
-    GemmParams bp{T, Fp, h, EPI_BF16, a.gu, nullptr, 2 * Fp, 0, 1};
-    bp.swiglu_bwd = 1;
-    bp.gu = a.gu;
-    bp.ld_gu = 2 * Fp;
-    bp.u_col = Fp;
-    CKR(gemm_p(ctx, GEMM_NN, bp, ctx->dh_b, w.wd, h, w.ldd, 2.0 * T * Fp * h));
-  }
-  if (Fp == F) {
-    CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, 2 * F, h, T, 2 * Fp, h, h));
+  // complete: [Wd], [Wg Wu], [Wo w_ffn], [w_attn Wq Wk Wv] (mixture of
+  // experts: [experts' Wgu Wd], [router], then the same two).
+  if (p.E > 0) {
+    CKR(moe_ffn_backward(st, l, w, a, g, GT(6), GT(7), GT(8)));
   } else {
-    CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, F, h, T, 2 * Fp, h, h));
-    CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu + Fp, a.m, GT(7), nullptr, F, h, T, 2 * Fp, h, h));
+    // h_out = h_mid + act Wd^T
+    CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dh_b, a.act, GT(8), nullptr, h, F, T, h, Fp, F));
+    CKR(grad_piece(st, g, l, 8, 8));
+    {  // dact = dh Wd, turned into (dg, du) in place over (g, u) by the epilogue
+      GemmParams bp{T, Fp, h, EPI_BF16, a.gu, nullptr, 2 * Fp, 0, 1};
+      bp.swiglu_bwd = 1;
+      bp.gu = a.gu;
+      bp.ld_gu = 2 * Fp;
+      bp.u_col = Fp;
+      CKR(gemm_p(ctx, GEMM_NN, bp, ctx->dh_b, w.wd, h, w.ldd, 2.0 * T * Fp * h));
+    }
+    if (Fp == F) {
+      CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, 2 * F, h, T, 2 * Fp, h, h));
+    } else {
+      CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, F, h, T, 2 * Fp, h, h));
+      CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu + Fp, a.m, GT(7), nullptr, F, h, T, 2 * Fp, h, h));
+    }
+    CKR(grad_piece(st, g, l, 6, 7));
+    CKR(gemm(ctx, GEMM_NN, EPI_F32, a.gu, w.wgu, ctx->dm, nullptr, T, h, 2 * Fp, 2 * Fp, h, h));
   }
-  CKR(grad_piece(st, g, l, 6, 7));
-  CKR(gemm(ctx, GEMM_NN, EPI_F32, a.gu, w.wgu, ctx->dm, nullptr, T, h, 2 * Fp, 2 * Fp, h, h));
   // RMSNorm 2 (+ residual): dh_mid written over h_mid (row-local, in place)
   CKL(rmsnorm_bwd(a.hmid, w.w2, a.rstd2, ctx->dm, ctx->dh, a.hmid, ctx->dhmid_b, GT(5), ctx->norm_ws, T, h, s));
   // h_mid = x + o Wo^T
@@ -1467,7 +1636,7 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
   std::string why;
   if (!cfg_valid(*cfg, &why)) {
     fprintf(stderr, "mt_create: %s\n", why.c_str());
-    return (cfg->n_experts || cfg->top_k || cfg->expert_ffn || cfg->hidden % 64 ||
+    return ((cfg->n_experts && cfg->param_dtype != MT_BF16) || cfg->hidden % 64 ||
             (cfg->head_dim != 16 && cfg->head_dim != 32 && cfg->head_dim != 64 && cfg->head_dim != 128))
                ? MT_ERR_UNSUPPORTED
                : MT_ERR_ARG;
@@ -1542,8 +1711,11 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
       (e = cudaHostAlloc((void**)&ctx->host_rows, (size_t)ctx->P.Tmax * ctx->P.h * ctx->P.esz, cudaHostAllocDefault)) !=
           cudaSuccess ||
       (e = cudaHostAlloc((void**)&ctx->host_grad_rows, (size_t)ctx->P.Tmax * ctx->P.h * 4, cudaHostAllocDefault)) !=
+          cudaSuccess ||
+      (e = cudaHostAlloc((void**)&ctx->moe_counts_host, ((size_t)ctx->P.E + 1) * 4, cudaHostAllocDefault)) !=
           cudaSuccess)
     return fail(MT_ERR_CUDA, "cudaHostAlloc", e);
+  ctx->moe_slot_counts.assign(std::max(1, cfg->max_K), std::vector<int>(ctx->P.E, 0));
   if (carve(ctx) != MT_OK) {
     mt_destroy(ctx);
     return MT_ERR_BUDGET;
@@ -1707,12 +1879,25 @@ int step_common(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) rc = set_err(ctx, MT_ERR_CUDA, cudaGetErrorString(e));
     }
+    if (rc == MT_OK) ctx->last_T = T;
     compute_stats(ctx);
     if (!ctx->trace)
       ctx->stats.step_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
   }
   if (cur != ctx->device) cudaSetDevice(cur);
   return rc;
+}
+
+int mt_get_routing(const mt_ctx* ctx, int32_t* host_out, size_t n) {
+  if (!ctx || !host_out) return MT_ERR_ARG;
+  if (ctx->cfg.n_experts == 0 || ctx->last_T == 0) return MT_ERR_STATE;
+  const size_t need = (size_t)ctx->cfg.n_layers * ctx->last_T * ctx->cfg.top_k;
+  if (n != need) return MT_ERR_ARG;
+  if (cudaMemcpy(host_out, ctx->moe_route, need * 4, cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return MT_ERR_CUDA;
+  }
+  return MT_OK;
 }
 
 int mt_get_stats(const mt_ctx* ctx, mt_stats* out) {
@@ -1774,6 +1959,7 @@ void mt_destroy(mt_ctx* ctx) {
   if (ctx->host_stage) cudaFreeHost(ctx->host_stage);
   if (ctx->host_rows) cudaFreeHost(ctx->host_rows);
   if (ctx->host_grad_rows) cudaFreeHost(ctx->host_grad_rows);
+  if (ctx->moe_counts_host) cudaFreeHost(ctx->moe_counts_host);
   delete ctx;
 }
 

@@ -26,6 +26,14 @@ LLAMA8B = oracle.Config(n_layers=32, hidden=4096, n_heads=32, n_kv_heads=8, head
                         vocab=128256, rope_theta=5e5, norm_eps=1e-5)
 
 
+# Mixture-of-experts workloads. The Qwen3-235B-style layer: hidden 4096, 64 q / 4 kv heads x 128, 128 experts,
+# top-8, expert FFN 1536, vocab 151936 (RoPE theta 1e6 and RMSNorm eps 1e-6 as in Qwen3; the pages give neither).
+QWEN3_MOE = oracle.Config(n_layers=8, hidden=4096, n_heads=64, n_kv_heads=4, head_dim=128, ffn_dim=0, vocab=151936,
+                          rope_theta=1e6, norm_eps=1e-6, n_experts=128, top_k=8, expert_ffn=1536)
+TINY_MOE = oracle.Config(n_layers=2, hidden=64, n_heads=4, n_kv_heads=2, head_dim=16, ffn_dim=0, vocab=256,
+                         rope_theta=1e4, norm_eps=1e-5, n_experts=8, top_k=2, expert_ffn=32)
+
+
 def with_layers(cfg: oracle.Config, n_layers: int) -> oracle.Config:
     d = dict(cfg.__dict__)
     d["n_layers"] = n_layers

@@ -8,7 +8,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.common import LLAMA8B, SMALL, TINY, TINY_GQA
+from tests.common import LLAMA8B, QWEN3_MOE, SMALL, TINY, TINY_GQA, TINY_MOE
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -24,7 +24,7 @@ def mt():
 def _cfg(mt, c, bf16=False, **kw):
     return mt.make_cfg(c.n_layers, c.hidden, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.vocab, c.rope_theta,
                        c.norm_eps, kw.get("max_batch", 2), kw.get("max_seq", 32), kw.get("max_K", 2),
-                       mt.MT_BF16 if bf16 else mt.MT_F32)
+                       mt.MT_BF16 if bf16 else mt.MT_F32, c.n_experts, c.top_k, c.expert_ffn)
 
 
 def test_header_symbols_are_exported(mt):
@@ -94,3 +94,31 @@ def test_create_without_gpu_fails_cleanly(mt):
     with pytest.raises(mt.MtError) as e:
         mt.mt_create(_cfg(mt, TINY), 1 << 40)
     assert e.value.code in (mt.MT_ERR_CUDA, mt.MT_ERR_BUDGET)
+
+
+@pytest.mark.parametrize("c", [TINY_MOE, QWEN3_MOE], ids=["tiny_moe", "qwen3_moe"])
+def test_moe_layout_matches_definition(mt, c):
+    cfg = _cfg(mt, c, True)
+    assert mt.mt_packed_bytes(cfg, mt.MT_BF16) == oracle.packed_bytes(c, True)
+    assert mt.mt_packed_bytes(cfg, mt.MT_F32) == oracle.packed_bytes(c, False)
+    for unit, t, name, shape, _ in oracle.tensor_list(c):
+        for bf16 in (False, True):
+            assert mt.mt_tensor_offset(cfg, mt.MT_BF16 if bf16 else mt.MT_F32, unit, t) == \
+                oracle.tensor_offset(c, unit, t, bf16), name
+
+
+def test_moe_budget_and_validation(mt):
+    """The Qwen3-style MoE layer (4.97 GB of bf16 weights) fits two weight
+    slots, two fp32 gradient slots and one block of routed activations well
+    inside the device; invalid expert settings are rejected."""
+    c = QWEN3_MOE
+    cfg = _cfg(mt, c, True, max_batch=1, max_seq=4096, max_K=2)
+    b = mt.mt_required_budget(cfg)
+    layer_bf16 = oracle.tensor_offset(c, 2, 0, True)[0] - oracle.tensor_offset(c, 1, 0, True)[0]
+    assert 6 * layer_bf16 < b < 6 * layer_bf16 + 12 * 2**30
+    assert mt.mt_required_budget(_cfg(mt, c, False, max_batch=1, max_seq=4096, max_K=2)) == 0  # fp32 params
+    import dataclasses
+    for kw in (dict(n_experts=12), dict(top_k=0), dict(top_k=9, n_experts=8), dict(expert_ffn=20),
+               dict(ffn_dim=1024)):
+        bad = dataclasses.replace(TINY_MOE, **kw)
+        assert mt.mt_required_budget(_cfg(mt, bad, True)) == 0, kw
