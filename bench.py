@@ -31,7 +31,12 @@ WORKLOADS = {
     "llama8b_long": (32, 4096, 32, 8, 128, 14336, 128256, 5e5, 1, 16384, 8, True),
     "small": (8, 1024, 16, 16, 64, 2816, 32000, 1e4, 4, 2048, 4, False),
     "tiny": (2, 64, 4, 4, 16, 172, 256, 1e4, 2, 32, 1, False),
+    # Qwen3-235B-style mixture-of-experts layers, the first 8 of 94 (host RAM bound)
+    "qwen3_moe": (8, 4096, 64, 4, 128, 0, 151936, 1e6, 1, 4096, 2, True),
 }
+# Mixture-of-experts workloads: (experts, top-k, expert FFN width)
+MOE = {"qwen3_moe": (128, 8, 1536)}
+NORM_EPS = {"qwen3_moe": 1e-6}
 METRIC = "train tokens/sec (fwd+bwd, weights streamed from host) at 8B shape; % roofline"
 _T0 = time.time()
 
@@ -99,18 +104,70 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-def model_flops(shape, B, S):
+def model_flops(shape, B, S, moe=None):
     """Algorithmic work of one step, as counted for the roofline: per decoder
     layer 2*T*P_lin for each of forward, recompute, input-gradient and
     weight-gradient products, plus causal attention (forward, recompute and
-    2.5x backward); head 4 GEMM-equivalents (two logit passes, dX, dW)."""
+    2.5x backward); head 4 GEMM-equivalents (two logit passes, dX, dW).
+    With experts (moe = (E, k, Fe)) a token passes through the router and k
+    experts: P_lin counts those, not all E (the streamed bytes do)."""
     L, h, nq, nkv, d, F, V = shape[:7]
     T = B * S
     P_lin = h * (nq * d) * 2 + 2 * h * (nkv * d) + 3 * h * F
+    if moe:
+        E, k, Fe = moe
+        P_lin += E * h + k * 3 * Fe * h
     A = 2.0 * B * nq * d * S * (S + 1)
     layer = 2.0 * T * P_lin * 4 + A * (1 + 1 + 2.5)
     head = 4 * 2.0 * T * V * h
     return layer, head, P_lin
+
+
+def layer_params(shape, moe=None):
+    """Matrix parameters of one decoder layer as streamed (all experts)."""
+    L, h, nq, nkv, d, F, V = shape[:7]
+    p = h * (nq * d) * 2 + 2 * h * (nkv * d) + 3 * h * F
+    if moe:
+        E, k, Fe = moe
+        p += E * h + E * 3 * Fe * h
+    return p
+
+
+def moe_gemm_algorithmic_bytes(shape, B, S, K, head_rows, moe, fuse_top=True):
+    """gemm_algorithmic_bytes for mixture-of-experts layers: attention
+    projections as in the dense layer; router; per expert its rows of the
+    gate|up and down products (bf16 operands, fp32 routed outputs and weight
+    gradients), every expert's weights read once per product kind. Launch
+    count assumes every expert receives rows."""
+    L, h, nq, nkv, d, F, V = shape[:7]
+    E, k, Fe = moe
+    T = B * S
+    R = T * k
+    qkv = (nq + 2 * nkv) * d
+    fwd = ((T * h + qkv * h + T * qkv) * 2 + (T * nq * d + h * nq * d) * 2 + T * h * 8 +
+           (T * h + E * h) * 2 + T * E * 4 +                       # router logits (fp32)
+           (R * h + E * 2 * Fe * h + R * 2 * Fe + R * Fe) * 2 +      # gate|up, writes g|u and act
+           (R * Fe + E * h * Fe) * 2 + R * h * 4)                   # down, fp32 routed outputs
+    bwd = ((R * h + R * Fe) * 2 + E * h * Fe * 4 +                  # dWd
+           (R * h + E * h * Fe) * 2 + 2 * R * 2 * Fe * 2 +          # d act -> (dg, du) in place
+           (R * 2 * Fe + R * h) * 2 + E * 2 * Fe * h * 4 +          # dWgu
+           (R * 2 * Fe + E * 2 * Fe * h) * 2 + R * h * 4 +          # d routed inputs
+           (T * E + E * h) * 2 + T * h * 8 +                        # dm += dr Wr
+           (T * E + T * h) * 2 + E * h * 4 +                        # dWr
+           (T * h + T * nq * d) * 2 + h * nq * d * 4 +              # dWo
+           (T * h + h * nq * d + T * nq * d) * 2 +                  # do
+           (T * qkv + T * h) * 2 + qkv * h * 4 +                    # dWqkv
+           (T * qkv + qkv * h) * 2 + T * h * 4)                     # dx
+    slices = (V + head_rows - 1) // head_rows
+    head = 0
+    for i in range(slices):
+        Rr = min(head_rows, V - i * head_rows)
+        head += 2 * ((T * h + Rr * h) * 2 + T * Rr * 4)
+        head += (T * Rr + Rr * h) * 2 + T * h * (4 if i == 0 else 8)
+        head += (T * Rr + T * h) * 2 + Rr * h * 4
+    top = L - K * ((L + K - 1) // K - 1)
+    n_fwd = L + (L - top if fuse_top else L)
+    return n_fwd * fwd + L * bwd + head, (3 + 2 * E) * n_fwd + (6 + 4 * E) * L + 4 * slices
 
 
 def gemm_algorithmic_bytes(shape, B, S, K, head_rows, fuse_top=True):
@@ -161,12 +218,12 @@ def replica_throughput(world, tokens_per_step, steps, seconds):
     return world * tokens_per_step * steps / seconds
 
 
-def head_slice_rows(shape, esz):
+def head_slice_rows(shape, esz, moe=None):
     """Rows of an LM-head vocab slice: the fewest equal slices (multiples of
     256 rows) whose bytes fit one packed decoder layer (as the library sizes
     them)."""
     L, h, nq, nkv, d, F, V = shape[:7]
-    layer = (2 * h + (nq * d) * h * 2 + 2 * (nkv * d) * h + 3 * F * h) * esz
+    layer = (2 * h + layer_params(shape, moe)) * esz
     ns = max(1, (V * h * esz + layer - 1) // layer)
     while True:
         r = min(V, (((V + ns - 1) // ns) + 255) // 256 * 256)
@@ -244,7 +301,7 @@ def host_link_probe(torch, nbytes=436 * 2**20):
     return out
 
 
-def cpu_oracle_sample(shape, S_sample, seed=5):
+def cpu_oracle_sample(shape, S_sample, seed=5, moe=None, eps=1e-5):
     """Time the CPU oracle (single thread) on one decoder layer plus the head
     of this shape at B=1, S=S_sample, and extrapolate to the full depth:
     t(L layers) = t(1 layer + head) + (L-1) * t_layer, with t_layer taken by
@@ -252,7 +309,8 @@ def cpu_oracle_sample(shape, S_sample, seed=5):
     import oracle
     import seedgen
     L, h, nq, nkv, d, F, V, theta = shape[:8]
-    cfg = oracle.Config(1, h, nq, nkv, d, F, V, theta, 1e-5)
+    E, k, Fe = moe or (0, 0, 0)
+    cfg = oracle.Config(1, h, nq, nkv, d, F, V, theta, eps, E, k, Fe)
     packed = np.zeros(oracle.packed_bytes(cfg, True), np.uint8)
     offs = []
     for unit, t, name, shp, is_gain in oracle.tensor_list(cfg):
@@ -263,7 +321,7 @@ def cpu_oracle_sample(shape, S_sample, seed=5):
     t0 = time.perf_counter()
     oracle.forward_backward(cfg, packed, tok, lab, bf16=True)
     t1 = time.perf_counter() - t0
-    layer_f, head_f, P_lin = model_flops((1, h, nq, nkv, d, F, V), 1, S_sample)
+    layer_f, head_f, P_lin = model_flops((1, h, nq, nkv, d, F, V), 1, S_sample, moe)
     layer_f_plain = layer_f * 3 / 4  # the oracle does no recompute
     frac_layer = layer_f_plain / (layer_f_plain + head_f * 3 / 4)
     t_layer = t1 * frac_layer
@@ -279,7 +337,8 @@ def run_reference(args, shape, B, S):
     S_sample = 8
     vals = []
     for i in range(args.warmup + args.steps):
-        v, t1 = cpu_oracle_sample(shape, S_sample, seed=100 + i)
+        v, t1 = cpu_oracle_sample(shape, S_sample, seed=100 + i, moe=MOE.get(args.workload),
+                                  eps=NORM_EPS.get(args.workload, 1e-5))
         if i >= args.warmup:
             vals.append(v)
     value = float(np.median(vals))
@@ -345,12 +404,15 @@ def main():
     import seedgen
     mt.build()
     L, h, nq, nkv, d, F, V, theta = shape
-    cfg = mt.make_cfg(L, h, nq, nkv, d, F, V, theta, 1e-5, B, S, K, mt.MT_BF16 if bf16 else mt.MT_F32)
+    moe = MOE.get(args.workload)
+    E, k_top, Fe = moe or (0, 0, 0)
+    eps = NORM_EPS.get(args.workload, 1e-5)
+    cfg = mt.make_cfg(L, h, nq, nkv, d, F, V, theta, eps, B, S, K, mt.MT_BF16 if bf16 else mt.MT_F32, E, k_top, Fe)
     budget = mt.mt_required_budget(cfg)
     log(f"workload {args.workload} L={L} B={B} S={S} K={K}: device arena {budget / 2**30:.2f} GiB")
     arena = torch.empty(budget, dtype=torch.uint8, device="cuda")
     streams = [torch.cuda.Stream() for _ in range(3)]
-    sess = mt.Session(mt.ModelShape(L, h, nq, nkv, d, F, V, theta, 1e-5), B, S, K,
+    sess = mt.Session(mt.ModelShape(L, h, nq, nkv, d, F, V, theta, eps, E, k_top, Fe), B, S, K,
                       mt.MT_BF16 if bf16 else mt.MT_F32, device_budget=budget, device_arena=arena.data_ptr(),
                       streams=[s.cuda_stream for s in streams])
     # Parameters: N(0, 0.02) matrices, unit RMSNorm gains, per-rank seed.
@@ -436,7 +498,8 @@ def main():
     peaks, peak_kind = read_peaks()
     gemm_tflops = kst["gemm_flop"] / (kst["gemm_ms"] / 1e3) / 1e12 if kst.get("gemm_ms") else None
     peak_tf = float(peaks.get("bf16_tflops_sustained", peaks.get("bf16_tflops")))
-    layer_f, head_f, P_lin = model_flops(shape, B, S)
+    layer_f, head_f, P_lin = model_flops(shape, B, S, moe)
+    P_bytes = layer_params(shape, moe)  # streamed matrix parameters of a layer
     step_flop = L * layer_f + head_f
     # Roofline of the whole step: per unit, the slower of its work at the
     # tensor-core peak and its streamed bytes at the measured host link.
@@ -444,13 +507,17 @@ def main():
     d2h_bw = link["d2h_concurrent_gbs"] * 1e9
     per_step_h2d = agg["h2d_bytes"] / steps
     per_step_d2h = agg["d2h_bytes"] / steps
-    layer_h2d = per_step_h2d * (L * P_lin * 2) / max(1.0, (L * P_lin * 2 + 2 * V * h * 2)) / L
-    t_layer = max(layer_f / (peak_tf * 1e12), layer_h2d / h2d_bw, 4.0 * (P_lin + 2 * h) / d2h_bw)
+    layer_h2d = per_step_h2d * (L * P_bytes * 2) / max(1.0, (L * P_bytes * 2 + 2 * V * h * 2)) / L
+    t_layer = max(layer_f / (peak_tf * 1e12), layer_h2d / h2d_bw, 4.0 * (P_bytes + 2 * h) / d2h_bw)
     t_head = max(head_f / (peak_tf * 1e12), (per_step_h2d - L * layer_h2d) / h2d_bw, (2.0 * V * h * 4) / d2h_bw)
     t_roof = L * t_layer + t_head
     ms_per_step = dev_ms / steps
-    gemm_bytes, gemm_launches = gemm_algorithmic_bytes(shape, B, S, K, head_slice_rows(shape, 2 if bf16 else 4),
-                                                       fuse_top=not args.no_fuse_top)
+    rows = head_slice_rows(shape, 2 if bf16 else 4, moe)
+    if moe:
+        gemm_bytes, gemm_launches = moe_gemm_algorithmic_bytes(shape, B, S, K, rows, moe,
+                                                               fuse_top=not args.no_fuse_top)
+    else:
+        gemm_bytes, gemm_launches = gemm_algorithmic_bytes(shape, B, S, K, rows, fuse_top=not args.no_fuse_top)
     traffic_known = (args.workload == "llama8b" and (L, B, S, K) == (32, 2, 4096, 4) and bf16
                      and not args.no_fuse_top and kst["n_gemm"] == GEMM_LAUNCHES_8B_STEP)
     line = {
@@ -469,6 +536,7 @@ def main():
         "config": {"workload": args.workload, "global_batch": B * world, "seq_len": S, "checkpoint_every": K,
                    "layers": L, "hidden": h, "heads": f"{nq}q/{nkv}kv x {d}", "ffn": F, "vocab": V,
                    "host_params": "bf16" if bf16 else "fp32", "parallelism": f"replicas x{world}",
+                   **({"experts": f"{E} x SwiGLU {Fe}, top-{k_top}, softmax router"} if moe else {}),
                    "l2": "inputs larger than L2 (every step streams all weights from host)",
                    "optimizer_step": f"host AdamW included ({args.optimizer})" if args.optimizer else "none (fwd+bwd)"},
         "e2e": {"value": e2e, "unit": "tokens/s", "h2d_bytes_per_step": int(per_step_h2d + 2 * T * 4),
@@ -508,15 +576,16 @@ def main():
         "loss": losses[-1],
         "init_s": init_s,
     }
+    sess.close()  # frees the pinned model before the oracle sample
+    del arena
     if not args.no_cpu_baseline and world == 1:
         log("timing the CPU oracle sample")
-        v, t1 = cpu_oracle_sample(shape, 8)
+        v, t1 = cpu_oracle_sample(shape, 8, moe=moe, eps=eps)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
                                 "sample": f"one decoder layer + LM head of the {args.workload} shape at B=1, S=8 "
                                           f"({t1:.1f} s single-threaded fp32 oracle), extrapolated linearly to "
                                           f"{L} layers; host has {os.cpu_count()} cores"}
     print(json.dumps(line), flush=True)
-    sess.close()
     if dist:
         dist.destroy_process_group()
 

@@ -56,6 +56,64 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
   n_blk = r / gsize;
 }
 
+// One output tile of the (possibly grouped) product: its row/column origin,
+// K range and operand offsets.
+struct TileInfo {
+  int m0, n0, nb;
+  int crow;        // row of C holding the tile's first row
+  int a_k0, b_k0;  // added to the K coordinate of A / of B
+  int b_n0;        // added to the row (NT) coordinate of B
+  int nkb;         // K steps
+  bool skip;
+};
+
+// A_MN marks the weight-gradient form (TN); B_MN without A_MN is NN.
+template <bool A_MN, bool B_MN>
+__device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, int num_m, int num_n, int tile_n,
+                                                int num_kb) {
+  TileInfo t;
+  const bool grouped = p.grp_seg != nullptr;
+  int e = 0, local = tile;
+  if (grouped && A_MN) {
+    e = tile / (num_m * num_n);
+    local = tile - e * num_m * num_n;
+  }
+  int mb, nb;
+  tile_coords(local, num_m, num_n, p.group_m, mb, nb);
+  t.m0 = mb * BM;
+  t.n0 = nb * tile_n;
+  t.nb = nb;
+  t.crow = t.m0;
+  t.a_k0 = t.b_k0 = t.b_n0 = 0;
+  t.nkb = num_kb;
+  t.skip = false;
+  if (grouped) {
+    if (A_MN) {  // TN: this expert's segment is the reduction
+      const int s0 = p.grp_seg[e], s1 = p.grp_seg[e + 1];
+      t.a_k0 = t.b_k0 = s0;
+      t.nkb = (s1 - s0) / BK;
+      t.crow = e * p.M + t.m0;
+    } else {
+      e = p.grp_tile_e[mb];
+      t.skip = e < 0;
+      if (!t.skip) {
+        if (B_MN) t.b_k0 = e * p.grp_b_rows;  // NN: the expert's K rows of B
+        else t.b_n0 = e * p.grp_b_rows;       // NT: the expert's rows of B
+      }
+    }
+  }
+  return t;
+}
+
+// Zeros over columns [n0, n0 + BN) of fp32 row `row` (an expert that
+// received no rows: its weight gradient is zero).
+template <int BN>
+__device__ __forceinline__ void zero_tile_row(const GemmParams& p, int row, bool row_ok, int n0) {
+  if (!row_ok) return;
+  float* out = (float*)p.C + (size_t)row * p.ldc;
+  for (int j = n0; j < n0 + BN && j < p.N; ++j) out[j] = 0.f;
+}
+
 // Store 32 fp32 values as bf16 at columns [col0, col0+32) of a row (partial
 // at the right edge).
 __device__ __forceinline__ void store_bf16_32(uint16_t* out, const float (&v)[32], int col0, int N, bool vec) {
@@ -323,7 +381,8 @@ __global__ void __launch_bounds__(192, 1)
 
   const int tile_n = p.gated ? BN / 2 : BN;  // gated tiles cover BN/2 features (gate + up halves)
   const int num_m = (p.M + BM - 1) / BM, num_n = (p.N + tile_n - 1) / tile_n;
-  const int num_tiles = num_m * num_n;
+  // grouped weight gradients: one M x N output per expert
+  const int num_tiles = num_m * num_n * ((p.grp_seg && A_MN) ? p.grp_E : 1);
   const int num_kb = (p.K + BK - 1) / BK;
 
   if (warp == 0) {
@@ -331,28 +390,29 @@ __global__ void __launch_bounds__(192, 1)
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
-        int mb, nb;
-        tile_coords(tile, num_m, num_n, p.group_m, mb, nb);
-        const int m0 = mb * BM, n0 = nb * tile_n;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        const TileInfo ti = decode_tile<A_MN, B_MN>(p, tile, num_m, num_n, tile_n, num_kb);
+        if (ti.skip) continue;
+        const int m0 = ti.m0, n0 = ti.n0;
+        for (int kb = 0; kb < ti.nkb; ++kb) {
           mbar_wait(&empty[stage], phase ^ 1, abort_flag, kErrTimeoutTma);
           mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
           uint8_t* a_dst = sA + stage * A_BYTES;
           uint8_t* b_dst = sB + stage * C::B_BYTES;
+          const int ka = ti.a_k0 + kb * BK, kb_ = ti.b_k0 + kb * BK;
           if (!A_MN) {
-            tma_load_2d(a_dst, &tmA, &full[stage], kb * BK, m0);
+            tma_load_2d(a_dst, &tmA, &full[stage], ka, m0);
           } else {
 #pragma unroll
-            for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * 8192, &tmA, &full[stage], m0 + 64 * j, kb * BK);
+            for (int j = 0; j < BM / 64; ++j) tma_load_2d(a_dst + j * 8192, &tmA, &full[stage], m0 + 64 * j, ka);
           }
           if (!B_MN && p.gated) {  // gate rows then the matching up rows
-            tma_load_2d(b_dst, &tmB, &full[stage], kb * BK, n0);
-            tma_load_2d(b_dst + (BN / 2) * 128, &tmB, &full[stage], kb * BK, p.u_off + n0);
+            tma_load_2d(b_dst, &tmB, &full[stage], kb_, ti.b_n0 + n0);
+            tma_load_2d(b_dst + (BN / 2) * 128, &tmB, &full[stage], kb_, ti.b_n0 + p.u_off + n0);
           } else if (!B_MN) {
-            tma_load_2d(b_dst, &tmB, &full[stage], kb * BK, n0);
+            tma_load_2d(b_dst, &tmB, &full[stage], kb_, ti.b_n0 + n0);
           } else {
 #pragma unroll
-            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, &full[stage], n0 + 64 * j, kb * BK);
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(b_dst + j * 8192, &tmB, &full[stage], n0 + 64 * j, kb_);
           }
           if (++stage == C::STAGES) {
             stage = 0;
@@ -368,13 +428,16 @@ __global__ void __launch_bounds__(192, 1)
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
-      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+      for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+        const TileInfo ti = decode_tile<A_MN, B_MN>(p, tile, num_m, num_n, tile_n, num_kb);
+        if (ti.skip) continue;
         const int acc = local & 1;
         const uint32_t acc_phase = (local >> 1) & 1;
+        ++local;
         mbar_wait(&tempty[acc], acc_phase ^ 1, abort_flag, kErrTimeoutMma);
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
-        for (int kb = 0; kb < num_kb; ++kb) {
+        for (int kb = 0; kb < ti.nkb; ++kb) {
           mbar_wait(&full[stage], phase, abort_flag, kErrTimeoutMma);
           tc_fence_after();
           const uint32_t a_base = smem_u32(sA + stage * A_BYTES);
@@ -391,22 +454,28 @@ __global__ void __launch_bounds__(192, 1)
             phase ^= 1;
           }
         }
-        tc_commit(&tfull[acc]);
+        tc_commit(&tfull[acc]);  // with no K steps: arrives once earlier work is done
       }
     }
     __syncwarp();
   } else {  // epilogue warps 2..5; warp w reads TMEM lanes 32*(w%4) .. +31
     const uint32_t q = warp & 3;
     int local = 0;
-    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
-      int mb, nb;
-      tile_coords(tile, num_m, num_n, p.group_m, mb, nb);
+    for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x) {
+      const TileInfo ti = decode_tile<A_MN, B_MN>(p, tile, num_m, num_n, tile_n, num_kb);
+      if (ti.skip) continue;
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      ++local;
       mbar_wait(&tfull[acc], acc_phase, abort_flag, kErrTimeoutEpi);
       tc_fence_after();
-      const int row = mb * BM + q * 32 + lane;
-      epilogue_tile<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, row, row < p.M, nb, tile_n);
+      const int r = ti.m0 + q * 32 + lane;  // row within this product's M
+      if (ti.nkb == 0) {
+        zero_tile_row<BN>(p, ti.crow + q * 32 + lane, r < p.M, ti.n0);
+      } else {
+        epilogue_tile<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, ti.crow + q * 32 + lane, r < p.M, ti.nb,
+                          tile_n);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -635,7 +704,9 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cu
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess) return -1;
     attr_set = true;
   }
-  const int tiles = ((p.M + BM - 1) / BM) * ((p.N + BN - 1) / BN);
+  const int tile_n = p.gated ? BN / 2 : BN;
+  const int tiles =
+      ((p.M + BM - 1) / BM) * ((p.N + tile_n - 1) / tile_n) * ((p.grp_seg && A_MN) ? p.grp_E : 1);
   const int grid = tiles < mt_host::num_sms() ? tiles : mt_host::num_sms();
   kern<<<grid, 192, C::SMEM, st>>>(ta, tb, p);
   count_launches(1);
@@ -684,12 +755,22 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
     p.group_m = gm < num_m ? gm : num_m;
   }
   if (p.gated && (mode != GEMM_NT || !p.act || (p.ld_act & 7) || (p.u_col & 7) || p.epi != EPI_BF16)) return -1;
+  const bool grouped = p.grp_seg != nullptr;
+  if (grouped) {
+    if (p.grp_E < 1 || p.rope_tab) return -1;
+    if (mode == GEMM_TN) {
+      if (p.gated || p.swiglu_bwd || p.epi != EPI_F32 || (p.K % BM)) return -1;
+    } else if (!p.grp_tile_e || p.grp_b_rows < 1 || (p.M % BM)) {
+      return -1;
+    }
+    if (mode == GEMM_NN && (p.grp_b_rows % BK || p.K != p.grp_b_rows)) return -1;  // K tiles stay in one expert
+  }
   if (p.swiglu_bwd && (mode != GEMM_NN || !p.gu || (p.ld_gu & 7) || (p.u_col & 7))) return -1;
   if (p.swiglu_bwd) p.vec = (((uintptr_t)p.gu & 15) == 0) ? 1 : 0;
   if (p.gated) p.vec = p.vec && (((uintptr_t)p.act & 15) == 0);
   // BN = 256 unless that leaves most SMs idle (gated tiles are always 256 wide).
   const int tiles256 = ((p.M + BM - 1) / BM) * ((p.N + 255) / 256);
-  const bool wide = tiles256 >= mt_host::num_sms() || p.gated;
+  const bool wide = tiles256 >= mt_host::num_sms() || p.gated || grouped;
   const int BN = wide ? 256 : 128;
   // Wide tiles run on SM pairs (MT_GEMM_PAIR=0 keeps them on single SMs).
   static int pair_mode = -1;
@@ -697,7 +778,7 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
     const char* e = getenv("MT_GEMM_PAIR");
     pair_mode = (e && e[0] == '0') ? 0 : 1;
   }
-  const bool pair = wide && pair_mode;
+  const bool pair = wide && pair_mode && !grouped;  // grouped products run on single SMs
   if (pair) {  // tile groups in units of 256-row blocks
     const int num_m2 = (p.M + 2 * BM - 1) / (2 * BM);
     const int gm = std::max(1, p.group_m / 2);
@@ -708,17 +789,18 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
   int rc = 0;
   if (mode == GEMM_NT) {  // A [M,K] K-major, B [N,K] K-major
     rc |= make_map(&ta, A, p.M, p.K, lda, 64, BM);
+    const int b_all = grouped ? p.grp_E * p.grp_b_rows : 0;  // every expert's rows
     if (p.gated)  // gate and up rows of one combined matrix, 128-row boxes
-      rc |= make_map(&tb, B, p.u_off + p.N, p.K, ldb, 64, 128);
+      rc |= make_map(&tb, B, grouped ? b_all : p.u_off + p.N, p.K, ldb, 64, 128);
     else
-      rc |= make_map(&tb, B, p.N, p.K, ldb, 64, b_rows);
+      rc |= make_map(&tb, B, grouped ? b_all : p.N, p.K, ldb, 64, b_rows);
     if (rc) return -1;
     if (pair) return launch_pair<false, false>(ta, tb, p, st);
     return wide ? launch<256, false, false>(ta, tb, p, st) : launch<128, false, false>(ta, tb, p, st);
   }
   if (mode == GEMM_NN) {  // A [M,K] K-major, B stored [K,N]: MN-major
     rc |= make_map(&ta, A, p.M, p.K, lda, 64, BM);
-    rc |= make_map(&tb, B, p.K, p.N, ldb, 64, 64);
+    rc |= make_map(&tb, B, grouped ? p.grp_E * p.grp_b_rows : p.K, p.N, ldb, 64, 64);
     if (rc) return -1;
     if (pair) return launch_pair<false, true>(ta, tb, p, st);
     return wide ? launch<256, false, true>(ta, tb, p, st) : launch<128, false, true>(ta, tb, p, st);

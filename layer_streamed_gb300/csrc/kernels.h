@@ -40,6 +40,19 @@ struct GemmParams {
   // replaced in place by dg = dact*u*silu'(g), du = dact*silu(g).
   int swiglu_bwd = 0, ld_gu = 0;
   uint16_t* gu = nullptr;
+  // Grouped form (mixture-of-experts products; one launch for all experts,
+  // single-CTA kernel). grp_seg[0..grp_E] (device): expert e owns rows
+  // [grp_seg[e], grp_seg[e+1]) of the routed-row operands, each segment a
+  // multiple of 128 rows (padding rows hold zeros).
+  //  NT, NN: M counts all padded rows; grp_tile_e[m / 128] (device) is the
+  //   expert owning 128-row block m (-1: unused, skipped); expert e's B starts
+  //   e * grp_b_rows rows further (NT: rows of B, NN: K rows of B).
+  //  TN: expert e's M x N output is rows [e*M, (e+1)*M) of C, its reduction
+  //   runs over its own segment (K = all padded rows); an empty segment
+  //   gives zeros.
+  const int* grp_seg = nullptr;
+  const int* grp_tile_e = nullptr;
+  int grp_E = 0, grp_b_rows = 0;
 };
 
 // C[M,N] = op(A) op(B) with bf16 operands, fp32 accumulation (see gemm.cu).
@@ -74,11 +87,14 @@ int swiglu_bwd(uint16_t* gu, const uint16_t* dact, int T, int F, int ld, cudaStr
 // here), log (optional) = a copy of sel.
 int moe_route(const float* r, int T, int E, int k, int32_t* sel, float* w, int32_t* counts, int32_t* log,
               cudaStream_t st);
-// perm[row] = slot, spos[slot] = row for the n = T*k slots.
-int moe_permute(const int32_t* sel, int n, int E, const int32_t* counts, int32_t* perm, int32_t* spos,
+// seg[0..E]: expert e's rows start at seg[e], each segment its count rounded
+// up to 128 rows; tile_e[b] (b < n_blocks): expert of 128-row block b, or -1.
+int moe_segments(const int32_t* counts, int E, int n_blocks, int32_t* seg, int32_t* tile_e, cudaStream_t st);
+// perm[row] = slot, spos[slot] = row for the n = T*k slots (rows from seg[e]).
+int moe_permute(const int32_t* sel, int n, int E, const int32_t* seg, int32_t* perm, int32_t* spos,
                 cudaStream_t st);
-// xp[row] = m[perm[row] / k] (bf16 [n, h]).
-int moe_gather(const uint16_t* m, const int32_t* perm, int n, int k, int h, uint16_t* xp, cudaStream_t st);
+// xp[spos[s]] = m[s / k] for the n slots (bf16 rows of h).
+int moe_gather(const uint16_t* m, const int32_t* spos, int n, int k, int h, uint16_t* xp, cudaStream_t st);
 // y[t] = hmid[t] + sum_j w[t,j] yp[spos[t,j]] (fp32).
 int moe_combine(const float* hmid, const float* yp, const int32_t* spos, const float* w, int T, int k, int h,
                 float* y, cudaStream_t st);

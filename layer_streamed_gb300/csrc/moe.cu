@@ -1,14 +1,15 @@
 // Routing kernels of the mixture-of-experts FFN (the MoE layer template of the
 // streamed workloads, Qwen3-MoE style: softmax router, top-k experts with
 // renormalised weights, SwiGLU experts). The expert products themselves run
-// on the tcgen05 GEMM of gemm.cu, one launch per expert over its contiguous
-// block of routed rows; these kernels move rows between token order and
-// expert order and carry the router's forward and backward.
+// on the grouped form of the tcgen05 GEMM of gemm.cu (one launch per product
+// for all experts); these kernels move rows between token order and expert
+// order and carry the router's forward and backward.
 //
 // Slots: token t's j-th choice is slot t*k + j. The rows of all slots are
-// grouped by expert (expert e's rows start at sum_{f<e} count_f) in
-// ascending slot order, so the grouping, and every sum below, is the same in
-// every run: results are bitwise reproducible.
+// grouped by expert in ascending slot order; expert e's segment starts at
+// sum_{f<e} roundup(count_f, 128), so every 128-row GEMM tile belongs to one
+// expert (the padding rows are zero). The grouping, and every sum below, is
+// the same in every run: results are bitwise reproducible.
 #include <algorithm>
 
 #include "common.cuh"
@@ -79,22 +80,47 @@ __global__ void moe_route_kernel(const float* __restrict__ r, int T, int E, int 
   }
 }
 
-// One block per expert: the rows of expert e in ascending slot order,
-// perm[row] = slot and spos[slot] = row.
-__global__ void __launch_bounds__(1024) moe_permute_kernel(const int32_t* __restrict__ sel, int n, int E,
-                                                           const int32_t* __restrict__ counts,
-                                                           int32_t* __restrict__ perm, int32_t* __restrict__ spos) {
-  __shared__ int warp_tot[32];
-  __shared__ int base_sh;
-  const int e = blockIdx.x;
-  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+// Segments of the routed rows: expert e owns rows [seg[e], seg[e+1]), its
+// count rounded up to a multiple of 128 (whole tiles of the grouped GEMM);
+// tile_e[b] = the expert owning 128-row block b, -1 past the last segment.
+__global__ void __launch_bounds__(1024) moe_segments_kernel(const int32_t* __restrict__ counts, int E, int n_blocks,
+                                                            int32_t* __restrict__ seg, int32_t* __restrict__ tile_e) {
+  __shared__ int s_seg[1025];
   if (threadIdx.x == 0) {
-    int b = 0;
-    for (int f = 0; f < e; ++f) b += counts[f];
-    base_sh = b;
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_seg[e] = acc;
+      acc += (counts[e] + 127) & ~127;
+    }
+    s_seg[E] = acc;
   }
   __syncthreads();
-  int running = base_sh;
+  for (int i = threadIdx.x; i <= E; i += blockDim.x) seg[i] = s_seg[i];
+  for (int b = threadIdx.x; b < n_blocks; b += blockDim.x) {
+    const int row = b * 128;
+    int e = -1;
+    if (row < s_seg[E]) {  // the last e with s_seg[e] <= row: its segment is non-empty and holds row
+      int lo = 0, hi = E - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (s_seg[mid] <= row) lo = mid;
+        else hi = mid - 1;
+      }
+      e = lo;
+    }
+    tile_e[b] = e;
+  }
+}
+
+// One block per expert: the rows of expert e in ascending slot order from
+// the start of its segment, perm[row] = slot and spos[slot] = row.
+__global__ void __launch_bounds__(1024) moe_permute_kernel(const int32_t* __restrict__ sel, int n, int E,
+                                                           const int32_t* __restrict__ seg,
+                                                           int32_t* __restrict__ perm, int32_t* __restrict__ spos) {
+  __shared__ int warp_tot[32];
+  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int running = seg[e];
   for (int c0 = 0; c0 < n; c0 += blockDim.x) {
     const int s = c0 + threadIdx.x;
     const bool hit = s < n && sel[s] == e;
@@ -117,11 +143,13 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int32_t* __rest
   }
 }
 
-// xp[row] = m[perm[row] / k] (bf16 rows of h, 16-byte copies).
-__global__ void moe_gather_kernel(const uint16_t* __restrict__ m, const int32_t* __restrict__ perm, int k, int h,
+// One block per slot s: xp[spos[s]] = m[s / k] (bf16 rows of h, 16-byte
+// copies; the padding rows of the segments are not touched).
+__global__ void moe_gather_kernel(const uint16_t* __restrict__ m, const int32_t* __restrict__ spos, int k, int h,
                                   uint16_t* __restrict__ xp) {
-  const int row = blockIdx.x;
-  const int t = perm[row] / k;
+  const int s = blockIdx.x;
+  const int t = s / k;
+  const int row = spos[s];
   const uint4* src = (const uint4*)(m + (size_t)t * h);
   uint4* dst = (uint4*)(xp + (size_t)row * h);
   for (int i = threadIdx.x; i < h / 8; i += blockDim.x) dst[i] = src[i];
@@ -240,17 +268,24 @@ int moe_route(const float* r, int T, int E, int k, int32_t* sel, float* w, int32
   return launched() ? 0 : -1;
 }
 
-int moe_permute(const int32_t* sel, int n, int E, const int32_t* counts, int32_t* perm, int32_t* spos,
-                cudaStream_t st) {
-  if (n < 1 || E < 1) return -1;
-  moe_permute_kernel<<<E, 1024, 0, st>>>(sel, n, E, counts, perm, spos);
+int moe_segments(const int32_t* counts, int E, int n_blocks, int32_t* seg, int32_t* tile_e, cudaStream_t st) {
+  if (E < 1 || E > 1024 || n_blocks < 1) return -1;
+  moe_segments_kernel<<<1, 1024, 0, st>>>(counts, E, n_blocks, seg, tile_e);
   count_launches(1);
   return launched() ? 0 : -1;
 }
 
-int moe_gather(const uint16_t* m, const int32_t* perm, int n, int k, int h, uint16_t* xp, cudaStream_t st) {
+int moe_permute(const int32_t* sel, int n, int E, const int32_t* seg, int32_t* perm, int32_t* spos,
+                cudaStream_t st) {
+  if (n < 1 || E < 1) return -1;
+  moe_permute_kernel<<<E, 1024, 0, st>>>(sel, n, E, seg, perm, spos);
+  count_launches(1);
+  return launched() ? 0 : -1;
+}
+
+int moe_gather(const uint16_t* m, const int32_t* spos, int n, int k, int h, uint16_t* xp, cudaStream_t st) {
   if (n < 1 || h % 8) return -1;
-  moe_gather_kernel<<<n, std::min(256, h / 8), 0, st>>>(m, perm, k, h, xp);
+  moe_gather_kernel<<<n, std::min(256, h / 8), 0, st>>>(m, spos, k, h, xp);
   count_launches(1);
   return launched() ? 0 : -1;
 }

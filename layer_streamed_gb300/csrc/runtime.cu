@@ -233,7 +233,7 @@ bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
     if (c.n_experts < 8 || c.n_experts > 1024 || c.n_experts % 8)
       return fail("n_experts must be a multiple of 8 in [8, 1024]");
     if (c.top_k < 1 || c.top_k > 32 || c.top_k > c.n_experts) return fail("top_k must be in [1, min(32, n_experts)]");
-    if (c.expert_ffn < 8 || c.expert_ffn % 8) return fail("expert_ffn must be a positive multiple of 8");
+    if (c.expert_ffn < 32 || c.expert_ffn % 32) return fail("expert_ffn must be a positive multiple of 32");
     if (c.param_dtype != MT_BF16) return fail("mixture-of-experts layers need bf16 params");
   }
   if (c.hidden % 64) return fail("hidden must be a multiple of 64");
@@ -258,6 +258,7 @@ struct Plan {
   // dims
   int L, h, nq, nkv, d, F, Fp, V, qd, kd, qkv, Tmax;
   int E, topk, Fe;  // mixture-of-experts FFN when E > 0 (F = Fp = 0)
+  int n_pad;        // routed rows incl. padding of every expert segment to 128 rows
   size_t esz;
   // slicing of vocab-sized units
   int head_rows, n_head_slices;
@@ -267,7 +268,7 @@ struct Plan {
   size_t o_x, o_a, o_rstd1, o_qkv, o_o, o_lse, o_hmid, o_m, o_rstd2, o_gu, o_act;
   // mixture-of-experts slot: router logits, selection, weights, slot <-> row
   // maps, and the routed rows (grouped by expert) with their activations
-  size_t o_r, o_sel, o_w, o_spos, o_perm, o_xp, o_gup, o_actp, o_yp;
+  size_t o_r, o_sel, o_w, o_spos, o_perm, o_seg, o_tile_e, o_xp, o_gup, o_actp, o_yp;
 };
 
 size_t layer_cast_bytes(const Plan& p) {  // device bf16 view of one layer (fp32 params)
@@ -293,6 +294,7 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   p.E = c.n_experts;
   p.topk = c.top_k;
   p.Fe = c.expert_ffn;
+  p.n_pad = p.E ? (int)rup((size_t)p.Tmax * p.topk + (size_t)p.E * 127, 128) : 0;
   std::vector<std::vector<size_t>> o;
   build_layout(c, p.esz, &o);
   const size_t layer_bytes = (o[1][8] + tensor_numel(c, 1, 8) * p.esz) - o[1][0];
@@ -335,16 +337,18 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   p.o_gu = take(T * 2 * p.Fp * 2);
   p.o_act = take(T * p.Fp * 2);
   {
-    const size_t E = p.E, R = T * p.topk, Fe = p.Fe;  // all zero for dense layers
+    const size_t E = p.E, R = T * p.topk, Rp = p.n_pad, Fe = p.Fe;  // all zero for dense layers
     p.o_r = take(T * E * 4);
     p.o_sel = take(R * 4);
     p.o_w = take(R * 4);
     p.o_spos = take(R * 4);
-    p.o_perm = take(R * 4);
-    p.o_xp = take(R * h * 2);
-    p.o_gup = take(R * 2 * Fe * 2);
-    p.o_actp = take(R * Fe * 2);
-    p.o_yp = take(R * h * 4);
+    p.o_perm = take(Rp * 4);
+    p.o_seg = take((E + 1) * 4);
+    p.o_tile_e = take(Rp / 128 * 4);
+    p.o_xp = take(Rp * h * 2);
+    p.o_gup = take(Rp * 2 * Fe * 2);
+    p.o_actp = take(Rp * Fe * 2);
+    p.o_yp = take(Rp * h * 4);
   }
   p.act_layer = rup(a, 4096);
   // fixed workspace (see Ctx::carve)
@@ -370,7 +374,7 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   ws((size_t)c.max_seq * p.d / 2 * 8);             // rope table
   ws(2 * 2 * (size_t)p.h * 4);                     // gains of the two weight slots
   ws((size_t)p.h * 4 * 2);                         // final norm gain (raw + fp32)
-  ws(T * p.topk * (size_t)p.h * 2);                // MoE: d(routed outputs) bf16
+  ws((size_t)p.n_pad * p.h * 2);                   // MoE: d(routed outputs) bf16
   ws(T * p.topk * 4);                              // MoE: d(weights)
   ws(T * (size_t)p.E * 2);                         // MoE: d(router logits) bf16
   ws(((size_t)p.E + 1) * 4);                       // MoE: expert counts
@@ -439,13 +443,10 @@ struct mt_ctx {
   float2 *ce_part, *rope_tab;
   int32_t *tok_d, *lab_d, *perm_d, *ids_d, *ids_start_d;
   // mixture-of-experts: d(routed outputs), d(weights), d(router logits),
-  // expert counts, the routing of every layer; pinned copy of the counts and
-  // the counts behind each activation slot (the expert GEMMs are launched
-  // per expert from the host)
+  // expert counts, the routing of every layer
   uint16_t *moe_dyp = nullptr, *moe_dr = nullptr;
   float* moe_dw = nullptr;
-  int32_t *moe_counts = nullptr, *moe_route = nullptr, *moe_counts_host = nullptr;
-  std::vector<std::vector<int>> moe_slot_counts;
+  int32_t *moe_counts = nullptr, *moe_route = nullptr;
   const void* host_params_dev = nullptr;  // device-side address of the bound host parameters
   void* wf_raw;
   int32_t* host_stage = nullptr;  // pinned: tokens, labels, perm, used ids, id ranges, loss
@@ -540,7 +541,7 @@ int carve(mt_ctx* ctx) {
   ctx->gains[1] = (float*)take(2 * (size_t)p.h * 4);
   ctx->wf_raw = take((size_t)p.h * 4);
   ctx->wf32 = (float*)take((size_t)p.h * 4);
-  ctx->moe_dyp = (uint16_t*)take(T * p.topk * h * 2);
+  ctx->moe_dyp = (uint16_t*)take((size_t)p.n_pad * h * 2);
   ctx->moe_dw = (float*)take(T * p.topk * 4);
   ctx->moe_dr = (uint16_t*)take(T * (size_t)p.E * 2);
   ctx->moe_counts = (int32_t*)take(((size_t)p.E + 1) * 4);
@@ -605,7 +606,7 @@ struct ActSlot {
   uint16_t *a, *qkv, *o, *m, *gu, *act;
   // mixture-of-experts
   float *r, *w, *yp;
-  int32_t *sel, *spos, *perm;
+  int32_t *sel, *spos, *perm, *seg, *tile_e;
   uint16_t *xp, *gup, *actp;
 };
 
@@ -629,6 +630,8 @@ ActSlot act_slot(mt_ctx* ctx, int K, int nb, int j) {
   s.w = (float*)(base + p.o_w);
   s.spos = (int32_t*)(base + p.o_spos);
   s.perm = (int32_t*)(base + p.o_perm);
+  s.seg = (int32_t*)(base + p.o_seg);
+  s.tile_e = (int32_t*)(base + p.o_tile_e);
   s.xp = (uint16_t*)(base + p.o_xp);
   s.gup = (uint16_t*)(base + p.o_gup);
   s.actp = (uint16_t*)(base + p.o_actp);
@@ -859,10 +862,11 @@ double attn_flop(const Step& st, const Plan& p) {
 }
 
 // Mixture-of-experts FFN forward of layer l: router logits, top-k routing,
-// rows grouped by expert, one gated gate|up GEMM (SwiGLU in the epilogue) and
-// one down GEMM per expert over its block of rows, then the weighted combine
-// into the residual stream, y = h_mid + sum_j w_j y_j. The expert counts come
-// back to the host, which launches the expert GEMMs.
+// rows grouped by expert in segments of whole 128-row tiles, one grouped
+// gate|up GEMM for all experts (SwiGLU in the epilogue) and one grouped down
+// GEMM, then the weighted combine into the residual stream,
+// y = h_mid + sum_j w_j y_j. Everything stays on the device: the tile
+// schedule of the grouped GEMMs is read from the segment table.
 int moe_ffn_forward(Step& st, int l, const LayerView& w, const ActSlot& a, float* y) {
   mt_ctx* ctx = st.ctx;
   const Plan& p = ctx->P;
@@ -870,32 +874,30 @@ int moe_ffn_forward(Step& st, int l, const LayerView& w, const ActSlot& a, float
   cudaStream_t s = ctx->s_comp;
   CKR(gemm(ctx, GEMM_NT, EPI_F32, a.m, w.wr, a.r, nullptr, T, E, h, h, h, E));
   CKL(moe_route(a.r, T, E, k, a.sel, a.w, ctx->moe_counts, ctx->moe_route + (size_t)(l - 1) * T * k, s));
-  CKL(moe_permute(a.sel, n, E, ctx->moe_counts, a.perm, a.spos, s));
-  CKL(moe_gather(a.m, a.perm, n, k, h, a.xp, s));
-  CK(cudaMemcpyAsync(ctx->moe_counts_host, ctx->moe_counts, (size_t)E * 4, cudaMemcpyDeviceToHost, s));
-  CK(cudaStreamSynchronize(s));
-  std::vector<int>& cnt = ctx->moe_slot_counts[(l - 1) % st.K];
-  int total = 0;
-  for (int e = 0; e < E; ++e) {
-    cnt[e] = ctx->moe_counts_host[e];
-    total += cnt[e];
+  CKL(moe_segments(ctx->moe_counts, E, p.n_pad / 128, a.seg, a.tile_e, s));
+  CKL(moe_permute(a.sel, n, E, a.seg, a.perm, a.spos, s));
+  CK(cudaMemsetAsync(a.xp, 0, (size_t)p.n_pad * h * 2, s));  // padding rows are zero
+  CKL(moe_gather(a.m, a.spos, n, k, h, a.xp, s));
+  {
+    GemmParams gp{p.n_pad, Fe, h, EPI_BF16, a.gup, nullptr, 2 * Fe, 0, 1};
+    gp.gated = 1;
+    gp.u_off = Fe;
+    gp.u_col = Fe;
+    gp.act = a.actp;
+    gp.ld_act = Fe;
+    gp.grp_seg = a.seg;
+    gp.grp_tile_e = a.tile_e;
+    gp.grp_E = E;
+    gp.grp_b_rows = 2 * Fe;
+    CKR(gemm_p(ctx, GEMM_NT, gp, a.xp, w.wgu, h, h, 2.0 * n * 2 * Fe * h));
   }
-  if (total != n) return set_err(ctx, MT_ERR_CUDA, "expert counts do not add up (device error)");
-  size_t off = 0;
-  for (int e = 0; e < E; ++e) {
-    const int Me = cnt[e];
-    if (Me > 0) {
-      GemmParams gp{Me, Fe, h, EPI_BF16, a.gup + off * 2 * Fe, nullptr, 2 * Fe, 0, 1};
-      gp.gated = 1;
-      gp.u_off = Fe;
-      gp.u_col = Fe;
-      gp.act = a.actp + off * Fe;
-      gp.ld_act = Fe;
-      CKR(gemm_p(ctx, GEMM_NT, gp, a.xp + off * h, w.wgu + (size_t)e * 2 * Fe * h, h, h, 2.0 * Me * 2 * Fe * h));
-      CKR(gemm(ctx, GEMM_NT, EPI_F32, a.actp + off * Fe, w.wd + (size_t)e * h * Fe, a.yp + off * h, nullptr, Me, h,
-               Fe, Fe, Fe, h));
-    }
-    off += (size_t)Me;
+  {
+    GemmParams gp{p.n_pad, h, Fe, EPI_F32, a.yp, nullptr, h, 0, 1};
+    gp.grp_seg = a.seg;
+    gp.grp_tile_e = a.tile_e;
+    gp.grp_E = E;
+    gp.grp_b_rows = h;
+    CKR(gemm_p(ctx, GEMM_NT, gp, a.actp, w.wd, Fe, Fe, 2.0 * n * h * Fe));
   }
   CKL(moe_combine(a.hmid, a.yp, a.spos, a.w, T, k, h, y, s));
   return MT_OK;
@@ -989,41 +991,47 @@ int grad_slot_release(Step& st, int g) {
 
 // Mixture-of-experts FFN backward of layer l, from dh (the gradient of the
 // layer output) to ctx->dm (the gradient of the FFN input m); writes the
-// experts' and the router's gradients and sends them to the host.
+// experts' and the router's gradients and sends them to the host. The four
+// expert products are grouped launches over the segment table of the
+// forward (or recompute) that filled this activation slot.
 int moe_ffn_backward(Step& st, int l, const LayerView& w, const ActSlot& a, int g, float* g_router,
                      float* g_gu, float* g_down) {
   mt_ctx* ctx = st.ctx;
   const Plan& p = ctx->P;
-  const int T = st.T, h = p.h, E = p.E, k = p.topk, Fe = p.Fe;
+  const int T = st.T, h = p.h, E = p.E, k = p.topk, Fe = p.Fe, n = T * k;
   cudaStream_t s = ctx->s_comp;
-  const std::vector<int>& cnt = ctx->moe_slot_counts[(l - 1) % st.K];
+  CK(cudaMemsetAsync(ctx->moe_dyp, 0, (size_t)p.n_pad * h * 2, s));  // padding rows are zero
   CKL(moe_combine_bwd(ctx->dh, a.yp, a.spos, a.w, T, k, h, ctx->moe_dyp, ctx->moe_dw, s));
   float* dxp = a.yp;  // the routed outputs are consumed: their rows take d(routed inputs)
-  size_t off = 0;
-  for (int e = 0; e < E; ++e) {
-    const int Me = cnt[e];
-    float* gd = g_down + (size_t)e * h * Fe;
-    float* ggu = g_gu + (size_t)e * 2 * Fe * h;
-    if (Me == 0) {  // no rows routed to e: its gradients are zero
-      CK(cudaMemsetAsync(gd, 0, (size_t)h * Fe * 4, s));
-      CK(cudaMemsetAsync(ggu, 0, (size_t)2 * Fe * h * 4, s));
-      continue;
-    }
-    const uint16_t* dy = ctx->moe_dyp + off * h;
-    uint16_t* gu = a.gup + off * 2 * Fe;
-    // y_e = act Wd_e^T: dWd_e = dY^T act, dact = dY Wd_e -> (dg, du) in place over (g, u)
-    CKR(gemm(ctx, GEMM_TN, EPI_F32, dy, a.actp + off * Fe, gd, nullptr, h, Fe, Me, h, Fe, Fe));
-    GemmParams bp{Me, Fe, h, EPI_BF16, gu, nullptr, 2 * Fe, 0, 1};
+  auto grouped = [&](GemmParams& gp, bool tn, int b_rows) {
+    gp.grp_seg = a.seg;
+    gp.grp_tile_e = tn ? nullptr : a.tile_e;
+    gp.grp_E = E;
+    gp.grp_b_rows = b_rows;
+  };
+  {  // y_e = act Wd_e^T: dWd_e = dY_e^T act_e (each expert's [h, Fe])
+    GemmParams gp{h, Fe, p.n_pad, EPI_F32, g_down, nullptr, Fe, 0, 1};
+    grouped(gp, true, 0);
+    CKR(gemm_p(ctx, GEMM_TN, gp, ctx->moe_dyp, a.actp, h, Fe, 2.0 * n * h * Fe));
+  }
+  {  // dact = dY Wd_e, turned into (dg, du) in place over (g, u) by the epilogue
+    GemmParams bp{p.n_pad, Fe, h, EPI_BF16, a.gup, nullptr, 2 * Fe, 0, 1};
     bp.swiglu_bwd = 1;
-    bp.gu = gu;
+    bp.gu = a.gup;
     bp.ld_gu = 2 * Fe;
     bp.u_col = Fe;
-    CKR(gemm_p(ctx, GEMM_NN, bp, dy, w.wd + (size_t)e * h * Fe, h, Fe, 2.0 * Me * Fe * h));
-    // g|u = x Wgu_e^T: dWgu_e = d(g|u)^T x, dx = d(g|u) Wgu_e
-    CKR(gemm(ctx, GEMM_TN, EPI_F32, gu, a.xp + off * h, ggu, nullptr, 2 * Fe, h, Me, 2 * Fe, h, h));
-    CKR(gemm(ctx, GEMM_NN, EPI_F32, gu, w.wgu + (size_t)e * 2 * Fe * h, dxp + off * h, nullptr, Me, h, 2 * Fe,
-             2 * Fe, h, h));
-    off += (size_t)Me;
+    grouped(bp, false, h);
+    CKR(gemm_p(ctx, GEMM_NN, bp, ctx->moe_dyp, w.wd, h, Fe, 2.0 * n * Fe * h));
+  }
+  {  // g|u = x Wgu_e^T: dWgu_e = d(g|u)_e^T x_e (each expert's [2Fe, h])
+    GemmParams gp{2 * Fe, h, p.n_pad, EPI_F32, g_gu, nullptr, h, 0, 1};
+    grouped(gp, true, 0);
+    CKR(gemm_p(ctx, GEMM_TN, gp, a.gup, a.xp, 2 * Fe, h, 2.0 * n * 2 * Fe * h));
+  }
+  {  // dx = d(g|u) Wgu_e
+    GemmParams gp{p.n_pad, h, 2 * Fe, EPI_F32, dxp, nullptr, h, 0, 1};
+    grouped(gp, false, 2 * Fe);
+    CKR(gemm_p(ctx, GEMM_NN, gp, a.gup, w.wgu, 2 * Fe, h, 2.0 * n * 2 * Fe * h));
   }
   CKR(grad_piece(st, g, l, 7, 8));
   CKL(moe_unpermute(dxp, a.spos, T, k, h, ctx->dm, s));
@@ -1711,11 +1719,8 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
       (e = cudaHostAlloc((void**)&ctx->host_rows, (size_t)ctx->P.Tmax * ctx->P.h * ctx->P.esz, cudaHostAllocDefault)) !=
           cudaSuccess ||
       (e = cudaHostAlloc((void**)&ctx->host_grad_rows, (size_t)ctx->P.Tmax * ctx->P.h * 4, cudaHostAllocDefault)) !=
-          cudaSuccess ||
-      (e = cudaHostAlloc((void**)&ctx->moe_counts_host, ((size_t)ctx->P.E + 1) * 4, cudaHostAllocDefault)) !=
           cudaSuccess)
     return fail(MT_ERR_CUDA, "cudaHostAlloc", e);
-  ctx->moe_slot_counts.assign(std::max(1, cfg->max_K), std::vector<int>(ctx->P.E, 0));
   if (carve(ctx) != MT_OK) {
     mt_destroy(ctx);
     return MT_ERR_BUDGET;
@@ -1959,7 +1964,6 @@ void mt_destroy(mt_ctx* ctx) {
   if (ctx->host_stage) cudaFreeHost(ctx->host_stage);
   if (ctx->host_rows) cudaFreeHost(ctx->host_rows);
   if (ctx->host_grad_rows) cudaFreeHost(ctx->host_grad_rows);
-  if (ctx->moe_counts_host) cudaFreeHost(ctx->moe_counts_host);
   delete ctx;
 }
 
