@@ -109,3 +109,41 @@ def test_routing_query_errors():
         with pytest.raises(mt.MtError):
             s.routing(9)  # wrong size
         assert s.routing(8).shape == (cfg.n_layers, 8, cfg.top_k)
+
+
+def test_qwen3_moe_shape_full_batch_properties():
+    """Two layers of the Qwen3-235B-style MoE shape (hidden 4096, 64 q / 4 kv
+    heads x 128, 128 experts x 1536, top-8, vocab 151936) at the benchmark's
+    batch (B=1, S=4096: 32768 routed rows), in the step's own launch
+    configuration. Properties that hold at any size: every token routes to 8
+    distinct experts; K=2 and K=1 give bitwise-identical gradients and
+    routing; with W_out = 0 the loss is ln(V) and every gradient except the
+    head's is exactly zero (nothing flows back from the head)."""
+    import math
+    from tests.common import QWEN3_MOE
+    torch, mt = need_gpu()
+    cfg = with_layers(QWEN3_MOE, 2)
+    B, S = 1, 4096
+    tok, lab = make_tokens(cfg, B, S, 241)
+    with moe_session(mt, cfg, B, S, 2) as s:
+        s.params[:] = make_params(cfg, 242, bf16=True)
+        loss2 = s.step(tok, lab, 2)
+        g2 = s.grads.copy()
+        r2 = s.routing(B * S)
+        srt = np.sort(r2, axis=2)
+        assert np.all(srt[..., 1:] != srt[..., :-1]) and r2.min() >= 0 and r2.max() < cfg.n_experts
+        loss1 = s.step(tok, lab, 1)
+        assert loss1 == loss2
+        assert np.array_equal(s.grads.view(np.uint32), g2.view(np.uint32))
+        assert np.array_equal(s.routing(B * S), r2)
+        del g2
+        assert math.isfinite(loss2) and 0.5 * math.log(cfg.vocab) < loss2 < 2.0 * math.log(cfg.vocab)
+        off, nb = oracle.tensor_offset(cfg, cfg.n_layers + 1, 1, True)
+        s.params[off:off + nb] = 0
+        loss0 = s.step(tok, lab, 2)
+        assert abs(loss0 - math.log(cfg.vocab)) < 1e-4 * math.log(cfg.vocab)
+        goff, gnb = oracle.tensor_offset(cfg, cfg.n_layers + 1, 1, False)
+        g = s.grads
+        assert not np.any(g[:goff // 4] != 0) and not np.any(g[(goff + gnb) // 4:] != 0)
+        assert np.any(g[goff // 4:(goff + gnb) // 4] != 0)
+    assert mt.mt_op_device_error() == 0
