@@ -32,13 +32,17 @@ namespace {
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;  // 16 KB
+// fp32 epilogue staging: per epilogue warp 32 rows x 32 columns, row stride
+// 36 floats (conflict-free 16-byte accesses both ways)
+constexpr int kStgStride = 36;
+constexpr int kStagingBytes = 4 * 32 * kStgStride * 4;  // 18 KB
 
 template <int BN>
 struct GemmCfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int STAGES = (BN == 256) ? 4 : 6;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + kStagingBytes;
   static constexpr int TMEM_COLS = 2 * BN;
 };
 
@@ -279,10 +283,13 @@ __device__ __forceinline__ void swiglu_bwd_epilogue(const GemmParams& p, uint32_
 }
 
 // Epilogue of one output tile for one warp: TMEM lanes of `tb` hold row
-// `row`; columns [nb * BN, nb * BN + BN) of C (gated tiles: tile_n features).
+// `row` (the warp's rows are consecutive); columns [nb * BN, nb * BN + BN) of
+// C (gated tiles: tile_n features). fp32 results of whole 32-column chunks go
+// through the warp's staging rows `stg` so that each group of 8 lanes stores
+// 128 contiguous bytes of one row.
 template <int BN>
 __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tb, int row, bool row_ok, int nb,
-                                              int tile_n) {
+                                              int tile_n, float* stg) {
   if (p.rope_tab || p.gated || p.swiglu_bwd) {
     if (p.rope_tab) rope_epilogue<BN>(p, tb, row, row_ok, nb * BN);
     else if (p.gated) gated_epilogue<BN>(p, tb, row, row_ok, nb * tile_n);
@@ -296,8 +303,38 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tb, 
     tmem_ld32(tb + c * 32, r);
     tmem_ld_wait();
     const int col0 = nb * BN + c * 32;
+    const bool full_cols = p.vec && col0 + 32 <= p.N;  // the same in every lane
+    if (p.epi != EPI_BF16 && full_cols && p.stage_f32) {
+      const unsigned valid = __ballot_sync(0xffffffffu, row_ok);
+      const int lane = threadIdx.x & 31;
+      const int wrow0 = row - lane;
+      __syncwarp();
+      float* srow = stg + lane * kStgStride;
+#pragma unroll
+      for (int v = 0; v < 8; ++v)
+        ((float4*)srow)[v] = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
+                                         __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+      __syncwarp();
+      const int sub = lane >> 3, c4 = (lane & 7) * 4;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int rr = 4 * i + sub;
+        if ((valid >> rr) & 1u) {
+          float4 w = *(const float4*)(stg + rr * kStgStride + c4);
+          const size_t off = (size_t)(wrow0 + rr) * p.ldc + col0 + c4;
+          if (p.epi == EPI_F32_ADD) {
+            const float4 a = *(const float4*)((const float*)p.addend + off);
+            w.x += a.x;
+            w.y += a.y;
+            w.z += a.z;
+            w.w += a.w;
+          }
+          *(float4*)((float*)p.C + off) = w;
+        }
+      }
+      continue;
+    }
     if (!row_ok || col0 >= p.N) continue;
-    const bool full_cols = p.vec && col0 + 32 <= p.N;
     if (p.epi == EPI_BF16) {
       uint16_t* out = (uint16_t*)p.C + (size_t)row * p.ldc + col0;
       if (full_cols) {
@@ -352,6 +389,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tempty = tfull + 2;
   uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  float* staging = (float*)(smem + C::STAGES * C::STAGE_BYTES + 256);  // after the barriers
 
   const uint32_t warp = warp_id(), lane = lane_id();
   if (threadIdx.x == 0) {
@@ -474,7 +512,7 @@ __global__ void __launch_bounds__(192, 1)
         zero_tile_row<BN>(p, ti.crow + q * 32 + lane, r < p.M, ti.n0);
       } else {
         epilogue_tile<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, ti.crow + q * 32 + lane, r < p.M, ti.nb,
-                          tile_n);
+                          tile_n, staging + q * 32 * kStgStride);
       }
       tc_fence_before();
       __syncwarp();
@@ -507,7 +545,7 @@ struct PairCfg {
   static constexpr int B_BYTES = 128 * BK * 2;            // this CTA's half of B: 16 KB
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;  // 32 KB
   static constexpr int STAGES = 6;
-  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+  static constexpr int SMEM = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/ + kStagingBytes;
 };
 
 template <bool A_MN, bool B_MN>
@@ -525,6 +563,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tempty = tfull + 2;             // even CTA: both CTAs drained the accumulator
   uint32_t* tmem_slot = (uint32_t*)(tempty + 2);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
+  float* staging = (float*)(smem + C::STAGES * C::STAGE_BYTES + 256);  // after the barriers
 
   const uint32_t warp = warp_id(), lane = lane_id();
   const uint32_t rank = cluster_rank();
@@ -641,7 +680,8 @@ __global__ void __launch_bounds__(192, 1)
       mbar_wait<true>(&tfull[acc], acc_phase, abort_flag, kErrTimeoutEpi);
       tc_fence_after();
       const int row = mb * 2 * BM + (int)rank * BM + q * 32 + lane;
-      epilogue_tile<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, row, row < p.M, nb, tile_n);
+      epilogue_tile<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, row, row < p.M, nb, tile_n,
+                        staging + q * 32 * kStgStride);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(tempty0 + acc * 8);
@@ -756,6 +796,9 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
   }
   if (p.gated && (mode != GEMM_NT || !p.act || (p.ld_act & 7) || (p.u_col & 7) || p.epi != EPI_BF16)) return -1;
   const bool grouped = p.grp_seg != nullptr;
+  // Staged fp32 stores pay off where a tile's reduction is short (grouped
+  // weight gradients: one expert's rows); long reductions hide the epilogue.
+  p.stage_f32 = (p.epi != EPI_BF16 && (grouped || p.K <= 1024)) ? 1 : 0;
   if (grouped) {
     if (p.grp_E < 1 || p.rope_tab) return -1;
     if (mode == GEMM_TN) {

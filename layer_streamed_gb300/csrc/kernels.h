@@ -53,6 +53,10 @@ struct GemmParams {
   const int* grp_seg = nullptr;
   const int* grp_tile_e = nullptr;
   int grp_E = 0, grp_b_rows = 0;
+  // set by gemm_bf16: fp32 results go through shared memory so that stores
+  // are whole 128-byte row segments (when the epilogue, not the mainloop,
+  // bounds the tile: short reductions)
+  int stage_f32 = 0;
 };
 
 // C[M,N] = op(A) op(B) with bf16 operands, fp32 accumulation (see gemm.cu).
