@@ -369,6 +369,8 @@ def main():
                     help="time train steps with the host AdamW: sync = mt_train_step (each unit updated as its "
                          "gradients land), async = mt_train_step_async (staleness 1); allocates three fp32 copies "
                          "of the model on the host, so use it with --layers at the 8B widths")
+    ap.add_argument("--grad-dtype", default="fp32", choices=["fp32", "bf16"],
+                    help="dtype of the streamed host gradients (bf16 halves the D2H bytes)")
     ap.add_argument("--layers", type=int, default=None, help="diagnostic override of the layer count")
     ap.add_argument("--seq", type=int, default=None, help="diagnostic override of the sequence length")
     ap.add_argument("--batch", type=int, default=None, help="diagnostic override of the batch")
@@ -407,14 +409,18 @@ def main():
     moe = MOE.get(args.workload)
     E, k_top, Fe = moe or (0, 0, 0)
     eps = NORM_EPS.get(args.workload, 1e-5)
-    cfg = mt.make_cfg(L, h, nq, nkv, d, F, V, theta, eps, B, S, K, mt.MT_BF16 if bf16 else mt.MT_F32, E, k_top, Fe)
+    grad_dtype = mt.MT_BF16 if args.grad_dtype == "bf16" else mt.MT_F32
+    if args.optimizer and grad_dtype != mt.MT_F32:
+        sys.exit("the host optimizer takes fp32 gradients")
+    cfg = mt.make_cfg(L, h, nq, nkv, d, F, V, theta, eps, B, S, K, mt.MT_BF16 if bf16 else mt.MT_F32, E, k_top, Fe,
+                      grad_dtype)
     budget = mt.mt_required_budget(cfg)
     log(f"workload {args.workload} L={L} B={B} S={S} K={K}: device arena {budget / 2**30:.2f} GiB")
     arena = torch.empty(budget, dtype=torch.uint8, device="cuda")
     streams = [torch.cuda.Stream() for _ in range(3)]
     sess = mt.Session(mt.ModelShape(L, h, nq, nkv, d, F, V, theta, eps, E, k_top, Fe), B, S, K,
                       mt.MT_BF16 if bf16 else mt.MT_F32, device_budget=budget, device_arena=arena.data_ptr(),
-                      streams=[s.cuda_stream for s in streams])
+                      streams=[s.cuda_stream for s in streams], grad_dtype=grad_dtype)
     # Parameters: N(0, 0.02) matrices, unit RMSNorm gains, per-rank seed.
     offs = []
     for unit in range(L + 2):
@@ -508,8 +514,9 @@ def main():
     per_step_h2d = agg["h2d_bytes"] / steps
     per_step_d2h = agg["d2h_bytes"] / steps
     layer_h2d = per_step_h2d * (L * P_bytes * 2) / max(1.0, (L * P_bytes * 2 + 2 * V * h * 2)) / L
-    t_layer = max(layer_f / (peak_tf * 1e12), layer_h2d / h2d_bw, 4.0 * (P_bytes + 2 * h) / d2h_bw)
-    t_head = max(head_f / (peak_tf * 1e12), (per_step_h2d - L * layer_h2d) / h2d_bw, (2.0 * V * h * 4) / d2h_bw)
+    gsz = 2.0 if args.grad_dtype == "bf16" else 4.0  # bytes per streamed gradient element
+    t_layer = max(layer_f / (peak_tf * 1e12), layer_h2d / h2d_bw, gsz * (P_bytes + 2 * h) / d2h_bw)
+    t_head = max(head_f / (peak_tf * 1e12), (per_step_h2d - L * layer_h2d) / h2d_bw, (2.0 * V * h * gsz) / d2h_bw)
     t_roof = L * t_layer + t_head
     ms_per_step = dev_ms / steps
     rows = head_slice_rows(shape, 2 if bf16 else 4, moe)
@@ -535,7 +542,8 @@ def main():
         "data": "synthetic",
         "config": {"workload": args.workload, "global_batch": B * world, "seq_len": S, "checkpoint_every": K,
                    "layers": L, "hidden": h, "heads": f"{nq}q/{nkv}kv x {d}", "ffn": F, "vocab": V,
-                   "host_params": "bf16" if bf16 else "fp32", "parallelism": f"replicas x{world}",
+                   "host_params": "bf16" if bf16 else "fp32", "host_grads": args.grad_dtype,
+                   "parallelism": f"replicas x{world}",
                    **({"experts": f"{E} x SwiGLU {Fe}, top-{k_top}, softmax router"} if moe else {}),
                    "l2": "inputs larger than L2 (every step streams all weights from host)",
                    "optimizer_step": f"host AdamW included ({args.optimizer})" if args.optimizer else "none (fwd+bwd)"},

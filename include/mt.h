@@ -76,6 +76,11 @@ typedef struct {
   int32_t max_batch, max_seq, max_K;
   int32_t param_dtype; /* mt_dtype */
   int32_t n_experts, top_k, expert_ffn;
+  /* dtype of the host gradient buffer (same packed layout with that element
+   * size): MT_F32 (0, the default) or MT_BF16 (gradients rounded to nearest
+   * even on the device before they stream back: half the D2H bytes; the host
+   * optimizer entry points take MT_F32 gradients only). */
+  int32_t grad_dtype;
 } mt_layer_cfg;
 
 typedef struct mt_ctx mt_ctx;
@@ -93,7 +98,7 @@ typedef struct mt_ctx mt_ctx;
  *  unit L+1      : 0 w_final_norm[h], 1 W_out[vocab, h]
  * Matrices are row-major [out, in] (y = x W^T). Every tensor starts on a
  * 256-byte boundary, every unit on a 4096-byte boundary. The gradient buffer
- * uses the same layout with fp32 elements. */
+ * uses the same layout with grad_dtype elements (fp32 by default). */
 size_t mt_packed_bytes(const mt_layer_cfg* cfg, mt_dtype dtype);
 
 /* Byte offset and byte size of tensor `tensor` of unit `unit` in the packed
@@ -130,7 +135,8 @@ int mt_bind_host_params(mt_ctx* ctx, const void* host_params, mt_dtype dtype);
  *  B, S           : 1 <= B*S, B <= max_batch, S <= max_seq
  *  K              : checkpoint interval, 1 <= K <= min(n_layers, max_K); n_layers % K
  *                   may be nonzero (the top block is then partial)
- *  host_grad_out  : pinned host fp32 buffer, mt_packed_bytes(cfg, MT_F32) bytes,
+ *  host_grad_out  : pinned host buffer of grad_dtype elements (fp32 by default),
+ *                   mt_packed_bytes(cfg, grad_dtype) bytes,
  *                   4096-byte aligned; OVERWRITTEN with dLoss/dtheta in the
  *                   packed layout (embedding rows of unused tokens are 0; the
  *                   padding bytes between tensors are written as 0)

@@ -60,7 +60,7 @@ class mt_layer_cfg(ctypes.Structure):
                 ("vocab", ctypes.c_int32), ("rope_theta", ctypes.c_float), ("norm_eps", ctypes.c_float),
                 ("max_batch", ctypes.c_int32), ("max_seq", ctypes.c_int32), ("max_K", ctypes.c_int32),
                 ("param_dtype", ctypes.c_int32), ("n_experts", ctypes.c_int32), ("top_k", ctypes.c_int32),
-                ("expert_ffn", ctypes.c_int32)]
+                ("expert_ffn", ctypes.c_int32), ("grad_dtype", ctypes.c_int32)]
 
 
 class mt_stats(ctypes.Structure):
@@ -169,9 +169,9 @@ def _check(rc: int, ctx=None):
 # ---------------------------------------------------------------------------
 def make_cfg(n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, rope_theta=1e4, norm_eps=1e-5,
              max_batch=1, max_seq=1, max_K=1, param_dtype=MT_F32, n_experts=0, top_k=0,
-             expert_ffn=0) -> mt_layer_cfg:
+             expert_ffn=0, grad_dtype=MT_F32) -> mt_layer_cfg:
     return mt_layer_cfg(n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab, rope_theta, norm_eps,
-                        max_batch, max_seq, max_K, param_dtype, n_experts, top_k, expert_ffn)
+                        max_batch, max_seq, max_K, param_dtype, n_experts, top_k, expert_ffn, grad_dtype)
 
 
 def mt_packed_bytes(cfg: mt_layer_cfg, dtype: int) -> int:
@@ -335,10 +335,13 @@ class Session:
     """
 
     def __init__(self, shape: ModelShape, max_batch: int, max_seq: int, max_K: int, param_dtype: int = MT_F32,
-                 device_budget: int | None = None, device_arena: int | None = None, streams=None):
+                 device_budget: int | None = None, device_arena: int | None = None, streams=None,
+                 grad_dtype: int = MT_F32):
         self.cfg = make_cfg(shape.n_layers, shape.hidden, shape.n_heads, shape.n_kv_heads, shape.head_dim,
                             shape.ffn_dim, shape.vocab, shape.rope_theta, shape.norm_eps, max_batch, max_seq,
-                            max_K, param_dtype, shape.n_experts, shape.top_k, shape.expert_ffn)
+                            max_K, param_dtype, shape.n_experts, shape.top_k, shape.expert_ffn, grad_dtype)
+        self.grad_dtype = grad_dtype
+        self._gnp = np.float32 if grad_dtype == MT_F32 else np.uint16  # bf16 gradients as bit patterns
         self.shape = shape
         self.param_dtype = param_dtype
         need = mt_required_budget(self.cfg)
@@ -352,11 +355,11 @@ class Session:
         else:
             self.ctx = mt_create(self.cfg, self.budget)
         self.param_bytes = mt_packed_bytes(self.cfg, param_dtype)
-        self.grad_bytes = mt_packed_bytes(self.cfg, MT_F32)
+        self.grad_bytes = mt_packed_bytes(self.cfg, grad_dtype)
         self._pp = mt_host_alloc(self.param_bytes)
         self._gp = mt_host_alloc(self.grad_bytes)
         self.params = host_array(self._pp, self.param_bytes)
-        self.grads = host_array(self._gp, self.grad_bytes, np.float32)
+        self.grads = host_array(self._gp, self.grad_bytes, self._gnp)
         mt_bind_host_params(self.ctx, self._pp, param_dtype)
 
     @property
@@ -377,7 +380,7 @@ class Session:
         """Attach AdamW state: `master` is the fp32 packed copy of the
         parameters (mt_packed_bytes(cfg, MT_F32) bytes as float32); the
         moments start at zero. The arrays are kept by the session."""
-        n = self.grad_bytes // 4
+        n = mt_packed_bytes(self.cfg, MT_F32) // 4
         self.opt_master = np.ascontiguousarray(master, dtype=np.float32).reshape(-1).copy()
         if self.opt_master.size != n:
             raise MtError(MT_ERR_ARG, "master copy has the wrong size")
@@ -399,7 +402,7 @@ class Session:
         ptr = self._gbufs[self._gturn]
         self._gturn ^= 1
         loss = mt_train_step_async(self.ctx, tokens, labels, K, ptr)
-        self.grads = host_array(ptr, self.grad_bytes, np.float32)
+        self.grads = host_array(ptr, self.grad_bytes, self._gnp)
         return loss
 
     def optimizer_flush(self) -> None:

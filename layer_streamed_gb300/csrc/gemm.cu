@@ -109,13 +109,18 @@ __device__ __forceinline__ TileInfo decode_tile(const GemmParams& p, int tile, i
   return t;
 }
 
-// Zeros over columns [n0, n0 + BN) of fp32 row `row` (an expert that
-// received no rows: its weight gradient is zero).
+// Zeros over columns [n0, n0 + BN) of row `row` (an expert that received
+// no rows: its weight gradient is zero).
 template <int BN>
 __device__ __forceinline__ void zero_tile_row(const GemmParams& p, int row, bool row_ok, int n0) {
   if (!row_ok) return;
-  float* out = (float*)p.C + (size_t)row * p.ldc;
-  for (int j = n0; j < n0 + BN && j < p.N; ++j) out[j] = 0.f;
+  if (p.epi == EPI_BF16) {
+    uint16_t* out = (uint16_t*)p.C + (size_t)row * p.ldc;
+    for (int j = n0; j < n0 + BN && j < p.N; ++j) out[j] = 0;
+  } else {
+    float* out = (float*)p.C + (size_t)row * p.ldc;
+    for (int j = n0; j < n0 + BN && j < p.N; ++j) out[j] = 0.f;
+  }
 }
 
 // Store 32 fp32 values as bf16 at columns [col0, col0+32) of a row (partial
@@ -802,7 +807,7 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
   if (grouped) {
     if (p.grp_E < 1 || p.rope_tab) return -1;
     if (mode == GEMM_TN) {
-      if (p.gated || p.swiglu_bwd || p.epi != EPI_F32 || (p.K % BM)) return -1;
+      if (p.gated || p.swiglu_bwd || p.epi == EPI_F32_ADD || (p.K % BM)) return -1;
     } else if (!p.grp_tile_e || p.grp_b_rows < 1 || (p.M % BM)) {
       return -1;
     }

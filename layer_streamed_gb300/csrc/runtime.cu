@@ -242,6 +242,7 @@ bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
   if (c.head_dim != 16 && c.head_dim != 32 && c.head_dim != 64 && c.head_dim != 128)
     return fail("head_dim must be 16, 32, 64 or 128");
   if (c.param_dtype != MT_F32 && c.param_dtype != MT_BF16) return fail("param_dtype must be MT_F32 or MT_BF16");
+  if (c.grad_dtype != MT_F32 && c.grad_dtype != MT_BF16) return fail("grad_dtype must be MT_F32 or MT_BF16");
   if (c.param_dtype == MT_BF16 && c.ffn_dim % 8) return fail("bf16 params need ffn_dim % 8 == 0");
   if (c.max_batch < 1 || c.max_seq < 1 || c.max_K < 1) return fail("max_batch, max_seq, max_K must be >= 1");
   if (!(c.rope_theta > 0.f) || !(c.norm_eps > 0.f)) return fail("rope_theta and norm_eps must be positive");
@@ -260,6 +261,8 @@ struct Plan {
   int E, topk, Fe;  // mixture-of-experts FFN when E > 0 (F = Fp = 0)
   int n_pad;        // routed rows incl. padding of every expert segment to 128 rows
   size_t esz;
+  size_t gesz;  // element size of the streamed gradients (4: fp32, 2: bf16)
+  int gepi;     // GEMM epilogue that writes a weight gradient
   // slicing of vocab-sized units
   int head_rows, n_head_slices;
   // sizes
@@ -291,6 +294,8 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   p.qkv = p.qd + 2 * p.kd;
   p.Tmax = c.max_batch * c.max_seq;
   p.esz = c.param_dtype == MT_BF16 ? 2 : 4;
+  p.gesz = c.grad_dtype == MT_BF16 ? 2 : 4;
+  p.gepi = p.gesz == 2 ? EPI_BF16 : EPI_F32;
   p.E = c.n_experts;
   p.topk = c.top_k;
   p.Fe = c.expert_ffn;
@@ -313,10 +318,12 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
     }
   };
   slices((size_t)p.h * p.esz, layer_bytes, &p.head_rows, &p.n_head_slices);
-  const size_t layer_grad_bytes = layer_bytes / p.esz * 4;
+  std::vector<std::vector<size_t>> og;
+  build_layout(c, p.gesz, &og);
+  const size_t layer_grad_bytes = (og[1][8] + tensor_numel(c, 1, 8) * p.gesz) - og[1][0];
   p.wbuf = rup(std::max(layer_bytes, (size_t)p.head_rows * p.h * p.esz), 4096);
   p.wcast = p.esz == 4 ? rup(std::max(layer_cast_bytes(p), (size_t)p.head_rows * p.h * 2), 4096) : 0;
-  p.gbuf = rup(std::max({layer_grad_bytes, (size_t)p.head_rows * p.h * 4, (size_t)p.h * 4}), 4096);
+  p.gbuf = rup(std::max({layer_grad_bytes, (size_t)p.head_rows * p.h * p.gesz, (size_t)p.h * p.gesz}), 4096);
   const size_t T = p.Tmax, h = p.h;
   p.ckpt_one = rup(T * h * 4, 256);
   size_t a = 0;
@@ -378,6 +385,7 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   ws(T * p.topk * 4);                              // MoE: d(weights)
   ws(T * (size_t)p.E * 2);                         // MoE: d(router logits) bf16
   ws(((size_t)p.E + 1) * 4);                       // MoE: expert counts
+  ws((size_t)p.h * 4);                             // a gain gradient before its bf16 rounding
   ws((size_t)p.L * T * p.topk * 4);                // MoE: routing of every layer
   p.fixed_ws = w;
   // dynamic part: checkpoints for ceil(L/K) blocks + K activation slots
@@ -416,7 +424,7 @@ struct OpSeg {
 struct mt_ctx {
   mt_layer_cfg cfg;
   Plan P;
-  std::vector<std::vector<size_t>> off_p, off_g;  // host param layout, fp32 grad layout
+  std::vector<std::vector<size_t>> off_p, off_g;  // host param layout, host gradient layout (grad_dtype)
   int device = 0;
   cudaStream_t s_comp = nullptr, s_h2d = nullptr, s_d2h = nullptr;
   bool own_streams = false;
@@ -447,6 +455,7 @@ struct mt_ctx {
   uint16_t *moe_dyp = nullptr, *moe_dr = nullptr;
   float* moe_dw = nullptr;
   int32_t *moe_counts = nullptr, *moe_route = nullptr;
+  float* gain_grad = nullptr;  // bf16 gradients: an RMSNorm gain's fp32 gradient before rounding
   const void* host_params_dev = nullptr;  // device-side address of the bound host parameters
   void* wf_raw;
   int32_t* host_stage = nullptr;  // pinned: tokens, labels, perm, used ids, id ranges, loss
@@ -545,6 +554,7 @@ int carve(mt_ctx* ctx) {
   ctx->moe_dw = (float*)take(T * p.topk * 4);
   ctx->moe_dr = (uint16_t*)take(T * (size_t)p.E * 2);
   ctx->moe_counts = (int32_t*)take(((size_t)p.E + 1) * 4);
+  ctx->gain_grad = (float*)take((size_t)p.h * 4);
   ctx->moe_route = (int32_t*)take((size_t)p.L * T * p.topk * 4);
   ctx->dyn = cur;
   cur += p.dyn_max;
@@ -970,10 +980,11 @@ int grad_piece(Step& st, int g, int l, int t0, int t1) {
   if (!ready) return set_err(ctx, MT_ERR_CUDA, "event pool");
   CK(cudaEventRecord(ready, ctx->s_comp));
   CK(cudaStreamWaitEvent(ctx->s_d2h, ready, 0));
-  const size_t span = ctx->off_g[l][t1] + tensor_numel(ctx->cfg, l, t1) * 4 - ctx->off_g[l][t0];
+  const size_t gesz = ctx->P.gesz;
+  const size_t span = ctx->off_g[l][t1] + tensor_numel(ctx->cfg, l, t1) * gesz - ctx->off_g[l][t0];
   SegScope sg(ctx, 2, ctx->s_d2h, (double)span);
   for (int t = t0; t <= t1; ++t) {
-    const size_t off = ctx->off_g[l][t], nb = tensor_numel(ctx->cfg, l, t) * 4;
+    const size_t off = ctx->off_g[l][t], nb = tensor_numel(ctx->cfg, l, t) * gesz;
     CK(cudaMemcpyAsync((uint8_t*)st.host_grad + off, (const uint8_t*)ctx->gbuf[g] + (off - u0), nb,
                        cudaMemcpyDeviceToHost, ctx->s_d2h));
     ctx->stats.d2h_bytes += (double)nb;
@@ -1010,7 +1021,7 @@ int moe_ffn_backward(Step& st, int l, const LayerView& w, const ActSlot& a, int 
     gp.grp_b_rows = b_rows;
   };
   {  // y_e = act Wd_e^T: dWd_e = dY_e^T act_e (each expert's [h, Fe])
-    GemmParams gp{h, Fe, p.n_pad, EPI_F32, g_down, nullptr, Fe, 0, 1};
+    GemmParams gp{h, Fe, p.n_pad, p.gepi, g_down, nullptr, Fe, 0, 1};
     grouped(gp, true, 0);
     CKR(gemm_p(ctx, GEMM_TN, gp, ctx->moe_dyp, a.actp, h, Fe, 2.0 * n * h * Fe));
   }
@@ -1024,7 +1035,7 @@ int moe_ffn_backward(Step& st, int l, const LayerView& w, const ActSlot& a, int 
     CKR(gemm_p(ctx, GEMM_NN, bp, ctx->moe_dyp, w.wd, h, Fe, 2.0 * n * Fe * h));
   }
   {  // g|u = x Wgu_e^T: dWgu_e = d(g|u)_e^T x_e (each expert's [2Fe, h])
-    GemmParams gp{2 * Fe, h, p.n_pad, EPI_F32, g_gu, nullptr, h, 0, 1};
+    GemmParams gp{2 * Fe, h, p.n_pad, p.gepi, g_gu, nullptr, h, 0, 1};
     grouped(gp, true, 0);
     CKR(gemm_p(ctx, GEMM_TN, gp, a.gup, a.xp, 2 * Fe, h, 2.0 * n * 2 * Fe * h));
   }
@@ -1038,7 +1049,7 @@ int moe_ffn_backward(Step& st, int l, const LayerView& w, const ActSlot& a, int 
   // router: dr, then dm += dr Wr and dWr = dr^T m
   CKL(moe_router_bwd(a.w, ctx->moe_dw, a.sel, T, k, E, ctx->moe_dr, s));
   CKR(gemm(ctx, GEMM_NN, EPI_F32_ADD, ctx->moe_dr, w.wr, ctx->dm, ctx->dm, T, h, E, E, h, h));
-  CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->moe_dr, a.m, g_router, nullptr, E, h, T, E, h, h));
+  CKR(gemm(ctx, GEMM_TN, p.gepi, ctx->moe_dr, a.m, g_router, nullptr, E, h, T, E, h, h));
   return grad_piece(st, g, l, 6, 6);
 }
 
@@ -1054,6 +1065,13 @@ int layer_backward(Step& st, int l, const LayerView& w) {
   float* G = ctx->gbuf[g];
   const size_t u0 = ctx->off_g[l][0];
   auto GT = [&](int t) { return (float*)((uint8_t*)G + (ctx->off_g[l][t] - u0)); };
+  // RMSNorm gain gradients come out in fp32; with bf16 gradients they are
+  // rounded into the staging buffer afterwards.
+  auto GGAIN = [&](int t) { return p.gesz == 2 ? ctx->gain_grad : GT(t); };
+  auto gain_grad_out = [&](int t) -> int {
+    if (p.gesz == 2) CKL(cast_f32_bf16(ctx->gain_grad, (uint16_t*)GT(t), (size_t)h, s));
+    return MT_OK;
+  };
   // Gradient tensors go to the host in four groups, each as soon as it is
   // complete: [Wd], [Wg Wu], [Wo w_ffn], [w_attn Wq Wk Wv] (mixture of
   // experts: [experts' Wgu Wd], [router], then the same two).
@@ -1061,7 +1079,7 @@ int layer_backward(Step& st, int l, const LayerView& w) {
     CKR(moe_ffn_backward(st, l, w, a, g, GT(6), GT(7), GT(8)));
   } else {
     // h_out = h_mid + act Wd^T
-    CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dh_b, a.act, GT(8), nullptr, h, F, T, h, Fp, F));
+    CKR(gemm(ctx, GEMM_TN, p.gepi, ctx->dh_b, a.act, GT(8), nullptr, h, F, T, h, Fp, F));
     CKR(grad_piece(st, g, l, 8, 8));
     {  // dact = dh Wd, turned into (dg, du) in place over (g, u) by the epilogue
       GemmParams bp{T, Fp, h, EPI_BF16, a.gu, nullptr, 2 * Fp, 0, 1};
@@ -1072,18 +1090,19 @@ int layer_backward(Step& st, int l, const LayerView& w) {
       CKR(gemm_p(ctx, GEMM_NN, bp, ctx->dh_b, w.wd, h, w.ldd, 2.0 * T * Fp * h));
     }
     if (Fp == F) {
-      CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, 2 * F, h, T, 2 * Fp, h, h));
+      CKR(gemm(ctx, GEMM_TN, p.gepi, a.gu, a.m, GT(6), nullptr, 2 * F, h, T, 2 * Fp, h, h));
     } else {
-      CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu, a.m, GT(6), nullptr, F, h, T, 2 * Fp, h, h));
-      CKR(gemm(ctx, GEMM_TN, EPI_F32, a.gu + Fp, a.m, GT(7), nullptr, F, h, T, 2 * Fp, h, h));
+      CKR(gemm(ctx, GEMM_TN, p.gepi, a.gu, a.m, GT(6), nullptr, F, h, T, 2 * Fp, h, h));
+      CKR(gemm(ctx, GEMM_TN, p.gepi, a.gu + Fp, a.m, GT(7), nullptr, F, h, T, 2 * Fp, h, h));
     }
     CKR(grad_piece(st, g, l, 6, 7));
     CKR(gemm(ctx, GEMM_NN, EPI_F32, a.gu, w.wgu, ctx->dm, nullptr, T, h, 2 * Fp, 2 * Fp, h, h));
   }
   // RMSNorm 2 (+ residual): dh_mid written over h_mid (row-local, in place)
-  CKL(rmsnorm_bwd(a.hmid, w.w2, a.rstd2, ctx->dm, ctx->dh, a.hmid, ctx->dhmid_b, GT(5), ctx->norm_ws, T, h, s));
+  CKL(rmsnorm_bwd(a.hmid, w.w2, a.rstd2, ctx->dm, ctx->dh, a.hmid, ctx->dhmid_b, GGAIN(5), ctx->norm_ws, T, h, s));
+  CKR(gain_grad_out(5));
   // h_mid = x + o Wo^T
-  CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dhmid_b, a.o, GT(4), nullptr, h, p.qd, T, h, p.qd, p.qd));
+  CKR(gemm(ctx, GEMM_TN, p.gepi, ctx->dhmid_b, a.o, GT(4), nullptr, h, p.qd, T, h, p.qd, p.qd));
   CKR(grad_piece(st, g, l, 4, 5));
   CKR(gemm(ctx, GEMM_NN, EPI_BF16, ctx->dhmid_b, w.wo, ctx->do_b, nullptr, T, p.qd, h, h, p.qd, p.qd));
   {
@@ -1093,10 +1112,11 @@ int layer_backward(Step& st, int l, const LayerView& w) {
                       ctx->dqkv + p.qd, ctx->dqkv + p.qd + p.kd, ctx->attn_ws, st.B, st.S, p.nq, p.nkv, p.d, p.qkv,
                       p.qkv, p.qd, s, ctx->rope_tab));
   }
-  CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dqkv, a.a, GT(1), nullptr, p.qkv, h, T, p.qkv, h, h));
+  CKR(gemm(ctx, GEMM_TN, p.gepi, ctx->dqkv, a.a, GT(1), nullptr, p.qkv, h, T, p.qkv, h, h));
   CKR(gemm(ctx, GEMM_NN, EPI_F32, ctx->dqkv, w.wqkv, ctx->dm, nullptr, T, h, p.qkv, p.qkv, h, h));
   // RMSNorm 1 (+ residual): new dh
-  CKL(rmsnorm_bwd(x, w.w1, a.rstd1, ctx->dm, a.hmid, ctx->dh, ctx->dh_b, GT(0), ctx->norm_ws, T, h, s));
+  CKL(rmsnorm_bwd(x, w.w1, a.rstd1, ctx->dm, a.hmid, ctx->dh, ctx->dh_b, GGAIN(0), ctx->norm_ws, T, h, s));
+  CKR(gain_grad_out(0));
   CKR(grad_piece(st, g, l, 0, 3));
   if (st.train || st.async) {
     st.landed[l] = next_event(ctx);
@@ -1151,14 +1171,14 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       for (int t = 0; t < tensors_in_unit(ctx->cfg, u); ++t) {
         const size_t off = ctx->off_g[u][t];
         if (off > pos) std::memset(gb + pos, 0, off - pos);
-        pos = off + tensor_numel(ctx->cfg, u, t) * 4;
+        pos = off + tensor_numel(ctx->cfg, u, t) * p.gesz;
       }
-    const size_t total = build_layout(ctx->cfg, 4, nullptr);
+    const size_t total = build_layout(ctx->cfg, p.gesz, nullptr);
     if (total > pos) std::memset(gb + pos, 0, total - pos);
   }
   auto start_zeroers = [&] {
     uint8_t* eg = (uint8_t*)st.host_grad + ctx->off_g[0][0];
-    const size_t nbytes = (size_t)p.V * h * 4;
+    const size_t nbytes = (size_t)p.V * h * p.gesz;
     const unsigned hw = std::max(1u, std::thread::hardware_concurrency());
     const size_t nthr = std::min<size_t>(std::max(1u, hw / 2), std::max<size_t>(1, nbytes >> 26));
     const size_t chunk = (nbytes / nthr + 4095) & ~(size_t)4095;
@@ -1353,14 +1373,15 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
           first_dxf = false;
           int g;
           CKR(grad_slot_begin(st, &g));
-          CKR(gemm(ctx, GEMM_TN, EPI_F32, ctx->dz, ctx->xf_b, ctx->gbuf[g], nullptr, rows, h, T, p.head_rows, h, h));
-          CKR(grad_slot_end(st, g, ctx->off_g[L + 1][1] + (size_t)r0 * h * 4, (size_t)rows * h * 4));
+          CKR(gemm(ctx, GEMM_TN, p.gepi, ctx->dz, ctx->xf_b, ctx->gbuf[g], nullptr, rows, h, T, p.head_rows, h, h));
+          CKR(grad_slot_end(st, g, ctx->off_g[L + 1][1] + (size_t)r0 * h * p.gesz, (size_t)rows * h * p.gesz));
           if (++head_pass2_count == p.n_head_slices) {
             // final norm backward -> dh_L, and its gain gradient
             CKR(grad_slot_begin(st, &g));
-            CKL(rmsnorm_bwd(ctx->h_top, ctx->wf32, ctx->rstd_f, ctx->dm, nullptr, ctx->dh, ctx->dh_b, ctx->gbuf[g],
-                            ctx->norm_ws, T, h, s));
-            CKR(grad_slot_end(st, g, ctx->off_g[L + 1][0], (size_t)h * 4));
+            CKL(rmsnorm_bwd(ctx->h_top, ctx->wf32, ctx->rstd_f, ctx->dm, nullptr, ctx->dh, ctx->dh_b,
+                            p.gesz == 2 ? ctx->gain_grad : ctx->gbuf[g], ctx->norm_ws, T, h, s));
+            if (p.gesz == 2) CKL(cast_f32_bf16(ctx->gain_grad, (uint16_t*)ctx->gbuf[g], (size_t)h, s));
+            CKR(grad_slot_end(st, g, ctx->off_g[L + 1][0], (size_t)h * p.gesz));
             if (st.train || st.async) {
               st.landed[L + 1] = next_event(ctx);
               if (!st.landed[L + 1]) return set_err(ctx, MT_ERR_CUDA, "event pool");
@@ -1497,8 +1518,9 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   // Scatter the embedding gradient rows into the (now cleared) host buffer.
   for (auto& x : zeroers) x.join();
   {
-    float* eg = (float*)((uint8_t*)st.host_grad + ctx->off_g[0][0]);
+    uint8_t* eg = (uint8_t*)st.host_grad + ctx->off_g[0][0];
     const float* src = ctx->host_grad_rows;
+    const size_t gesz = p.gesz;
     const int nthr = (int)std::min<unsigned>(8, std::max(1u, std::thread::hardware_concurrency() / 2));
     std::vector<std::thread> sth;
     const int per = (n_ids + nthr - 1) / nthr;
@@ -1506,7 +1528,15 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       const int u0 = i * per, u1 = std::min(n_ids, u0 + per);
       if (u0 >= u1) break;
       sth.emplace_back([=] {
-        for (int u = u0; u < u1; ++u) std::memcpy(eg + (size_t)ids[u] * h, src + (size_t)u * h, (size_t)h * 4);
+        for (int u = u0; u < u1; ++u) {
+          const float* row = src + (size_t)u * h;
+          if (gesz == 4) {
+            std::memcpy(eg + (size_t)ids[u] * h * 4, row, (size_t)h * 4);
+          } else {
+            uint16_t* dst = (uint16_t*)eg + (size_t)ids[u] * h;
+            for (int c = 0; c < h; ++c) dst[c] = host_bf16_rne(row[c]);
+          }
+        }
       });
     }
     for (auto& x : sth) x.join();
@@ -1658,7 +1688,7 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
     return MT_ERR_BUDGET;
   }
   build_layout(*cfg, ctx->P.esz, &ctx->off_p);
-  build_layout(*cfg, 4, &ctx->off_g);
+  build_layout(*cfg, ctx->P.gesz, &ctx->off_g);
   const char* tr = getenv("MT_TRACE");
   ctx->trace = tr ? atoi(tr) : 1;
   if (ctx->trace < 0 || ctx->trace > 2) ctx->trace = 1;
@@ -1808,6 +1838,8 @@ int mt_bind_optimizer(mt_ctx* ctx, const mt_adamw_cfg* opt, float* master, float
   if (!(opt->lr >= 0.f) || !(opt->beta1 >= 0.f && opt->beta1 < 1.f) || !(opt->beta2 >= 0.f && opt->beta2 < 1.f) ||
       !(opt->eps > 0.f) || !(opt->weight_decay >= 0.f))
     return set_err(ctx, MT_ERR_ARG, "AdamW hyper-parameters out of range");
+  if (ctx->cfg.grad_dtype != MT_F32)
+    return set_err(ctx, MT_ERR_UNSUPPORTED, "the host optimizer takes fp32 gradients (grad_dtype = MT_F32)");
   ctx->opt = *opt;
   ctx->opt_master = master;
   ctx->opt_m = m;
@@ -1827,6 +1859,7 @@ int mt_adamw_update(const mt_layer_cfg* cfg, const mt_adamw_cfg* opt, int64_t st
   if (unit_begin < 0 || unit_end > cfg->n_layers + 2 || unit_begin > unit_end) return MT_ERR_ARG;
   std::string why;
   if (!cfg_valid(*cfg, &why)) return MT_ERR_ARG;
+  if (cfg->grad_dtype != MT_F32) return MT_ERR_UNSUPPORTED;
   std::vector<std::vector<size_t>> off32, offp;
   const size_t esz = params_dtype == MT_BF16 ? 2 : 4;
   build_layout(*cfg, 4, &off32);
