@@ -235,9 +235,10 @@ def head_slice_rows(shape, esz, moe=None):
 # DRAM traffic of the GEMM launches of one 8B step (B=2, S=4096, K=4), from
 # ncu (dram__bytes_read.sum + dram__bytes_write.sum over the 508 GEMM launches
 # of the second step of `python bench.py --steps 1 --warmup 1
-# --no-cpu-baseline`, cold cache between launches): 566.4 GB. Valid for the
-# paired-SM GEMM kernel as committed with that capture.
-GEMM_TRAFFIC_8B_STEP = 566.38e9
+# --no-cpu-baseline`, cold cache between launches): 621.2 GB with the GEMM
+# kernels as committed with that capture (earlier captures on other boxes and
+# kernel builds: 566.4 and 687.9 GB).
+GEMM_TRAFFIC_8B_STEP = 621.2e9
 GEMM_LAUNCHES_8B_STEP = 508
 
 

@@ -704,7 +704,11 @@ __global__ void __launch_bounds__(192, 1)
 template <bool A_MN, bool B_MN>
 int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cudaStream_t st) {
   auto kern = gemm_pair_kernel<A_MN, B_MN>;
-  static int max_clusters = 0;
+  // shared memory without the fp32 staging rows unless this launch stages
+  const int smem = p.stage_f32 ? PairCfg::SMEM : PairCfg::SMEM - kStagingBytes;
+  static int max_clusters_v[2] = {0, 0};
+  int& max_clusters = max_clusters_v[p.stage_f32 ? 1 : 0];
+  static bool attr_set = false;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -712,13 +716,16 @@ int launch_pair(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& 
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.blockDim = dim3(192);
-  cfg.dynamicSmemBytes = PairCfg::SMEM;
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!max_clusters) {
+  if (!attr_set) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, PairCfg::SMEM) != cudaSuccess)
       return -1;
+    attr_set = true;
+  }
+  if (!max_clusters) {
     cfg.gridDim = dim3(2 * (mt_host::num_sms() / 2));
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, (const void*)kern, &cfg) != cudaSuccess || n <= 0) {
@@ -753,7 +760,8 @@ int launch(const CUtensorMap& ta, const CUtensorMap& tb, const GemmParams& p, cu
   const int tiles =
       ((p.M + BM - 1) / BM) * ((p.N + tile_n - 1) / tile_n) * ((p.grp_seg && A_MN) ? p.grp_E : 1);
   const int grid = tiles < mt_host::num_sms() ? tiles : mt_host::num_sms();
-  kern<<<grid, 192, C::SMEM, st>>>(ta, tb, p);
+  const int smem = p.stage_f32 ? C::SMEM : C::SMEM - kStagingBytes;  // staging rows only when used
+  kern<<<grid, 192, smem, st>>>(ta, tb, p);
   count_launches(1);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

@@ -147,3 +147,16 @@ def test_qwen3_moe_shape_full_batch_properties():
         assert not np.any(g[:goff // 4] != 0) and not np.any(g[(goff + gnb) // 4:] != 0)
         assert np.any(g[goff // 4:(goff + gnb) // 4] != 0)
     assert mt.mt_op_device_error() == 0
+
+
+@pytest.mark.parametrize("E,k", [(8, 1), (8, 8), (16, 3)], ids=["top1", "all_experts", "top3_of_16"])
+def test_moe_routing_degenerate_cases(E, k):
+    """Top-1 routing; every expert chosen by every token (the mixture is then
+    the full softmax mixture and no row is padded away from any expert); an
+    odd k. Same comparison against the oracle."""
+    cfg = oracle.Config(n_layers=2, hidden=64, n_heads=4, n_kv_heads=2, head_dim=16, ffn_dim=0, vocab=256,
+                        rope_theta=1e4, norm_eps=1e-5, n_experts=E, top_k=k, expert_ffn=32)
+    tok, lab, packed, loss, grads, route = run_moe(cfg, 2, 24, 2, 251 + E + k, 252)
+    check_against_oracle(cfg, tok, lab, packed, loss, grads, route, min_agree=0.85)
+    if k == E:
+        assert np.all(np.sort(route, axis=2) == np.arange(E))
