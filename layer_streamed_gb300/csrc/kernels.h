@@ -94,9 +94,9 @@ int moe_route(const float* r, int T, int E, int k, int32_t* sel, float* w, int32
 // seg[0..E]: expert e's rows start at seg[e], each segment its count rounded
 // up to 128 rows; tile_e[b] (b < n_blocks): expert of 128-row block b, or -1.
 int moe_segments(const int32_t* counts, int E, int n_blocks, int32_t* seg, int32_t* tile_e, cudaStream_t st);
-// perm[row] = slot, spos[slot] = row for the n = T*k slots (rows from seg[e]).
-int moe_permute(const int32_t* sel, int n, int E, const int32_t* seg, int32_t* perm, int32_t* spos,
-                cudaStream_t st);
+// spos[slot] = row for the n = T*k slots (expert e's rows from seg[e], in
+// ascending slot order).
+int moe_permute(const int32_t* sel, int n, int E, const int32_t* seg, int32_t* spos, cudaStream_t st);
 // xp[spos[s]] = m[s / k] for the n slots (bf16 rows of h).
 int moe_gather(const uint16_t* m, const int32_t* spos, int n, int k, int h, uint16_t* xp, cudaStream_t st);
 // y[t] = hmid[t] + sum_j w[t,j] yp[spos[t,j]] (fp32).

@@ -113,10 +113,10 @@ __global__ void __launch_bounds__(1024) moe_segments_kernel(const int32_t* __res
 }
 
 // One block per expert: the rows of expert e in ascending slot order from
-// the start of its segment, perm[row] = slot and spos[slot] = row.
+// the start of its segment, spos[slot] = row.
 __global__ void __launch_bounds__(1024) moe_permute_kernel(const int32_t* __restrict__ sel, int n, int E,
                                                            const int32_t* __restrict__ seg,
-                                                           int32_t* __restrict__ perm, int32_t* __restrict__ spos) {
+                                                           int32_t* __restrict__ spos) {
   __shared__ int warp_tot[32];
   const int e = blockIdx.x;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
@@ -135,7 +135,6 @@ __global__ void __launch_bounds__(1024) moe_permute_kernel(const int32_t* __rest
     }
     if (hit) {
       const int row = running + before + __popc(bal & ((1u << lane) - 1u));
-      perm[row] = s;
       spos[s] = row;
     }
     running += total;
@@ -275,10 +274,9 @@ int moe_segments(const int32_t* counts, int E, int n_blocks, int32_t* seg, int32
   return launched() ? 0 : -1;
 }
 
-int moe_permute(const int32_t* sel, int n, int E, const int32_t* seg, int32_t* perm, int32_t* spos,
-                cudaStream_t st) {
+int moe_permute(const int32_t* sel, int n, int E, const int32_t* seg, int32_t* spos, cudaStream_t st) {
   if (n < 1 || E < 1) return -1;
-  moe_permute_kernel<<<E, 1024, 0, st>>>(sel, n, E, seg, perm, spos);
+  moe_permute_kernel<<<E, 1024, 0, st>>>(sel, n, E, seg, spos);
   count_launches(1);
   return launched() ? 0 : -1;
 }

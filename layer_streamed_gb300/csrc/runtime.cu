@@ -271,7 +271,7 @@ struct Plan {
   size_t o_x, o_a, o_rstd1, o_qkv, o_o, o_lse, o_hmid, o_m, o_rstd2, o_gu, o_act;
   // mixture-of-experts slot: router logits, selection, weights, slot <-> row
   // maps, and the routed rows (grouped by expert) with their activations
-  size_t o_r, o_sel, o_w, o_spos, o_perm, o_seg, o_tile_e, o_xp, o_gup, o_actp, o_yp;
+  size_t o_r, o_sel, o_w, o_spos, o_seg, o_tile_e, o_xp, o_gup, o_actp, o_yp;
 };
 
 size_t layer_cast_bytes(const Plan& p) {  // device bf16 view of one layer (fp32 params)
@@ -349,7 +349,6 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
     p.o_sel = take(R * 4);
     p.o_w = take(R * 4);
     p.o_spos = take(R * 4);
-    p.o_perm = take(Rp * 4);
     p.o_seg = take((E + 1) * 4);
     p.o_tile_e = take(Rp / 128 * 4);
     p.o_xp = take(Rp * h * 2);
@@ -616,7 +615,7 @@ struct ActSlot {
   uint16_t *a, *qkv, *o, *m, *gu, *act;
   // mixture-of-experts
   float *r, *w, *yp;
-  int32_t *sel, *spos, *perm, *seg, *tile_e;
+  int32_t *sel, *spos, *seg, *tile_e;
   uint16_t *xp, *gup, *actp;
 };
 
@@ -639,7 +638,6 @@ ActSlot act_slot(mt_ctx* ctx, int K, int nb, int j) {
   s.sel = (int32_t*)(base + p.o_sel);
   s.w = (float*)(base + p.o_w);
   s.spos = (int32_t*)(base + p.o_spos);
-  s.perm = (int32_t*)(base + p.o_perm);
   s.seg = (int32_t*)(base + p.o_seg);
   s.tile_e = (int32_t*)(base + p.o_tile_e);
   s.xp = (uint16_t*)(base + p.o_xp);
@@ -885,7 +883,7 @@ int moe_ffn_forward(Step& st, int l, const LayerView& w, const ActSlot& a, float
   CKR(gemm(ctx, GEMM_NT, EPI_F32, a.m, w.wr, a.r, nullptr, T, E, h, h, h, E));
   CKL(moe_route(a.r, T, E, k, a.sel, a.w, ctx->moe_counts, ctx->moe_route + (size_t)(l - 1) * T * k, s));
   CKL(moe_segments(ctx->moe_counts, E, p.n_pad / 128, a.seg, a.tile_e, s));
-  CKL(moe_permute(a.sel, n, E, a.seg, a.perm, a.spos, s));
+  CKL(moe_permute(a.sel, n, E, a.seg, a.spos, s));
   CK(cudaMemsetAsync(a.xp, 0, (size_t)p.n_pad * h * 2, s));  // padding rows are zero
   CKL(moe_gather(a.m, a.spos, n, k, h, a.xp, s));
   {
