@@ -106,6 +106,27 @@ def test_bitwise_identical_across_K():
             assert np.array_equal(g.view(np.uint32), base.view(np.uint32)), K
 
 
+def test_small_config_full_size_bitwise_across_K_and_runs():
+    """The small decoder at its full size (8 layers, hidden 1024, 16 x 64
+    heads, FFN 2816, vocab 32000, B=4, S=2048, fp32 host master weights):
+    gradients bitwise identical for K = 4, 1, 2 and for a repeated K = 4."""
+    torch, mt = need_gpu()
+    cfg = SMALL
+    B, S = 4, 2048
+    tok, lab = make_tokens(cfg, B, S, 51)
+    out = []
+    with open_session(mt, cfg, B, S, 4) as s:
+        s.params[:] = make_params(cfg, 52)
+        for K in (4, 1, 2, 4):
+            loss = s.step(tok, lab, K)
+            out.append((K, loss, s.grads.copy()))
+    _, l0, g0 = out[0]
+    for K, loss, g in out[1:]:
+        assert loss == l0, K
+        assert np.array_equal(g.view(np.uint32), g0.view(np.uint32)), K
+    assert np.all(np.isfinite(g0))
+
+
 def test_gradient_buffer_fully_written():
     """Every byte of the gradient buffer is defined after a step: tensors hold
     the gradient, the padding between tensors is zero (whatever it held)."""
