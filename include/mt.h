@@ -69,7 +69,7 @@ typedef enum { MT_F32 = 0, MT_BF16 = 1 } mt_dtype;
  * with weights p_j / sum of the chosen p; each a SwiGLU MLP of width
  * expert_ffn; out = sum_j w_j y_j. No shared expert, no auxiliary loss.
  * Then ffn_dim = 0, n_experts a multiple of 8 in [8, 1024], top_k in
- * [1, min(32, n_experts)], expert_ffn % 8 == 0, and MT_BF16 params. */
+ * [1, min(32, n_experts)], expert_ffn % 32 == 0, and MT_BF16 params. */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
   float rope_theta, norm_eps;
