@@ -395,6 +395,23 @@ size_t mt_op_lmhead_ce_workspace(int T, int V, int h);
 int mt_op_lmhead_ce(const void* X, const void* W, const int32_t* labels, float scale, float* dX, float* dW,
                     float* loss_dev, void* workspace, int T, int V, int h, void* stream);
 
+/* Mixture-of-experts FFN forward on device buffers (the routed part of a
+ * MoE layer, as the streamed step runs it): router logits r = m Wr^T, top_k
+ * experts of largest logit per token (equal: lower index), weights
+ * renormalised over the k, grouped SwiGLU expert GEMMs, and
+ * out[t] = resid[t] + sum_j w_tj y_{e_tj}(m_t).
+ *  m bf16 [T, h]; Wr bf16 [E, h]; Wgu bf16 [E, 2*Fe, h] (each expert's gate
+ *  rows then up rows); Wd bf16 [E, h, Fe]; resid fp32 [T, h]; out fp32
+ *  [T, h] (not aliasing resid); route int32 [T, top_k] receives the experts
+ *  (descending logit). workspace: mt_op_moe_workspace(T, h, E, top_k, Fe)
+ *  bytes of device memory, 256-byte aligned, owned by the caller.
+ * Same limits as the MoE layer (h % 64 == 0, E % 8 == 0 and <= 1024,
+ * top_k <= min(32, E), Fe % 32 == 0); MT_ERR_ARG otherwise. */
+size_t mt_op_moe_workspace(int T, int h, int E, int top_k, int Fe);
+int mt_op_moe_ffn_fwd(const void* m, const void* Wr, const void* Wgu, const void* Wd, const float* resid,
+                      float* out, int32_t* route, void* workspace, int T, int h, int E, int top_k, int Fe,
+                      void* stream);
+
 /* Device error word of the kernels (barrier timeouts etc.): returns and
  * clears it (0 = none). Synchronizes the device. */
 int mt_op_device_error(void);

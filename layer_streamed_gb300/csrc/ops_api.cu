@@ -1,6 +1,8 @@
 // Kernel-level C entry points (declared in include/mt.h): thin argument
 // checks in front of the layer-template launchers, for tests and
 // measurement. They allocate nothing.
+#include <algorithm>
+
 #include "../../include/mt.h"
 #include "common.cuh"
 #include "kernels.h"
@@ -14,9 +16,101 @@ inline int rc(int r) {
   return cudaPeekAtLastError() != cudaSuccess ? MT_ERR_CUDA : MT_ERR_ARG;
 }
 size_t rup(size_t x, size_t a) { return (x + a - 1) / a * a; }
+// Carving of the mixture-of-experts workspace (byte offsets, 256-aligned).
+struct MoeWs {
+  size_t r, sel, w, spos, counts, seg, tile_e, xp, gup, actp, yp, total;
+  int n_pad;
+};
+MoeWs moe_ws(int T, int h, int E, int k, int Fe) {
+  MoeWs o;
+  const size_t n = (size_t)T * k;
+  o.n_pad = (int)rup(n + (size_t)E * 127, 128);
+  size_t a = 0;
+  auto take = [&](size_t b) {
+    const size_t r = a;
+    a += rup(b, 256);
+    return r;
+  };
+  o.r = take((size_t)T * E * 4);
+  o.sel = take(n * 4);
+  o.w = take(n * 4);
+  o.spos = take(n * 4);
+  o.counts = take(((size_t)E + 1) * 4);
+  o.seg = take(((size_t)E + 1) * 4);
+  o.tile_e = take((size_t)o.n_pad / 128 * 4);
+  o.xp = take((size_t)o.n_pad * h * 2);
+  o.gup = take((size_t)o.n_pad * 2 * Fe * 2);
+  o.actp = take((size_t)o.n_pad * Fe * 2);
+  o.yp = take((size_t)o.n_pad * h * 4);
+  o.total = a;
+  return o;
+}
+bool moe_dims_ok(int T, int h, int E, int k, int Fe) {
+  return T >= 1 && h >= 64 && h % 64 == 0 && E >= 8 && E <= 1024 && E % 8 == 0 && k >= 1 && k <= 32 && k <= E &&
+         Fe >= 32 && Fe % 32 == 0 && (double)T * k * std::max(h, 2 * Fe) < 2147483647.0 * 4;
+}
 }  // namespace
 
 extern "C" {
+
+size_t mt_op_moe_workspace(int T, int h, int E, int top_k, int Fe) {
+  if (!moe_dims_ok(T, h, E, top_k, Fe)) return 0;
+  return moe_ws(T, h, E, top_k, Fe).total;
+}
+
+int mt_op_moe_ffn_fwd(const void* m, const void* Wr, const void* Wgu, const void* Wd, const float* resid,
+                      float* out, int32_t* route, void* workspace, int T, int h, int E, int top_k, int Fe,
+                      void* stream) {
+  if (!m || !Wr || !Wgu || !Wd || !resid || !out || !route || !workspace) return MT_ERR_ARG;
+  if (!moe_dims_ok(T, h, E, top_k, Fe) || ((uintptr_t)workspace & 255)) return MT_ERR_ARG;
+  const MoeWs o = moe_ws(T, h, E, top_k, Fe);
+  uint8_t* ws = (uint8_t*)workspace;
+  float* r = (float*)(ws + o.r);
+  int32_t* sel = (int32_t*)(ws + o.sel);
+  float* w = (float*)(ws + o.w);
+  int32_t* spos = (int32_t*)(ws + o.spos);
+  int32_t* counts = (int32_t*)(ws + o.counts);
+  int32_t* seg = (int32_t*)(ws + o.seg);
+  int32_t* tile_e = (int32_t*)(ws + o.tile_e);
+  uint16_t* xp = (uint16_t*)(ws + o.xp);
+  uint16_t* gup = (uint16_t*)(ws + o.gup);
+  uint16_t* actp = (uint16_t*)(ws + o.actp);
+  float* yp = (float*)(ws + o.yp);
+  const int n = T * top_k;
+  cudaStream_t st = S(stream);
+  {
+    GemmParams gp{T, E, h, EPI_F32, r, nullptr, E, 0, 1};
+    if (gemm_bf16(GEMM_NT, gp, m, Wr, h, h, st)) return rc(-1);
+  }
+  if (moe_route(r, T, E, top_k, sel, w, counts, route, st) || moe_segments(counts, E, o.n_pad / 128, seg, tile_e, st) ||
+      moe_permute(sel, n, E, seg, spos, st))
+    return rc(-1);
+  if (cudaMemsetAsync(xp, 0, (size_t)o.n_pad * h * 2, st) != cudaSuccess) return MT_ERR_CUDA;
+  if (moe_gather((const uint16_t*)m, spos, n, top_k, h, xp, st)) return rc(-1);
+  {
+    GemmParams gp{o.n_pad, Fe, h, EPI_BF16, gup, nullptr, 2 * Fe, 0, 1};
+    gp.gated = 1;
+    gp.u_off = Fe;
+    gp.u_col = Fe;
+    gp.act = actp;
+    gp.ld_act = Fe;
+    gp.grp_seg = seg;
+    gp.grp_tile_e = tile_e;
+    gp.grp_E = E;
+    gp.grp_b_rows = 2 * Fe;
+    if (gemm_bf16(GEMM_NT, gp, xp, Wgu, h, h, st)) return rc(-1);
+  }
+  {
+    GemmParams gp{o.n_pad, h, Fe, EPI_F32, yp, nullptr, h, 0, 1};
+    gp.grp_seg = seg;
+    gp.grp_tile_e = tile_e;
+    gp.grp_E = E;
+    gp.grp_b_rows = h;
+    if (gemm_bf16(GEMM_NT, gp, actp, Wd, Fe, Fe, st)) return rc(-1);
+  }
+  return rc(moe_combine(resid, yp, spos, w, T, top_k, h, out, st));
+}
+
 
 int mt_op_gemm(int mode, int epi, const void* A, const void* B, void* C, const void* addend, int M, int N, int K,
                int lda, int ldb, int ldc, void* stream) {

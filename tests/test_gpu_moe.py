@@ -160,3 +160,75 @@ def test_moe_routing_degenerate_cases(E, k):
     check_against_oracle(cfg, tok, lab, packed, loss, grads, route, min_agree=0.85)
     if k == E:
         assert np.all(np.sort(route, axis=2) == np.arange(E))
+
+
+def _moe_op(torch, mt, m, wr, wgu, wd, k):
+    """Run mt_op_moe_ffn_fwd on device bf16 tensors; returns (out, route)."""
+    T, h = m.shape
+    E, Fe = wr.shape[0], wd.shape[2]
+    resid = torch.zeros((T, h), dtype=torch.float32, device="cuda")
+    out = torch.empty((T, h), dtype=torch.float32, device="cuda")
+    route = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    ws = torch.empty(mt.mt_op_moe_workspace(T, h, E, k, Fe), dtype=torch.uint8, device="cuda")
+    mt.mt_op_moe_ffn_fwd(m, wr, wgu, wd, resid, out, route, ws, T, h, E, k, Fe)
+    torch.cuda.synchronize()
+    assert mt.mt_op_device_error() == 0
+    return out.cpu().numpy(), route.cpu().numpy()
+
+
+def _bf16_dev(torch, shape, gen, std):
+    return (torch.randn(shape, generator=gen, device="cuda") * std).to(torch.bfloat16)
+
+
+def _host(t):
+    return t.float().cpu().numpy()
+
+
+def test_moe_op_matches_oracle():
+    """The layer's MoE forward as one entry point (router, routing, grouped
+    expert GEMMs, combine), ragged tokens, against the oracle with the GPU's
+    choices forced; the choices must be the oracle's own."""
+    torch, mt = need_gpu()
+    T, h, E, k, Fe = 77, 128, 16, 4, 64
+    gen = torch.Generator(device="cuda").manual_seed(261)
+    m = _bf16_dev(torch, (T, h), gen, 1.0)
+    wr, wgu, wd = (_bf16_dev(torch, s, gen, 0.05) for s in ((E, h), (E, 2 * Fe, h), (E, h, Fe)))
+    out, route = _moe_op(torch, mt, m, wr, wgu, wd, k)
+    ref, own, *_ = oracle.moe_ffn(_host(m), _host(wr), _host(wgu), _host(wd), k)
+    assert np.array_equal(np.sort(route, axis=1), np.sort(own, axis=1))
+    ref_forced, *_ = oracle.moe_ffn(_host(m), _host(wr), _host(wgu), _host(wd), k, route_in=route)
+    from tests.common import rel_l2
+    assert rel_l2(out, ref_forced) < 1.5e-2
+
+
+def test_moe_op_sampled_at_qwen3_shape():
+    """The MoE forward at the Qwen3-style layer's full size (T=4096 tokens,
+    hidden 4096, 128 experts x 1536, top-8: 32768 routed rows), checked on
+    sampled tokens: their chosen experts are the top-8 of their logits
+    (recomputed in double), and their outputs match the oracle run on just
+    those tokens and the experts they use (the renormalised weights depend
+    only on the chosen logits, so dropping the other experts changes
+    nothing)."""
+    torch, mt = need_gpu()
+    T, h, E, k, Fe = 4096, 4096, 128, 8, 1536
+    gen = torch.Generator(device="cuda").manual_seed(271)
+    m = _bf16_dev(torch, (T, h), gen, 1.0)
+    wr, wgu, wd = (_bf16_dev(torch, s, gen, 0.02) for s in ((E, h), (E, 2 * Fe, h), (E, h, Fe)))
+    out, route = _moe_op(torch, mt, m, wr, wgu, wd, k)
+    rng = np.random.default_rng(272)
+    tok = np.sort(rng.choice(T, 6, replace=False))
+    m_s = _host(m[torch.as_tensor(tok, device="cuda")]).astype(np.float64)
+    r64 = m_s @ _host(wr).astype(np.float64).T
+    for i, t in enumerate(tok):
+        chosen = np.zeros(E, bool)
+        chosen[route[t]] = True
+        assert chosen.sum() == k
+        assert r64[i, chosen].min() >= r64[i, ~chosen].max() - 1e-3 * np.abs(r64[i]).max()
+    used = np.unique(route[tok])
+    idx = torch.as_tensor(used, device="cuda")
+    remap = {e: j for j, e in enumerate(used)}
+    route_sub = np.vectorize(remap.get)(route[tok]).astype(np.int32)
+    ref, *_ = oracle.moe_ffn(m_s.astype(np.float32), _host(wr[idx]), _host(wgu[idx]), _host(wd[idx]), k,
+                             route_in=route_sub)
+    from tests.common import rel_l2
+    assert rel_l2(out[tok], ref) < 1.5e-2
