@@ -66,6 +66,38 @@ def test_train_step_is_step_then_update(bf16):
     assert runs[1][0] < runs[0][0]  # one AdamW step on the same batch lowers its loss
 
 
+def test_train_step_mixture_of_experts():
+    """The same equality for a mixture-of-experts model (router and expert
+    tensors are updated like any other), and the loss falls."""
+    from tests.common import TINY_MOE
+    torch, mt = need_gpu()
+    cfg = TINY_MOE
+    shape = mt.ModelShape(cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
+                          cfg.vocab, cfg.rope_theta, cfg.norm_eps, cfg.n_experts, cfg.top_k, cfg.expert_ffn)
+    tok, lab = make_tokens(cfg, 2, 32, 33)
+    packed = make_params(cfg, 34, bf16=True)
+    opt = mt.adamw_cfg(2e-3, 0.9, 0.999, 1e-8, 0.01)
+    units = cfg.n_layers + 2
+    losses = []
+    with mt.Session(shape, 2, 32, 2, mt.MT_BF16) as s:
+        s.params[:] = packed
+        s.bind_optimizer(opt, _master_f32(cfg, packed, True), n_threads=3)
+        for i in range(2):
+            losses.append(s.train_step(tok, lab, 2))
+        p_train = s.params.copy()
+    with mt.Session(shape, 2, 32, 2, mt.MT_BF16) as s:
+        s.params[:] = packed
+        master = _master_f32(cfg, packed, True)
+        m = np.zeros_like(master)
+        v = np.zeros_like(master)
+        for i in range(2):
+            assert s.step(tok, lab, 2) == losses[i]
+            mt.mt_adamw_update(s.cfg, opt, i + 1, 0, units, master.ctypes.data, m.ctypes.data, v.ctypes.data,
+                               s.grads_ptr, s.params_ptr, mt.MT_BF16, 2)
+        assert np.array_equal(s.params, p_train)
+    assert losses[1] < losses[0]
+
+
 def test_train_step_needs_an_optimizer():
     torch, mt = need_gpu()
     cfg = TINY_GQA
