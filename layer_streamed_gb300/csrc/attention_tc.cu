@@ -58,21 +58,6 @@ constexpr uint32_t tile_bytes() {
   return ((D + 63) / 64) * BOX;
 }
 
-// Write columns [32c, 32c+32) of row r of a [128][128] K-major swizzled tile.
-__device__ __forceinline__ void st_tile_row32(uint8_t* tile, int r, int c, const float (&v)[32]) {
-  uint8_t* rowp = tile + (c >> 1) * 16384 + r * 128;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const int chunk = (c & 1) * 4 + i;
-    uint4 w;
-    w.x = pack_bf2(v[8 * i + 0], v[8 * i + 1]);
-    w.y = pack_bf2(v[8 * i + 2], v[8 * i + 3]);
-    w.z = pack_bf2(v[8 * i + 4], v[8 * i + 5]);
-    w.w = pack_bf2(v[8 * i + 6], v[8 * i + 7]);
-    *(uint4*)(rowp + ((chunk ^ (r & 7)) << 4)) = w;
-  }
-}
-
 // K-major A/B descriptor of the k-th 16-wide step of a [128][64*n] tile.
 __device__ __forceinline__ uint64_t kmaj_desc(const uint8_t* tile, int kk) {
   return make_sdesc(smem_u32(tile) + (kk >> 2) * BOX + (kk & 3) * 32, 16, 1024);

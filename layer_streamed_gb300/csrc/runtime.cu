@@ -717,7 +717,6 @@ struct Step {
   bool train = false;                 // apply the optimizer as gradients land
   bool async = false;                 // apply the previous step's update, publishing units as they land
   std::vector<cudaEvent_t> landed;    // per unit (train steps): its gradients are on the host
-  const Plan& P() const { return ctx->P; }
 };
 
 void plan_sequence(Step& st) {
@@ -1889,7 +1888,7 @@ int step_common(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B
   int cur = 0;
   cudaGetDevice(&cur);
   if (cur != ctx->device) cudaSetDevice(ctx->device);
-  Step st{ctx, B, S, T, K, (ctx->cfg.n_layers + K - 1) / K, host_grad_out, {}, {}, {}};
+  Step st{ctx, B, S, T, K, (ctx->cfg.n_layers + K - 1) / K, host_grad_out, {}, {}, {}, false, false, {}};
   st.train = train;
   if (train || async_) st.landed.assign(ctx->cfg.n_layers + 2, nullptr);
   st.async = async_;
