@@ -330,27 +330,59 @@ def cpu_oracle_sample(shape, S_sample, seed=5, moe=None, eps=1e-5):
     return S_sample / t_full, t1
 
 
+def cpu_oracle_full_step(shape, B, S, seed=5, moe=None, eps=1e-5, bf16=False):
+    """Time one whole step of the CPU oracle (single thread) at the workload's
+    own size (only for workloads where that takes seconds, e.g. the tiny
+    decoder). Returns (tokens/s, seconds)."""
+    import oracle
+    import seedgen
+    L, h, nq, nkv, d, F, V, theta = shape[:8]
+    E, k, Fe = moe or (0, 0, 0)
+    cfg = oracle.Config(L, h, nq, nkv, d, F, V, theta, eps, E, k, Fe)
+    packed = np.zeros(oracle.packed_bytes(cfg, bf16), np.uint8)
+    offs = []
+    for unit, t, name, shp, is_gain in oracle.tensor_list(cfg):
+        off, nb = oracle.tensor_offset(cfg, unit, t, bf16)
+        offs.append((unit, t, off, int(np.prod(shp)), is_gain))
+    seedgen.fill_packed_params(packed.ctypes.data, offs, bf16, seed)
+    tok, lab = seedgen.tokens_and_labels(B, S, V, seed + 1)
+    t0 = time.perf_counter()
+    oracle.forward_backward(cfg, packed, tok, lab, bf16=bf16)
+    t1 = time.perf_counter() - t0
+    return B * S / t1, t1
+
+
+FULL_STEP_BASELINE = {"tiny"}  # workloads whose CPU baseline is a whole oracle step
+
+
 def run_reference(args, shape, B, S):
     """The reference arm: the CPU oracle as it stands, timed on this host."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
     S_sample = 8
+    full = args.workload in FULL_STEP_BASELINE
     vals = []
     for i in range(args.warmup + args.steps):
-        v, t1 = cpu_oracle_sample(shape, S_sample, seed=100 + i, moe=MOE.get(args.workload),
-                                  eps=NORM_EPS.get(args.workload, 1e-5))
+        if full:
+            v, t1 = cpu_oracle_full_step(shape, B, S, seed=100 + i, moe=MOE.get(args.workload),
+                                         eps=NORM_EPS.get(args.workload, 1e-5),
+                                         bf16=bool(WORKLOADS[args.workload][11]))
+        else:
+            v, t1 = cpu_oracle_sample(shape, S_sample, seed=100 + i, moe=MOE.get(args.workload),
+                                      eps=NORM_EPS.get(args.workload, 1e-5))
         if i >= args.warmup:
             vals.append(v)
     value = float(np.median(vals))
+    sample = (f"whole step of the {args.workload} workload at B={B}, S={S}, single-threaded fp32 oracle" if full else
+              f"one decoder layer + LM head of the {args.workload} shape at B=1, S={S_sample}, single-threaded fp32 "
+              f"oracle, extrapolated linearly to {shape[0]} layers")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": args.workload, "global_batch": B, "seq_len": S, "parallelism": "replicas"},
-        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                         "sample": f"one decoder layer + LM head of the {args.workload} shape at B=1, S={S_sample}, "
-                                   f"single-threaded fp32 oracle, extrapolated linearly to {shape[0]} layers"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -589,11 +621,16 @@ def main():
     del arena
     if not args.no_cpu_baseline and world == 1:
         log("timing the CPU oracle sample")
-        v, t1 = cpu_oracle_sample(shape, 8, moe=moe, eps=eps)
-        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle",
-                                "sample": f"one decoder layer + LM head of the {args.workload} shape at B=1, S=8 "
-                                          f"({t1:.1f} s single-threaded fp32 oracle), extrapolated linearly to "
-                                          f"{L} layers; host has {os.cpu_count()} cores"}
+        if args.workload in FULL_STEP_BASELINE and not (args.layers or args.seq or args.batch):
+            v, t1 = cpu_oracle_full_step(shape, B, S, moe=moe, eps=eps, bf16=bf16)
+            sample = (f"whole step of the {args.workload} workload at B={B}, S={S} ({t1:.2f} s single-threaded "
+                      f"fp32 oracle); host has {os.cpu_count()} cores")
+        else:
+            v, t1 = cpu_oracle_sample(shape, 8, moe=moe, eps=eps)
+            sample = (f"one decoder layer + LM head of the {args.workload} shape at B=1, S=8 ({t1:.1f} s "
+                      f"single-threaded fp32 oracle), extrapolated linearly to {L} layers; host has "
+                      f"{os.cpu_count()} cores")
+        line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
     if dist:
         dist.destroy_process_group()
