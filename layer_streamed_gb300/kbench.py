@@ -3,6 +3,7 @@
   python -m layer_streamed_gb300.kbench gemm --mode nt --M 8192 --N 28672 --K 4096 [--reps 20]
   python -m layer_streamed_gb300.kbench attn --B 2 --S 4096 --heads 32 --kv-heads 8 --head-dim 128 [--bwd]
   python -m layer_streamed_gb300.kbench norm --T 8192 --h 4096 [--bwd]
+  python -m layer_streamed_gb300.kbench moe --T 4096 --h 4096 --experts 128 --top-k 8 --expert-ffn 1536
 
 Inputs are random bf16 tensors on the current GPU (larger than L2 at the 8B
 shapes); each launch is timed with CUDA events on the launching stream after
@@ -91,6 +92,25 @@ def bench_norm(args) -> dict:
             "gbs": nbytes / ms / 1e6}
 
 
+def bench_moe(args) -> dict:
+    """Mixture-of-experts FFN forward (mt_op_moe_ffn_fwd): router, routing,
+    grouped gate|up and down expert GEMMs, combine. TFLOP/s counts the
+    routed rows' expert products and the router."""
+    T, h, E, k, Fe = args.T, args.h, args.experts, args.top_k, args.expert_ffn
+    m = torch.randn((T, h), device="cuda").to(torch.bfloat16)
+    wr = (torch.randn((E, h), device="cuda") * 0.02).to(torch.bfloat16)
+    wgu = (torch.randn((E, 2 * Fe, h), device="cuda") * 0.02).to(torch.bfloat16)
+    wd = (torch.randn((E, h, Fe), device="cuda") * 0.02).to(torch.bfloat16)
+    resid = torch.zeros((T, h), device="cuda")
+    out = torch.empty((T, h), device="cuda")
+    route = torch.empty((T, k), device="cuda", dtype=torch.int32)
+    ws = torch.empty(mt.mt_op_moe_workspace(T, h, E, k, Fe), device="cuda", dtype=torch.uint8)
+    ms = _time(lambda: mt.mt_op_moe_ffn_fwd(m, wr, wgu, wd, resid, out, route, ws, T, h, E, k, Fe), args.reps)
+    flop = 2.0 * T * E * h + 2.0 * T * k * 3 * Fe * h
+    return {"kernel": "moe_ffn_fwd", "T": T, "h": h, "experts": E, "top_k": k, "expert_ffn": Fe, "ms": ms,
+            "tflops": flop / ms / 1e9}
+
+
 def main():
     ap = argparse.ArgumentParser()
     sub = ap.add_subparsers(dest="op", required=True)
@@ -114,9 +134,16 @@ def main():
     n.add_argument("--h", type=int, default=4096)
     n.add_argument("--bwd", action="store_true")
     n.add_argument("--reps", type=int, default=20)
+    e = sub.add_parser("moe")
+    e.add_argument("--T", type=int, default=4096)
+    e.add_argument("--h", type=int, default=4096)
+    e.add_argument("--experts", type=int, default=128)
+    e.add_argument("--top-k", type=int, default=8)
+    e.add_argument("--expert-ffn", type=int, default=1536)
+    e.add_argument("--reps", type=int, default=20)
     args = ap.parse_args()
     mt.build()
-    res = {"gemm": bench_gemm, "attn": bench_attn, "norm": bench_norm}[args.op](args)
+    res = {"gemm": bench_gemm, "attn": bench_attn, "norm": bench_norm, "moe": bench_moe}[args.op](args)
     res["device_error"] = mt.mt_op_device_error()
     print(json.dumps(res), flush=True)
 
