@@ -412,6 +412,17 @@ int mt_op_moe_ffn_fwd(const void* m, const void* Wr, const void* Wgu, const void
                       float* out, int32_t* route, void* workspace, int T, int h, int E, int top_k, int Fe,
                       void* stream);
 
+/* Its backward: runs the forward of mt_op_moe_ffn_fwd on the same inputs
+ * (same routing, written to route) and then, for dout = dLoss/d(out) fp32
+ * [T, h]: dm fp32 [T, h] (gradient of m, the router's path included),
+ * dWr fp32 [E, h], dWgu fp32 [E, 2*Fe, h], dWd fp32 [E, h, Fe] (all written;
+ * zero for experts that received no token). workspace:
+ * mt_op_moe_bwd_workspace(T, h, E, top_k, Fe) bytes, 256-byte aligned. */
+size_t mt_op_moe_bwd_workspace(int T, int h, int E, int top_k, int Fe);
+int mt_op_moe_ffn_bwd(const void* m, const void* Wr, const void* Wgu, const void* Wd, const float* dout, float* dm,
+                      float* dWr, float* dWgu, float* dWd, int32_t* route, void* workspace, int T, int h, int E,
+                      int top_k, int Fe, void* stream);
+
 /* Device error word of the kernels (barrier timeouts etc.): returns and
  * clears it (0 = none). Synchronizes the device. */
 int mt_op_device_error(void);

@@ -45,7 +45,8 @@ EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_crea
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
            "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error",
            "mt_adamw_update", "mt_bind_optimizer", "mt_train_step", "mt_train_step_async", "mt_optimizer_flush",
-           "mt_get_routing", "mt_op_moe_workspace", "mt_op_moe_ffn_fwd")
+           "mt_get_routing", "mt_op_moe_workspace", "mt_op_moe_ffn_fwd", "mt_op_moe_bwd_workspace",
+           "mt_op_moe_ffn_bwd")
 
 
 class MtError(RuntimeError):
@@ -148,6 +149,8 @@ def lib() -> ctypes.CDLL:
         "mt_op_device_error": (i32, []),
         "mt_op_moe_workspace": (sz, [i32, i32, i32, i32, i32]),
         "mt_op_moe_ffn_fwd": (i32, [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, vp]),
+        "mt_op_moe_bwd_workspace": (sz, [i32, i32, i32, i32, i32]),
+        "mt_op_moe_ffn_bwd": (i32, [vp] * 11 + [i32, i32, i32, i32, i32, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -540,6 +543,16 @@ def mt_op_moe_workspace(T, h, E, top_k, Fe) -> int:
 def mt_op_moe_ffn_fwd(m, Wr, Wgu, Wd, resid, out, route, workspace, T, h, E, top_k, Fe, stream=None):
     _check(lib().mt_op_moe_ffn_fwd(_ptr(m), _ptr(Wr), _ptr(Wgu), _ptr(Wd), _ptr(resid), _ptr(out), _ptr(route),
                                    _ptr(workspace), T, h, E, top_k, Fe, _stream(stream)))
+
+
+def mt_op_moe_bwd_workspace(T, h, E, top_k, Fe) -> int:
+    return lib().mt_op_moe_bwd_workspace(T, h, E, top_k, Fe)
+
+
+def mt_op_moe_ffn_bwd(m, Wr, Wgu, Wd, dout, dm, dWr, dWgu, dWd, route, workspace, T, h, E, top_k, Fe, stream=None):
+    _check(lib().mt_op_moe_ffn_bwd(_ptr(m), _ptr(Wr), _ptr(Wgu), _ptr(Wd), _ptr(dout), _ptr(dm), _ptr(dWr),
+                                   _ptr(dWgu), _ptr(dWd), _ptr(route), _ptr(workspace), T, h, E, top_k, Fe,
+                                   _stream(stream)))
 
 
 def mt_op_lmhead_ce_workspace(T, V, h) -> int:

@@ -19,6 +19,7 @@ size_t rup(size_t x, size_t a) { return (x + a - 1) / a * a; }
 // Carving of the mixture-of-experts workspace (byte offsets, 256-aligned).
 struct MoeWs {
   size_t r, sel, w, spos, counts, seg, tile_e, xp, gup, actp, yp, total;
+  size_t dyp, dw, dr, total_bwd;  // backward only
   int n_pad;
 };
 MoeWs moe_ws(int T, int h, int E, int k, int Fe) {
@@ -43,7 +44,74 @@ MoeWs moe_ws(int T, int h, int E, int k, int Fe) {
   o.actp = take((size_t)o.n_pad * Fe * 2);
   o.yp = take((size_t)o.n_pad * h * 4);
   o.total = a;
+  o.dyp = take((size_t)o.n_pad * h * 2);
+  o.dw = take(n * 4);
+  o.dr = take((size_t)T * E * 2);
+  o.total_bwd = a;
   return o;
+}
+
+// Device pointers of the carved workspace.
+struct MoeBufs {
+  float *r, *w, *yp;
+  int32_t *sel, *spos, *counts, *seg, *tile_e;
+  uint16_t *xp, *gup, *actp, *dyp, *dr;
+  float* dw;
+};
+MoeBufs moe_bufs(const MoeWs& o, void* workspace) {
+  uint8_t* ws = (uint8_t*)workspace;
+  MoeBufs b;
+  b.r = (float*)(ws + o.r);
+  b.sel = (int32_t*)(ws + o.sel);
+  b.w = (float*)(ws + o.w);
+  b.spos = (int32_t*)(ws + o.spos);
+  b.counts = (int32_t*)(ws + o.counts);
+  b.seg = (int32_t*)(ws + o.seg);
+  b.tile_e = (int32_t*)(ws + o.tile_e);
+  b.xp = (uint16_t*)(ws + o.xp);
+  b.gup = (uint16_t*)(ws + o.gup);
+  b.actp = (uint16_t*)(ws + o.actp);
+  b.yp = (float*)(ws + o.yp);
+  b.dyp = (uint16_t*)(ws + o.dyp);
+  b.dw = (float*)(ws + o.dw);
+  b.dr = (uint16_t*)(ws + o.dr);
+  return b;
+}
+
+// The routed part of the forward up to the experts' outputs y (rows in
+// expert order): router, routing, segments, gather, grouped gate|up (SwiGLU
+// epilogue) and grouped down products.
+int moe_fwd_core(const void* m, const void* Wr, const void* Wgu, const void* Wd, int32_t* route, const MoeWs& o,
+                 const MoeBufs& b, int T, int h, int E, int k, int Fe, cudaStream_t st) {
+  const int n = T * k;
+  {
+    GemmParams gp{T, E, h, EPI_F32, b.r, nullptr, E, 0, 1};
+    if (gemm_bf16(GEMM_NT, gp, m, Wr, h, h, st)) return -1;
+  }
+  if (moe_route(b.r, T, E, k, b.sel, b.w, b.counts, route, st) ||
+      moe_segments(b.counts, E, o.n_pad / 128, b.seg, b.tile_e, st) || moe_permute(b.sel, n, E, b.seg, b.spos, st))
+    return -1;
+  if (cudaMemsetAsync(b.xp, 0, (size_t)o.n_pad * h * 2, st) != cudaSuccess) return -1;
+  if (moe_gather((const uint16_t*)m, b.spos, n, k, h, b.xp, st)) return -1;
+  {
+    GemmParams gp{o.n_pad, Fe, h, EPI_BF16, b.gup, nullptr, 2 * Fe, 0, 1};
+    gp.gated = 1;
+    gp.u_off = Fe;
+    gp.u_col = Fe;
+    gp.act = b.actp;
+    gp.ld_act = Fe;
+    gp.grp_seg = b.seg;
+    gp.grp_tile_e = b.tile_e;
+    gp.grp_E = E;
+    gp.grp_b_rows = 2 * Fe;
+    if (gemm_bf16(GEMM_NT, gp, b.xp, Wgu, h, h, st)) return -1;
+  }
+  GemmParams gp{o.n_pad, h, Fe, EPI_F32, b.yp, nullptr, h, 0, 1};
+  gp.grp_seg = b.seg;
+  gp.grp_tile_e = b.tile_e;
+  gp.grp_E = E;
+  gp.grp_b_rows = h;
+  return gemm_bf16(GEMM_NT, gp, b.actp, Wd, Fe, Fe, st);
 }
 bool moe_dims_ok(int T, int h, int E, int k, int Fe) {
   return T >= 1 && h >= 64 && h % 64 == 0 && E >= 8 && E <= 1024 && E % 8 == 0 && k >= 1 && k <= 32 && k <= E &&
@@ -64,51 +132,67 @@ int mt_op_moe_ffn_fwd(const void* m, const void* Wr, const void* Wgu, const void
   if (!m || !Wr || !Wgu || !Wd || !resid || !out || !route || !workspace) return MT_ERR_ARG;
   if (!moe_dims_ok(T, h, E, top_k, Fe) || ((uintptr_t)workspace & 255)) return MT_ERR_ARG;
   const MoeWs o = moe_ws(T, h, E, top_k, Fe);
-  uint8_t* ws = (uint8_t*)workspace;
-  float* r = (float*)(ws + o.r);
-  int32_t* sel = (int32_t*)(ws + o.sel);
-  float* w = (float*)(ws + o.w);
-  int32_t* spos = (int32_t*)(ws + o.spos);
-  int32_t* counts = (int32_t*)(ws + o.counts);
-  int32_t* seg = (int32_t*)(ws + o.seg);
-  int32_t* tile_e = (int32_t*)(ws + o.tile_e);
-  uint16_t* xp = (uint16_t*)(ws + o.xp);
-  uint16_t* gup = (uint16_t*)(ws + o.gup);
-  uint16_t* actp = (uint16_t*)(ws + o.actp);
-  float* yp = (float*)(ws + o.yp);
-  const int n = T * top_k;
+  const MoeBufs b = moe_bufs(o, workspace);
   cudaStream_t st = S(stream);
-  {
-    GemmParams gp{T, E, h, EPI_F32, r, nullptr, E, 0, 1};
-    if (gemm_bf16(GEMM_NT, gp, m, Wr, h, h, st)) return rc(-1);
+  if (moe_fwd_core(m, Wr, Wgu, Wd, route, o, b, T, h, E, top_k, Fe, st)) return rc(-1);
+  return rc(moe_combine(resid, b.yp, b.spos, b.w, T, top_k, h, out, st));
+}
+
+size_t mt_op_moe_bwd_workspace(int T, int h, int E, int top_k, int Fe) {
+  if (!moe_dims_ok(T, h, E, top_k, Fe)) return 0;
+  return moe_ws(T, h, E, top_k, Fe).total_bwd;
+}
+
+int mt_op_moe_ffn_bwd(const void* m, const void* Wr, const void* Wgu, const void* Wd, const float* dout, float* dm,
+                      float* dWr, float* dWgu, float* dWd, int32_t* route, void* workspace, int T, int h, int E,
+                      int top_k, int Fe, void* stream) {
+  if (!m || !Wr || !Wgu || !Wd || !dout || !dm || !dWr || !dWgu || !dWd || !route || !workspace) return MT_ERR_ARG;
+  if (!moe_dims_ok(T, h, E, top_k, Fe) || ((uintptr_t)workspace & 255)) return MT_ERR_ARG;
+  const MoeWs o = moe_ws(T, h, E, top_k, Fe);
+  const MoeBufs b = moe_bufs(o, workspace);
+  const int k = top_k;
+  cudaStream_t st = S(stream);
+  if (moe_fwd_core(m, Wr, Wgu, Wd, route, o, b, T, h, E, k, Fe, st)) return rc(-1);
+  if (cudaMemsetAsync(b.dyp, 0, (size_t)o.n_pad * h * 2, st) != cudaSuccess) return MT_ERR_CUDA;
+  if (moe_combine_bwd(dout, b.yp, b.spos, b.w, T, k, h, b.dyp, b.dw, st)) return rc(-1);
+  auto grouped = [&](GemmParams& gp, bool tn, int b_rows) {
+    gp.grp_seg = b.seg;
+    gp.grp_tile_e = tn ? nullptr : b.tile_e;
+    gp.grp_E = E;
+    gp.grp_b_rows = b_rows;
+  };
+  {  // dWd_e = dY_e^T act_e
+    GemmParams gp{h, Fe, o.n_pad, EPI_F32, dWd, nullptr, Fe, 0, 1};
+    grouped(gp, true, 0);
+    if (gemm_bf16(GEMM_TN, gp, b.dyp, b.actp, h, Fe, st)) return rc(-1);
   }
-  if (moe_route(r, T, E, top_k, sel, w, counts, route, st) || moe_segments(counts, E, o.n_pad / 128, seg, tile_e, st) ||
-      moe_permute(sel, n, E, seg, spos, st))
-    return rc(-1);
-  if (cudaMemsetAsync(xp, 0, (size_t)o.n_pad * h * 2, st) != cudaSuccess) return MT_ERR_CUDA;
-  if (moe_gather((const uint16_t*)m, spos, n, top_k, h, xp, st)) return rc(-1);
-  {
-    GemmParams gp{o.n_pad, Fe, h, EPI_BF16, gup, nullptr, 2 * Fe, 0, 1};
-    gp.gated = 1;
-    gp.u_off = Fe;
+  {  // dact = dY Wd_e -> (dg, du) in place over (g, u)
+    GemmParams gp{o.n_pad, Fe, h, EPI_BF16, b.gup, nullptr, 2 * Fe, 0, 1};
+    gp.swiglu_bwd = 1;
+    gp.gu = b.gup;
+    gp.ld_gu = 2 * Fe;
     gp.u_col = Fe;
-    gp.act = actp;
-    gp.ld_act = Fe;
-    gp.grp_seg = seg;
-    gp.grp_tile_e = tile_e;
-    gp.grp_E = E;
-    gp.grp_b_rows = 2 * Fe;
-    if (gemm_bf16(GEMM_NT, gp, xp, Wgu, h, h, st)) return rc(-1);
+    grouped(gp, false, h);
+    if (gemm_bf16(GEMM_NN, gp, b.dyp, Wd, h, Fe, st)) return rc(-1);
   }
-  {
-    GemmParams gp{o.n_pad, h, Fe, EPI_F32, yp, nullptr, h, 0, 1};
-    gp.grp_seg = seg;
-    gp.grp_tile_e = tile_e;
-    gp.grp_E = E;
-    gp.grp_b_rows = h;
-    if (gemm_bf16(GEMM_NT, gp, actp, Wd, Fe, Fe, st)) return rc(-1);
+  {  // dWgu_e = d(g|u)_e^T x_e
+    GemmParams gp{2 * Fe, h, o.n_pad, EPI_F32, dWgu, nullptr, h, 0, 1};
+    grouped(gp, true, 0);
+    if (gemm_bf16(GEMM_TN, gp, b.gup, b.xp, 2 * Fe, h, st)) return rc(-1);
   }
-  return rc(moe_combine(resid, yp, spos, w, T, top_k, h, out, st));
+  {  // d x (routed rows, over y's rows) = d(g|u) Wgu_e
+    GemmParams gp{o.n_pad, h, 2 * Fe, EPI_F32, b.yp, nullptr, h, 0, 1};
+    grouped(gp, false, 2 * Fe);
+    if (gemm_bf16(GEMM_NN, gp, b.gup, Wgu, 2 * Fe, h, st)) return rc(-1);
+  }
+  if (moe_unpermute(b.yp, b.spos, T, k, h, dm, st) || moe_router_bwd(b.w, b.dw, b.sel, T, k, E, b.dr, st))
+    return rc(-1);
+  {  // dm += dr Wr
+    GemmParams gp{T, h, E, EPI_F32_ADD, dm, dm, h, 0, 1};
+    if (gemm_bf16(GEMM_NN, gp, b.dr, Wr, E, h, st)) return rc(-1);
+  }
+  GemmParams gp{E, h, T, EPI_F32, dWr, nullptr, h, 0, 1};  // dWr = dr^T m
+  return rc(gemm_bf16(GEMM_TN, gp, b.dr, m, E, h, st));
 }
 
 
