@@ -122,3 +122,16 @@ def test_moe_budget_and_validation(mt):
                dict(ffn_dim=1024)):
         bad = dataclasses.replace(TINY_MOE, **kw)
         assert mt.mt_required_budget(_cfg(mt, bad, True)) == 0, kw
+
+
+def test_moe_op_workspace_and_argument_checks(mt):
+    """Host-side checks of the kernel-level MoE entry points (no GPU work)."""
+    assert mt.mt_op_moe_workspace(4096, 4096, 128, 8, 1536) > 0
+    assert mt.mt_op_moe_bwd_workspace(4096, 4096, 128, 8, 1536) > mt.mt_op_moe_workspace(4096, 4096, 128, 8, 1536)
+    for bad in ((0, 4096, 128, 8, 1536), (8, 100, 128, 8, 1536), (8, 4096, 12, 8, 1536), (8, 4096, 8, 9, 1536),
+                (8, 4096, 128, 8, 1000)):
+        assert mt.mt_op_moe_workspace(*bad) == 0 and mt.mt_op_moe_bwd_workspace(*bad) == 0
+    L = mt.lib()
+    assert L.mt_op_moe_ffn_fwd(None, None, None, None, None, None, None, None, 8, 4096, 128, 8, 1536, None) == \
+        mt.MT_ERR_ARG
+    assert L.mt_op_moe_ffn_bwd(*([None] * 11), 8, 4096, 128, 8, 1536, None) == mt.MT_ERR_ARG

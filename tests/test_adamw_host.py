@@ -109,3 +109,39 @@ def test_adamw_argument_errors():
             mt.mt_adamw_update(cfg, mt.adamw_cfg(), step, u0, u1, a.ctypes.data, a.ctypes.data, a.ctypes.data,
                                a.ctypes.data, a.ctypes.data, mt.MT_F32, 1)
         assert e.value.code == mt.MT_ERR_ARG
+
+
+def test_host_adamw_mixture_of_experts_layout():
+    """The update runs over every tensor of a mixture-of-experts model's
+    layout (router, experts' gate|up and down matrices) exactly as over a
+    dense one: the same element-wise rule against the oracle."""
+    from tests.common import TINY_MOE
+    c = TINY_MOE
+    cfg = mt.make_cfg(c.n_layers, c.hidden, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.vocab,
+                      param_dtype=mt.MT_BF16, n_experts=c.n_experts, top_k=c.top_k, expert_ffn=c.expert_ffn)
+    f32 = lambda x: float(np.float32(x))
+    opt = AdamW(lr=f32(1e-3), beta1=f32(0.9), beta2=f32(0.999), eps=f32(1e-8), weight_decay=f32(0.01))
+    master, m, v, g, mask = _state(cfg, c, 7)
+    params = _params_of(cfg, c, master, mt.MT_BF16)
+    th_ref, _, _ = adamw_step(opt, 2, master, m, v, g)
+    mt.mt_adamw_update(cfg, mt.adamw_cfg(opt.lr, opt.beta1, opt.beta2, opt.eps, opt.weight_decay), 2, 0,
+                       c.n_layers + 2, master.ctypes.data, m.ctypes.data, v.ctypes.data, g.ctypes.data,
+                       params.ctypes.data, mt.MT_BF16, 2)
+    start = _state(cfg, c, 7)[0]
+    assert np.max(np.abs((master.astype(np.float64) - start) - (th_ref - start))) <= 1e-3 * opt.lr
+    assert np.array_equal(params, _params_of(cfg, c, master, mt.MT_BF16))
+    # the router and expert tensors moved
+    for t in (6, 7, 8):
+        off, nb = mt.mt_tensor_offset(cfg, mt.MT_F32, 1, t)
+        assert np.any(master[off // 4:(off + nb) // 4] != start[off // 4:(off + nb) // 4])
+
+
+def test_host_adamw_refuses_bf16_gradients():
+    c = TINY
+    cfg = mt.make_cfg(c.n_layers, c.hidden, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.vocab,
+                      grad_dtype=mt.MT_BF16)
+    a = np.zeros(mt.mt_packed_bytes(cfg, mt.MT_F32) // 4, np.float32)
+    with pytest.raises(mt.MtError) as e:
+        mt.mt_adamw_update(cfg, mt.adamw_cfg(), 1, 0, 1, a.ctypes.data, a.ctypes.data, a.ctypes.data,
+                           a.ctypes.data, a.ctypes.data, mt.MT_F32, 1)
+    assert e.value.code == mt.MT_ERR_UNSUPPORTED
