@@ -40,6 +40,8 @@
 #include "common.cuh"
 #include "kernels.h"
 
+#include <nvtx3/nvToolsExt.h>
+
 using namespace mt;
 
 namespace mt {
@@ -470,6 +472,7 @@ struct mt_ctx {
   bool fuse_top = true;
   bool debug_sync = false;  // MT_DEBUG_SYNC=1: wait for every unit, report progress on stderr
   bool serial = false;      // MT_SERIAL=1: no copy/compute overlap (ablation)
+  bool nvtx = false;        // MT_NVTX=1: an NVTX range around the issue of every unit (for nsys)
   std::string timeline;     // MT_TIMELINE=path: write the step's segments as CSV
   std::vector<Seg> segs;
   std::vector<OpSeg> opsegs;
@@ -706,6 +709,19 @@ int gemm(mt_ctx* ctx, int mode, int epi, const void* A, const void* B, void* C, 
 // The step
 // ===========================================================================
 namespace {
+
+// An NVTX range (host side) around the issue of one unit, so that a
+// system profiler attributes the unit's copies and kernels to it; a no-op
+// unless enabled (and nearly free when no tool is attached).
+struct NvtxRange {
+  bool on;
+  NvtxRange(bool enable, const char* name) : on(enable) {
+    if (on) nvtxRangePushA(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtxRangePop();
+  }
+};
 
 struct Step {
   mt_ctx* ctx;
@@ -1337,6 +1353,14 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
     const int slot = st.slot_of[i];
     const bool fresh = st.needs_load[i];
     if (fresh) CK(cudaStreamWaitEvent(s, ctx->ev_wready[slot], 0));
+    char label[48] = "";
+    if (ctx->nvtx) {
+      if (it.kind == IT_LAYER)
+        snprintf(label, sizeof label, "layer %d %s", std::abs(it.index), it.index > 0 ? "forward" : "backward");
+      else
+        snprintf(label, sizeof label, "head slice %d pass %d", it.index, (int)i >= L + p.n_head_slices ? 2 : 1);
+    }
+    NvtxRange nr(ctx->nvtx, label);
     {
       SegScope sg(ctx, 0, s, 0, (int)i);
       if (it.kind == IT_LAYER) {
@@ -1697,6 +1721,8 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
   if (ts && atoi(ts) > 0) ctx->trace_sample = atoi(ts);
   const char* se = getenv("MT_SERIAL");
   ctx->serial = se && se[0] == '1';
+  const char* nv = getenv("MT_NVTX");
+  ctx->nvtx = nv && nv[0] == '1';
   const char* tl = getenv("MT_TIMELINE");
   if (tl) ctx->timeline = tl;
   auto fail = [&](int code, const char* m, cudaError_t e) {
