@@ -79,7 +79,7 @@ def lib():
         L.oracle_packed_bytes.argtypes = [P(_Cfg), i32]
         L.oracle_packed_bytes.restype = sz
         L.oracle_tensor_offset.argtypes = [P(_Cfg), i32, i32, i32, P(sz), P(sz)]
-        L.oracle_forward_backward_f32.argtypes = [P(_Cfg), vp, i32, vp, vp, i32, i32, dbl, vp, P(dbl), vp, vp, vp]
+        L.oracle_forward_backward_f32.argtypes = [P(_Cfg), vp, i32, vp, vp, i32, i32, dbl, vp, P(dbl), vp, vp, vp, vp]
         L.oracle_forward_backward_f64.argtypes = [P(_Cfg), vp, vp, vp, i32, i32, dbl, vp, P(dbl), vp, vp]
         L.oracle_matmul.argtypes = [i32, i32, vp, vp, vp, i32, i32, i32]
         L.oracle_matmul_sampled.argtypes = [i32, vp, vp, i32, i32, i32, vp, vp, ctypes.c_int64, vp]
@@ -156,13 +156,14 @@ def _routing(cfg: Config, T: int, route_in, want_route: bool):
 
 def forward_backward(cfg: Config, params: np.ndarray, tokens: np.ndarray, labels: np.ndarray, bf16: bool = False,
                      scale: float | None = None, token_losses: bool = False, route_in=None,
-                     want_route: bool = False):
+                     want_route: bool = False, want_logits: bool = False):
     """fp32 step. params: packed bytes (fp32 or bf16 layout).
 
     Returns (loss, packed fp32 grads), plus the per-position CE terms [B, S]
     when token_losses is set, plus the experts selected in every layer
-    ([L, B*S, top_k]) when want_route is set. route_in forces that selection
-    (mixture-of-experts layers only)."""
+    ([L, B*S, top_k]) when want_route is set, plus every layer's router
+    logits ([L, B*S, n_experts]) when want_logits is set. route_in forces
+    that selection (mixture-of-experts layers only)."""
     tokens = np.ascontiguousarray(tokens, dtype=np.int32)
     labels = np.ascontiguousarray(labels, dtype=np.int32)
     B, S = tokens.shape
@@ -173,8 +174,10 @@ def forward_backward(cfg: Config, params: np.ndarray, tokens: np.ndarray, labels
     c = cfg.c()
     tl = np.empty((B, S), dtype=np.float32) if token_losses else None
     rin, rout = _routing(cfg, B * S, route_in, want_route)
+    logits = np.zeros((cfg.n_layers, B * S, cfg.n_experts), dtype=np.float32) if want_logits else None
     rc = lib().oracle_forward_backward_f32(ctypes.byref(c), _p(params), 1 if bf16 else 0, _p(tokens), _p(labels),
-                                           B, S, scale, _p(grads), ctypes.byref(loss), _p(tl), _p(rin), _p(rout))
+                                           B, S, scale, _p(grads), ctypes.byref(loss), _p(tl), _p(rin), _p(rout),
+                                           _p(logits))
     if rc != 0:
         raise ValueError("oracle rejected its arguments")
     out = (loss.value, grads)
@@ -182,6 +185,8 @@ def forward_backward(cfg: Config, params: np.ndarray, tokens: np.ndarray, labels
         out += (tl,)
     if want_route:
         out += (rout,)
+    if want_logits:
+        out += (logits,)
     return out
 
 

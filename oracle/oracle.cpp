@@ -362,13 +362,16 @@ struct MoeAct {
 };
 
 // Writes out [T, h]. route_in (optional, [T, k]) replaces the selection by the
-// given experts (validated by the caller); route_out (optional) receives it.
+// given experts (validated by the caller); route_out (optional) receives it;
+// logits_out (optional, [T, E]) receives the router logits r.
 template <class S>
 void moe_fwd(const Dims& D, const S* m, const S* Wr, const S* Wgu, const S* Wd, int T, const int32_t* route_in,
-             int32_t* route_out, MoeAct<S>& A, S* out) {
+             int32_t* route_out, MoeAct<S>& A, S* out, float* logits_out = nullptr) {
   const int E = D.E, k = D.topk, Fe = D.Fe, h = D.h;
   std::vector<S> r((size_t)T * E);
   mm_nt(m, Wr, r.data(), T, E, h);
+  if (logits_out)
+    for (size_t i = 0; i < r.size(); ++i) logits_out[i] = (float)r[i];
   A.p.assign((size_t)T * E, S(0));
   A.sel.assign((size_t)T * k, 0);
   A.w.assign((size_t)T * k, S(0));
@@ -530,7 +533,7 @@ struct LayerAct {
 template <class S>
 S forward_backward(const Dims& D, const S* P, const int32_t* tok, const int32_t* lab, int B, int Sq, S scale,
                    S* G, float* tok_loss = nullptr, const int32_t* route_in = nullptr,
-                   int32_t* route_out = nullptr) {
+                   int32_t* route_out = nullptr, float* logits_out = nullptr) {
   const int T = B * Sq, h = D.h, qd = D.nq * D.d, kd = D.nkv * D.d, F = D.F, V = D.V;
   auto off = [&](int unit, int t) { return layout_offset(D, 4, unit, t) / 4; };
   const size_t total = layout_offset(D, 4, D.L + 2, 0) / 4;
@@ -566,7 +569,8 @@ S forward_backward(const Dims& D, const S* P, const int32_t* tok, const int32_t*
     if (D.E > 0) {
       const size_t rs = (size_t)T * D.topk;
       moe_fwd(D, A.m.data(), P + off(u, 6), P + off(u, 7), P + off(u, 8), T, route_in ? route_in + l * rs : nullptr,
-              route_out ? route_out + l * rs : nullptr, A.moe, tmp.data());
+              route_out ? route_out + l * rs : nullptr, A.moe, tmp.data(),
+              logits_out ? logits_out + (size_t)l * T * D.E : nullptr);
       hcur = A.hmid;
       for (size_t i = 0; i < (size_t)T * h; ++i) hcur[i] += tmp[i];
       continue;
@@ -712,13 +716,15 @@ static int check_tokens(const Dims& D, const int32_t* tok, const int32_t* lab, i
 // token_losses (optional, [B*S]): the unscaled CE term of every position.
 // Mixture-of-experts layers: route_in (optional, [L][B*S][top_k]) forces the
 // selected experts of every layer and position; route_out (optional, same
-// shape) receives the selection used.
+// shape) receives the selection used; router_logits (optional,
+// [L][B*S][n_experts]) receives every layer's router logits.
 int oracle_forward_backward_f32(const oracle_cfg* c, const void* params, int dtype, const int32_t* tokens,
                                 const int32_t* labels, int B, int S, double scale, float* grads, double* loss,
-                                float* token_losses, const int32_t* route_in, int32_t* route_out) {
+                                float* token_losses, const int32_t* route_in, int32_t* route_out,
+                                float* router_logits) {
   const Dims D = to_dims(c);
   if (!valid_dims(D) || B < 1 || S < 1 || check_tokens(D, tokens, labels, B * S)) return -1;
-  if (!valid_routing(D, route_in, B * S) || (route_out && D.E == 0)) return -1;
+  if (!valid_routing(D, route_in, B * S) || ((route_out || router_logits) && D.E == 0)) return -1;
   const size_t n32 = layout_offset(D, 4, D.L + 2, 0) / 4;
   std::vector<float> P(n32, 0.f);
   if (dtype == 0) {
@@ -734,7 +740,7 @@ int oracle_forward_backward_f32(const oracle_cfg* c, const void* params, int dty
       }
   }
   *loss = forward_backward<float>(D, P.data(), tokens, labels, B, S, (float)scale, grads, token_losses, route_in,
-                                  route_out);
+                                  route_out, router_logits);
   return 0;
 }
 
@@ -750,26 +756,22 @@ int oracle_forward_backward_f64(const oracle_cfg* c, const double* params, const
   return 0;
 }
 
+}  // extern "C"
+
 // ---- single operations (float in/out; acc selects float or double math) ----
 #define ORACLE_DISPATCH(acc, FN_F, FN_D) \
   do {                                    \
     if (acc) { FN_D; } else { FN_F; }     \
   } while (0)
 
-}  // extern "C"
 template <class S>
 static std::vector<S> widen(const float* p, size_t n) {
   return std::vector<S>(p, p + n);
 }
-extern "C" {
-}  // extern "C"
 template <class S>
 static void narrow(const std::vector<S>& v, float* p) {
   for (size_t i = 0; i < v.size(); ++i) p[i] = (float)v[i];
 }
-extern "C" {
-
-}  // extern "C"
 template <class S>
 static void op_matmul(int mode, const float* A, const float* Bm, float* Y, int M, int N, int K) {
   // mode 0: Y = A[M,K] B[N,K]^T; 1: Y = A[M,K] B[K,N]; 2: Y = A[K,M]^T B[K,N]

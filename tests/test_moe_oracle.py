@@ -217,3 +217,28 @@ def test_routing_arguments_validated():
         oracle.forward_backward(cfg, packed, tok, lab, route_in=bad)
     with pytest.raises(ValueError):
         oracle.forward_backward(DENSE, make_params(DENSE, 5), tok, lab, want_route=True)
+
+
+def test_exported_router_logits_decide_the_selection():
+    """The router logits the oracle exports are the ones its selection is
+    made from: every layer's chosen experts are the k largest exported logits
+    (ties to the lower index). A layer's logits depend on the routing of the
+    layers below it only: forcing another routing in the first layer leaves
+    its logits unchanged and changes the second layer's. A dense model has
+    no logits to export."""
+    cfg = TINY_MOE
+    packed = make_params(cfg, 61)
+    tok, lab = make_tokens(cfg, 2, 16, 62)
+    loss, _, route, logits = oracle.forward_backward(cfg, packed, tok, lab, want_route=True, want_logits=True)
+    L, T, k = route.shape
+    assert logits.shape == (L, T, cfg.n_experts)
+    for l in range(L):
+        order = np.argsort(-logits[l].astype(np.float64), axis=1, kind="stable")[:, :k]
+        assert np.array_equal(np.sort(order, axis=1), np.sort(route[l], axis=1)), l
+    forced = route.copy()
+    forced[0] = (route[0] + 1) % cfg.n_experts
+    _, _, logits2 = oracle.forward_backward(cfg, packed, tok, lab, route_in=forced, want_logits=True)
+    assert np.array_equal(logits2[0], logits[0])
+    assert not np.array_equal(logits2[1], logits[1])
+    with pytest.raises(ValueError):
+        oracle.forward_backward(DENSE, make_params(DENSE, 63), tok, lab, want_logits=True)
