@@ -266,68 +266,139 @@ def numa_pages(addrs) -> dict:
 
 
 def host_link_probe(torch, nbytes=436 * 2**20):
-    """Pinned H2D alone, D2H alone, and both at once (GB/s), CUDA events."""
+    """Pinned H2D alone, D2H alone, and both at once (GB/s), from fresh
+    torch pinned buffers. Each copy is timed with CUDA events on its own
+    stream, so the concurrent run gives one figure per direction (best of
+    five)."""
     host_a = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     host_b = torch.empty(nbytes, dtype=torch.uint8, pin_memory=True)
     dev_a = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     dev_b = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
     s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
 
-    def timed(fn, reps=5):
-        best = 1e9
+    def run(h2d, d2h, reps=5):
+        best_h = best_d = 1e9
         for _ in range(reps):
             torch.cuda.synchronize()
-            t0 = time.perf_counter()
-            fn()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            if h2d:
+                ev[0].record(s1)
+                with torch.cuda.stream(s1):
+                    dev_a.copy_(host_a, non_blocking=True)
+                ev[1].record(s1)
+            if d2h:
+                ev[2].record(s2)
+                with torch.cuda.stream(s2):
+                    host_b.copy_(dev_b, non_blocking=True)
+                ev[3].record(s2)
             torch.cuda.synchronize()
-            best = min(best, time.perf_counter() - t0)
-        return best
+            if h2d:
+                best_h = min(best_h, ev[0].elapsed_time(ev[1]) / 1e3)
+            if d2h:
+                best_d = min(best_d, ev[2].elapsed_time(ev[3]) / 1e3)
+        return best_h, best_d
 
-    def h2d():
-        with torch.cuda.stream(s1):
-            dev_a.copy_(host_a, non_blocking=True)
-
-    def d2h():
-        with torch.cuda.stream(s2):
-            host_b.copy_(dev_b, non_blocking=True)
-
-    def both():
-        h2d()
-        d2h()
-
-    t_h2d, t_d2h, t_both = timed(h2d), timed(d2h), timed(both)
+    t_h2d, _ = run(True, False)
+    _, t_d2h = run(False, True)
+    t_bh, t_bd = run(True, True)
     out = {"h2d_gbs": nbytes / t_h2d / 1e9, "d2h_gbs": nbytes / t_d2h / 1e9,
-           "h2d_concurrent_gbs": nbytes / t_both / 1e9, "d2h_concurrent_gbs": nbytes / t_both / 1e9}
+           "h2d_concurrent_gbs": nbytes / t_bh / 1e9, "d2h_concurrent_gbs": nbytes / t_bd / 1e9}
     del host_a, host_b, dev_a, dev_b
     return out
 
 
-def cpu_oracle_sample(shape, S_sample, seed=5, moe=None, eps=1e-5):
-    """Time the CPU oracle (single thread) on one decoder layer plus the head
-    of this shape at B=1, S=S_sample, and extrapolate to the full depth:
-    t(L layers) = t(1 layer + head) + (L-1) * t_layer, with t_layer taken by
-    the layer's share of the sample's work."""
+def replay_summary(r: dict) -> dict:
+    """Totals and distribution of a copy-only replay of the weight stream."""
+    g = np.asarray(r["copy_gbs"], dtype=np.float64)
+    return {"copies": r["n_copies"], "gbs": r["bytes"] / max(r["ms"], 1e-9) / 1e6,
+            "copy_gbs_min": float(g.min()) if g.size else None,
+            "copy_gbs_p10": float(np.percentile(g, 10)) if g.size else None,
+            "copy_gbs_p50": float(np.percentile(g, 50)) if g.size else None,
+            "slow_copies_below_100gbs": int(np.sum(g < 100.0))}
+
+
+def _oracle_timed_step(shape, n_layers, vocab, S, seed, moe=None, eps=1e-5):
+    """Seconds of one single-threaded oracle step of a model with the given
+    layer count and vocabulary (the workload's widths) at B=1, S."""
     import oracle
     import seedgen
     L, h, nq, nkv, d, F, V, theta = shape[:8]
     E, k, Fe = moe or (0, 0, 0)
-    cfg = oracle.Config(1, h, nq, nkv, d, F, V, theta, eps, E, k, Fe)
+    cfg = oracle.Config(n_layers, h, nq, nkv, d, F, vocab, theta, eps, E, k, Fe)
     packed = np.zeros(oracle.packed_bytes(cfg, True), np.uint8)
     offs = []
     for unit, t, name, shp, is_gain in oracle.tensor_list(cfg):
         off, nb = oracle.tensor_offset(cfg, unit, t, True)
         offs.append((unit, t, off, int(np.prod(shp)), is_gain))
     seedgen.fill_packed_params(packed.ctypes.data, offs, True, seed)
-    tok, lab = seedgen.tokens_and_labels(1, S_sample, V, seed + 1)
+    tok, lab = seedgen.tokens_and_labels(1, S, vocab, seed + 1)
     t0 = time.perf_counter()
     oracle.forward_backward(cfg, packed, tok, lab, bf16=True)
-    t1 = time.perf_counter() - t0
-    layer_f, head_f, P_lin = model_flops((1, h, nq, nkv, d, F, V), 1, S_sample, moe)
-    layer_f_plain = layer_f * 3 / 4  # the oracle does no recompute
-    frac_layer = layer_f_plain / (layer_f_plain + head_f * 3 / 4)
-    t_layer = t1 * frac_layer
-    t_full = t1 + (L - 1) * t_layer
-    return S_sample / t_full, t1
+    return time.perf_counter() - t0
+
+
+def _oracle_timed_attention(shape, S, seed):
+    """Seconds of the oracle's causal attention forward + backward over all
+    heads of one sequence of length S."""
+    import oracle
+    import seedgen
+    L, h, nq, nkv, d = shape[:5]
+    q, do = (seedgen.normal(S * nq * d, seed + i, 9, 1.0).reshape(1, S, nq, d) for i in (0, 1))
+    k, v = (seedgen.normal(S * nkv * d, seed + i, 9, 1.0).reshape(1, S, nkv, d) for i in (2, 3))
+    t0 = time.perf_counter()
+    oracle.attention(q, k, v, do)
+    return time.perf_counter() - t0
+
+
+class CpuFit:
+    """The single-threaded CPU oracle timed on pieces of one training step
+    of the workload and extrapolated to the whole step (each piece one
+    oracle call on one thread, run one after another):
+      - one decoder layer of the workload's widths with a 256-entry
+        vocabulary (head negligible) at B=1, S=S1 and S=S2: t = c0 + c1 S,
+        c0 the work done once per call (the oracle transposes every weight
+        matrix for its forward products), c1 the work per token (its loops
+        stream every weight matrix once per token in each of the forward,
+        input-gradient and weight-gradient products);
+      - causal attention forward + backward over all heads of one sequence
+        at S_attn: a S_attn^2, extrapolated quadratically in the sequence
+        length (the S1/S2 layers hold a negligible attention part);
+      - the LM head and loss: the same three loop nests over V*h weights
+        instead of the layer's P_lin, so c0 and c1 scaled by V*h / P_lin
+        (the softmax over the vocabulary adds O(V) per token, negligible).
+    step(B, S) = L (c0 + c1 T + a S^2 B) + (V h / P_lin)(c0 + c1 T), T = B S."""
+
+    def __init__(self, shape, moe=None, eps=1e-5, seed=5, S1=8, S2=40, S_attn=512):
+        self.shape, self.moe, self.eps, self.seed = shape, moe, eps, seed
+        self.S1, self.S2, self.S_attn = S1, S2, S_attn
+        t1 = _oracle_timed_step(shape, 1, 256, S1, seed, moe, eps)
+        t2 = _oracle_timed_step(shape, 1, 256, S2, seed, moe, eps)
+        self.c1 = max(0.0, (t2 - t1) / (S2 - S1))
+        self.c0 = max(0.0, t1 - self.c1 * S1)
+        self.t_attn = _oracle_timed_attention(shape, S_attn, seed)
+        self.a = self.t_attn / S_attn ** 2
+        L, h, nq, nkv, d, F, V = shape[:7]
+        self.head_ratio = V * h / layer_params(shape, moe)
+        self.cpu_seconds = t1 + t2 + self.t_attn
+
+    def step_seconds(self, B, S, scale=1.0):
+        L = self.shape[0]
+        T = B * S
+        lin = self.c0 + self.c1 * T
+        return scale * (L * (lin + self.a * S * S * B) + self.head_ratio * lin)
+
+    def resample(self):
+        """Re-time the cheapest piece (attention at S_attn); its ratio to
+        the fitted value rescales the extrapolated step."""
+        return _oracle_timed_attention(self.shape, self.S_attn, self.seed) / self.t_attn
+
+    def describe(self, B, S):
+        L = self.shape[0]
+        return (f"single-threaded fp32 oracle timed on one layer of the workload's widths (256-entry vocabulary) at "
+                f"B=1, S={self.S1} and S={self.S2} and on causal attention forward+backward over all heads at "
+                f"S={self.S_attn}; extrapolated to {L} layers and the LM head at B={B}, S={S}: linear terms linearly "
+                f"in tokens (the head as the layer's per-weight cost times V*h), attention quadratically in sequence "
+                f"length (extrapolated; {self.cpu_seconds:.1f} s of CPU work; host has {os.cpu_count()} cores)")
 
 
 def cpu_oracle_full_step(shape, B, S, seed=5, moe=None, eps=1e-5, bf16=False):
@@ -356,27 +427,28 @@ FULL_STEP_BASELINE = {"tiny"}  # workloads whose CPU baseline is a whole oracle 
 
 
 def run_reference(args, shape, B, S):
-    """The reference arm: the CPU oracle as it stands, timed on this host."""
+    """The reference arm: the CPU oracle as it stands, timed on this host.
+    The whole-step workloads time one oracle step per step; the others fit
+    the piecewise model once (CpuFit) and re-time its cheapest piece each
+    step, rescaling the extrapolated step by it."""
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    S_sample = 8
     full = args.workload in FULL_STEP_BASELINE
+    moe, eps = MOE.get(args.workload), NORM_EPS.get(args.workload, 1e-5)
     vals = []
+    fit = None if full else CpuFit(shape, moe=moe, eps=eps)
     for i in range(args.warmup + args.steps):
         if full:
-            v, t1 = cpu_oracle_full_step(shape, B, S, seed=100 + i, moe=MOE.get(args.workload),
-                                         eps=NORM_EPS.get(args.workload, 1e-5),
+            v, t1 = cpu_oracle_full_step(shape, B, S, seed=100 + i, moe=moe, eps=eps,
                                          bf16=bool(WORKLOADS[args.workload][11]))
         else:
-            v, t1 = cpu_oracle_sample(shape, S_sample, seed=100 + i, moe=MOE.get(args.workload),
-                                      eps=NORM_EPS.get(args.workload, 1e-5))
+            v = B * S / fit.step_seconds(B, S, fit.resample())
         if i >= args.warmup:
             vals.append(v)
     value = float(np.median(vals))
     sample = (f"whole step of the {args.workload} workload at B={B}, S={S}, single-threaded fp32 oracle" if full else
-              f"one decoder layer + LM head of the {args.workload} shape at B=1, S={S_sample}, single-threaded fp32 "
-              f"oracle, extrapolated linearly to {shape[0]} layers")
+              fit.describe(B, S) + "; each step re-times the attention piece and rescales by it")
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
@@ -398,6 +470,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fuse-top", action="store_true", help="recompute the top block too")
     ap.add_argument("--serial", action="store_true", help="ablation: serialise weight copies and compute")
+    ap.add_argument("--no-page-touch", action="store_true",
+                    help="ablation: no host page touches ahead of the weight copies (MT_PAGE_TOUCH=0)")
     ap.add_argument("--optimizer", nargs="?", const="sync", choices=["sync", "async"], default=None,
                     help="time train steps with the host AdamW: sync = mt_train_step (each unit updated as its "
                          "gradients land), async = mt_train_step_async (staleness 1); allocates three fp32 copies "
@@ -428,6 +502,8 @@ def main():
         os.environ["MT_FUSE_TOP_BLOCK"] = "0"
     if args.serial:
         os.environ["MT_SERIAL"] = "1"
+    if args.no_page_touch:
+        os.environ["MT_PAGE_TOUCH"] = "0"
     import torch
     torch.cuda.set_device(local)
     dist = None
@@ -484,6 +560,12 @@ def main():
     log(f"pinned pages per NUMA node: {placement}")
     link = host_link_probe(torch)
     log(f"host link {link}")
+    # the same weight stream, copies only, from the bound parameter buffer:
+    # with nothing else running, then with the host page touches of the step
+    replay_before = replay_summary(sess.replay_weight_stream(K))
+    log(f"weight-stream replay from the bound buffer: {replay_before}")
+    replay_touch = replay_summary(sess.replay_weight_stream(K, mt.MT_REPLAY_TOUCH))
+    log(f"weight-stream replay with page touches: {replay_touch}")
     for i in range(args.warmup):
         t1 = time.perf_counter()
         step_fn(tok, lab, K)
@@ -499,6 +581,7 @@ def main():
     wall0 = time.perf_counter()
     ev0.record(comp)
     losses = []
+    copy_p = []   # per step: min, p10, p50 of the weight copies' GB/s
     host_ms = []  # per step: wall time of the call minus its device span (host preparation and finishing)
     for _ in range(args.steps):
         t_call = time.perf_counter()
@@ -506,8 +589,12 @@ def main():
         call_ms = (time.perf_counter() - t_call) * 1e3
         st = sess.stats()
         host_ms.append(call_ms - st["step_ms"])
+        copy_p.append((st["h2d_copy_gbs_min"], st["h2d_copy_gbs_p10"], st["h2d_copy_gbs_p50"]))
         for k, v in st.items():
-            agg[k] = agg.get(k, 0) + v
+            if isinstance(v, list):
+                agg[k] = [a + b for a, b in zip(agg.get(k, [0.0] * len(v)), v)]
+            else:
+                agg[k] = agg.get(k, 0) + v
     ev1.record(d2h_stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -517,6 +604,9 @@ def main():
     # region, with every GEMM/attention launch bracketed by CUDA events on the
     # compute stream (events around launches stall the copy pipeline, so the
     # timed steps run without them).
+    replay_r = sess.replay_weight_stream(K)
+    replay_after = replay_summary(replay_r)
+    log(f"weight-stream replay after the timed steps: {replay_after}")
     sess.set_tracing(2, 1)
     sess.step(tok, lab, K)
     kst = sess.stats()
@@ -604,6 +694,26 @@ def main():
                           # effective rates of the step's own copies (bytes / summed copy time)
                           "h2d_copy_gbs": agg["h2d_bytes"] / max(1e-9, agg["h2d_ms"]) / 1e6,
                           "d2h_copy_gbs": agg["d2h_bytes"] / max(1e-9, agg["d2h_ms"]) / 1e6},
+        # where the copy time goes: per phase of the step, the in-step copy
+        # rates; per copy, their spread; and the same weight stream replayed
+        # with nothing beside it, from the bound buffer, before the warm-up
+        # and after the timed steps
+        "link_diagnostics": {
+            "in_step_gbs_by_phase": {
+                ph: {"h2d": (agg["h2d_phase_bytes"][i] / agg["h2d_phase_ms"][i] / 1e6) if agg["h2d_phase_ms"][i] else None,
+                     "d2h": (agg["d2h_phase_bytes"][i] / agg["d2h_phase_ms"][i] / 1e6) if agg["d2h_phase_ms"][i] else None}
+                for i, ph in enumerate(("forward", "head", "recompute", "backward"))},
+            "in_step_h2d_copy_gbs": {"min": float(np.min([c[0] for c in copy_p])),
+                                     "p10_median_over_steps": float(np.median([c[1] for c in copy_p])),
+                                     "p50_median_over_steps": float(np.median([c[2] for c in copy_p]))},
+            "replay_bound_buffer_before": replay_before,
+            "replay_bound_buffer_with_page_touch": replay_touch,
+            "replay_bound_buffer_after": replay_after,
+            "page_touch_threads": int(os.environ.get("MT_PAGE_TOUCH", "4")),
+            "page_touch_ms_per_step": agg["page_touch_ms"] / steps,
+            "probe_fresh_buffer": link,
+            "host_numa_node_of_gpu": replay_r["host_numa_node"],
+        },
         "optimizer": ({"kind": "host AdamW, " + ("per-unit as gradients land (mt_train_step)"
                                                   if args.optimizer == "sync" else
                                                   "staleness 1, units published as they land (mt_train_step_async)"),
@@ -626,10 +736,9 @@ def main():
             sample = (f"whole step of the {args.workload} workload at B={B}, S={S} ({t1:.2f} s single-threaded "
                       f"fp32 oracle); host has {os.cpu_count()} cores")
         else:
-            v, t1 = cpu_oracle_sample(shape, 8, moe=moe, eps=eps)
-            sample = (f"one decoder layer + LM head of the {args.workload} shape at B=1, S=8 ({t1:.1f} s "
-                      f"single-threaded fp32 oracle), extrapolated linearly to {L} layers; host has "
-                      f"{os.cpu_count()} cores")
+            fit = CpuFit(shape, moe=moe, eps=eps)
+            v = B * S / fit.step_seconds(B, S)
+            sample = fit.describe(B, S)
         line["cpu_baseline"] = {"value": v, "unit": "tokens/s", "cores": 1, "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
     if dist:

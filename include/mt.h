@@ -170,6 +170,21 @@ typedef struct {
    * units, measured on the optimizer thread) and the part of it after the
    * step's last device work had finished (not hidden behind the step). */
   double optimizer_ms, optimizer_exposed_ms;
+  /* Trace level >= 1: the weight copies (H2D) and gradient copies (D2H) of
+   * the step by phase, [0] forward, [1] LM head (both passes), [2] block
+   * recompute, [3] backward (the embedding rows are not counted): bytes and
+   * summed copy durations. */
+  double h2d_phase_bytes[4], h2d_phase_ms[4], d2h_phase_bytes[4], d2h_phase_ms[4];
+  /* Trace level >= 1: rates of the step's individual weight copies (GB/s),
+   * minimum, 10th, 50th and 90th percentile. */
+  double h2d_copy_gbs_min, h2d_copy_gbs_p10, h2d_copy_gbs_p50, h2d_copy_gbs_p90;
+  /* Host page toucher (env MT_PAGE_TOUCH = number of host threads, default
+   * 4, 0 = off): before each weight copy, host threads read one byte of
+   * every 4 KB page of its host range, two copies ahead of the copy stream,
+   * so that pages whose host-side mapping lapsed are restored by the CPU
+   * instead of stalling the copy engine page by page. Busiest thread's
+   * reading time in the step (ms). */
+  double page_touch_ms;
 } mt_stats;
 int mt_get_stats(const mt_ctx* ctx, mt_stats* out);
 
@@ -185,6 +200,32 @@ int mt_get_routing(const mt_ctx* ctx, int32_t* host_out, size_t n);
  * bracketed by events (kernel durations; this perturbs the step's own
  * timing, so measure step time at level 1). sample >= 1. */
 int mt_set_tracing(mt_ctx* ctx, int level, int sample);
+
+/* Copy-only replay of a step's weight stream: the host-to-device copies
+ * mt_forward_backward issues for checkpoint interval K (every layer's packed
+ * weights and every LM-head vocab slice, in the step's order, from the bound
+ * host parameters into the two device weight buffers), issued back to back
+ * on the weight-in stream with no kernels and no gradient copies beside
+ * them. flags: 0 = no host threads either; MT_REPLAY_TOUCH = with the host
+ * page toucher the step runs (one byte of every 4 KB page of each copy's
+ * host range read by host threads two copies ahead of the copy stream).
+ * Each copy is timed with CUDA events; copy_gbs_out (optional, max_copies
+ * floats) receives the rate of each copy in GB/s, in order. A diagnostic of
+ * the host link as the bound buffer sees it, apart from the step (MegaTrain,
+ * section 技术新颖性: the transfer must keep up with the compute it hides
+ * under). Synchronous; the weight buffers' contents are overwritten (the
+ * next step reloads them anyway). MT_ERR_STATE without bound parameters;
+ * MT_ERR_ARG for K outside [1, min(L, max_K)]. */
+#define MT_REPLAY_TOUCH 1
+typedef struct {
+  int32_t n_copies, reserved;
+  double bytes, ms;        /* total bytes and summed copy durations */
+  int32_t host_numa_node;  /* cudaDevAttrHostNumaId of the context's device (-1: none) */
+  int32_t reserved2;
+  double touch_ms;         /* MT_REPLAY_TOUCH: busiest toucher thread's time spent reading */
+} mt_replay_result;
+int mt_replay_weight_stream(mt_ctx* ctx, int K, int flags, float* copy_gbs_out, int max_copies,
+                            mt_replay_result* out);
 
 /* Arena partition of a context (bytes). */
 typedef struct {
@@ -243,7 +284,12 @@ int mt_train_step(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int
  * update through step k-1. host_grad_out must not be the previous call's
  * buffer (alternate two pinned buffers): that one is still being read. The
  * first call applies no update. mt_optimizer_flush applies the pending
- * update (after the last call); mt_train_step refuses while one is pending. */
+ * update (after the last call); mt_train_step refuses while one is pending.
+ * A call that fails part-way leaves the pending update pending and records,
+ * per unit, whether its update was already computed into the master and
+ * moments and whether it was already published; the next call (or the
+ * flush) completes each unit's update exactly once, never applying it
+ * twice. */
 int mt_train_step_async(mt_ctx* ctx, const int32_t* tokens, const int32_t* labels, int B, int S, int K,
                         float* host_grad_out, float* loss_out);
 int mt_optimizer_flush(mt_ctx* ctx);
@@ -311,9 +357,10 @@ int mt_op_rmsnorm_bwd(const float* x, const float* w, const float* rstd, const f
  * every GPU that loads libmt.so holds until the process exits.
  *  - Limit: ceil(T/32) * h must be <= 1,048,576 (e.g. T = 8192 tokens at
  *    h = 4096); larger sizes return MT_ERR_BUDGET before anything runs.
- *  - The first call on each device looks up the array's device address
- *    (cudaGetSymbolAddress, with that device current); make that first call
- *    before any stream capture begins.
+ *  - The first call in each CUDA context (per device) looks up the array's
+ *    device address (cudaGetSymbolAddress, with that device current) and
+ *    caches it for that context; make that first call before any stream
+ *    capture begins. A device reset or a new context gets a fresh lookup.
  *  - All calls share the one array and it keeps the last call's contents:
  *    calls whose executions overlap on the GPU (e.g. on two streams without
  *    ordering between them) race on it and give wrong results. The

@@ -45,7 +45,7 @@ EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_crea
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
            "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error",
            "mt_adamw_update", "mt_bind_optimizer", "mt_train_step", "mt_train_step_async", "mt_optimizer_flush",
-           "mt_get_routing", "mt_op_moe_workspace", "mt_op_moe_ffn_fwd", "mt_op_moe_bwd_workspace",
+           "mt_get_routing", "mt_replay_weight_stream", "mt_op_moe_workspace", "mt_op_moe_ffn_fwd", "mt_op_moe_bwd_workspace",
            "mt_op_moe_ffn_bwd")
 
 
@@ -72,7 +72,18 @@ class mt_stats(ctypes.Structure):
                 ("timing_enabled", ctypes.c_int32), ("gemm_ms", ctypes.c_double), ("gemm_flop", ctypes.c_double),
                 ("attn_ms", ctypes.c_double), ("attn_flop", ctypes.c_double), ("n_gemm", ctypes.c_int32),
                 ("n_attn", ctypes.c_int32), ("n_launches", ctypes.c_int32), ("reserved", ctypes.c_int32),
-                ("optimizer_ms", ctypes.c_double), ("optimizer_exposed_ms", ctypes.c_double)]
+                ("optimizer_ms", ctypes.c_double), ("optimizer_exposed_ms", ctypes.c_double),
+                ("h2d_phase_bytes", ctypes.c_double * 4), ("h2d_phase_ms", ctypes.c_double * 4),
+                ("d2h_phase_bytes", ctypes.c_double * 4), ("d2h_phase_ms", ctypes.c_double * 4),
+                ("h2d_copy_gbs_min", ctypes.c_double), ("h2d_copy_gbs_p10", ctypes.c_double),
+                ("h2d_copy_gbs_p50", ctypes.c_double), ("h2d_copy_gbs_p90", ctypes.c_double),
+                ("page_touch_ms", ctypes.c_double)]
+
+
+class mt_replay_result(ctypes.Structure):
+    _fields_ = [("n_copies", ctypes.c_int32), ("reserved", ctypes.c_int32), ("bytes", ctypes.c_double),
+                ("ms", ctypes.c_double), ("host_numa_node", ctypes.c_int32), ("reserved2", ctypes.c_int32),
+                ("touch_ms", ctypes.c_double)]
 
 
 class mt_adamw_cfg(ctypes.Structure):
@@ -120,6 +131,7 @@ def lib() -> ctypes.CDLL:
         "mt_adamw_update": (i32, [cfgp, P(mt_adamw_cfg), ctypes.c_int64, i32, i32, vp, vp, vp, vp, vp, i32, i32]),
         "mt_get_stats": (i32, [vp, P(mt_stats)]),
         "mt_get_routing": (i32, [vp, vp, sz]),
+        "mt_replay_weight_stream": (i32, [vp, i32, i32, vp, i32, P(mt_replay_result)]),
         "mt_set_tracing": (i32, [vp, i32, i32]),
         "mt_get_memory_plan": (i32, [vp, P(mt_memory_plan)]),
         "mt_last_error": (ctypes.c_char_p, [vp]),
@@ -263,7 +275,25 @@ def mt_adamw_update(cfg, opt: mt_adamw_cfg, step: int, unit_begin: int, unit_end
 def mt_get_stats(ctx) -> dict:
     s = mt_stats()
     _check(lib().mt_get_stats(ctx, ctypes.byref(s)), ctx)
-    return {f: getattr(s, f) for f, _ in mt_stats._fields_}
+    out = {}
+    for f, _ in mt_stats._fields_:
+        v = getattr(s, f)
+        out[f] = list(v) if isinstance(v, ctypes.Array) else v
+    return out
+
+
+MT_REPLAY_TOUCH = 1
+
+
+def mt_replay_weight_stream(ctx, K: int, flags: int = 0, max_copies: int = 4096) -> dict:
+    """Copy-only replay of the step's weight stream (see include/mt.h):
+    totals, the host NUMA node of the device and every copy's GB/s."""
+    r = mt_replay_result()
+    rates = np.zeros(max_copies, dtype=np.float32)
+    _check(lib().mt_replay_weight_stream(ctx, K, flags, rates.ctypes.data, max_copies, ctypes.byref(r)), ctx)
+    n = min(r.n_copies, max_copies)
+    return {"n_copies": r.n_copies, "bytes": r.bytes, "ms": r.ms, "host_numa_node": r.host_numa_node,
+            "touch_ms": r.touch_ms, "copy_gbs": rates[:n].astype(float).tolist()}
 
 
 def mt_get_routing(ctx, n_layers: int, T: int, top_k: int) -> np.ndarray:
@@ -415,6 +445,9 @@ class Session:
 
     def stats(self) -> dict:
         return mt_get_stats(self.ctx)
+
+    def replay_weight_stream(self, K: int, flags: int = 0) -> dict:
+        return mt_replay_weight_stream(self.ctx, K, flags)
 
     def routing(self, T: int) -> np.ndarray:
         """[n_layers, T, top_k] experts chosen in the last step of T tokens."""

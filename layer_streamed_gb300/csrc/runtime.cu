@@ -23,6 +23,7 @@
 //    result is identical; RoundPipe's "fused stage" observation).
 #include <algorithm>
 #include <chrono>
+#include <memory>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -420,6 +421,109 @@ struct OpSeg {
   double flop;
 };
 
+// Host page toucher. Reads one byte of every 4 KB of the host ranges the
+// step's copies are about to read (weights) or write (gradients), from a few
+// host threads, a fixed number of weight copies ahead of the weight stream
+// (paced on per-copy completion events). Measured on the GB300 machines: pinned
+// host pages that only the GPU accesses lose their mapping on the host side
+// after some idle time (in 4 KB units), and the copy engines then stall on
+// every such page (4-13 GB/s instead of 211 GB/s for weight copies, 28 GB/s
+// for gradient copies); a CPU read of each 4 KB page restores the mapping
+// cheaply, so the copy that follows runs at the link rate. The touches are
+// reads only: no byte of either buffer is changed.
+class PageToucher {
+ public:
+  struct Range {
+    const uint8_t* p;
+    size_t bytes;
+    int wait;  // touch once weight copy `wait` has completed (-1: at once)
+  };
+  PageToucher() = default;
+  PageToucher(const PageToucher&) = delete;
+  PageToucher& operator=(const PageToucher&) = delete;
+  ~PageToucher() { stop(); }
+
+  // Touch ranges[0..] in order with nthreads threads (each a contiguous part
+  // of every range); range r waits for weight copy r.wait (of n_copies) to
+  // complete.
+  void start(std::vector<Range> ranges, size_t n_copies, int nthreads, int device) {
+    r_ = std::move(ranges);
+    ev_.assign(n_copies, nullptr);
+    touched_.reset(new std::atomic<int>[r_.size() + 1]);
+    for (size_t j = 0; j <= r_.size(); ++j) touched_[j] = 0;
+    n_ = std::max(1, nthreads);
+    busy_.assign(n_, 0.0);
+    for (int w = 0; w < n_; ++w) th_.emplace_back([this, w, device] { run(w, device); });
+  }
+  // Weight copy j has been issued; `done` completes with it (copies are
+  // published in order).
+  void published(size_t j, cudaEvent_t done) {
+    if (j >= ev_.size()) return;
+    ev_[j] = done;
+    published_.store(j + 1, std::memory_order_release);
+  }
+  // Wait (bounded) until every thread has touched range j.
+  bool wait_touched(size_t j, double seconds) {
+    if (th_.empty() || j >= r_.size()) return true;
+    const auto t0 = std::chrono::steady_clock::now();
+    while (touched_[j].load(std::memory_order_acquire) < n_) {
+      if (std::chrono::duration<double>(std::chrono::steady_clock::now() - t0).count() > seconds) return false;
+      std::this_thread::sleep_for(std::chrono::microseconds(20));
+    }
+    return true;
+  }
+  void stop() {
+    stop_ = true;
+    for (auto& t : th_)
+      if (t.joinable()) t.join();
+    th_.clear();
+  }
+  double busy_ms() const {
+    double b = 0;
+    for (double x : busy_) b = std::max(b, x);
+    return b;
+  }
+
+ private:
+  void run(int w, int device) {
+    cudaSetDevice(device);
+    double busy = 0;
+    uint64_t acc = 0;
+    for (size_t j = 0; j < r_.size() && !stop_; ++j) {
+      if (r_[j].wait >= 0 && (size_t)r_[j].wait < ev_.size()) {
+        const size_t k = (size_t)r_[j].wait;
+        while (published_.load(std::memory_order_acquire) <= k) {
+          if (stop_) return;
+          std::this_thread::sleep_for(std::chrono::microseconds(20));
+        }
+        while (cudaEventQuery(ev_[k]) == cudaErrorNotReady) {
+          if (stop_) return;
+          std::this_thread::sleep_for(std::chrono::microseconds(50));
+        }
+      }
+      const auto t0 = std::chrono::steady_clock::now();
+      const size_t pages = (r_[j].bytes + 4095) / 4096;
+      const size_t per = (pages + n_ - 1) / n_;
+      const volatile uint8_t* q = r_[j].p;
+      for (size_t pg = (size_t)w * per; pg < std::min(pages, (size_t)(w + 1) * per); ++pg) acc += q[pg * 4096];
+      busy += std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
+      touched_[j].fetch_add(1, std::memory_order_release);
+    }
+    cudaGetLastError();
+    busy_[w] = busy;
+    sink_ += acc;
+  }
+  std::vector<Range> r_;
+  std::vector<cudaEvent_t> ev_;
+  std::unique_ptr<std::atomic<int>[]> touched_;
+  std::atomic<size_t> published_{0};
+  std::atomic<bool> stop_{false};
+  std::atomic<uint64_t> sink_{0};
+  std::vector<std::thread> th_;
+  std::vector<double> busy_;
+  int n_ = 1;
+};
+
 }  // namespace
 
 struct mt_ctx {
@@ -436,8 +540,13 @@ struct mt_ctx {
   int opt_threads = 0;
   int64_t opt_step = 1;
   // asynchronous form (mt_train_step_async): gradients of the previous call,
-  // whose update is applied during the next call
+  // whose update is applied during the next call, and per unit how far that
+  // update has gone (0 not computed, 1 computed into the master and
+  // moments, 2 also published to the streamed copy), so that a call that
+  // fails part-way is completed by the next call or mt_optimizer_flush
+  // without applying any unit's update twice
   const float* opt_pending = nullptr;
+  std::vector<uint8_t> opt_state;
   cudaEvent_t ev_wready[2], ev_wfree[2], ev_bwd_done[2], ev_gfree[2], ev_done = nullptr;
   uint8_t* arena = nullptr;
   size_t arena_bytes = 0;
@@ -483,10 +592,13 @@ struct mt_ctx {
   size_t ev_used = 0;
   cudaEvent_t ev_base = nullptr;
   int fault_kind = 0, fault_nth = 0, fault_count = 0;
-  // resident weight slots
-  Item slot_item[2];
-  bool slot_valid[2];
   int gslot = 0;
+  // phase of every position of the step's unit sequence (0 forward, 1 LM
+  // head, 2 recompute, 3 backward) and the position being issued, for the
+  // per-phase copy statistics
+  std::vector<int8_t> unit_phase;
+  int cur_unit = -1;
+  int touch_threads = 4;  // host page toucher threads (MT_PAGE_TOUCH; 0: off)
 };
 
 namespace {
@@ -733,6 +845,8 @@ struct Step {
   bool train = false;                 // apply the optimizer as gradients land
   bool async = false;                 // apply the previous step's update, publishing units as they land
   std::vector<cudaEvent_t> landed;    // per unit (train steps): its gradients are on the host
+  std::vector<int> load_index;        // per position of seq: index among the step's weight copies (-1: none)
+  PageToucher* toucher = nullptr;
 };
 
 void plan_sequence(Step& st) {
@@ -771,24 +885,65 @@ void plan_sequence(Step& st) {
   }
 }
 
+// Host byte range (offset into the bound parameters, bytes) that one use of
+// a streamed unit copies: a layer's packed weights, or an LM-head vocab slice.
+void load_range(const mt_ctx* ctx, const Item& it, size_t* src_off, size_t* bytes) {
+  const Plan& p = ctx->P;
+  if (it.kind == IT_LAYER) {
+    const int l = std::abs(it.index);
+    *src_off = ctx->off_p[l][0];
+    *bytes = ctx->off_p[l][8] + tensor_numel(ctx->cfg, l, 8) * p.esz - *src_off;
+  } else {
+    const int r0 = it.index * p.head_rows, rows = std::min(p.head_rows, p.V - r0);
+    *src_off = ctx->off_p[p.L + 1][1] + (size_t)r0 * p.h * p.esz;
+    *bytes = (size_t)rows * p.h * p.esz;
+  }
+}
+
+// Host ranges to touch ahead of the step's copies, in the order the copies
+// use them: each weight copy's source, paced two weight copies ahead of it,
+// and (when grad_out is given) each gradient copy's destination next to the
+// weight copy that precedes the unit producing it. index receives, per
+// position of the unit sequence, its weight copy's index (-1: none);
+// *n_copies the number of weight copies.
+std::vector<PageToucher::Range> touch_plan(const mt_ctx* ctx, const Step& st, const uint8_t* grad_out,
+                                           std::vector<int>* index, size_t* n_copies) {
+  const Plan& p = ctx->P;
+  std::vector<PageToucher::Range> r;
+  index->assign(st.seq.size(), -1);
+  int copies = 0, last = -1;
+  for (size_t i = 0; i < st.seq.size(); ++i) {
+    const Item& it = st.seq[i];
+    if (st.needs_load[i]) {
+      size_t off, bytes;
+      load_range(ctx, it, &off, &bytes);
+      last = copies++;
+      (*index)[i] = last;
+      r.push_back({(const uint8_t*)ctx->host_params + off, bytes, last - 2});
+    }
+    if (!grad_out) continue;
+    const bool pass2 = it.kind == IT_HEAD && (int)i >= p.L + p.n_head_slices;
+    if (it.kind == IT_LAYER && it.index < 0) {  // a layer's backward: its whole gradient unit
+      const int l = -it.index;
+      const size_t g0 = ctx->off_g[l][0], g1 = ctx->off_g[l][8] + tensor_numel(ctx->cfg, l, 8) * p.gesz;
+      r.push_back({grad_out + g0, g1 - g0, last - 2});
+    } else if (pass2) {  // a head slice's weight gradient
+      const int r0 = it.index * p.head_rows, rows = std::min(p.head_rows, p.V - r0);
+      r.push_back({grad_out + ctx->off_g[p.L + 1][1] + (size_t)r0 * p.h * p.gesz, (size_t)rows * p.h * p.gesz,
+                   last - 2});
+    }
+  }
+  *n_copies = (size_t)copies;
+  return r;
+}
+
 // H2D copy of step i's weights into its slot (weight stream).
 int issue_load(Step& st, size_t i) {
   mt_ctx* ctx = st.ctx;
-  const Plan& p = ctx->P;
-  const Item it = st.seq[i];
   const int slot = st.slot_of[i];
   const uint8_t* hp = (const uint8_t*)ctx->host_params;
   size_t src_off = 0, bytes = 0;
-  const int L = p.L;
-  if (it.kind == IT_LAYER) {
-    const int l = std::abs(it.index);
-    src_off = ctx->off_p[l][0];
-    bytes = ctx->off_p[l][8] + tensor_numel(ctx->cfg, l, 8) * p.esz - src_off;
-  } else {
-    const int r0 = it.index * p.head_rows, rows = std::min(p.head_rows, p.V - r0);
-    src_off = ctx->off_p[L + 1][1] + (size_t)r0 * p.h * p.esz;
-    bytes = (size_t)rows * p.h * p.esz;
-  }
+  load_range(ctx, st.seq[i], &src_off, &bytes);
   if (ctx->fault_kind == 1 && ++ctx->fault_count == ctx->fault_nth)
     return set_err(ctx, MT_ERR_CUDA, "injected copy-issue failure");
   CK(cudaStreamWaitEvent(ctx->s_h2d, ctx->ev_wfree[slot], 0));
@@ -798,6 +953,12 @@ int issue_load(Step& st, size_t i) {
     CK(cudaMemcpyAsync(ctx->wbuf[slot], hp + src_off, bytes, cudaMemcpyHostToDevice, ctx->s_h2d));
   }
   CK(cudaEventRecord(ctx->ev_wready[slot], ctx->s_h2d));
+  if (st.toucher && st.load_index[i] >= 0) {
+    cudaEvent_t done = next_event(ctx);
+    if (!done) return set_err(ctx, MT_ERR_CUDA, "event pool");
+    CK(cudaEventRecord(done, ctx->s_h2d));
+    st.toucher->published((size_t)st.load_index[i], done);
+  }
   ctx->stats.h2d_bytes += (double)bytes;
   ctx->stats.n_h2d += 1;
   return MT_OK;
@@ -971,7 +1132,7 @@ int grad_slot_end(Step& st, int g, size_t host_off, size_t bytes) {
   CK(cudaEventRecord(ctx->ev_bwd_done[g], ctx->s_comp));
   CK(cudaStreamWaitEvent(ctx->s_d2h, ctx->ev_bwd_done[g], 0));
   {
-    SegScope sg(ctx, 2, ctx->s_d2h, (double)bytes);
+    SegScope sg(ctx, 2, ctx->s_d2h, (double)bytes, ctx->cur_unit);
     CK(cudaMemcpyAsync((uint8_t*)st.host_grad + host_off, ctx->gbuf[g], bytes, cudaMemcpyDeviceToHost, ctx->s_d2h));
   }
   CK(cudaEventRecord(ctx->ev_gfree[g], ctx->s_d2h));
@@ -995,7 +1156,7 @@ int grad_piece(Step& st, int g, int l, int t0, int t1) {
   CK(cudaStreamWaitEvent(ctx->s_d2h, ready, 0));
   const size_t gesz = ctx->P.gesz;
   const size_t span = ctx->off_g[l][t1] + tensor_numel(ctx->cfg, l, t1) * gesz - ctx->off_g[l][t0];
-  SegScope sg(ctx, 2, ctx->s_d2h, (double)span);
+  SegScope sg(ctx, 2, ctx->s_d2h, (double)span, ctx->cur_unit);
   for (int t = t0; t <= t1; ++t) {
     const size_t off = ctx->off_g[l][t], nb = tensor_numel(ctx->cfg, l, t) * gesz;
     CK(cudaMemcpyAsync((uint8_t*)st.host_grad + off, (const uint8_t*)ctx->gbuf[g] + (off - u0), nb,
@@ -1236,8 +1397,11 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       const auto t0 = std::chrono::steady_clock::now();
       for (int u = L + 1; u >= 0; --u) {  // the order in which this step's units become publishable
         if (arun.abort) return;
-        adamw_units(ctx->cfg, ctx->off_g, ctx->off_p, p.esz, coef, u, u + 1, ctx->opt_master, ctx->opt_m,
-                    ctx->opt_v, ctx->opt_pending, nullptr, nthr);
+        if (ctx->opt_state[u] == 0) {  // not yet computed (by an earlier call that failed part-way)
+          adamw_units(ctx->cfg, ctx->off_g, ctx->off_p, p.esz, coef, u, u + 1, ctx->opt_master, ctx->opt_m,
+                      ctx->opt_v, ctx->opt_pending, nullptr, nthr);
+          ctx->opt_state[u] = 1;
+        }
         arun.done[u] = 1;
       }
       arun.busy_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t0).count();
@@ -1305,6 +1469,24 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   plan_sequence(st);
   const size_t n = st.seq.size();
   ctx->stats.n_units = (int)n;
+  ctx->unit_phase.assign(n + 1, 3);  // position n: the embedding gradient (backward)
+  for (size_t i = 0; i < n; ++i) {
+    const Item& it = st.seq[i];
+    ctx->unit_phase[i] = it.kind == IT_HEAD ? 1 : it.index < 0 ? 3 : (int)i < L ? 0 : 2;
+  }
+  ctx->cur_unit = -1;
+  // Host pages of the weight copies are touched two copies ahead of the
+  // copy stream; the first copy waits (bounded) for its own pages.
+  PageToucher toucher;
+  if (ctx->touch_threads > 0) {
+    size_t n_copies = 0;
+    std::vector<PageToucher::Range> plan = touch_plan(ctx, st, (const uint8_t*)st.host_grad, &st.load_index, &n_copies);
+    // the embedding gradient rows land in the context's own pinned staging
+    plan.push_back({(const uint8_t*)ctx->host_grad_rows, (size_t)n_ids * h * 4, (int)n_copies - 2});
+    toucher.start(std::move(plan), n_copies, ctx->touch_threads, ctx->device);
+    st.toucher = &toucher;
+    toucher.wait_touched(0, 2.0);
+  }
   if (st.needs_load[0]) CKR(issue_load(st, 0));
 
   // Embedding: h_0 = E[tok]. CPU threads gather the T rows from the host
@@ -1352,6 +1534,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
     const Item it = st.seq[i];
     const int slot = st.slot_of[i];
     const bool fresh = st.needs_load[i];
+    ctx->cur_unit = (int)i;
     if (fresh) CK(cudaStreamWaitEvent(s, ctx->ev_wready[slot], 0));
     char label[48] = "";
     if (ctx->nvtx) {
@@ -1444,6 +1627,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
         return true;
       };
       for (int u = L + 1; u >= 0; --u) {
+        if (ctx->opt_state[u] == 2) continue;  // published by an earlier call that failed part-way
         bool ok = true;
         if (u >= 1) {
           ok = wait_until([&] {
@@ -1464,6 +1648,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
         }
         publish_units(ctx->cfg, ctx->off_g, ctx->off_p, p.esz, u, u + 1, ctx->opt_master,
                       const_cast<void*>(ctx->host_params), nthr);
+        ctx->opt_state[u] = 2;
       }
     });
   }
@@ -1521,7 +1706,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   CK(cudaEventRecord(emb_done, s));
   CK(cudaStreamWaitEvent(ctx->s_d2h, emb_done, 0));
   {
-    SegScope sg(ctx, 2, ctx->s_d2h, (double)n_ids * h * 4);
+    SegScope sg(ctx, 2, ctx->s_d2h, (double)n_ids * h * 4, (int)n);
     CK(cudaMemcpyAsync(ctx->host_grad_rows, ctx->dm, (size_t)n_ids * h * 4, cudaMemcpyDeviceToHost, ctx->s_d2h));
   }
   ctx->stats.d2h_bytes += (double)n_ids * h * 4;
@@ -1536,6 +1721,8 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   CK(cudaEventRecord(ctx->ev_done, ctx->s_d2h));
   CKR(wait_event(ctx, ctx->ev_done, 3600.0));
   *loss_out = *loss_host;
+  toucher.stop();
+  ctx->stats.page_touch_ms = toucher.busy_ms();
   // Scatter the embedding gradient rows into the (now cleared) host buffer.
   for (auto& x : zeroers) x.join();
   {
@@ -1607,6 +1794,7 @@ void compute_stats(mt_ctx* ctx) {
     double a, b;
   };
   std::vector<Iv> comp, h2d, d2h;
+  std::vector<double> rates;  // GB/s of each weight copy
   double end = 0;
   for (auto& sg : ctx->segs) {
     float ta = 0, tb = 0;
@@ -1617,6 +1805,20 @@ void compute_stats(mt_ctx* ctx) {
     if (sg.stream == 0) comp.push_back(v);
     else if (sg.stream == 1) h2d.push_back(v);
     else d2h.push_back(v);
+    if (sg.stream != 0 && sg.unit >= 0 && sg.unit < (int)ctx->unit_phase.size()) {
+      const int ph = ctx->unit_phase[sg.unit];
+      (sg.stream == 1 ? ctx->stats.h2d_phase_bytes : ctx->stats.d2h_phase_bytes)[ph] += sg.bytes;
+      (sg.stream == 1 ? ctx->stats.h2d_phase_ms : ctx->stats.d2h_phase_ms)[ph] += tb - ta;
+      if (sg.stream == 1 && tb > ta) rates.push_back(sg.bytes / ((tb - ta) * 1e6));
+    }
+  }
+  if (!rates.empty()) {
+    std::sort(rates.begin(), rates.end());
+    auto pct = [&](double q) { return rates[std::min(rates.size() - 1, (size_t)(q * (rates.size() - 1) + 0.5))]; };
+    ctx->stats.h2d_copy_gbs_min = rates.front();
+    ctx->stats.h2d_copy_gbs_p10 = pct(0.1);
+    ctx->stats.h2d_copy_gbs_p50 = pct(0.5);
+    ctx->stats.h2d_copy_gbs_p90 = pct(0.9);
   }
   if (!ctx->timeline.empty()) {
     FILE* f = fopen(ctx->timeline.c_str(), "w");
@@ -1725,6 +1927,8 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
   ctx->nvtx = nv && nv[0] == '1';
   const char* tl = getenv("MT_TIMELINE");
   if (tl) ctx->timeline = tl;
+  const char* pt = getenv("MT_PAGE_TOUCH");
+  if (pt) ctx->touch_threads = std::max(0, std::min(64, atoi(pt)));
   auto fail = [&](int code, const char* m, cudaError_t e) {
     fprintf(stderr, "mt_create: %s: %s\n", m, cudaGetErrorString(e));
     mt_destroy(ctx);
@@ -1837,9 +2041,12 @@ int mt_train_step_async(mt_ctx* ctx, const int32_t* tokens, const int32_t* label
     return set_err(ctx, MT_ERR_ARG, "the previous call's gradient buffer is still being read; alternate two buffers");
   const bool pending = ctx->opt_pending != nullptr;
   const int rc = step_common(ctx, tokens, labels, B, S, K, host_grad_out, loss_out, false, true);
+  // On failure the pending update stays pending: opt_state records the units
+  // already computed or published, which the next call or the flush skips.
   if (rc != MT_OK) return rc;
   if (pending) ctx->opt_step += 1;
   ctx->opt_pending = host_grad_out;
+  ctx->opt_state.assign((size_t)ctx->cfg.n_layers + 2, 0);
   return MT_OK;
 }
 
@@ -1849,10 +2056,18 @@ int mt_optimizer_flush(mt_ctx* ctx) {
   if (!ctx->opt_pending) return MT_OK;
   const int nthr = ctx->opt_threads > 0 ? ctx->opt_threads : (int)std::max(1u, std::thread::hardware_concurrency());
   const int L = ctx->cfg.n_layers;
-  adamw_units(ctx->cfg, ctx->off_g, ctx->off_p, ctx->P.esz, adam_coef(ctx->opt, ctx->opt_step), 0, L + 2,
-              ctx->opt_master, ctx->opt_m, ctx->opt_v, ctx->opt_pending, const_cast<void*>(ctx->host_params), nthr);
+  const AdamCoef coef = adam_coef(ctx->opt, ctx->opt_step);
+  for (int u = 0; u < L + 2; ++u) {
+    if (ctx->opt_state[u] == 0)  // compute and publish
+      adamw_units(ctx->cfg, ctx->off_g, ctx->off_p, ctx->P.esz, coef, u, u + 1, ctx->opt_master, ctx->opt_m,
+                  ctx->opt_v, ctx->opt_pending, const_cast<void*>(ctx->host_params), nthr);
+    else if (ctx->opt_state[u] == 1)  // computed by a call that failed before publishing it
+      publish_units(ctx->cfg, ctx->off_g, ctx->off_p, ctx->P.esz, u, u + 1, ctx->opt_master,
+                    const_cast<void*>(ctx->host_params), nthr);
+  }
   ctx->opt_step += 1;
   ctx->opt_pending = nullptr;
+  ctx->opt_state.assign((size_t)L + 2, 0);
   return MT_OK;
 }
 
@@ -1870,6 +2085,7 @@ int mt_bind_optimizer(mt_ctx* ctx, const mt_adamw_cfg* opt, float* master, float
   ctx->opt_threads = n_threads;
   ctx->opt_step = 1;
   ctx->opt_pending = nullptr;
+  ctx->opt_state.assign((size_t)ctx->cfg.n_layers + 2, 0);
   ctx->opt_bound = true;
   return MT_OK;
 }
@@ -1965,6 +2181,70 @@ int mt_get_stats(const mt_ctx* ctx, mt_stats* out) {
   if (!ctx || !out) return MT_ERR_ARG;
   *out = ctx->stats;
   return MT_OK;
+}
+
+int mt_replay_weight_stream(mt_ctx* ctx, int K, int flags, float* copy_gbs_out, int max_copies,
+                            mt_replay_result* out) {
+  if (!ctx || !out || max_copies < 0) return set_err(ctx, MT_ERR_ARG, "null argument");
+  if (!ctx->host_params) return set_err(ctx, MT_ERR_STATE, "no parameters bound");
+  if (K < 1 || K > ctx->cfg.max_K || K > ctx->cfg.n_layers) return set_err(ctx, MT_ERR_ARG, "K outside [1, min(L, max_K)]");
+  *out = mt_replay_result{};
+  int node = -1;
+  if (cudaDeviceGetAttribute(&node, cudaDevAttrHostNumaId, ctx->device) != cudaSuccess) node = -1;
+  cudaGetLastError();
+  out->host_numa_node = node;
+  int cur = 0;
+  cudaGetDevice(&cur);
+  if (cur != ctx->device) cudaSetDevice(ctx->device);
+  Step st{ctx, 1, 1, 1, K, (ctx->cfg.n_layers + K - 1) / K, nullptr, {}, {}, {}, false, false, {}};
+  plan_sequence(st);
+  const uint8_t* hp = (const uint8_t*)ctx->host_params;
+  std::vector<std::pair<cudaEvent_t, cudaEvent_t>> ev;
+  std::vector<double> bytes;
+  PageToucher toucher;
+  std::vector<int> load_index;
+  if (flags & MT_REPLAY_TOUCH) {
+    size_t n_copies = 0;
+    std::vector<PageToucher::Range> plan = touch_plan(ctx, st, nullptr, &load_index, &n_copies);
+    toucher.start(std::move(plan), n_copies, std::max(1, ctx->touch_threads), ctx->device);
+    toucher.wait_touched(0, 2.0);
+  }
+  int rc = MT_OK;
+  for (size_t i = 0; i < st.seq.size() && rc == MT_OK; ++i) {
+    if (!st.needs_load[i]) continue;
+    size_t src_off, nb;
+    load_range(ctx, st.seq[i], &src_off, &nb);
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
+      if (a) cudaEventDestroy(a);
+      rc = set_err(ctx, MT_ERR_CUDA, "event create");
+      break;
+    }
+    ev.push_back({a, b});
+    bytes.push_back((double)nb);
+    if (cudaEventRecord(a, ctx->s_h2d) != cudaSuccess ||
+        cudaMemcpyAsync(ctx->wbuf[st.slot_of[i]], hp + src_off, nb, cudaMemcpyHostToDevice, ctx->s_h2d) != cudaSuccess ||
+        cudaEventRecord(b, ctx->s_h2d) != cudaSuccess)
+      rc = set_err(ctx, MT_ERR_CUDA, std::string("replay copy: ") + cudaGetErrorString(cudaGetLastError()));
+    if (flags & MT_REPLAY_TOUCH) toucher.published((size_t)load_index[i], b);
+  }
+  if (cudaStreamSynchronize(ctx->s_h2d) != cudaSuccess && rc == MT_OK)
+    rc = set_err(ctx, MT_ERR_CUDA, std::string("replay: ") + cudaGetErrorString(cudaGetLastError()));
+  for (size_t i = 0; i < ev.size(); ++i) {
+    float ms = 0;
+    if (rc == MT_OK && cudaEventElapsedTime(&ms, ev[i].first, ev[i].second) == cudaSuccess) {
+      out->bytes += bytes[i];
+      out->ms += ms;
+      if (copy_gbs_out && (int)i < max_copies) copy_gbs_out[i] = ms > 0 ? (float)(bytes[i] / (ms * 1e6)) : 0.f;
+    }
+    cudaEventDestroy(ev[i].first);
+    cudaEventDestroy(ev[i].second);
+  }
+  toucher.stop();
+  out->n_copies = (int32_t)ev.size();
+  out->touch_ms = toucher.busy_ms();
+  if (cur != ctx->device) cudaSetDevice(cur);
+  return rc;
 }
 
 int mt_set_tracing(mt_ctx* ctx, int level, int sample) {
