@@ -1,11 +1,14 @@
 // Bandwidth-bound kernels of the layer template: RMSNorm forward/backward,
-// RoPE, SwiGLU forward/backward, embedding gather / deterministic
+// RoPE, SwiGLU forward/backward, the embedding gradient's deterministic
 // scatter-add, weight casts, and the cross-entropy reductions of the loss
 // anchor ("MegaTrain", section 方法步骤详情, stage 2: loss and head gradient).
 // All global accesses are 128-bit and coalesced where the shapes allow;
 // reductions are warp shuffles plus a fixed-order cross-warp step, so every
 // result is bitwise reproducible run to run.
 #include <mutex>
+#include <vector>
+
+#include <cuda.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -35,27 +38,47 @@ __device__ __forceinline__ void store_bf16x4(uint16_t* dst, float a, float b, fl
 }
 
 // ---------------------------------------------------------------------------
-// RMSNorm forward: one block per row.
+// RMSNorm forward: a 128-thread block per row; each thread loads its V float4
+// of the row once into registers (all of a row's loads are in flight
+// together), the block reduces the sum of squares, and the same registers
+// produce the bf16 output, so x is read from memory once. Up to 16 blocks
+// share an SM, which keeps enough rows' loads in flight to cover HBM latency.
 // ---------------------------------------------------------------------------
-__global__ void rmsnorm_fwd_kernel(const float* __restrict__ x, const float* __restrict__ w, uint16_t* __restrict__ y,
-                                   float* __restrict__ rstd, int h, float eps) {
-  __shared__ float red[32];
+constexpr int kNormFwdThreads = 128;
+
+template <int V>
+__global__ void __launch_bounds__(kNormFwdThreads) rmsnorm_fwd_kernel(const float* __restrict__ x,
+                                                                     const float* __restrict__ w,
+                                                                     uint16_t* __restrict__ y,
+                                                                     float* __restrict__ rstd, int h, float eps) {
+  __shared__ float red[kNormFwdThreads / 32];
   const size_t t = blockIdx.x;
   const float4* xr = (const float4*)(x + t * h);
   const float4* w4 = (const float4*)w;
-  const int n4 = h >> 2;
+  const int n4 = h >> 2, tid = threadIdx.x;
+  float4 v[V];
   float ss = 0.f;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    const float4 v = xr[i];
-    ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int i = tid + k * kNormFwdThreads;
+    v[k] = i < n4 ? __ldcs(xr + i) : make_float4(0.f, 0.f, 0.f, 0.f);
   }
-  ss = block_sum(ss, red);
+#pragma unroll
+  for (int k = 0; k < V; ++k) ss += v[k].x * v[k].x + v[k].y * v[k].y + v[k].z * v[k].z + v[k].w * v[k].w;
+  ss = warp_sum(ss);
+  if ((tid & 31) == 0) red[tid >> 5] = ss;
+  __syncthreads();
+  ss = (red[0] + red[1]) + (red[2] + red[3]);
   const float r = rsqrtf(ss / (float)h + eps);
-  if (threadIdx.x == 0) rstd[t] = r;
+  if (tid == 0) rstd[t] = r;
   uint16_t* yr = y + t * h;
-  for (int i = threadIdx.x; i < n4; i += blockDim.x) {
-    const float4 v = xr[i], g = w4[i];
-    store_bf16x4(yr + 4 * i, v.x * r * g.x, v.y * r * g.y, v.z * r * g.z, v.w * r * g.w);
+#pragma unroll
+  for (int k = 0; k < V; ++k) {
+    const int i = tid + k * kNormFwdThreads;
+    if (i < n4) {
+      const float4 g = w4[i];
+      store_bf16x4(yr + 4 * i, v[k].x * r * g.x, v[k].y * r * g.y, v[k].z * r * g.z, v[k].w * r * g.w);
+    }
   }
 }
 
@@ -314,39 +337,6 @@ __global__ void swiglu_bwd_kernel(uint16_t* gu, const uint16_t* __restrict__ dac
 // ---------------------------------------------------------------------------
 // Embedding
 // ---------------------------------------------------------------------------
-__global__ void embed_gather_kernel(const void* __restrict__ E, int bf16, int row0, int rows,
-                                    const int32_t* __restrict__ tok, float* __restrict__ h0, int h) {
-  const int t = blockIdx.x;
-  const int v = tok[t] - row0;
-  if (v < 0 || v >= rows) return;
-  float4* dst = (float4*)(h0 + (size_t)t * h);
-  for (int i = threadIdx.x; i < h / 4; i += blockDim.x) {
-    if (bf16) {
-      const uint2 u = ((const uint2*)((const uint16_t*)E + (size_t)v * h))[i];
-      dst[i] = make_float4(bf2f(u.x & 0xffff), bf2f(u.x >> 16), bf2f(u.y & 0xffff), bf2f(u.y >> 16));
-    } else {
-      dst[i] = ((const float4*)((const float*)E + (size_t)v * h))[i];
-    }
-  }
-}
-
-__global__ void embed_scatter_kernel(const int32_t* __restrict__ perm, const int32_t* __restrict__ start, int row0,
-                                     const float* __restrict__ dh0, float* __restrict__ dE, int h) {
-  const int r = blockIdx.x;
-  const int s0 = start[row0 + r], s1 = start[row0 + r + 1];
-  float4* dst = (float4*)(dE + (size_t)r * h);
-  for (int i = threadIdx.x; i < h / 4; i += blockDim.x) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int j = s0; j < s1; ++j) {
-      const float4 g = ((const float4*)(dh0 + (size_t)perm[j] * h))[i];
-      acc.x += g.x;
-      acc.y += g.y;
-      acc.z += g.z;
-      acc.w += g.w;
-    }
-    dst[i] = acc;
-  }
-}
 
 // Compact form: one block per distinct token id u (rows perm[start[u] ..
 // start[u+1]) in ascending position order); the row sum goes to row u of
@@ -522,8 +512,13 @@ inline unsigned blocks_for(size_t n, int threads) { return (unsigned)((n + threa
 }  // namespace
 
 int rmsnorm_fwd(const float* x, const float* w, uint16_t* y, float* rstd, int T, int h, float eps, cudaStream_t st) {
-  if (T <= 0 || h <= 0 || (h & 3)) return -1;
-  rmsnorm_fwd_kernel<<<T, kThreads, 0, st>>>(x, w, y, rstd, h, eps);
+  if (T <= 0 || h <= 0 || (h & 3) || h > 16 * 4 * kNormFwdThreads) return -1;
+  const int n4 = h / 4;
+  if (n4 <= kNormFwdThreads) rmsnorm_fwd_kernel<1><<<T, kNormFwdThreads, 0, st>>>(x, w, y, rstd, h, eps);
+  else if (n4 <= 2 * kNormFwdThreads) rmsnorm_fwd_kernel<2><<<T, kNormFwdThreads, 0, st>>>(x, w, y, rstd, h, eps);
+  else if (n4 <= 4 * kNormFwdThreads) rmsnorm_fwd_kernel<4><<<T, kNormFwdThreads, 0, st>>>(x, w, y, rstd, h, eps);
+  else if (n4 <= 8 * kNormFwdThreads) rmsnorm_fwd_kernel<8><<<T, kNormFwdThreads, 0, st>>>(x, w, y, rstd, h, eps);
+  else rmsnorm_fwd_kernel<16><<<T, kNormFwdThreads, 0, st>>>(x, w, y, rstd, h, eps);
   count_launches(1);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
@@ -582,21 +577,6 @@ int swiglu_bwd(uint16_t* gu, const uint16_t* dact, int T, int F, int ld, cudaStr
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }
 
-int embed_gather(const void* E_slice, bool bf16, int row0, int rows, const int32_t* tok, float* h0, int T, int h,
-                 cudaStream_t st) {
-  if (T <= 0 || (h & 3)) return -1;
-  embed_gather_kernel<<<T, 256, 0, st>>>(E_slice, bf16 ? 1 : 0, row0, rows, tok, h0, h);
-  count_launches(1);
-  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
-}
-
-int embed_scatter(const int32_t* perm, const int32_t* start, int row0, int rows, const float* dh0, float* dE, int h,
-                  cudaStream_t st) {
-  if (rows <= 0 || (h & 3)) return -1;
-  embed_scatter_kernel<<<rows, 256, 0, st>>>(perm, start, row0, dh0, dE, h);
-  count_launches(1);
-  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
-}
 
 int embed_scatter_rows(const int32_t* perm, const int32_t* start, int n_ids, const float* dh0, float* rows, int h,
                        cudaStream_t st) {
@@ -666,28 +646,64 @@ int ce_slice_grad(const float* logits, int T, int R, int ld, int row0, const int
 // of the gain gradient) lives in a fixed array in this library's device
 // image instead of a caller buffer. Every GPU that loads the library keeps
 // the array (4 MiB) until the process exits. Host code cannot use the
-// array's name as a device address, so the address is looked up once per
-// device with cudaGetSymbolAddress (on the first call on that device, with
-// that device current) and cached.
+// array's name as a device address, so the address is looked up with
+// cudaGetSymbolAddress (with the device current) the first time the entry
+// point runs in a given CUDA context, and cached per (device, context): the
+// address belongs to the context, so a device reset or another context on
+// the same device gets a lookup of its own.
 // ---------------------------------------------------------------------------
 namespace {
 constexpr size_t kNoAllocPartials = (size_t)1 << 20;  // floats: ceil(T/32) * h must not exceed this
 __device__ __align__(256) float g_norm_bwd_scratch[kNoAllocPartials];
 
-constexpr int kMaxDevices = 64;
-float* g_scratch_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+  int dev;
+  unsigned long long ctx_id;  // cuCtxGetId: unique over the process's lifetime, never reused
+  float* ptr;
+};
+std::vector<ScratchEntry> g_scratch_cache;
 std::mutex g_scratch_mu;
+
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+template <class Fn>
+Fn driver_fn(const char* name) {
+  void* f = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion(name, &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess)
+    f = nullptr;
+  cudaGetLastError();
+  return (Fn)f;
+}
+
+// The current context's unique id, or false if the driver cannot tell.
+bool current_ctx_id(unsigned long long* id) {
+  static const CtxGetCurrentFn get_current = driver_fn<CtxGetCurrentFn>("cuCtxGetCurrent");
+  static const CtxGetIdFn get_id = driver_fn<CtxGetIdFn>("cuCtxGetId");
+  CUcontext c = nullptr;
+  return get_current && get_id && get_current(&c) == CUDA_SUCCESS && c && get_id(c, id) == CUDA_SUCCESS;
+}
 
 int scratch_for_current_device(float** out) {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+  unsigned long long id = 0;
+  const bool keyed = current_ctx_id(&id);
   std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_norm_bwd_scratch) != cudaSuccess || !p) return -1;
-    g_scratch_ptr[dev] = (float*)p;
+  if (keyed)
+    for (const ScratchEntry& e : g_scratch_cache)
+      if (e.dev == dev && e.ctx_id == id) {
+        *out = e.ptr;
+        return 0;
+      }
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_norm_bwd_scratch) != cudaSuccess || !p) return -1;
+  if (keyed) {
+    if (g_scratch_cache.size() >= 256) g_scratch_cache.erase(g_scratch_cache.begin());
+    g_scratch_cache.push_back({dev, id, (float*)p});
   }
-  *out = g_scratch_ptr[dev];
+  *out = (float*)p;  // without a context id the address is looked up on every call
   return 0;
 }
 }  // namespace

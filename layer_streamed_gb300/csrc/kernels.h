@@ -111,14 +111,6 @@ int moe_unpermute(const float* dxp, const int32_t* spos, int T, int k, int h, fl
 int moe_router_bwd(const float* w, const float* dw, const int32_t* sel, int T, int k, int E, uint16_t* dr,
                    cudaStream_t st);
 
-// Embedding rows [row0, row0+rows) of E (fp32 or bf16, row stride h):
-// h0[t] = E[tok[t]] for tokens in range.
-int embed_gather(const void* E_slice, bool bf16, int row0, int rows, const int32_t* tok, float* h0, int T, int h,
-                 cudaStream_t st);
-// dE[v - row0] = sum over t with tok[t] = v (in ascending t) of dh0[t], for
-// every v in the slice; perm/start: tokens stably sorted by id (CSR over vocab).
-int embed_scatter(const int32_t* perm, const int32_t* start, int row0, int rows, const float* dh0, float* dE, int h,
-                  cudaStream_t st);
 
 // Compact form over the n_ids distinct token ids: rows[u] = sum over the
 // positions perm[start[u] .. start[u+1]) of dh0 ([n_ids, h] fp32 output).

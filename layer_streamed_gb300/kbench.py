@@ -1,6 +1,7 @@
 """Kernel benchmark CLI: time one layer-template kernel at a given shape.
 
   python -m layer_streamed_gb300.kbench gemm --mode nt --M 8192 --N 28672 --K 4096 [--reps 20]
+  python -m layer_streamed_gb300.kbench gemm --shape dm        (one of the 8B step's GEMM launches)
   python -m layer_streamed_gb300.kbench attn --B 2 --S 4096 --heads 32 --kv-heads 8 --head-dim 128 [--bwd]
   python -m layer_streamed_gb300.kbench norm --T 8192 --h 4096 [--bwd]
   python -m layer_streamed_gb300.kbench moe --T 4096 --h 4096 --experts 128 --top-k 8 --expert-ffn 1536
@@ -33,18 +34,67 @@ def _time(fn, reps: int, warmup: int = 3) -> float:
     return a.elapsed_time(b) / reps
 
 
+# The GEMM launches of one decoder layer of the 8B step (T = 8192 tokens,
+# hidden 4096, q|k|v 6144, FFN 14336) and of one LM-head vocab slice (42752
+# rows): name -> (mode, M, N, K, output / fused epilogue), N counting the
+# columns the launch writes (gate-up: g and u).
+STEP_SHAPES_8B = {
+    "qkv_rope": ("nt", 8192, 6144, 4096, "rope"),
+    "o_proj": ("nt", 8192, 4096, 4096, "f32add"),
+    "gate_up": ("nt", 8192, 28672, 4096, "gated"),
+    "down": ("nt", 8192, 4096, 14336, "f32add"),
+    "dWd": ("tn", 4096, 14336, 8192, "f32"),
+    "dact_swiglu": ("nn", 8192, 14336, 4096, "swiglu_bwd"),
+    "dWgu": ("tn", 28672, 4096, 8192, "f32"),
+    "dm": ("nn", 8192, 4096, 28672, "f32"),
+    "dWo": ("tn", 4096, 4096, 8192, "f32"),
+    "do": ("nn", 8192, 4096, 4096, "bf16"),
+    "dWqkv": ("tn", 6144, 4096, 8192, "f32"),
+    "dx": ("nn", 8192, 4096, 6144, "f32"),
+    "head_logits": ("nt", 8192, 42752, 4096, "f32"),
+    "head_dX": ("nn", 8192, 4096, 42752, "f32add"),
+    "head_dW": ("tn", 42752, 4096, 8192, "f32"),
+}
+# Launches of each in one step at the 8B configuration (32 layers, K = 4,
+# top block not recomputed: 60 forward passes of a layer, 32 backward; three
+# vocab slices, each with two logits passes, one dX and one dW product).
+STEP_LAUNCHES_8B = {"qkv_rope": 60, "o_proj": 60, "gate_up": 60, "down": 60, "dWd": 32, "dact_swiglu": 32,
+                    "dWgu": 32, "dm": 32, "dWo": 32, "do": 32, "dWqkv": 32, "dx": 32, "head_logits": 6,
+                    "head_dX": 3, "head_dW": 3}
+
+
 def bench_gemm(args) -> dict:
+    if args.shape:
+        args.mode, args.M, args.N, args.K, args.out = STEP_SHAPES_8B[args.shape]
     M, N, K = args.M, args.N, args.K
     mode = {"nt": mt.MT_GEMM_NT, "nn": mt.MT_GEMM_NN, "tn": mt.MT_GEMM_TN}[args.mode]
     a_shape = (M, K) if args.mode in ("nt", "nn") else (K, M)
     b_shape = (N, K) if args.mode == "nt" else (K, N)
     A = torch.randn(a_shape, device="cuda").to(torch.bfloat16)
     B = (torch.randn(b_shape, device="cuda") * 0.02).to(torch.bfloat16)
-    epi = {"bf16": mt.MT_EPI_BF16, "f32": mt.MT_EPI_F32}[args.out]
-    C = torch.empty((M, N), device="cuda", dtype=torch.bfloat16 if args.out == "bf16" else torch.float32)
-    ms = _time(lambda: mt.mt_op_gemm(mode, epi, A, B, C, None, M, N, K, a_shape[1], b_shape[1], N), args.reps)
+    out = args.out
+    if out in ("bf16", "f32", "f32add"):
+        epi = {"bf16": mt.MT_EPI_BF16, "f32": mt.MT_EPI_F32, "f32add": mt.MT_EPI_F32_ADD}[out]
+        C = torch.empty((M, N), device="cuda", dtype=torch.bfloat16 if out == "bf16" else torch.float32)
+        add = torch.randn((M, N), device="cuda") if out == "f32add" else None
+        fn = lambda: mt.mt_op_gemm(mode, epi, A, B, C, add, M, N, K, a_shape[1], b_shape[1], N)
+    elif out == "rope":  # q|k|v with RoPE on the first (n_q + n_kv) heads of 128 (S = 4096 per sequence)
+        C = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+        tab = torch.empty(4096 * 128, device="cuda")
+        fn = lambda: mt.mt_op_gemm_rope(A, B, C, M, N, K, K, K, N, tab, 4096, 128, 5e5, N - 1024)
+    elif out == "gated":  # g|u with act = silu(g) u: N = 2F
+        F = N // 2
+        GU = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+        ACT = torch.empty((M, F), device="cuda", dtype=torch.bfloat16)
+        fn = lambda: mt.mt_op_gemm_swiglu(A, B, GU, ACT, M, F, K, K, K, F)
+    elif out == "swiglu_bwd":  # d(act) = dY Wd turned into (dg, du) over g|u in place: N = F
+        GU = torch.randn((M, 2 * N), device="cuda").to(torch.bfloat16)
+        fn = lambda: mt.mt_op_gemm_swiglu_bwd(A, B, GU, M, N, K, K, N, N)
+    else:
+        raise SystemExit(f"unknown output {out}")
+    ms = _time(fn, args.reps)
     flop = 2.0 * M * N * K
-    return {"kernel": "gemm", "mode": args.mode, "M": M, "N": N, "K": K, "out": args.out, "ms": ms,
+    return {"kernel": "gemm", "shape": args.shape, "mode": args.mode, "M": M, "N": N, "K": K, "out": out, "ms": ms,
             "tflops": flop / ms / 1e9}
 
 
@@ -119,7 +169,9 @@ def main():
     g.add_argument("--M", type=int, default=8192)
     g.add_argument("--N", type=int, default=28672)
     g.add_argument("--K", type=int, default=4096)
-    g.add_argument("--out", default="bf16", choices=["bf16", "f32"])
+    g.add_argument("--out", default="bf16", choices=["bf16", "f32", "f32add", "rope", "gated", "swiglu_bwd"])
+    g.add_argument("--shape", default=None, choices=sorted(STEP_SHAPES_8B),
+                   help="one of the 8B step's GEMM launches (sets mode, M, N, K and the epilogue)")
     g.add_argument("--reps", type=int, default=20)
     a = sub.add_parser("attn")
     a.add_argument("--B", type=int, default=2)

@@ -156,3 +156,40 @@ def test_async_steps_follow_the_staleness_one_schedule():
         update(3, grads[2])
         for x, y in zip((s.params, master, m, v), final):
             assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
+
+
+@pytest.mark.parametrize("kind,nth", [(1, 3), (2, 1)], ids=["copy_issue_fails", "final_wait_times_out"])
+def test_failed_async_step_applies_the_pending_update_once(kind, nth):
+    """An asynchronous step that fails part-way (a host-side injected fault:
+    the third weight-copy issue fails, or the final wait times out while the
+    GPU and the publisher are still working) leaves its pending update
+    pending; the flush that follows completes it, and every unit's update is
+    applied exactly once: master, moments and streamed parameters equal one
+    mt_adamw_update of the first step's gradients."""
+    torch, mt = need_gpu()
+    cfg = with_layers(TINY_GQA, 3)
+    shape = mt.ModelShape(cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim,
+                          cfg.vocab, cfg.rope_theta, cfg.norm_eps)
+    tok0, lab0 = make_tokens(cfg, 2, 32, 60)
+    tok1, lab1 = make_tokens(cfg, 2, 32, 61)
+    packed = make_params(cfg, 62)
+    opt = mt.adamw_cfg(3e-3, 0.9, 0.999, 1e-8, 0.01)
+    units = cfg.n_layers + 2
+    with mt.Session(shape, 2, 32, 2, mt.MT_F32) as s:
+        s.params[:] = packed
+        s.bind_optimizer(opt, _master_f32(cfg, packed, False), n_threads=3)
+        s.train_step_async(tok0, lab0, 2)
+        g0 = s.grads.copy()
+        mt.mt_debug_inject_fault(s.ctx, kind, nth)
+        with pytest.raises(mt.MtError):
+            s.train_step_async(tok1, lab1, 2)
+        mt.mt_debug_inject_fault(s.ctx, 0, 0)
+        s.optimizer_flush()
+        got = (s.params.copy(), s.opt_master.copy(), s.opt_m.copy(), s.opt_v.copy())
+    master = _master_f32(cfg, packed, False)
+    m, v = np.zeros_like(master), np.zeros_like(master)
+    params = packed.copy()
+    mt.mt_adamw_update(s.cfg, opt, 1, 0, units, master.ctypes.data, m.ctypes.data, v.ctypes.data, g0.ctypes.data,
+                       params.ctypes.data, mt.MT_F32, 2)
+    for x, y in zip((params, master, m, v), got):
+        assert np.array_equal(np.asarray(x).view(np.uint8), np.asarray(y).view(np.uint8))
