@@ -232,14 +232,30 @@ def head_slice_rows(shape, esz, moe=None):
         ns += 1
 
 
-# DRAM traffic of the GEMM launches of one 8B step (B=2, S=4096, K=4), from
-# ncu (dram__bytes_read.sum + dram__bytes_write.sum over the 508 GEMM launches
-# of the second step of `python bench.py --steps 1 --warmup 1
-# --no-cpu-baseline`, cold cache between launches): 621.2 GB with the GEMM
-# kernels as committed with that capture (earlier captures on other boxes and
-# kernel builds: 566.4 and 687.9 GB).
-GEMM_TRAFFIC_8B_STEP = 621.2e9
-GEMM_LAUNCHES_8B_STEP = 508
+# DRAM bytes (read + written) of each GEMM launch of the 8B step, one launch
+# of each shape captured cold-cache by ncu (dram__bytes_read.sum +
+# dram__bytes_write.sum) with `kbench gemm --shape <name>`; the summary,
+# commands and algorithmic bytes are in
+# profiles/gemm_dram_traffic_8b_step_shapes.md. Taken with the GEMM kernels
+# as committed with that summary; when the GEMM kernels change, the figure
+# must be captured again.
+GEMM_TRAFFIC_8B = {
+    "qkv_rope": 296457728, "o_proj": 495506688, "gate_up": 1647651072, "down": 1476332800, "dWd": 1072178432,
+    "dact_swiglu": 1457163008, "dWgu": 2729005312, "dm": 2535826688, "dWo": 332630272, "do": 201263104,
+    "dWqkv": 521314560, "dx": 546606336, "head_logits": 2647050752, "head_dX": 4271706624, "head_dW": 4829711104,
+}
+# Launches of each per step at the 8B configuration (32 layers, K=4, top
+# block not recomputed; three vocab slices of the head).
+GEMM_LAUNCHES_8B = {"qkv_rope": 60, "o_proj": 60, "gate_up": 60, "down": 60, "dWd": 32, "dact_swiglu": 32,
+                    "dWgu": 32, "dm": 32, "dWo": 32, "do": 32, "dWqkv": 32, "dx": 32, "head_logits": 6,
+                    "head_dX": 3, "head_dW": 3}
+
+
+def gemm_traffic_per_launch_8b() -> float:
+    """DRAM bytes per GEMM launch of one 8B step: the per-shape captures
+    weighted by each shape's launches."""
+    n = sum(GEMM_LAUNCHES_8B.values())
+    return sum(GEMM_TRAFFIC_8B[k] * GEMM_LAUNCHES_8B[k] for k in GEMM_LAUNCHES_8B) / n
 
 
 def numa_pages(addrs) -> dict:
@@ -649,7 +665,7 @@ def main():
     else:
         gemm_bytes, gemm_launches = gemm_algorithmic_bytes(shape, B, S, K, rows, fuse_top=not args.no_fuse_top)
     traffic_known = (args.workload == "llama8b" and (L, B, S, K) == (32, 2, 4096, 4) and bf16
-                     and not args.no_fuse_top and kst["n_gemm"] == GEMM_LAUNCHES_8B_STEP)
+                     and not args.no_fuse_top and kst["n_gemm"] == sum(GEMM_LAUNCHES_8B.values()))
     line = {
         "metric": METRIC,
         "value": value,
@@ -675,8 +691,9 @@ def main():
         "gpu_launches": int(agg["n_launches"]),
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": peak_tf, "unit": "TFLOP/s",
                      "frac": (gemm_tflops / peak_tf) if gemm_tflops else None,
-                     "traffic": (GEMM_TRAFFIC_8B_STEP / GEMM_LAUNCHES_8B_STEP) if traffic_known else None,
-                     "traffic_unit": "bytes per launch (ncu, cold cache)",
+                     "traffic": gemm_traffic_per_launch_8b() if traffic_known else None,
+                     "traffic_unit": "bytes per launch (ncu, cold cache, per-shape captures weighted by the "
+                                     "step's launches)",
                      "algorithmic_bytes_per_launch": gemm_bytes / max(1, gemm_launches),
                      "kernel": "gemm_pair_kernel / gemm_kernel (tcgen05; all GEMM launches of one step, "
                                "event-timed per launch)",
