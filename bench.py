@@ -492,6 +492,9 @@ def main():
                     help="time train steps with the host AdamW: sync = mt_train_step (each unit updated as its "
                          "gradients land), async = mt_train_step_async (staleness 1); allocates three fp32 copies "
                          "of the model on the host, so use it with --layers at the 8B widths")
+    ap.add_argument("--param-dtype", default=None, choices=["bf16", "fp8"],
+                    help="host weight format of the bf16 workloads: bf16 (the default) or fp8 (E4M3 codes with one "
+                         "scale per row, dequantised to bf16 on the device: half the streamed weight bytes)")
     ap.add_argument("--grad-dtype", default="fp32", choices=["fp32", "bf16"],
                     help="dtype of the streamed host gradients (bf16 halves the D2H bytes)")
     ap.add_argument("--layers", type=int, default=None, help="diagnostic override of the layer count")
@@ -507,6 +510,9 @@ def main():
         wl[8] = args.batch
     shape, (B, S, K, bf16) = tuple(wl[:8]), wl[8:]
     K = min(K, shape[0])
+    fp8 = args.param_dtype == "fp8"
+    if fp8 and not bf16:
+        sys.exit("--param-dtype fp8 applies to the bf16 workloads")
     if args.impl == "reference":
         return run_reference(args, shape, B, S)
 
@@ -537,26 +543,33 @@ def main():
     grad_dtype = mt.MT_BF16 if args.grad_dtype == "bf16" else mt.MT_F32
     if args.optimizer and grad_dtype != mt.MT_F32:
         sys.exit("the host optimizer takes fp32 gradients")
-    cfg = mt.make_cfg(L, h, nq, nkv, d, F, V, theta, eps, B, S, K, mt.MT_BF16 if bf16 else mt.MT_F32, E, k_top, Fe,
-                      grad_dtype)
+    pdt = mt.MT_FP8 if fp8 else (mt.MT_BF16 if bf16 else mt.MT_F32)
+    cfg = mt.make_cfg(L, h, nq, nkv, d, F, V, theta, eps, B, S, K, pdt, E, k_top, Fe, grad_dtype)
     budget = mt.mt_required_budget(cfg)
     log(f"workload {args.workload} L={L} B={B} S={S} K={K}: device arena {budget / 2**30:.2f} GiB")
     arena = torch.empty(budget, dtype=torch.uint8, device="cuda")
     streams = [torch.cuda.Stream() for _ in range(3)]
     sess = mt.Session(mt.ModelShape(L, h, nq, nkv, d, F, V, theta, eps, E, k_top, Fe), B, S, K,
-                      mt.MT_BF16 if bf16 else mt.MT_F32, device_budget=budget, device_arena=arena.data_ptr(),
+                      pdt, device_budget=budget, device_arena=arena.data_ptr(),
                       streams=[s.cuda_stream for s in streams], grad_dtype=grad_dtype)
     # Parameters: N(0, 0.02) matrices, unit RMSNorm gains, per-rank seed.
     offs = []
+    fill_dt = mt.MT_BF16 if bf16 else mt.MT_F32  # FP8 params are quantised from seeded bf16 values
     for unit in range(L + 2):
         nt = 1 if unit == 0 else (9 if unit <= L else 2)
         for t in range(nt):
-            off, nbytes = sess.offset(unit, t)
+            off, nbytes = sess.offset(unit, t, fill_dt)
             is_gain = (unit >= 1 and unit <= L and t in (0, 5)) or (unit == L + 1 and t == 0)
             offs.append((unit, t, off, nbytes // (2 if bf16 else 4), is_gain))
     log(f"context created; pinned host params {sess.param_bytes / 2**30:.2f} GiB, grads {sess.grad_bytes / 2**30:.2f} GiB")
     t0 = time.perf_counter()
-    seedgen.fill_packed_params(sess.params_ptr, offs, bf16, seed=21 + rank)
+    if fp8:
+        src = np.zeros(mt.mt_packed_bytes(cfg, mt.MT_BF16), np.uint8)
+        seedgen.fill_packed_params(src.ctypes.data, offs, True, seed=21 + rank)
+        mt.mt_quantize_params_fp8(cfg, src.ctypes.data, mt.MT_BF16, sess.params_ptr, 0)
+        del src
+    else:
+        seedgen.fill_packed_params(sess.params_ptr, offs, bf16, seed=21 + rank)
     init_s = time.perf_counter() - t0
     tok, lab = seedgen.tokens_and_labels(B, S, V, seed=22 + rank)
 
@@ -681,7 +694,8 @@ def main():
         "data": "synthetic",
         "config": {"workload": args.workload, "global_batch": B * world, "seq_len": S, "checkpoint_every": K,
                    "layers": L, "hidden": h, "heads": f"{nq}q/{nkv}kv x {d}", "ffn": F, "vocab": V,
-                   "host_params": "bf16" if bf16 else "fp32", "host_grads": args.grad_dtype,
+                   "host_params": "fp8 (E4M3, row scales)" if fp8 else ("bf16" if bf16 else "fp32"),
+                   "host_grads": args.grad_dtype,
                    "parallelism": f"replicas x{world}",
                    **({"experts": f"{E} x SwiGLU {Fe}, top-{k_top}, softmax router"} if moe else {}),
                    "l2": "inputs larger than L2 (every step streams all weights from host)",

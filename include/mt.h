@@ -50,14 +50,15 @@ typedef enum {
   MT_ERR_DEVICE = -9       /* a kernel reported an internal error through the device error word */
 } mt_status;
 
-typedef enum { MT_F32 = 0, MT_BF16 = 1 } mt_dtype;
+typedef enum { MT_F32 = 0, MT_BF16 = 1, MT_FP8 = 2 } mt_dtype;
 
 /* Model and capacity description.
  * Shapes: hidden h, n_heads query heads and n_kv_heads key/value heads of
  * head_dim d (n_heads % n_kv_heads == 0; query head j reads KV head
  * j / (n_heads / n_kv_heads)), SwiGLU FFN width ffn_dim, untied vocab.
  * Supported: h % 64 == 0, d in {16, 32, 64, 128}, for MT_BF16 params
- * ffn_dim % 8 == 0; any ffn_dim >= 1 for MT_F32 params.
+ * ffn_dim % 8 == 0; any ffn_dim >= 1 for MT_F32 params; for MT_FP8 params
+ * (dense layers only) ffn_dim % 16 == 0.
  * max_batch * max_seq bounds the tokens of one call; max_K bounds the
  * checkpoint interval. param_dtype is the dtype of the host parameters that
  * will be bound. n_experts = top_k = expert_ffn = 0: dense SwiGLU FFN.
@@ -98,12 +99,33 @@ typedef struct mt_ctx mt_ctx;
  *  unit L+1      : 0 w_final_norm[h], 1 W_out[vocab, h]
  * Matrices are row-major [out, in] (y = x W^T). Every tensor starts on a
  * 256-byte boundary, every unit on a 4096-byte boundary. The gradient buffer
- * uses the same layout with grad_dtype elements (fp32 by default). */
+ * uses the same layout with grad_dtype elements (fp32 by default).
+ *
+ * MT_FP8 (opt-in weight-streaming variant, "use lower precision formats such
+ * as FP8 to further reduce the PCIe bandwidth pressure", MegaTrain, section
+ * 未来方向): every matrix tensor is its FP8 E4M3 codes, row-major [rows,
+ * cols] (one byte each), followed at the next 16-byte boundary by one fp32
+ * scale per row; the RMSNorm gains are fp32. The weight the step computes
+ * with is bf16(e4m3(code) * scale) (fp32 product, then round to nearest
+ * even), formed on the device for layers and head slices and on the host
+ * for the embedding rows. Half the streamed bytes of bf16. Gradients stay
+ * fp32 (or bf16) in their own layout; the host optimizer does not publish
+ * FP8 (MT_ERR_UNSUPPORTED). */
 size_t mt_packed_bytes(const mt_layer_cfg* cfg, mt_dtype dtype);
 
 /* Byte offset and byte size of tensor `tensor` of unit `unit` in the packed
  * layout of `dtype`. Returns MT_ERR_ARG for an unknown unit/tensor. */
 int mt_tensor_offset(const mt_layer_cfg* cfg, mt_dtype dtype, int unit, int tensor, size_t* off, size_t* bytes);
+
+/* Quantise a packed model (layout of src_dtype, MT_F32 or MT_BF16) into the
+ * MT_FP8 layout: per matrix row, scale = max|w| / 448 (1 for an all-zero
+ * row) and each code the E4M3 value nearest to w / scale (ties to even,
+ * saturating at 448); gains copied as fp32. dst: mt_packed_bytes(cfg,
+ * MT_FP8) bytes. Host threads (0 = one per core); needs no GPU.
+ * MT_ERR_ARG for a non-finite weight or bad arguments, MT_ERR_UNSUPPORTED for
+ * mixture-of-experts layers. */
+int mt_quantize_params_fp8(const mt_layer_cfg* cfg, const void* src, mt_dtype src_dtype, void* dst,
+                           int32_t n_threads);
 
 /* Device bytes a context needs for cfg (all K in [1, max_K], batches up to
  * max_batch x max_seq): two weight buffers, two gradient staging buffers,

@@ -27,7 +27,7 @@ LIB_PATH = os.path.join(_HERE, "libmt.so")
 
 MT_OK, MT_ERR_ARG, MT_ERR_BUDGET, MT_ERR_NOT_PINNED, MT_ERR_ALIGN = 0, -1, -2, -3, -4
 MT_ERR_CUDA, MT_ERR_TIMEOUT, MT_ERR_STATE, MT_ERR_UNSUPPORTED, MT_ERR_DEVICE = -5, -6, -7, -8, -9
-MT_F32, MT_BF16 = 0, 1
+MT_F32, MT_BF16, MT_FP8 = 0, 1, 2
 MT_GEMM_NT, MT_GEMM_NN, MT_GEMM_TN = 0, 1, 2
 MT_EPI_BF16, MT_EPI_F32, MT_EPI_F32_ADD = 0, 1, 2
 
@@ -45,7 +45,7 @@ EXPORTS = ("mt_packed_bytes", "mt_tensor_offset", "mt_required_budget", "mt_crea
            "mt_op_attention_fwd", "mt_op_attention_bwd_workspace", "mt_op_attention_bwd", "mt_op_swiglu_fwd",
            "mt_op_swiglu_bwd", "mt_op_lmhead_ce_workspace", "mt_op_lmhead_ce", "mt_op_device_error",
            "mt_adamw_update", "mt_bind_optimizer", "mt_train_step", "mt_train_step_async", "mt_optimizer_flush",
-           "mt_get_routing", "mt_replay_weight_stream", "mt_op_moe_workspace", "mt_op_moe_ffn_fwd", "mt_op_moe_bwd_workspace",
+           "mt_get_routing", "mt_replay_weight_stream", "mt_quantize_params_fp8", "mt_op_moe_workspace", "mt_op_moe_ffn_fwd", "mt_op_moe_bwd_workspace",
            "mt_op_moe_ffn_bwd")
 
 
@@ -132,6 +132,7 @@ def lib() -> ctypes.CDLL:
         "mt_get_stats": (i32, [vp, P(mt_stats)]),
         "mt_get_routing": (i32, [vp, vp, sz]),
         "mt_replay_weight_stream": (i32, [vp, i32, i32, vp, i32, P(mt_replay_result)]),
+        "mt_quantize_params_fp8": (i32, [cfgp, vp, i32, vp, i32]),
         "mt_set_tracing": (i32, [vp, i32, i32]),
         "mt_get_memory_plan": (i32, [vp, P(mt_memory_plan)]),
         "mt_last_error": (ctypes.c_char_p, [vp]),
@@ -283,6 +284,12 @@ def mt_get_stats(ctx) -> dict:
 
 
 MT_REPLAY_TOUCH = 1
+
+
+def mt_quantize_params_fp8(cfg, src: int, src_dtype: int, dst: int, n_threads: int = 0) -> None:
+    """Quantise a packed fp32/bf16 model at host address src into the FP8
+    layout at dst (mt_packed_bytes(cfg, MT_FP8) bytes); see include/mt.h."""
+    _check(lib().mt_quantize_params_fp8(ctypes.byref(cfg), src, src_dtype, dst, n_threads))
 
 
 def mt_replay_weight_stream(ctx, K: int, flags: int = 0, max_copies: int = 4096) -> dict:

@@ -5,10 +5,12 @@
 // All global accesses are 128-bit and coalesced where the shapes allow;
 // reductions are warp shuffles plus a fixed-order cross-warp step, so every
 // result is bitwise reproducible run to run.
+#include <algorithm>
 #include <mutex>
 #include <vector>
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -591,6 +593,50 @@ int cast_rows_f32_bf16(const float* src, uint16_t* dst, int rows_src, int rows_d
   if (rows_src <= 0 || rows_dst < rows_src || cols <= 0 || ld_dst < cols) return -1;
   cast_rows_kernel<<<blocks_for((size_t)rows_dst * ld_dst, 256), 256, 0, st>>>(src, dst, rows_src, rows_dst, cols,
                                                                                ld_dst);
+  count_launches(1);
+  return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
+}
+
+// FP8 weights (e4m3, one fp32 scale per row) to bf16: dst[r][c] =
+// bf16(float(q[r][c]) * scale[r]), the product rounded to fp32 and then to
+// bf16, both to nearest even. Every e4m3 value is exact in f16, so the
+// conversion e4m3 -> f16 -> f32 is exact. A thread converts 16 codes (one
+// 16-byte load, two 16-byte stores); cols % 16 == 0.
+__global__ void dequant_fp8_rows_kernel(const uint8_t* __restrict__ q, const float* __restrict__ scales, int rows,
+                                        int cols, uint16_t* __restrict__ dst, int ld_dst) {
+  const int c16 = cols >> 4;
+  const size_t n = (size_t)rows * c16;
+  for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n; i += (size_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / c16), c = (int)(i % c16) * 16;
+    const uint4 v = __ldcs((const uint4*)(q + (size_t)r * cols + c));
+    const float s = scales[r];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint16_t pair = (uint16_t)(w[k] >> (16 * hh));
+        uint32_t h2;
+        asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"(pair));
+        const float lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xffffu)));
+        const float hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
+        o[2 * k + hh] = pack_bf2(__fmul_rn(lo, s), __fmul_rn(hi, s));
+      }
+    uint4* d = (uint4*)(dst + (size_t)r * ld_dst + c);
+    d[0] = make_uint4(o[0], o[1], o[2], o[3]);
+    d[1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+}
+
+int dequant_fp8_rows(const uint8_t* q, const float* scales, int rows, int cols, uint16_t* dst, int ld_dst,
+                     cudaStream_t st) {
+  if (rows <= 0 || cols <= 0 || (cols & 15) || ld_dst < cols || (ld_dst & 7) || ((uintptr_t)q & 15) ||
+      ((uintptr_t)dst & 15) || ((uintptr_t)scales & 3))
+    return -1;
+  const size_t n = (size_t)rows * (cols / 16);
+  const unsigned blocks = (unsigned)std::min<size_t>((n + 255) / 256, (size_t)mt_host::num_sms() * 8);
+  dequant_fp8_rows_kernel<<<blocks, 256, 0, st>>>(q, scales, rows, cols, dst, ld_dst);
   count_launches(1);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
 }

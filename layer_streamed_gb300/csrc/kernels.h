@@ -123,6 +123,11 @@ int cast_bf16_f32(const uint16_t* src, float* dst, size_t n, cudaStream_t st);
 int cast_rows_f32_bf16(const float* src, uint16_t* dst, int rows_src, int rows_dst, int cols, int ld_dst,
                        cudaStream_t st);
 int gains_to_f32(const void* src, bool bf16, float* dst, int n, cudaStream_t st);
+// FP8 e4m3 rows with one fp32 scale per row to bf16 (dst row stride ld_dst):
+// dst[r][c] = bf16(float(q[r][c]) * scales[r]); cols % 16 == 0, q and dst
+// 16-byte aligned.
+int dequant_fp8_rows(const uint8_t* q, const float* scales, int rows, int cols, uint16_t* dst, int ld_dst,
+                     cudaStream_t st);
 
 // Cross-entropy over vocab slices of materialised fp32 logits [T, R] (row
 // stride ld): per-row (max, sum exp) partials, merged in slice order.

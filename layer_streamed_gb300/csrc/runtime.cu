@@ -82,7 +82,30 @@ size_t tensor_numel(const mt_layer_cfg& c, int u, int t) {
   }
 }
 
-// offsets[u][t] in bytes for element size esz; returns total bytes.
+bool is_gain(const mt_layer_cfg& c, int u, int t) {
+  return (u >= 1 && u <= c.n_layers && (t == 0 || t == 5)) || (u == c.n_layers + 1 && t == 0);
+}
+
+// Columns (the reduction width) of a matrix tensor of a dense model.
+size_t tensor_cols(const mt_layer_cfg& c, int u, int t) {
+  if (u >= 1 && u <= c.n_layers && t == 4) return (size_t)c.n_heads * c.head_dim;  // Wo[h, qd]
+  if (u >= 1 && u <= c.n_layers && t == 8) return (size_t)c.ffn_dim;              // Wd[h, F]
+  return (size_t)c.hidden;
+}
+
+// Bytes of one packed tensor. esz 4 / 2: fp32 / bf16 elements. esz 1: the
+// FP8 layout: every matrix is its e4m3 codes, row-major [rows, cols], then
+// (at the next 16-byte boundary) one fp32 scale per row; the RMSNorm gains
+// stay fp32.
+size_t tensor_bytes(const mt_layer_cfg& c, int u, int t, size_t esz) {
+  const size_t n = tensor_numel(c, u, t);
+  if (esz != 1) return n * esz;
+  if (is_gain(c, u, t)) return n * 4;
+  return rup(n, 16) + n / tensor_cols(c, u, t) * 4;
+}
+
+// offsets[u][t] in bytes for element size esz (1: FP8 with row scales);
+// returns total bytes.
 size_t build_layout(const mt_layer_cfg& c, size_t esz, std::vector<std::vector<size_t>>* offs) {
   size_t pos = 0;
   if (offs) offs->assign(c.n_layers + 2, {});
@@ -91,11 +114,52 @@ size_t build_layout(const mt_layer_cfg& c, size_t esz, std::vector<std::vector<s
     for (int t = 0; t < tensors_in_unit(c, u); ++t) {
       pos = rup(pos, 256);
       if (offs) (*offs)[u].push_back(pos);
-      pos += tensor_numel(c, u, t) * esz;
+      pos += tensor_bytes(c, u, t, esz);
     }
   }
   return rup(pos, 4096);
 }
+
+size_t dtype_esz(int dtype) { return dtype == MT_BF16 ? 2 : dtype == MT_FP8 ? 1 : 4; }
+
+// ---------------------------------------------------------------------------
+// FP8 e4m3 (the OCP 8-bit format E4M3: sign, 4 exponent bits with bias 7, 3
+// mantissa bits; no infinities; S.1111.111 is NaN; largest finite 448) and
+// the row-scaled weight encoding of the FP8 packed layout.
+// ---------------------------------------------------------------------------
+float e4m3_decode(uint8_t code) {
+  const int e = (code >> 3) & 15, m = code & 7;
+  float v;
+  if (e == 15 && m == 7) v = NAN;
+  else if (e == 0) v = std::ldexp((float)m, -9);
+  else v = std::ldexp(1.f + m / 8.f, e - 7);
+  return (code & 0x80) ? -v : v;
+}
+
+// Nearest e4m3 value (ties to even mantissa), saturating at +-448. x finite.
+uint8_t e4m3_encode(float x) {
+  const uint8_t sign = std::signbit(x) ? 0x80 : 0;
+  const float a = std::fabs(x);
+  if (a >= 448.f) return sign | 0x7E;
+  if (a < 0.015625f) {  // below 2^-6: subnormal steps of 2^-9 (8 steps reach the smallest normal)
+    const int m = (int)std::nearbyint(a * 512.f);  // exact scaling, then round half to even
+    return sign | (uint8_t)m;                          // m == 8 is exactly the code of 2^-6
+  }
+  int e;
+  std::frexp(a, &e);  // a = f 2^e, f in [0.5, 1)
+  e -= 1;             // a in [2^e, 2^(e+1)), e in [-6, 8]
+  int m = (int)std::nearbyint((std::ldexp(a, -e) - 1.f) * 8.f);
+  if (m == 8) {
+    m = 0;
+    e += 1;
+  }
+  if (e > 8 || (e == 8 && m > 6)) return sign | 0x7E;
+  return sign | (uint8_t)(((e + 7) << 3) | m);
+}
+
+// bf16 bits of the dequantised weight: bf16(float(code) * scale).
+inline uint16_t host_bf16_rne(float f);
+uint16_t e4m3_dequant_bf16(uint8_t code, float scale) { return host_bf16_rne(e4m3_decode(code) * scale); }
 
 // ---------------------------------------------------------------------------
 // AdamW on the host (MegaTrain stage 4), fp32, over packed units.
@@ -118,7 +182,7 @@ AdamCoef adam_coef(const mt_adamw_cfg& o, int64_t step) {
   return c;
 }
 
-inline uint16_t host_bf16_rne(float f) {
+inline uint16_t host_bf16_rne(float f) {  // round to nearest even
   uint32_t u;
   std::memcpy(&u, &f, 4);
   if ((u & 0x7f800000u) == 0x7f800000u && (u & 0x7fffffu)) return (uint16_t)((u >> 16) | 0x40);  // quiet NaN
@@ -244,7 +308,9 @@ bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
   if (c.n_heads % c.n_kv_heads) return fail("n_heads must be a multiple of n_kv_heads");
   if (c.head_dim != 16 && c.head_dim != 32 && c.head_dim != 64 && c.head_dim != 128)
     return fail("head_dim must be 16, 32, 64 or 128");
-  if (c.param_dtype != MT_F32 && c.param_dtype != MT_BF16) return fail("param_dtype must be MT_F32 or MT_BF16");
+  if (c.param_dtype != MT_F32 && c.param_dtype != MT_BF16 && c.param_dtype != MT_FP8)
+    return fail("param_dtype must be MT_F32, MT_BF16 or MT_FP8");
+  if (c.param_dtype == MT_FP8 && c.ffn_dim % 16) return fail("FP8 params need ffn_dim % 16 == 0");
   if (c.grad_dtype != MT_F32 && c.grad_dtype != MT_BF16) return fail("grad_dtype must be MT_F32 or MT_BF16");
   if (c.param_dtype == MT_BF16 && c.ffn_dim % 8) return fail("bf16 params need ffn_dim % 8 == 0");
   if (c.max_batch < 1 || c.max_seq < 1 || c.max_K < 1) return fail("max_batch, max_seq, max_K must be >= 1");
@@ -277,7 +343,14 @@ struct Plan {
   size_t o_r, o_sel, o_w, o_spos, o_seg, o_tile_e, o_xp, o_gup, o_actp, o_yp;
 };
 
-size_t layer_cast_bytes(const Plan& p) {  // device bf16 view of one layer (fp32 params)
+// Bytes of a head vocab slice of `rows` rows in a weight buffer (FP8: the
+// codes, then the row scales at the next 256-byte boundary).
+size_t head_slice_bytes(const Plan& p, int rows) {
+  if (p.esz == 1) return rup((size_t)rows * p.h, 256) + (size_t)rows * 4;
+  return (size_t)rows * p.h * p.esz;
+}
+
+size_t layer_cast_bytes(const Plan& p) {  // device bf16 view of one layer (fp32 or FP8 params)
   return rup((size_t)p.qkv * p.h * 2, 256) + rup((size_t)p.h * p.qd * 2, 256) + rup((size_t)2 * p.Fp * p.h * 2, 256) +
          rup((size_t)p.h * p.Fp * 2, 256);
 }
@@ -290,13 +363,13 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   p.nkv = c.n_kv_heads;
   p.d = c.head_dim;
   p.F = c.ffn_dim;
-  p.Fp = c.param_dtype == MT_BF16 ? c.ffn_dim : (int)rup(c.ffn_dim, 8);
+  p.Fp = c.param_dtype == MT_F32 ? (int)rup(c.ffn_dim, 8) : c.ffn_dim;
   p.V = c.vocab;
   p.qd = p.nq * p.d;
   p.kd = p.nkv * p.d;
   p.qkv = p.qd + 2 * p.kd;
   p.Tmax = c.max_batch * c.max_seq;
-  p.esz = c.param_dtype == MT_BF16 ? 2 : 4;
+  p.esz = dtype_esz(c.param_dtype);
   p.gesz = c.grad_dtype == MT_BF16 ? 2 : 4;
   p.gepi = p.gesz == 2 ? EPI_BF16 : EPI_F32;
   p.E = c.n_experts;
@@ -305,8 +378,9 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
   p.n_pad = p.E ? (int)rup((size_t)p.Tmax * p.topk + (size_t)p.E * 127, 128) : 0;
   std::vector<std::vector<size_t>> o;
   build_layout(c, p.esz, &o);
-  const size_t layer_bytes = (o[1][8] + tensor_numel(c, 1, 8) * p.esz) - o[1][0];
+  const size_t layer_bytes = (o[1][8] + tensor_bytes(c, 1, 8, p.esz)) - o[1][0];
   // vocab slices: the fewest equal slices (multiples of 256 rows) that fit a layer buffer
+  // (FP8: a slice's codes, then its row scales at the next 256-byte boundary)
   auto slices = [&](size_t row_bytes, size_t cap, int* rows, int* n) {
     int ns = (int)std::max<size_t>(1, (p.V * row_bytes + cap - 1) / cap);
     while (true) {
@@ -320,12 +394,14 @@ bool make_plan(const mt_layer_cfg& c, Plan* P) {
       ++ns;
     }
   };
-  slices((size_t)p.h * p.esz, layer_bytes, &p.head_rows, &p.n_head_slices);
+  if (p.esz == 1) slices((size_t)p.h + 4, layer_bytes - 256, &p.head_rows, &p.n_head_slices);
+  else slices((size_t)p.h * p.esz, layer_bytes, &p.head_rows, &p.n_head_slices);
   std::vector<std::vector<size_t>> og;
   build_layout(c, p.gesz, &og);
   const size_t layer_grad_bytes = (og[1][8] + tensor_numel(c, 1, 8) * p.gesz) - og[1][0];
-  p.wbuf = rup(std::max(layer_bytes, (size_t)p.head_rows * p.h * p.esz), 4096);
-  p.wcast = p.esz == 4 ? rup(std::max(layer_cast_bytes(p), (size_t)p.head_rows * p.h * 2), 4096) : 0;
+  p.wbuf = rup(std::max(layer_bytes, head_slice_bytes(p, p.head_rows)), 4096);
+  // fp32 and FP8 host params are turned into a bf16 view on the device
+  p.wcast = p.esz != 2 ? rup(std::max(layer_cast_bytes(p), (size_t)p.head_rows * p.h * 2), 4096) : 0;
   p.gbuf = rup(std::max({layer_grad_bytes, (size_t)p.head_rows * p.h * p.gesz, (size_t)p.h * p.gesz}), 4096);
   const size_t T = p.Tmax, h = p.h;
   p.ckpt_one = rup(T * h * 4, 256);
@@ -887,18 +963,34 @@ void plan_sequence(Step& st) {
 
 // Host byte range (offset into the bound parameters, bytes) that one use of
 // a streamed unit copies: a layer's packed weights, or an LM-head vocab slice.
-void load_range(const mt_ctx* ctx, const Item& it, size_t* src_off, size_t* bytes) {
+// FP8 head slices have a second range, their row scales (*scale_bytes > 0),
+// copied to the weight buffer at head_scale_dst(rows).
+void load_range(const mt_ctx* ctx, const Item& it, size_t* src_off, size_t* bytes, size_t* scale_off = nullptr,
+                size_t* scale_bytes = nullptr) {
   const Plan& p = ctx->P;
+  if (scale_bytes) *scale_bytes = 0;
   if (it.kind == IT_LAYER) {
     const int l = std::abs(it.index);
     *src_off = ctx->off_p[l][0];
-    *bytes = ctx->off_p[l][8] + tensor_numel(ctx->cfg, l, 8) * p.esz - *src_off;
+    *bytes = ctx->off_p[l][8] + tensor_bytes(ctx->cfg, l, 8, p.esz) - *src_off;
   } else {
     const int r0 = it.index * p.head_rows, rows = std::min(p.head_rows, p.V - r0);
-    *src_off = ctx->off_p[p.L + 1][1] + (size_t)r0 * p.h * p.esz;
-    *bytes = (size_t)rows * p.h * p.esz;
+    if (p.esz == 1) {
+      *src_off = ctx->off_p[p.L + 1][1] + (size_t)r0 * p.h;
+      *bytes = (size_t)rows * p.h;
+      if (scale_off && scale_bytes) {
+        *scale_off = ctx->off_p[p.L + 1][1] + rup((size_t)p.V * p.h, 16) + (size_t)r0 * 4;
+        *scale_bytes = (size_t)rows * 4;
+      }
+    } else {
+      *src_off = ctx->off_p[p.L + 1][1] + (size_t)r0 * p.h * p.esz;
+      *bytes = (size_t)rows * p.h * p.esz;
+    }
   }
 }
+// Where an FP8 head slice's row scales sit in its weight buffer.
+size_t head_scale_dst(const Plan& p, int rows) { return rup((size_t)rows * p.h, 256); }
+int head_slice_rows(const Plan& p, int s) { return std::min(p.head_rows, p.V - s * p.head_rows); }
 
 // Host ranges to touch ahead of the step's copies, in the order the copies
 // use them: each weight copy's source, paced two weight copies ahead of it,
@@ -915,11 +1007,12 @@ std::vector<PageToucher::Range> touch_plan(const mt_ctx* ctx, const Step& st, co
   for (size_t i = 0; i < st.seq.size(); ++i) {
     const Item& it = st.seq[i];
     if (st.needs_load[i]) {
-      size_t off, bytes;
-      load_range(ctx, it, &off, &bytes);
+      size_t off, bytes, soff = 0, sbytes = 0;
+      load_range(ctx, it, &off, &bytes, &soff, &sbytes);
       last = copies++;
       (*index)[i] = last;
       r.push_back({(const uint8_t*)ctx->host_params + off, bytes, last - 2});
+      if (sbytes) r.push_back({(const uint8_t*)ctx->host_params + soff, sbytes, last - 2});
     }
     if (!grad_out) continue;
     const bool pass2 = it.kind == IT_HEAD && (int)i >= p.L + p.n_head_slices;
@@ -942,16 +1035,20 @@ int issue_load(Step& st, size_t i) {
   mt_ctx* ctx = st.ctx;
   const int slot = st.slot_of[i];
   const uint8_t* hp = (const uint8_t*)ctx->host_params;
-  size_t src_off = 0, bytes = 0;
-  load_range(ctx, st.seq[i], &src_off, &bytes);
+  size_t src_off = 0, bytes = 0, scale_off = 0, scale_bytes = 0;
+  load_range(ctx, st.seq[i], &src_off, &bytes, &scale_off, &scale_bytes);
   if (ctx->fault_kind == 1 && ++ctx->fault_count == ctx->fault_nth)
     return set_err(ctx, MT_ERR_CUDA, "injected copy-issue failure");
   CK(cudaStreamWaitEvent(ctx->s_h2d, ctx->ev_wfree[slot], 0));
   if (ctx->serial && i > 0) CK(cudaStreamWaitEvent(ctx->s_h2d, ctx->ev_wfree[st.slot_of[i - 1]], 0));
   {
-    SegScope sg(ctx, 1, ctx->s_h2d, (double)bytes, (int)i);
+    SegScope sg(ctx, 1, ctx->s_h2d, (double)(bytes + scale_bytes), (int)i);
     CK(cudaMemcpyAsync(ctx->wbuf[slot], hp + src_off, bytes, cudaMemcpyHostToDevice, ctx->s_h2d));
+    if (scale_bytes)
+      CK(cudaMemcpyAsync(ctx->wbuf[slot] + head_scale_dst(ctx->P, head_slice_rows(ctx->P, st.seq[i].index)),
+                         hp + scale_off, scale_bytes, cudaMemcpyHostToDevice, ctx->s_h2d));
   }
+  bytes += scale_bytes;
   CK(cudaEventRecord(ctx->ev_wready[slot], ctx->s_h2d));
   if (st.toucher && st.load_index[i] >= 0) {
     cudaEvent_t done = next_event(ctx);
@@ -994,7 +1091,23 @@ int bind_layer(Step& st, int l, int slot, bool fresh, LayerView* v) {
     uint16_t* co = cqkv + rup((size_t)p.qkv * p.h * 2, 256) / 2;
     uint16_t* cgu = co + rup((size_t)p.h * p.qd * 2, 256) / 2;
     uint16_t* cd = cgu + rup((size_t)2 * p.Fp * p.h * 2, 256) / 2;
-    if (fresh) {
+    if (fresh && p.esz == 1) {
+      // FP8 codes with row scales -> the bf16 view (Wq, Wk, Wv stacked as one
+      // q|k|v matrix; Wg then Wu; Fp == F for FP8)
+      auto deq = [&](int t, int rows, int cols, uint16_t* dst, int ld) {
+        const uint8_t* q = at(t);
+        return dequant_fp8_rows(q, (const float*)(q + rup((size_t)rows * cols, 16)), rows, cols, dst, ld, ctx->s_comp);
+      };
+      CKL(deq(1, p.qd, p.h, cqkv, p.h));
+      CKL(deq(2, p.kd, p.h, cqkv + (size_t)p.qd * p.h, p.h));
+      CKL(deq(3, p.kd, p.h, cqkv + (size_t)(p.qd + p.kd) * p.h, p.h));
+      CKL(deq(4, p.h, p.qd, co, p.qd));
+      CKL(deq(6, p.F, p.h, cgu, p.h));
+      CKL(deq(7, p.F, p.h, cgu + (size_t)p.Fp * p.h, p.h));
+      CKL(deq(8, p.h, p.F, cd, p.Fp));
+      CKL(gains_to_f32(at(0), false, g, p.h, ctx->s_comp));
+      CKL(gains_to_f32(at(5), false, g + p.h, p.h, ctx->s_comp));
+    } else if (fresh) {
       // Wq, Wk, Wv are contiguous in the packed layout (hidden % 64 == 0)
       CKL(cast_rows_f32_bf16((const float*)at(1), cqkv, p.qkv, p.qkv, p.h, p.h, ctx->s_comp));
       CKL(cast_rows_f32_bf16((const float*)at(4), co, p.h, p.h, p.qd, p.qd, ctx->s_comp));
@@ -1021,7 +1134,12 @@ const uint16_t* bind_head(Step& st, int s, int slot, bool fresh, int* rows) {
   const int r0 = s * p.head_rows;
   *rows = std::min(p.head_rows, p.V - r0);
   if (p.esz == 2) return (const uint16_t*)ctx->wbuf[slot];
-  if (fresh) {
+  if (fresh && p.esz == 1) {
+    const uint8_t* q = ctx->wbuf[slot];
+    if (dequant_fp8_rows(q, (const float*)(q + head_scale_dst(p, *rows)), *rows, p.h, ctx->wcast[slot], p.h,
+                         ctx->s_comp))
+      return nullptr;
+  } else if (fresh) {
     if (cast_rows_f32_bf16((const float*)ctx->wbuf[slot], ctx->wcast[slot], *rows, *rows, p.h, p.h, ctx->s_comp))
       return nullptr;
   }
@@ -1457,7 +1575,7 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   }
   // Final-norm gain: tiny copy on the weight stream.
   {
-    const size_t wf_bytes = (size_t)h * p.esz;
+    const size_t wf_bytes = (size_t)h * (p.esz == 2 ? 2 : 4);  // FP8 layouts keep the gains fp32
     CK(cudaMemcpyAsync(ctx->wf_raw, (const uint8_t*)ctx->host_params + ctx->off_p[L + 1][0], wf_bytes,
                        cudaMemcpyHostToDevice, ctx->s_h2d));
     cudaEvent_t e = next_event(ctx);
@@ -1493,8 +1611,12 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
   // table into a contiguous pinned buffer (the first layer's weights are
   // already streaming), then one copy brings them to the device.
   {
-    const size_t row_bytes = (size_t)h * p.esz;
+    // staged rows: fp32 for fp32 params, bf16 otherwise (FP8 rows are
+    // dequantised by the gathering threads: bf16(code * row scale))
+    const size_t row_bytes = (size_t)h * (p.esz == 4 ? 4 : 2);
     const uint8_t* E = (const uint8_t*)ctx->host_params + ctx->off_p[0][0];
+    const float* E_scale = (const float*)(E + rup((size_t)p.V * h, 16));
+    const bool fp8 = p.esz == 1;
     uint8_t* dst = ctx->host_rows;
     const int nthr = (int)std::min<unsigned>(16, std::max(1u, std::thread::hardware_concurrency()));
     std::vector<std::thread> gth;
@@ -1503,7 +1625,16 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
       const int t0 = i * per, t1 = std::min(T, t0 + per);
       if (t0 >= t1) break;
       gth.emplace_back([=] {
-        for (int t = t0; t < t1; ++t) std::memcpy(dst + (size_t)t * row_bytes, E + (size_t)tokens[t] * row_bytes, row_bytes);
+        for (int t = t0; t < t1; ++t) {
+          if (fp8) {
+            const uint8_t* src = E + (size_t)tokens[t] * h;
+            const float sc = E_scale[tokens[t]];
+            uint16_t* out = (uint16_t*)(dst + (size_t)t * row_bytes);
+            for (int c = 0; c < h; ++c) out[c] = e4m3_dequant_bf16(src[c], sc);
+          } else {
+            std::memcpy(dst + (size_t)t * row_bytes, E + (size_t)tokens[t] * row_bytes, row_bytes);
+          }
+        }
       });
     }
     for (auto& x : gth) x.join();
@@ -1519,12 +1650,12 @@ int run_step(Step& st, const int32_t* tokens, const int32_t* labels, float* loss
     }
     CK(cudaEventRecord(rows_in, ctx->s_h2d));
     CK(cudaStreamWaitEvent(s, rows_in, 0));
-    if (p.esz == 2) {
+    if (p.esz != 4) {
       SegScope sg(ctx, 0, s, 0, -1);
       CKL(cast_bf16_f32(ctx->xf_b, ckpt(ctx, 0), (size_t)T * h, s));
     }
   }
-  ctx->stats.h2d_bytes += (double)T * h * p.esz;
+  ctx->stats.h2d_bytes += (double)T * h * (p.esz == 4 ? 4 : 2);
   int head_pass2_count = 0;
   bool first_dxf = true;
   for (size_t i = 0; i < n; ++i) {
@@ -1869,19 +2000,90 @@ extern "C" {
 
 size_t mt_packed_bytes(const mt_layer_cfg* cfg, mt_dtype dtype) {
   if (!cfg || cfg->n_layers < 1) return 0;
-  return build_layout(*cfg, dtype == MT_BF16 ? 2 : 4, nullptr);
+  if (dtype == MT_FP8 && cfg->n_experts) return 0;  // FP8 layouts are defined for dense layers
+  return build_layout(*cfg, dtype_esz(dtype), nullptr);
 }
 
 int mt_tensor_offset(const mt_layer_cfg* cfg, mt_dtype dtype, int unit, int tensor, size_t* off, size_t* bytes) {
   if (!cfg || !off || !bytes || unit < 0 || unit > cfg->n_layers + 1 || tensor < 0 ||
-      tensor >= tensors_in_unit(*cfg, unit))
+      tensor >= tensors_in_unit(*cfg, unit) || (dtype == MT_FP8 && cfg->n_experts))
     return MT_ERR_ARG;
   std::vector<std::vector<size_t>> o;
-  const size_t esz = dtype == MT_BF16 ? 2 : 4;
+  const size_t esz = dtype_esz(dtype);
   build_layout(*cfg, esz, &o);
   *off = o[unit][tensor];
-  *bytes = tensor_numel(*cfg, unit, tensor) * esz;
+  *bytes = tensor_bytes(*cfg, unit, tensor, esz);
   return MT_OK;
+}
+
+int mt_quantize_params_fp8(const mt_layer_cfg* cfg, const void* src, mt_dtype src_dtype, void* dst,
+                           int32_t n_threads) {
+  if (!cfg || !src || !dst || n_threads < 0 || cfg->n_layers < 1) return MT_ERR_ARG;
+  if (src_dtype != MT_F32 && src_dtype != MT_BF16) return MT_ERR_ARG;
+  if (cfg->n_experts) return MT_ERR_UNSUPPORTED;
+  const mt_layer_cfg& c = *cfg;
+  std::vector<std::vector<size_t>> os, od;
+  const size_t es = dtype_esz(src_dtype);
+  build_layout(c, es, &os);
+  build_layout(c, 1, &od);
+  const uint8_t* S = (const uint8_t*)src;
+  uint8_t* Dp = (uint8_t*)dst;
+  auto val = [&](const uint8_t* base, size_t i) -> float {
+    if (es == 4) return ((const float*)base)[i];
+    uint32_t u = (uint32_t)((const uint16_t*)base)[i] << 16;
+    float f;
+    std::memcpy(&f, &u, 4);
+    return f;
+  };
+  // one task per tensor row block; every row is quantised independently
+  struct Job {
+    const uint8_t* s;
+    uint8_t* d;
+    size_t rows, cols;
+    bool gain;
+  };
+  std::vector<Job> jobs;
+  for (int u = 0; u <= c.n_layers + 1; ++u)
+    for (int t = 0; t < tensors_in_unit(c, u); ++t) {
+      const size_t n = tensor_numel(c, u, t);
+      if (is_gain(c, u, t)) {
+        jobs.push_back({S + os[u][t], Dp + od[u][t], 1, n, true});
+      } else {
+        const size_t cols = tensor_cols(c, u, t);
+        jobs.push_back({S + os[u][t], Dp + od[u][t], n / cols, cols, false});
+      }
+    }
+  std::atomic<int> bad{0};
+  auto run_rows = [&](const Job& j, size_t r0, size_t r1) {
+    if (j.gain) {
+      for (size_t i = 0; i < j.cols; ++i) ((float*)j.d)[i] = val(j.s, i);
+      return;
+    }
+    float* scales = (float*)(j.d + rup(j.rows * j.cols, 16));
+    for (size_t r = r0; r < r1; ++r) {
+      float amax = 0.f;
+      for (size_t cc = 0; cc < j.cols; ++cc) {
+        const float v = val(j.s, r * j.cols + cc);
+        if (!std::isfinite(v)) bad = 1;
+        amax = std::max(amax, std::fabs(v));
+      }
+      const float sc = amax > 0.f ? amax / 448.f : 1.f;
+      scales[r] = sc;
+      for (size_t cc = 0; cc < j.cols; ++cc) j.d[r * j.cols + cc] = e4m3_encode(val(j.s, r * j.cols + cc) / sc);
+    }
+  };
+  const int nthr = n_threads > 0 ? n_threads : (int)std::max(1u, std::thread::hardware_concurrency());
+  std::vector<std::thread> th;
+  for (int w = 0; w < nthr; ++w)
+    th.emplace_back([&, w] {
+      for (const Job& j : jobs) {
+        const size_t per = (j.rows + nthr - 1) / nthr;
+        const size_t r0 = (size_t)w * per, r1 = std::min(j.rows, r0 + per);
+        if (j.gain ? w == 0 : r0 < r1) run_rows(j, r0, r1);
+      }
+    });
+  for (auto& x : th) x.join();
+  return bad ? MT_ERR_ARG : MT_OK;
 }
 
 size_t mt_required_budget(const mt_layer_cfg* cfg) {
@@ -1898,6 +2100,7 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
   if (!cfg_valid(*cfg, &why)) {
     fprintf(stderr, "mt_create: %s\n", why.c_str());
     return ((cfg->n_experts && cfg->param_dtype != MT_BF16) || cfg->hidden % 64 ||
+            (cfg->param_dtype == MT_FP8 && cfg->ffn_dim % 16) ||
             (cfg->head_dim != 16 && cfg->head_dim != 32 && cfg->head_dim != 64 && cfg->head_dim != 128))
                ? MT_ERR_UNSUPPORTED
                : MT_ERR_ARG;
@@ -1973,7 +2176,8 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
     return fail(MT_ERR_CUDA, "event create", e);
   const size_t stage_ints = 5 * (size_t)ctx->P.Tmax + 1 + 64;
   if ((e = cudaHostAlloc((void**)&ctx->host_stage, stage_ints * 4, cudaHostAllocDefault)) != cudaSuccess ||
-      (e = cudaHostAlloc((void**)&ctx->host_rows, (size_t)ctx->P.Tmax * ctx->P.h * ctx->P.esz, cudaHostAllocDefault)) !=
+      (e = cudaHostAlloc((void**)&ctx->host_rows, (size_t)ctx->P.Tmax * ctx->P.h * (ctx->P.esz == 4 ? 4 : 2),
+                         cudaHostAllocDefault)) !=
           cudaSuccess ||
       (e = cudaHostAlloc((void**)&ctx->host_grad_rows, (size_t)ctx->P.Tmax * ctx->P.h * 4, cudaHostAllocDefault)) !=
           cudaSuccess)
@@ -2078,6 +2282,8 @@ int mt_bind_optimizer(mt_ctx* ctx, const mt_adamw_cfg* opt, float* master, float
     return set_err(ctx, MT_ERR_ARG, "AdamW hyper-parameters out of range");
   if (ctx->cfg.grad_dtype != MT_F32)
     return set_err(ctx, MT_ERR_UNSUPPORTED, "the host optimizer takes fp32 gradients (grad_dtype = MT_F32)");
+  if (ctx->cfg.param_dtype == MT_FP8)
+    return set_err(ctx, MT_ERR_UNSUPPORTED, "the host optimizer publishes fp32 or bf16 parameters, not FP8");
   ctx->opt = *opt;
   ctx->opt_master = master;
   ctx->opt_m = m;
@@ -2094,6 +2300,7 @@ int mt_adamw_update(const mt_layer_cfg* cfg, const mt_adamw_cfg* opt, int64_t st
                     int32_t unit_end, float* master, float* m, float* v, const float* grads, void* params,
                     mt_dtype params_dtype, int32_t n_threads) {
   if (!cfg || !opt || !master || !m || !v || !grads || !params || step < 1 || n_threads < 0) return MT_ERR_ARG;
+  if (params_dtype == MT_FP8) return MT_ERR_UNSUPPORTED;
   if (params_dtype != MT_F32 && params_dtype != MT_BF16) return MT_ERR_ARG;
   if (unit_begin < 0 || unit_end > cfg->n_layers + 2 || unit_begin > unit_end) return MT_ERR_ARG;
   std::string why;
@@ -2212,8 +2419,8 @@ int mt_replay_weight_stream(mt_ctx* ctx, int K, int flags, float* copy_gbs_out, 
   int rc = MT_OK;
   for (size_t i = 0; i < st.seq.size() && rc == MT_OK; ++i) {
     if (!st.needs_load[i]) continue;
-    size_t src_off, nb;
-    load_range(ctx, st.seq[i], &src_off, &nb);
+    size_t src_off, nb, soff = 0, sbytes = 0;
+    load_range(ctx, st.seq[i], &src_off, &nb, &soff, &sbytes);
     cudaEvent_t a = nullptr, b = nullptr;
     if (cudaEventCreate(&a) != cudaSuccess || cudaEventCreate(&b) != cudaSuccess) {
       if (a) cudaEventDestroy(a);
@@ -2221,9 +2428,12 @@ int mt_replay_weight_stream(mt_ctx* ctx, int K, int flags, float* copy_gbs_out, 
       break;
     }
     ev.push_back({a, b});
-    bytes.push_back((double)nb);
+    bytes.push_back((double)(nb + sbytes));
+    uint8_t* dst = ctx->wbuf[st.slot_of[i]];
     if (cudaEventRecord(a, ctx->s_h2d) != cudaSuccess ||
-        cudaMemcpyAsync(ctx->wbuf[st.slot_of[i]], hp + src_off, nb, cudaMemcpyHostToDevice, ctx->s_h2d) != cudaSuccess ||
+        cudaMemcpyAsync(dst, hp + src_off, nb, cudaMemcpyHostToDevice, ctx->s_h2d) != cudaSuccess ||
+        (sbytes && cudaMemcpyAsync(dst + head_scale_dst(ctx->P, head_slice_rows(ctx->P, st.seq[i].index)),
+                                   hp + soff, sbytes, cudaMemcpyHostToDevice, ctx->s_h2d) != cudaSuccess) ||
         cudaEventRecord(b, ctx->s_h2d) != cudaSuccess)
       rc = set_err(ctx, MT_ERR_CUDA, std::string("replay copy: ") + cudaGetErrorString(cudaGetLastError()));
     if (flags & MT_REPLAY_TOUCH) toucher.published((size_t)load_index[i], b);
