@@ -58,7 +58,7 @@ typedef enum { MT_F32 = 0, MT_BF16 = 1, MT_FP8 = 2 } mt_dtype;
  * j / (n_heads / n_kv_heads)), SwiGLU FFN width ffn_dim, untied vocab.
  * Supported: h % 64 == 0, d in {16, 32, 64, 128}, for MT_BF16 params
  * ffn_dim % 8 == 0; any ffn_dim >= 1 for MT_F32 params; for MT_FP8 params
- * (dense layers only) ffn_dim % 16 == 0.
+ * ffn_dim % 16 == 0.
  * max_batch * max_seq bounds the tokens of one call; max_K bounds the
  * checkpoint interval. param_dtype is the dtype of the host parameters that
  * will be bound. n_experts = top_k = expert_ffn = 0: dense SwiGLU FFN.
@@ -70,7 +70,8 @@ typedef enum { MT_F32 = 0, MT_BF16 = 1, MT_FP8 = 2 } mt_dtype;
  * with weights p_j / sum of the chosen p; each a SwiGLU MLP of width
  * expert_ffn; out = sum_j w_j y_j. No shared expert, no auxiliary loss.
  * Then ffn_dim = 0, n_experts a multiple of 8 in [8, 1024], top_k in
- * [1, min(32, n_experts)], expert_ffn % 32 == 0, and MT_BF16 params. */
+ * [1, min(32, n_experts)], expert_ffn % 32 == 0, and MT_BF16 or MT_FP8
+ * params. */
 typedef struct {
   int32_t n_layers, hidden, n_heads, n_kv_heads, head_dim, ffn_dim, vocab;
   float rope_theta, norm_eps;

@@ -89,8 +89,9 @@ bool is_gain(const mt_layer_cfg& c, int u, int t) {
 // Columns (the reduction width) of a matrix tensor of a dense model.
 size_t tensor_cols(const mt_layer_cfg& c, int u, int t) {
   if (u >= 1 && u <= c.n_layers && t == 4) return (size_t)c.n_heads * c.head_dim;  // Wo[h, qd]
-  if (u >= 1 && u <= c.n_layers && t == 8) return (size_t)c.ffn_dim;              // Wd[h, F]
-  return (size_t)c.hidden;
+  if (u >= 1 && u <= c.n_layers && t == 8)  // Wd[h, F], or every expert's Wd[h, Fe]
+    return (size_t)(c.n_experts ? c.expert_ffn : c.ffn_dim);
+  return (size_t)c.hidden;  // mixture of experts: Wr[E, h] and Wgu[E * 2Fe, h] rows
 }
 
 // Bytes of one packed tensor. esz 4 / 2: fp32 / bf16 elements. esz 1: the
@@ -301,7 +302,8 @@ bool cfg_valid(const mt_layer_cfg& c, std::string* why) {
       return fail("n_experts must be a multiple of 8 in [8, 1024]");
     if (c.top_k < 1 || c.top_k > 32 || c.top_k > c.n_experts) return fail("top_k must be in [1, min(32, n_experts)]");
     if (c.expert_ffn < 32 || c.expert_ffn % 32) return fail("expert_ffn must be a positive multiple of 32");
-    if (c.param_dtype != MT_BF16) return fail("mixture-of-experts layers need bf16 params");
+    if (c.param_dtype != MT_BF16 && c.param_dtype != MT_FP8)
+      return fail("mixture-of-experts layers need bf16 or FP8 params");
   }
   if (c.hidden % 64) return fail("hidden must be a multiple of 64");
   if (c.hidden > 8192) return fail("hidden above 8192 is not supported");
@@ -351,8 +353,11 @@ size_t head_slice_bytes(const Plan& p, int rows) {
 }
 
 size_t layer_cast_bytes(const Plan& p) {  // device bf16 view of one layer (fp32 or FP8 params)
-  return rup((size_t)p.qkv * p.h * 2, 256) + rup((size_t)p.h * p.qd * 2, 256) + rup((size_t)2 * p.Fp * p.h * 2, 256) +
-         rup((size_t)p.h * p.Fp * 2, 256);
+  const size_t attn = rup((size_t)p.qkv * p.h * 2, 256) + rup((size_t)p.h * p.qd * 2, 256);
+  if (p.E > 0)  // router, every expert's gate|up and down
+    return attn + rup((size_t)p.E * p.h * 2, 256) + rup((size_t)p.E * 2 * p.Fe * p.h * 2, 256) +
+           rup((size_t)p.E * p.h * p.Fe * 2, 256);
+  return attn + rup((size_t)2 * p.Fp * p.h * 2, 256) + rup((size_t)p.h * p.Fp * 2, 256);
 }
 
 bool make_plan(const mt_layer_cfg& c, Plan* P) {
@@ -1091,6 +1096,38 @@ int bind_layer(Step& st, int l, int slot, bool fresh, LayerView* v) {
     uint16_t* co = cqkv + rup((size_t)p.qkv * p.h * 2, 256) / 2;
     uint16_t* cgu = co + rup((size_t)p.h * p.qd * 2, 256) / 2;
     uint16_t* cd = cgu + rup((size_t)2 * p.Fp * p.h * 2, 256) / 2;
+    if (p.esz == 1 && p.E > 0) {
+      // mixture of experts: router, every expert's gate|up rows and down
+      // matrices, expert by expert as in the packed layout
+      uint16_t* cr = co + rup((size_t)p.h * p.qd * 2, 256) / 2;
+      uint16_t* cegu = cr + rup((size_t)p.E * p.h * 2, 256) / 2;
+      uint16_t* ced = cegu + rup((size_t)p.E * 2 * p.Fe * p.h * 2, 256) / 2;
+      if (fresh) {
+        auto deq = [&](int t, size_t rows, int cols, uint16_t* dst) {
+          const uint8_t* q = at(t);
+          return dequant_fp8_rows(q, (const float*)(q + rup(rows * cols, 16)), (int)rows, cols, dst, cols,
+                                  ctx->s_comp);
+        };
+        CKL(deq(1, p.qd, p.h, cqkv));
+        CKL(deq(2, p.kd, p.h, cqkv + (size_t)p.qd * p.h));
+        CKL(deq(3, p.kd, p.h, cqkv + (size_t)(p.qd + p.kd) * p.h));
+        CKL(deq(4, p.h, p.qd, co));
+        CKL(deq(6, p.E, p.h, cr));
+        CKL(deq(7, (size_t)p.E * 2 * p.Fe, p.h, cegu));
+        CKL(deq(8, (size_t)p.E * p.h, p.Fe, ced));
+        CKL(gains_to_f32(at(0), false, g, p.h, ctx->s_comp));
+        CKL(gains_to_f32(at(5), false, g + p.h, p.h, ctx->s_comp));
+      }
+      v->wqkv = cqkv;
+      v->wo = co;
+      v->wr = cr;
+      v->wgu = cegu;
+      v->wd = ced;
+      v->ldd = p.Fe;
+      v->w1 = g;
+      v->w2 = g + p.h;
+      return MT_OK;
+    }
     if (fresh && p.esz == 1) {
       // FP8 codes with row scales -> the bf16 view (Wq, Wk, Wv stacked as one
       // q|k|v matrix; Wg then Wu; Fp == F for FP8)
@@ -2000,13 +2037,12 @@ extern "C" {
 
 size_t mt_packed_bytes(const mt_layer_cfg* cfg, mt_dtype dtype) {
   if (!cfg || cfg->n_layers < 1) return 0;
-  if (dtype == MT_FP8 && cfg->n_experts) return 0;  // FP8 layouts are defined for dense layers
   return build_layout(*cfg, dtype_esz(dtype), nullptr);
 }
 
 int mt_tensor_offset(const mt_layer_cfg* cfg, mt_dtype dtype, int unit, int tensor, size_t* off, size_t* bytes) {
   if (!cfg || !off || !bytes || unit < 0 || unit > cfg->n_layers + 1 || tensor < 0 ||
-      tensor >= tensors_in_unit(*cfg, unit) || (dtype == MT_FP8 && cfg->n_experts))
+      tensor >= tensors_in_unit(*cfg, unit))
     return MT_ERR_ARG;
   std::vector<std::vector<size_t>> o;
   const size_t esz = dtype_esz(dtype);
@@ -2020,7 +2056,6 @@ int mt_quantize_params_fp8(const mt_layer_cfg* cfg, const void* src, mt_dtype sr
                            int32_t n_threads) {
   if (!cfg || !src || !dst || n_threads < 0 || cfg->n_layers < 1) return MT_ERR_ARG;
   if (src_dtype != MT_F32 && src_dtype != MT_BF16) return MT_ERR_ARG;
-  if (cfg->n_experts) return MT_ERR_UNSUPPORTED;
   const mt_layer_cfg& c = *cfg;
   std::vector<std::vector<size_t>> os, od;
   const size_t es = dtype_esz(src_dtype);
@@ -2099,7 +2134,7 @@ static int create_impl(const mt_layer_cfg* cfg, size_t budget, void* arena, void
   std::string why;
   if (!cfg_valid(*cfg, &why)) {
     fprintf(stderr, "mt_create: %s\n", why.c_str());
-    return ((cfg->n_experts && cfg->param_dtype != MT_BF16) || cfg->hidden % 64 ||
+    return ((cfg->n_experts && cfg->param_dtype != MT_BF16 && cfg->param_dtype != MT_FP8) || cfg->hidden % 64 ||
             (cfg->param_dtype == MT_FP8 && cfg->ffn_dim % 16) ||
             (cfg->head_dim != 16 && cfg->head_dim != 32 && cfg->head_dim != 64 && cfg->head_dim != 128))
                ? MT_ERR_UNSUPPORTED

@@ -23,14 +23,14 @@ TINY176 = oracle.Config(n_layers=3, hidden=64, n_heads=4, n_kv_heads=2, head_dim
 
 def _shape(mt, c):
     return mt.ModelShape(c.n_layers, c.hidden, c.n_heads, c.n_kv_heads, c.head_dim, c.ffn_dim, c.vocab, c.rope_theta,
-                         c.norm_eps)
+                         c.norm_eps, c.n_experts, c.top_k, c.expert_ffn)
 
 
 def _fp8_and_bf16_models(mt, cfg, seed, B, S, K):
     """(FP8 packed params, the bf16 packed model of its dequantised weights)."""
     src = make_params(cfg, seed, bf16=True)
     lcfg = mt.make_cfg(cfg.n_layers, cfg.hidden, cfg.n_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ffn_dim, cfg.vocab,
-                       cfg.rope_theta, cfg.norm_eps, B, S, K, mt.MT_FP8)
+                       cfg.rope_theta, cfg.norm_eps, B, S, K, mt.MT_FP8, cfg.n_experts, cfg.top_k, cfg.expert_ffn)
     fp8 = np.zeros(mt.mt_packed_bytes(lcfg, mt.MT_FP8), np.uint8)
     mt.mt_quantize_params_fp8(lcfg, src.ctypes.data, mt.MT_BF16, fp8.ctypes.data, 0)
     deq = np.zeros(oracle.packed_bytes(cfg, True), np.uint8)
@@ -41,8 +41,8 @@ def _fp8_and_bf16_models(mt, cfg, seed, B, S, K):
             g = fp8[off8:off8 + 4 * shape[0]].view(np.float32)
             assert np.all(bf16_bits_to_f32((g.view(np.uint32) >> 16).astype(np.uint16)) == g)
             deq[off16:off16 + nb16] = ((g.view(np.uint32) >> 16).astype(np.uint16)).view(np.uint8)
-        else:
-            codes, scales = fp8_tensor(fp8, off8, *shape)
+        else:  # matrices; an expert tensor [E, rows, cols] is E * rows rows
+            codes, scales = fp8_tensor(fp8, off8, int(np.prod(shape[:-1])), shape[-1])
             deq[off16:off16 + nb16] = dequant_rows_bf16_bits(codes, scales).view(np.uint8).ravel()
     return fp8, deq
 
@@ -67,6 +67,27 @@ def test_fp8_step_equals_bf16_step_on_dequantised_weights(cfg, B, S, K):
     lb, gb = _step(mt, cfg, mt.MT_BF16, deq, tok, lab, K, K)
     assert l8 == lb
     assert np.array_equal(g8.view(np.uint32), gb.view(np.uint32))
+    assert mt.mt_op_device_error() == 0
+
+
+def test_fp8_mixture_of_experts_step_equals_bf16_step_on_dequantised_weights():
+    """Router and expert matrices streamed as FP8 (one scale per row of each
+    expert's matrices): same gradients and routing, bit for bit, as the bf16
+    step on the dequantised weights."""
+    torch, mt = need_gpu()
+    from tests.common import TINY_MOE
+    cfg = with_layers(TINY_MOE, 3)
+    fp8, deq = _fp8_and_bf16_models(mt, cfg, 91, 2, 32, 2)
+    tok, lab = make_tokens(cfg, 2, 32, 92)
+    out = []
+    for dtype, params in ((mt.MT_FP8, fp8), (mt.MT_BF16, deq)):
+        with mt.Session(_shape(mt, cfg), 2, 32, 2, dtype) as s:
+            s.params[:] = params
+            loss = s.step(tok, lab, 2)
+            out.append((loss, s.grads.copy(), s.routing(64)))
+    assert out[0][0] == out[1][0]
+    assert np.array_equal(out[0][1].view(np.uint32), out[1][1].view(np.uint32))
+    assert np.array_equal(out[0][2], out[1][2])
     assert mt.mt_op_device_error() == 0
 
 
