@@ -240,9 +240,10 @@ def head_slice_rows(shape, esz, moe=None):
 # as committed with that summary; when the GEMM kernels change, the figure
 # must be captured again.
 GEMM_TRAFFIC_8B = {
-    "qkv_rope": 296457728, "o_proj": 495506688, "gate_up": 1647651072, "down": 1476332800, "dWd": 1072178432,
-    "dact_swiglu": 1457163008, "dWgu": 2729005312, "dm": 2535826688, "dWo": 332630272, "do": 201263104,
-    "dWqkv": 521314560, "dx": 546606336, "head_logits": 2647050752, "head_dX": 4271706624, "head_dW": 4829711104,
+    "qkv_rope": 291063296, "o_proj": 507722240, "gate_up": 1806588416, "down": 1509592320, "dWd": 1095791872,
+    "dact_swiglu": 1423328768, "dWgu": 2951109632, "dm": 2688931328, "dWo": 337852672, "do": 200612608,
+    "dWqkv": 525176320, "dx": 549968128, "head_logits": 3039382784, "head_dX": 4527798784,
+    "head_dW": 4957469696,
 }
 # Launches of each per step at the 8B configuration (32 layers, K=4, top
 # block not recomputed; three vocab slices of the head).

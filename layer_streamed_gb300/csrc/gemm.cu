@@ -301,18 +301,37 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tb, 
     else swiglu_bwd_epilogue<BN>(p, tb, row, row_ok, nb * BN);
     return;
   }
+  // The addend may be C itself (a residual added in place), so the compiler
+  // keeps each addend load behind the previous store; the loads of a chunk
+  // are therefore all issued up front, before its accumulator is read.
+  const unsigned valid = __ballot_sync(0xffffffffu, row_ok);
+  const int lane = threadIdx.x & 31;
+  const int wrow0 = row - lane;
+  const int sub = lane >> 3, c4 = (lane & 7) * 4;
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t r[32];
+    const int col0 = nb * BN + c * 32;
+    const bool full_cols = p.vec && col0 + 32 <= p.N;  // the same in every lane
+    const bool staged = p.epi != EPI_BF16 && full_cols && p.stage_f32;
+    float4 a[8];
+    if (p.epi == EPI_F32_ADD && full_cols) {
+      const float* add = (const float*)p.addend;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        a[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (staged) {
+          const int rr = 4 * i + sub;
+          if ((valid >> rr) & 1u) a[i] = *(const float4*)(add + (size_t)(wrow0 + rr) * p.ldc + col0 + c4);
+        } else if (row_ok) {
+          a[i] = *(const float4*)(add + (size_t)row * p.ldc + col0 + 4 * i);
+        }
+      }
+    }
     __syncwarp();
     tmem_ld32(tb + c * 32, r);
     tmem_ld_wait();
-    const int col0 = nb * BN + c * 32;
-    const bool full_cols = p.vec && col0 + 32 <= p.N;  // the same in every lane
-    if (p.epi != EPI_BF16 && full_cols && p.stage_f32) {
-      const unsigned valid = __ballot_sync(0xffffffffu, row_ok);
-      const int lane = threadIdx.x & 31;
-      const int wrow0 = row - lane;
+    if (staged) {
       __syncwarp();
       float* srow = stg + lane * kStgStride;
 #pragma unroll
@@ -320,21 +339,18 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tb, 
         ((float4*)srow)[v] = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
                                          __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
       __syncwarp();
-      const int sub = lane >> 3, c4 = (lane & 7) * 4;
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int rr = 4 * i + sub;
         if ((valid >> rr) & 1u) {
           float4 w = *(const float4*)(stg + rr * kStgStride + c4);
-          const size_t off = (size_t)(wrow0 + rr) * p.ldc + col0 + c4;
           if (p.epi == EPI_F32_ADD) {
-            const float4 a = *(const float4*)((const float*)p.addend + off);
-            w.x += a.x;
-            w.y += a.y;
-            w.z += a.z;
-            w.w += a.w;
+            w.x += a[i].x;
+            w.y += a[i].y;
+            w.z += a[i].z;
+            w.w += a[i].w;
           }
-          *(float4*)((float*)p.C + off) = w;
+          *(float4*)((float*)p.C + (size_t)(wrow0 + rr) * p.ldc + col0 + c4) = w;
         }
       }
       continue;
@@ -365,11 +381,10 @@ __device__ __forceinline__ void epilogue_tile(const GemmParams& p, uint32_t tb, 
           float4 w = make_float4(__uint_as_float(r[4 * v + 0]), __uint_as_float(r[4 * v + 1]),
                                  __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
           if (add) {
-            const float4 a = ((const float4*)add)[v];
-            w.x += a.x;
-            w.y += a.y;
-            w.z += a.z;
-            w.w += a.w;
+            w.x += a[v].x;
+            w.y += a[v].y;
+            w.z += a[v].z;
+            w.w += a[v].w;
           }
           ((float4*)out)[v] = w;
         }
@@ -809,9 +824,9 @@ int gemm_bf16(int mode, const GemmParams& pin, const void* A, const void* B, int
   }
   if (p.gated && (mode != GEMM_NT || !p.act || (p.ld_act & 7) || (p.u_col & 7) || p.epi != EPI_BF16)) return -1;
   const bool grouped = p.grp_seg != nullptr;
-  // Staged fp32 stores pay off where a tile's reduction is short (grouped
-  // weight gradients: one expert's rows); long reductions hide the epilogue.
-  p.stage_f32 = (p.epi != EPI_BF16 && (grouped || p.K <= 1024)) ? 1 : 0;
+  // fp32 outputs go through the shared-memory staging rows (coalesced
+  // 128-byte row segments); bf16 outputs are stored straight from registers.
+  p.stage_f32 = p.epi != EPI_BF16 ? 1 : 0;
   if (grouped) {
     if (p.grp_E < 1 || p.rope_tab) return -1;
     if (mode == GEMM_TN) {
