@@ -52,8 +52,12 @@ __device__ __forceinline__ float bf2f(uint16_t b) { return __uint_as_float((uint
 __device__ __forceinline__ uint16_t f2bf(float f) {  // round to nearest even
   return __bfloat16_as_ushort(__float2bfloat16_rn(f));
 }
+// Two floats to a bf16 pair (lo in the low half), each rounded to nearest
+// even, in one conversion instruction (the first source goes to the upper half).
 __device__ __forceinline__ uint32_t pack_bf2(float lo, float hi) {
-  return (uint32_t)f2bf(lo) | ((uint32_t)f2bf(hi) << 16);
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
