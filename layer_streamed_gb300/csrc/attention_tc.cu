@@ -293,24 +293,22 @@ __global__ void __launch_bounds__(384, 1)
       tc_commit(&k_empty[0]);
       for (int t = 0; t < tB; ++t) {
         const bool next = t + 1 < tB;
+        // V(t) and K(t+1) are waited for here, while the softmax of tile A
+        // still runs: between the products of one tile a wait would leave
+        // the tensor core idle (its issue queue holds little work).
         mbar_wait(&v_full[t & 1], (t >> 1) & 1, abort_flag, kErrTimeoutAttn);
+        if (next) mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
         if (t < tA) {
           mbar_wait(&p_full[0], t & 1, abort_flag, kErrTimeoutAttn);
           tc_fence_after();
           issue_pv(0, t);
-          if (t + 1 < tA) {
-            mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
-            tc_fence_after();
-            issue_s(0, t + 1);
-          }
+          if (t + 1 < tA) issue_s(0, t + 1);
         }
         mbar_wait(&p_full[1], t & 1, abort_flag, kErrTimeoutAttn);
         tc_fence_after();
         issue_pv(1, t);
         tc_commit(&v_empty[t & 1]);
         if (next) {
-          mbar_wait(&k_full[(t + 1) & 1], ((t + 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
-          tc_fence_after();
           issue_s(1, t + 1);
           tc_commit(&k_empty[(t + 1) & 1]);
         }
