@@ -434,7 +434,7 @@ int mt_op_attention_fwd(const void* q, const void* k, const void* v, void* o, fl
  * (overwritten); do_ bf16 [B*S, ldo]; workspace fp32 of
  * mt_op_attention_bwd_workspace(B,S,n_heads) floats, 16-byte aligned (it
  * receives per-row delta = rowsum(dO * O) and the log-sum-exp in log2 units,
- * S padded to a multiple of 64). Deterministic. */
+ * S padded to a multiple of 128). Deterministic. */
 size_t mt_op_attention_bwd_workspace(int B, int S, int n_heads);
 int mt_op_attention_bwd(const void* q, const void* k, const void* v, const void* o, const void* do_, const float* lse,
                         void* dq, void* dk, void* dv, float* workspace, int B, int S, int n_heads, int n_kv_heads,

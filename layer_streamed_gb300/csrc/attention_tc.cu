@@ -96,8 +96,8 @@ struct AttnArgs {
   uint16_t* o;       // fwd output / unused
   float* lse;        // [B, nq, S] natural log
   const float* lse_in;
-  const float* delta;  // backward: [B, nq, pad64(S)] (see the delta kernel)
-  const float* lse2;   // backward: [B, nq, pad64(S)] log-sum-exp in log2 units
+  const float* delta;  // backward: [B, nq, pad128(S)] (see the delta kernel)
+  const float* lse2;   // backward: [B, nq, pad128(S)] log-sum-exp in log2 units
   uint16_t *dq, *dk, *dv;
   int B, S, nq, nkv, ldq, ldkv, ldo;
   float scale_log2;  // log2(e) / sqrt(d)
@@ -215,8 +215,13 @@ __global__ void __launch_bounds__(384, 1)
 
   const int nqt = (a.S + TILE - 1) / TILE;
   const int npairs = (nqt + 1) / 2;
-  const int m = npairs - 1 - (int)blockIdx.x;  // longest pairs first
-  const int j = blockIdx.y, b = blockIdx.z;
+  // Blocks start roughly in linear order: the pair index is the slowest
+  // coordinate, so every head's longest pairs start first (longest first
+  // over the whole grid, which keeps the tail short).
+  const int lin = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+  const int hb = lin % (a.nq * a.B);
+  const int m = npairs - 1 - lin / (a.nq * a.B);
+  const int j = hb % a.nq, b = hb / a.nq;
   const int g = j / (a.nq / a.nkv);
   const int tA = 2 * m + 1, tB = 2 * m + 2;  // KV tiles seen by tile A / tile B
   const uint32_t warp = warp_id(), lane = lane_id();
@@ -435,49 +440,26 @@ __global__ void __launch_bounds__(384, 1)
 }
 
 // ===========================================================================
-// Backward. Both passes iterate over 64-row sub-tiles of the loop dimension,
-// so that S/dP fit twice in tensor memory (double buffer); operands stream
-// through a four-stage ring. 12 warps: warp 0 TMA, warp 1 MMA issue, warps
-// 4-7 and 8-11 are two elementwise warpgroups that split the 64 columns of
-// each sub-tile (warpgroup A columns 0-31, B 32-63); thread = row of the
-// 128-row tile. The MMA thread issues the score products of sub-tile i+1
-// before the gradient products of sub-tile i, so elementwise work overlaps
-// the tensor core. The elementwise warps write P^T and dS^T (or dS) as bf16
-// pairs over columns of their S and dP buffers that they have already read
-// (see packed_col), and the gradient products read them from tensor memory
-// as their A operand; tensor
-// core operations of one thread run in issue order, so the score products of
-// sub-tile i+2 (which overwrite those buffers) follow the gradient products
-// of sub-tile i. Operand layout of a [64 rows][64] box: 8 KB, 128-byte swizzle.
+// Backward. Both passes work on 128-row tiles of queries and keys, so every
+// product is 128 wide (narrower tcgen05 products run well below the tensor
+// core's rate). 12 warps: warp 0 TMA, warp 1 MMA issue, warps 4-7 and 8-11
+// are two elementwise warpgroups that split the 128 columns of a tile
+// (warpgroup A columns 0-63, B 64-127); thread = row of the 128-row tile.
+// The elementwise warps write P^T and dS^T (or dS) as bf16 pairs over
+// columns of their S and dP buffers that they have already read (see
+// packed_col128), and the gradient products read them from tensor memory as
+// their A operand; tensor-core operations of one thread run in issue order,
+// so a later score product that overwrites those buffers follows the
+// gradient products that read them.
 //
 // The delta kernel also writes, per (sequence, query head), the log-sum-exp
-// in log2 units over S padded to a multiple of 64 (+inf on the padding, so
+// in log2 units over S padded to a multiple of 128 (+inf on the padding, so
 // padded query rows get probability 0) beside delta (0 on the padding).
 // ===========================================================================
-constexpr int SUB = 64;
-constexpr int SBOX = 64 * 64 * 2;  // one [64 rows][64] bf16 box = 8 KB
-constexpr int kStages = 4;
+constexpr int kDkvStages = 2;  // Q / dO tiles in flight in the dK/dV pass
 
-__host__ __device__ constexpr int pad64(int S) { return (S + 63) & ~63; }
+__host__ __device__ constexpr int pad128(int S) { return (S + 127) & ~127; }
 
-template <int D>
-constexpr uint32_t sub_bytes() {
-  return ((D + 63) / 64) * SBOX;
-}
-// K-major descriptor of the k-th 16-wide step of a [64 rows][64*n] sub-tile.
-__device__ __forceinline__ uint64_t kmaj_desc_sub(const uint8_t* tile, int kk) {
-  return make_sdesc(smem_u32(tile) + (kk >> 2) * SBOX + (kk & 3) * 32, 16, 1024);
-}
-// MN-major descriptor (N = head dim, K = 64 rows) of the k-th 16-row step.
-__device__ __forceinline__ uint64_t mnmaj_desc_sub(const uint8_t* tile, int kk) {
-  return make_sdesc(smem_u32(tile) + kk * 2048, SBOX, 1024);
-}
-template <int D>
-__device__ __forceinline__ void load_head_sub(uint8_t* dst, const CUtensorMap* map, uint64_t* bar, int head, int row0,
-                                              int b) {
-#pragma unroll
-  for (int i = 0; i < (D + 63) / 64; ++i) tma_load_4d(dst + i * SBOX, map, bar, i * 64, head, row0, b);
-}
 // Untiled bulk copy global -> shared; both addresses 16-byte aligned, size a
 // multiple of 16.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
@@ -486,12 +468,6 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
                "l"(src), "r"(bytes), "r"(smem_u32(bar))
                : "memory");
 }
-// Packed bf16 operands in tensor memory: each elementwise warpgroup writes
-// its 32 columns as 16 pairs over the first half of its own 32 columns of the
-// buffer (warpgroup A columns [0, 16), B [32, 48)), i.e. only over values it
-// has already read itself. K step kk (16 wide) of the operand therefore sits
-// at packed column kk * 8 for kk < 2 and 32 + (kk - 2) * 8 after.
-__device__ __forceinline__ uint32_t packed_col(int kk) { return kk < 2 ? kk * 8 : 32 + (kk - 2) * 8; }
 
 // 32 values of one row as 16 bf16 pairs into tensor-memory columns [col, col+16).
 __device__ __forceinline__ void tmem_st_bf16x32(uint32_t col, const float (&v)[32]) {
@@ -501,18 +477,26 @@ __device__ __forceinline__ void tmem_st_bf16x32(uint32_t col, const float (&v)[3
   tmem_st16(col, pk);
 }
 
+// K step kk (16 rows of the 128-wide loop dimension) of a packed bf16
+// operand: warpgroup kk / 4 wrote its 64 columns as 32 pairs at the start of
+// its own 64-column range.
+__device__ __forceinline__ uint32_t packed_col128(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+
 // dK/dV pass: CTA = (128-row KV tile kt, KV head g, sequence b); loop over the
-// query heads of the group and the 64-row query sub-tiles at or after kt.
-// TMEM: S^T [2 x 64] +0 (P^T packed over it), dP^T [2 x 64] +128 (dS^T
-// packed over it), dV +256, dK +384.
+// query heads of the group and the 128-row query tiles at or after kt. Per
+// step: S^T = K Q^T and dP^T = V dO^T, then P^T = exp2(S^T - lse), dS^T =
+// P^T (dP^T - delta) by the elementwise warps, then dV += P^T dO and dK +=
+// dS^T Q. TMEM: S^T +0 (P^T packed over it), dP^T +128 (dS^T packed over
+// it), dV +256, dK +384: full, so the score products of step i+1 follow the
+// gradient products of step i.
 template <int D>
 struct DkvSmem {
   static constexpr int K = 0;
   static constexpr int V = K + tile_bytes<D>();
-  static constexpr int Q0 = V + tile_bytes<D>();                   // [kStages] Q sub-tiles
-  static constexpr int DO0 = Q0 + kStages * sub_bytes<D>();        // [kStages] dO sub-tiles
-  static constexpr int LD0 = DO0 + kStages * sub_bytes<D>();       // [kStages] lse2[64], delta[64]
-  static constexpr int BAR = LD0 + kStages * 512;
+  static constexpr int Q0 = V + tile_bytes<D>();                      // [kDkvStages] Q tiles
+  static constexpr int DO0 = Q0 + kDkvStages * tile_bytes<D>();       // [kDkvStages] dO tiles
+  static constexpr int LD0 = DO0 + kDkvStages * tile_bytes<D>();      // [kDkvStages] lse2[128], delta[128]
+  static constexpr int BAR = LD0 + kDkvStages * 1024;
   static constexpr int TOTAL = BAR + 256;
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
 };
@@ -527,35 +511,36 @@ __global__ void __launch_bounds__(384, 1)
   uint8_t* sm = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
   uint64_t* bars = (uint64_t*)(sm + L::BAR);
   uint64_t* kv_full = bars + 0;
-  uint64_t* qdo_full = bars + 1;                // [kStages]
-  uint64_t* qdo_empty = bars + 1 + kStages;     // [kStages]
-  uint64_t* s_full = bars + 1 + 2 * kStages;    // [2]
-  uint64_t* p_full = bars + 3 + 2 * kStages;    // [2]
-  uint64_t* pd_done = bars + 5 + 2 * kStages;   // [2]
-  uint32_t* tmem_slot = (uint32_t*)(bars + 7 + 2 * kStages);
+  uint64_t* qdo_full = bars + 1;                  // [kDkvStages]
+  uint64_t* qdo_empty = bars + 1 + kDkvStages;    // [kDkvStages]
+  uint64_t* s_full = bars + 1 + 2 * kDkvStages;   // S^T and dP^T of this step are in tensor memory
+  uint64_t* p_full = bars + 2 + 2 * kDkvStages;   // P^T and dS^T are written
+  uint64_t* pd_done = bars + 3 + 2 * kDkvStages;  // the last gradient products are complete
+  uint32_t* tmem_slot = (uint32_t*)(bars + 4 + 2 * kDkvStages);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
-  const int nsub = (a.S + SUB - 1) / SUB;
-  const int kt = (int)blockIdx.x;
-  const int g = blockIdx.y, b = blockIdx.z;
+  const int nqt = (a.S + TILE - 1) / TILE;
+  // longest tiles (the first KV tiles see the most queries) first over the
+  // whole grid: the tile index is the slowest coordinate of the linear order
+  const int lin = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+  const int gb = lin % (a.nkv * a.B);
+  const int kt = lin / (a.nkv * a.B);
+  const int g = gb % a.nkv, b = gb / a.nkv;
   const int grp = a.nq / a.nkv;
-  const int first = 2 * kt;              // first query sub-tile that can see this KV tile
-  const int per_head = nsub - first;
+  const int per_head = nqt - kt;  // query tiles at or after the KV tile
   const int iters = grp * per_head;
-  const int Sp = pad64(a.S);
+  const int Sp = pad128(a.S);
   const uint32_t warp = warp_id(), lane = lane_id();
 
   if (threadIdx.x == 0) {
     mbar_init(kv_full, 1);
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kDkvStages; ++i) {
       mbar_init(&qdo_full[i], 1);
       mbar_init(&qdo_empty[i], 1);
     }
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 8);
-      mbar_init(&pd_done[i], 1);
-    }
+    mbar_init(s_full, 1);
+    mbar_init(p_full, 8);
+    mbar_init(pd_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -579,103 +564,100 @@ __global__ void __launch_bounds__(384, 1)
       load_head_tile<D>(sm + L::V, &tv, kv_full, g, kt * TILE, b);
       for (int it = 0; it < iters; ++it) {
         const int j = g * grp + it / per_head;
-        const int qs = first + it % per_head;
-        const int st = it % kStages;
-        mbar_wait(&qdo_empty[st], ((it / kStages) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
-        mbar_arrive_expect_tx(&qdo_full[st], 2 * sub_bytes<D>() + 512);
-        load_head_sub<D>(sm + L::Q0 + st * sub_bytes<D>(), &tq, &qdo_full[st], j, qs * SUB, b);
-        load_head_sub<D>(sm + L::DO0 + st * sub_bytes<D>(), &tdo, &qdo_full[st], j, qs * SUB, b);
-        const size_t ro = ((size_t)b * a.nq + j) * Sp + (size_t)qs * SUB;
-        bulk_load(sm + L::LD0 + st * 512, a.lse2 + ro, 256, &qdo_full[st]);
-        bulk_load(sm + L::LD0 + st * 512 + 256, a.delta + ro, 256, &qdo_full[st]);
+        const int qt = kt + it % per_head;
+        const int st = it % kDkvStages;
+        mbar_wait(&qdo_empty[st], ((it / kDkvStages) & 1) ^ 1, abort_flag, kErrTimeoutAttn);
+        mbar_arrive_expect_tx(&qdo_full[st], 2 * tile_bytes<D>() + 1024);
+        load_head_tile<D>(sm + L::Q0 + st * tile_bytes<D>(), &tq, &qdo_full[st], j, qt * TILE, b);
+        load_head_tile<D>(sm + L::DO0 + st * tile_bytes<D>(), &tdo, &qdo_full[st], j, qt * TILE, b);
+        const size_t ro = ((size_t)b * a.nq + j) * Sp + (size_t)qt * TILE;
+        bulk_load(sm + L::LD0 + st * 1024, a.lse2 + ro, 512, &qdo_full[st]);
+        bulk_load(sm + L::LD0 + st * 1024 + 512, a.delta + ro, 512, &qdo_full[st]);
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     if (lane == 0) {
-      constexpr uint32_t IDESC_S = make_idesc(128, SUB, false, false);
+      constexpr uint32_t IDESC_S = make_idesc(128, 128, false, false);
       constexpr uint32_t IDESC_G = make_idesc(128, D < 64 ? 64 : D, false, true);
       constexpr int KS = D / 16;
-      auto issue_grad = [&](int i) {
-        const int buf = i & 1, st = i % kStages;
-        mbar_wait(&p_full[buf], (i >> 1) & 1, abort_flag, kErrTimeoutAttn);
-        tc_fence_after();
-        const uint8_t* q = sm + L::Q0 + st * sub_bytes<D>();
-        const uint8_t* dout = sm + L::DO0 + st * sub_bytes<D>();
-#pragma unroll
-        for (int kk = 0; kk < SUB / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q  (A operands in TMEM)
-          const uint32_t acc = (i > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_ts(tmem + 256, tmem + buf * 64 + packed_col(kk), mnmaj_desc_sub(dout, kk), IDESC_G, acc);
-          tc_mma_ts(tmem + 384, tmem + 128 + buf * 64 + packed_col(kk), mnmaj_desc_sub(q, kk), IDESC_G, acc);
-        }
-        tc_commit(&pd_done[buf]);
-        tc_commit(&qdo_empty[st]);
-      };
       mbar_wait(kv_full, 0, abort_flag, kErrTimeoutAttn);
       for (int it = 0; it < iters; ++it) {
-        const int buf = it & 1, st = it % kStages;
-        mbar_wait(&qdo_full[st], (it / kStages) & 1, abort_flag, kErrTimeoutAttn);
+        const int st = it % kDkvStages;
+        const uint8_t* q = sm + L::Q0 + st * tile_bytes<D>();
+        const uint8_t* dout = sm + L::DO0 + st * tile_bytes<D>();
+        mbar_wait(&qdo_full[st], (it / kDkvStages) & 1, abort_flag, kErrTimeoutAttn);
         tc_fence_after();
-        const uint8_t* q = sm + L::Q0 + st * sub_bytes<D>();
-        const uint8_t* dout = sm + L::DO0 + st * sub_bytes<D>();
 #pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {  // S^T = K Q^T ; dP^T = V dO^T
-          tc_mma(tmem + buf * 64, kmaj_desc(sm + L::K, kk), kmaj_desc_sub(q, kk), IDESC_S, kk > 0 ? 1u : 0u);
-          tc_mma(tmem + 128 + buf * 64, kmaj_desc(sm + L::V, kk), kmaj_desc_sub(dout, kk), IDESC_S,
-                 kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < KS; ++kk)  // S^T = K Q^T
+          tc_mma(tmem, kmaj_desc(sm + L::K, kk), kmaj_desc(q, kk), IDESC_S, kk > 0 ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk)  // dP^T = V dO^T
+          tc_mma(tmem + 128, kmaj_desc(sm + L::V, kk), kmaj_desc(dout, kk), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(s_full);
+        mbar_wait(p_full, it & 1, abort_flag, kErrTimeoutAttn);
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < TILE / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q  (A operands in TMEM)
+          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+          tc_mma_ts(tmem + 256, tmem + packed_col128(kk), mnmaj_desc(dout, kk), IDESC_G, acc);
+          tc_mma_ts(tmem + 384, tmem + 128 + packed_col128(kk), mnmaj_desc(q, kk), IDESC_G, acc);
         }
-        tc_commit(&s_full[buf]);
-        if (it > 0) issue_grad(it - 1);
+        tc_commit(&qdo_empty[st]);
       }
-      issue_grad(iters - 1);
+      tc_commit(pd_done);
     }
     __syncwarp();
   } else if (warp >= 4) {
-    const int half = warp >= 8 ? 1 : 0;  // which 32 of the 64 columns
+    const int half = warp >= 8 ? 1 : 0;  // which 64 of the 128 query columns
     const uint32_t q4 = warp & 3;
     const int r = q4 * 32 + lane;        // KV row of the tile
     const int srow = kt * TILE + r;      // KV position
     const uint32_t lane_base = (q4 * 32) << 16;
-    const int cbase = half * 32;
+    const int cbase = half * 64;
     for (int it = 0; it < iters; ++it) {
-      const int buf = it & 1, st = it % kStages;
-      const int q0 = (first + it % per_head) * SUB;
-      const float* s_lse = (const float*)(sm + L::LD0 + st * 512);
-      const float* s_delta = s_lse + 64;
-      mbar_wait(&s_full[buf], (it >> 1) & 1, abort_flag, kErrTimeoutAttn);
+      const int st = it % kDkvStages;
+      const int q0 = (kt + it % per_head) * TILE;
+      const float* s_lse = (const float*)(sm + L::LD0 + st * 1024);
+      const float* s_delta = s_lse + 128;
+      mbar_wait(s_full, it & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
-      uint32_t sv[32], dv[32];
-      __syncwarp();
-      tmem_ld32(tmem + lane_base + buf * 64 + cbase, sv);
-      tmem_ld32(tmem + lane_base + 128 + buf * 64 + cbase, dv);
-      tmem_ld_wait();
-      float p[32], ds[32];
       const bool need_mask = q0 + cbase < srow + 1;  // padded query rows have lse2 = +inf
-      float lse_c[32], del_c[32];  // this warpgroup's 32 columns, 16-byte loads (the stage is 512-byte aligned)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 l4 = ((const float4*)(s_lse + cbase))[i], d4 = ((const float4*)(s_delta + cbase))[i];
-        lse_c[4 * i] = l4.x, lse_c[4 * i + 1] = l4.y, lse_c[4 * i + 2] = l4.z, lse_c[4 * i + 3] = l4.w;
-        del_c[4 * i] = d4.x, del_c[4 * i + 1] = d4.y, del_c[4 * i + 2] = d4.z, del_c[4 * i + 3] = d4.w;
+      for (int c = 0; c < 2; ++c) {  // two 32-column chunks of this warpgroup's 64
+        const int col = cbase + 32 * c;
+        uint32_t sv[32], dv[32];
+        __syncwarp();
+        tmem_ld32(tmem + lane_base + col, sv);
+        tmem_ld32(tmem + lane_base + 128 + col, dv);
+        tmem_ld_wait();
+        float p[32], ds[32];
+        float lse_c[32], del_c[32];  // 16-byte loads (the stage is 1024-byte aligned)
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 l4 = ((const float4*)(s_lse + col))[i], d4 = ((const float4*)(s_delta + col))[i];
+          lse_c[4 * i] = l4.x, lse_c[4 * i + 1] = l4.y, lse_c[4 * i + 2] = l4.z, lse_c[4 * i + 3] = l4.w;
+          del_c[4 * i] = d4.x, del_c[4 * i + 1] = d4.y, del_c[4 * i + 2] = d4.z, del_c[4 * i + 3] = d4.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -lse_c[i]));
+          if (need_mask && q0 + col + i < srow) pv = 0.f;  // query must be at or after the key
+          p[i] = pv;
+          ds[i] = pv * (__uint_as_float(dv[i]) - del_c[i]);
+        }
+        // pairs over this warpgroup's own first 32 columns (chunk c at +16c),
+        // which hold values it has already read
+        __syncwarp();
+        tmem_st_bf16x32(tmem + lane_base + cbase + 16 * c, p);
+        tmem_st_bf16x32(tmem + lane_base + 128 + cbase + 16 * c, ds);
       }
-#pragma unroll
-      for (int i = 0; i < 32; ++i) {
-        float pv = ex2_approx(fmaf(__uint_as_float(sv[i]), a.scale_log2, -lse_c[i]));
-        if (need_mask && q0 + cbase + i < srow) pv = 0.f;  // query must be at or after the key
-        p[i] = pv;
-      }
-      __syncwarp();
-      tmem_st_bf16x32(tmem + lane_base + buf * 64 + cbase, p);  // in flight while dS^T is computed
-#pragma unroll
-      for (int i = 0; i < 32; ++i) ds[i] = p[i] * (__uint_as_float(dv[i]) - del_c[i]);
-      __syncwarp();
-      tmem_st_bf16x32(tmem + lane_base + 128 + buf * 64 + cbase, ds);
       tmem_st_wait();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&p_full[buf]);
+      if (lane == 0) mbar_arrive(p_full);
     }
-    mbar_wait(&pd_done[(iters - 1) & 1], ((iters - 1) >> 1) & 1, abort_flag, kErrTimeoutAttn);
+    mbar_wait(pd_done, 0, abort_flag, kErrTimeoutAttn);
     tc_fence_after();
     // epilogue: warpgroup A writes dV, warpgroup B writes dK (rotated back by RoPE if requested)
     const bool row_ok = srow < a.S;
@@ -715,9 +697,6 @@ struct DqSmem {
   static constexpr int ALLOC = (TOTAL + 1024 > 118 * 1024) ? TOTAL + 1024 : 118 * 1024;
 };
 
-// K step kk (16 KV rows) of the packed dS operand: warpgroup kk / 4 wrote
-// its 64 columns as 32 pairs at the start of its own 64-column range.
-__device__ __forceinline__ uint32_t packed_col128(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
 
 template <int D>
 __global__ void __launch_bounds__(384, 1)
@@ -741,8 +720,12 @@ __global__ void __launch_bounds__(384, 1)
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int nqt = (a.S + TILE - 1) / TILE;
-  const int qt = nqt - 1 - (int)blockIdx.x;  // longest tiles first
-  const int j = blockIdx.y, b = blockIdx.z;
+  // longest tiles first over the whole grid (the tile index is the slowest
+  // coordinate of the linear block order)
+  const int lin = (int)(blockIdx.x + gridDim.x * (blockIdx.y + gridDim.y * blockIdx.z));
+  const int hb = lin % (a.nq * a.B);
+  const int qt = nqt - 1 - lin / (a.nq * a.B);
+  const int j = hb % a.nq, b = hb / a.nq;
   const int g = j / (a.nq / a.nkv);
   const int iters = qt + 1;  // KV tiles at or before the query tile
   const uint32_t warp = warp_id(), lane = lane_id();
@@ -844,7 +827,7 @@ __global__ void __launch_bounds__(384, 1)
     const int trow = qt * TILE + r;
     const uint32_t lane_base = (q4 * 32) << 16;
     const bool row_ok = trow < a.S;
-    const size_t ri = ((size_t)b * a.nq + j) * pad64(a.S) + (row_ok ? trow : 0);
+    const size_t ri = ((size_t)b * a.nq + j) * pad128(a.S) + (row_ok ? trow : 0);
     const float lse2 = row_ok ? a.lse2[ri] : INFINITY;  // rows past S get probability 0
     const float dl = row_ok ? a.delta[ri] : 0.f;
     for (int it = 0; it < iters; ++it) {
@@ -978,11 +961,9 @@ int fwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, AttnArgs
 template <int D>
 int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* o, const uint16_t* dout,
                AttnArgs& a, float* delta, cudaStream_t st) {
-  // dK/dV pass: K, V in 128-row tiles, Q, dO in 64-row sub-tiles;
-  // dQ pass: everything in 128-row tiles.
-  CUtensorMap tq64, tdo64, tk128, tv128, tq128, tdo128;
-  if (head_map(&tq64, q, D, a.nq, a.S, a.B, a.ldq, 64) || head_map(&tdo64, dout, D, a.nq, a.S, a.B, a.ldo, 64) ||
-      head_map(&tk128, k, D, a.nkv, a.S, a.B, a.ldkv) || head_map(&tv128, v, D, a.nkv, a.S, a.B, a.ldkv) ||
+  // both passes: everything in 128-row tiles
+  CUtensorMap tk128, tv128, tq128, tdo128;
+  if (head_map(&tk128, k, D, a.nkv, a.S, a.B, a.ldkv) || head_map(&tv128, v, D, a.nkv, a.S, a.B, a.ldkv) ||
       head_map(&tq128, q, D, a.nq, a.S, a.B, a.ldq) || head_map(&tdo128, dout, D, a.nq, a.S, a.B, a.ldo))
     return -1;
   static bool init = false;
@@ -991,7 +972,7 @@ int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const ui
       return -1;
     init = true;
   }
-  const int Sp = pad64(a.S);
+  const int Sp = pad128(a.S);
   const size_t rows = (size_t)a.B * Sp * a.nq;
   float* lse2 = delta + rows;
   attn_delta_tc_kernel<<<(unsigned)((rows * 16 + 255) / 256), 256, 0, st>>>(o, dout, a.lse_in, delta, lse2, a.B, a.S,
@@ -999,7 +980,7 @@ int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const ui
   a.delta = delta;
   a.lse2 = lse2;
   const int nt = (a.S + TILE - 1) / TILE;
-  attn_bwd_dkv_tc_kernel<D><<<dim3(nt, a.nkv, a.B), 384, DkvSmem<D>::ALLOC, st>>>(tq64, tk128, tv128, tdo64, a);
+  attn_bwd_dkv_tc_kernel<D><<<dim3(nt, a.nkv, a.B), 384, DkvSmem<D>::ALLOC, st>>>(tq128, tk128, tv128, tdo128, a);
   attn_bwd_dq_tc_kernel<D><<<dim3(nt, a.nq, a.B), 384, DqSmem<D>::ALLOC, st>>>(tq128, tk128, tv128, tdo128, a);
   count_launches(3);
   return cudaPeekAtLastError() == cudaSuccess ? 0 : -1;
@@ -1007,7 +988,7 @@ int bwd_launch(const uint16_t* q, const uint16_t* k, const uint16_t* v, const ui
 
 }  // namespace
 
-size_t attention_bwd_workspace(int B, int S, int nq) { return 2 * (size_t)B * nq * pad64(S); }
+size_t attention_bwd_workspace(int B, int S, int nq) { return 2 * (size_t)B * nq * pad128(S); }
 
 namespace {
 
