@@ -479,8 +479,11 @@ __device__ __forceinline__ void tmem_st_bf16x32(uint32_t col, const float (&v)[3
 
 // K step kk (16 rows of the 128-wide loop dimension) of a packed bf16
 // operand: warpgroup kk / 4 wrote its 64 columns as 32 pairs at the start of
-// its own 64-column range.
+// its own 64-column range (dQ pass).
 __device__ __forceinline__ uint32_t packed_col128(int kk) { return (kk >> 2) * 64 + (kk & 3) * 8; }
+// The same for the dK/dV pass, whose 32-column chunks alternate between the
+// warpgroups: K step kk sits in chunk kk / 2, at +8 for its second 16 rows.
+__device__ __forceinline__ uint32_t packed_col_dkv(int kk) { return (kk >> 1) * 32 + (kk & 1) * 8; }
 
 // dK/dV pass: CTA = (128-row KV tile kt, KV head g, sequence b); loop over the
 // query heads of the group and the 128-row query tiles at or after kt. Per
@@ -488,7 +491,11 @@ __device__ __forceinline__ uint32_t packed_col128(int kk) { return (kk >> 2) * 6
 // P^T (dP^T - delta) by the elementwise warps, then dV += P^T dO and dK +=
 // dS^T Q. TMEM: S^T +0 (P^T packed over it), dP^T +128 (dS^T packed over
 // it), dV +256, dK +384: full, so the score products of step i+1 follow the
-// gradient products of step i.
+// gradient products of step i. The elementwise warps do the first 64
+// queries of a step first (warpgroup w: columns 32w..32w+31), then the last
+// 64 (64+32w..), and signal each half, so the gradient products of the first
+// half run while the second is computed. Pairs of chunk (c, w) go over the
+// first 16 of its own 32 columns: K step kk at packed_col_dkv(kk).
 template <int D>
 struct DkvSmem {
   static constexpr int K = 0;
@@ -514,9 +521,9 @@ __global__ void __launch_bounds__(384, 1)
   uint64_t* qdo_full = bars + 1;                  // [kDkvStages]
   uint64_t* qdo_empty = bars + 1 + kDkvStages;    // [kDkvStages]
   uint64_t* s_full = bars + 1 + 2 * kDkvStages;   // S^T and dP^T of this step are in tensor memory
-  uint64_t* p_full = bars + 2 + 2 * kDkvStages;   // P^T and dS^T are written
-  uint64_t* pd_done = bars + 3 + 2 * kDkvStages;  // the last gradient products are complete
-  uint32_t* tmem_slot = (uint32_t*)(bars + 4 + 2 * kDkvStages);
+  uint64_t* p_full = bars + 2 + 2 * kDkvStages;   // [2] P^T and dS^T of the first / last 64 queries written
+  uint64_t* pd_done = bars + 4 + 2 * kDkvStages;  // the last gradient products are complete
+  uint32_t* tmem_slot = (uint32_t*)(bars + 5 + 2 * kDkvStages);
   volatile int* abort_flag = (volatile int*)(tmem_slot + 1);
 
   const int nqt = (a.S + TILE - 1) / TILE;
@@ -539,7 +546,8 @@ __global__ void __launch_bounds__(384, 1)
       mbar_init(&qdo_empty[i], 1);
     }
     mbar_init(s_full, 1);
-    mbar_init(p_full, 8);
+    mbar_init(&p_full[0], 8);
+    mbar_init(&p_full[1], 8);
     mbar_init(pd_done, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -595,13 +603,16 @@ __global__ void __launch_bounds__(384, 1)
         for (int kk = 0; kk < KS; ++kk)  // dP^T = V dO^T
           tc_mma(tmem + 128, kmaj_desc(sm + L::V, kk), kmaj_desc(dout, kk), IDESC_S, kk > 0 ? 1u : 0u);
         tc_commit(s_full);
-        mbar_wait(p_full, it & 1, abort_flag, kErrTimeoutAttn);
-        tc_fence_after();
 #pragma unroll
-        for (int kk = 0; kk < TILE / 16; ++kk) {  // dV += P^T dO ; dK += dS^T Q  (A operands in TMEM)
-          const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
-          tc_mma_ts(tmem + 256, tmem + packed_col128(kk), mnmaj_desc(dout, kk), IDESC_G, acc);
-          tc_mma_ts(tmem + 384, tmem + 128 + packed_col128(kk), mnmaj_desc(q, kk), IDESC_G, acc);
+        for (int h = 0; h < 2; ++h) {  // the two 64-query halves, as the elementwise warps finish them
+          mbar_wait(&p_full[h], it & 1, abort_flag, kErrTimeoutAttn);
+          tc_fence_after();
+#pragma unroll
+          for (int kk = 4 * h; kk < 4 * h + 4; ++kk) {  // dV += P^T dO ; dK += dS^T Q  (A operands in TMEM)
+            const uint32_t acc = (it > 0 || kk > 0) ? 1u : 0u;
+            tc_mma_ts(tmem + 256, tmem + packed_col_dkv(kk), mnmaj_desc(dout, kk), IDESC_G, acc);
+            tc_mma_ts(tmem + 384, tmem + 128 + packed_col_dkv(kk), mnmaj_desc(q, kk), IDESC_G, acc);
+          }
         }
         tc_commit(&qdo_empty[st]);
       }
@@ -609,12 +620,11 @@ __global__ void __launch_bounds__(384, 1)
     }
     __syncwarp();
   } else if (warp >= 4) {
-    const int half = warp >= 8 ? 1 : 0;  // which 64 of the 128 query columns
+    const int half = warp >= 8 ? 1 : 0;  // warpgroup: columns 32 * half + 64 * c of chunk c
     const uint32_t q4 = warp & 3;
     const int r = q4 * 32 + lane;        // KV row of the tile
     const int srow = kt * TILE + r;      // KV position
     const uint32_t lane_base = (q4 * 32) << 16;
-    const int cbase = half * 64;
     for (int it = 0; it < iters; ++it) {
       const int st = it % kDkvStages;
       const int q0 = (kt + it % per_head) * TILE;
@@ -622,10 +632,10 @@ __global__ void __launch_bounds__(384, 1)
       const float* s_delta = s_lse + 128;
       mbar_wait(s_full, it & 1, abort_flag, kErrTimeoutAttn);
       tc_fence_after();
-      const bool need_mask = q0 + cbase < srow + 1;  // padded query rows have lse2 = +inf
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {  // two 32-column chunks of this warpgroup's 64
-        const int col = cbase + 32 * c;
+      for (int c = 0; c < 2; ++c) {  // the first 64 queries, then the last 64
+        const int col = 64 * c + 32 * half;
+        const bool need_mask = q0 + col < srow + 1;  // padded query rows have lse2 = +inf
         uint32_t sv[32], dv[32];
         __syncwarp();
         tmem_ld32(tmem + lane_base + col, sv);
@@ -646,16 +656,15 @@ __global__ void __launch_bounds__(384, 1)
           p[i] = pv;
           ds[i] = pv * (__uint_as_float(dv[i]) - del_c[i]);
         }
-        // pairs over this warpgroup's own first 32 columns (chunk c at +16c),
-        // which hold values it has already read
+        // pairs over the first 16 of this chunk's columns, already read
         __syncwarp();
-        tmem_st_bf16x32(tmem + lane_base + cbase + 16 * c, p);
-        tmem_st_bf16x32(tmem + lane_base + 128 + cbase + 16 * c, ds);
+        tmem_st_bf16x32(tmem + lane_base + col, p);
+        tmem_st_bf16x32(tmem + lane_base + 128 + col, ds);
+        tmem_st_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&p_full[c]);
       }
-      tmem_st_wait();
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
     }
     mbar_wait(pd_done, 0, abort_flag, kErrTimeoutAttn);
     tc_fence_after();
