@@ -209,7 +209,13 @@ __device__ __forceinline__ void rope_epilogue(const GemmParams& p, uint32_t tbas
   }
 }
 
-__device__ __forceinline__ float silu_sig(float g) { return 1.f / (1.f + __expf(-g)); }
+// sigmoid(g) = 1 / (1 + e^-g), the reciprocal by the hardware's approximate
+// reciprocal (1 ulp; +0 for an infinite denominator).
+__device__ __forceinline__ float silu_sig(float g) {
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.f + __expf(-g)));
+  return r;
+}
 
 __device__ __forceinline__ void load_bf16_32(const uint16_t* src, float (&v)[32], int col0, int N, bool vec) {
   if (vec && col0 + 32 <= N) {
@@ -258,11 +264,72 @@ __device__ __forceinline__ void gated_epilogue(const GemmParams& p, uint32_t tba
 }
 
 // SwiGLU backward epilogue: the accumulator is dact for features
-// [n0, n0 + BN); g and u are read from gu and replaced by dg and du.
+// [n0, n0 + BN); g and u are read from gu and replaced by dg and du. Where
+// the whole tile is in range and 16-byte aligned, the next chunk's g and u
+// are loaded before this chunk is computed (their latency then overlaps the
+// work; the addresses differ from this chunk's stores).
+__device__ __forceinline__ void swiglu_bwd_32(const uint32_t (&rd)[32], float (&g)[32], float (&u)[32]) {
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    const float d = __uint_as_float(rd[i]);
+    const float sg = silu_sig(g[i]);
+    const float dg = d * u[i] * sg * (1.f + g[i] * (1.f - sg));
+    u[i] = d * g[i] * sg;  // du
+    g[i] = dg;
+  }
+}
+__device__ __forceinline__ void unpack_bf16x8(const uint4 (&w)[4], float (&v)[32]) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      v[8 * k + 2 * e] = bf2f(ws[e] & 0xffff);
+      v[8 * k + 2 * e + 1] = bf2f(ws[e] >> 16);
+    }
+  }
+}
 template <int BN>
 __device__ __forceinline__ void swiglu_bwd_epilogue(const GemmParams& p, uint32_t tbase, int row, bool row_ok,
                                                     int n0) {
   uint16_t* gurow = p.gu + (size_t)row * p.ld_gu;
+  if (p.vec && n0 + BN <= p.N) {  // the same in every lane
+    uint4 gn[4], un[4];
+    auto fetch = [&](int c) {
+      if (!row_ok) return;
+      const uint4* gp = (const uint4*)(gurow + n0 + 32 * c);
+      const uint4* up = (const uint4*)(gurow + p.u_col + n0 + 32 * c);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        gn[k] = gp[k];
+        un[k] = up[k];
+      }
+    };
+    fetch(0);
+#pragma unroll 1
+    for (int c = 0; c < BN / 32; ++c) {
+      uint4 gc[4], uc[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        gc[k] = gn[k];
+        uc[k] = un[k];
+      }
+      if (c + 1 < BN / 32) fetch(c + 1);
+      uint32_t rd[32];
+      __syncwarp();
+      tmem_ld32(tbase + c * 32, rd);
+      tmem_ld_wait();
+      if (!row_ok) continue;
+      float g[32], u[32];
+      unpack_bf16x8(gc, g);
+      unpack_bf16x8(uc, u);
+      swiglu_bwd_32(rd, g, u);
+      const int col0 = n0 + c * 32;
+      store_bf16_32(gurow + col0, g, col0, p.N, true);
+      store_bf16_32(gurow + p.u_col + col0, u, col0, p.N, true);
+    }
+    return;
+  }
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     uint32_t rd[32];
@@ -274,16 +341,26 @@ __device__ __forceinline__ void swiglu_bwd_epilogue(const GemmParams& p, uint32_
     float g[32], u[32];
     load_bf16_32(gurow + col0, g, col0, p.N, p.vec);
     load_bf16_32(gurow + p.u_col + col0, u, col0, p.N, p.vec);
-#pragma unroll
-    for (int i = 0; i < 32; ++i) {
-      const float d = __uint_as_float(rd[i]);
-      const float sg = silu_sig(g[i]);
-      const float dg = d * u[i] * sg * (1.f + g[i] * (1.f - sg));
-      u[i] = d * g[i] * sg;  // du
-      g[i] = dg;
-    }
+    swiglu_bwd_32(rd, g, u);
     store_bf16_32(gurow + col0, g, col0, p.N, p.vec);
     store_bf16_32(gurow + p.u_col + col0, u, col0, p.N, p.vec);
+  }
+}
+
+// g and u of the SwiGLU backward for one row of a tile, pulled into L2 while
+// the tile's products still run, so that the epilogue's loads hit L2. Only
+// addresses inside the row's valid columns are touched. (The fp32 residual
+// of the add epilogue is not prefetched: its loads are issued ahead of the
+// accumulator read already, and an L2 prefetch measured slower there.)
+template <int BN>
+__device__ __forceinline__ void prefetch_epilogue_inputs(const GemmParams& p, int row, bool row_ok, int n0) {
+  if (!p.swiglu_bwd || !row_ok || n0 >= p.N) return;
+  const int ncols = min(BN, p.N - n0);
+  const char* g = (const char*)(p.gu + (size_t)row * p.ld_gu + n0);
+  const char* u = (const char*)(p.gu + (size_t)row * p.ld_gu + p.u_col + n0);
+  for (int off = 0; off < ncols * 2; off += 128) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(g + off));
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(u + off));
   }
 }
 
@@ -525,9 +602,10 @@ __global__ void __launch_bounds__(192, 1)
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
       ++local;
+      const int r = ti.m0 + q * 32 + lane;  // row within this product's M
+      if (ti.nkb > 0) prefetch_epilogue_inputs<BN>(p, ti.crow + q * 32 + lane, r < p.M, ti.nb * BN);
       mbar_wait(&tfull[acc], acc_phase, abort_flag, kErrTimeoutEpi);
       tc_fence_after();
-      const int r = ti.m0 + q * 32 + lane;  // row within this product's M
       if (ti.nkb == 0) {
         zero_tile_row<BN>(p, ti.crow + q * 32 + lane, r < p.M, ti.n0);
       } else {
@@ -697,9 +775,10 @@ __global__ void __launch_bounds__(192, 1)
       tile_coords(tile, num_m, num_n, p.group_m, mb, nb);
       const int acc = local & 1;
       const uint32_t acc_phase = (local >> 1) & 1;
+      const int row = mb * 2 * BM + (int)rank * BM + q * 32 + lane;
+      prefetch_epilogue_inputs<BN>(p, row, row < p.M, nb * BN);
       mbar_wait<true>(&tfull[acc], acc_phase, abort_flag, kErrTimeoutEpi);
       tc_fence_after();
-      const int row = mb * 2 * BM + (int)rank * BM + q * 32 + lane;
       epilogue_tile<BN>(p, tmem_base + ((q * 32) << 16) + acc * BN, row, row < p.M, nb, tile_n,
                         staging + q * 32 * kStgStride);
       tc_fence_before();
