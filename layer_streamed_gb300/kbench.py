@@ -9,7 +9,10 @@
 Inputs are random bf16 tensors on the current GPU (larger than L2 at the 8B
 shapes); each launch is timed with CUDA events on the launching stream after
 warm-up. Prints one JSON line with the per-launch time and TFLOP/s (GB/s
-of algorithmic traffic for the norms).
+of algorithmic traffic for the norms). The qkv_rope shape goes through
+mt_op_gemm_rope, which rebuilds the cos/sin table on every call (about
+0.08 ms at S = 4096); the training step builds it once per sequence length,
+so its QKV projection is the GEMM alone.
 """
 from __future__ import annotations
 
