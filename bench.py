@@ -240,10 +240,10 @@ def head_slice_rows(shape, esz, moe=None):
 # as committed with that summary; when the GEMM kernels change, the figure
 # must be captured again.
 GEMM_TRAFFIC_8B = {
-    "qkv_rope": 291063296, "o_proj": 507722240, "gate_up": 1806588416, "down": 1509592320, "dWd": 1095791872,
-    "dact_swiglu": 1423328768, "dWgu": 2951109632, "dm": 2688931328, "dWo": 337852672, "do": 200612608,
-    "dWqkv": 525176320, "dx": 549968128, "head_logits": 3039382784, "head_dX": 4527798784,
-    "head_dW": 4957469696,
+    "qkv_rope": 301616384, "o_proj": 508946432, "gate_up": 1629239552, "down": 1530027520, "dWd": 1100619520,
+    "dact_swiglu": 1536381184, "dWgu": 3216824320, "dm": 3643644928, "dWo": 336235776, "do": 201520128,
+    "dWqkv": 525138688, "dx": 559515136, "head_logits": 2931604992, "head_dX": 5587098624,
+    "head_dW": 5480545024,
 }
 # Launches of each per step at the 8B configuration (32 layers, K=4, top
 # block not recomputed; three vocab slices of the head).
