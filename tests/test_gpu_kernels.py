@@ -233,7 +233,8 @@ def test_swiglu_forward_backward(F, ld):
     check(out[:, ld:ld + F], du_ref, (U16 + 1e-5) * np.abs(du_ref), "du")
 
 
-@pytest.mark.parametrize("d,S,nq,nkv", [(16, 32, 4, 4), (64, 200, 4, 2), (128, 130, 8, 2), (128, 1, 2, 1)])
+@pytest.mark.parametrize("d,S,nq,nkv", [(16, 32, 4, 4), (64, 200, 4, 2), (128, 130, 8, 2), (128, 1, 2, 1),
+                                         (128, 300, 16, 1)])
 def test_attention_forward_backward(d, S, nq, nkv):
     torch, mt = need_gpu()
     B = 2
